@@ -1,0 +1,259 @@
+"""Python binding of the hybrid decode-attention C ABI (include/hybrid_decode.h).
+
+Argument marshalling only: every step of the path runs in the CUDA kernels of
+``libhybriddecode.so``.  PyTorch provides device memory and streams; tensors
+are passed as raw device pointers.  Importing this package loads the in-tree
+library and raises if it has not been built -- there is no fallback.
+
+Names follow the C entry points: ``hybrid_decode_init``, ``rope_append_kv``,
+``decode_attn_sliding``, ``decode_attn_full``, ``decode_step`` (plus
+``hybrid_decode_destroy`` and the helpers).  Each call raises ``HDError``
+carrying the hd_status when the library rejects it.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass, field
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIBRARY = os.path.join(PKG, "libhybriddecode.so")
+
+HD_SLIDING, HD_FULL = 0, 1
+HD_LAYOUT_AUTO, HD_LAYOUT_RING, HD_LAYOUT_ROLL = 0, 1, 2
+STATUS = {0: "HD_OK", 1: "HD_ERR_INVALID_ARG", 2: "HD_ERR_UNSUPPORTED", 3: "HD_ERR_CAPACITY",
+          4: "HD_ERR_CUDA", 5: "HD_ERR_STATE"}
+DEVERR = {1: "HD_DEVERR_CONTEXT_NEGATIVE", 2: "HD_DEVERR_CONTEXT_CAPACITY",
+          4: "HD_DEVERR_CONTEXT_PLAN", 8: "HD_DEVERR_WAIT_TIMEOUT"}
+
+if not os.path.exists(LIBRARY):
+    raise ImportError(f"{LIBRARY} is missing: build it with full_gqa_decode_gb300.build.build() "
+                      "(or __graft_entry__.build()); there is no non-CUDA fallback")
+_lib = ctypes.CDLL(LIBRARY)
+
+
+class HDError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(status, status)}")
+        self.status = status
+
+
+class hd_config(ctypes.Structure):
+    _fields_ = [("num_layers", ctypes.c_int32), ("layer_types", ctypes.POINTER(ctypes.c_int32)),
+                ("num_q_heads", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("sliding_window", ctypes.c_int32),
+                ("rotary_dim_sliding", ctypes.c_int32), ("rotary_dim_full", ctypes.c_int32),
+                ("rope_theta_sliding", ctypes.c_double), ("rope_theta_full", ctypes.c_double),
+                ("cache_layout", ctypes.c_int32), ("max_batch", ctypes.c_int32),
+                ("max_context", ctypes.c_int32)]
+
+
+class hd_kv_cache(ctypes.Structure):
+    _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("seq_stride", ctypes.c_int64),
+                ("capacity", ctypes.c_int32)]
+
+
+class hd_layer_io(ctypes.Structure):
+    _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("cache", hd_kv_cache), ("sink", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("lse", ctypes.c_void_p)]
+
+
+_c = ctypes
+_P = _c.c_void_p
+_i32, _i64 = _c.c_int32, _c.c_int64
+_SIGS = {
+    "hd_validate_config": [_c.POINTER(hd_config)],
+    "hd_plan_split": [_i32, _i32, _i32, _i32, _c.POINTER(_i32), _c.POINTER(_i32)],
+    "hybrid_decode_init": [_c.POINTER(hd_config), _c.POINTER(_P)],
+    "hybrid_decode_destroy": [_P],
+    "rope_append_kv": [_P, _i32, _i32, _P, _P, _P, _P, _P, hd_kv_cache, _P],
+    "decode_attn_sliding": [_P, _i32, _i32, _P, _P, hd_kv_cache, _P, _P, _P, _P],
+    "decode_attn_full": [_P, _i32, _i32, _P, _i32, _P, hd_kv_cache, _P, _P, _P, _P],
+    "decode_step": [_P, _i32, _P, _i32, _c.POINTER(hd_layer_io), _P],
+    "hybrid_decode_device_errors": [_P, _c.POINTER(_i32), _P],
+    "hybrid_decode_launch_count": [_P, _c.POINTER(_i64)],
+    "hybrid_decode_set_profiling": [_P, _i32],
+    "hybrid_decode_profile": [_P, _c.POINTER(_c.c_double), _c.POINTER(_i64)],
+}
+for _name, _args in _SIGS.items():
+    _fn = getattr(_lib, _name)
+    _fn.argtypes = _args
+    _fn.restype = _c.c_int
+_lib.hd_status_string.argtypes = [_c.c_int]
+_lib.hd_status_string.restype = _c.c_char_p
+
+
+def _check(status: int, what: str) -> None:
+    if status != 0:
+        raise HDError(status, what)
+
+
+def _ptr(t: torch.Tensor | None) -> int | None:
+    if t is None:
+        return None
+    return t.data_ptr()
+
+
+def _check_sink(sink, num_q_heads: int, like: torch.Tensor) -> None:
+    """Sink checks of vllm/models/hy_v4/nvidia/flashmla_sparse.py (`_validate_sinks`,
+    `_sinks_for_query`): fp32, shape (num_q_heads,), on the query's device."""
+    if sink is None:
+        return
+    if sink.dtype != torch.float32:
+        raise ValueError(f"sink must be float32, got {sink.dtype}")
+    if sink.dim() != 1 or sink.shape[0] != num_q_heads:
+        raise ValueError(f"sink must have shape ({num_q_heads},), got {tuple(sink.shape)}")
+    if sink.device != like.device:
+        raise ValueError(f"sink and query must be on the same device ({sink.device} vs {like.device})")
+    if not sink.is_contiguous():
+        raise ValueError("sink must be contiguous")
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+@dataclass
+class Config:
+    """Model shape; field meanings follow ``hd_config`` in include/hybrid_decode.h."""
+    layer_types: list
+    num_q_heads: int = 8
+    num_kv_heads: int = 2
+    head_dim: int = 256
+    sliding_window: int = 512
+    rotary_dim_sliding: int = 256
+    rotary_dim_full: int = 64
+    rope_theta_sliding: float = 1.0e4
+    rope_theta_full: float = 5.0e6
+    cache_layout: int = HD_LAYOUT_AUTO
+    max_batch: int = 1
+    max_context: int = 4096
+    _types: object = field(default=None, repr=False)
+
+    def to_c(self) -> hd_config:
+        self._types = (ctypes.c_int32 * len(self.layer_types))(*self.layer_types)
+        return hd_config(len(self.layer_types), self._types, self.num_q_heads, self.num_kv_heads,
+                         self.head_dim, self.sliding_window, self.rotary_dim_sliding,
+                         self.rotary_dim_full, self.rope_theta_sliding, self.rope_theta_full,
+                         self.cache_layout, self.max_batch, self.max_context)
+
+
+def kv_cache(k: torch.Tensor, v: torch.Tensor) -> hd_kv_cache:
+    """Describe a cache pair shaped [batch, num_kv_heads, capacity, head_dim] (bf16, CUDA)."""
+    if k.shape != v.shape or k.dim() != 4 or k.stride() != v.stride():
+        raise ValueError("k and v caches must share a [batch, kv_heads, capacity, head_dim] layout")
+    if k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+        raise ValueError("caches must be bf16")
+    if k.stride(3) != 1 or k.stride(2) != k.shape[3] or k.stride(1) != k.shape[2] * k.shape[3]:
+        raise ValueError("each sequence's cache must be contiguous [kv_heads, capacity, head_dim]")
+    return hd_kv_cache(k.data_ptr(), v.data_ptr(), k.stride(0), k.shape[2])
+
+
+def hd_validate_config(cfg: Config) -> int:
+    return _lib.hd_validate_config(ctypes.byref(cfg.to_c()))
+
+
+def hd_plan_split(batch: int, num_kv_heads: int, max_keys: int, num_sms: int) -> tuple[int, int]:
+    ck, nc = ctypes.c_int32(), ctypes.c_int32()
+    _check(_lib.hd_plan_split(batch, num_kv_heads, max_keys, num_sms, ctypes.byref(ck),
+                              ctypes.byref(nc)), "hd_plan_split")
+    return ck.value, nc.value
+
+
+def hd_status_string(status: int) -> str:
+    return _lib.hd_status_string(status).decode()
+
+
+class Context:
+    """Owns one ``hd_ctx``; create it with ``hybrid_decode_init``."""
+
+    def __init__(self, handle: int, cfg: Config):
+        self.handle = handle
+        self.cfg = cfg
+
+    def close(self) -> None:
+        if self.handle:
+            _check(_lib.hybrid_decode_destroy(self.handle), "hybrid_decode_destroy")
+            self.handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def hybrid_decode_init(cfg: Config) -> Context:
+    h = ctypes.c_void_p()
+    _check(_lib.hybrid_decode_init(ctypes.byref(cfg.to_c()), ctypes.byref(h)), "hybrid_decode_init")
+    return Context(h.value, cfg)
+
+
+def hybrid_decode_destroy(ctx: Context) -> None:
+    ctx.close()
+
+
+def rope_append_kv(ctx: Context, layer: int, context: torch.Tensor, q, k, v, q_rot, cache: hd_kv_cache,
+                   stream=None) -> None:
+    _check(_lib.rope_append_kv(ctx.handle, layer, q.shape[0], _ptr(context), _ptr(q), _ptr(k), _ptr(v),
+                               _ptr(q_rot), cache, _stream(stream)), "rope_append_kv")
+
+
+def decode_attn_sliding(ctx: Context, layer: int, context, q_rot, cache: hd_kv_cache, sink, out, lse,
+                        stream=None) -> None:
+    _check_sink(sink, ctx.cfg.num_q_heads, q_rot)
+    _check(_lib.decode_attn_sliding(ctx.handle, layer, q_rot.shape[0], _ptr(context), _ptr(q_rot),
+                                    cache, _ptr(sink), _ptr(out), _ptr(lse), _stream(stream)),
+           "decode_attn_sliding")
+
+
+def decode_attn_full(ctx: Context, layer: int, context, q_rot, cache: hd_kv_cache, sink, out, lse,
+                     max_context_hint: int = 0, stream=None) -> None:
+    _check_sink(sink, ctx.cfg.num_q_heads, q_rot)
+    _check(_lib.decode_attn_full(ctx.handle, layer, q_rot.shape[0], _ptr(context), max_context_hint,
+                                 _ptr(q_rot), cache, _ptr(sink), _ptr(out), _ptr(lse),
+                                 _stream(stream)), "decode_attn_full")
+
+
+def layer_io(q, k, v, cache: hd_kv_cache, sink, out, lse) -> hd_layer_io:
+    if sink is not None:
+        _check_sink(sink, q.shape[1], q)
+    return hd_layer_io(_ptr(q), _ptr(k), _ptr(v), cache, _ptr(sink), _ptr(out), _ptr(lse))
+
+
+def decode_step(ctx: Context, context: torch.Tensor, layers: list, batch: int,
+                max_context_hint: int = 0, stream=None) -> None:
+    arr = (hd_layer_io * len(layers))(*layers)
+    _check(_lib.decode_step(ctx.handle, batch, _ptr(context), max_context_hint, arr, _stream(stream)),
+           "decode_step")
+
+
+def hybrid_decode_device_errors(ctx: Context, stream=None) -> int:
+    f = ctypes.c_int32()
+    _check(_lib.hybrid_decode_device_errors(ctx.handle, ctypes.byref(f), _stream(stream)),
+           "hybrid_decode_device_errors")
+    return f.value
+
+
+def hybrid_decode_launch_count(ctx: Context) -> int:
+    n = ctypes.c_int64()
+    _check(_lib.hybrid_decode_launch_count(ctx.handle, ctypes.byref(n)), "hybrid_decode_launch_count")
+    return n.value
+
+
+def hybrid_decode_set_profiling(ctx: Context, enable: bool) -> None:
+    _check(_lib.hybrid_decode_set_profiling(ctx.handle, int(enable)), "hybrid_decode_set_profiling")
+
+
+def hybrid_decode_profile(ctx: Context) -> tuple[float, int]:
+    ms, n = ctypes.c_double(), ctypes.c_int64()
+    _check(_lib.hybrid_decode_profile(ctx.handle, ctypes.byref(ms), ctypes.byref(n)),
+           "hybrid_decode_profile")
+    return ms.value, n.value

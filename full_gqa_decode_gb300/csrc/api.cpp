@@ -1,0 +1,530 @@
+// Host side of the C ABI declared in include/hybrid_decode.h: argument
+// validation, the context (RoPE tables, split-K workspace, ring staging rows),
+// the split plan, TMA tensor maps and the kernel launches.
+//
+// The configuration checks mirror `SparkStepConfig.__post_init__` of
+// vllm_omni/edge/spark_export.py (heads divisible by kv heads, known layer
+// types, known cache layout); the sink checks mirror `_validate_sinks` of
+// vllm/models/hy_v4/nvidia/flashmla_sparse.py (fp32 by type here, one value
+// per query head, NULL for no sink).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "hd_internal.h"
+
+using namespace hd;
+
+namespace {
+
+struct MapCacheEntry {
+    const void *k = nullptr, *v = nullptr;
+    int64_t seq_stride = 0;
+    int32_t capacity = 0, batch = 0;
+    CUtensorMap kmap, vmap;
+};
+
+struct DeviceTable {
+    float2 *data = nullptr;  // [max_context + 1][rotary_dim / 2]
+    int32_t rotary_dim = 0;
+};
+
+}  // namespace
+
+struct hd_ctx {
+    hd_config cfg;
+    std::vector<int32_t> layer_types;
+    int device = 0;
+    int num_sms = 0;
+    int group = 1;
+    int sliding_layout = HD_LAYOUT_RING;
+    DeviceTable table_sliding, table_full;
+    float *part_o = nullptr;
+    float2 *part_ml = nullptr;
+    int64_t part_slots = 0;              // capacity in (sequence, chunk) pairs
+    __nv_bfloat16 *stage_k = nullptr;    // [num_layers][max_batch][Hkv][D]
+    __nv_bfloat16 *stage_v = nullptr;
+    float *q_rot = nullptr;              // [max_batch][Hq][D] for decode_step
+    int32_t *err = nullptr;
+    int64_t launches = 0;
+    std::vector<MapCacheEntry> maps;     // one per layer
+    bool profiling = false;
+    std::vector<cudaEvent_t> ev_begin, ev_end;
+    size_t ev_used = 0;
+};
+
+namespace {
+
+constexpr int kProfileEvents = 4096;
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
+
+int sliding_capacity(const hd_ctx *ctx) {
+    return ctx->sliding_layout == HD_LAYOUT_ROLL ? ctx->cfg.sliding_window
+                                                 : ctx->cfg.sliding_window - 1;
+}
+
+// Encodes the 4-D view {D, capacity, Hkv, batch} of one cache tensor with
+// 64 x kStageKeys boxes and the 128-byte swizzle the consumers index by.
+bool encode_cache_map(CUtensorMap *map, const void *base, int64_t seq_stride, int capacity,
+                      int num_kv_heads, int batch) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)capacity,
+                                (cuuint64_t)num_kv_heads, (cuuint64_t)batch};
+    const cuuint64_t strides[3] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)capacity * kHeadDim * 2,
+                                   (cuuint64_t)seq_stride * 2};
+    const cuuint32_t box[4] = {(cuuint32_t)kBoxCols, (cuuint32_t)kStageKeys, 1, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
+                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+hd_status maps_for(hd_ctx *ctx, int layer, const hd_kv_cache &c, int batch, const CUtensorMap **km,
+                   const CUtensorMap **vm) {
+    MapCacheEntry &e = ctx->maps[layer];
+    if (e.k != c.k || e.v != c.v || e.seq_stride != c.seq_stride || e.capacity != c.capacity ||
+        e.batch != batch) {
+        if (!encode_cache_map(&e.kmap, c.k, c.seq_stride, c.capacity, ctx->cfg.num_kv_heads, batch) ||
+            !encode_cache_map(&e.vmap, c.v, c.seq_stride, c.capacity, ctx->cfg.num_kv_heads, batch)) {
+            e.k = e.v = nullptr;
+            return HD_ERR_CUDA;
+        }
+        e.k = c.k;
+        e.v = c.v;
+        e.seq_stride = c.seq_stride;
+        e.capacity = c.capacity;
+        e.batch = batch;
+    }
+    *km = &e.kmap;
+    *vm = &e.vmap;
+    return HD_OK;
+}
+
+hd_status check_cache(const hd_ctx *ctx, const hd_kv_cache &c) {
+    if (!c.k || !c.v || !aligned16(c.k) || !aligned16(c.v)) return HD_ERR_INVALID_ARG;
+    if (c.capacity <= 0 || c.seq_stride % 8 != 0) return HD_ERR_INVALID_ARG;
+    if (c.seq_stride < (int64_t)ctx->cfg.num_kv_heads * c.capacity * kHeadDim)
+        return HD_ERR_INVALID_ARG;
+    return HD_OK;
+}
+
+hd_status check_call(const hd_ctx *ctx, int layer, int batch, const int32_t *context) {
+    if (!ctx) return HD_ERR_INVALID_ARG;
+    if (layer < 0 || layer >= ctx->cfg.num_layers) return HD_ERR_INVALID_ARG;
+    if (batch <= 0 || !context) return HD_ERR_INVALID_ARG;
+    if (batch > ctx->cfg.max_batch) return HD_ERR_CAPACITY;
+    return HD_OK;
+}
+
+hd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? HD_OK : HD_ERR_CUDA; }
+
+// Largest (sequence, chunk) product a call may need, over every batch size and
+// key bound: the chunk count is largest at the top of each chunk-size range.
+int64_t worst_part_slots(int max_batch, int num_kv_heads, int max_keys, int num_sms) {
+    int64_t worst = 0;
+    for (int b = 1; b <= max_batch; ++b) {
+        std::vector<int> probes{max_keys};
+        for (int t = kChunkMin; t < kChunkMax; t *= 2) {
+            // keys at which the plan leaves chunk size t: units * keys > t * target
+            const int64_t target = 8LL * num_sms;
+            const int64_t k = (int64_t)t * target / ((int64_t)b * num_kv_heads);
+            if (k < max_keys) probes.push_back((int)k);
+        }
+        for (int k : probes) {
+            int32_t ck = 0, nc = 0;
+            hd_plan_split(b, num_kv_heads, k < 1 ? 1 : k, num_sms, &ck, &nc);
+            if ((int64_t)b * nc > worst) worst = (int64_t)b * nc;
+        }
+    }
+    return worst;
+}
+
+hd_status build_table(DeviceTable *t, int rotary_dim, double theta, int max_context) {
+    const int half = rotary_dim / 2;
+    t->rotary_dim = rotary_dim;
+    if (half == 0) return HD_OK;
+    std::vector<double> inv(half);
+    for (int i = 0; i < half; ++i) inv[i] = 1.0 / std::pow(theta, (double)(2 * i) / rotary_dim);
+    const size_t n = (size_t)(max_context + 1) * half;
+    std::vector<float2> host(n);
+    for (int64_t p = 0; p <= max_context; ++p)
+        for (int i = 0; i < half; ++i) {
+            const double ang = (double)p * inv[i];
+            host[(size_t)p * half + i] = make_float2((float)std::cos(ang), (float)std::sin(ang));
+        }
+    if (cudaMalloc(&t->data, n * sizeof(float2)) != cudaSuccess) return HD_ERR_CUDA;
+    if (cudaMemcpy(t->data, host.data(), n * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess)
+        return HD_ERR_CUDA;
+    return HD_OK;
+}
+
+void free_ctx(hd_ctx *ctx) {
+    if (!ctx) return;
+    cudaFree(ctx->table_sliding.data);
+    cudaFree(ctx->table_full.data);
+    cudaFree(ctx->part_o);
+    cudaFree(ctx->part_ml);
+    cudaFree(ctx->stage_k);
+    cudaFree(ctx->stage_v);
+    cudaFree(ctx->q_rot);
+    cudaFree(ctx->err);
+    for (auto e : ctx->ev_begin) cudaEventDestroy(e);
+    for (auto e : ctx->ev_end) cudaEventDestroy(e);
+    delete ctx;
+}
+
+hd_status launch_attention(hd_ctx *ctx, int layer, int batch, const int32_t *context, int max_keys,
+                           int key_set, const float *q_rot, const hd_kv_cache &cache,
+                           const float *sink, void *out, float *lse, cudaStream_t stream) {
+    const CUtensorMap *km = nullptr, *vm = nullptr;
+    hd_status st = maps_for(ctx, layer, cache, batch, &km, &vm);
+    if (st != HD_OK) return st;
+    int32_t chunk_keys = 0, num_chunks = 0;
+    st = hd_plan_split(batch, ctx->cfg.num_kv_heads, max_keys, ctx->num_sms, &chunk_keys, &num_chunks);
+    if (st != HD_OK) return st;
+    if ((int64_t)batch * num_chunks > ctx->part_slots) return HD_ERR_CAPACITY;
+
+    SplitArgs sa{};
+    sa.context = context;
+    sa.q_rot = q_rot;
+    sa.part_o = ctx->part_o;
+    sa.part_ml = ctx->part_ml;
+    sa.err = ctx->err;
+    sa.num_q_heads = ctx->cfg.num_q_heads;
+    sa.num_kv_heads = ctx->cfg.num_kv_heads;
+    sa.chunk_keys = chunk_keys;
+    sa.max_chunks = num_chunks;
+    sa.key_set = key_set;
+    sa.capacity = cache.capacity;
+    sa.window = ctx->cfg.sliding_window;
+    sa.max_context = ctx->cfg.max_context;
+
+    const bool timed = ctx->profiling && key_set == KEYS_FULL && ctx->ev_used < ctx->ev_begin.size();
+    if (timed && cudaEventRecord(ctx->ev_begin[ctx->ev_used], stream) != cudaSuccess)
+        return HD_ERR_CUDA;
+    st = cuda_status(launch_split(km, vm, sa, batch, ctx->group, stream));
+    if (st != HD_OK) return st;
+    ++ctx->launches;
+    if (timed) {
+        if (cudaEventRecord(ctx->ev_end[ctx->ev_used], stream) != cudaSuccess) return HD_ERR_CUDA;
+        ++ctx->ev_used;
+    }
+
+    CombineArgs ca{};
+    ca.context = context;
+    ca.q_rot = q_rot;
+    ca.part_o = ctx->part_o;
+    ca.part_ml = ctx->part_ml;
+    ca.sink = sink;
+    ca.out = static_cast<__nv_bfloat16 *>(out);
+    ca.lse = lse;
+    const size_t stage_off = (size_t)layer * ctx->cfg.max_batch * ctx->cfg.num_kv_heads * kHeadDim;
+    ca.stage_k = ctx->stage_k + stage_off;
+    ca.stage_v = ctx->stage_v + stage_off;
+    ca.cache_k = static_cast<__nv_bfloat16 *>(cache.k);
+    ca.cache_v = static_cast<__nv_bfloat16 *>(cache.v);
+    ca.seq_stride = cache.seq_stride;
+    ca.capacity = cache.capacity;
+    ca.err = ctx->err;
+    ca.num_q_heads = ctx->cfg.num_q_heads;
+    ca.num_kv_heads = ctx->cfg.num_kv_heads;
+    ca.chunk_keys = chunk_keys;
+    ca.max_chunks = num_chunks;
+    ca.key_set = key_set;
+    ca.window = ctx->cfg.sliding_window;
+    ca.max_context = ctx->cfg.max_context;
+    st = cuda_status(launch_combine(ca, batch, ctx->group, stream));
+    if (st == HD_OK) ++ctx->launches;
+    return st;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *hd_status_string(hd_status s) {
+    switch (s) {
+    case HD_OK: return "ok";
+    case HD_ERR_INVALID_ARG: return "invalid argument";
+    case HD_ERR_UNSUPPORTED: return "unsupported shape";
+    case HD_ERR_CAPACITY: return "capacity exceeded";
+    case HD_ERR_CUDA: return "CUDA error";
+    case HD_ERR_STATE: return "invalid state";
+    }
+    return "unknown status";
+}
+
+hd_status hd_validate_config(const hd_config *cfg) {
+    if (!cfg || cfg->num_layers <= 0 || !cfg->layer_types) return HD_ERR_INVALID_ARG;
+    if (cfg->num_q_heads <= 0 || cfg->num_kv_heads <= 0) return HD_ERR_INVALID_ARG;
+    if (cfg->num_q_heads % cfg->num_kv_heads != 0) return HD_ERR_INVALID_ARG;
+    for (int i = 0; i < cfg->num_layers; ++i)
+        if (cfg->layer_types[i] != HD_SLIDING && cfg->layer_types[i] != HD_FULL)
+            return HD_ERR_INVALID_ARG;
+    if (cfg->cache_layout != HD_LAYOUT_AUTO && cfg->cache_layout != HD_LAYOUT_RING &&
+        cfg->cache_layout != HD_LAYOUT_ROLL)
+        return HD_ERR_INVALID_ARG;
+    if (cfg->sliding_window < 2 || cfg->max_batch <= 0 || cfg->max_context < 0)
+        return HD_ERR_INVALID_ARG;
+    if (cfg->max_batch > 65535) return HD_ERR_CAPACITY;
+    for (int rot : {cfg->rotary_dim_sliding, cfg->rotary_dim_full})
+        if (rot < 0 || rot % 2 != 0 || rot > cfg->head_dim) return HD_ERR_INVALID_ARG;
+    if (!(cfg->rope_theta_sliding > 0.0) || !(cfg->rope_theta_full > 0.0)) return HD_ERR_INVALID_ARG;
+    if (cfg->head_dim != kHeadDim) return HD_ERR_UNSUPPORTED;
+    const int g = cfg->num_q_heads / cfg->num_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return HD_ERR_UNSUPPORTED;
+    return HD_OK;
+}
+
+hd_status hd_plan_split(int32_t batch, int32_t num_kv_heads, int32_t max_keys, int32_t num_sms,
+                        int32_t *chunk_keys, int32_t *num_chunks) {
+    if (batch <= 0 || num_kv_heads <= 0 || max_keys < 0 || num_sms <= 0 || !chunk_keys || !num_chunks)
+        return HD_ERR_INVALID_ARG;
+    // Aim at about eight CTAs per SM over the whole grid: enough to cover the
+    // per-CTA ramp-up and ragged lengths, with chunks of 64..512 keys.
+    const int64_t target = 8LL * num_sms;
+    const int64_t want = ((int64_t)batch * num_kv_heads * max_keys + target - 1) / target;
+    int t = kChunkMin;
+    while (t < want && t < kChunkMax) t *= 2;
+    *chunk_keys = t;
+    *num_chunks = (int32_t)((max_keys + t - 1) / t);
+    return HD_OK;
+}
+
+hd_status hybrid_decode_init(const hd_config *cfg, hd_ctx **out_ctx) {
+    if (!out_ctx) return HD_ERR_INVALID_ARG;
+    *out_ctx = nullptr;
+    hd_status st = hd_validate_config(cfg);
+    if (st != HD_OK) return st;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return HD_ERR_STATE;
+    cudaDeviceProp prop;
+    if (cudaGetDeviceProperties(&prop, dev) != cudaSuccess) return HD_ERR_STATE;
+    if (prop.major != 10 || prop.minor != 3) return HD_ERR_UNSUPPORTED;  // built for sm_103a only
+    if (!encode_fn()) return HD_ERR_CUDA;
+
+    hd_ctx *ctx = new (std::nothrow) hd_ctx();
+    if (!ctx) return HD_ERR_CAPACITY;
+    ctx->cfg = *cfg;
+    ctx->layer_types.assign(cfg->layer_types, cfg->layer_types + cfg->num_layers);
+    ctx->cfg.layer_types = ctx->layer_types.data();
+    ctx->device = dev;
+    ctx->num_sms = prop.multiProcessorCount;
+    ctx->group = cfg->num_q_heads / cfg->num_kv_heads;
+    ctx->sliding_layout = cfg->cache_layout == HD_LAYOUT_ROLL ? HD_LAYOUT_ROLL : HD_LAYOUT_RING;
+    ctx->maps.resize(cfg->num_layers);
+
+    bool any_sliding = false, any_full = false;
+    for (int t : ctx->layer_types) (t == HD_SLIDING ? any_sliding : any_full) = true;
+    st = HD_OK;
+    if (any_sliding)
+        st = build_table(&ctx->table_sliding, cfg->rotary_dim_sliding, cfg->rope_theta_sliding,
+                         cfg->max_context);
+    if (st == HD_OK && any_full)
+        st = build_table(&ctx->table_full, cfg->rotary_dim_full, cfg->rope_theta_full,
+                         cfg->max_context);
+    if (st != HD_OK) {
+        free_ctx(ctx);
+        return st;
+    }
+    const int Hq = cfg->num_q_heads, Hkv = cfg->num_kv_heads, B = cfg->max_batch;
+    int64_t slots = 0;
+    if (any_full)
+        slots = worst_part_slots(B, Hkv, cfg->max_context + 1, ctx->num_sms);
+    if (any_sliding) {
+        const int64_t s = worst_part_slots(B, Hkv, cfg->sliding_window, ctx->num_sms);
+        if (s > slots) slots = s;
+    }
+    ctx->part_slots = slots;
+    bool ok = cudaMalloc(&ctx->part_o, (size_t)slots * Hq * kHeadDim * sizeof(float)) == cudaSuccess &&
+              cudaMalloc(&ctx->part_ml, (size_t)slots * Hq * sizeof(float2)) == cudaSuccess &&
+              cudaMalloc(&ctx->q_rot, (size_t)B * Hq * kHeadDim * sizeof(float)) == cudaSuccess &&
+              cudaMalloc(&ctx->err, sizeof(int32_t)) == cudaSuccess &&
+              cudaMemset(ctx->err, 0, sizeof(int32_t)) == cudaSuccess;
+    const size_t stage = (size_t)cfg->num_layers * B * Hkv * kHeadDim;
+    ok = ok && cudaMalloc(&ctx->stage_k, stage * sizeof(__nv_bfloat16)) == cudaSuccess &&
+         cudaMalloc(&ctx->stage_v, stage * sizeof(__nv_bfloat16)) == cudaSuccess;
+    if (!ok) {
+        free_ctx(ctx);
+        return HD_ERR_CUDA;
+    }
+    *out_ctx = ctx;
+    return HD_OK;
+}
+
+hd_status hybrid_decode_destroy(hd_ctx *ctx) {
+    if (!ctx) return HD_ERR_INVALID_ARG;
+    cudaDeviceSynchronize();
+    free_ctx(ctx);
+    return HD_OK;
+}
+
+hd_status rope_append_kv(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
+                         const void *q, const void *k, const void *v, float *q_rot,
+                         hd_kv_cache cache, void *stream) {
+    hd_status st = check_call(ctx, layer, batch, context);
+    if (st != HD_OK) return st;
+    if (!q || !k || !v || !q_rot || !aligned16(q_rot)) return HD_ERR_INVALID_ARG;
+    if ((st = check_cache(ctx, cache)) != HD_OK) return st;
+    const bool sliding = ctx->layer_types[layer] == HD_SLIDING;
+    if (sliding && cache.capacity != sliding_capacity(ctx)) return HD_ERR_CAPACITY;
+    const DeviceTable &tab = sliding ? ctx->table_sliding : ctx->table_full;
+    const int key_set = !sliding ? KEYS_FULL
+                                 : (ctx->sliding_layout == HD_LAYOUT_ROLL ? KEYS_ROLL : KEYS_RING);
+    RopeArgs a{};
+    a.context = context;
+    a.q = static_cast<const __nv_bfloat16 *>(q);
+    a.k = static_cast<const __nv_bfloat16 *>(k);
+    a.v = static_cast<const __nv_bfloat16 *>(v);
+    a.q_rot = q_rot;
+    a.table = tab.data;
+    a.err = ctx->err;
+    a.num_q_heads = ctx->cfg.num_q_heads;
+    a.num_kv_heads = ctx->cfg.num_kv_heads;
+    a.rotary_dim = tab.rotary_dim;
+    a.key_set = key_set;
+    a.window = ctx->cfg.sliding_window;
+    a.max_context = ctx->cfg.max_context;
+    if (key_set == KEYS_RING) {
+        const size_t off = (size_t)layer * ctx->cfg.max_batch * ctx->cfg.num_kv_heads * kHeadDim;
+        a.dst_k = ctx->stage_k + off;
+        a.dst_v = ctx->stage_v + off;
+        a.seq_stride = (int64_t)ctx->cfg.num_kv_heads * kHeadDim;
+        a.capacity = 1;
+    } else {
+        a.dst_k = static_cast<__nv_bfloat16 *>(cache.k);
+        a.dst_v = static_cast<__nv_bfloat16 *>(cache.v);
+        a.seq_stride = cache.seq_stride;
+        a.capacity = cache.capacity;
+    }
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    st = cuda_status(launch_rope_append(a, batch, s));
+    if (st != HD_OK) return st;
+    ++ctx->launches;
+    if (key_set == KEYS_ROLL) {
+        st = cuda_status(launch_roll_window(a, batch, s));
+        if (st == HD_OK) ++ctx->launches;
+    }
+    return st;
+}
+
+hd_status decode_attn_sliding(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
+                              const float *q_rot, hd_kv_cache cache, const float *sink, void *out,
+                              float *lse, void *stream) {
+    hd_status st = check_call(ctx, layer, batch, context);
+    if (st != HD_OK) return st;
+    if (ctx->layer_types[layer] != HD_SLIDING) return HD_ERR_STATE;
+    if (!q_rot || !out || !lse || !aligned16(q_rot)) return HD_ERR_INVALID_ARG;
+    if ((st = check_cache(ctx, cache)) != HD_OK) return st;
+    if (cache.capacity != sliding_capacity(ctx)) return HD_ERR_CAPACITY;
+    const bool roll = ctx->sliding_layout == HD_LAYOUT_ROLL;
+    return launch_attention(ctx, layer, batch, context, roll ? ctx->cfg.sliding_window : cache.capacity,
+                            roll ? KEYS_ROLL : KEYS_RING, q_rot, cache, sink, out, lse,
+                            static_cast<cudaStream_t>(stream));
+}
+
+hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
+                           int32_t max_context_hint, const float *q_rot, hd_kv_cache cache,
+                           const float *sink, void *out, float *lse, void *stream) {
+    hd_status st = check_call(ctx, layer, batch, context);
+    if (st != HD_OK) return st;
+    if (ctx->layer_types[layer] != HD_FULL) return HD_ERR_STATE;
+    if (!q_rot || !out || !lse || !aligned16(q_rot)) return HD_ERR_INVALID_ARG;
+    if ((st = check_cache(ctx, cache)) != HD_OK) return st;
+    if (max_context_hint < 0) return HD_ERR_INVALID_ARG;
+    const int hint = max_context_hint == 0 ? ctx->cfg.max_context : max_context_hint;
+    if (hint > ctx->cfg.max_context) return HD_ERR_CAPACITY;
+    if (hint + 1 > cache.capacity) return HD_ERR_CAPACITY;
+    return launch_attention(ctx, layer, batch, context, hint + 1, KEYS_FULL, q_rot, cache, sink, out,
+                            lse, static_cast<cudaStream_t>(stream));
+}
+
+hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_t max_context_hint,
+                      const hd_layer_io *layers, void *stream) {
+    if (!ctx || !layers) return HD_ERR_INVALID_ARG;
+    for (int i = 0; i < ctx->cfg.num_layers; ++i) {
+        const hd_layer_io &L = layers[i];
+        hd_status st = rope_append_kv(ctx, i, batch, context, L.q, L.k, L.v, ctx->q_rot, L.cache, stream);
+        if (st != HD_OK) return st;
+        if (ctx->layer_types[i] == HD_SLIDING)
+            st = decode_attn_sliding(ctx, i, batch, context, ctx->q_rot, L.cache, L.sink, L.out, L.lse,
+                                     stream);
+        else
+            st = decode_attn_full(ctx, i, batch, context, max_context_hint, ctx->q_rot, L.cache, L.sink,
+                                  L.out, L.lse, stream);
+        if (st != HD_OK) return st;
+    }
+    return HD_OK;
+}
+
+hd_status hybrid_decode_device_errors(hd_ctx *ctx, int32_t *flags, void *stream) {
+    if (!ctx || !flags) return HD_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t host = 0;
+    if (cudaMemcpyAsync(&host, ctx->err, sizeof host, cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaMemsetAsync(ctx->err, 0, sizeof host, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return HD_ERR_CUDA;
+    *flags = host;
+    return HD_OK;
+}
+
+hd_status hybrid_decode_launch_count(hd_ctx *ctx, int64_t *launches) {
+    if (!ctx || !launches) return HD_ERR_INVALID_ARG;
+    *launches = ctx->launches;
+    return HD_OK;
+}
+
+hd_status hybrid_decode_set_profiling(hd_ctx *ctx, int32_t enable) {
+    if (!ctx) return HD_ERR_INVALID_ARG;
+    if (enable && ctx->ev_begin.empty()) {
+        ctx->ev_begin.resize(kProfileEvents);
+        ctx->ev_end.resize(kProfileEvents);
+        for (int i = 0; i < kProfileEvents; ++i)
+            if (cudaEventCreate(&ctx->ev_begin[i]) != cudaSuccess ||
+                cudaEventCreate(&ctx->ev_end[i]) != cudaSuccess)
+                return HD_ERR_CUDA;
+    }
+    ctx->profiling = enable != 0;
+    ctx->ev_used = 0;
+    return HD_OK;
+}
+
+hd_status hybrid_decode_profile(hd_ctx *ctx, double *total_ms, int64_t *launches) {
+    if (!ctx || !total_ms || !launches) return HD_ERR_INVALID_ARG;
+    double sum = 0.0;
+    for (size_t i = 0; i < ctx->ev_used; ++i) {
+        if (cudaEventSynchronize(ctx->ev_end[i]) != cudaSuccess) return HD_ERR_CUDA;
+        float ms = 0.f;
+        if (cudaEventElapsedTime(&ms, ctx->ev_begin[i], ctx->ev_end[i]) != cudaSuccess)
+            return HD_ERR_CUDA;
+        sum += ms;
+    }
+    *total_ms = sum;
+    *launches = (int64_t)ctx->ev_used;
+    ctx->ev_used = 0;
+    return HD_OK;
+}
+
+}  // extern "C"

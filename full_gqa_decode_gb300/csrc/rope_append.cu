@@ -1,0 +1,159 @@
+// Partial Neox RoPE of q and the new k, and the store of the new K/V entry.
+//
+// vllm_omni/edge/spark_export.py, `_rope`: the leading rotary_dim dims are
+// rotated as two halves (x1, x2) -> (x1*cos - x2*sin, x2*cos + x1*sin); the
+// rest pass through.  `_angles` supplies cos/sin at the token's position,
+// which is the number of previous tokens c.  The cache branches of
+// `_Layer.forward` decide where the entry goes: append for full layers, the
+// ring slot for this position (staged here, committed after the ring was
+// read), or a window shifted by one (roll).
+//
+// q is rotated in fp32 (it only feeds the attention).  The stored key is
+// rotated in fp64 from the fp32 table values: both products are exact, so
+// the result is one rounding of the exact rotation, and it is then rounded
+// once to bf16 via round-to-odd to binary32 (Boldo & Melquiond, "Emulation of
+// FMA and correctly rounded sums: proved algorithms using rounding to odd",
+// IEEE TC 2008): an odd-rounded binary32 carries enough bits that its
+// round-to-nearest-even to bf16 equals the direct rounding of the double.
+#include "hd_internal.h"
+
+namespace hd {
+namespace {
+
+__device__ __forceinline__ void set_err(int32_t *err, int32_t bit) { atomicOr(err, bit); }
+
+// One round-to-nearest-even of a double to bf16, through round-to-odd binary32.
+__device__ __forceinline__ __nv_bfloat16 f64_to_bf16_rne(double x) {
+    float t = __double2float_rz(x);
+    if ((double)t != x && isfinite(t)) {
+        unsigned u = __float_as_uint(t) | 1u;   // sticky bit: round to odd
+        t = __uint_as_float(u);
+    }
+    return __float2bfloat16_rn(t);
+}
+
+// Rotated value of dim d of one head vector x (bf16, global), fp32 path.
+__device__ __forceinline__ float rope_f32(const __nv_bfloat16 *x, int d, int rot, const float2 *cs) {
+    if (d >= rot) return __bfloat162float(x[d]);
+    const int half = rot >> 1;
+    const int i = d < half ? d : d - half;
+    const float x1 = __bfloat162float(x[i]), x2 = __bfloat162float(x[i + half]);
+    const float2 t = cs[i];
+    return d < half ? fmaf(x1, t.x, -x2 * t.y) : fmaf(x2, t.x, x1 * t.y);
+}
+
+// Rotated, bf16-rounded value of dim d of the new key (fp64 path).
+__device__ __forceinline__ __nv_bfloat16 rope_key_bf16(const __nv_bfloat16 *x, int d, int rot,
+                                                       const float2 *cs) {
+    if (d >= rot) return x[d];
+    const int half = rot >> 1;
+    const int i = d < half ? d : d - half;
+    const double x1 = (double)__bfloat162float(x[i]), x2 = (double)__bfloat162float(x[i + half]);
+    const double c = (double)cs[i].x, s = (double)cs[i].y;
+    const double y = d < half ? (x1 * c - x2 * s) : (x2 * c + x1 * s);
+    return f64_to_bf16_rne(y);
+}
+
+// Returns the context of sequence b, or -1 after flagging an unusable one.
+__device__ __forceinline__ int checked_context(const RopeArgs &a, int b) {
+    const int c = a.context[b];
+    if (c < 0) {
+        if (threadIdx.x == 0) set_err(a.err, HD_DEVERR_CONTEXT_NEGATIVE);
+        return -1;
+    }
+    if (c > a.max_context) {
+        if (threadIdx.x == 0) set_err(a.err, HD_DEVERR_CONTEXT_PLAN);
+        return -1;
+    }
+    return c;
+}
+
+// One CTA per sequence: q of every head, and (full / ring) the new K/V entry.
+__global__ void __launch_bounds__(256) rope_append_kernel(const RopeArgs a) {
+    const int b = blockIdx.x;
+    const int c = checked_context(a, b);
+    if (c < 0) return;
+    const int D = kHeadDim, rot = a.rotary_dim;
+    const float2 *cs = a.table + (size_t)c * (rot >> 1);
+
+    const __nv_bfloat16 *qb = a.q + (size_t)b * a.num_q_heads * D;
+    float *qr = a.q_rot + (size_t)b * a.num_q_heads * D;
+    for (int idx = threadIdx.x; idx < a.num_q_heads * D; idx += blockDim.x) {
+        const int h = idx / D, d = idx % D;
+        qr[idx] = rope_f32(qb + (size_t)h * D, d, rot, cs);
+    }
+    if (a.key_set == KEYS_ROLL) return;  // the roll kernel stores K/V
+    int slot = 0;
+    if (a.key_set == KEYS_FULL) {
+        if (c >= a.capacity) {
+            if (threadIdx.x == 0) set_err(a.err, HD_DEVERR_CONTEXT_CAPACITY);
+            return;
+        }
+        slot = c;
+    }
+    const __nv_bfloat16 *kb = a.k + (size_t)b * a.num_kv_heads * D;
+    const __nv_bfloat16 *vb = a.v + (size_t)b * a.num_kv_heads * D;
+    for (int idx = threadIdx.x; idx < a.num_kv_heads * D; idx += blockDim.x) {
+        const int h = idx / D, d = idx % D;
+        const size_t o = (size_t)b * a.seq_stride + ((size_t)h * a.capacity + slot) * D + d;
+        a.dst_k[o] = rope_key_bf16(kb + (size_t)h * D, d, rot, cs);
+        a.dst_v[o] = vb[idx];
+    }
+}
+
+// One CTA per (kv head, sequence) of a roll-layout sliding layer: shift the
+// window down by one row once it is full, then write the new entry at the end.
+// Rows move in groups of 8 (one 16-byte chunk per thread for K and for V):
+// each group is read in full before any of it is overwritten, and the next
+// group's first row is written only after the next read phase.
+__global__ void __launch_bounds__(256) roll_window_kernel(const RopeArgs a) {
+    const int h = blockIdx.x, b = blockIdx.y;
+    const int c = checked_context(a, b);
+    if (c < 0) return;
+    const int D = kHeadDim, W = a.window;
+    const size_t base = (size_t)b * a.seq_stride + (size_t)h * a.capacity * D;
+    uint4 *K4 = reinterpret_cast<uint4 *>(a.dst_k + base);
+    uint4 *V4 = reinterpret_cast<uint4 *>(a.dst_v + base);
+    constexpr int kChunksPerRow = kHeadDim * 2 / 16;  // 32
+    int row_new = c;
+    if (c >= W) {
+        row_new = W - 1;
+        const int r_local = threadIdx.x / kChunksPerRow, ch = threadIdx.x % kChunksPerRow;
+        for (int r0 = 0; r0 < W - 1; r0 += 8) {
+            const int src = r0 + 1 + r_local;
+            uint4 kk = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
+            const bool live = src <= W - 1;
+            if (live) {
+                kk = K4[(size_t)src * kChunksPerRow + ch];
+                vv = V4[(size_t)src * kChunksPerRow + ch];
+            }
+            __syncthreads();
+            if (live) {
+                K4[(size_t)(src - 1) * kChunksPerRow + ch] = kk;
+                V4[(size_t)(src - 1) * kChunksPerRow + ch] = vv;
+            }
+            __syncthreads();
+        }
+    }
+    const float2 *cs = a.table + (size_t)c * (a.rotary_dim >> 1);
+    const __nv_bfloat16 *kh = a.k + ((size_t)b * a.num_kv_heads + h) * D;
+    const __nv_bfloat16 *vh = a.v + ((size_t)b * a.num_kv_heads + h) * D;
+    for (int d = threadIdx.x; d < D; d += blockDim.x) {
+        a.dst_k[base + (size_t)row_new * D + d] = rope_key_bf16(kh, d, a.rotary_dim, cs);
+        a.dst_v[base + (size_t)row_new * D + d] = vh[d];
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_rope_append(const RopeArgs &a, int batch, cudaStream_t s) {
+    rope_append_kernel<<<batch, 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_roll_window(const RopeArgs &a, int batch, cudaStream_t s) {
+    roll_window_kernel<<<dim3(a.num_kv_heads, batch), 256, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace hd

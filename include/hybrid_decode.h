@@ -1,0 +1,203 @@
+/*
+ * hybrid_decode.h -- C ABI of the GB300 (sm_103a) decode-attention library for
+ * a hybrid sliding-window / full-attention GQA model.
+ *
+ * The operation is one autoregressive decode step of attention with the KV
+ * cache passed in and out as explicit caller-owned tensors, as stated by
+ * vllm_omni/edge/spark_export.py (module docstring; `SparkDecodeStep`,
+ * `_Layer.forward`).  Per layer and sequence b, with c = context[b] previous
+ * tokens (the new token sits at position c):
+ *   - rotate q and the new k with Neox-style partial RoPE (`_rope`, `_angles`):
+ *     the first rotary_dim dims as half-pairs, the rest passing through;
+ *     sliding layers use their own rotary_dim/theta, full layers theirs;
+ *   - score  s_j = q_rot . K_j / sqrt(head_dim)  over the layer's key set and
+ *     take one softmax (`_Layer.forward`, ring and roll branches).  Query head
+ *     h reads kv head h / (num_q_heads / num_kv_heads) (GQA fold);
+ *   - key set: full layers score positions 0..c; sliding layers the window
+ *     max(0, c-window+1)..c, the window counting the current token
+ *     (`SparkStepConfig.cache_len`);
+ *   - lse = log(sum_j exp(s_j)) (natural log, without the sink); with a
+ *     per-head fp32 sink the output is multiplied by
+ *     exp(lse) / (exp(lse) + exp(sink[h]))   (flashmla_sparse.py,
+ *     `HYV4FlashMLASparseImpl` docstring); a sink of -inf is no sink;
+ *   - cache update: full layers append at index c; sliding ring layouts write
+ *     slot c mod (window-1), after the cached entries have been scored; the
+ *     sliding roll layout shifts its window by one once full and appends
+ *     (`cache_layout` docstring; ring and roll branches).
+ *
+ * Numeric contract: bf16 q/k/v/caches/out, fp32 accumulation, fp32 lse.  RoPE
+ * tables hold fp32 cos/sin evaluated in fp64 at init.  The written key is
+ * bf16_rne(k1*c - k2*s) / bf16_rne(k2*c + k1*s) computed in fp64 from the fp32
+ * table values, so it is reproducible bit for bit; V is stored bit for bit.
+ *
+ * Memory and ownership: every tensor argument is a DEVICE pointer owned by the
+ * caller (PyTorch allocates them); the library owns only the hd_ctx and the
+ * device workspace it allocates in hybrid_decode_init (RoPE tables, split-K
+ * partials, the ring staging rows).  No call after init allocates.  Every call
+ * taking a `stream` (a cudaStream_t; NULL = legacy default stream) is
+ * asynchronous on that stream.  Calls that use one hd_ctx must be ordered on
+ * one stream (the workspace is shared).
+ *
+ * Errors: every call returns an hd_status and nothing throws or aborts across
+ * the ABI.  Arguments that can be checked on the host are checked before any
+ * launch.  Values only the device sees (context lengths) are checked by the
+ * kernels, which skip the offending sequence and record a bit in the context's
+ * device error word; read and clear it with hybrid_decode_device_errors.
+ *
+ * Layouts (all row-major, elements):
+ *   q, out           [batch][num_q_heads][head_dim]
+ *   k, v (new token) [batch][num_kv_heads][head_dim]
+ *   q_rot            [batch][num_q_heads][head_dim] fp32
+ *   lse              [batch][num_q_heads] fp32
+ *   sink             [num_q_heads] fp32
+ *   cache k / v      sequence b starts at b * seq_stride; within it
+ *                    [num_kv_heads][capacity][head_dim]
+ */
+#ifndef HYBRID_DECODE_H
+#define HYBRID_DECODE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    HD_OK = 0,
+    HD_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad enum, misaligned buffer */
+    HD_ERR_UNSUPPORTED = 2,  /* a shape this build does not implement (head_dim != 256, group > 8) */
+    HD_ERR_CAPACITY = 3,     /* batch > max_batch, cache capacity too small, context hint too large */
+    HD_ERR_CUDA = 4,         /* a CUDA runtime/driver call or a launch failed */
+    HD_ERR_STATE = 5         /* wrong layer type for the call, or no device available */
+} hd_status;
+
+typedef enum { HD_SLIDING = 0, HD_FULL = 1 } hd_layer_type;
+
+/* Cache layout of sliding layers (spark_export.py, `SparkStepConfig.cache_layout`):
+ * AUTO picks RING for sliding layers; full layers always append. */
+typedef enum { HD_LAYOUT_AUTO = 0, HD_LAYOUT_RING = 1, HD_LAYOUT_ROLL = 2 } hd_layout;
+
+/* Bits of the device error word (hybrid_decode_device_errors). */
+enum {
+    HD_DEVERR_CONTEXT_NEGATIVE = 1,  /* context[b] < 0                                     */
+    HD_DEVERR_CONTEXT_CAPACITY = 2,  /* full layer: context[b] >= cache capacity            */
+    HD_DEVERR_CONTEXT_PLAN = 4,      /* context[b] > max_context (table / split plan)       */
+    HD_DEVERR_WAIT_TIMEOUT = 8       /* a pipeline wait gave up after its time limit        */
+};
+
+typedef struct hd_ctx hd_ctx;
+
+/* Model shape (spark_export.py, `SparkStepConfig`), validated like its
+ * `__post_init__`: num_q_heads must be a multiple of num_kv_heads, every layer
+ * type must be HD_SLIDING or HD_FULL, the layout must be one of hd_layout. */
+typedef struct {
+    int32_t num_layers;
+    const int32_t *layer_types;    /* host array [num_layers] of hd_layer_type        */
+    int32_t num_q_heads;
+    int32_t num_kv_heads;          /* num_q_heads / num_kv_heads <= 8                  */
+    int32_t head_dim;              /* 256                                              */
+    int32_t sliding_window;        /* window counting the current token (512)          */
+    int32_t rotary_dim_sliding;    /* even, <= head_dim (256)                          */
+    int32_t rotary_dim_full;       /* even, <= head_dim (64)                           */
+    double rope_theta_sliding;     /* 1e4                                              */
+    double rope_theta_full;        /* 5e6                                              */
+    int32_t cache_layout;          /* hd_layout for the sliding layers                 */
+    int32_t max_batch;             /* largest batch any call passes                    */
+    int32_t max_context;           /* largest context (previous tokens) any call uses  */
+} hd_config;
+
+/* One layer's KV cache (caller-owned device memory, bf16). capacity is the
+ * number of entries per (sequence, kv head): window-1 for a sliding ring,
+ * window for a sliding roll window, at least max_context+1 for a full layer.
+ * seq_stride >= num_kv_heads*capacity*head_dim and a multiple of 8; k and v
+ * 16-byte aligned. */
+typedef struct {
+    void *k;
+    void *v;
+    int64_t seq_stride;
+    int32_t capacity;
+} hd_kv_cache;
+
+/* Per-layer tensors of a whole decode step (decode_step). */
+typedef struct {
+    const void *q;        /* bf16 [batch][num_q_heads][head_dim]                   */
+    const void *k;        /* bf16 [batch][num_kv_heads][head_dim]                  */
+    const void *v;        /* bf16 [batch][num_kv_heads][head_dim]                  */
+    hd_kv_cache cache;
+    const float *sink;    /* fp32 [num_q_heads] or NULL (no sink)                  */
+    void *out;            /* bf16 [batch][num_q_heads][head_dim]                   */
+    float *lse;           /* fp32 [batch][num_q_heads]                             */
+} hd_layer_io;
+
+/* Pure host check of a configuration (no device use). */
+hd_status hd_validate_config(const hd_config *cfg);
+
+/* Split-K plan used for a layer call (pure host function, no device use):
+ * keys per chunk and the number of chunks (the grid's key dimension) for
+ * `batch` sequences of at most `max_keys` scored cache keys on `num_sms` SMs. */
+hd_status hd_plan_split(int32_t batch, int32_t num_kv_heads, int32_t max_keys, int32_t num_sms,
+                        int32_t *chunk_keys, int32_t *num_chunks);
+
+/* Creates a context on the current CUDA device: validates cfg, builds the
+ * RoPE tables for positions 0..max_context (cos/sin in fp64, stored fp32) and
+ * allocates the workspace sized by max_batch/max_context.  Synchronous. */
+hd_status hybrid_decode_init(const hd_config *cfg, hd_ctx **out_ctx);
+
+/* Frees the context and its workspace (synchronises the device first). */
+hd_status hybrid_decode_destroy(hd_ctx *ctx);
+
+/* Rotates q (written to q_rot, fp32) and the new k for one layer, and stores
+ * the new K/V entry: full layers at index context[b]; sliding ring layers into
+ * the context's staging row (committed to slot context[b] mod (window-1) by
+ * decode_attn_sliding after it has read the ring); sliding roll layers shift
+ * their window by one when it is full and append.  (spark_export.py `_rope`,
+ * `_angles`, `_Layer.forward` cache branches.) */
+hd_status rope_append_kv(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
+                         const void *q, const void *k, const void *v, float *q_rot,
+                         hd_kv_cache cache, void *stream);
+
+/* Attention of a sliding layer over its window: the ring's valid slots plus
+ * the staged new entry (ring), or the rolled window (roll); split-K over the
+ * keys, then an LSE combine that applies the sink, writes out/lse and commits
+ * the staged ring entry.  Must follow rope_append_kv of the same layer on the
+ * same stream. */
+hd_status decode_attn_sliding(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
+                              const float *q_rot, hd_kv_cache cache, const float *sink,
+                              void *out, float *lse, void *stream);
+
+/* Attention of a full layer over positions 0..context[b] (the new entry was
+ * appended by rope_append_kv): split-K over chunks of keys sized from
+ * max_context_hint (an upper bound on every context[b] of this call, <=
+ * max_context; 0 means max_context), then the LSE combine with the sink. */
+hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
+                           int32_t max_context_hint, const float *q_rot, hd_kv_cache cache,
+                           const float *sink, void *out, float *lse, void *stream);
+
+/* One decode step over all layers in order: rope_append_kv then the layer's
+ * attention, with q_rot held in the context's workspace.  `layers` is a host
+ * array [num_layers]. */
+hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_t max_context_hint,
+                      const hd_layer_io *layers, void *stream);
+
+/* Reads and clears the device error word (HD_DEVERR_* bits).  Synchronises
+ * `stream`. */
+hd_status hybrid_decode_device_errors(hd_ctx *ctx, int32_t *flags, void *stream);
+
+/* Kernel launches issued by this context since init (host counter). */
+hd_status hybrid_decode_launch_count(hd_ctx *ctx, int64_t *launches);
+
+/* Profiling: when enabled, the split-K kernel of every decode_attn_full call
+ * is bracketed by CUDA events on its stream.  hybrid_decode_profile
+ * synchronises, returns the summed kernel time and launch count since the
+ * last reset, and resets them. */
+hd_status hybrid_decode_set_profiling(hd_ctx *ctx, int32_t enable);
+hd_status hybrid_decode_profile(hd_ctx *ctx, double *total_ms, int64_t *launches);
+
+/* Static text for a status code. */
+const char *hd_status_string(hd_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* HYBRID_DECODE_H */

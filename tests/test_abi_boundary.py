@@ -1,0 +1,89 @@
+"""The C-ABI library builds, loads and exports every entry point its headers
+declare; host-side validation and planning behave as documented.  No GPU."""
+import ctypes
+import glob
+import os
+import re
+import subprocess
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        names += re.findall(r"^(?:hd_status|const char \*)\s*(\w+)\s*\(", text, re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for want in ("hybrid_decode_init", "rope_append_kv", "decode_attn_sliding", "decode_attn_full",
+                 "decode_step", "hybrid_decode_destroy", "hd_status_string"):
+        assert want in names
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    lib = ctypes.CDLL(libpath)
+    nm = subprocess.run(["nm", "-D", "--defined-only", libpath], capture_output=True, text=True,
+                        check=True).stdout
+    exported = set(re.findall(r"\s[TW]\s+(\w+)$", nm, re.M))
+    for name in declared_functions():
+        assert name in exported, f"{name} is declared but not exported"
+        assert hasattr(lib, name)
+
+
+def test_status_strings(hd):
+    assert hd.hd_status_string(0) == "ok"
+    assert hd.hd_status_string(3) == "capacity exceeded"
+
+
+def _cfg(hd, **kw):
+    base = dict(layer_types=[hd.HD_SLIDING] * 3 + [hd.HD_FULL], max_batch=4, max_context=4096)
+    base.update(kw)
+    return hd.Config(**base)
+
+
+def test_validate_config_mirrors_post_init(hd):
+    assert hd.hd_validate_config(_cfg(hd)) == 0
+    assert hd.hd_validate_config(_cfg(hd, num_q_heads=6, num_kv_heads=4)) == 1   # not a multiple
+    assert hd.hd_validate_config(_cfg(hd, layer_types=[0, 1, 7])) == 1          # unknown layer type
+    assert hd.hd_validate_config(_cfg(hd, cache_layout=3)) == 1                 # unknown layout
+    assert hd.hd_validate_config(_cfg(hd, rotary_dim_full=63)) == 1             # odd rotary dim
+    assert hd.hd_validate_config(_cfg(hd, rotary_dim_sliding=512)) == 1         # beyond head_dim
+    assert hd.hd_validate_config(_cfg(hd, rope_theta_full=0.0)) == 1
+    assert hd.hd_validate_config(_cfg(hd, max_batch=0)) == 1
+    assert hd.hd_validate_config(_cfg(hd, head_dim=128, rotary_dim_sliding=128)) == 2
+    assert hd.hd_validate_config(_cfg(hd, num_q_heads=32, num_kv_heads=2)) == 2  # group 16
+    for g in (1, 2, 4, 8):
+        assert hd.hd_validate_config(_cfg(hd, num_q_heads=2 * g, num_kv_heads=2)) == 0
+
+
+@pytest.mark.parametrize("batch,max_keys", [(1, 4097), (64, 32769), (4, 131073), (256, 8193),
+                                            (64, 511), (1, 1), (2, 0), (256, 512)])
+def test_plan_split_covers_the_keys(hd, batch, max_keys):
+    ck, nc = hd.hd_plan_split(batch, 2, max_keys, 152)
+    assert ck in (64, 128, 256, 512)
+    assert nc * ck >= max_keys and (nc - 1) * ck < max(max_keys, 1)
+
+
+def test_plan_split_long_context_uses_many_chunks(hd):
+    ck, nc = hd.hd_plan_split(4, 2, 131073, 152)
+    assert nc >= 64
+
+
+def test_plan_split_rejects_bad_arguments(hd):
+    with pytest.raises(hd.HDError):
+        hd.hd_plan_split(0, 2, 10, 152)
+
+
+def test_init_without_a_gpu_fails_cleanly(hd):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    with pytest.raises(hd.HDError) as e:
+        hd.hybrid_decode_init(_cfg(hd))
+    assert e.value.status in (4, 5)
