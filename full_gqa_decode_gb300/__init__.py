@@ -153,7 +153,17 @@ def kv_cache(k: torch.Tensor, v: torch.Tensor) -> hd_kv_cache:
         raise ValueError("caches must be bf16")
     if k.stride(3) != 1 or k.stride(2) != k.shape[3] or k.stride(1) != k.shape[2] * k.shape[3]:
         raise ValueError("each sequence's cache must be contiguous [kv_heads, capacity, head_dim]")
-    return hd_kv_cache(k.data_ptr(), v.data_ptr(), k.stride(0), k.shape[2])
+    if not k.is_cuda or not v.is_cuda:
+        raise ValueError("caches must be CUDA tensors")
+    c = hd_kv_cache(k.data_ptr(), v.data_ptr(), k.stride(0), k.shape[2])
+    c.batch = k.shape[0]  # sequences the tensors hold; calls may not pass a larger batch
+    return c
+
+
+def _check_batch(cache: hd_kv_cache, batch: int) -> None:
+    held = getattr(cache, "batch", None)
+    if held is not None and held < batch:
+        raise ValueError(f"cache holds {held} sequences, call passes batch {batch}")
 
 
 def hd_validate_config(cfg: Config) -> int:
@@ -202,6 +212,7 @@ def hybrid_decode_destroy(ctx: Context) -> None:
 
 def rope_append_kv(ctx: Context, layer: int, context: torch.Tensor, q, k, v, q_rot, cache: hd_kv_cache,
                    stream=None) -> None:
+    _check_batch(cache, q.shape[0])
     _check(_lib.rope_append_kv(ctx.handle, layer, q.shape[0], _ptr(context), _ptr(q), _ptr(k), _ptr(v),
                                _ptr(q_rot), cache, _stream(stream)), "rope_append_kv")
 
@@ -209,6 +220,7 @@ def rope_append_kv(ctx: Context, layer: int, context: torch.Tensor, q, k, v, q_r
 def decode_attn_sliding(ctx: Context, layer: int, context, q_rot, cache: hd_kv_cache, sink, out, lse,
                         stream=None) -> None:
     _check_sink(sink, ctx.cfg.num_q_heads, q_rot)
+    _check_batch(cache, q_rot.shape[0])
     _check(_lib.decode_attn_sliding(ctx.handle, layer, q_rot.shape[0], _ptr(context), _ptr(q_rot),
                                     cache, _ptr(sink), _ptr(out), _ptr(lse), _stream(stream)),
            "decode_attn_sliding")
@@ -217,6 +229,7 @@ def decode_attn_sliding(ctx: Context, layer: int, context, q_rot, cache: hd_kv_c
 def decode_attn_full(ctx: Context, layer: int, context, q_rot, cache: hd_kv_cache, sink, out, lse,
                      max_context_hint: int = 0, stream=None) -> None:
     _check_sink(sink, ctx.cfg.num_q_heads, q_rot)
+    _check_batch(cache, q_rot.shape[0])
     _check(_lib.decode_attn_full(ctx.handle, layer, q_rot.shape[0], _ptr(context), max_context_hint,
                                  _ptr(q_rot), cache, _ptr(sink), _ptr(out), _ptr(lse),
                                  _stream(stream)), "decode_attn_full")
@@ -225,6 +238,7 @@ def decode_attn_full(ctx: Context, layer: int, context, q_rot, cache: hd_kv_cach
 def layer_io(q, k, v, cache: hd_kv_cache, sink, out, lse) -> hd_layer_io:
     if sink is not None:
         _check_sink(sink, q.shape[1], q)
+    _check_batch(cache, q.shape[0])
     return hd_layer_io(_ptr(q), _ptr(k), _ptr(v), cache, _ptr(sink), _ptr(out), _ptr(lse))
 
 
