@@ -1,0 +1,506 @@
+"""Benchmark of the hybrid decode-attention step on GB300.
+
+Workload (default): the 28-layer step ([sliding x3, full] x7, Spark-X2.5
+shape from vllm_omni/edge/spark_export.py) at batch 64 with per-sequence
+contexts uniform in [512, 32768], 8 q / 2 kv heads, head_dim 256, bf16 KV
+contiguous per sequence with a lengths array, sink fp32 N(0,1).  One step =
+rope_append_kv + attention for every layer, through decode_step.
+
+Metric: KV-read HBM GB/s = scored-key bytes per step / step time, where a
+scored key costs one bf16 K row and one bf16 V row per kv head (1024 B at
+head_dim 256); sliding layers score min(c, 511) + 1 keys, full layers c + 1.
+The line also gives us per step, the roofline of the dominant kernel (the
+full-layer split-K pass), the oracle timed on the host cores, an end-to-end
+figure with host buffers, and the batch-1 28-layer step as a secondary figure.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Multi-GPU (torchrun, one rank per GPU): every rank runs the same per-GPU
+workload on its own sequences (weak scaling, no data-path collective); the
+step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import concurrent.futures as cf
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+KV_ROW_BYTES = 2 * synth.HEAD_DIM * 2       # K row + V row, bf16, one kv head
+DEFAULT_WORKLOAD = "step28_b64_c512_32768"
+SECONDARY_WORKLOAD = "step28_b1_c4096"
+METRIC = "KV-read HBM GB/s (% of GB300 peak); µs per 28-layer decode step"
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_split_full_b64_traffic.txt")
+
+
+# ------------------------------------------------------------------ helpers --
+
+def scored_keys(layer_type: int, context: np.ndarray, layout: int) -> np.ndarray:
+    if layer_type == synth.FULL:
+        return context.astype(np.int64) + 1
+    keep = synth.WINDOW - 1 if layout != synth.LAYOUT_ROLL else synth.WINDOW
+    if layout == synth.LAYOUT_ROLL:
+        return np.minimum(context.astype(np.int64) + 1, keep)
+    return np.minimum(context.astype(np.int64), keep) + 1
+
+
+def step_bytes(types, context, num_kv_heads, layout) -> int:
+    return int(sum(scored_keys(t, context, layout).sum() for t in types) * num_kv_heads * KV_ROW_BYTES)
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": d["hbm_gbs"], "source": "measured"}
+    return {"hbm_gbs": 6800.0, "source": "fallback"}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for f in ("attn_decode.cu", "hd_internal.h"):
+        with open(os.path.join(ROOT, "full_gqa_decode_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic():
+    """DRAM bytes per launch of the full-layer split kernel from the committed ncu
+    summary, or None when the summary is absent or the kernel changed since."""
+    if not os.path.exists(PROFILE_SUMMARY):
+        return None
+    kv = {}
+    with open(PROFILE_SUMMARY) as f:
+        for line in f:
+            if ":" in line:
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+    if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        import torch
+        self.proc = None
+        try:
+            self.gpu = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            self.gpu = str(device.index)
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_dev{device.index}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            self.proc.wait(timeout=5)
+            self.fh.close()
+
+    def summary(self) -> dict:
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                except ValueError:
+                    continue
+                for n, val in zip(names, parts[5:9]):
+                    if val.lower() == "active":
+                        reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------- distributed plumbing --
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("HD_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def barrier(world: int, device=None):
+    if world > 1:
+        import torch.distributed as dist
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def reduce_timing(elapsed_ms: float, units: float, world: int, device=None) -> tuple[float, float]:
+    """Max of the step time over ranks and the sum of the work units over ranks."""
+    if world == 1:
+        return elapsed_ms, units
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([elapsed_ms], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), float(u.item())
+
+
+# ------------------------------------------------------------- the workload --
+
+class Workload:
+    """Device-resident inputs of one workload (caches, per-layer q/k/v, outputs)."""
+
+    def __init__(self, name: str, device, seed: int = 0, layout: int = synth.LAYOUT_AUTO):
+        import torch
+        import full_gqa_decode_gb300 as hd
+        spec = synth.WORKLOADS[name]
+        self.name, self.spec, self.layout = name, spec, layout
+        self.types = list(spec["layer_types"])
+        self.B, self.Hq, self.Hkv = spec["batch"], spec["num_q_heads"], spec["num_kv_heads"]
+        D = synth.HEAD_DIM
+        rng = synth.generator(seed)
+        self.context = synth.context_lengths(rng, spec["lengths"], self.B)
+        self.max_ctx = int(self.context.max())
+        sink = synth.sink_vector(rng, spec["sink"], self.Hq)
+        self.cfg = hd.Config(layer_types=self.types, num_q_heads=self.Hq, num_kv_heads=self.Hkv,
+                             cache_layout=layout, max_batch=self.B, max_context=self.max_ctx)
+        self.ctx = hd.hybrid_decode_init(self.cfg)
+        self.context_d = torch.from_numpy(self.context).to(device)
+        self.sink = None if sink is None else sink.to(device)
+        ring = layout != synth.LAYOUT_ROLL
+        self.layers, self.io = [], []
+        for i, t in enumerate(self.types):
+            cap = (synth.WINDOW - 1 if ring else synth.WINDOW) if t == synth.SLIDING else self.max_ctx + 1
+            kc = torch.empty(self.B, self.Hkv, cap, D, dtype=torch.bfloat16, device=device)
+            vc = torch.empty_like(kc)
+            synth.cuda_normal_bf16_(kc, seed * 1000 + 2 * i + 1)
+            synth.cuda_normal_bf16_(vc, seed * 1000 + 2 * i + 2)
+            g = torch.Generator(device=device)
+            g.manual_seed(seed * 1000 + 500 + i)
+            q = torch.randn(self.B, self.Hq, D, generator=g, device=device).to(torch.bfloat16)
+            k = torch.randn(self.B, self.Hkv, D, generator=g, device=device).to(torch.bfloat16)
+            v = torch.randn(self.B, self.Hkv, D, generator=g, device=device).to(torch.bfloat16)
+            out = torch.empty(self.B, self.Hq, D, dtype=torch.bfloat16, device=device)
+            lse = torch.empty(self.B, self.Hq, dtype=torch.float32, device=device)
+            cache = hd.kv_cache(kc, vc)
+            self.layers.append(dict(q=q, k=k, v=v, kc=kc, vc=vc, out=out, lse=lse, cache=cache))
+            self.io.append(hd.layer_io(q, k, v, cache, self.sink, out, lse))
+        self.bytes = step_bytes(self.types, self.context, self.Hkv, layout)
+        full_idx = [i for i, t in enumerate(self.types) if t == synth.FULL]
+        self.full_layer_bytes = (int(scored_keys(synth.FULL, self.context, layout).sum()) * self.Hkv
+                                 * KV_ROW_BYTES) if full_idx else 0
+
+    def step(self, stream=None):
+        import full_gqa_decode_gb300 as hd
+        hd.decode_step(self.ctx, self.context_d, self.io, self.B, self.max_ctx, stream)
+
+
+def time_steps(run, steps: int, warmup: int, world: int, device) -> float:
+    """ms per step over `steps` steps (after `warmup`), CUDA events on the current stream."""
+    import torch
+    for _ in range(warmup):
+        run()
+    torch.cuda.synchronize()
+    barrier(world, device)
+    torch.cuda.synchronize()
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    start.record()
+    for _ in range(steps):
+        run()
+    end.record()
+    torch.cuda.synchronize()
+    barrier(world, device)
+    torch.cuda.synchronize()
+    return start.elapsed_time(end) / steps
+
+
+# ------------------------------------------------------------- CPU baseline --
+
+def oracle_sample(layer_caches, context, types, Hq, Hkv, sink, rng, threads):
+    """Times the oracle on one [S,S,S,F] block of the step for the given sequences.
+    layer_caches: per layer (kc, vc) uint16 arrays [B, Hkv, cap, D]. Returns (seconds, bytes)."""
+    import oracle
+    orc = oracle.load()
+    D = synth.HEAD_DIM
+    B = len(context)
+    jobs = []
+    for li, t in enumerate(types):
+        rot, theta = synth.ROPE[t]
+        kc, vc = layer_caches[li]
+        for b in range(B):
+            q = synth.bits(synth.normal_bf16(rng, (1, Hq, D)))
+            k = synth.bits(synth.normal_bf16(rng, (1, Hkv, D)))
+            v = synth.bits(synth.normal_bf16(rng, (1, Hkv, D)))
+            jobs.append(dict(layer_type=t, layout=synth.LAYOUT_RING, window=synth.WINDOW, rotary_dim=rot,
+                             rope_theta=theta, context=context[b:b + 1], q=q, k=k, v=v,
+                             kcache=np.ascontiguousarray(kc[b:b + 1]), vcache=np.ascontiguousarray(vc[b:b + 1]),
+                             sink=sink))
+    nbytes = step_bytes(types, context, Hkv, synth.LAYOUT_RING)
+    t0 = time.perf_counter()
+    with cf.ThreadPoolExecutor(threads) as ex:   # ctypes releases the GIL in the oracle
+        list(ex.map(lambda j: orc.decode_layer(**j), jobs))
+    return time.perf_counter() - t0, nbytes
+
+
+def host_block_caches(spec, context, rng):
+    """Host-generated caches of one [S,S,S,F] block (for the reference arm)."""
+    B, Hkv, D = len(context), spec["num_kv_heads"], synth.HEAD_DIM
+    out = []
+    for t in [synth.SLIDING, synth.SLIDING, synth.SLIDING, synth.FULL]:
+        cap = synth.WINDOW - 1 if t == synth.SLIDING else int(context.max()) + 1
+        kc = np.empty((B, Hkv, cap, D), np.uint16)
+        vc = np.empty_like(kc)
+        for b in range(B):
+            n = min(int(context[b]), cap)
+            kc[b] = 0x7FC0
+            vc[b] = 0x7FC0
+            kc[b, :, :n] = synth.bits(synth.normal_bf16(rng, (Hkv, n, D)))
+            vc[b, :, :n] = synth.bits(synth.normal_bf16(rng, (Hkv, n, D)))
+        out.append((kc, vc))
+    return out
+
+
+def cpu_threads() -> int:
+    return len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
+
+
+# ----------------------------------------------------------------- the arms --
+
+def run_reference(args, world, rank) -> int:
+    """The oracle, as it stands, on the host cores: each step is a bounded sample
+    (one [S,S,S,F] block of the step over every sequence)."""
+    if rank != 0:
+        return 0
+    spec = synth.WORKLOADS[args.workload]
+    rng = synth.generator(0)
+    context = synth.context_lengths(rng, spec["lengths"], spec["batch"])
+    sink = synth.sink_vector(rng, spec["sink"], spec["num_q_heads"])
+    sink = None if sink is None else sink.numpy()
+    caches = host_block_caches(spec, context, rng)
+    threads = cpu_threads()
+    block = [synth.SLIDING, synth.SLIDING, synth.SLIDING, synth.FULL]
+    for _ in range(args.warmup):
+        oracle_sample(caches, context, block, spec["num_q_heads"], spec["num_kv_heads"], sink, rng, threads)
+    secs, nbytes = 0.0, 0
+    for _ in range(args.steps):
+        s, n = oracle_sample(caches, context, block, spec["num_q_heads"], spec["num_kv_heads"], sink, rng,
+                             threads)
+        secs += s
+        nbytes += n
+    gbs = nbytes / secs / 1e9
+    full_bytes = step_bytes(spec["layer_types"], context, spec["num_kv_heads"], synth.LAYOUT_RING)
+    sample = (f"one [sliding x3, full] block of the 28-layer step over all {len(context)} sequences "
+              f"({nbytes // args.steps / 1e9:.2f} GB of scored KV per step); fp64 oracle, "
+              f"{threads} host threads")
+    line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(full_bytes / (gbs * 1e9) * 1e3, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": args.workload, "global_batch": int(len(context)),
+                       "contexts": "uniform [512, 32768]" if spec["lengths"][0] == "uniform" else str(spec["lengths"]),
+                       "l2": "inputs larger than L2", "parallelism": f"dp{world}"},
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args, world, rank, local) -> int:
+    import torch
+    import full_gqa_decode_gb300 as hd
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    peaks = measured_peaks()
+    wl = Workload(args.workload, device, seed=rank)
+    consumer = hd.HD_CONSUMER_TENSOR_CORE if args.consumer == "tensor-core" else hd.HD_CONSUMER_CUDA_CORE
+    hd.hybrid_decode_set_consumer(wl.ctx, consumer)
+    torch.cuda.synchronize()
+
+    # device-resident timed region (W warm-up steps first, then exactly K timed steps)
+    hd.hybrid_decode_set_profiling(wl.ctx, True)
+    with ClockSampler(device) as clocks:
+        for _ in range(args.warmup):
+            wl.step()
+        torch.cuda.synchronize()
+        hd.hybrid_decode_profile(wl.ctx)  # drop the warm-up records
+        n0 = hd.hybrid_decode_launch_count(wl.ctx)
+        ms = time_steps(wl.step, args.steps, 0, world, device)
+        n1 = hd.hybrid_decode_launch_count(wl.ctx)
+        split_ms, split_launches = hd.hybrid_decode_profile(wl.ctx)
+    hd.hybrid_decode_set_profiling(wl.ctx, False)
+    clk = clocks.summary()
+    flags = hd.hybrid_decode_device_errors(wl.ctx)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x} during the benchmark")
+    ms_max, total_bytes = reduce_timing(ms, wl.bytes, world, device)
+    gbs = total_bytes / (ms_max * 1e-3) / 1e9
+
+    # roofline of the dominant kernel: the full-layer split-K pass
+    avg_split_ms = split_ms / max(split_launches, 1)
+    achieved = wl.full_layer_bytes / (avg_split_ms * 1e-3) / 1e9 if split_launches else None
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
+                "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None,
+                "traffic": profiled_traffic(), "kernel": f"attn_layer_kernel, full layers ({args.consumer})",
+                "algorithmic_bytes_per_launch": wl.full_layer_bytes,
+                "avg_launch_ms": round(avg_split_ms, 4), "peak_source": peaks["source"]}
+
+    # end to end: host buffers, copies inside the timed region
+    e2e = e2e_measure(wl, args, world, device)
+
+    result = None
+    if rank == 0:
+        cpu = cpu_baseline(wl, device)
+        secondary = secondary_batch1(device, args, consumer) if args.secondary else None
+        result = {"metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
+                  "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
+                  "us_per_step": round(ms_max * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+                  "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                  "frac_of_peak_hbm": round(gbs / peaks["hbm_gbs"], 4),
+                  "config": {"workload": wl.name, "global_batch": wl.B * world, "per_gpu_batch": wl.B,
+                             "layers": "28 = [sliding x3, full] x7", "heads": f"{wl.Hq} q / {wl.Hkv} kv",
+                             "head_dim": synth.HEAD_DIM, "contexts": "uniform [512, 32768] per sequence",
+                             "max_context": wl.max_ctx, "kv_bytes_per_step": wl.bytes,
+                             "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world}"},
+                  "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                  "gpu_launches": int(n1 - n0), "clocks": clk}
+        if secondary:
+            result["secondary"] = secondary
+        print(json.dumps(result), flush=True)
+    return 0
+
+
+def e2e_measure(wl, args, world, device) -> dict:
+    """Same metric through the public API with pinned host buffers: every step copies
+    that step's q/k/v (all layers) and contexts host->device and reads out/lse back."""
+    import torch
+    host_in = [(l["q"].cpu().pin_memory(), l["k"].cpu().pin_memory(), l["v"].cpu().pin_memory())
+               for l in wl.layers]
+    host_ctx = torch.from_numpy(wl.context).pin_memory()
+    host_out = [(torch.empty_like(l["out"], device="cpu").pin_memory(),
+                 torch.empty_like(l["lse"], device="cpu").pin_memory()) for l in wl.layers]
+    h2d = sum(t.numel() * t.element_size() for trip in host_in for t in trip) + host_ctx.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for pair in host_out for t in pair)
+
+    def run():
+        wl.context_d.copy_(host_ctx, non_blocking=True)
+        for (q, k, v), l in zip(host_in, wl.layers):
+            l["q"].copy_(q, non_blocking=True)
+            l["k"].copy_(k, non_blocking=True)
+            l["v"].copy_(v, non_blocking=True)
+        wl.step()
+        for (o, s), l in zip(host_out, wl.layers):
+            o.copy_(l["out"], non_blocking=True)
+            s.copy_(l["lse"], non_blocking=True)
+    ms = time_steps(run, args.steps, args.warmup, world, device)
+    ms_max, total = reduce_timing(ms, wl.bytes, world, device)
+    return {"value": round(total / (ms_max * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "ms_per_step": round(ms_max, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+
+
+def cpu_baseline(wl, device) -> dict:
+    """The oracle on the host cores, on the first [S,S,S,F] block of this very
+    workload (caches copied from the device before timing; compute only timed)."""
+    block = list(range(4))
+    caches = []
+    for i in block:
+        l = wl.layers[i]
+        caches.append((synth.bits(l["kc"]), synth.bits(l["vc"])))
+    sink = None if wl.sink is None else wl.sink.cpu().numpy()
+    threads = cpu_threads()
+    secs, nbytes = oracle_sample(caches, wl.context, [wl.types[i] for i in block], wl.Hq, wl.Hkv, sink,
+                                 synth.generator(99), threads)
+    return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
+            "sample": f"layers 0-3 ([sliding x3, full]) of the step over all {len(wl.context)} sequences, "
+                      f"{nbytes / 1e9:.2f} GB scored KV, {secs:.1f} s"}
+
+
+def secondary_batch1(device, args, consumer) -> dict:
+    """The 28-layer step at batch 1, context 4096 (launch-latency bound), launched
+    eagerly and replayed from a CUDA graph of one decode_step."""
+    import torch
+    import full_gqa_decode_gb300 as hd
+    wl = Workload(SECONDARY_WORKLOAD, device, seed=7)
+    hd.hybrid_decode_set_consumer(wl.ctx, consumer)
+    steps, warm = max(args.steps, 20), max(args.warmup, 3)
+    ms = time_steps(wl.step, steps, warm, 1, device)
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        wl.step()
+    torch.cuda.current_stream(device).wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        wl.step()
+    ms_graph = time_steps(graph.replay, steps, warm, 1, device)
+    return {"workload": SECONDARY_WORKLOAD, "us_per_step": round(ms * 1e3, 1),
+            "us_per_step_cuda_graph": round(ms_graph * 1e3, 1),
+            "kv_GBps_cuda_graph": round(wl.bytes / (ms_graph * 1e-3) / 1e9, 1),
+            "kv_bytes_per_step": wl.bytes, "roofline_us": round(wl.bytes / (measured_peaks()["hbm_gbs"] * 1e9) * 1e6, 1)}
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
+    ap.add_argument("--no-secondary", dest="secondary", action="store_false")
+    ap.add_argument("--consumer", choices=["tensor-core", "cuda-core"], default="tensor-core",
+                    help="inner loop of the attention kernels")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+    if args.impl == "reference":
+        return run_reference(args, world, rank)
+    return run_ours(args, world, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

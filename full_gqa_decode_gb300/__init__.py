@@ -23,6 +23,7 @@ LIBRARY = os.path.join(PKG, "libhybriddecode.so")
 
 HD_SLIDING, HD_FULL = 0, 1
 HD_LAYOUT_AUTO, HD_LAYOUT_RING, HD_LAYOUT_ROLL = 0, 1, 2
+HD_CONSUMER_CUDA_CORE, HD_CONSUMER_TENSOR_CORE = 0, 1
 STATUS = {0: "HD_OK", 1: "HD_ERR_INVALID_ARG", 2: "HD_ERR_UNSUPPORTED", 3: "HD_ERR_CAPACITY",
           4: "HD_ERR_CUDA", 5: "HD_ERR_STATE"}
 DEVERR = {1: "HD_DEVERR_CONTEXT_NEGATIVE", 2: "HD_DEVERR_CONTEXT_CAPACITY",
@@ -77,6 +78,7 @@ _SIGS = {
     "hybrid_decode_launch_count": [_P, _c.POINTER(_i64)],
     "hybrid_decode_set_profiling": [_P, _i32],
     "hybrid_decode_profile": [_P, _c.POINTER(_c.c_double), _c.POINTER(_i64)],
+    "hybrid_decode_set_consumer": [_P, _i32],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -271,3 +273,8 @@ def hybrid_decode_profile(ctx: Context) -> tuple[float, int]:
     _check(_lib.hybrid_decode_profile(ctx.handle, ctypes.byref(ms), ctypes.byref(n)),
            "hybrid_decode_profile")
     return ms.value, n.value
+
+
+def hybrid_decode_set_consumer(ctx: Context, consumer: int) -> None:
+    """HD_CONSUMER_CUDA_CORE or HD_CONSUMER_TENSOR_CORE (the default)."""
+    _check(_lib.hybrid_decode_set_consumer(ctx.handle, consumer), "hybrid_decode_set_consumer")

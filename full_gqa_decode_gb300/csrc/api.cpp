@@ -48,8 +48,9 @@ struct hd_ctx {
     int64_t part_slots = 0;              // capacity in (sequence, chunk) pairs
     __nv_bfloat16 *stage_k = nullptr;    // [num_layers][max_batch][Hkv][D]
     __nv_bfloat16 *stage_v = nullptr;
-    float *q_rot = nullptr;              // [max_batch][Hq][D] for decode_step
+    int32_t *counters = nullptr;         // [max_batch][Hkv] chunk tickets, zero between calls
     int32_t *err = nullptr;
+    int consumer = CONSUMER_MMA;
     int64_t launches = 0;
     std::vector<MapCacheEntry> maps;     // one per layer
     bool profiling = false;
@@ -147,7 +148,7 @@ int64_t worst_part_slots(int max_batch, int num_kv_heads, int max_keys, int num_
         std::vector<int> probes{max_keys};
         for (int t = kChunkMin; t < kChunkMax; t *= 2) {
             // keys at which the plan leaves chunk size t: units * keys > t * target
-            const int64_t target = 8LL * num_sms;
+            const int64_t target = 2LL * num_sms;
             const int64_t k = (int64_t)t * target / ((int64_t)b * num_kv_heads);
             if (k < max_keys) probes.push_back((int)k);
         }
@@ -187,76 +188,107 @@ void free_ctx(hd_ctx *ctx) {
     cudaFree(ctx->part_ml);
     cudaFree(ctx->stage_k);
     cudaFree(ctx->stage_v);
-    cudaFree(ctx->q_rot);
+    cudaFree(ctx->counters);
     cudaFree(ctx->err);
     for (auto e : ctx->ev_begin) cudaEventDestroy(e);
     for (auto e : ctx->ev_end) cudaEventDestroy(e);
     delete ctx;
 }
 
-hd_status launch_attention(hd_ctx *ctx, int layer, int batch, const int32_t *context, int max_keys,
-                           int key_set, const float *q_rot, const hd_kv_cache &cache,
-                           const float *sink, void *out, float *lse, cudaStream_t stream) {
+// Launches the fused layer kernel (see attn_decode.cu) for one layer call.
+struct LayerCall {
+    int layer, batch;
+    const int32_t *context;
+    int max_keys;           // bound on the cached keys any sequence scores (split plan)
+    int key_set, new_kind, commit;
+    const void *q_bf16;     // rotate q in the kernel, or
+    const float *q_rot;     // take it rotated
+    const void *new_k, *new_v;
+    hd_kv_cache cache;
+    const float *sink;
+    void *out;
+    float *lse;
+};
+
+hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream) {
     const CUtensorMap *km = nullptr, *vm = nullptr;
-    hd_status st = maps_for(ctx, layer, cache, batch, &km, &vm);
+    hd_status st = maps_for(ctx, L.layer, L.cache, L.batch, &km, &vm);
     if (st != HD_OK) return st;
     int32_t chunk_keys = 0, num_chunks = 0;
-    st = hd_plan_split(batch, ctx->cfg.num_kv_heads, max_keys, ctx->num_sms, &chunk_keys, &num_chunks);
+    st = hd_plan_split(L.batch, ctx->cfg.num_kv_heads, L.max_keys, ctx->num_sms, &chunk_keys, &num_chunks);
     if (st != HD_OK) return st;
-    if ((int64_t)batch * num_chunks > ctx->part_slots) return HD_ERR_CAPACITY;
+    if ((int64_t)L.batch * num_chunks > ctx->part_slots) return HD_ERR_CAPACITY;
+    // The combine keeps a weight per (head, chunk) plus a float4 row per head in the stage ring.
+    if (((size_t)ctx->group * num_chunks + 3) * sizeof(float) + (size_t)ctx->group * 64 * 16 >
+        (size_t)kStages * kStageBytes)
+        return HD_ERR_CAPACITY;
+    const bool sliding = ctx->layer_types[L.layer] == HD_SLIDING;
+    const DeviceTable &tab = sliding ? ctx->table_sliding : ctx->table_full;
 
-    SplitArgs sa{};
-    sa.context = context;
-    sa.q_rot = q_rot;
-    sa.part_o = ctx->part_o;
-    sa.part_ml = ctx->part_ml;
-    sa.err = ctx->err;
-    sa.num_q_heads = ctx->cfg.num_q_heads;
-    sa.num_kv_heads = ctx->cfg.num_kv_heads;
-    sa.chunk_keys = chunk_keys;
-    sa.max_chunks = num_chunks;
-    sa.key_set = key_set;
-    sa.capacity = cache.capacity;
-    sa.window = ctx->cfg.sliding_window;
-    sa.max_context = ctx->cfg.max_context;
+    LayerArgs a{};
+    a.context = L.context;
+    a.q_bf16 = static_cast<const __nv_bfloat16 *>(L.q_bf16);
+    a.q_rot = L.q_rot;
+    a.table = tab.data;
+    a.rotary_dim = tab.rotary_dim;
+    a.new_k = static_cast<const __nv_bfloat16 *>(L.new_k);
+    a.new_v = static_cast<const __nv_bfloat16 *>(L.new_v);
+    a.new_kind = L.new_kind;
+    a.commit = L.commit;
+    a.key_set = L.key_set;
+    a.cache_k = static_cast<__nv_bfloat16 *>(L.cache.k);
+    a.cache_v = static_cast<__nv_bfloat16 *>(L.cache.v);
+    a.seq_stride = L.cache.seq_stride;
+    a.capacity = L.cache.capacity;
+    a.sink = L.sink;
+    a.out = static_cast<__nv_bfloat16 *>(L.out);
+    a.lse = L.lse;
+    a.part_o = ctx->part_o;
+    a.part_ml = ctx->part_ml;
+    a.counters = ctx->counters;
+    a.err = ctx->err;
+    a.num_q_heads = ctx->cfg.num_q_heads;
+    a.num_kv_heads = ctx->cfg.num_kv_heads;
+    a.chunk_keys = chunk_keys;
+    a.max_chunks = num_chunks;
+    a.window = ctx->cfg.sliding_window;
+    a.max_context = ctx->cfg.max_context;
 
-    const bool timed = ctx->profiling && key_set == KEYS_FULL && ctx->ev_used < ctx->ev_begin.size();
+    const bool timed = ctx->profiling && !sliding && ctx->ev_used < ctx->ev_begin.size();
     if (timed && cudaEventRecord(ctx->ev_begin[ctx->ev_used], stream) != cudaSuccess)
         return HD_ERR_CUDA;
-    st = cuda_status(launch_split(km, vm, sa, batch, ctx->group, stream));
+    st = cuda_status(launch_layer(km, vm, a, L.batch, ctx->group, ctx->consumer, stream));
     if (st != HD_OK) return st;
     ++ctx->launches;
     if (timed) {
         if (cudaEventRecord(ctx->ev_end[ctx->ev_used], stream) != cudaSuccess) return HD_ERR_CUDA;
         ++ctx->ev_used;
     }
+    return HD_OK;
+}
 
-    CombineArgs ca{};
-    ca.context = context;
-    ca.q_rot = q_rot;
-    ca.part_o = ctx->part_o;
-    ca.part_ml = ctx->part_ml;
-    ca.sink = sink;
-    ca.out = static_cast<__nv_bfloat16 *>(out);
-    ca.lse = lse;
-    const size_t stage_off = (size_t)layer * ctx->cfg.max_batch * ctx->cfg.num_kv_heads * kHeadDim;
-    ca.stage_k = ctx->stage_k + stage_off;
-    ca.stage_v = ctx->stage_v + stage_off;
-    ca.cache_k = static_cast<__nv_bfloat16 *>(cache.k);
-    ca.cache_v = static_cast<__nv_bfloat16 *>(cache.v);
-    ca.seq_stride = cache.seq_stride;
-    ca.capacity = cache.capacity;
-    ca.err = ctx->err;
-    ca.num_q_heads = ctx->cfg.num_q_heads;
-    ca.num_kv_heads = ctx->cfg.num_kv_heads;
-    ca.chunk_keys = chunk_keys;
-    ca.max_chunks = num_chunks;
-    ca.key_set = key_set;
-    ca.window = ctx->cfg.sliding_window;
-    ca.max_context = ctx->cfg.max_context;
-    st = cuda_status(launch_combine(ca, batch, ctx->group, stream));
-    if (st == HD_OK) ++ctx->launches;
-    return st;
+const __nv_bfloat16 *stage_row(const hd_ctx *ctx, const __nv_bfloat16 *base, int layer) {
+    return base + (size_t)layer * ctx->cfg.max_batch * ctx->cfg.num_kv_heads * kHeadDim;
+}
+
+// Host checks shared by the attention entry points and decode_step.
+hd_status check_attention(const hd_ctx *ctx, int layer, int batch, const int32_t *context,
+                          const hd_kv_cache &cache, const void *out, const float *lse) {
+    hd_status st = check_call(ctx, layer, batch, context);
+    if (st != HD_OK) return st;
+    if (!out || !lse) return HD_ERR_INVALID_ARG;
+    if ((st = check_cache(ctx, cache)) != HD_OK) return st;
+    if (ctx->layer_types[layer] == HD_SLIDING && cache.capacity != sliding_capacity(ctx))
+        return HD_ERR_CAPACITY;
+    return HD_OK;
+}
+
+hd_status full_hint(const hd_ctx *ctx, int32_t max_context_hint, const hd_kv_cache &cache, int *hint) {
+    if (max_context_hint < 0) return HD_ERR_INVALID_ARG;
+    *hint = max_context_hint == 0 ? ctx->cfg.max_context : max_context_hint;
+    if (*hint > ctx->cfg.max_context) return HD_ERR_CAPACITY;
+    if (*hint + 1 > cache.capacity) return HD_ERR_CAPACITY;
+    return HD_OK;
 }
 
 }  // namespace
@@ -301,14 +333,16 @@ hd_status hd_plan_split(int32_t batch, int32_t num_kv_heads, int32_t max_keys, i
                         int32_t *chunk_keys, int32_t *num_chunks) {
     if (batch <= 0 || num_kv_heads <= 0 || max_keys < 0 || num_sms <= 0 || !chunk_keys || !num_chunks)
         return HD_ERR_INVALID_ARG;
-    // Aim at about eight CTAs per SM over the whole grid: enough to cover the
-    // per-CTA ramp-up and ragged lengths, with chunks of 64..512 keys.
-    const int64_t target = 8LL * num_sms;
+    // Aim at one wave of two resident CTAs per SM for the longest sequence
+    // bound, with chunks of 64..512 keys: short sliding layers get few, long
+    // chunks; long full layers get many 512-key chunks, which also balance
+    // ragged lengths across waves.
+    const int64_t target = 2LL * num_sms;
     const int64_t want = ((int64_t)batch * num_kv_heads * max_keys + target - 1) / target;
     int t = kChunkMin;
     while (t < want && t < kChunkMax) t *= 2;
     *chunk_keys = t;
-    *num_chunks = (int32_t)((max_keys + t - 1) / t);
+    *num_chunks = max_keys > 0 ? (int32_t)((max_keys + t - 1) / t) : 1;
     return HD_OK;
 }
 
@@ -359,7 +393,8 @@ hd_status hybrid_decode_init(const hd_config *cfg, hd_ctx **out_ctx) {
     ctx->part_slots = slots;
     bool ok = cudaMalloc(&ctx->part_o, (size_t)slots * Hq * kHeadDim * sizeof(float)) == cudaSuccess &&
               cudaMalloc(&ctx->part_ml, (size_t)slots * Hq * sizeof(float2)) == cudaSuccess &&
-              cudaMalloc(&ctx->q_rot, (size_t)B * Hq * kHeadDim * sizeof(float)) == cudaSuccess &&
+              cudaMalloc(&ctx->counters, (size_t)B * Hkv * sizeof(int32_t)) == cudaSuccess &&
+              cudaMemset(ctx->counters, 0, (size_t)B * Hkv * sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&ctx->err, sizeof(int32_t)) == cudaSuccess &&
               cudaMemset(ctx->err, 0, sizeof(int32_t)) == cudaSuccess;
     const size_t stage = (size_t)cfg->num_layers * B * Hkv * kHeadDim;
@@ -390,7 +425,7 @@ hd_status rope_append_kv(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_
     const bool sliding = ctx->layer_types[layer] == HD_SLIDING;
     if (sliding && cache.capacity != sliding_capacity(ctx)) return HD_ERR_CAPACITY;
     const DeviceTable &tab = sliding ? ctx->table_sliding : ctx->table_full;
-    const int key_set = !sliding ? KEYS_FULL
+    const int key_set = !sliding ? KEYS_FULL_CACHED
                                  : (ctx->sliding_layout == HD_LAYOUT_ROLL ? KEYS_ROLL : KEYS_RING);
     RopeArgs a{};
     a.context = context;
@@ -432,49 +467,124 @@ hd_status rope_append_kv(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_
 hd_status decode_attn_sliding(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
                               const float *q_rot, hd_kv_cache cache, const float *sink, void *out,
                               float *lse, void *stream) {
-    hd_status st = check_call(ctx, layer, batch, context);
+    hd_status st = check_attention(ctx, layer, batch, context, cache, out, lse);
     if (st != HD_OK) return st;
     if (ctx->layer_types[layer] != HD_SLIDING) return HD_ERR_STATE;
-    if (!q_rot || !out || !lse || !aligned16(q_rot)) return HD_ERR_INVALID_ARG;
-    if ((st = check_cache(ctx, cache)) != HD_OK) return st;
-    if (cache.capacity != sliding_capacity(ctx)) return HD_ERR_CAPACITY;
+    if (!q_rot || !aligned16(q_rot)) return HD_ERR_INVALID_ARG;
     const bool roll = ctx->sliding_layout == HD_LAYOUT_ROLL;
-    return launch_attention(ctx, layer, batch, context, roll ? ctx->cfg.sliding_window : cache.capacity,
-                            roll ? KEYS_ROLL : KEYS_RING, q_rot, cache, sink, out, lse,
-                            static_cast<cudaStream_t>(stream));
+    LayerCall L{};
+    L.layer = layer;
+    L.batch = batch;
+    L.context = context;
+    L.max_keys = roll ? ctx->cfg.sliding_window : cache.capacity;
+    L.key_set = roll ? KEYS_ROLL : KEYS_RING;
+    L.new_kind = roll ? NEW_NONE : NEW_STAGED;
+    L.commit = roll ? COMMIT_NONE : COMMIT_RING;
+    L.q_rot = q_rot;
+    L.new_k = stage_row(ctx, ctx->stage_k, layer);
+    L.new_v = stage_row(ctx, ctx->stage_v, layer);
+    L.cache = cache;
+    L.sink = sink;
+    L.out = out;
+    L.lse = lse;
+    return launch_layer_call(ctx, L, static_cast<cudaStream_t>(stream));
 }
 
 hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
                            int32_t max_context_hint, const float *q_rot, hd_kv_cache cache,
                            const float *sink, void *out, float *lse, void *stream) {
-    hd_status st = check_call(ctx, layer, batch, context);
+    hd_status st = check_attention(ctx, layer, batch, context, cache, out, lse);
     if (st != HD_OK) return st;
     if (ctx->layer_types[layer] != HD_FULL) return HD_ERR_STATE;
-    if (!q_rot || !out || !lse || !aligned16(q_rot)) return HD_ERR_INVALID_ARG;
-    if ((st = check_cache(ctx, cache)) != HD_OK) return st;
-    if (max_context_hint < 0) return HD_ERR_INVALID_ARG;
-    const int hint = max_context_hint == 0 ? ctx->cfg.max_context : max_context_hint;
-    if (hint > ctx->cfg.max_context) return HD_ERR_CAPACITY;
-    if (hint + 1 > cache.capacity) return HD_ERR_CAPACITY;
-    return launch_attention(ctx, layer, batch, context, hint + 1, KEYS_FULL, q_rot, cache, sink, out,
-                            lse, static_cast<cudaStream_t>(stream));
+    if (!q_rot || !aligned16(q_rot)) return HD_ERR_INVALID_ARG;
+    int hint = 0;
+    if ((st = full_hint(ctx, max_context_hint, cache, &hint)) != HD_OK) return st;
+    LayerCall L{};
+    L.layer = layer;
+    L.batch = batch;
+    L.context = context;
+    L.max_keys = hint + 1;
+    L.key_set = KEYS_FULL_CACHED;
+    L.new_kind = NEW_NONE;
+    L.commit = COMMIT_NONE;
+    L.q_rot = q_rot;
+    L.cache = cache;
+    L.sink = sink;
+    L.out = out;
+    L.lse = lse;
+    return launch_layer_call(ctx, L, static_cast<cudaStream_t>(stream));
 }
 
+// One kernel per layer: q is rotated in the CTA prologue, the new key is
+// rotated, scored and stored by the combine (roll layouts shift first).
 hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_t max_context_hint,
                       const hd_layer_io *layers, void *stream) {
     if (!ctx || !layers) return HD_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
     for (int i = 0; i < ctx->cfg.num_layers; ++i) {
-        const hd_layer_io &L = layers[i];
-        hd_status st = rope_append_kv(ctx, i, batch, context, L.q, L.k, L.v, ctx->q_rot, L.cache, stream);
+        const hd_layer_io &io = layers[i];
+        hd_status st = check_attention(ctx, i, batch, context, io.cache, io.out, io.lse);
         if (st != HD_OK) return st;
-        if (ctx->layer_types[i] == HD_SLIDING)
-            st = decode_attn_sliding(ctx, i, batch, context, ctx->q_rot, L.cache, L.sink, L.out, L.lse,
-                                     stream);
-        else
-            st = decode_attn_full(ctx, i, batch, context, max_context_hint, ctx->q_rot, L.cache, L.sink,
-                                  L.out, L.lse, stream);
-        if (st != HD_OK) return st;
+        if (!io.q || !io.k || !io.v) return HD_ERR_INVALID_ARG;
+        const bool sliding = ctx->layer_types[i] == HD_SLIDING;
+        const bool roll = sliding && ctx->sliding_layout == HD_LAYOUT_ROLL;
+        LayerCall L{};
+        L.layer = i;
+        L.batch = batch;
+        L.context = context;
+        L.q_bf16 = io.q;
+        L.new_k = io.k;
+        L.new_v = io.v;
+        L.cache = io.cache;
+        L.sink = io.sink;
+        L.out = io.out;
+        L.lse = io.lse;
+        if (!sliding) {
+            int hint = 0;
+            if ((st = full_hint(ctx, max_context_hint, io.cache, &hint)) != HD_OK) return st;
+            L.max_keys = hint;
+            L.key_set = KEYS_FULL_PREV;
+            L.new_kind = NEW_ROTATE;
+            L.commit = COMMIT_APPEND;
+        } else if (!roll) {
+            L.max_keys = io.cache.capacity;
+            L.key_set = KEYS_RING;
+            L.new_kind = NEW_ROTATE;
+            L.commit = COMMIT_RING;
+        } else {
+            RopeArgs r{};
+            r.context = context;
+            r.k = static_cast<const __nv_bfloat16 *>(io.k);
+            r.v = static_cast<const __nv_bfloat16 *>(io.v);
+            r.table = ctx->table_sliding.data;
+            r.dst_k = static_cast<__nv_bfloat16 *>(io.cache.k);
+            r.dst_v = static_cast<__nv_bfloat16 *>(io.cache.v);
+            r.seq_stride = io.cache.seq_stride;
+            r.capacity = io.cache.capacity;
+            r.err = ctx->err;
+            r.num_q_heads = ctx->cfg.num_q_heads;
+            r.num_kv_heads = ctx->cfg.num_kv_heads;
+            r.rotary_dim = ctx->table_sliding.rotary_dim;
+            r.key_set = KEYS_ROLL;
+            r.window = ctx->cfg.sliding_window;
+            r.max_context = ctx->cfg.max_context;
+            if ((st = cuda_status(launch_roll_window(r, batch, s))) != HD_OK) return st;
+            ++ctx->launches;
+            L.max_keys = ctx->cfg.sliding_window;
+            L.key_set = KEYS_ROLL;
+            L.new_kind = NEW_NONE;
+            L.commit = COMMIT_NONE;
+        }
+        if ((st = launch_layer_call(ctx, L, s)) != HD_OK) return st;
     }
+    return HD_OK;
+}
+
+hd_status hybrid_decode_set_consumer(hd_ctx *ctx, int32_t consumer) {
+    if (!ctx) return HD_ERR_INVALID_ARG;
+    if (consumer != HD_CONSUMER_CUDA_CORE && consumer != HD_CONSUMER_TENSOR_CORE)
+        return HD_ERR_INVALID_ARG;
+    ctx->consumer = consumer == HD_CONSUMER_TENSOR_CORE ? CONSUMER_MMA : CONSUMER_FMA;
     return HD_OK;
 }
 

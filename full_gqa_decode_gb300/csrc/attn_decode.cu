@@ -1,26 +1,32 @@
-// Split-K flash-decoding for one layer of the hybrid model, and the LSE
-// combine that folds in the per-head sink.
+// One decode-attention layer of the hybrid model in one kernel: partial RoPE
+// of q, split-K flash-decoding over the cached keys, and an LSE combine that
+// scores the new entry, folds in the per-head sink and stores the entry.
 //
 // The math is the scaled-dot-product attention of
 // vllm_omni/edge/spark_export.py (`_Layer.forward`: scores = q.k/sqrt(d),
 // softmax over keys, weights @ values, GQA by viewing q as (kv, group, d)),
 // computed blockwise with an online softmax, which that page notes is
-// numerically the same as one fused softmax (ring-branch comment).  The sink
-// follows vllm/models/hy_v4/nvidia/flashmla_sparse.py
+// numerically the same as one fused softmax (ring-branch comment).  The new
+// entry is scored apart from the cache, as that comment's two-key-set form
+// does.  The sink follows vllm/models/hy_v4/nvidia/flashmla_sparse.py
 // (`HYV4FlashMLASparseImpl`): out *= exp(lse) / (exp(lse) + exp(sink)).
 //
-// Split pass: one CTA per (chunk of keys, kv head, sequence).  A producer warp
-// streams the chunk's K and V rows through a 3-stage shared-memory ring with
-// TMA tensor loads (128-byte swizzle, completion on an mbarrier); four
+// Grid: one CTA per (chunk of cached keys, kv head, sequence).  A producer
+// warp streams the chunk's K and V rows through a 3-stage shared-memory ring
+// with TMA tensor loads (128-byte swizzle, completion on mbarriers); four
 // consumer warps each take 8 keys of every 32-key stage, so each K/V row is
 // read from HBM once for the whole GQA group.  Scores are kept in log2 units
-// (q is pre-scaled by log2(e)/sqrt(d)).  The CTA writes an unnormalised
-// partial (o, m, l) per query head.
+// (q is pre-scaled by log2(e)/sqrt(d)).  Two consumers exist: CUDA-core FMA
+// with warp-shuffle reductions, and tensor-core mma.sync (bf16 in, fp32
+// accumulate) where q is split into a bf16 high and low part on the padded
+// rows of the MMA tile so the scores keep fp32 accuracy.
 //
-// Combine: one CTA per (kv head, sequence) merges the partials of all chunks
-// (and, for a sliding ring, the staged new entry), normalises, applies the
-// sink, writes out/lse, and commits the staged ring entry to its slot now
-// that every read of the ring has finished.
+// Each CTA writes an unnormalised partial (o, m, l) per query head, then takes
+// a ticket on a per-(sequence, kv head) counter.  The CTA that draws the last
+// ticket -- every other chunk of that (sequence, kv head) has finished reading
+// -- merges all partials and the new entry, writes out/lse, stores the new
+// K/V entry (ring slot or append) and resets the counter.  Nothing waits on
+// another CTA.
 #include "hd_internal.h"
 
 namespace hd {
@@ -28,9 +34,10 @@ namespace {
 
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kQScale = kLog2e * 0.0625f;   // log2(e) / sqrt(256)
 constexpr int kConsumerWarps = 4;
 constexpr int kKeysPerWarp = kStageKeys / kConsumerWarps;  // 8
-constexpr int kSplitThreads = (kConsumerWarps + 1) * 32;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
 
 // ------------------------------------------------------------ PTX helpers --
@@ -90,6 +97,39 @@ __device__ __forceinline__ float fast_exp2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                              uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// D += A(16x8 bf16, row) * B(8x8 bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0));
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
 __device__ __forceinline__ void unpack_bf16x8(const uint4 &r, float (&f)[8]) {
     const uint32_t w[4] = {r.x, r.y, r.z, r.w};
 #pragma unroll
@@ -98,47 +138,286 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &r, float (&f)[8]) {
         f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
 }
+// Byte offset of 16-byte chunk c (0..31) of row r in a stage's K or V region:
+// box c/8, swizzled chunk (c%8)^(r%8) inside the 128-byte row.
+__device__ __forceinline__ uint32_t tile_offset(int r, int c) {
+    return (c >> 3) * kBoxBytes + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
+}
 
-// Number of cache keys the split pass scores for context c, or -1 (flagged)
-// when c cannot be served.  Identical in the split and the combine kernels.
-__device__ __forceinline__ int split_keys(int c, int key_set, int capacity, int window,
-                                          int max_context, int chunk_keys, int max_chunks,
-                                          int32_t *err, bool report) {
-    int bit = 0, n = 0;
-    if (c < 0) bit = HD_DEVERR_CONTEXT_NEGATIVE;
-    else if (c > max_context) bit = HD_DEVERR_CONTEXT_PLAN;
-    else if (key_set == KEYS_RING) n = min(c, capacity);
-    else if (key_set == KEYS_ROLL) n = min(c + 1, window);
-    else if (c >= capacity) bit = HD_DEVERR_CONTEXT_CAPACITY;
-    else n = c + 1;
-    if (!bit && (n + chunk_keys - 1) / chunk_keys > max_chunks) bit = HD_DEVERR_CONTEXT_PLAN;
-    if (bit) {
-        if (report) atomicOr(err, bit);
+// One round-to-nearest-even of a double to bf16, through round-to-odd binary32
+// (Boldo & Melquiond, IEEE TC 2008): the odd-rounded binary32 keeps enough bits
+// that rounding it to bf16 equals rounding the double directly.
+__device__ __forceinline__ float f64_to_bf16_value(double x) {
+    float t = __double2float_rz(x);
+    if ((double)t != x && isfinite(t)) t = __uint_as_float(__float_as_uint(t) | 1u);
+    return __bfloat162float(__float2bfloat16_rn(t));
+}
+
+// Scored cache keys of sequence context c, or -1 (and the error bit) when c
+// cannot be served by this call.
+__device__ __forceinline__ int cached_keys(const LayerArgs &a, int c, int *bit) {
+    *bit = 0;
+    if (c < 0) { *bit = HD_DEVERR_CONTEXT_NEGATIVE; return -1; }
+    if (c > a.max_context) { *bit = HD_DEVERR_CONTEXT_PLAN; return -1; }
+    int n;
+    switch (a.key_set) {
+    case KEYS_RING: n = min(c, a.capacity); break;
+    case KEYS_ROLL: n = min(c + 1, a.window); break;
+    case KEYS_FULL_CACHED: n = c + 1; break;
+    default: n = c; break;  // KEYS_FULL_PREV
+    }
+    if (n > a.capacity || (a.commit == COMMIT_APPEND && c >= a.capacity)) {
+        *bit = HD_DEVERR_CONTEXT_CAPACITY;
         return -1;
     }
+    if ((n + a.chunk_keys - 1) / a.chunk_keys > a.max_chunks) { *bit = HD_DEVERR_CONTEXT_PLAN; return -1; }
     return n;
 }
 
-// --------------------------------------------------------------- split pass --
+// ---------------------------------------------------------- the consumers --
+
+// CUDA-core consumer: lane owns dims [8*lane, 8*lane+8) of every row; each
+// score is a warp-shuffle reduction.
 template <int G>
-__global__ void __launch_bounds__(kSplitThreads, 2)
-    attn_split_kernel(const __grid_constant__ CUtensorMap kmap,
-                      const __grid_constant__ CUtensorMap vmap, const SplitArgs a) {
+struct FmaConsumer {
+    float qv[G][8], m[G], l[G], acc[G][8];
+
+    __device__ void init(const float *q_s, int lane) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                qv[h][i] = q_s[h * kHeadDim + lane * 8 + i];
+                acc[h][i] = 0.f;
+            }
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+        }
+    }
+
+    // Rows [row0, row0 + kKeysPerWarp) of a stage; the first nvalid are keys.
+    __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane) {
+        constexpr int KB = G >= 8 ? 4 : kKeysPerWarp;  // keeps scores, q and acc in registers
+        const int c = lane;
+#pragma unroll
+        for (int sb = 0; sb < kKeysPerWarp; sb += KB) {
+            const int nv = nvalid - sb;
+            if (nv <= 0) break;  // warp-uniform
+            float sc[KB][G];
+#pragma unroll
+            for (int r = 0; r < KB; ++r) {
+                const int row = row0 + sb + r;
+                float kf[8];
+                unpack_bf16x8(*reinterpret_cast<const uint4 *>(kst + tile_offset(row, c)), kf);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float d = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) d = fmaf(qv[h][i], kf[i], d);
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+                    sc[r][h] = (r < nv) ? d : -INFINITY;
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float mx = sc[0][h];
+#pragma unroll
+                for (int r = 1; r < KB; ++r) mx = fmaxf(mx, sc[r][h]);
+                const float mn = fmaxf(m[h], mx);
+                const float alpha = fast_exp2(m[h] - mn);  // m = -inf -> 0
+                m[h] = mn;
+                l[h] *= alpha;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[h][i] *= alpha;
+#pragma unroll
+                for (int r = 0; r < KB; ++r) {
+                    const float p = (r < nv) ? fast_exp2(sc[r][h] - mn) : 0.f;
+                    sc[r][h] = p;
+                    l[h] += p;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < KB; ++r) {
+                if (r < nv) {  // rows past the key set may hold NaN: never touch them
+                    float vf[8];
+                    unpack_bf16x8(*reinterpret_cast<const uint4 *>(vst + tile_offset(row0 + sb + r, c)), vf);
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[h][i] = fmaf(sc[r][h], vf[i], acc[h][i]);
+                }
+            }
+        }
+    }
+
+    __device__ void store(float *red_o, float *red_m, float *red_l, int warp, int lane) const {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float4 *dst = reinterpret_cast<float4 *>(red_o + (warp * G + h) * kHeadDim + lane * 8);
+            dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+            dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
+            if (lane == 0) {
+                red_m[warp * G + h] = m[h];
+                red_l[warp * G + h] = l[h];
+            }
+        }
+    }
+};
+
+// Tensor-core consumer.  S = Q K^T with m16n8k16: rows 0..G-1 of the A tile
+// hold bf16(q) and rows 8..8+G-1 hold bf16(q - bf16(q)), so row r plus row r+8
+// of S is q.k to fp32 accuracy; the 8 keys of a warp are the N dimension and
+// the K rows come straight from the swizzled TMA tile with ldmatrix.  The
+// accumulator of S is, register for register, the B operand of
+// O^T += V^T P^T (m16n8k8: dims on M, 8 keys on K, heads on N), whose A
+// operand is V read with ldmatrix.trans.
+template <int G>
+struct MmaConsumer {
+    uint32_t qa[16][4];
+    float o[16][4];   // O^T tile mt: rows dims 16mt + gid (+8), cols heads 2*t4 (+1)
+    float m_run, l_run;  // for head gid; l_run sums this lane's keys only
+
+    __device__ void init(const float *q_s, int lane) {
+        const int gid = lane >> 2, t4 = lane & 3;
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) {
+            uint32_t r[4] = {0u, 0u, 0u, 0u};
+            if (gid < G) {
+                const float *qh = q_s + gid * kHeadDim + 16 * ks + 2 * t4;
+                const float x0 = qh[0], x1 = qh[1], x2 = qh[8], x3 = qh[9];
+                const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+                const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+                const float h2 = __bfloat162float(__float2bfloat16_rn(x2));
+                const float h3 = __bfloat162float(__float2bfloat16_rn(x3));
+                r[0] = pack_bf16(h0, h1);
+                r[1] = pack_bf16(x0 - h0, x1 - h1);
+                r[2] = pack_bf16(h2, h3);
+                r[3] = pack_bf16(x2 - h2, x3 - h3);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) qa[ks][j] = r[j];
+        }
+#pragma unroll
+        for (int mt = 0; mt < 16; ++mt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[mt][j] = 0.f;
+        m_run = -INFINITY;
+        l_run = 0.f;
+    }
+
+    __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane) {
+        const int gid = lane >> 2, t4 = lane & 3;
+        const int lrow = row0 + (lane & 7), lsub = lane >> 3;
+        const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
+        float s[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kbase + tile_offset(lrow, 4 * p + lsub), b0, b1, b2, b3);
+            mma_16816(s, qa[2 * p], b0, b1);
+            mma_16816(s, qa[2 * p + 1], b2, b3);
+        }
+        const bool ok0 = gid < G && 2 * t4 < nvalid, ok1 = gid < G && 2 * t4 + 1 < nvalid;
+        const float s0 = ok0 ? s[0] + s[2] : -INFINITY;
+        const float s1 = ok1 ? s[1] + s[3] : -INFINITY;
+        float mx = fmaxf(s0, s1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m_run, mx);
+        const float alpha = (mn == -INFINITY) ? 1.f : fast_exp2(m_run - mn);
+        const float p0 = ok0 ? fast_exp2(s0 - mn) : 0.f;
+        const float p1 = ok1 ? fast_exp2(s1 - mn) : 0.f;
+        l_run = fmaf(l_run, alpha, p0 + p1);
+        m_run = mn;
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * t4);      // head 2*t4
+            const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * t4 + 4);  // head 2*t4+1
+#pragma unroll
+            for (int mt = 0; mt < 16; ++mt) {
+                o[mt][0] *= a_lo;
+                o[mt][1] *= a_hi;
+                o[mt][2] *= a_lo;
+                o[mt][3] *= a_hi;
+            }
+        }
+        const uint32_t pb = pack_bf16(p0, p1);
+        // Rows past the key set may hold NaN; 0 * NaN would poison the sum.
+        uint32_t vmask = 0xFFFFFFFFu;
+        if (nvalid < kKeysPerWarp)
+            vmask = (2 * t4 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 1 < nvalid ? 0xFFFF0000u : 0u);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(vbase + tile_offset(lrow, 4 * p + lsub), a0, a1, a2, a3);
+            mma_1688(o[2 * p], a0 & vmask, a1 & vmask, pb);
+            mma_1688(o[2 * p + 1], a2 & vmask, a3 & vmask, pb);
+        }
+    }
+
+    __device__ void store(float *red_o, float *red_m, float *red_l, int warp, int lane) const {
+        const int gid = lane >> 2, t4 = lane & 3;
+        float l = l_run;
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        if (t4 == 0 && gid < G) {
+            red_m[warp * G + gid] = m_run;
+            red_l[warp * G + gid] = l;
+        }
+        const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+#pragma unroll
+        for (int mt = 0; mt < 16; ++mt) {
+            const int d = 16 * mt + gid;
+            if (h0 < G) {
+                red_o[(warp * G + h0) * kHeadDim + d] = o[mt][0];
+                red_o[(warp * G + h0) * kHeadDim + d + 8] = o[mt][2];
+            }
+            if (h1 < G) {
+                red_o[(warp * G + h1) * kHeadDim + d] = o[mt][1];
+                red_o[(warp * G + h1) * kHeadDim + d + 8] = o[mt][3];
+            }
+        }
+    }
+};
+
+// ------------------------------------------------------------- the kernel --
+
+template <int G, int CONSUMER>
+__global__ void __launch_bounds__(kThreads, 2)
+    attn_layer_kernel(const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap, const LayerArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + kStages * kStageBytes);
+    float *q_s = reinterpret_cast<float *>(smem + kStages * kStageBytes);    // [G][256]
+    float *knew_s = q_s + G * kHeadDim;                                        // [256]
+    float *vnew_s = knew_s + kHeadDim;                                         // [256]
+    float *misc = vnew_s + kHeadDim;                                           // [32]
+    uint64_t *full = reinterpret_cast<uint64_t *>(misc + 32);
     uint64_t *empty = full + kStages;
+    int *flag_s = reinterpret_cast<int *>(empty + kStages);
 
     const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-    const int n = split_keys(a.context[b], a.key_set, a.capacity, a.window, a.max_context,
-                             a.chunk_keys, a.max_chunks, a.err,
-                             chunk == 0 && kvh == 0 && threadIdx.x == 0);
-    const int start = chunk * a.chunk_keys;
-    if (n < 0 || start >= n) return;  // uniform over the CTA
-    const int end = min(start + a.chunk_keys, n);
-    const int nst = (end - start + kStageKeys - 1) / kStageKeys;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int c = a.context[b];
+    int bit = 0;
+    const int n = cached_keys(a, c, &bit);
+    if (n < 0) {
+        if (chunk == 0) {  // this CTA reports and poisons the outputs of the group
+            if (threadIdx.x == 0) atomicOr(a.err, bit);
+            for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
+                const int hg = kvh * G + i / kHeadDim;
+                a.out[((size_t)b * a.num_q_heads + hg) * kHeadDim + i % kHeadDim] = __float2bfloat16_rn(NAN);
+                if (i % kHeadDim == 0) a.lse[(size_t)b * a.num_q_heads + hg] = NAN;
+            }
+        }
+        return;
+    }
+    const int nchunks = max(1, (n + a.chunk_keys - 1) / a.chunk_keys);
+    if (chunk >= nchunks) return;  // uniform over the CTA
+    const int start = chunk * a.chunk_keys;
+    const int end = min(start + a.chunk_keys, n);
+    const int nst = end > start ? (end - start + kStageKeys - 1) / kStageKeys : 0;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -147,12 +426,32 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
         }
         fence_mbar_init();
     }
+    // q of the group, rotated here from bf16 or taken pre-rotated, scaled to log2 units.
+    const float2 *cs = a.q_bf16 ? a.table + (size_t)c * (a.rotary_dim >> 1) : nullptr;
+    for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
+        const int h = i / kHeadDim, d = i % kHeadDim;
+        const size_t row = ((size_t)b * a.num_q_heads + kvh * G + h) * kHeadDim;
+        float x;
+        if (a.q_bf16 == nullptr) {
+            x = a.q_rot[row + d];
+        } else if (d >= a.rotary_dim) {
+            x = __bfloat162float(a.q_bf16[row + d]);
+        } else {
+            const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
+            const float x1 = __bfloat162float(a.q_bf16[row + j]);
+            const float x2 = __bfloat162float(a.q_bf16[row + j + half]);
+            const float2 t = cs[j];
+            x = d < half ? fmaf(x1, t.x, -x2 * t.y) : fmaf(x2, t.x, x1 * t.y);
+        }
+        q_s[i] = x * kQScale;
+    }
     __syncthreads();
 
-    float m[G], l[G], acc[G][8];
+    float *red_o = reinterpret_cast<float *>(smem);             // reuses the stage ring
+    float *red_m = red_o + kConsumerWarps * G * kHeadDim;
+    float *red_l = red_m + kConsumerWarps * G;
     if (warp == kConsumerWarps) {
-        // Producer: one elected lane issues every load of the chunk.
-        if (lane == 0) {
+        if (lane == 0) {  // producer: one lane issues every load of the chunk
             for (int s = 0; s < nst; ++s) {
                 const int slot = s % kStages;
                 if (s >= kStages && !mbar_wait(&empty[slot], ((s / kStages) - 1) & 1)) {
@@ -171,249 +470,218 @@ __global__ void __launch_bounds__(kSplitThreads, 2)
                                 j * kBoxCols, row, kvh, b);
             }
         }
+        __syncthreads();
+        __syncthreads();
     } else {
-        // Consumer: lane owns dims [8*lane, 8*lane+8), i.e. 16-byte chunk (lane&7)
-        // of box (lane>>3); the 128-byte swizzle puts chunk j of row r at j^(r&7).
-        const float qscale = kLog2e * 0.0625f;  // log2(e) / sqrt(256)
-        float qv[G][8];
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            const float4 *qp = reinterpret_cast<const float4 *>(
-                a.q_rot + ((size_t)b * a.num_q_heads + kvh * G + h) * kHeadDim + lane * 8);
-            const float4 x0 = qp[0], x1 = qp[1];
-            qv[h][0] = x0.x * qscale; qv[h][1] = x0.y * qscale;
-            qv[h][2] = x0.z * qscale; qv[h][3] = x0.w * qscale;
-            qv[h][4] = x1.x * qscale; qv[h][5] = x1.y * qscale;
-            qv[h][6] = x1.z * qscale; qv[h][7] = x1.w * qscale;
-            m[h] = -INFINITY;
-            l[h] = 0.f;
-#pragma unroll
-            for (int i = 0; i < 8; ++i) acc[h][i] = 0.f;
-        }
-        const int box = lane >> 3, cidx = lane & 7;
+        typename std::conditional<CONSUMER == CONSUMER_MMA, MmaConsumer<G>, FmaConsumer<G>>::type cons;
+        cons.init(q_s, lane);
         for (int s = 0; s < nst; ++s) {
             const int slot = s % kStages;
             if (!mbar_wait(&full[slot], (s / kStages) & 1)) {
                 if (lane == 0) atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
                 break;
             }
-            const uint8_t *kst = smem + slot * kStageBytes + box * kBoxBytes;
-            const uint8_t *vst = kst + kBoxesPerRow * kBoxBytes;
-            // Keys are scored in sub-batches of KB so that the scores of a
-            // sub-batch, q and the accumulators all stay in registers.
-            constexpr int KB = G >= 8 ? 4 : kKeysPerWarp;
-            const int key_base = start + s * kStageKeys + warp * kKeysPerWarp;
-#pragma unroll
-            for (int sb = 0; sb < kKeysPerWarp; sb += KB) {
-                const int row0 = warp * kKeysPerWarp + sb;
-                const int nvalid = min(KB, end - (key_base + sb));
-                if (nvalid <= 0) break;  // warp-uniform
-                float sc[KB][G];
-#pragma unroll
-                for (int r = 0; r < KB; ++r) {
-                    const int row = row0 + r;
-                    const uint4 raw =
-                        *reinterpret_cast<const uint4 *>(kst + row * 128 + ((cidx ^ (row & 7)) << 4));
-                    float kf[8];
-                    unpack_bf16x8(raw, kf);
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        float d = 0.f;
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) d = fmaf(qv[h][i], kf[i], d);
-#pragma unroll
-                        for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
-                        sc[r][h] = (r < nvalid) ? d : -INFINITY;
-                    }
-                }
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    float mx = sc[0][h];
-#pragma unroll
-                    for (int r = 1; r < KB; ++r) mx = fmaxf(mx, sc[r][h]);
-                    const float mn = fmaxf(m[h], mx);
-                    const float alpha = fast_exp2(m[h] - mn);  // m = -inf -> 0
-                    m[h] = mn;
-                    l[h] *= alpha;
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[h][i] *= alpha;
-#pragma unroll
-                    for (int r = 0; r < KB; ++r) {
-                        const float p = (r < nvalid) ? fast_exp2(sc[r][h] - mn) : 0.f;
-                        sc[r][h] = p;
-                        l[h] += p;
-                    }
-                }
-#pragma unroll
-                for (int r = 0; r < KB; ++r) {
-                    if (r < nvalid) {  // rows past the key set may hold NaN: never touch them
-                        const int row = row0 + r;
-                        const uint4 raw = *reinterpret_cast<const uint4 *>(
-                            vst + row * 128 + ((cidx ^ (row & 7)) << 4));
-                        float vf[8];
-                        unpack_bf16x8(raw, vf);
-#pragma unroll
-                        for (int h = 0; h < G; ++h)
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) acc[h][i] = fmaf(sc[r][h], vf[i], acc[h][i]);
-                    }
-                }
-            }
+            const uint8_t *kst = smem + slot * kStageBytes;
+            const int row0 = warp * kKeysPerWarp;
+            const int nvalid = min(kKeysPerWarp, end - (start + s * kStageKeys + row0));
+            if (nvalid > 0) cons.consume(kst, kst + kBoxesPerRow * kBoxBytes, row0, nvalid, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
         }
+        __syncthreads();  // every stage consumed: the ring is free for the warp merge
+        cons.store(red_o, red_m, red_l, warp, lane);
+        __syncthreads();
     }
-    __syncthreads();  // every stage consumed: the ring is free for the warp merge
 
-    float *red_o = reinterpret_cast<float *>(smem);             // [warps][G][256]
-    float *red_m = red_o + kConsumerWarps * G * kHeadDim;       // [warps][G]
-    float *red_l = red_m + kConsumerWarps * G;
-    if (warp < kConsumerWarps) {
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float4 *dst = reinterpret_cast<float4 *>(red_o + (warp * G + h) * kHeadDim + lane * 8);
-            dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
-            dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
-            if (lane == 0) {
-                red_m[warp * G + h] = m[h];
-                red_l[warp * G + h] = l[h];
-            }
-        }
-    }
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < G * kHeadDim; idx += blockDim.x) {
-        const int h = idx / kHeadDim, d = idx % kHeadDim;
+    // Merge the warps into this chunk's partial.
+    const size_t pbase = ((size_t)b * a.num_q_heads + kvh * G) * a.max_chunks;
+    for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
+        const int h = i / kHeadDim, d = i % kHeadDim;
         float M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * G + h]);
         float o = 0.f, L = 0.f;
 #pragma unroll
         for (int w = 0; w < kConsumerWarps; ++w) {
-            const float wt = fast_exp2(red_m[w * G + h] - M);
+            const float wt = (M == -INFINITY) ? 0.f : fast_exp2(red_m[w * G + h] - M);
             o = fmaf(wt, red_o[(w * G + h) * kHeadDim + d], o);
             L = fmaf(wt, red_l[w * G + h], L);
         }
-        const size_t pi = ((size_t)b * a.num_q_heads + kvh * G + h) * a.max_chunks + chunk;
-        a.part_o[pi * kHeadDim + d] = o;
-        if (d == 0) a.part_ml[pi] = make_float2(M, L);
+        const size_t pi = pbase + (size_t)h * a.max_chunks + chunk;
+        __stcg(a.part_o + pi * kHeadDim + d, o);
+        if (d == 0) __stcg(reinterpret_cast<float2 *>(a.part_ml) + pi, make_float2(M, L));
     }
-}
 
-// ----------------------------------------------------------------- combine --
-template <int G>
-__global__ void __launch_bounds__(kHeadDim) attn_combine_kernel(const CombineArgs a) {
-    const int kvh = blockIdx.x, b = blockIdx.y, d = threadIdx.x;
-    const int warp = d >> 5, lane = d & 31;
-    __shared__ float red[kHeadDim / 32][G];
-    __shared__ float s_new[G];
-    const int c = a.context[b];
-    const int n = split_keys(c, a.key_set, a.capacity, a.window, a.max_context, a.chunk_keys,
-                             a.max_chunks, a.err, false);
-    if (n < 0) {
-        for (int h = 0; h < G; ++h) {
-            const int hg = kvh * G + h;
-            a.out[((size_t)b * a.num_q_heads + hg) * kHeadDim + d] = __float2bfloat16_rn(NAN);
-            if (d == 0) a.lse[(size_t)b * a.num_q_heads + hg] = NAN;
-        }
-        return;
+    // Ticket: the last chunk of this (sequence, kv head) to finish does the combine.
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        int *ctr = a.counters + (size_t)b * a.num_kv_heads + kvh;
+        const int ticket = atomicAdd(ctr, 1);
+        const int last = ticket == nchunks - 1;
+        if (last) atomicExch(ctr, 0);  // ready for the next call on this stream
+        *flag_s = last;
+        __threadfence();
     }
-    const int nchunks = (n + a.chunk_keys - 1) / a.chunk_keys;
-    const bool ring = a.key_set == KEYS_RING;
-    float vn = 0.f;
-    if (ring) {
-        const size_t e = ((size_t)b * a.num_kv_heads + kvh) * kHeadDim + d;
-        const float kn = __bfloat162float(a.stage_k[e]);
-        vn = __bfloat162float(a.stage_v[e]);
-#pragma unroll
-        for (int h = 0; h < G; ++h) {
-            float p = a.q_rot[((size_t)b * a.num_q_heads + kvh * G + h) * kHeadDim + d] * kn;
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) p += __shfl_xor_sync(0xffffffffu, p, off);
-            if (lane == 0) red[warp][h] = p;
+    __syncthreads();
+    if (!*flag_s) return;
+
+    // ---- combine (one CTA per sequence and kv head) ----
+    const bool has_new = a.new_kind != NEW_NONE;
+    if (has_new) {
+        const size_t e = ((size_t)b * a.num_kv_heads + kvh) * kHeadDim;
+        for (int d = threadIdx.x; d < kHeadDim; d += blockDim.x) {
+            float kn;
+            if (a.new_kind == NEW_STAGED || d >= a.rotary_dim) {
+                kn = __bfloat162float(a.new_k[e + d]);
+            } else {  // rotate the new key in fp64 from the fp32 table, round once to bf16
+                const float2 *tc = a.table + (size_t)c * (a.rotary_dim >> 1);
+                const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
+                const double x1 = __bfloat162float(a.new_k[e + j]);
+                const double x2 = __bfloat162float(a.new_k[e + j + half]);
+                const double cc = tc[j].x, ss = tc[j].y;
+                kn = f64_to_bf16_value(d < half ? x1 * cc - x2 * ss : x2 * cc + x1 * ss);
+            }
+            knew_s[d] = kn;
+            vnew_s[d] = __bfloat162float(a.new_v[e + d]);
         }
         __syncthreads();
-        if (d < G) {
+    }
+    // Per head: M = max(chunk maxima, new score), chunk weights 2^(m_j - M) and
+    // L = sum of weighted chunk sums (+ the new entry).  Warp w takes heads w, w+5, ...
+    float *wts = reinterpret_cast<float *>(smem);   // [G][nchunks] (the stage ring is free)
+    float *head_s = misc;                           // [G] scale = sink factor / L
+    float *wnew_s = misc + kMaxGroup;               // [G] weight of the new entry
+    const float2 *pml = reinterpret_cast<const float2 *>(a.part_ml);
+    for (int h = warp; h < G; h += kThreads / 32) {
+        const size_t ph = pbase + (size_t)h * a.max_chunks;
+        float s_new = -INFINITY;
+        if (has_new) {
             float t = 0.f;
+            for (int d = lane; d < kHeadDim; d += 32) t = fmaf(q_s[h * kHeadDim + d], knew_s[d], t);
 #pragma unroll
-            for (int w = 0; w < kHeadDim / 32; ++w) t += red[w][d];
-            s_new[d] = t * (kLog2e * 0.0625f);
+            for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+            s_new = t;
         }
-        __syncthreads();
+        float M = s_new;
+        for (int j = lane; j < nchunks; j += 32) M = fmaxf(M, __ldcg(pml + ph + j).x);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float L = 0.f;
+        for (int j = lane; j < nchunks; j += 32) {
+            const float2 ml = __ldcg(pml + ph + j);
+            const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+            wts[h * nchunks + j] = w;
+            L = fmaf(w, ml.y, L);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        const float w_new = has_new ? exp2f(s_new - M) : 0.f;
+        L += w_new;
+        if (lane == 0) {
+            const int hg = kvh * G + h;
+            const float lse = (M + log2f(L)) * kLn2;
+            const float f = a.sink ? 1.f / (1.f + expf(a.sink[hg] - lse)) : 1.f;
+            head_s[h] = f / L;
+            wnew_s[h] = w_new;
+            a.lse[(size_t)b * a.num_q_heads + hg] = lse;
+        }
     }
-#pragma unroll 1
-    for (int h = 0; h < G; ++h) {
-        const int hg = kvh * G + h;
-        const size_t pb = ((size_t)b * a.num_q_heads + hg) * a.max_chunks;
-        float M = ring ? s_new[h] : -INFINITY;
-        for (int j = 0; j < nchunks; ++j) M = fmaxf(M, a.part_ml[pb + j].x);
-        float o = 0.f, L = 0.f;
-        for (int j = 0; j < nchunks; ++j) {
-            const float2 ml = a.part_ml[pb + j];
-            const float wt = exp2f(ml.x - M);
-            L = fmaf(wt, ml.y, L);
-            o = fmaf(wt, a.part_o[(pb + j) * kHeadDim + d], o);
+    __syncthreads();
+    // Outputs: thread t < 128 owns dims [4*(t%64), +4) of every head for the
+    // chunks of parity t/64; the two parities meet in shared memory.
+    float4 *half_s = reinterpret_cast<float4 *>(wts + ((G * nchunks + 3) & ~3));   // [G][64], 16-byte aligned
+    const int dq = threadIdx.x & 63, parity = threadIdx.x >> 6;
+    float4 acc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (parity < 2) {
+        const float4 *po = reinterpret_cast<const float4 *>(a.part_o) + pbase * (kHeadDim / 4) + dq;
+        for (int j = parity; j < nchunks; j += 2) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float w = wts[h * nchunks + j];
+                const float4 v = __ldcg(po + ((size_t)h * a.max_chunks + j) * (kHeadDim / 4));
+                acc[h].x = fmaf(w, v.x, acc[h].x);
+                acc[h].y = fmaf(w, v.y, acc[h].y);
+                acc[h].z = fmaf(w, v.z, acc[h].z);
+                acc[h].w = fmaf(w, v.w, acc[h].w);
+            }
         }
-        if (ring) {
-            const float wt = exp2f(s_new[h] - M);
-            L += wt;
-            o = fmaf(wt, vn, o);
-        }
-        const float lse = (M + log2f(L)) * kLn2;
-        float f = 1.f;
-        if (a.sink) f = 1.f / (1.f + expf(a.sink[hg] - lse));
-        a.out[((size_t)b * a.num_q_heads + hg) * kHeadDim + d] = __float2bfloat16_rn(o / L * f);
-        if (d == 0) a.lse[(size_t)b * a.num_q_heads + hg] = lse;
     }
-    if (ring) {
-        const int slot = c % a.capacity;
-        const size_t e = ((size_t)b * a.num_kv_heads + kvh) * kHeadDim + d;
-        const size_t o = (size_t)b * a.seq_stride + ((size_t)kvh * a.capacity + slot) * kHeadDim + d;
-        a.cache_k[o] = a.stage_k[e];
-        a.cache_v[o] = a.stage_v[e];
+    if (parity == 1) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) half_s[h * 64 + dq] = acc[h];
+    }
+    __syncthreads();
+    if (parity == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float4 o1 = half_s[h * 64 + dq];
+            float o[4] = {acc[h].x + o1.x, acc[h].y + o1.y, acc[h].z + o1.z, acc[h].w + o1.w};
+            const float sc = head_s[h], wn = wnew_s[h];
+            __nv_bfloat16 r[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (has_new) o[i] = fmaf(wn, vnew_s[4 * dq + i], o[i]);
+                r[i] = __float2bfloat16_rn(o[i] * sc);
+            }
+            uint2 packed;
+            packed.x = (uint32_t)__bfloat16_as_ushort(r[0]) | ((uint32_t)__bfloat16_as_ushort(r[1]) << 16);
+            packed.y = (uint32_t)__bfloat16_as_ushort(r[2]) | ((uint32_t)__bfloat16_as_ushort(r[3]) << 16);
+            *reinterpret_cast<uint2 *>(a.out + ((size_t)b * a.num_q_heads + kvh * G + h) * kHeadDim + 4 * dq) = packed;
+        }
+    }
+    // Store the new entry now that every chunk of this (sequence, kv head) has read the cache.
+    if (has_new && a.commit != COMMIT_NONE) {
+        const int slot = a.commit == COMMIT_RING ? c % a.capacity : c;
+        const size_t o = (size_t)b * a.seq_stride + ((size_t)kvh * a.capacity + slot) * kHeadDim;
+        for (int d = threadIdx.x; d < kHeadDim; d += blockDim.x) {
+            a.cache_k[o + d] = __float2bfloat16_rn(knew_s[d]);   // exact: knew_s holds bf16 values
+            a.cache_v[o + d] = __float2bfloat16_rn(vnew_s[d]);
+        }
     }
 }
 
-template <int G>
-cudaError_t split_g(const CUtensorMap *km, const CUtensorMap *vm, const SplitArgs &a, int batch,
-                    cudaStream_t s) {
+template <int G, int CONSUMER>
+cudaError_t launch_g(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
+                     cudaStream_t s) {
     static bool configured = false;
-    const size_t smem = split_smem_bytes();
+    const size_t smem = layer_smem_bytes();
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_split_kernel<G>,
+        cudaError_t e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    attn_split_kernel<G><<<dim3(a.max_chunks, a.num_kv_heads, batch), kSplitThreads, smem, s>>>(
+    attn_layer_kernel<G, CONSUMER><<<dim3(a.max_chunks, a.num_kv_heads, batch), kThreads, smem, s>>>(
         *km, *vm, a);
     return cudaGetLastError();
 }
 
-}  // namespace
-
-size_t split_smem_bytes() { return 1024 + kStages * kStageBytes + 2 * kStages * sizeof(uint64_t); }
-
-cudaError_t launch_split(const CUtensorMap *km, const CUtensorMap *vm, const SplitArgs &a, int batch,
-                         int group, cudaStream_t s) {
+template <int CONSUMER>
+cudaError_t launch_c(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
+                     int group, cudaStream_t s) {
     switch (group) {
-    case 1: return split_g<1>(km, vm, a, batch, s);
-    case 2: return split_g<2>(km, vm, a, batch, s);
-    case 4: return split_g<4>(km, vm, a, batch, s);
-    case 8: return split_g<8>(km, vm, a, batch, s);
+    case 1: return launch_g<1, CONSUMER>(km, vm, a, batch, s);
+    case 2: return launch_g<2, CONSUMER>(km, vm, a, batch, s);
+    case 4: return launch_g<4, CONSUMER>(km, vm, a, batch, s);
+    case 8: return launch_g<8, CONSUMER>(km, vm, a, batch, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
-cudaError_t launch_combine(const CombineArgs &a, int batch, int group, cudaStream_t s) {
-    const dim3 grid(a.num_kv_heads, batch);
-    switch (group) {
-    case 1: attn_combine_kernel<1><<<grid, kHeadDim, 0, s>>>(a); break;
-    case 2: attn_combine_kernel<2><<<grid, kHeadDim, 0, s>>>(a); break;
-    case 4: attn_combine_kernel<4><<<grid, kHeadDim, 0, s>>>(a); break;
-    case 8: attn_combine_kernel<8><<<grid, kHeadDim, 0, s>>>(a); break;
-    default: return cudaErrorInvalidValue;
-    }
-    return cudaGetLastError();
+}  // namespace
+
+size_t layer_smem_bytes() {
+    return 1024 + kStages * kStageBytes + (kMaxGroup * kHeadDim + 2 * kHeadDim + 32) * sizeof(float) +
+           2 * kStages * sizeof(uint64_t) + 16;
+}
+
+cudaError_t launch_layer(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
+                         int group, int consumer, cudaStream_t s) {
+    return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA>(km, vm, a, batch, group, s)
+                                    : launch_c<CONSUMER_FMA>(km, vm, a, batch, group, s);
 }
 
 }  // namespace hd

@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <type_traits>
 
 #include "hybrid_decode.h"
 
@@ -23,44 +24,48 @@ constexpr int kStageBytes = 2 * kBoxesPerRow * kBoxBytes;         // K + V: 32 K
 constexpr int kChunkMin = 64;
 constexpr int kChunkMax = 512;
 
-// Which keys a split CTA scores for sequence b with c = context[b] previous tokens.
+// Which cache rows the split pass scores for sequence b with c = context[b].
 enum KeySet : int32_t {
-    KEYS_RING = 0,  // cached ring slots [0, min(c, capacity)); the new entry is scored by the combine
-    KEYS_ROLL = 1,  // rolled window [0, min(c + 1, window)) (the new entry is already in it)
-    KEYS_FULL = 2   // positions [0, c] (the new entry was appended at index c)
+    KEYS_RING = 0,         // ring slots [0, min(c, capacity)); the new entry is scored apart
+    KEYS_ROLL = 1,         // rolled window [0, min(c + 1, window)), the new entry already in it
+    KEYS_FULL_CACHED = 2,  // positions [0, c]: the new entry was appended at index c
+    KEYS_FULL_PREV = 3     // positions [0, c): the new entry is scored apart and appended
 };
-
-// Split-K pass: one CTA per (chunk, kv head, sequence).
-struct SplitArgs {
-    const int32_t *context;
-    const float *q_rot;      // [batch][Hq][D]
-    float *part_o;           // [batch][Hq][max_chunks][D] unnormalised partial outputs
-    float2 *part_ml;         // [batch][Hq][max_chunks] (running max in log2 units, sum)
-    int32_t *err;
-    int32_t num_q_heads, num_kv_heads;
-    int32_t chunk_keys, max_chunks;
-    int32_t key_set, capacity, window, max_context;
+// Where the new entry comes from when it is scored apart from the cache.
+enum NewEntry : int32_t {
+    NEW_NONE = 0,     // already in the scored cache rows
+    NEW_ROTATE = 1,   // bf16 k of the step, rotated (fp64, one rounding) in the kernel
+    NEW_STAGED = 2    // already rotated and rounded (ring staging row)
 };
+// Where the new entry is stored once every chunk has read the cache.
+enum Commit : int32_t { COMMIT_NONE = 0, COMMIT_APPEND = 1, COMMIT_RING = 2 };
+enum Consumer : int32_t { CONSUMER_FMA = 0, CONSUMER_MMA = 1 };
 
-// LSE combine + sink + ring commit: one CTA per (kv head, sequence).
-struct CombineArgs {
+// One attention layer: one CTA per (chunk, kv head, sequence); the last CTA of
+// each (sequence, kv head) combines the chunks.
+struct LayerArgs {
     const int32_t *context;
-    const float *q_rot;
-    const float *part_o;
-    const float2 *part_ml;
-    const float *sink;                 // [Hq] or null
-    __nv_bfloat16 *out;                // [batch][Hq][D]
-    float *lse;                        // [batch][Hq]
-    const __nv_bfloat16 *stage_k;      // ring staging [batch][Hkv][D] (KEYS_RING only)
-    const __nv_bfloat16 *stage_v;
-    __nv_bfloat16 *cache_k;            // ring commit target (KEYS_RING only)
+    const __nv_bfloat16 *q_bf16;   // [batch][Hq][D], rotated in the kernel ...
+    const float *q_rot;            // ... or already rotated, fp32 (when q_bf16 is null)
+    const float2 *table;           // [max_context + 1][rotary_dim / 2] (cos, sin)
+    int32_t rotary_dim;
+    const __nv_bfloat16 *new_k;    // [batch][Hkv][D] (NEW_ROTATE: raw k; NEW_STAGED: staged)
+    const __nv_bfloat16 *new_v;
+    int32_t new_kind, commit, key_set;
+    __nv_bfloat16 *cache_k;        // cache of the layer (also the store target)
     __nv_bfloat16 *cache_v;
     int64_t seq_stride;
     int32_t capacity;
+    const float *sink;             // [Hq] or null
+    __nv_bfloat16 *out;            // [batch][Hq][D]
+    float *lse;                    // [batch][Hq]
+    float *part_o;                 // [batch][Hq][max_chunks][D] unnormalised partial outputs
+    float2 *part_ml;               // [batch][Hq][max_chunks] (max in log2 units, sum)
+    int32_t *counters;             // [max_batch][Hkv], zero between calls
     int32_t *err;
     int32_t num_q_heads, num_kv_heads;
     int32_t chunk_keys, max_chunks;
-    int32_t key_set, window, max_context;
+    int32_t window, max_context;
 };
 
 // Partial RoPE of q and the new k, and the K/V store.
@@ -82,9 +87,8 @@ struct RopeArgs {
 
 cudaError_t launch_rope_append(const RopeArgs &a, int batch, cudaStream_t s);
 cudaError_t launch_roll_window(const RopeArgs &a, int batch, cudaStream_t s);
-cudaError_t launch_split(const CUtensorMap *kmap, const CUtensorMap *vmap, const SplitArgs &a,
-                         int batch, int group, cudaStream_t s);
-cudaError_t launch_combine(const CombineArgs &a, int batch, int group, cudaStream_t s);
-size_t split_smem_bytes();
+cudaError_t launch_layer(const CUtensorMap *kmap, const CUtensorMap *vmap, const LayerArgs &a,
+                         int batch, int group, int consumer, cudaStream_t s);
+size_t layer_smem_bytes();
 
 }  // namespace hd

@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(256) rope_append_kernel(const RopeArgs a) {
     }
     if (a.key_set == KEYS_ROLL) return;  // the roll kernel stores K/V
     int slot = 0;
-    if (a.key_set == KEYS_FULL) {
+    if (a.key_set == KEYS_FULL_CACHED) {
         if (c >= a.capacity) {
             if (threadIdx.x == 0) set_err(a.err, HD_DEVERR_CONTEXT_CAPACITY);
             return;

@@ -173,11 +173,22 @@ hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int3
                            int32_t max_context_hint, const float *q_rot, hd_kv_cache cache,
                            const float *sink, void *out, float *lse, void *stream);
 
-/* One decode step over all layers in order: rope_append_kv then the layer's
- * attention, with q_rot held in the context's workspace.  `layers` is a host
- * array [num_layers]. */
+/* One decode step over all layers in order, with the same results as
+ * rope_append_kv followed by the layer's attention call, in one kernel per
+ * layer: q is rotated in the attention kernel and the new entry is rotated,
+ * scored and stored (appended, or written to its ring slot after the ring was
+ * read) by the combine; a roll layout first shifts its window.  `layers` is a
+ * host array [num_layers]. */
 hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_t max_context_hint,
                       const hd_layer_io *layers, void *stream);
+
+/* Inner loop of the attention kernels (same results within the stated
+ * tolerance; the default is the tensor-core one):
+ *   HD_CONSUMER_CUDA_CORE   fp32 FMA with warp-shuffle reductions;
+ *   HD_CONSUMER_TENSOR_CORE mma.sync bf16 (q split into a bf16 high and low
+ *                           part) with fp32 accumulation. */
+enum { HD_CONSUMER_CUDA_CORE = 0, HD_CONSUMER_TENSOR_CORE = 1 };
+hd_status hybrid_decode_set_consumer(hd_ctx *ctx, int32_t consumer);
 
 /* Reads and clears the device error word (HD_DEVERR_* bits).  Synchronises
  * `stream`. */

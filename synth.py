@@ -43,6 +43,11 @@ WORKLOADS = {
     # Seven full layers only, batch 4 at context 131072.
     "full7_b4_c131072": dict(layer_types=[FULL] * 7, batch=4, num_q_heads=8, num_kv_heads=2,
                              lengths=("fixed", 131072), sink=("normal", 1.0, 0.0)),
+    # A small block for profiler captures: [S,S,S,F], batch 16, same length mix
+    # (about 1 GB of full-layer cache: larger than L2, a few GB on the device).
+    "block4_b16_c512_32768": dict(layer_types=[SLIDING, SLIDING, SLIDING, FULL], batch=16,
+                                  num_q_heads=8, num_kv_heads=2, lengths=("uniform", 512, 32768),
+                                  sink=("normal", 1.0, 0.0)),
     # Group 8: batch 256, 90% at 8192 and 10% (26 of 256) uniform in [1, 512];
     # sink N(0, variance 2) with a quarter of the heads at -inf.
     "step28_b256_g8_mixed": dict(layer_types=SPARK_LAYER_TYPES, batch=256, num_q_heads=16,

@@ -20,10 +20,17 @@ def _need_gpu():
         pytest.skip("needs a CUDA GPU")
 
 
-def make_ctx(hd, layer_types, Hq=8, Hkv=2, layout=0, max_batch=4, max_context=2048):
-    return hd.hybrid_decode_init(hd.Config(layer_types=layer_types, num_q_heads=Hq, num_kv_heads=Hkv,
-                                           cache_layout=layout, max_batch=max_batch,
-                                           max_context=max_context))
+CONSUMERS = ["tensor_core", "cuda_core"]
+
+
+def make_ctx(hd, layer_types, Hq=8, Hkv=2, layout=0, max_batch=4, max_context=2048,
+             consumer="tensor_core"):
+    ctx = hd.hybrid_decode_init(hd.Config(layer_types=layer_types, num_q_heads=Hq, num_kv_heads=Hkv,
+                                          cache_layout=layout, max_batch=max_batch,
+                                          max_context=max_context))
+    hd.hybrid_decode_set_consumer(ctx, hd.HD_CONSUMER_TENSOR_CORE if consumer == "tensor_core"
+                                  else hd.HD_CONSUMER_CUDA_CORE)
+    return ctx
 
 
 def sink_for(rng, kind, Hq):
@@ -34,11 +41,12 @@ def sink_for(rng, kind, Hq):
     return synth.sink_vector(rng, ("normal", 2.0 ** 0.5, 0.25), Hq)  # a quarter at -inf
 
 
+@pytest.mark.parametrize("consumer", CONSUMERS)
 @pytest.mark.parametrize("c", [64, 700])
-def test_tiny_hybrid_pair(hd, orc, c):
+def test_tiny_hybrid_pair(hd, orc, c, consumer):
     """1 sliding (ring of 511) + 1 full layer, batch 2, 8/2 heads, sink N(0,1)."""
     rng = synth.generator(0)
-    ctx = make_ctx(hd, [SLIDING, FULL], max_batch=2, max_context=1024)
+    ctx = make_ctx(hd, [SLIDING, FULL], max_batch=2, max_context=1024, consumer=consumer)
     sink = synth.sink_vector(rng, ("normal", 1.0, 0.0), 8)
     check_layer(hd, orc, ctx, 0, SLIDING, RING, LayerCase(rng, 2, 8, 2, 511, [c, c], sink=sink))
     check_layer(hd, orc, ctx, 1, FULL, 0, LayerCase(rng, 2, 8, 2, 1025, [c, c], sink=sink))
@@ -47,12 +55,13 @@ def test_tiny_hybrid_pair(hd, orc, c):
 RING_CONTEXTS = [0, 1, 31, 32, 33, 64, 200, 510, 511, 512, 513, 700, 1021, 1022, 1023, 5000]
 
 
+@pytest.mark.parametrize("consumer", CONSUMERS)
 @pytest.mark.parametrize("g", [1, 2, 4, 8])
 @pytest.mark.parametrize("sink_kind", ["none", "normal", "neg_inf"])
-def test_sliding_ring_contexts(hd, orc, g, sink_kind):
+def test_sliding_ring_contexts(hd, orc, g, sink_kind, consumer):
     rng = synth.generator(100 + g)
     B, Hkv = len(RING_CONTEXTS), 2
-    ctx = make_ctx(hd, [SLIDING], Hq=g * Hkv, max_batch=B, max_context=5000)
+    ctx = make_ctx(hd, [SLIDING], Hq=g * Hkv, max_batch=B, max_context=5000, consumer=consumer)
     case = LayerCase(rng, B, g * Hkv, Hkv, 511, RING_CONTEXTS, sink=sink_for(rng, sink_kind, g * Hkv))
     check_layer(hd, orc, ctx, 0, SLIDING, RING, case)
 
@@ -60,12 +69,13 @@ def test_sliding_ring_contexts(hd, orc, g, sink_kind):
 FULL_CONTEXTS = [0, 1, 31, 32, 63, 64, 65, 127, 128, 511, 512, 513, 1000, 2047, 3001, 4096]
 
 
+@pytest.mark.parametrize("consumer", CONSUMERS)
 @pytest.mark.parametrize("g", [1, 2, 4, 8])
 @pytest.mark.parametrize("sink_kind", ["none", "normal", "neg_inf"])
-def test_full_contexts(hd, orc, g, sink_kind):
+def test_full_contexts(hd, orc, g, sink_kind, consumer):
     rng = synth.generator(200 + g)
     B, Hkv = len(FULL_CONTEXTS), 2
-    ctx = make_ctx(hd, [FULL], Hq=g * Hkv, max_batch=B, max_context=4096)
+    ctx = make_ctx(hd, [FULL], Hq=g * Hkv, max_batch=B, max_context=4096, consumer=consumer)
     case = LayerCase(rng, B, g * Hkv, Hkv, 4097, FULL_CONTEXTS, sink=sink_for(rng, sink_kind, g * Hkv))
     check_layer(hd, orc, ctx, 0, FULL, 0, case)
 
@@ -145,14 +155,15 @@ def test_multistep_lockstep(hd, orc):
         assert_bits_equal(vd, vc_ref, f"V cache after {steps} steps ({layer_type}, {layout})")
 
 
+@pytest.mark.parametrize("consumer", CONSUMERS)
 @pytest.mark.parametrize("layout", [RING, ROLL])
-def test_decode_step_28_layers(hd, orc, layout):
+def test_decode_step_28_layers(hd, orc, layout, consumer):
     """decode_step over the 28-layer [S,S,S,F]x7 step vs the oracle layer by layer."""
     rng = synth.generator(31)
     B, Hq, Hkv, D = 2, 8, 2, 256
     context = np.array([700, 1500], np.int32)
     types = synth.SPARK_LAYER_TYPES
-    ctx = make_ctx(hd, types, layout=layout, max_batch=B, max_context=2048)
+    ctx = make_ctx(hd, types, layout=layout, max_batch=B, max_context=2048, consumer=consumer)
     sink = synth.sink_vector(rng, ("normal", 1.0, 0.0), Hq)
     cases, ios, outs = [], [], []
     for t in types:
@@ -177,13 +188,55 @@ def test_decode_step_28_layers(hd, orc, layout):
         assert_bits_equal(vd, ref["vcache"], f"layer {i} V cache")
 
 
-def test_group8_mixed_lengths_with_neg_inf_sinks(hd, orc):
+@pytest.mark.parametrize("consumer", CONSUMERS)
+def test_group8_mixed_lengths_with_neg_inf_sinks(hd, orc, consumer):
     """High-group shape: 16 q / 2 kv heads, 90% long and 10% short sequences,
     sink N(0, variance 2) with a quarter of the heads at -inf."""
     rng = synth.generator(41)
     B, Hq, Hkv = 20, 16, 2
     context = synth.context_lengths(rng, ("mixed", 2048, 0.10, 512), B)
     sink = synth.sink_vector(rng, ("normal", 2.0 ** 0.5, 0.25), Hq)
-    ctx = make_ctx(hd, [SLIDING, FULL], Hq=Hq, max_batch=B, max_context=2048)
+    ctx = make_ctx(hd, [SLIDING, FULL], Hq=Hq, max_batch=B, max_context=2048, consumer=consumer)
     check_layer(hd, orc, ctx, 0, SLIDING, RING, LayerCase(rng, B, Hq, Hkv, 511, context, sink=sink))
     check_layer(hd, orc, ctx, 1, FULL, 0, LayerCase(rng, B, Hq, Hkv, 2049, context, sink=sink))
+
+
+@pytest.mark.parametrize("layout", [RING, ROLL])
+def test_decode_step_multistep_lockstep(hd, orc, layout):
+    """40 consecutive decode_step calls of a [S,S,S,F] block from contexts that cross
+    the window; every output and, at the end, every cache equals the oracle's."""
+    rng = synth.generator(51)
+    B, Hq, Hkv, D, steps = 2, 8, 2, 256, 40
+    types = [SLIDING, SLIDING, SLIDING, FULL]
+    start = np.array([490, 3], np.int32)
+    ctx = make_ctx(hd, types, layout=layout, max_batch=B, max_context=600)
+    sink = synth.sink_vector(rng, ("normal", 1.0, 0.0), Hq)
+    caps = [(511 if layout == RING else 512) if t == SLIDING else 601 for t in types]
+    host = [[synth.bits(c) for c in (LayerCase(rng, B, Hq, Hkv, cap, start).kc,
+                                      LayerCase(rng, B, Hq, Hkv, cap, start).vc)] for cap in caps]
+    dev = [(synth.from_bits(k).cuda(), synth.from_bits(v).cuda()) for k, v in host]
+    for s_ in range(steps):
+        context = start + s_
+        ios, outs, refs = [], [], []
+        for i, t in enumerate(types):
+            q = synth.normal_bf16(rng, (B, Hq, D))
+            k = synth.normal_bf16(rng, (B, Hkv, D))
+            v = synth.normal_bf16(rng, (B, Hkv, D))
+            rot, theta = synth.ROPE[t]
+            refs.append(orc.decode_layer(layer_type=t, layout=layout if t == SLIDING else 0, window=512,
+                                         rotary_dim=rot, rope_theta=theta, context=context,
+                                         q=synth.bits(q), k=synth.bits(k), v=synth.bits(v),
+                                         kcache=host[i][0], vcache=host[i][1], sink=sink.numpy()))
+            out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+            lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+            keep = (q.cuda(), k.cuda(), v.cuda(), sink.cuda())
+            ios.append(hd.layer_io(keep[0], keep[1], keep[2], hd.kv_cache(*dev[i]), keep[3], out, lse))
+            outs.append((out, lse, keep))
+        hd.decode_step(ctx, torch.from_numpy(context).cuda(), ios, B)
+        for i in range(len(types)):
+            assert_out_close(outs[i][0], refs[i]["out"], f"step {s_} layer {i} out")
+            assert_lse_close(outs[i][1], refs[i]["lse"], f"step {s_} layer {i} lse")
+    assert hd.hybrid_decode_device_errors(ctx) == 0
+    for i in range(len(types)):
+        assert_bits_equal(dev[i][0], host[i][0], f"layer {i} K cache")
+        assert_bits_equal(dev[i][1], host[i][1], f"layer {i} V cache")
