@@ -79,6 +79,7 @@ _SIGS = {
     "hybrid_decode_set_profiling": [_P, _i32],
     "hybrid_decode_profile": [_P, _c.POINTER(_c.c_double), _c.POINTER(_i64)],
     "hybrid_decode_set_consumer": [_P, _i32],
+    "decode_attn_full_static_scratch": [_i32, _i32, _i32, _P, _i32, _P, hd_kv_cache, _P, _P, _P, _P],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -278,3 +279,18 @@ def hybrid_decode_profile(ctx: Context) -> tuple[float, int]:
 def hybrid_decode_set_consumer(ctx: Context, consumer: int) -> None:
     """HD_CONSUMER_CUDA_CORE or HD_CONSUMER_TENSOR_CORE (the default)."""
     _check(_lib.hybrid_decode_set_consumer(ctx.handle, consumer), "hybrid_decode_set_consumer")
+
+
+def decode_attn_full_static_scratch(num_kv_heads: int, context, max_context: int, q_rot,
+                                    cache: hd_kv_cache, sink, out, lse, stream=None) -> None:
+    """Full-layer attention without a context and without any allocation: for
+    callers that cannot allocate device memory while running.  The scratch is a
+    64 MiB array inside the library, shared by all calls: calls that overlap on
+    the GPU race, so order them on one stream.  See include/hybrid_decode.h."""
+    batch, num_q_heads = q_rot.shape[0], q_rot.shape[1]
+    _check_sink(sink, num_q_heads, q_rot)
+    _check_batch(cache, batch)
+    _check(_lib.decode_attn_full_static_scratch(batch, num_q_heads, num_kv_heads, _ptr(context),
+                                                max_context, _ptr(q_rot), cache, _ptr(sink), _ptr(out),
+                                                _ptr(lse), _stream(stream)),
+           "decode_attn_full_static_scratch")

@@ -204,6 +204,29 @@ hd_status hybrid_decode_launch_count(hd_ctx *ctx, int64_t *launches);
 hd_status hybrid_decode_set_profiling(hd_ctx *ctx, int32_t enable);
 hd_status hybrid_decode_profile(hd_ctx *ctx, double *total_ms, int64_t *launches);
 
+/* Full-layer attention that allocates nothing (no counterpart in the paper;
+ * it exists for callers that cannot call cudaMalloc once running, such as a
+ * plugin inside a runtime that pre-plans every device allocation, or a
+ * serving loop where cudaMalloc/cudaFree could synchronise the device).
+ * Same result as decode_attn_full (after rope_append_kv appended the new
+ * entry at index context[b]; scores positions 0..context[b]), but it needs no
+ * hd_ctx: the caller passes the inputs and outputs and the shape, and the
+ * split-K scratch lives in one 64 MiB file-scope device array of the library
+ * (held on every GPU that uses the library until the process exits).
+ *   max_context  upper bound on every context[b] of this call; max_context+1
+ *                <= cache.capacity.
+ * Returns HD_ERR_CAPACITY when the call's scratch (about batch * num_q_heads *
+ * chunks * 1032 bytes, chunks = ceil((max_context+1)/chunk) with chunk <= 512)
+ * would exceed 64 MiB.  All calls share the array and it keeps the last
+ * call's contents (the tickets are cleared at every call), so calls that
+ * overlap on the GPU race: order them on one stream.  The first call on a
+ * device looks up the array's address for that device; make it before any
+ * stream capture.  Invalid contexts give NaN out/lse for that sequence. */
+hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                          const int32_t *context, int32_t max_context,
+                                          const float *q_rot, hd_kv_cache cache, const float *sink,
+                                          void *out, float *lse, void *stream);
+
 /* Static text for a status code. */
 const char *hd_status_string(hd_status status);
 
