@@ -42,7 +42,7 @@ KV_ROW_BYTES = 2 * synth.HEAD_DIM * 2       # K row + V row, bf16, one kv head
 DEFAULT_WORKLOAD = "step28_b64_c512_32768"
 SECONDARY_WORKLOAD = "step28_b1_c4096"
 METRIC = "KV-read HBM GB/s (% of GB300 peak); µs per 28-layer decode step"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_split_full_b64_traffic.txt")
+PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_layer_kernel_full_b64_traffic.txt")
 
 
 # ------------------------------------------------------------------ helpers --
@@ -232,6 +232,8 @@ class Workload:
         full_idx = [i for i, t in enumerate(self.types) if t == synth.FULL]
         self.full_layer_bytes = (int(scored_keys(synth.FULL, self.context, layout).sum()) * self.Hkv
                                  * KV_ROW_BYTES) if full_idx else 0
+        self.sliding_layer_bytes = (int(scored_keys(synth.SLIDING, self.context, layout).sum()) * self.Hkv
+                                    * KV_ROW_BYTES)
 
     def step(self, stream=None):
         import full_gqa_decode_gb300 as hd
@@ -366,11 +368,13 @@ def run_ours(args, world, rank, local) -> int:
         for _ in range(args.warmup):
             wl.step()
         torch.cuda.synchronize()
-        hd.hybrid_decode_profile(wl.ctx)  # drop the warm-up records
+        for t in (hd.HD_SLIDING, hd.HD_FULL):
+            hd.hybrid_decode_profile(wl.ctx, t)  # drop the warm-up records
         n0 = hd.hybrid_decode_launch_count(wl.ctx)
         ms = time_steps(wl.step, args.steps, 0, world, device)
         n1 = hd.hybrid_decode_launch_count(wl.ctx)
-        split_ms, split_launches = hd.hybrid_decode_profile(wl.ctx)
+        split_ms, split_launches = hd.hybrid_decode_profile(wl.ctx, hd.HD_FULL)
+        slide_ms, slide_launches = hd.hybrid_decode_profile(wl.ctx, hd.HD_SLIDING)
     hd.hybrid_decode_set_profiling(wl.ctx, False)
     clk = clocks.summary()
     flags = hd.hybrid_decode_device_errors(wl.ctx)
@@ -388,6 +392,12 @@ def run_ours(args, world, rank, local) -> int:
                 "traffic": profiled_traffic(), "kernel": f"attn_layer_kernel, full layers ({args.consumer})",
                 "algorithmic_bytes_per_launch": wl.full_layer_bytes,
                 "avg_launch_ms": round(avg_split_ms, 4), "peak_source": peaks["source"]}
+    if slide_launches:
+        avg_slide = slide_ms / slide_launches
+        roofline["sliding_layers"] = {
+            "achieved": round(wl.sliding_layer_bytes / (avg_slide * 1e-3) / 1e9, 1),
+            "frac": round(wl.sliding_layer_bytes / (avg_slide * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
+            "algorithmic_bytes_per_launch": wl.sliding_layer_bytes, "avg_launch_ms": round(avg_slide, 4)}
 
     # end to end: host buffers, copies inside the timed region
     e2e = e2e_measure(wl, args, world, device)

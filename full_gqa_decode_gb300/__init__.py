@@ -77,7 +77,7 @@ _SIGS = {
     "hybrid_decode_device_errors": [_P, _c.POINTER(_i32), _P],
     "hybrid_decode_launch_count": [_P, _c.POINTER(_i64)],
     "hybrid_decode_set_profiling": [_P, _i32],
-    "hybrid_decode_profile": [_P, _c.POINTER(_c.c_double), _c.POINTER(_i64)],
+    "hybrid_decode_profile": [_P, _i32, _c.POINTER(_c.c_double), _c.POINTER(_i64)],
     "hybrid_decode_set_consumer": [_P, _i32],
     "decode_attn_full_static_scratch": [_i32, _i32, _i32, _P, _i32, _P, hd_kv_cache, _P, _P, _P, _P],
 }
@@ -269,9 +269,10 @@ def hybrid_decode_set_profiling(ctx: Context, enable: bool) -> None:
     _check(_lib.hybrid_decode_set_profiling(ctx.handle, int(enable)), "hybrid_decode_set_profiling")
 
 
-def hybrid_decode_profile(ctx: Context) -> tuple[float, int]:
+def hybrid_decode_profile(ctx: Context, layer_type: int = HD_FULL) -> tuple[float, int]:
+    """(summed kernel milliseconds, launches) of the given layer type since the last read."""
     ms, n = ctypes.c_double(), ctypes.c_int64()
-    _check(_lib.hybrid_decode_profile(ctx.handle, ctypes.byref(ms), ctypes.byref(n)),
+    _check(_lib.hybrid_decode_profile(ctx.handle, layer_type, ctypes.byref(ms), ctypes.byref(n)),
            "hybrid_decode_profile")
     return ms.value, n.value
 

@@ -54,8 +54,8 @@ struct hd_ctx {
     int64_t launches = 0;
     std::vector<MapCacheEntry> maps;     // one per layer
     bool profiling = false;
-    std::vector<cudaEvent_t> ev_begin, ev_end;
-    size_t ev_used = 0;
+    std::vector<cudaEvent_t> ev_begin, ev_end;  // [2][kProfileEvents]: per layer type
+    size_t ev_used[2] = {0, 0};
 };
 
 namespace {
@@ -254,15 +254,16 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     a.window = ctx->cfg.sliding_window;
     a.max_context = ctx->cfg.max_context;
 
-    const bool timed = ctx->profiling && !sliding && ctx->ev_used < ctx->ev_begin.size();
-    if (timed && cudaEventRecord(ctx->ev_begin[ctx->ev_used], stream) != cudaSuccess)
-        return HD_ERR_CUDA;
+    const int type = sliding ? HD_SLIDING : HD_FULL;
+    const size_t slot = (size_t)type * kProfileEvents + ctx->ev_used[type];
+    const bool timed = ctx->profiling && ctx->ev_used[type] < (size_t)kProfileEvents;
+    if (timed && cudaEventRecord(ctx->ev_begin[slot], stream) != cudaSuccess) return HD_ERR_CUDA;
     st = cuda_status(launch_layer(km, vm, a, L.batch, ctx->group, ctx->consumer, stream));
     if (st != HD_OK) return st;
     ++ctx->launches;
     if (timed) {
-        if (cudaEventRecord(ctx->ev_end[ctx->ev_used], stream) != cudaSuccess) return HD_ERR_CUDA;
-        ++ctx->ev_used;
+        if (cudaEventRecord(ctx->ev_end[slot], stream) != cudaSuccess) return HD_ERR_CUDA;
+        ++ctx->ev_used[type];
     }
     return HD_OK;
 }
@@ -609,31 +610,34 @@ hd_status hybrid_decode_launch_count(hd_ctx *ctx, int64_t *launches) {
 hd_status hybrid_decode_set_profiling(hd_ctx *ctx, int32_t enable) {
     if (!ctx) return HD_ERR_INVALID_ARG;
     if (enable && ctx->ev_begin.empty()) {
-        ctx->ev_begin.resize(kProfileEvents);
-        ctx->ev_end.resize(kProfileEvents);
-        for (int i = 0; i < kProfileEvents; ++i)
+        ctx->ev_begin.resize(2 * kProfileEvents);
+        ctx->ev_end.resize(2 * kProfileEvents);
+        for (int i = 0; i < 2 * kProfileEvents; ++i)
             if (cudaEventCreate(&ctx->ev_begin[i]) != cudaSuccess ||
                 cudaEventCreate(&ctx->ev_end[i]) != cudaSuccess)
                 return HD_ERR_CUDA;
     }
     ctx->profiling = enable != 0;
-    ctx->ev_used = 0;
+    ctx->ev_used[0] = ctx->ev_used[1] = 0;
     return HD_OK;
 }
 
-hd_status hybrid_decode_profile(hd_ctx *ctx, double *total_ms, int64_t *launches) {
+hd_status hybrid_decode_profile(hd_ctx *ctx, int32_t layer_type, double *total_ms, int64_t *launches) {
     if (!ctx || !total_ms || !launches) return HD_ERR_INVALID_ARG;
+    if (layer_type != HD_SLIDING && layer_type != HD_FULL) return HD_ERR_INVALID_ARG;
     double sum = 0.0;
-    for (size_t i = 0; i < ctx->ev_used; ++i) {
-        if (cudaEventSynchronize(ctx->ev_end[i]) != cudaSuccess) return HD_ERR_CUDA;
+    const size_t n = ctx->ev_used[layer_type];
+    for (size_t i = 0; i < n; ++i) {
+        const size_t slot = (size_t)layer_type * kProfileEvents + i;
+        if (cudaEventSynchronize(ctx->ev_end[slot]) != cudaSuccess) return HD_ERR_CUDA;
         float ms = 0.f;
-        if (cudaEventElapsedTime(&ms, ctx->ev_begin[i], ctx->ev_end[i]) != cudaSuccess)
+        if (cudaEventElapsedTime(&ms, ctx->ev_begin[slot], ctx->ev_end[slot]) != cudaSuccess)
             return HD_ERR_CUDA;
         sum += ms;
     }
     *total_ms = sum;
-    *launches = (int64_t)ctx->ev_used;
-    ctx->ev_used = 0;
+    *launches = (int64_t)n;
+    ctx->ev_used[layer_type] = 0;
     return HD_OK;
 }
 

@@ -39,6 +39,10 @@ constexpr int kConsumerWarps = 4;
 constexpr int kKeysPerWarp = kStageKeys / kConsumerWarps;  // 8
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
+// Inside the stage ring (free once every stage is consumed): the warp buffers
+// [warps][G][256] + (m, l) and the combine weights start at 0; this chunk's
+// merged partial [G][256] + (m, l) sits past both.
+constexpr int kOwnPartialOffset = 48 * 1024;
 
 // ------------------------------------------------------------ PTX helpers --
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -310,14 +314,17 @@ struct MmaConsumer {
         const int gid = lane >> 2, t4 = lane & 3;
         const int lrow = row0 + (lane & 7), lsub = lane >> 3;
         const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
-        float s[4] = {0.f, 0.f, 0.f, 0.f};
+        // Two accumulators (even / odd k-steps) halve the dependent MMA chain.
+        float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
             uint32_t b0, b1, b2, b3;
             ldsm_x4(kbase + tile_offset(lrow, 4 * p + lsub), b0, b1, b2, b3);
             mma_16816(s, qa[2 * p], b0, b1);
-            mma_16816(s, qa[2 * p + 1], b2, b3);
+            mma_16816(s2, qa[2 * p + 1], b2, b3);
         }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s[j] += s2[j];
         const bool ok0 = gid < G && 2 * t4 < nvalid, ok1 = gid < G && 2 * t4 + 1 < nvalid;
         const float s0 = ok0 ? s[0] + s[2] : -INFINITY;
         const float s1 = ok1 ? s[1] + s[3] : -INFINITY;
@@ -392,13 +399,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     float *q_s = reinterpret_cast<float *>(smem + kStages * kStageBytes);    // [G][256]
     float *knew_s = q_s + G * kHeadDim;                                        // [256]
     float *vnew_s = knew_s + kHeadDim;                                         // [256]
-    float *misc = vnew_s + kHeadDim;                                           // [32]
+    float *kraw_s = vnew_s + kHeadDim;                                         // [256]
+    float2 *tab_s = reinterpret_cast<float2 *>(kraw_s + kHeadDim);             // [128]
+    float *misc = reinterpret_cast<float *>(tab_s + kHeadDim / 2);             // [32]
     uint64_t *full = reinterpret_cast<uint64_t *>(misc + 32);
     uint64_t *empty = full + kStages;
     int *flag_s = reinterpret_cast<int *>(empty + kStages);
 
     const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Programmatic dependent launch: the next layer's grid may be scheduled
+    // while this one finishes, but no global memory is touched before every
+    // write of the previous grid in the stream is complete and visible.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int c = a.context[b];
     int bit = 0;
     const int n = cached_keys(a, c, &bit);
@@ -445,6 +459,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         q_s[i] = x * kQScale;
     }
+    // Inputs of the combine (new entry, its rotary row, the sink), fetched with q
+    // so the CTA that ends up combining does not wait on global loads later.
     __syncthreads();
 
     float *red_o = reinterpret_cast<float *>(smem);             // reuses the stage ring
@@ -493,8 +509,11 @@ __global__ void __launch_bounds__(kThreads, 2)
         __syncthreads();
     }
 
-    // Merge the warps into this chunk's partial.
+    // Merge the warps into this chunk's partial: kept in shared memory (past the
+    // warp buffers) and, when the sequence has several chunks, written out.
     const size_t pbase = ((size_t)b * a.num_q_heads + kvh * G) * a.max_chunks;
+    float *own_o = reinterpret_cast<float *>(smem + kOwnPartialOffset);   // [G][256]
+    float2 *own_ml = reinterpret_cast<float2 *>(own_o + G * kHeadDim);    // [G]
     for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
         const int h = i / kHeadDim, d = i % kHeadDim;
         float M = -INFINITY;
@@ -507,49 +526,61 @@ __global__ void __launch_bounds__(kThreads, 2)
             o = fmaf(wt, red_o[(w * G + h) * kHeadDim + d], o);
             L = fmaf(wt, red_l[w * G + h], L);
         }
-        const size_t pi = pbase + (size_t)h * a.max_chunks + chunk;
-        __stcg(a.part_o + pi * kHeadDim + d, o);
-        if (d == 0) __stcg(reinterpret_cast<float2 *>(a.part_ml) + pi, make_float2(M, L));
+        own_o[i] = o;
+        if (d == 0) own_ml[h] = make_float2(M, L);
+        if (nchunks > 1) {
+            const size_t pi = pbase + (size_t)h * a.max_chunks + chunk;
+            __stcg(a.part_o + pi * kHeadDim + d, o);
+            if (d == 0) __stcg(reinterpret_cast<float2 *>(a.part_ml) + pi, make_float2(M, L));
+        }
     }
+    __syncthreads();
 
     // Ticket: the last chunk of this (sequence, kv head) to finish does the combine.
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        int *ctr = a.counters + (size_t)b * a.num_kv_heads + kvh;
-        const int ticket = atomicAdd(ctr, 1);
-        const int last = ticket == nchunks - 1;
-        if (last) atomicExch(ctr, 0);  // ready for the next call on this stream
-        *flag_s = last;
-        __threadfence();
+    // The acq_rel atomic publishes this CTA's partial (ordered after the barrier)
+    // and, for the last CTA, makes every other chunk's partial visible.
+    if (nchunks > 1) {
+        if (threadIdx.x == 0) {
+            int *ctr = a.counters + (size_t)b * a.num_kv_heads + kvh;
+            int ticket;
+            asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(ticket) : "l"(ctr) : "memory");
+            const int last = ticket == nchunks - 1;
+            if (last) atomicExch(ctr, 0);  // ready for the next call on this stream
+            *flag_s = last;
+        }
+        __syncthreads();
+        if (!*flag_s) return;
     }
-    __syncthreads();
-    if (!*flag_s) return;
 
     // ---- combine (one CTA per sequence and kv head) ----
     const bool has_new = a.new_kind != NEW_NONE;
     if (has_new) {
         const size_t e = ((size_t)b * a.num_kv_heads + kvh) * kHeadDim;
         for (int d = threadIdx.x; d < kHeadDim; d += blockDim.x) {
+            kraw_s[d] = __bfloat162float(a.new_k[e + d]);
+            vnew_s[d] = __bfloat162float(a.new_v[e + d]);
+        }
+        if (a.new_kind == NEW_ROTATE)
+            for (int j = threadIdx.x; j < (a.rotary_dim >> 1); j += blockDim.x)
+                tab_s[j] = a.table[(size_t)c * (a.rotary_dim >> 1) + j];
+        __syncthreads();
+        for (int d = threadIdx.x; d < kHeadDim; d += blockDim.x) {
             float kn;
             if (a.new_kind == NEW_STAGED || d >= a.rotary_dim) {
-                kn = __bfloat162float(a.new_k[e + d]);
+                kn = kraw_s[d];
             } else {  // rotate the new key in fp64 from the fp32 table, round once to bf16
-                const float2 *tc = a.table + (size_t)c * (a.rotary_dim >> 1);
                 const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
-                const double x1 = __bfloat162float(a.new_k[e + j]);
-                const double x2 = __bfloat162float(a.new_k[e + j + half]);
-                const double cc = tc[j].x, ss = tc[j].y;
+                const double x1 = kraw_s[j], x2 = kraw_s[j + half];
+                const double cc = tab_s[j].x, ss = tab_s[j].y;
                 kn = f64_to_bf16_value(d < half ? x1 * cc - x2 * ss : x2 * cc + x1 * ss);
             }
             knew_s[d] = kn;
-            vnew_s[d] = __bfloat162float(a.new_v[e + d]);
         }
         __syncthreads();
     }
     // Per head: M = max(chunk maxima, new score), chunk weights 2^(m_j - M) and
     // L = sum of weighted chunk sums (+ the new entry).  Warp w takes heads w, w+5, ...
-    float *wts = reinterpret_cast<float *>(smem);   // [G][nchunks] (the stage ring is free)
+    float *wts = reinterpret_cast<float *>(smem);   // [G][nchunks] (the warp buffers are free)
     float *head_s = misc;                           // [G] scale = sink factor / L
     float *wnew_s = misc + kMaxGroup;               // [G] weight of the new entry
     const float2 *pml = reinterpret_cast<const float2 *>(a.part_ml);
@@ -563,16 +594,35 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
             s_new = t;
         }
+        // Chunk (m, l) pairs: lane j holds chunks j, j+32, ... (one load each).
+        constexpr int kPerLane = 4;
+        float2 ml[kPerLane];
         float M = s_new;
-        for (int j = lane; j < nchunks; j += 32) M = fmaxf(M, __ldcg(pml + ph + j).x);
+#pragma unroll
+        for (int r = 0; r < kPerLane; ++r) {
+            const int j = lane + 32 * r;
+            ml[r] = make_float2(-INFINITY, 0.f);
+            if (j < nchunks) ml[r] = nchunks == 1 ? own_ml[h] : __ldcg(pml + ph + j);
+            M = fmaxf(M, ml[r].x);
+        }
+        for (int j = lane + 32 * kPerLane; j < nchunks; j += 32) M = fmaxf(M, __ldcg(pml + ph + j).x);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
         float L = 0.f;
-        for (int j = lane; j < nchunks; j += 32) {
-            const float2 ml = __ldcg(pml + ph + j);
-            const float w = (ml.x == -INFINITY) ? 0.f : exp2f(ml.x - M);
+#pragma unroll
+        for (int r = 0; r < kPerLane; ++r) {
+            const int j = lane + 32 * r;
+            if (j < nchunks) {
+                const float w = (ml[r].x == -INFINITY) ? 0.f : exp2f(ml[r].x - M);
+                wts[h * nchunks + j] = w;
+                L = fmaf(w, ml[r].y, L);
+            }
+        }
+        for (int j = lane + 32 * kPerLane; j < nchunks; j += 32) {
+            const float2 m2 = __ldcg(pml + ph + j);
+            const float w = (m2.x == -INFINITY) ? 0.f : exp2f(m2.x - M);
             wts[h * nchunks + j] = w;
-            L = fmaf(w, ml.y, L);
+            L = fmaf(w, m2.y, L);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
@@ -595,7 +645,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     float4 acc[G];
 #pragma unroll
     for (int h = 0; h < G; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (parity < 2) {
+    if (nchunks == 1) {
+        if (parity == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float4 v = reinterpret_cast<const float4 *>(own_o)[h * 64 + dq];
+                const float w = wts[h];
+                acc[h] = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
+            }
+        }
+    } else if (parity < 2) {
         const float4 *po = reinterpret_cast<const float4 *>(a.part_o) + pbase * (kHeadDim / 4) + dq;
         for (int j = parity; j < nchunks; j += 2) {
 #pragma unroll
@@ -647,16 +706,24 @@ template <int G, int CONSUMER>
 cudaError_t launch_g(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
                      cudaStream_t s) {
     static bool configured = false;
-    const size_t smem = layer_smem_bytes();
+    const size_t smem = layer_smem_bytes(G);
     if (!configured) {
         cudaError_t e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = true;
     }
-    attn_layer_kernel<G, CONSUMER><<<dim3(a.max_chunks, a.num_kv_heads, batch), kThreads, smem, s>>>(
-        *km, *vm, a);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.max_chunks, a.num_kv_heads, batch);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_layer_kernel<G, CONSUMER>, *km, *vm, a);
 }
 
 template <int CONSUMER>
@@ -673,8 +740,8 @@ cudaError_t launch_c(const CUtensorMap *km, const CUtensorMap *vm, const LayerAr
 
 }  // namespace
 
-size_t layer_smem_bytes() {
-    return 1024 + kStages * kStageBytes + (kMaxGroup * kHeadDim + 2 * kHeadDim + 32) * sizeof(float) +
+size_t layer_smem_bytes(int group) {
+    return 1024 + kStages * kStageBytes + ((size_t)group * kHeadDim + 4 * kHeadDim + 32) * sizeof(float) +
            2 * kStages * sizeof(uint64_t) + 16;
 }
 

@@ -89,6 +89,6 @@ cudaError_t launch_rope_append(const RopeArgs &a, int batch, cudaStream_t s);
 cudaError_t launch_roll_window(const RopeArgs &a, int batch, cudaStream_t s);
 cudaError_t launch_layer(const CUtensorMap *kmap, const CUtensorMap *vmap, const LayerArgs &a,
                          int batch, int group, int consumer, cudaStream_t s);
-size_t layer_smem_bytes();
+size_t layer_smem_bytes(int group);
 
 }  // namespace hd

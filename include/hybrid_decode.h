@@ -197,12 +197,13 @@ hd_status hybrid_decode_device_errors(hd_ctx *ctx, int32_t *flags, void *stream)
 /* Kernel launches issued by this context since init (host counter). */
 hd_status hybrid_decode_launch_count(hd_ctx *ctx, int64_t *launches);
 
-/* Profiling: when enabled, the split-K kernel of every decode_attn_full call
- * is bracketed by CUDA events on its stream.  hybrid_decode_profile
- * synchronises, returns the summed kernel time and launch count since the
- * last reset, and resets them. */
+/* Profiling: when enabled, every attention-kernel launch is bracketed by CUDA
+ * events on its stream (up to 4096 launches per layer type between reads).
+ * hybrid_decode_profile synchronises on them and returns, for layers of the
+ * given hd_layer_type, the summed kernel time and launch count since the last
+ * read, then resets that type's records. */
 hd_status hybrid_decode_set_profiling(hd_ctx *ctx, int32_t enable);
-hd_status hybrid_decode_profile(hd_ctx *ctx, double *total_ms, int64_t *launches);
+hd_status hybrid_decode_profile(hd_ctx *ctx, int32_t layer_type, double *total_ms, int64_t *launches);
 
 /* Full-layer attention that allocates nothing (no counterpart in the paper;
  * it exists for callers that cannot call cudaMalloc once running, such as a

@@ -48,6 +48,11 @@ WORKLOADS = {
     "block4_b16_c512_32768": dict(layer_types=[SLIDING, SLIDING, SLIDING, FULL], batch=16,
                                   num_q_heads=8, num_kv_heads=2, lengths=("uniform", 512, 32768),
                                   sink=("normal", 1.0, 0.0)),
+    # Four sliding layers at batch 64 (268 MB of ring caches): profiler captures of
+    # the sliding-layer kernel at the batch of the 28-layer step.
+    "sliding4_b64_c512_32768": dict(layer_types=[SLIDING] * 4, batch=64, num_q_heads=8,
+                                    num_kv_heads=2, lengths=("uniform", 512, 32768),
+                                    sink=("normal", 1.0, 0.0)),
     # Group 8: batch 256, 90% at 8192 and 10% (26 of 256) uniform in [1, 512];
     # sink N(0, variance 2) with a quarter of the heads at -inf.
     "step28_b256_g8_mixed": dict(layer_types=SPARK_LAYER_TYPES, batch=256, num_q_heads=16,
