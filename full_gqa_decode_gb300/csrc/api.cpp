@@ -9,7 +9,9 @@
 // per query head, NULL for no sink).
 #include <cudaTypedefs.h>
 
+#include <climits>
 #include <cmath>
+#include <cstdint>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -18,6 +20,24 @@
 #include "hd_internal.h"
 
 using namespace hd;
+
+// Chunk size: the smallest power of two (64 .. kChunkMax keys) that gives about
+// one wave of two resident CTAs per SM for the longest sequence bound.  Short
+// sliding layers get a few chunks per sequence; long full layers get long
+// chunks (fewer per-CTA ramps, measured faster than filling whole waves with
+// shorter ones); batch 1 gets many short chunks.  Chunks grow further if the
+// workspace bound requires it.
+void hd::plan_split(int64_t batch, int64_t num_kv_heads, int64_t max_keys, int64_t num_sms,
+                    int64_t max_slots, int32_t *chunk_keys, int32_t *num_chunks) {
+    const int64_t target = 2 * num_sms;
+    const int64_t want = (batch * num_kv_heads * max_keys + target - 1) / target;
+    int64_t t = kChunkMin;
+    while (t < want && t < kChunkMax) t *= 2;
+    auto chunks = [&](int64_t tt) { return max_keys > 0 ? (max_keys + tt - 1) / tt : 1; };
+    while (t < kChunkMax && batch * chunks(t) > max_slots) t *= 2;
+    *chunk_keys = (int32_t)t;
+    *num_chunks = (int32_t)chunks(t);
+}
 
 namespace {
 
@@ -140,25 +160,11 @@ hd_status check_call(const hd_ctx *ctx, int layer, int batch, const int32_t *con
 
 hd_status cuda_status(cudaError_t e) { return e == cudaSuccess ? HD_OK : HD_ERR_CUDA; }
 
-// Largest (sequence, chunk) product a call may need, over every batch size and
-// key bound: the chunk count is largest at the top of each chunk-size range.
-int64_t worst_part_slots(int max_batch, int num_kv_heads, int max_keys, int num_sms) {
-    int64_t worst = 0;
-    for (int b = 1; b <= max_batch; ++b) {
-        std::vector<int> probes{max_keys};
-        for (int t = kChunkMin; t < kChunkMax; t *= 2) {
-            // keys at which the plan leaves chunk size t: units * keys > t * target
-            const int64_t target = 2LL * num_sms;
-            const int64_t k = (int64_t)t * target / ((int64_t)b * num_kv_heads);
-            if (k < max_keys) probes.push_back((int)k);
-        }
-        for (int k : probes) {
-            int32_t ck = 0, nc = 0;
-            hd_plan_split(b, num_kv_heads, k < 1 ? 1 : k, num_sms, &ck, &nc);
-            if ((int64_t)b * nc > worst) worst = (int64_t)b * nc;
-        }
-    }
-    return worst;
+// Workspace bound in (sequence, chunk) pairs: the largest chunk always fits
+// (max_batch * ceil(max_keys / kChunkMax)); smaller chunks are allowed up to
+// about two waves of CTAs on top of that.
+int64_t part_slot_capacity(int max_batch, int max_keys, int num_sms) {
+    return (int64_t)max_batch * ((max_keys + kChunkMax - 1) / kChunkMax) + 4LL * num_sms;
 }
 
 hd_status build_table(DeviceTable *t, int rotary_dim, double theta, int max_context) {
@@ -215,8 +221,8 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     hd_status st = maps_for(ctx, L.layer, L.cache, L.batch, &km, &vm);
     if (st != HD_OK) return st;
     int32_t chunk_keys = 0, num_chunks = 0;
-    st = hd_plan_split(L.batch, ctx->cfg.num_kv_heads, L.max_keys, ctx->num_sms, &chunk_keys, &num_chunks);
-    if (st != HD_OK) return st;
+    plan_split(L.batch, ctx->cfg.num_kv_heads, L.max_keys, ctx->num_sms, ctx->part_slots, &chunk_keys,
+               &num_chunks);
     if ((int64_t)L.batch * num_chunks > ctx->part_slots) return HD_ERR_CAPACITY;
     // The combine keeps a weight per (head, chunk) plus a float4 row per head in the stage ring.
     if (((size_t)ctx->group * num_chunks + 3) * sizeof(float) + (size_t)ctx->group * 64 * 16 >
@@ -334,16 +340,7 @@ hd_status hd_plan_split(int32_t batch, int32_t num_kv_heads, int32_t max_keys, i
                         int32_t *chunk_keys, int32_t *num_chunks) {
     if (batch <= 0 || num_kv_heads <= 0 || max_keys < 0 || num_sms <= 0 || !chunk_keys || !num_chunks)
         return HD_ERR_INVALID_ARG;
-    // Aim at one wave of two resident CTAs per SM for the longest sequence
-    // bound, with chunks of 64..512 keys: short sliding layers get few, long
-    // chunks; long full layers get many 512-key chunks, which also balance
-    // ragged lengths across waves.
-    const int64_t target = 2LL * num_sms;
-    const int64_t want = ((int64_t)batch * num_kv_heads * max_keys + target - 1) / target;
-    int t = kChunkMin;
-    while (t < want && t < kChunkMax) t *= 2;
-    *chunk_keys = t;
-    *num_chunks = max_keys > 0 ? (int32_t)((max_keys + t - 1) / t) : 1;
+    plan_split(batch, num_kv_heads, max_keys, num_sms, INT64_MAX, chunk_keys, num_chunks);
     return HD_OK;
 }
 
@@ -385,10 +382,9 @@ hd_status hybrid_decode_init(const hd_config *cfg, hd_ctx **out_ctx) {
     }
     const int Hq = cfg->num_q_heads, Hkv = cfg->num_kv_heads, B = cfg->max_batch;
     int64_t slots = 0;
-    if (any_full)
-        slots = worst_part_slots(B, Hkv, cfg->max_context + 1, ctx->num_sms);
+    if (any_full) slots = part_slot_capacity(B, cfg->max_context + 1, ctx->num_sms);
     if (any_sliding) {
-        const int64_t s = worst_part_slots(B, Hkv, cfg->sliding_window, ctx->num_sms);
+        const int64_t s = part_slot_capacity(B, cfg->sliding_window, ctx->num_sms);
         if (s > slots) slots = s;
     }
     ctx->part_slots = slots;

@@ -22,7 +22,12 @@ constexpr int kBoxesPerRow = kHeadDim / kBoxCols;                 // 4
 constexpr int kBoxBytes = kStageKeys * 128;                       // 4 KiB
 constexpr int kStageBytes = 2 * kBoxesPerRow * kBoxBytes;         // K + V: 32 KiB
 constexpr int kChunkMin = 64;
-constexpr int kChunkMax = 512;
+constexpr int kChunkMax = 2048;
+
+// Split plan: keys per chunk (a power of two from kChunkMin to kChunkMax) and
+// chunks per sequence for `max_keys` keys, keeping batch * chunks <= max_slots.
+void plan_split(int64_t batch, int64_t num_kv_heads, int64_t max_keys, int64_t num_sms,
+                int64_t max_slots, int32_t *chunk_keys, int32_t *num_chunks);
 
 // Which cache rows the split pass scores for sequence b with c = context[b].
 enum KeySet : int32_t {

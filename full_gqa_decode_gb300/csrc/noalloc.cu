@@ -108,8 +108,11 @@ extern "C" hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_
         cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         return HD_ERR_STATE;
     int32_t chunk_keys = 0, num_chunks = 0;
-    hd_status st = hd_plan_split(batch, num_kv_heads, max_context + 1, num_sms, &chunk_keys, &num_chunks);
-    if (st != HD_OK) return st;
+    hd_status st = HD_OK;
+    // Chunks no larger in number than the array can hold at the largest chunk size.
+    const int64_t per_slot = (int64_t)num_q_heads * (hd::kHeadDim * sizeof(float) + sizeof(float2));
+    hd::plan_split(batch, num_kv_heads, max_context + 1, num_sms, (int64_t)(kScratchBytes / 2) / per_slot,
+                   &chunk_keys, &num_chunks);
 
     // Scratch layout and the size limit: calls needing more than the array are refused.
     const size_t slots = (size_t)batch * num_q_heads * num_chunks;

@@ -133,8 +133,10 @@ typedef struct {
 hd_status hd_validate_config(const hd_config *cfg);
 
 /* Split-K plan used for a layer call (pure host function, no device use):
- * keys per chunk and the number of chunks (the grid's key dimension) for
- * `batch` sequences of at most `max_keys` scored cache keys on `num_sms` SMs. */
+ * keys per chunk (a power of two from 64 to 2048) and the number of chunks
+ * (the grid's key dimension) for `batch` sequences of at most `max_keys`
+ * scored cache keys on `num_sms` SMs.  A call on a context uses the same
+ * model, bounded by the context's workspace. */
 hd_status hd_plan_split(int32_t batch, int32_t num_kv_heads, int32_t max_keys, int32_t num_sms,
                         int32_t *chunk_keys, int32_t *num_chunks);
 
@@ -217,7 +219,7 @@ hd_status hybrid_decode_profile(hd_ctx *ctx, int32_t layer_type, double *total_m
  *   max_context  upper bound on every context[b] of this call; max_context+1
  *                <= cache.capacity.
  * Returns HD_ERR_CAPACITY when the call's scratch (about batch * num_q_heads *
- * chunks * 1032 bytes, chunks = ceil((max_context+1)/chunk) with chunk <= 512)
+ * chunks * 1032 bytes, chunks = ceil((max_context+1)/chunk) with chunk <= 2048)
  * would exceed 64 MiB.  All calls share the array and it keeps the last
  * call's contents (the tickets are cleared at every call), so calls that
  * overlap on the GPU race: order them on one stream.  The first call on a
