@@ -24,6 +24,7 @@ LIBRARY = os.path.join(PKG, "libhybriddecode.so")
 HD_SLIDING, HD_FULL = 0, 1
 HD_LAYOUT_AUTO, HD_LAYOUT_RING, HD_LAYOUT_ROLL = 0, 1, 2
 HD_CONSUMER_CUDA_CORE, HD_CONSUMER_TENSOR_CORE = 0, 1
+HD_PROFILE_SLIDING, HD_PROFILE_FULL = 1 << HD_SLIDING, 1 << HD_FULL
 STATUS = {0: "HD_OK", 1: "HD_ERR_INVALID_ARG", 2: "HD_ERR_UNSUPPORTED", 3: "HD_ERR_CAPACITY",
           4: "HD_ERR_CUDA", 5: "HD_ERR_STATE"}
 DEVERR = {1: "HD_DEVERR_CONTEXT_NEGATIVE", 2: "HD_DEVERR_CONTEXT_CAPACITY",
@@ -265,8 +266,9 @@ def hybrid_decode_launch_count(ctx: Context) -> int:
     return n.value
 
 
-def hybrid_decode_set_profiling(ctx: Context, enable: bool) -> None:
-    _check(_lib.hybrid_decode_set_profiling(ctx.handle, int(enable)), "hybrid_decode_set_profiling")
+def hybrid_decode_set_profiling(ctx: Context, mask: int) -> None:
+    """mask of layer types to bracket with events: HD_PROFILE_SLIDING | HD_PROFILE_FULL, or 0."""
+    _check(_lib.hybrid_decode_set_profiling(ctx.handle, int(mask)), "hybrid_decode_set_profiling")
 
 
 def hybrid_decode_profile(ctx: Context, layer_type: int = HD_FULL) -> tuple[float, int]:

@@ -22,21 +22,32 @@
 using namespace hd;
 
 // Chunk size: the smallest power of two (64 .. kChunkMax keys) that gives about
-// one wave of two resident CTAs per SM for the longest sequence bound.  Short
-// sliding layers get a few chunks per sequence; long full layers get long
-// chunks (fewer per-CTA ramps, measured faster than filling whole waves with
-// shorter ones); batch 1 gets many short chunks.  Chunks grow further if the
-// workspace bound requires it.
+// one CTA per SM over the grid for the longest sequence bound.  If that grid
+// fits in one CTA per SM, it runs so, with the deep ring (one CTA streams as
+// much as two); otherwise the plan aims at two resident CTAs per SM with the
+// default ring.  Short sliding layers get one or a few chunks per sequence;
+// long full layers get long chunks (fewer per-CTA ramps, measured faster than
+// filling whole waves with shorter ones); batch 1 gets many short chunks.
+// Chunks grow further if the workspace bound requires it.
 void hd::plan_split(int64_t batch, int64_t num_kv_heads, int64_t max_keys, int64_t num_sms,
-                    int64_t max_slots, int32_t *chunk_keys, int32_t *num_chunks) {
-    const int64_t target = 2 * num_sms;
-    const int64_t want = (batch * num_kv_heads * max_keys + target - 1) / target;
-    int64_t t = kChunkMin;
-    while (t < want && t < kChunkMax) t *= 2;
+                    int64_t max_slots, int32_t *chunk_keys, int32_t *num_chunks, int32_t *stages) {
     auto chunks = [&](int64_t tt) { return max_keys > 0 ? (max_keys + tt - 1) / tt : 1; };
-    while (t < kChunkMax && batch * chunks(t) > max_slots) t *= 2;
+    auto pick = [&](int64_t target) {
+        const int64_t want = (batch * num_kv_heads * max_keys + target - 1) / target;
+        int64_t t = kChunkMin;
+        while (t < want && t < kChunkMax) t *= 2;
+        while (t < kChunkMax && batch * chunks(t) > max_slots) t *= 2;
+        return t;
+    };
+    int64_t t = pick(num_sms);
+    int32_t st = kDeepStages;
+    if (batch * num_kv_heads * chunks(t) > num_sms) {
+        t = pick(2 * num_sms);
+        st = kStages;
+    }
     *chunk_keys = (int32_t)t;
     *num_chunks = (int32_t)chunks(t);
+    if (stages) *stages = st;
 }
 
 namespace {
@@ -73,7 +84,7 @@ struct hd_ctx {
     int consumer = CONSUMER_MMA;
     int64_t launches = 0;
     std::vector<MapCacheEntry> maps;     // one per layer
-    bool profiling = false;
+    int32_t profile_mask = 0;           // bit (1 << layer type): bracket that type's launches
     std::vector<cudaEvent_t> ev_begin, ev_end;  // [2][kProfileEvents]: per layer type
     size_t ev_used[2] = {0, 0};
 };
@@ -220,9 +231,9 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     const CUtensorMap *km = nullptr, *vm = nullptr;
     hd_status st = maps_for(ctx, L.layer, L.cache, L.batch, &km, &vm);
     if (st != HD_OK) return st;
-    int32_t chunk_keys = 0, num_chunks = 0;
+    int32_t chunk_keys = 0, num_chunks = 0, stages = kStages;
     plan_split(L.batch, ctx->cfg.num_kv_heads, L.max_keys, ctx->num_sms, ctx->part_slots, &chunk_keys,
-               &num_chunks);
+               &num_chunks, &stages);
     if ((int64_t)L.batch * num_chunks > ctx->part_slots) return HD_ERR_CAPACITY;
     // The combine keeps a weight per (head, chunk) plus a float4 row per head in the stage ring.
     if (((size_t)ctx->group * num_chunks + 3) * sizeof(float) + (size_t)ctx->group * 64 * 16 >
@@ -262,9 +273,9 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
 
     const int type = sliding ? HD_SLIDING : HD_FULL;
     const size_t slot = (size_t)type * kProfileEvents + ctx->ev_used[type];
-    const bool timed = ctx->profiling && ctx->ev_used[type] < (size_t)kProfileEvents;
+    const bool timed = (ctx->profile_mask & (1 << type)) && ctx->ev_used[type] < (size_t)kProfileEvents;
     if (timed && cudaEventRecord(ctx->ev_begin[slot], stream) != cudaSuccess) return HD_ERR_CUDA;
-    st = cuda_status(launch_layer(km, vm, a, L.batch, ctx->group, ctx->consumer, stream));
+    st = cuda_status(launch_layer(km, vm, a, L.batch, ctx->group, ctx->consumer, stages, stream));
     if (st != HD_OK) return st;
     ++ctx->launches;
     if (timed) {
@@ -604,7 +615,7 @@ hd_status hybrid_decode_launch_count(hd_ctx *ctx, int64_t *launches) {
 }
 
 hd_status hybrid_decode_set_profiling(hd_ctx *ctx, int32_t enable) {
-    if (!ctx) return HD_ERR_INVALID_ARG;
+    if (!ctx || enable < 0 || enable > 3) return HD_ERR_INVALID_ARG;
     if (enable && ctx->ev_begin.empty()) {
         ctx->ev_begin.resize(2 * kProfileEvents);
         ctx->ev_end.resize(2 * kProfileEvents);
@@ -613,7 +624,7 @@ hd_status hybrid_decode_set_profiling(hd_ctx *ctx, int32_t enable) {
                 cudaEventCreate(&ctx->ev_end[i]) != cudaSuccess)
                 return HD_ERR_CUDA;
     }
-    ctx->profiling = enable != 0;
+    ctx->profile_mask = enable;
     ctx->ev_used[0] = ctx->ev_used[1] = 0;
     return HD_OK;
 }

@@ -101,6 +101,11 @@ __device__ __forceinline__ float fast_exp2(float x) {
     asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+__device__ __forceinline__ float fast_log2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
                                         uint32_t &r3) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -155,6 +160,27 @@ __device__ __forceinline__ float f64_to_bf16_value(double x) {
     float t = __double2float_rz(x);
     if ((double)t != x && isfinite(t)) t = __uint_as_float(__float_as_uint(t) | 1u);
     return __bfloat162float(__float2bfloat16_rn(t));
+}
+
+// Loads what the combine needs from global memory: the new entry (raw k for
+// NEW_ROTATE, the staged key otherwise), its value row, the rotary row at
+// position c, and the group's sink values.
+// Threads [0, nthreads) share the work.
+template <int G>
+__device__ __forceinline__ void load_combine_inputs(const LayerArgs &a, int b, int kvh, int c, float *kraw_s,
+                                                    float *vnew_s, float2 *tab_s, float *sink_s, int nthreads) {
+    const int t = threadIdx.x;
+    if (a.new_kind != NEW_NONE) {
+        const size_t e = ((size_t)b * a.num_kv_heads + kvh) * kHeadDim;
+        for (int d = t; d < kHeadDim; d += nthreads) {
+            kraw_s[d] = __bfloat162float(a.new_k[e + d]);
+            vnew_s[d] = __bfloat162float(a.new_v[e + d]);
+        }
+        if (a.new_kind == NEW_ROTATE)
+            for (int j = t; j < (a.rotary_dim >> 1); j += nthreads)
+                tab_s[j] = a.table[(size_t)c * (a.rotary_dim >> 1) + j];
+    }
+    if (t < G) sink_s[t] = a.sink ? a.sink[kvh * G + t] : 0.f;
 }
 
 // Scored cache keys of sequence context c, or -1 (and the error bit) when c
@@ -389,22 +415,22 @@ struct MmaConsumer {
 
 // ------------------------------------------------------------- the kernel --
 
-template <int G, int CONSUMER>
-__global__ void __launch_bounds__(kThreads, 2)
+template <int G, int CONSUMER, int S>
+__global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
     attn_layer_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const LayerArgs a) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float *q_s = reinterpret_cast<float *>(smem + kStages * kStageBytes);    // [G][256]
+    float *q_s = reinterpret_cast<float *>(smem + S * kStageBytes);          // [G][256]
     float *knew_s = q_s + G * kHeadDim;                                        // [256]
     float *vnew_s = knew_s + kHeadDim;                                         // [256]
     float *kraw_s = vnew_s + kHeadDim;                                         // [256]
     float2 *tab_s = reinterpret_cast<float2 *>(kraw_s + kHeadDim);             // [128]
     float *misc = reinterpret_cast<float *>(tab_s + kHeadDim / 2);             // [32]
     uint64_t *full = reinterpret_cast<uint64_t *>(misc + 32);
-    uint64_t *empty = full + kStages;
-    int *flag_s = reinterpret_cast<int *>(empty + kStages);
+    uint64_t *empty = full + S;
+    int *flag_s = reinterpret_cast<int *>(empty + S);
 
     const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -434,7 +460,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int nst = end > start ? (end - start + kStageKeys - 1) / kStageKeys : 0;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
         }
@@ -459,8 +485,10 @@ __global__ void __launch_bounds__(kThreads, 2)
         }
         q_s[i] = x * kQScale;
     }
-    // Inputs of the combine (new entry, its rotary row, the sink), fetched with q
-    // so the CTA that ends up combining does not wait on global loads later.
+    // A sequence with a single chunk is combined by this CTA: fetch the
+    // combine's inputs now, in the same round as q.
+    const bool has_new = a.new_kind != NEW_NONE;
+    if (nchunks == 1) load_combine_inputs<G>(a, b, kvh, c, kraw_s, vnew_s, tab_s, misc + 2 * kMaxGroup, kThreads);
     __syncthreads();
 
     float *red_o = reinterpret_cast<float *>(smem);             // reuses the stage ring
@@ -469,8 +497,8 @@ __global__ void __launch_bounds__(kThreads, 2)
     if (warp == kConsumerWarps) {
         if (lane == 0) {  // producer: one lane issues every load of the chunk
             for (int s = 0; s < nst; ++s) {
-                const int slot = s % kStages;
-                if (s >= kStages && !mbar_wait(&empty[slot], ((s / kStages) - 1) & 1)) {
+                const int slot = s % S;
+                if (s >= S && !mbar_wait(&empty[slot], ((s / S) - 1) & 1)) {
                     atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
@@ -492,8 +520,8 @@ __global__ void __launch_bounds__(kThreads, 2)
         typename std::conditional<CONSUMER == CONSUMER_MMA, MmaConsumer<G>, FmaConsumer<G>>::type cons;
         cons.init(q_s, lane);
         for (int s = 0; s < nst; ++s) {
-            const int slot = s % kStages;
-            if (!mbar_wait(&full[slot], (s / kStages) & 1)) {
+            const int slot = s % S;
+            if (!mbar_wait(&full[slot], (s / S) & 1)) {
                 if (lane == 0) atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
                 break;
             }
@@ -553,17 +581,26 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 
     // ---- combine (one CTA per sequence and kv head) ----
-    const bool has_new = a.new_kind != NEW_NONE;
-    if (has_new) {
-        const size_t e = ((size_t)b * a.num_kv_heads + kvh) * kHeadDim;
-        for (int d = threadIdx.x; d < kHeadDim; d += blockDim.x) {
-            kraw_s[d] = __bfloat162float(a.new_k[e + d]);
-            vnew_s[d] = __bfloat162float(a.new_v[e + d]);
+    // Every global input of the combine is requested in one round: the new
+    // entry, its rotary row and the sink (unless the prologue fetched them),
+    // and each warp's chunk maxima and sums.
+    float *sink_s = misc + 2 * kMaxGroup;           // [G]
+    if (nchunks > 1) load_combine_inputs<G>(a, b, kvh, c, kraw_s, vnew_s, tab_s, sink_s, kThreads);
+    const float2 *pml = reinterpret_cast<const float2 *>(a.part_ml);
+    constexpr int kPerLane = 4;
+    float2 ml[kPerLane];
+    {
+        const int h = warp < G ? warp : 0;
+        const size_t ph = pbase + (size_t)h * a.max_chunks;
+#pragma unroll
+        for (int r = 0; r < kPerLane; ++r) {
+            const int j = lane + 32 * r;
+            ml[r] = make_float2(-INFINITY, 0.f);
+            if (j < nchunks) ml[r] = nchunks == 1 ? own_ml[h] : __ldcg(pml + ph + j);
         }
-        if (a.new_kind == NEW_ROTATE)
-            for (int j = threadIdx.x; j < (a.rotary_dim >> 1); j += blockDim.x)
-                tab_s[j] = a.table[(size_t)c * (a.rotary_dim >> 1) + j];
-        __syncthreads();
+    }
+    __syncthreads();
+    if (has_new) {
         for (int d = threadIdx.x; d < kHeadDim; d += blockDim.x) {
             float kn;
             if (a.new_kind == NEW_STAGED || d >= a.rotary_dim) {
@@ -583,9 +620,16 @@ __global__ void __launch_bounds__(kThreads, 2)
     float *wts = reinterpret_cast<float *>(smem);   // [G][nchunks] (the warp buffers are free)
     float *head_s = misc;                           // [G] scale = sink factor / L
     float *wnew_s = misc + kMaxGroup;               // [G] weight of the new entry
-    const float2 *pml = reinterpret_cast<const float2 *>(a.part_ml);
     for (int h = warp; h < G; h += kThreads / 32) {
         const size_t ph = pbase + (size_t)h * a.max_chunks;
+        if (h != warp) {  // a second head for this warp: its pairs were not preloaded
+#pragma unroll
+            for (int r = 0; r < kPerLane; ++r) {
+                const int j = lane + 32 * r;
+                ml[r] = make_float2(-INFINITY, 0.f);
+                if (j < nchunks) ml[r] = nchunks == 1 ? own_ml[h] : __ldcg(pml + ph + j);
+            }
+        }
         float s_new = -INFINITY;
         if (has_new) {
             float t = 0.f;
@@ -594,17 +638,9 @@ __global__ void __launch_bounds__(kThreads, 2)
             for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
             s_new = t;
         }
-        // Chunk (m, l) pairs: lane j holds chunks j, j+32, ... (one load each).
-        constexpr int kPerLane = 4;
-        float2 ml[kPerLane];
         float M = s_new;
 #pragma unroll
-        for (int r = 0; r < kPerLane; ++r) {
-            const int j = lane + 32 * r;
-            ml[r] = make_float2(-INFINITY, 0.f);
-            if (j < nchunks) ml[r] = nchunks == 1 ? own_ml[h] : __ldcg(pml + ph + j);
-            M = fmaxf(M, ml[r].x);
-        }
+        for (int r = 0; r < kPerLane; ++r) M = fmaxf(M, ml[r].x);
         for (int j = lane + 32 * kPerLane; j < nchunks; j += 32) M = fmaxf(M, __ldcg(pml + ph + j).x);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
@@ -613,25 +649,26 @@ __global__ void __launch_bounds__(kThreads, 2)
         for (int r = 0; r < kPerLane; ++r) {
             const int j = lane + 32 * r;
             if (j < nchunks) {
-                const float w = (ml[r].x == -INFINITY) ? 0.f : exp2f(ml[r].x - M);
+                const float w = (ml[r].x == -INFINITY) ? 0.f : fast_exp2(ml[r].x - M);
                 wts[h * nchunks + j] = w;
                 L = fmaf(w, ml[r].y, L);
             }
         }
         for (int j = lane + 32 * kPerLane; j < nchunks; j += 32) {
             const float2 m2 = __ldcg(pml + ph + j);
-            const float w = (m2.x == -INFINITY) ? 0.f : exp2f(m2.x - M);
+            const float w = (m2.x == -INFINITY) ? 0.f : fast_exp2(m2.x - M);
             wts[h * nchunks + j] = w;
             L = fmaf(w, m2.y, L);
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-        const float w_new = has_new ? exp2f(s_new - M) : 0.f;
+        const float w_new = has_new ? fast_exp2(s_new - M) : 0.f;
         L += w_new;
         if (lane == 0) {
             const int hg = kvh * G + h;
-            const float lse = (M + log2f(L)) * kLn2;
-            const float f = a.sink ? 1.f / (1.f + expf(a.sink[hg] - lse)) : 1.f;
+            const float lse = (M + fast_log2(L)) * kLn2;
+            // exp(lse) / (exp(lse) + exp(sink)) = 1 / (1 + 2^((sink - lse) * log2 e))
+            const float f = a.sink ? 1.f / (1.f + fast_exp2((sink_s[h] - lse) * kLog2e)) : 1.f;
             head_s[h] = f / L;
             wnew_s[h] = w_new;
             a.lse[(size_t)b * a.num_q_heads + hg] = lse;
@@ -702,13 +739,13 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
 }
 
-template <int G, int CONSUMER>
+template <int G, int CONSUMER, int S>
 cudaError_t launch_g(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
                      cudaStream_t s) {
     static bool configured = false;
-    const size_t smem = layer_smem_bytes(G);
+    const size_t smem = layer_smem_bytes(G, S);
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER>,
+        cudaError_t e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER, S>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = true;
@@ -723,32 +760,35 @@ cudaError_t launch_g(const CUtensorMap *km, const CUtensorMap *vm, const LayerAr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_layer_kernel<G, CONSUMER>, *km, *vm, a);
+    return cudaLaunchKernelEx(&cfg, attn_layer_kernel<G, CONSUMER, S>, *km, *vm, a);
 }
 
-template <int CONSUMER>
+template <int CONSUMER, int S>
 cudaError_t launch_c(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
                      int group, cudaStream_t s) {
     switch (group) {
-    case 1: return launch_g<1, CONSUMER>(km, vm, a, batch, s);
-    case 2: return launch_g<2, CONSUMER>(km, vm, a, batch, s);
-    case 4: return launch_g<4, CONSUMER>(km, vm, a, batch, s);
-    case 8: return launch_g<8, CONSUMER>(km, vm, a, batch, s);
+    case 1: return launch_g<1, CONSUMER, S>(km, vm, a, batch, s);
+    case 2: return launch_g<2, CONSUMER, S>(km, vm, a, batch, s);
+    case 4: return launch_g<4, CONSUMER, S>(km, vm, a, batch, s);
+    case 8: return launch_g<8, CONSUMER, S>(km, vm, a, batch, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-size_t layer_smem_bytes(int group) {
-    return 1024 + kStages * kStageBytes + ((size_t)group * kHeadDim + 4 * kHeadDim + 32) * sizeof(float) +
-           2 * kStages * sizeof(uint64_t) + 16;
+size_t layer_smem_bytes(int group, int stages) {
+    return 1024 + (size_t)stages * kStageBytes + ((size_t)group * kHeadDim + 4 * kHeadDim + 32) * sizeof(float) +
+           2 * (size_t)stages * sizeof(uint64_t) + 16;
 }
 
 cudaError_t launch_layer(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
-                         int group, int consumer, cudaStream_t s) {
-    return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA>(km, vm, a, batch, group, s)
-                                    : launch_c<CONSUMER_FMA>(km, vm, a, batch, group, s);
+                         int group, int consumer, int stages, cudaStream_t s) {
+    if (stages == kDeepStages)
+        return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA, kDeepStages>(km, vm, a, batch, group, s)
+                                        : launch_c<CONSUMER_FMA, kDeepStages>(km, vm, a, batch, group, s);
+    return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA, kStages>(km, vm, a, batch, group, s)
+                                    : launch_c<CONSUMER_FMA, kStages>(km, vm, a, batch, group, s);
 }
 
 }  // namespace hd

@@ -16,7 +16,8 @@ namespace hd {
 constexpr int kHeadDim = 256;     // head_dim this build implements
 constexpr int kMaxGroup = 8;      // query heads per kv head
 constexpr int kStageKeys = 32;    // keys per pipeline stage (rows of one TMA box)
-constexpr int kStages = 3;        // stages in flight per CTA
+constexpr int kStages = 3;        // stages per CTA with two CTAs per SM (the default)
+constexpr int kDeepStages = 6;    // stages per CTA with one CTA per SM (grids of at most one CTA per SM)
 constexpr int kBoxCols = 64;      // bf16 columns per 128-byte swizzled box row
 constexpr int kBoxesPerRow = kHeadDim / kBoxCols;                 // 4
 constexpr int kBoxBytes = kStageKeys * 128;                       // 4 KiB
@@ -27,7 +28,7 @@ constexpr int kChunkMax = 2048;
 // Split plan: keys per chunk (a power of two from kChunkMin to kChunkMax) and
 // chunks per sequence for `max_keys` keys, keeping batch * chunks <= max_slots.
 void plan_split(int64_t batch, int64_t num_kv_heads, int64_t max_keys, int64_t num_sms,
-                int64_t max_slots, int32_t *chunk_keys, int32_t *num_chunks);
+                int64_t max_slots, int32_t *chunk_keys, int32_t *num_chunks, int32_t *stages = nullptr);
 
 // Which cache rows the split pass scores for sequence b with c = context[b].
 enum KeySet : int32_t {
@@ -93,7 +94,7 @@ struct RopeArgs {
 cudaError_t launch_rope_append(const RopeArgs &a, int batch, cudaStream_t s);
 cudaError_t launch_roll_window(const RopeArgs &a, int batch, cudaStream_t s);
 cudaError_t launch_layer(const CUtensorMap *kmap, const CUtensorMap *vmap, const LayerArgs &a,
-                         int batch, int group, int consumer, cudaStream_t s);
-size_t layer_smem_bytes(int group);
+                         int batch, int group, int consumer, int stages, cudaStream_t s);
+size_t layer_smem_bytes(int group, int stages);
 
 }  // namespace hd

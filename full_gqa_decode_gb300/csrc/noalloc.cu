@@ -111,8 +111,9 @@ extern "C" hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_
     hd_status st = HD_OK;
     // Chunks no larger in number than the array can hold at the largest chunk size.
     const int64_t per_slot = (int64_t)num_q_heads * (hd::kHeadDim * sizeof(float) + sizeof(float2));
+    int32_t stages = hd::kStages;
     hd::plan_split(batch, num_kv_heads, max_context + 1, num_sms, (int64_t)(kScratchBytes / 2) / per_slot,
-                   &chunk_keys, &num_chunks);
+                   &chunk_keys, &num_chunks, &stages);
 
     // Scratch layout and the size limit: calls needing more than the array are refused.
     const size_t slots = (size_t)batch * num_q_heads * num_chunks;
@@ -158,6 +159,7 @@ extern "C" hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_
     a.max_chunks = num_chunks;
     a.window = 0;
     a.max_context = max_context;
-    return hd::launch_layer(&kmap, &vmap, a, batch, group, hd::CONSUMER_MMA, s) == cudaSuccess ? HD_OK
-                                                                                            : HD_ERR_CUDA;
+    return hd::launch_layer(&kmap, &vmap, a, batch, group, hd::CONSUMER_MMA, stages, s) == cudaSuccess
+               ? HD_OK
+               : HD_ERR_CUDA;
 }

@@ -199,11 +199,15 @@ hd_status hybrid_decode_device_errors(hd_ctx *ctx, int32_t *flags, void *stream)
 /* Kernel launches issued by this context since init (host counter). */
 hd_status hybrid_decode_launch_count(hd_ctx *ctx, int64_t *launches);
 
-/* Profiling: when enabled, every attention-kernel launch is bracketed by CUDA
- * events on its stream (up to 4096 launches per layer type between reads).
- * hybrid_decode_profile synchronises on them and returns, for layers of the
- * given hd_layer_type, the summed kernel time and launch count since the last
- * read, then resets that type's records. */
+/* Profiling: `enable` is a mask of layer types, bit (1 << hd_layer_type):
+ * HD_PROFILE_SLIDING, HD_PROFILE_FULL, both, or 0 (off).  Attention-kernel
+ * launches of the selected types are bracketed by CUDA events on their stream
+ * (up to 4096 launches per type between reads); an event between two launches
+ * serialises them, so the unselected types keep overlapping launch latency.
+ * hybrid_decode_profile synchronises on the events and returns, for layers of
+ * the given hd_layer_type, the summed kernel time and launch count since the
+ * last read, then resets that type's records. */
+enum { HD_PROFILE_SLIDING = 1 << HD_SLIDING, HD_PROFILE_FULL = 1 << HD_FULL };
 hd_status hybrid_decode_set_profiling(hd_ctx *ctx, int32_t enable);
 hd_status hybrid_decode_profile(hd_ctx *ctx, int32_t layer_type, double *total_ms, int64_t *launches);
 

@@ -78,5 +78,5 @@ def test_plan_split_long_context_uses_many_chunks(hd):
 def test_plan_split_shapes(hd):
     assert hd.hd_plan_split(4, 2, 131073, 152) == (2048, 65)   # long context: >= 64 chunks
     assert hd.hd_plan_split(64, 2, 32769, 152) == (2048, 17)   # batch-64 full layers
-    assert hd.hd_plan_split(64, 2, 511, 152) == (256, 2)       # batch-64 ring layers
+    assert hd.hd_plan_split(64, 2, 511, 152) == (512, 1)       # batch-64 ring layers: one chunk
     assert hd.hd_plan_split(1, 2, 4097, 152) == (64, 65)       # batch 1: many short chunks
