@@ -60,6 +60,24 @@ def step_bytes(types, context, num_kv_heads, layout) -> int:
     return int(sum(scored_keys(t, context, layout).sum() for t in types) * num_kv_heads * KV_ROW_BYTES)
 
 
+def describe_layers(types) -> str:
+    n_full = sum(1 for t in types if t == synth.FULL)
+    if list(types) == synth.SPARK_LAYER_TYPES:
+        return f"{len(types)} = [sliding x3, full] x7"
+    return f"{len(types)} ({len(types) - n_full} sliding, {n_full} full)"
+
+
+def describe_lengths(recipe) -> str:
+    kind = recipe[0]
+    if kind == "fixed":
+        return f"{recipe[1]} for every sequence"
+    if kind == "uniform":
+        return f"uniform [{recipe[1]}, {recipe[2]}] per sequence"
+    if kind == "mixed":
+        return f"{recipe[1]}, with {recipe[2]:.0%} of sequences uniform in [1, {recipe[3]}]"
+    return str(recipe)
+
+
 def measured_peaks() -> dict:
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -261,7 +279,7 @@ def time_steps(run, steps: int, warmup: int, world: int, device) -> float:
 
 # ------------------------------------------------------------- CPU baseline --
 
-def oracle_sample(layer_caches, context, types, Hq, Hkv, sink, rng, threads):
+def oracle_sample(layer_caches, context, types, Hq, Hkv, sink, rng, threads, layout=synth.LAYOUT_RING):
     """Times the oracle on one [S,S,S,F] block of the step for the given sequences.
     layer_caches: per layer (kc, vc) uint16 arrays [B, Hkv, cap, D]. Returns (seconds, bytes)."""
     import oracle
@@ -276,11 +294,11 @@ def oracle_sample(layer_caches, context, types, Hq, Hkv, sink, rng, threads):
             q = synth.bits(synth.normal_bf16(rng, (1, Hq, D)))
             k = synth.bits(synth.normal_bf16(rng, (1, Hkv, D)))
             v = synth.bits(synth.normal_bf16(rng, (1, Hkv, D)))
-            jobs.append(dict(layer_type=t, layout=synth.LAYOUT_RING, window=synth.WINDOW, rotary_dim=rot,
+            jobs.append(dict(layer_type=t, layout=layout, window=synth.WINDOW, rotary_dim=rot,
                              rope_theta=theta, context=context[b:b + 1], q=q, k=k, v=v,
                              kcache=np.ascontiguousarray(kc[b:b + 1]), vcache=np.ascontiguousarray(vc[b:b + 1]),
                              sink=sink))
-    nbytes = step_bytes(types, context, Hkv, synth.LAYOUT_RING)
+    nbytes = step_bytes(types, context, Hkv, layout)
     t0 = time.perf_counter()
     with cf.ThreadPoolExecutor(threads) as ex:   # ctypes releases the GIL in the oracle
         list(ex.map(lambda j: orc.decode_layer(**j), jobs))
@@ -357,7 +375,8 @@ def run_ours(args, world, rank, local) -> int:
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     peaks = measured_peaks()
-    wl = Workload(args.workload, device, seed=rank)
+    layout = synth.LAYOUT_ROLL if args.layout == "roll" else synth.LAYOUT_RING
+    wl = Workload(args.workload, device, seed=rank, layout=layout)
     consumer = hd.HD_CONSUMER_TENSOR_CORE if args.consumer == "tensor-core" else hd.HD_CONSUMER_CUDA_CORE
     hd.hybrid_decode_set_consumer(wl.ctx, consumer)
     torch.cuda.synchronize()
@@ -403,6 +422,11 @@ def run_ours(args, world, rank, local) -> int:
             "frac": round(wl.sliding_layer_bytes / (avg_slide * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
             "algorithmic_bytes_per_launch": wl.sliding_layer_bytes, "avg_launch_ms": round(avg_slide, 4)}
 
+    read_peak = read_stream_probe(device)
+    if read_peak and achieved:
+        roofline["read_stream_probe_gbs"] = round(read_peak, 1)
+        roofline["frac_of_read_stream"] = round(achieved / read_peak, 4)
+
     # end to end: host buffers, copies inside the timed region
     e2e = e2e_measure(wl, args, world, device)
 
@@ -416,9 +440,10 @@ def run_ours(args, world, rank, local) -> int:
                   "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
                   "frac_of_peak_hbm": round(gbs / peaks["hbm_gbs"], 4),
                   "config": {"workload": wl.name, "global_batch": wl.B * world, "per_gpu_batch": wl.B,
-                             "layers": "28 = [sliding x3, full] x7", "heads": f"{wl.Hq} q / {wl.Hkv} kv",
-                             "head_dim": synth.HEAD_DIM, "contexts": "uniform [512, 32768] per sequence",
+                             "layers": describe_layers(wl.types), "heads": f"{wl.Hq} q / {wl.Hkv} kv",
+                             "head_dim": synth.HEAD_DIM, "contexts": describe_lengths(wl.spec["lengths"]),
                              "max_context": wl.max_ctx, "kv_bytes_per_step": wl.bytes,
+                             "sliding_layout": args.layout,
                              "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world}"},
                   "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                   "gpu_launches": int(n1 - n0), "clocks": clk}
@@ -426,6 +451,30 @@ def run_ours(args, world, rank, local) -> int:
             result["secondary"] = secondary
         print(json.dumps(result), flush=True)
     return 0
+
+
+def read_stream_probe(device, gib: int = 4):
+    """GB/s of a pure TMA read stream over a fresh buffer (the library's probe),
+    median of 5 passes after 2 warm-up passes; None if memory is short."""
+    import torch
+    import full_gqa_decode_gb300 as hd
+    try:
+        buf = torch.empty(gib << 30, dtype=torch.uint8, device=device)
+    except torch.OutOfMemoryError:
+        return None
+    buf.fill_(1)
+    for _ in range(2):
+        hd.hybrid_decode_read_probe(buf)
+    times, nbytes = [], 0
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        nbytes = hd.hybrid_decode_read_probe(buf)
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    del buf
+    return nbytes / (statistics.median(times) * 1e-3) / 1e9
 
 
 def e2e_measure(wl, args, world, device) -> dict:
@@ -466,8 +515,9 @@ def cpu_baseline(wl, device) -> dict:
         caches.append((synth.bits(l["kc"]), synth.bits(l["vc"])))
     sink = None if wl.sink is None else wl.sink.cpu().numpy()
     threads = cpu_threads()
+    layout = synth.LAYOUT_ROLL if wl.layout == synth.LAYOUT_ROLL else synth.LAYOUT_RING
     secs, nbytes = oracle_sample(caches, wl.context, [wl.types[i] for i in block], wl.Hq, wl.Hkv, sink,
-                                 synth.generator(99), threads)
+                                 synth.generator(99), threads, layout)
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"layers 0-3 ([sliding x3, full]) of the step over all {len(wl.context)} sequences, "
                       f"{nbytes / 1e9:.2f} GB scored KV, {secs:.1f} s"}
@@ -507,6 +557,8 @@ def main(argv=None) -> int:
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
     ap.add_argument("--consumer", choices=["tensor-core", "cuda-core"], default="tensor-core",
                     help="inner loop of the attention kernels")
+    ap.add_argument("--layout", choices=["ring", "roll"], default="ring",
+                    help="cache layout of the sliding layers")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

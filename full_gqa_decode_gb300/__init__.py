@@ -81,6 +81,7 @@ _SIGS = {
     "hybrid_decode_profile": [_P, _i32, _c.POINTER(_c.c_double), _c.POINTER(_i64)],
     "hybrid_decode_set_consumer": [_P, _i32],
     "decode_attn_full_static_scratch": [_i32, _i32, _i32, _P, _i32, _P, hd_kv_cache, _P, _P, _P, _P],
+    "hybrid_decode_read_probe": [_P, _i64, _P],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -297,3 +298,12 @@ def decode_attn_full_static_scratch(num_kv_heads: int, context, max_context: int
                                                 max_context, _ptr(q_rot), cache, _ptr(sink), _ptr(out),
                                                 _ptr(lse), _stream(stream)),
            "decode_attn_full_static_scratch")
+
+
+def hybrid_decode_read_probe(buffer: torch.Tensor, stream=None) -> int:
+    """One pass of a pure read stream over a device buffer; returns the bytes the
+    pass covers (a whole number of 32 KiB stages per CTA).  Time it with events."""
+    nbytes = buffer.numel() * buffer.element_size()
+    _check(_lib.hybrid_decode_read_probe(_ptr(buffer), nbytes, _stream(stream)), "hybrid_decode_read_probe")
+    ctas = 2 * torch.cuda.get_device_properties(buffer.device).multi_processor_count
+    return (nbytes // (32 * 1024) // ctas) * ctas * 32 * 1024

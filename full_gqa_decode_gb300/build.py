@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIBRARY = os.path.join(PKG, "libhybriddecode.so")
-SOURCES = ["api.cpp", "rope_append.cu", "attn_decode.cu", "noalloc.cu"]
+SOURCES = ["api.cpp", "rope_append.cu", "attn_decode.cu", "noalloc.cu", "read_probe.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

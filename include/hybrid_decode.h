@@ -234,6 +234,14 @@ hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_q_heads, in
                                           const float *q_rot, hd_kv_cache cache, const float *sink,
                                           void *out, float *lse, void *stream);
 
+/* Measurement utility (no counterpart in the pages): one pass of a pure read
+ * stream over `bytes` of the device buffer (16-byte aligned), through shared
+ * memory with 1-D bulk copies, two CTAs per SM, no arithmetic; the caller
+ * times it on `stream`.  Gives the read bandwidth HBM delivers on this part,
+ * next to the copy figure (which counts a read and a write per byte).  Reads
+ * a whole number of 32 KiB stages per CTA and may leave a tail unread. */
+hd_status hybrid_decode_read_probe(const void *buffer, int64_t bytes, void *stream);
+
 /* Static text for a status code. */
 const char *hd_status_string(hd_status status);
 
