@@ -82,6 +82,7 @@ _SIGS = {
     "hybrid_decode_set_consumer": [_P, _i32],
     "decode_attn_full_static_scratch": [_i32, _i32, _i32, _P, _i32, _P, hd_kv_cache, _P, _P, _P, _P],
     "hybrid_decode_read_probe": [_P, _i64, _P],
+    "hybrid_decode_inject_lost_copy": [_P, _i32],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -307,3 +308,8 @@ def hybrid_decode_read_probe(buffer: torch.Tensor, stream=None) -> int:
     _check(_lib.hybrid_decode_read_probe(_ptr(buffer), nbytes, _stream(stream)), "hybrid_decode_read_probe")
     ctas = 2 * torch.cuda.get_device_properties(buffer.device).multi_processor_count
     return (nbytes // (32 * 1024) // ctas) * ctas * 32 * 1024
+
+
+def hybrid_decode_inject_lost_copy(ctx: Context, stage: int) -> None:
+    """Test hook: attention producers stop issuing copies at `stage` (-1: off)."""
+    _check(_lib.hybrid_decode_inject_lost_copy(ctx.handle, stage), "hybrid_decode_inject_lost_copy")

@@ -82,6 +82,7 @@ struct hd_ctx {
     int32_t *counters = nullptr;         // [max_batch][Hkv] chunk tickets, zero between calls
     int32_t *err = nullptr;
     int consumer = CONSUMER_MMA;
+    int32_t drop_stage = -1;             // test hook, see hybrid_decode_inject_lost_copy
     int64_t launches = 0;
     std::vector<MapCacheEntry> maps;     // one per layer
     int32_t profile_mask = 0;           // bit (1 << layer type): bracket that type's launches
@@ -270,6 +271,7 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     a.max_chunks = num_chunks;
     a.window = ctx->cfg.sliding_window;
     a.max_context = ctx->cfg.max_context;
+    a.drop_stage = ctx->drop_stage;
 
     const int type = sliding ? HD_SLIDING : HD_FULL;
     const size_t slot = (size_t)type * kProfileEvents + ctx->ev_used[type];
@@ -585,6 +587,12 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
         }
         if ((st = launch_layer_call(ctx, L, s)) != HD_OK) return st;
     }
+    return HD_OK;
+}
+
+hd_status hybrid_decode_inject_lost_copy(hd_ctx *ctx, int32_t stage) {
+    if (!ctx || stage < -1) return HD_ERR_INVALID_ARG;
+    ctx->drop_stage = stage;
     return HD_OK;
 }
 

@@ -497,6 +497,7 @@ __global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
     if (warp == kConsumerWarps) {
         if (lane == 0) {  // producer: one lane issues every load of the chunk
             for (int s = 0; s < nst; ++s) {
+                if (s == a.drop_stage) break;  // test hook: a copy that never arrives
                 const int slot = s % S;
                 if (s >= S && !mbar_wait(&empty[slot], ((s / S) - 1) & 1)) {
                     atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);

@@ -72,6 +72,7 @@ struct LayerArgs {
     int32_t num_q_heads, num_kv_heads;
     int32_t chunk_keys, max_chunks;
     int32_t window, max_context;
+    int32_t drop_stage;            // test hook: producers stop issuing at this stage (-1: off)
 };
 
 // Partial RoPE of q and the new k, and the K/V store.

@@ -192,6 +192,14 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
 enum { HD_CONSUMER_CUDA_CORE = 0, HD_CONSUMER_TENSOR_CORE = 1 };
 hd_status hybrid_decode_set_consumer(hd_ctx *ctx, int32_t consumer);
 
+/* Test hook for failure detection (no counterpart in the pages).  With
+ * stage >= 0, the copy producer of every attention CTA stops issuing copies at
+ * that pipeline stage, as if the copy were lost; the consumers' waits, bounded
+ * to one second, run out, the kernel records HD_DEVERR_WAIT_TIMEOUT and
+ * returns (outputs of affected sequences are then meaningless), and the
+ * context stays usable.  -1 (the default) turns it off. */
+hd_status hybrid_decode_inject_lost_copy(hd_ctx *ctx, int32_t stage);
+
 /* Reads and clears the device error word (HD_DEVERR_* bits).  Synchronises
  * `stream`. */
 hd_status hybrid_decode_device_errors(hd_ctx *ctx, int32_t *flags, void *stream);

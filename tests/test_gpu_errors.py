@@ -114,3 +114,32 @@ def test_sink_checks_mirror_the_page(hd):
                 torch.zeros(8)):                                       # other device
         with pytest.raises(ValueError):
             hd.decode_attn_sliding(ctx, 0, ctx_d, qrot, cache, bad, out, lse)
+
+
+def test_lost_copy_times_out_and_the_context_recovers(hd, orc):
+    """A copy that never arrives: the bounded waits run out (about one second),
+    the kernel reports HD_DEVERR_WAIT_TIMEOUT and returns; the same context then
+    gives correct results again."""
+    import time
+    rng = synth.generator(9)
+    ctx = _ctx(hd, [FULL], max_batch=2, max_context=1024)
+    case = LayerCase(rng, 2, 8, 2, 1025, [300, 900], sink=synth.sink_vector(rng, ("normal", 1.0, 0.0), 8))
+    dev = torch.device("cuda")
+    context = torch.from_numpy(case.context).to(dev)
+    kc, vc = case.kc.to(dev), case.vc.to(dev)
+    cache = hd.kv_cache(kc, vc)
+    qrot, out, lse = _bufs(2)
+    hd.rope_append_kv(ctx, 0, context, case.q.to(dev), case.k.to(dev), case.v.to(dev), qrot, cache)
+    hd.hybrid_decode_inject_lost_copy(ctx, 1)
+    t0 = time.time()
+    hd.decode_attn_full(ctx, 0, context, qrot, cache, case.sink.to(dev), out, lse)
+    flags = hd.hybrid_decode_device_errors(ctx)
+    elapsed = time.time() - t0
+    assert flags & 8, f"expected a wait timeout, flags {flags:#x}"
+    assert 0.5 < elapsed < 30.0, elapsed
+    hd.hybrid_decode_inject_lost_copy(ctx, -1)
+    hd.decode_attn_full(ctx, 0, context, qrot, cache, case.sink.to(dev), out, lse)
+    assert hd.hybrid_decode_device_errors(ctx) == 0
+    ref = oracle_layer(orc, case, FULL, 0)
+    assert_out_close(out, ref["out"])
+    assert_lse_close(lse, ref["lse"])
