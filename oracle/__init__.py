@@ -107,7 +107,7 @@ class Oracle:
                                            ctypes.c_int64, _i64p, _i64p]
         lib.orc_decode_layer.restype = ctypes.c_int
         lib.orc_decode_layer.argtypes = [ctypes.POINTER(OrcLayer), _i32p, _u16p, _u16p, _u16p,
-                                         _u16p, _u16p, _f32p, _f64p, _f64p, _f64p, _u16p]
+                                         _u16p, _u16p, _f32p, _f32p, _f64p, _f64p, _f64p, _u16p]
         self.lib = lib
         self.path = path
 
@@ -168,11 +168,12 @@ class Oracle:
 
     # -- one layer ----------------------------------------------------------
     def decode_layer(self, *, layer_type: int, layout: int, window: int, rotary_dim: int,
-                     rope_theta: float, context, q, k, v, kcache, vcache, sink=None):
+                     rope_theta: float, context, q, k, v, kcache, vcache, sink=None, gate=None):
         """One decode step of one layer; kcache/vcache are updated in place.
 
         q [B,Hq,D], k/v [B,Hkv,D] and the caches [B,Hkv,cap,D] are uint16 bf16
-        bit patterns; ``context`` is int32 [B]; ``sink`` float32 [Hq] or None.
+        bit patterns; ``context`` is int32 [B]; ``sink`` float32 [Hq] or None;
+        ``gate`` float32 [B, Hq] output-gate logits or None.
         Returns dict(out [B,Hq,D] f64, lse [B,Hq] f64, qrot [B,Hq,D] f64,
         k_written [B,Hkv,D] uint16).
         """
@@ -192,10 +193,14 @@ class Oracle:
         sk = None
         if sink is not None:
             sk = np.ascontiguousarray(sink, dtype=np.float32)
+        gt = None
+        if gate is not None:
+            gt = np.ascontiguousarray(gate, dtype=np.float32).reshape(B, Hq)
         rc = self.lib.orc_decode_layer(ctypes.byref(L), _ptr(ctx, _i32p), _ptr(q, _u16p),
                                        _ptr(k, _u16p), _ptr(v, _u16p), _ptr(kcache, _u16p),
                                        _ptr(vcache, _u16p),
                                        _ptr(sk, _f32p) if sk is not None else None,
+                                       _ptr(gt, _f32p) if gt is not None else None,
                                        _ptr(out, _f64p), _ptr(lse, _f64p), _ptr(qrot, _f64p),
                                        _ptr(kw, _u16p))
         if rc != 0:

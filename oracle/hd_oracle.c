@@ -33,6 +33,11 @@
  *   R5  lse is the natural-log log-sum-exp of the scaled scores, without the
  *       sink; the sink multiplies the output by exp(lse)/(exp(lse)+exp(sink))
  *       ([hyv4] HYV4FlashMLASparseImpl docstring).  A sink of -inf is no sink.
+ *   R6  the optional output gate multiplies each query head's attention output
+ *       by sigmoid(gate logit) after the sink ([spark] `_Layer.forward`: the
+ *       attention output, viewed per head, times sigmoid(g_proj(h))); the
+ *       logits are an input here (the projection lies outside the path) and
+ *       do not change lse.
  *
  * Every function below names what pins it in the test suite (tests/).
  */
@@ -243,6 +248,7 @@ static void load_row(const uint16_t *src, int head_dim, double *dst)
  * shift).  Query head h reads kv head h / group_size ([spark]: q is viewed as
  * (kv, group, d), so consecutive query heads share a kv head).
  *
+ * gate, if not NULL, holds [B][Hq] logits of the per-head output gate (R6).
  * Outputs: out [B][Hq][D] and lse [B][Hq] in fp64; optionally the rotated
  * queries qrot [B][Hq][D] and the written keys k_written [B][Hkv][D] (bf16).
  * kcache/vcache [B] x seq_stride, each sequence [Hkv][capacity][D] bf16, are
@@ -254,7 +260,7 @@ static void load_row(const uint16_t *src, int head_dim, double *dst)
 int orc_decode_layer(const orc_layer *L, const int32_t *context,
                      const uint16_t *q, const uint16_t *k, const uint16_t *v,
                      uint16_t *kcache, uint16_t *vcache, const float *sink,
-                     double *out, double *lse, double *qrot,
+                     const float *gate, double *out, double *lse, double *qrot,
                      uint16_t *k_written)
 {
     const int B = L->batch, Hq = L->num_q_heads, Hkv = L->num_kv_heads;
@@ -339,8 +345,14 @@ int orc_decode_layer(const orc_layer *L, const int32_t *context,
                     memcpy(qrot + ((int64_t)b * Hq + h) * D, qr, sizeof(double) * D);
                 const int has_sink = sink != NULL;
                 const double sk = has_sink ? (double)sink[h] : 0.0;
-                orc_attend(qr, D, (int)n, keys, vals, has_sink, sk,
-                           out + ((int64_t)b * Hq + h) * D, lse + (int64_t)b * Hq + h);
+                double *o = out + ((int64_t)b * Hq + h) * D;
+                orc_attend(qr, D, (int)n, keys, vals, has_sink, sk, o, lse + (int64_t)b * Hq + h);
+                if (gate) {
+                    /* sigmoid(x) = 1 / (1 + exp(-x)); exp(-inf) = 0 gives exactly 1 */
+                    const double gf = 1.0 / (1.0 + exp(-(double)gate[(int64_t)b * Hq + h]));
+                    for (int d = 0; d < D; ++d)
+                        o[d] *= gf;
+                }
             }
 
             /* Cache update, after scoring (R3, R4). */

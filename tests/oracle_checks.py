@@ -422,6 +422,32 @@ def check_history_model(orc):
                 assert abs(r["lse"][0, h] - lse) < 1e-12, (layer_type, layout, c, h)
 
 
+def check_output_gate(orc):
+    """The output gate scales each head by sigmoid(logit) (scipy expit), leaves
+    lse alone, is exactly a no-op at +inf, halves at 0 and zeroes at -inf."""
+    rng = np.random.default_rng(16)
+    B, Hq, Hkv, D = 2, 4, 2, 16
+    ctx = np.array([5, 0], np.int32)
+    base = dict(layer_type=FULL, layout=0, window=512, rotary_dim=8, rope_theta=1e4, context=ctx)
+    kc = _bf16_bits_random(rng, (B, Hkv, 8, D))
+    vc = _bf16_bits_random(rng, (B, Hkv, 8, D))
+    q = _bf16_bits_random(rng, (B, Hq, D))
+    k = _bf16_bits_random(rng, (B, Hkv, D))
+    v = _bf16_bits_random(rng, (B, Hkv, D))
+    sink = rng.standard_normal(Hq).astype(np.float32)
+    plain = _layer(orc, kcache=kc.copy(), vcache=vc.copy(), q=q, k=k, v=v, sink=sink, **base)
+    logits = rng.standard_normal((B, Hq)).astype(np.float32) * 3
+    gated = orc.decode_layer(kcache=kc.copy(), vcache=vc.copy(), q=q, k=k, v=v, sink=sink, gate=logits, **base)
+    want = plain["out"] * sps.expit(logits.astype(np.float64))[:, :, None]
+    assert np.allclose(gated["out"], want, rtol=1e-14, atol=1e-15)
+    assert np.array_equal(gated["lse"], plain["lse"])
+    special = np.array([[np.inf, 0.0, -np.inf, np.inf]] * B, np.float32)
+    g2 = orc.decode_layer(kcache=kc.copy(), vcache=vc.copy(), q=q, k=k, v=v, sink=sink, gate=special, **base)
+    assert np.array_equal(g2["out"][:, 0], plain["out"][:, 0])
+    assert np.array_equal(g2["out"][:, 1], plain["out"][:, 1] * 0.5)
+    assert np.all(g2["out"][:, 2] == 0.0)
+
+
 # -------------------------------------------------------------- footprint --
 
 def check_kv_cache_bytes_golden(orc):

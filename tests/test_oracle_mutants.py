@@ -35,6 +35,7 @@ MUTANTS = [
     ("full cache keeps one less", "if (layer_type != ORC_SLIDING)\n        return context;",
      "if (layer_type != ORC_SLIDING)\n        return context > 0 ? context - 1 : 0;"),
     ("footprint counts K only", "int64_t per_entry = 2LL *", "int64_t per_entry = 1LL *"),
+    ("gate sign", "exp(-(double)gate[", "exp((double)gate["),
 ]
 
 
