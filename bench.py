@@ -11,7 +11,8 @@ scored key costs one bf16 K row and one bf16 V row per kv head (1024 B at
 head_dim 256); sliding layers score min(c, 511) + 1 keys, full layers c + 1.
 The line also gives us per step, the roofline of the dominant kernel (the
 full-layer split-K pass), the oracle timed on the host cores, an end-to-end
-figure with host buffers, and the batch-1 28-layer step as a secondary figure.
+figure with host buffers, the same step with the per-head output gate, and the
+batch-1 28-layer step as a secondary figure.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 Multi-GPU (torchrun, one rank per GPU): every rank runs the same per-GPU
@@ -229,7 +230,7 @@ class Workload:
         self.context_d = torch.from_numpy(self.context).to(device)
         self.sink = None if sink is None else sink.to(device)
         ring = layout != synth.LAYOUT_ROLL
-        self.layers, self.io = [], []
+        self.layers, self.io, self.io_gated = [], [], []
         for i, t in enumerate(self.types):
             cap = (synth.WINDOW - 1 if ring else synth.WINDOW) if t == synth.SLIDING else self.max_ctx + 1
             kc = torch.empty(self.B, self.Hkv, cap, D, dtype=torch.bfloat16, device=device)
@@ -246,6 +247,10 @@ class Workload:
             cache = hd.kv_cache(kc, vc)
             self.layers.append(dict(q=q, k=k, v=v, kc=kc, vc=vc, out=out, lse=lse, cache=cache))
             self.io.append(hd.layer_io(q, k, v, cache, self.sink, out, lse))
+            # per-step output-gate logits N(0, 1) for the gated variant of the step
+            gate = torch.randn(self.B, self.Hq, generator=g, device=device)
+            self.layers[-1]["gate"] = gate
+            self.io_gated.append(hd.layer_io(q, k, v, cache, self.sink, out, lse, gate=gate))
         self.bytes = step_bytes(self.types, self.context, self.Hkv, layout)
         full_idx = [i for i, t in enumerate(self.types) if t == synth.FULL]
         self.full_layer_bytes = (int(scored_keys(synth.FULL, self.context, layout).sum()) * self.Hkv
@@ -253,9 +258,10 @@ class Workload:
         self.sliding_layer_bytes = (int(scored_keys(synth.SLIDING, self.context, layout).sum()) * self.Hkv
                                     * KV_ROW_BYTES)
 
-    def step(self, stream=None):
+    def step(self, stream=None, gated=False):
         import full_gqa_decode_gb300 as hd
-        hd.decode_step(self.ctx, self.context_d, self.io, self.B, self.max_ctx, stream)
+        hd.decode_step(self.ctx, self.context_d, self.io_gated if gated else self.io, self.B, self.max_ctx,
+                       stream)
 
 
 def time_steps(run, steps: int, warmup: int, world: int, device) -> float:
@@ -430,6 +436,13 @@ def run_ours(args, world, rank, local) -> int:
     # end to end: host buffers, copies inside the timed region
     e2e = e2e_measure(wl, args, world, device)
 
+    # the same step with the per-head output gate fused into every layer's epilogue,
+    # against the ungated step timed the same way (no profiling events)
+    plain_ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
+    gated_ms = time_steps(lambda: wl.step(gated=True), args.steps, args.warmup, 1, device)
+    if hd.hybrid_decode_device_errors(wl.ctx):
+        raise RuntimeError("device error flags during the gated step")
+
     result = None
     if rank == 0:
         cpu = cpu_baseline(wl, device)
@@ -447,6 +460,10 @@ def run_ours(args, world, rank, local) -> int:
                              "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world}"},
                   "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                   "gpu_launches": int(n1 - n0), "clocks": clk}
+        result["output_gate"] = {"ms_per_step": round(gated_ms, 4),
+                                 "value": round(wl.bytes / (gated_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                                 "ungated_ms_per_step": round(plain_ms, 4),
+                                 "overhead_vs_ungated": round(gated_ms / plain_ms - 1.0, 4)}
         if secondary:
             result["secondary"] = secondary
         print(json.dumps(result), flush=True)

@@ -60,7 +60,7 @@ class hd_kv_cache(ctypes.Structure):
 class hd_layer_io(ctypes.Structure):
     _fields_ = [("q", ctypes.c_void_p), ("k", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("cache", hd_kv_cache), ("sink", ctypes.c_void_p), ("out", ctypes.c_void_p),
-                ("lse", ctypes.c_void_p)]
+                ("lse", ctypes.c_void_p), ("gate", ctypes.c_void_p)]
 
 
 _c = ctypes
@@ -72,8 +72,8 @@ _SIGS = {
     "hybrid_decode_init": [_c.POINTER(hd_config), _c.POINTER(_P)],
     "hybrid_decode_destroy": [_P],
     "rope_append_kv": [_P, _i32, _i32, _P, _P, _P, _P, _P, hd_kv_cache, _P],
-    "decode_attn_sliding": [_P, _i32, _i32, _P, _P, hd_kv_cache, _P, _P, _P, _P],
-    "decode_attn_full": [_P, _i32, _i32, _P, _i32, _P, hd_kv_cache, _P, _P, _P, _P],
+    "decode_attn_sliding": [_P, _i32, _i32, _P, _P, hd_kv_cache, _P, _P, _P, _P, _P],
+    "decode_attn_full": [_P, _i32, _i32, _P, _i32, _P, hd_kv_cache, _P, _P, _P, _P, _P],
     "decode_step": [_P, _i32, _P, _i32, _c.POINTER(hd_layer_io), _P],
     "hybrid_decode_device_errors": [_P, _c.POINTER(_i32), _P],
     "hybrid_decode_launch_count": [_P, _c.POINTER(_i64)],
@@ -116,6 +116,20 @@ def _check_sink(sink, num_q_heads: int, like: torch.Tensor) -> None:
         raise ValueError(f"sink and query must be on the same device ({sink.device} vs {like.device})")
     if not sink.is_contiguous():
         raise ValueError("sink must be contiguous")
+
+
+def _check_gate(gate, batch: int, num_q_heads: int, like: torch.Tensor) -> None:
+    """Output-gate logits: fp32, shape (batch, num_q_heads), contiguous, on the query's device."""
+    if gate is None:
+        return
+    if gate.dtype != torch.float32:
+        raise ValueError(f"gate must be float32, got {gate.dtype}")
+    if tuple(gate.shape) != (batch, num_q_heads):
+        raise ValueError(f"gate must have shape ({batch}, {num_q_heads}), got {tuple(gate.shape)}")
+    if gate.device != like.device:
+        raise ValueError(f"gate and query must be on the same device ({gate.device} vs {like.device})")
+    if not gate.is_contiguous():
+        raise ValueError("gate must be contiguous")
 
 
 def _stream(stream) -> int | None:
@@ -224,28 +238,31 @@ def rope_append_kv(ctx: Context, layer: int, context: torch.Tensor, q, k, v, q_r
 
 
 def decode_attn_sliding(ctx: Context, layer: int, context, q_rot, cache: hd_kv_cache, sink, out, lse,
-                        stream=None) -> None:
+                        stream=None, gate=None) -> None:
     _check_sink(sink, ctx.cfg.num_q_heads, q_rot)
+    _check_gate(gate, q_rot.shape[0], ctx.cfg.num_q_heads, q_rot)
     _check_batch(cache, q_rot.shape[0])
     _check(_lib.decode_attn_sliding(ctx.handle, layer, q_rot.shape[0], _ptr(context), _ptr(q_rot),
-                                    cache, _ptr(sink), _ptr(out), _ptr(lse), _stream(stream)),
+                                    cache, _ptr(sink), _ptr(gate), _ptr(out), _ptr(lse), _stream(stream)),
            "decode_attn_sliding")
 
 
 def decode_attn_full(ctx: Context, layer: int, context, q_rot, cache: hd_kv_cache, sink, out, lse,
-                     max_context_hint: int = 0, stream=None) -> None:
+                     max_context_hint: int = 0, stream=None, gate=None) -> None:
     _check_sink(sink, ctx.cfg.num_q_heads, q_rot)
+    _check_gate(gate, q_rot.shape[0], ctx.cfg.num_q_heads, q_rot)
     _check_batch(cache, q_rot.shape[0])
     _check(_lib.decode_attn_full(ctx.handle, layer, q_rot.shape[0], _ptr(context), max_context_hint,
-                                 _ptr(q_rot), cache, _ptr(sink), _ptr(out), _ptr(lse),
+                                 _ptr(q_rot), cache, _ptr(sink), _ptr(gate), _ptr(out), _ptr(lse),
                                  _stream(stream)), "decode_attn_full")
 
 
-def layer_io(q, k, v, cache: hd_kv_cache, sink, out, lse) -> hd_layer_io:
+def layer_io(q, k, v, cache: hd_kv_cache, sink, out, lse, gate=None) -> hd_layer_io:
     if sink is not None:
         _check_sink(sink, q.shape[1], q)
+    _check_gate(gate, q.shape[0], q.shape[1], q)
     _check_batch(cache, q.shape[0])
-    return hd_layer_io(_ptr(q), _ptr(k), _ptr(v), cache, _ptr(sink), _ptr(out), _ptr(lse))
+    return hd_layer_io(_ptr(q), _ptr(k), _ptr(v), cache, _ptr(sink), _ptr(out), _ptr(lse), _ptr(gate))
 
 
 def decode_step(ctx: Context, context: torch.Tensor, layers: list, batch: int,

@@ -224,6 +224,7 @@ struct LayerCall {
     const void *new_k, *new_v;
     hd_kv_cache cache;
     const float *sink;
+    const float *gate;
     void *out;
     float *lse;
 };
@@ -259,6 +260,7 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     a.seq_stride = L.cache.seq_stride;
     a.capacity = L.cache.capacity;
     a.sink = L.sink;
+    a.gate = L.gate;
     a.out = static_cast<__nv_bfloat16 *>(L.out);
     a.lse = L.lse;
     a.part_o = ctx->part_o;
@@ -475,8 +477,8 @@ hd_status rope_append_kv(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_
 }
 
 hd_status decode_attn_sliding(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
-                              const float *q_rot, hd_kv_cache cache, const float *sink, void *out,
-                              float *lse, void *stream) {
+                              const float *q_rot, hd_kv_cache cache, const float *sink, const float *gate,
+                              void *out, float *lse, void *stream) {
     hd_status st = check_attention(ctx, layer, batch, context, cache, out, lse);
     if (st != HD_OK) return st;
     if (ctx->layer_types[layer] != HD_SLIDING) return HD_ERR_STATE;
@@ -495,6 +497,7 @@ hd_status decode_attn_sliding(hd_ctx *ctx, int32_t layer, int32_t batch, const i
     L.new_v = stage_row(ctx, ctx->stage_v, layer);
     L.cache = cache;
     L.sink = sink;
+    L.gate = gate;
     L.out = out;
     L.lse = lse;
     return launch_layer_call(ctx, L, static_cast<cudaStream_t>(stream));
@@ -502,7 +505,7 @@ hd_status decode_attn_sliding(hd_ctx *ctx, int32_t layer, int32_t batch, const i
 
 hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
                            int32_t max_context_hint, const float *q_rot, hd_kv_cache cache,
-                           const float *sink, void *out, float *lse, void *stream) {
+                           const float *sink, const float *gate, void *out, float *lse, void *stream) {
     hd_status st = check_attention(ctx, layer, batch, context, cache, out, lse);
     if (st != HD_OK) return st;
     if (ctx->layer_types[layer] != HD_FULL) return HD_ERR_STATE;
@@ -520,6 +523,7 @@ hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int3
     L.q_rot = q_rot;
     L.cache = cache;
     L.sink = sink;
+    L.gate = gate;
     L.out = out;
     L.lse = lse;
     return launch_layer_call(ctx, L, static_cast<cudaStream_t>(stream));
@@ -547,6 +551,7 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
         L.new_v = io.v;
         L.cache = io.cache;
         L.sink = io.sink;
+        L.gate = io.gate;
         L.out = io.out;
         L.lse = io.lse;
         if (!sliding) {

@@ -9,7 +9,10 @@
 // numerically the same as one fused softmax (ring-branch comment).  The new
 // entry is scored apart from the cache, as that comment's two-key-set form
 // does.  The sink follows vllm/models/hy_v4/nvidia/flashmla_sparse.py
-// (`HYV4FlashMLASparseImpl`): out *= exp(lse) / (exp(lse) + exp(sink)).
+// (`HYV4FlashMLASparseImpl`): out *= exp(lse) / (exp(lse) + exp(sink)).  The
+// optional output gate of spark_export.py (`_Layer.forward`: each head's
+// attention output times sigmoid of its gate logit) is applied in the same
+// epilogue scale.
 //
 // Grid: one CTA per (chunk of cached keys, kv head, sequence).  A producer
 // warp streams the chunk's K and V rows through a 3-stage shared-memory ring
@@ -164,11 +167,12 @@ __device__ __forceinline__ float f64_to_bf16_value(double x) {
 
 // Loads what the combine needs from global memory: the new entry (raw k for
 // NEW_ROTATE, the staged key otherwise), its value row, the rotary row at
-// position c, and the group's sink values.
+// position c, and the group's sink values and output-gate logits.
 // Threads [0, nthreads) share the work.
 template <int G>
 __device__ __forceinline__ void load_combine_inputs(const LayerArgs &a, int b, int kvh, int c, float *kraw_s,
-                                                    float *vnew_s, float2 *tab_s, float *sink_s, int nthreads) {
+                                                    float *vnew_s, float2 *tab_s, float *sink_s, float *gate_s,
+                                                    int nthreads) {
     const int t = threadIdx.x;
     if (a.new_kind != NEW_NONE) {
         const size_t e = ((size_t)b * a.num_kv_heads + kvh) * kHeadDim;
@@ -180,7 +184,10 @@ __device__ __forceinline__ void load_combine_inputs(const LayerArgs &a, int b, i
             for (int j = t; j < (a.rotary_dim >> 1); j += nthreads)
                 tab_s[j] = a.table[(size_t)c * (a.rotary_dim >> 1) + j];
     }
-    if (t < G) sink_s[t] = a.sink ? a.sink[kvh * G + t] : 0.f;
+    if (t < G) {
+        sink_s[t] = a.sink ? a.sink[kvh * G + t] : 0.f;
+        gate_s[t] = a.gate ? a.gate[(size_t)b * a.num_q_heads + kvh * G + t] : 0.f;
+    }
 }
 
 // Scored cache keys of sequence context c, or -1 (and the error bit) when c
@@ -488,7 +495,9 @@ __global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
     // A sequence with a single chunk is combined by this CTA: fetch the
     // combine's inputs now, in the same round as q.
     const bool has_new = a.new_kind != NEW_NONE;
-    if (nchunks == 1) load_combine_inputs<G>(a, b, kvh, c, kraw_s, vnew_s, tab_s, misc + 2 * kMaxGroup, kThreads);
+    if (nchunks == 1)
+        load_combine_inputs<G>(a, b, kvh, c, kraw_s, vnew_s, tab_s, misc + 2 * kMaxGroup, misc + 3 * kMaxGroup,
+                               kThreads);
     __syncthreads();
 
     float *red_o = reinterpret_cast<float *>(smem);             // reuses the stage ring
@@ -583,10 +592,11 @@ __global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
 
     // ---- combine (one CTA per sequence and kv head) ----
     // Every global input of the combine is requested in one round: the new
-    // entry, its rotary row and the sink (unless the prologue fetched them),
-    // and each warp's chunk maxima and sums.
+    // entry, its rotary row, the sink and the gate logits (unless the prologue
+    // fetched them), and each warp's chunk maxima and sums.
     float *sink_s = misc + 2 * kMaxGroup;           // [G]
-    if (nchunks > 1) load_combine_inputs<G>(a, b, kvh, c, kraw_s, vnew_s, tab_s, sink_s, kThreads);
+    float *gate_s = misc + 3 * kMaxGroup;           // [G]
+    if (nchunks > 1) load_combine_inputs<G>(a, b, kvh, c, kraw_s, vnew_s, tab_s, sink_s, gate_s, kThreads);
     const float2 *pml = reinterpret_cast<const float2 *>(a.part_ml);
     constexpr int kPerLane = 4;
     float2 ml[kPerLane];
@@ -619,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
     // Per head: M = max(chunk maxima, new score), chunk weights 2^(m_j - M) and
     // L = sum of weighted chunk sums (+ the new entry).  Warp w takes heads w, w+5, ...
     float *wts = reinterpret_cast<float *>(smem);   // [G][nchunks] (the warp buffers are free)
-    float *head_s = misc;                           // [G] scale = sink factor / L
+    float *head_s = misc;                           // [G] scale = sink factor * gate / L
     float *wnew_s = misc + kMaxGroup;               // [G] weight of the new entry
     for (int h = warp; h < G; h += kThreads / 32) {
         const size_t ph = pbase + (size_t)h * a.max_chunks;
@@ -669,7 +679,9 @@ __global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
             const int hg = kvh * G + h;
             const float lse = (M + fast_log2(L)) * kLn2;
             // exp(lse) / (exp(lse) + exp(sink)) = 1 / (1 + 2^((sink - lse) * log2 e))
-            const float f = a.sink ? 1.f / (1.f + fast_exp2((sink_s[h] - lse) * kLog2e)) : 1.f;
+            float f = a.sink ? 1.f / (1.f + fast_exp2((sink_s[h] - lse) * kLog2e)) : 1.f;
+            // output gate: sigmoid(g) = 1 / (1 + 2^(-g * log2 e)); lse is not gated
+            if (a.gate) f *= 1.f / (1.f + fast_exp2(-gate_s[h] * kLog2e));
             head_s[h] = f / L;
             wnew_s[h] = w_new;
             a.lse[(size_t)b * a.num_q_heads + hg] = lse;

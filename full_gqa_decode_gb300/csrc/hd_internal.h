@@ -63,6 +63,7 @@ struct LayerArgs {
     int64_t seq_stride;
     int32_t capacity;
     const float *sink;             // [Hq] or null
+    const float *gate;             // [batch][Hq] output-gate logits or null
     __nv_bfloat16 *out;            // [batch][Hq][D]
     float *lse;                    // [batch][Hq]
     float *part_o;                 // [batch][Hq][max_chunks][D] unnormalised partial outputs

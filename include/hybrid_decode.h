@@ -20,6 +20,11 @@
  *     per-head fp32 sink the output is multiplied by
  *     exp(lse) / (exp(lse) + exp(sink[h]))   (flashmla_sparse.py,
  *     `HYV4FlashMLASparseImpl` docstring); a sink of -inf is no sink;
+ *   - optional output gate: with per-step gate logits g[b][h] the output is
+ *     then multiplied by sigmoid(g) = 1/(1+exp(-g)) (spark_export.py
+ *     `_Layer.forward`, the sigmoid of the gate projection times the
+ *     attention output); lse is not gated.  The logits come from a
+ *     projection outside this library and are passed in;
  *   - cache update: full layers append at index c; sliding ring layouts write
  *     slot c mod (window-1), after the cached entries have been scored; the
  *     sliding roll layout shifts its window by one once full and appends
@@ -50,6 +55,7 @@
  *   q_rot            [batch][num_q_heads][head_dim] fp32
  *   lse              [batch][num_q_heads] fp32
  *   sink             [num_q_heads] fp32
+ *   gate             [batch][num_q_heads] fp32 logits
  *   cache k / v      sequence b starts at b * seq_stride; within it
  *                    [num_kv_heads][capacity][head_dim]
  */
@@ -127,6 +133,7 @@ typedef struct {
     const float *sink;    /* fp32 [num_q_heads] or NULL (no sink)                  */
     void *out;            /* bf16 [batch][num_q_heads][head_dim]                   */
     float *lse;           /* fp32 [batch][num_q_heads]                             */
+    const float *gate;    /* fp32 [batch][num_q_heads] gate logits or NULL (none)  */
 } hd_layer_io;
 
 /* Pure host check of a configuration (no device use). */
@@ -160,20 +167,21 @@ hd_status rope_append_kv(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_
 
 /* Attention of a sliding layer over its window: the ring's valid slots plus
  * the staged new entry (ring), or the rolled window (roll); split-K over the
- * keys, then an LSE combine that applies the sink, writes out/lse and commits
- * the staged ring entry.  Must follow rope_append_kv of the same layer on the
- * same stream. */
+ * keys, then an LSE combine that applies the sink and the output gate (either
+ * may be NULL), writes out/lse and commits the staged ring entry.  Must
+ * follow rope_append_kv of the same layer on the same stream. */
 hd_status decode_attn_sliding(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
                               const float *q_rot, hd_kv_cache cache, const float *sink,
-                              void *out, float *lse, void *stream);
+                              const float *gate, void *out, float *lse, void *stream);
 
 /* Attention of a full layer over positions 0..context[b] (the new entry was
  * appended by rope_append_kv): split-K over chunks of keys sized from
  * max_context_hint (an upper bound on every context[b] of this call, <=
- * max_context; 0 means max_context), then the LSE combine with the sink. */
+ * max_context; 0 means max_context), then the LSE combine with the sink and
+ * the output gate (either may be NULL). */
 hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
                            int32_t max_context_hint, const float *q_rot, hd_kv_cache cache,
-                           const float *sink, void *out, float *lse, void *stream);
+                           const float *sink, const float *gate, void *out, float *lse, void *stream);
 
 /* One decode step over all layers in order, with the same results as
  * rope_append_kv followed by the layer's attention call, in one kernel per

@@ -33,7 +33,7 @@
  *   R5  lse is the natural-log log-sum-exp of the scaled scores, without the
  *       sink; the sink multiplies the output by exp(lse)/(exp(lse)+exp(sink))
  *       ([hyv4] HYV4FlashMLASparseImpl docstring).  A sink of -inf is no sink.
- *   R6  the optional output gate multiplies each query head's attention output
+ *   R13 the optional output gate multiplies each query head's attention output
  *       by sigmoid(gate logit) after the sink ([spark] `_Layer.forward`: the
  *       attention output, viewed per head, times sigmoid(g_proj(h))); the
  *       logits are an input here (the projection lies outside the path) and

@@ -111,6 +111,17 @@ def sink_vector(rng: np.random.Generator, recipe, num_q_heads: int):
     return torch.from_numpy(s)
 
 
+def gate_logits(rng: np.random.Generator, batch: int, num_q_heads: int, std: float = 1.0,
+                specials: bool = False):
+    """fp32 [batch][num_q_heads] output-gate logits N(0, std^2); with ``specials``
+    the first sequence's heads cycle through +inf, -inf, 0, 30 and -30."""
+    g = (rng.standard_normal((batch, num_q_heads)) * std).astype(np.float32)
+    if specials:
+        vals = np.array([np.inf, -np.inf, 0.0, 30.0, -30.0], np.float32)
+        g[0] = vals[np.arange(num_q_heads) % len(vals)]
+    return torch.from_numpy(g)
+
+
 def cache_with_history(rng: np.random.Generator, batch: int, num_kv_heads: int, capacity: int,
                        written, head_dim: int = HEAD_DIM) -> torch.Tensor:
     """bf16 cache [B, Hkv, capacity, D]: entries [0, written[b]) random N(0,1), the rest NaN."""

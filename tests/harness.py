@@ -50,7 +50,7 @@ class LayerCase:
     """Seeded inputs of one layer call: q/k/v, caches with `written` valid entries."""
 
     def __init__(self, rng, batch, num_q_heads, num_kv_heads, capacity, context, written=None,
-                 sink=None):
+                 sink=None, gate=None):
         D = synth.HEAD_DIM
         self.context = np.asarray(context, np.int32)
         self.q = synth.normal_bf16(rng, (batch, num_q_heads, D))
@@ -61,6 +61,7 @@ class LayerCase:
         self.kc = synth.cache_with_history(rng, batch, num_kv_heads, capacity, written, D)
         self.vc = synth.cache_with_history(rng, batch, num_kv_heads, capacity, written, D)
         self.sink = sink
+        self.gate = gate  # fp32 [batch][num_q_heads] output-gate logits, or None
 
 
 def oracle_layer(orc, case: LayerCase, layer_type: int, layout: int, rotary_dim=None, theta=None):
@@ -70,7 +71,8 @@ def oracle_layer(orc, case: LayerCase, layer_type: int, layout: int, rotary_dim=
                          window=synth.WINDOW, rotary_dim=rotary_dim or rot, rope_theta=theta or th,
                          context=case.context, q=synth.bits(case.q), k=synth.bits(case.k),
                          v=synth.bits(case.v), kcache=kc, vcache=vc,
-                         sink=None if case.sink is None else case.sink.numpy())
+                         sink=None if case.sink is None else case.sink.numpy(),
+                         gate=None if case.gate is None else case.gate.numpy())
     r["kcache"], r["vcache"] = kc, vc
     return r
 
@@ -85,12 +87,13 @@ def gpu_layer(hd, ctx, layer: int, layer_type: int, case: LayerCase, max_context
     lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
     cache = hd.kv_cache(kd, vd)
     sink = None if case.sink is None else case.sink.to(dev)
+    gate = None if case.gate is None else case.gate.to(dev)
     hd.rope_append_kv(ctx, layer, ctx_d, case.q.to(dev), case.k.to(dev), case.v.to(dev), qrot, cache)
     if layer_type == SLIDING:
-        hd.decode_attn_sliding(ctx, layer, ctx_d, qrot, cache, sink, out, lse)
+        hd.decode_attn_sliding(ctx, layer, ctx_d, qrot, cache, sink, out, lse, gate=gate)
     else:
         hd.decode_attn_full(ctx, layer, ctx_d, qrot, cache, sink, out, lse,
-                            max_context_hint=max_context_hint)
+                            max_context_hint=max_context_hint, gate=gate)
     torch.cuda.synchronize()
     flags = hd.hybrid_decode_device_errors(ctx)
     return {"qrot": qrot, "out": out, "lse": lse, "kcache": kd, "vcache": vd, "flags": flags}
