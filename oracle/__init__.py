@@ -28,7 +28,9 @@ LIBRARY = os.path.join(HERE, "libhd_oracle.so")
 
 SLIDING, FULL = 0, 1
 LAYOUT_RING, LAYOUT_ROLL = 1, 2
+KV_BF16, KV_FP8_E4M3 = 0, 1
 
+_u8p = ctypes.POINTER(ctypes.c_uint8)
 _i32p = ctypes.POINTER(ctypes.c_int32)
 _i64p = ctypes.POINTER(ctypes.c_int64)
 _u16p = ctypes.POINTER(ctypes.c_uint16)
@@ -49,6 +51,7 @@ class OrcLayer(ctypes.Structure):
         ("rope_theta", ctypes.c_double),
         ("capacity", ctypes.c_int32),
         ("seq_stride", ctypes.c_int64),
+        ("kv_dtype", ctypes.c_int32),
     ]
 
 
@@ -106,8 +109,13 @@ class Oracle:
                                            ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_int64, _i64p, _i64p]
         lib.orc_decode_layer.restype = ctypes.c_int
+        lib.orc_e4m3_to_f64.restype = ctypes.c_double
+        lib.orc_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+        lib.orc_f64_to_e4m3.restype = ctypes.c_uint8
+        lib.orc_f64_to_e4m3.argtypes = [ctypes.c_double]
         lib.orc_decode_layer.argtypes = [ctypes.POINTER(OrcLayer), _i32p, _u16p, _u16p, _u16p,
-                                         _u16p, _u16p, _f32p, _f32p, _f64p, _f64p, _f64p, _u16p]
+                                         ctypes.c_void_p, ctypes.c_void_p, _f32p, _f32p, _f32p, _f32p,
+                                         _f64p, _f64p, _f64p, ctypes.c_void_p]
         self.lib = lib
         self.path = path
 
@@ -120,6 +128,15 @@ class Oracle:
         a = np.asarray(x, dtype=np.float64)
         return np.array([self.lib.orc_f64_to_bf16(float(v)) for v in a.ravel()],
                         dtype=np.uint16).reshape(a.shape)
+
+    def e4m3_to_f64(self, codes) -> np.ndarray:
+        a = np.asarray(codes, dtype=np.uint8)
+        return np.array([self.lib.orc_e4m3_to_f64(int(c)) for c in a.ravel()]).reshape(a.shape)
+
+    def f64_to_e4m3(self, x) -> np.ndarray:
+        a = np.asarray(x, dtype=np.float64)
+        return np.array([self.lib.orc_f64_to_e4m3(float(v)) for v in a.ravel()],
+                        dtype=np.uint8).reshape(a.shape)
 
     # -- rotary -------------------------------------------------------------
     def rope_angles(self, position: int, rotary_dim: int, theta: float):
@@ -168,28 +185,40 @@ class Oracle:
 
     # -- one layer ----------------------------------------------------------
     def decode_layer(self, *, layer_type: int, layout: int, window: int, rotary_dim: int,
-                     rope_theta: float, context, q, k, v, kcache, vcache, sink=None, gate=None):
+                     rope_theta: float, context, q, k, v, kcache, vcache, sink=None, gate=None,
+                     k_scale=None, v_scale=None):
         """One decode step of one layer; kcache/vcache are updated in place.
 
-        q [B,Hq,D], k/v [B,Hkv,D] and the caches [B,Hkv,cap,D] are uint16 bf16
-        bit patterns; ``context`` is int32 [B]; ``sink`` float32 [Hq] or None;
-        ``gate`` float32 [B, Hq] output-gate logits or None.
+        q [B,Hq,D] and k/v [B,Hkv,D] are uint16 bf16 bit patterns; the caches
+        [B,Hkv,cap,D] are uint16 bf16 bits, or uint8 E4M3 codes with fp32
+        ``k_scale``/``v_scale`` [Hkv]; ``context`` is int32 [B]; ``sink``
+        float32 [Hq] or None; ``gate`` float32 [B, Hq] output-gate logits or None.
         Returns dict(out [B,Hq,D] f64, lse [B,Hq] f64, qrot [B,Hq,D] f64,
-        k_written [B,Hkv,D] uint16).
+        k_written [B,Hkv,D] in the cache's element type).
         """
-        for name, a in (("q", q), ("k", k), ("v", v), ("kcache", kcache), ("vcache", vcache)):
+        for name, a in (("q", q), ("k", k), ("v", v)):
             if a.dtype != np.uint16 or not a.flags.c_contiguous:
                 raise ValueError(f"{name} must be C-contiguous uint16 bf16 bits")
+        fp8 = kcache.dtype == np.uint8
+        for name, a in (("kcache", kcache), ("vcache", vcache)):
+            if a.dtype != (np.uint8 if fp8 else np.uint16) or not a.flags.c_contiguous:
+                raise ValueError(f"{name} must be C-contiguous, uint16 bf16 bits or uint8 E4M3 codes")
+        if fp8 and (k_scale is None or v_scale is None):
+            raise ValueError("an FP8 cache needs k_scale and v_scale")
         B, Hq, D = q.shape
         Hkv = k.shape[1]
         cap = kcache.shape[2]
         ctx = np.ascontiguousarray(context, dtype=np.int32)
         L = OrcLayer(B, Hq, Hkv, D, layer_type, layout, window, rotary_dim, float(rope_theta),
-                     cap, Hkv * cap * D)
+                     cap, Hkv * cap * D, KV_FP8_E4M3 if fp8 else KV_BF16)
         out = np.zeros((B, Hq, D))
         lse = np.zeros((B, Hq))
         qrot = np.zeros((B, Hq, D))
-        kw = np.zeros((B, Hkv, D), np.uint16)
+        kw = np.zeros((B, Hkv, D), np.uint8 if fp8 else np.uint16)
+        ksc = vsc = None
+        if fp8:
+            ksc = np.ascontiguousarray(k_scale, dtype=np.float32)
+            vsc = np.ascontiguousarray(v_scale, dtype=np.float32)
         sk = None
         if sink is not None:
             sk = np.ascontiguousarray(sink, dtype=np.float32)
@@ -197,12 +226,14 @@ class Oracle:
         if gate is not None:
             gt = np.ascontiguousarray(gate, dtype=np.float32).reshape(B, Hq)
         rc = self.lib.orc_decode_layer(ctypes.byref(L), _ptr(ctx, _i32p), _ptr(q, _u16p),
-                                       _ptr(k, _u16p), _ptr(v, _u16p), _ptr(kcache, _u16p),
-                                       _ptr(vcache, _u16p),
+                                       _ptr(k, _u16p), _ptr(v, _u16p), kcache.ctypes.data,
+                                       vcache.ctypes.data,
+                                       _ptr(ksc, _f32p) if ksc is not None else None,
+                                       _ptr(vsc, _f32p) if vsc is not None else None,
                                        _ptr(sk, _f32p) if sk is not None else None,
                                        _ptr(gt, _f32p) if gt is not None else None,
                                        _ptr(out, _f64p), _ptr(lse, _f64p), _ptr(qrot, _f64p),
-                                       _ptr(kw, _u16p))
+                                       kw.ctypes.data)
         if rc != 0:
             raise ValueError(f"oracle rejected the layer arguments (code {rc})")
         return {"out": out, "lse": lse, "qrot": qrot, "k_written": kw}

@@ -38,6 +38,15 @@
  *       attention output, viewed per head, times sigmoid(g_proj(h))); the
  *       logits are an input here (the projection lies outside the path) and
  *       do not change lse.
+ *   R14 FP8 KV cache (an extension the pages name only as prior art: FlashMLA's
+ *       FP8 KV cache, [hyv4] `is_fp8_kvcache`): entries are OCP FP8 E4M3 codes
+ *       with one fp32 scale per kv head for K and one for V; a cached value is
+ *       decode(code) * scale.  The new entry is quantised as
+ *       code = e4m3(x / scale) with x the fp64 rotated key (as in R2) or the
+ *       bf16 value, the division rounded once in fp64 and the result rounded
+ *       once to e4m3 (nearest, ties to even), finite values beyond the largest
+ *       code saturating to +-448.  The new entry is scored as stored (its
+ *       dequantised value).
  *
  * Every function below names what pins it in the test suite (tests/).
  */
@@ -96,6 +105,56 @@ uint16_t orc_f64_to_bf16(double x)
     uint32_t u;
     memcpy(&u, &f, sizeof u);
     return sign | (uint16_t)(u >> 16);
+}
+
+/* ------------------------------------------------------ fp8 e4m3 (R14) --- */
+
+/* OCP FP8 E4M3 ("e4m3fn"): sign, 4 exponent bits with bias 7, 3 mantissa
+ * bits; no infinities; S.1111.111 is NaN; the largest finite value is
+ * 1.75 * 2^8 = 448; exponent field 0 holds the subnormals m * 2^-9.
+ * Pinned by: all 256 codes against torch's float8_e4m3fn -> float32 cast. */
+double orc_e4m3_to_f64(uint8_t code)
+{
+    int sign = code >> 7, e = (code >> 3) & 15, m = code & 7;
+    if (e == 15 && m == 7)
+        return NAN;
+    double v = (e == 0) ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    return sign ? -v : v;
+}
+
+/* One round-to-nearest-even from a double to E4M3, saturating: the double is
+ * scaled so that one E4M3 quantum (2^(E-3) for a value in [2^E, 2^(E+1)),
+ * 2^-9 below 2^-6) becomes 1.0, rounded with rint() (ties to even) and scaled
+ * back; results above 448, and infinities, become +-448; NaN stays NaN.
+ * Pinned by: round trip of every finite code, brute-force nearest (ties to
+ * the even code) on random and midpoint doubles, and torch's cast on binary32
+ * inputs within range. */
+uint8_t orc_f64_to_e4m3(double x)
+{
+    if (isnan(x))
+        return 0x7F;
+    uint8_t sign = signbit(x) ? 0x80 : 0;
+    double a = fabs(x);
+    if (isinf(a))
+        return sign | 0x7E;
+    if (a == 0.0)
+        return sign;
+    int e;
+    frexp(a, &e);
+    int E = e - 1;                     /* a in [2^E, 2^(E+1)) */
+    if (E < -6)
+        E = -6;                        /* subnormals share the 2^-9 quantum */
+    double v = ldexp(rint(ldexp(a, 3 - E)), E - 3);
+    if (v > 448.0)
+        return sign | 0x7E;
+    if (v == 0.0)
+        return sign;
+    frexp(v, &e);
+    E = e - 1;                         /* rounding may have moved v up one binade */
+    if (E < -6)
+        return sign | (uint8_t)ldexp(v, 9);               /* subnormal: m * 2^-9 */
+    int mant = (int)ldexp(v, 3 - E) - 8;                   /* v = (8 + m) * 2^(E-3) */
+    return sign | (uint8_t)((E + 7) << 3) | (uint8_t)mant;
 }
 
 /* ---------------------------------------------------------- rotary (R1) --- */
@@ -223,6 +282,9 @@ void orc_kv_cache_bytes(int num_layers, const int32_t *layer_types,
 
 /* ------------------------------------------------------ one decode layer --- */
 
+#define ORC_KV_BF16 0
+#define ORC_KV_FP8_E4M3 1
+
 typedef struct {
     int32_t batch, num_q_heads, num_kv_heads, head_dim;
     int32_t layer_type;   /* ORC_SLIDING / ORC_FULL                           */
@@ -232,12 +294,27 @@ typedef struct {
     double rope_theta;
     int32_t capacity;     /* entries per (sequence, kv head) in the cache      */
     int64_t seq_stride;   /* elements between consecutive sequences' caches    */
+    int32_t kv_dtype;     /* ORC_KV_BF16 or ORC_KV_FP8_E4M3 (R14)              */
 } orc_layer;
 
 static void load_row(const uint16_t *src, int head_dim, double *dst)
 {
     for (int d = 0; d < head_dim; ++d)
         dst[d] = orc_bf16_to_f64(src[d]);
+}
+
+/* One cached K or V row in fp64: bf16 bits, or E4M3 codes times the scale. */
+static void load_cached_row(const orc_layer *L, const void *cache, int64_t index, double scale,
+                            double *dst)
+{
+    const int D = L->head_dim;
+    if (L->kv_dtype == ORC_KV_FP8_E4M3) {
+        const uint8_t *src = (const uint8_t *)cache + index * D;
+        for (int d = 0; d < D; ++d)
+            dst[d] = orc_e4m3_to_f64(src[d]) * scale;
+    } else {
+        load_row((const uint16_t *)cache + index * D, D, dst);
+    }
 }
 
 /* One decode step of one layer ([spark] `_Layer.forward` without the
@@ -248,25 +325,32 @@ static void load_row(const uint16_t *src, int head_dim, double *dst)
  * shift).  Query head h reads kv head h / group_size ([spark]: q is viewed as
  * (kv, group, d), so consecutive query heads share a kv head).
  *
- * gate, if not NULL, holds [B][Hq] logits of the per-head output gate (R6).
+ * gate, if not NULL, holds [B][Hq] logits of the per-head output gate (R13).
  * Outputs: out [B][Hq][D] and lse [B][Hq] in fp64; optionally the rotated
- * queries qrot [B][Hq][D] and the written keys k_written [B][Hkv][D] (bf16).
- * kcache/vcache [B] x seq_stride, each sequence [Hkv][capacity][D] bf16, are
- * updated in place.  Returns ORC_OK, or an error before touching any output
+ * queries qrot [B][Hq][D] and the written keys k_written [B][Hkv][D] (bf16
+ * bits, or E4M3 codes for an FP8 cache).  kcache/vcache [B] x seq_stride, each
+ * sequence [Hkv][capacity][D] of bf16 bits or E4M3 codes (L->kv_dtype), are
+ * updated in place; an FP8 cache takes k_scale/v_scale [Hkv] (R14).  Returns ORC_OK, or an error before touching any output
  * when an argument or a context length does not fit the layer.
  * Pinned by: the brute-force and invariant tests on the pieces above, plus
  * sliding == full at context <= window-1, ring == roll, and the multi-step
  * history simulation. */
 int orc_decode_layer(const orc_layer *L, const int32_t *context,
                      const uint16_t *q, const uint16_t *k, const uint16_t *v,
-                     uint16_t *kcache, uint16_t *vcache, const float *sink,
-                     const float *gate, double *out, double *lse, double *qrot,
-                     uint16_t *k_written)
+                     void *kcache, void *vcache, const float *k_scale, const float *v_scale,
+                     const float *sink, const float *gate, double *out, double *lse,
+                     double *qrot, void *k_written)
 {
     const int B = L->batch, Hq = L->num_q_heads, Hkv = L->num_kv_heads;
     const int D = L->head_dim, rot = L->rotary_dim;
     if (B < 0 || Hq <= 0 || Hkv <= 0 || D <= 0 || Hq % Hkv != 0)
         return ORC_ERR_ARG;
+    const int fp8 = L->kv_dtype == ORC_KV_FP8_E4M3;
+    if (!fp8 && L->kv_dtype != ORC_KV_BF16)
+        return ORC_ERR_ARG;
+    if (fp8 && (!k_scale || !v_scale))
+        return ORC_ERR_ARG;
+    const size_t esize = fp8 ? 1 : 2;   /* bytes per cache element */
     if (rot < 0 || rot > D || rot % 2 != 0)
         return ORC_ERR_ARG;
     if (L->layer_type != ORC_SLIDING && L->layer_type != ORC_FULL)
@@ -299,24 +383,39 @@ int orc_decode_layer(const orc_layer *L, const int32_t *context,
     double *keys = (double *)malloc(sizeof(double) * (size_t)max_keys * D);
     double *vals = (double *)malloc(sizeof(double) * (size_t)max_keys * D);
     uint16_t *kb = (uint16_t *)malloc(sizeof(uint16_t) * D);
+    uint8_t *kq = (uint8_t *)malloc((size_t)D);   /* FP8: new K and V codes */
+    uint8_t *vq = (uint8_t *)malloc((size_t)D);
     int rc = ORC_OK;
 
     for (int b = 0; b < B; ++b) {
         const int64_t c = context[b];
         orc_rope_angles(c, rot, L->rope_theta, cs, sn);
         for (int kv = 0; kv < Hkv; ++kv) {
-            uint16_t *kc = kcache + b * L->seq_stride + (int64_t)kv * L->capacity * D;
-            uint16_t *vc = vcache + b * L->seq_stride + (int64_t)kv * L->capacity * D;
+            const int64_t head_off = (b * L->seq_stride + (int64_t)kv * L->capacity * D) * (int64_t)esize;
+            uint8_t *kc = (uint8_t *)kcache + head_off;
+            uint8_t *vc = (uint8_t *)vcache + head_off;
             const uint16_t *kin = k + ((int64_t)b * Hkv + kv) * D;
             const uint16_t *vin = v + ((int64_t)b * Hkv + kv) * D;
+            const double ks = fp8 ? (double)k_scale[kv] : 1.0;
+            const double vs = fp8 ? (double)v_scale[kv] : 1.0;
 
-            /* New key: rotate in fp64, round once to bf16 (R2). */
+            /* New key: rotate in fp64, round once to bf16 (R2), or divide by
+             * the scale in fp64 and round once to E4M3 (R14); V likewise. */
             load_row(kin, D, x);
             orc_rope_f64(x, D, rot, cs, sn, knew);
-            for (int d = 0; d < D; ++d)
-                kb[d] = orc_f64_to_bf16(knew[d]);
+            for (int d = 0; d < D; ++d) {
+                if (fp8) {
+                    kq[d] = orc_f64_to_e4m3(knew[d] / ks);
+                    vq[d] = orc_f64_to_e4m3(orc_bf16_to_f64(vin[d]) / vs);
+                } else {
+                    kb[d] = orc_f64_to_bf16(knew[d]);
+                }
+            }
+            const void *knew_bits = fp8 ? (const void *)kq : (const void *)kb;
+            const void *vnew_bits = fp8 ? (const void *)vq : (const void *)vin;
             if (k_written)
-                memcpy(k_written + ((int64_t)b * Hkv + kv) * D, kb, sizeof(uint16_t) * D);
+                memcpy((uint8_t *)k_written + ((int64_t)b * Hkv + kv) * D * (int64_t)esize, knew_bits,
+                       esize * D);
 
             /* Key set of this step: the cached entries the layout keeps, then
              * the new entry (its own phase, stored precision). */
@@ -330,11 +429,11 @@ int orc_decode_layer(const orc_layer *L, const int32_t *context,
                 goto done;
             }
             for (int64_t j = first; j < cached; ++j, ++n) {
-                load_row(kc + j * D, D, keys + n * D);
-                load_row(vc + j * D, D, vals + n * D);
+                load_cached_row(L, kc, j, ks, keys + n * D);
+                load_cached_row(L, vc, j, vs, vals + n * D);
             }
-            load_row(kb, D, keys + n * D);
-            load_row(vin, D, vals + n * D);
+            load_cached_row(L, knew_bits, 0, ks, keys + n * D);   /* scored as stored */
+            load_cached_row(L, vnew_bits, 0, vs, vals + n * D);
             ++n;
 
             for (int hh = 0; hh < g; ++hh) {
@@ -361,8 +460,8 @@ int orc_decode_layer(const orc_layer *L, const int32_t *context,
                 slot = c % (L->window - 1);
             } else if (roll) {
                 if (c >= L->window) {
-                    memmove(kc, kc + D, sizeof(uint16_t) * (size_t)(L->window - 1) * D);
-                    memmove(vc, vc + D, sizeof(uint16_t) * (size_t)(L->window - 1) * D);
+                    memmove(kc, kc + D * esize, esize * (size_t)(L->window - 1) * D);
+                    memmove(vc, vc + D * esize, esize * (size_t)(L->window - 1) * D);
                     slot = L->window - 1;
                 } else {
                     slot = c;
@@ -374,12 +473,12 @@ int orc_decode_layer(const orc_layer *L, const int32_t *context,
                 rc = ORC_ERR_CAPACITY;
                 goto done;
             }
-            memcpy(kc + slot * D, kb, sizeof(uint16_t) * D);
-            memcpy(vc + slot * D, vin, sizeof(uint16_t) * D);
+            memcpy(kc + slot * D * (int64_t)esize, knew_bits, esize * D);
+            memcpy(vc + slot * D * (int64_t)esize, vnew_bits, esize * D);
         }
     }
 done:
     free(cs); free(sn); free(x); free(qr); free(knew);
-    free(keys); free(vals); free(kb);
+    free(keys); free(vals); free(kb); free(kq); free(vq);
     return rc;
 }

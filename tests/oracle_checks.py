@@ -20,6 +20,12 @@ step, vllm/models/hy_v4/nvidia/flashmla_sparse.py for the sink):
                      token-by-token history model (a plain list of every past
                      token) that the cache bookkeeping must reproduce
   footprint          the page's 4k-context KV figures (tests/golden)
+  output gate        scipy expit per head; exact values at +inf, 0 and -inf
+  fp8 e4m3 (R14)     all 256 codes against torch's float8_e4m3fn cast, round trip,
+                     brute-force nearest-even on random and midpoint doubles,
+                     saturation; FP8 layers against a scipy brute force on the
+                     dequantised cache, against the bf16 layer on values both
+                     formats hold exactly, and against the history model
 """
 from __future__ import annotations
 
@@ -446,6 +452,210 @@ def check_output_gate(orc):
     assert np.array_equal(g2["out"][:, 0], plain["out"][:, 0])
     assert np.array_equal(g2["out"][:, 1], plain["out"][:, 1] * 0.5)
     assert np.all(g2["out"][:, 2] == 0.0)
+
+
+# --------------------------------------------------------------- fp8 e4m3 --
+
+NAN_CODE = np.uint8(0x7F)
+
+
+def _e4m3_table():
+    """All 256 codes decoded by torch's float8_e4m3fn -> float32 cast."""
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    return codes.view(torch.float8_e4m3fn).float().double().numpy()
+
+
+def _e4m3_nearest(x, table):
+    """Brute force: the code of x's sign whose value is nearest to x, ties to the
+    code with an even mantissa; beyond the largest finite value, that value."""
+    if np.isnan(x):
+        return 0x7F
+    sign = 0x80 if np.signbit(x) else 0
+    if abs(x) > 448.0:
+        return sign | 0x7E
+    codes = [c for c in range(sign, sign + 128) if not np.isnan(table[c])]
+    dist = [abs(x - table[c]) for c in codes]
+    best = min(dist)
+    ties = [c for c, d_ in zip(codes, dist) if d_ == best]
+    if len(ties) > 1:
+        ties = [c for c in ties if c % 2 == 0]
+    assert len(ties) == 1, (x, ties)
+    return ties[0]
+
+
+def _random_codes(rng, shape):
+    c = rng.integers(0, 256, size=shape).astype(np.uint8)
+    c[(c & 0x7F) == 0x7F] = 0x3C  # no NaN codes among written entries
+    return c
+
+
+def check_e4m3_decode_matches_torch(orc):
+    want = _e4m3_table()
+    got = orc.e4m3_to_f64(np.arange(256))
+    nan = np.isnan(want)
+    assert nan.sum() == 2 and want[0x7E] == 448.0 and want[0x01] == 2.0 ** -9
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan], want[~nan])
+    assert np.array_equal(np.signbit(got[~nan]), np.signbit(want[~nan]))
+
+
+def check_e4m3_round_trip(orc):
+    table = _e4m3_table()
+    finite = np.array([c for c in range(256) if not np.isnan(table[c])], np.uint8)
+    assert np.array_equal(orc.f64_to_e4m3(orc.e4m3_to_f64(finite)), finite)
+
+
+def check_e4m3_nearest_even_brute_force(orc):
+    table = _e4m3_table()
+    rng = np.random.default_rng(17)
+    mags = np.exp2(rng.uniform(-12.0, 9.2, size=1500))
+    xs = list(mags * np.where(rng.random(1500) < 0.5, -1.0, 1.0))
+    pos = np.sort(np.unique(table[:0x7F]))                 # +0 .. 448
+    mids = (pos[:-1] + pos[1:]) / 2                        # exact ties in fp64
+    xs += list(mids) + list(-mids) + list(np.nextafter(mids, 0)) + list(np.nextafter(mids, 1e9))
+    xs += [0.0, -0.0, 448.0, 449.0, 464.0, 464.0001, 480.0, 1e30, -1e30, 2.0 ** -10, 2.0 ** -11,
+           3 * 2.0 ** -11, 1e-300]
+    got = orc.f64_to_e4m3(np.array(xs))
+    want = np.array([_e4m3_nearest(x, table) for x in xs], np.uint8)
+    bad = np.nonzero(got != want)[0]
+    assert bad.size == 0, f"e4m3 rounding differs at {xs[bad[0]]!r}: {got[bad[0]]:#x} vs {want[bad[0]]:#x}"
+    assert list(orc.f64_to_e4m3(np.array([np.inf, -np.inf]))) == [0x7E, 0xFE]
+    assert (orc.f64_to_e4m3(np.array([np.nan]))[0] & 0x7F) == 0x7F
+
+
+def check_e4m3_matches_torch_on_binary32(orc):
+    rng = np.random.default_rng(18)
+    x = (np.exp2(rng.uniform(-11.0, 8.8, size=4000)) * np.where(rng.random(4000) < 0.5, -1, 1)).astype(np.float32)
+    x = x[np.abs(x) <= 448.0]
+    want = torch.from_numpy(x).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(orc.f64_to_e4m3(x.astype(np.float64)), want)
+
+
+def _fp8_case(rng, B, Hkv, cap, D, written):
+    kc = np.full((B, Hkv, cap, D), NAN_CODE, np.uint8)
+    vc = kc.copy()
+    for b in range(B):
+        n = written[b]
+        kc[b, :, :n] = _random_codes(rng, (Hkv, n, D))
+        vc[b, :, :n] = _random_codes(rng, (Hkv, n, D))
+    return kc, vc
+
+
+def check_fp8_layer_vs_brute_force(orc):
+    """FP8 full and ring layers: written codes are the brute-force nearest codes of
+    the fp64 rotated key / scale (and value / scale); out and lse are a scipy
+    brute force over the dequantised key set."""
+    table = _e4m3_table()
+    rng = np.random.default_rng(19)
+    B, Hq, Hkv, D, rot, theta = 2, 4, 2, 16, 8, 1e4
+    g = Hq // Hkv
+    for layer_type, layout, cap, ctx in ((FULL, 0, 12, np.array([5, 11], np.int32)),
+                                         (SLIDING, RING, 7, np.array([3, 12], np.int32))):
+        written = np.minimum(ctx, cap)
+        kc, vc = _fp8_case(rng, B, Hkv, cap, D, written)
+        q = _bf16_bits_random(rng, (B, Hq, D))
+        k = _bf16_bits_random(rng, (B, Hkv, D), std=3.0)
+        v = _bf16_bits_random(rng, (B, Hkv, D), std=3.0)
+        ks = rng.uniform(0.004, 0.02, Hkv).astype(np.float32)
+        vs = rng.uniform(0.004, 0.02, Hkv).astype(np.float32)
+        sink = rng.standard_normal(Hq).astype(np.float32)
+        kc0, vc0 = kc.copy(), vc.copy()
+        r = _layer(orc, layer_type=layer_type, layout=layout, window=8, rotary_dim=rot, rope_theta=theta,
+                   context=ctx, q=q, k=k, v=v, kcache=kc, vcache=vc, sink=sink, k_scale=ks, v_scale=vs)
+        for b in range(B):
+            c_, s_ = orc.rope_angles(int(ctx[b]), rot, theta)
+            qr = _rope_complex(_bits_to_f64(q[b]), rot, c_, s_)
+            kr = _rope_complex(_bits_to_f64(k[b]), rot, c_, s_)
+            kq = np.array([[_e4m3_nearest(t / float(ks[h]), table) for t in kr[h]] for h in range(Hkv)], np.uint8)
+            vf = _bits_to_f64(v[b])
+            vq = np.array([[_e4m3_nearest(t / float(vs[h]), table) for t in vf[h]] for h in range(Hkv)], np.uint8)
+            assert np.array_equal(r["k_written"][b], kq), "written key codes"
+            if layer_type == FULL:
+                slots, lo = [int(ctx[b])], 0
+                idx = list(range(int(ctx[b])))
+            else:
+                c = int(ctx[b])
+                idx = [p % cap for p in range(max(0, c - cap), c)]
+                slots = [c % cap]
+            kd = table[kc0[b][:, idx]] * ks[:, None, None]
+            vd = table[vc0[b][:, idx]] * vs[:, None, None]
+            keys = np.concatenate([kd, table[kq][:, None] * ks[:, None, None]], axis=1)
+            vals = np.concatenate([vd, table[vq][:, None] * vs[:, None, None]], axis=1)
+            for h in range(Hq):
+                sc = keys[h // g] @ qr[h] / math.sqrt(D)
+                lse = sps.logsumexp(sc)
+                out = sps.softmax(sc) @ vals[h // g] * sps.expit(lse - sink[h])
+                assert np.allclose(r["out"][b, h], out, rtol=1e-12, atol=1e-12), (layer_type, b, h)
+                assert abs(r["lse"][b, h] - lse) < 1e-12
+            assert np.array_equal(kc[b][:, slots[0]], kq) and np.array_equal(vc[b][:, slots[0]], vq)
+
+
+def check_fp8_equals_bf16_on_shared_values(orc):
+    """With a power-of-two scale and values both formats hold exactly (and no
+    rotation), the FP8 layer and the bf16 layer compute bit-identical results and
+    write the same values."""
+    rng = np.random.default_rng(20)
+    B, Hq, Hkv, D = 2, 4, 2, 16
+    scale = np.float32(2.0 ** -5)
+    table = _e4m3_table()
+    ctx = np.array([6, 9], np.int32)
+    for layer_type, layout, cap in ((FULL, 0, 10), (SLIDING, RING, 7), (SLIDING, ROLL, 8)):
+        written = np.minimum(ctx, cap)
+        kc, vc = _fp8_case(rng, B, Hkv, cap, D, written)
+        to_bf16 = lambda codes: torch.from_numpy(table[codes] * float(scale)).to(torch.bfloat16).view(
+            torch.int16).numpy().view(np.uint16).copy()
+        kb = np.where(kc == NAN_CODE, NAN_BITS, to_bf16(np.where(kc == NAN_CODE, 0, kc)))
+        vb = np.where(vc == NAN_CODE, NAN_BITS, to_bf16(np.where(vc == NAN_CODE, 0, vc)))
+        knew_codes = _random_codes(rng, (B, Hkv, D))
+        vnew_codes = _random_codes(rng, (B, Hkv, D))
+        q = _bf16_bits_random(rng, (B, Hq, D))
+        sink = rng.standard_normal(Hq).astype(np.float32)
+        args = dict(layer_type=layer_type, layout=layout, window=8, rotary_dim=0, rope_theta=1e4,
+                    context=ctx, q=q, k=to_bf16(knew_codes), v=to_bf16(vnew_codes), sink=sink)
+        a = _layer(orc, kcache=kc, vcache=vc, k_scale=np.full(Hkv, scale), v_scale=np.full(Hkv, scale), **args)
+        b = _layer(orc, kcache=kb, vcache=vb, **args)
+        assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["lse"], b["lse"]), layer_type
+        assert np.array_equal(a["k_written"], knew_codes)
+        assert np.array_equal(b["k_written"], to_bf16(knew_codes))
+        for fp8_cache, bf16_cache in ((kc, kb), (vc, vb)):
+            held = fp8_cache != NAN_CODE
+            assert np.array_equal(to_bf16(np.where(held, fp8_cache, 0))[held], bf16_cache[held])
+            assert np.all(bf16_cache[~held] == NAN_BITS)
+
+
+def check_fp8_history_model(orc):
+    """FP8 ring, roll and full caches over many steps from empty against a plain
+    list of every past token's codes (brute-force quantised)."""
+    table = _e4m3_table()
+    rng = np.random.default_rng(21)
+    Hq, Hkv, D, rot = 4, 2, 16, 8
+    g = Hq // Hkv
+    ks = np.array([0.01, 0.02], np.float32)
+    vs = np.array([0.015, 0.005], np.float32)
+    for layer_type, layout, window, steps in ((SLIDING, RING, 8, 24), (SLIDING, ROLL, 8, 24), (FULL, 0, 8, 14)):
+        cap = (window - 1 if layout == RING else window) if layer_type == SLIDING else steps + 1
+        kc = np.full((1, Hkv, cap, D), NAN_CODE, np.uint8)
+        vc = kc.copy()
+        past_k, past_v = [], []
+        for c in range(steps):
+            q = _bf16_bits_random(rng, (1, Hq, D))
+            k = _bf16_bits_random(rng, (1, Hkv, D))
+            v = _bf16_bits_random(rng, (1, Hkv, D))
+            r = _layer(orc, layer_type=layer_type, layout=layout, window=window, rotary_dim=rot,
+                       rope_theta=1e4, context=np.array([c], np.int32), q=q, k=k, v=v,
+                       kcache=kc, vcache=vc, k_scale=ks, v_scale=vs)
+            past_k.append(r["k_written"][0])
+            vf = _bits_to_f64(v[0])
+            past_v.append(np.array([[_e4m3_nearest(t / float(vs[h]), table) for t in vf[h]]
+                                    for h in range(Hkv)], np.uint8))
+            lo = max(0, c - window + 1) if layer_type == SLIDING else 0
+            keys = table[np.stack(past_k[lo:c + 1], axis=1)] * ks[:, None, None]
+            vals = table[np.stack(past_v[lo:c + 1], axis=1)] * vs[:, None, None]
+            for h in range(Hq):
+                sc = keys[h // g] @ r["qrot"][0, h] / math.sqrt(D)
+                out = sps.softmax(sc) @ vals[h // g]
+                assert np.allclose(r["out"][0, h], out, rtol=1e-12, atol=1e-12), (layer_type, layout, c, h)
+                assert abs(r["lse"][0, h] - sps.logsumexp(sc)) < 1e-12
 
 
 # -------------------------------------------------------------- footprint --

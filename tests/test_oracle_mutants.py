@@ -25,17 +25,27 @@ MUTANTS = [
     ("sink sign", "exp(sink - *lse)", "exp(*lse - sink)"),
     ("sink applied twice", "out[d] *= f;", "out[d] *= f * f;"),
     ("gqa mapping transposed", "const int h = kv * g + hh;", "const int h = hh * Hkv + kv;"),
-    ("value row is the key", "load_row(vin, D, vals + n * D);", "load_row(kb, D, vals + n * D);"),
-    ("new key not rotated", "load_row(kb, D, keys + n * D);", "load_row(kin, D, keys + n * D);"),
+    ("value row is the key", "load_cached_row(L, vnew_bits, 0, vs, vals + n * D);",
+     "load_cached_row(L, knew_bits, 0, vs, vals + n * D);"),
+    ("new key not rotated", "(const void *)kq : (const void *)kb;", "(const void *)kq : (const void *)kin;"),
     ("ring slot off by one", "slot = c % (L->window - 1);", "slot = (c + 1) % (L->window - 1);"),
     ("roll keeps the oldest", "first = 1; /*", "first = 0; /*"),
     ("roll never shifts", "if (c >= L->window) {", "if (c > 1000000000) {"),
     ("bf16 truncates", "double r = rint(ldexp(a, 7 - E));", "double r = floor(ldexp(a, 7 - E));"),
-    ("bf16 exponent", "int E = e - 1;", "int E = e;"),
+    ("bf16 exponent", "int E = e - 1;           /* a = (2m)", "int E = e;           /* a = (2m)"),
     ("full cache keeps one less", "if (layer_type != ORC_SLIDING)\n        return context;",
      "if (layer_type != ORC_SLIDING)\n        return context > 0 ? context - 1 : 0;"),
     ("footprint counts K only", "int64_t per_entry = 2LL *", "int64_t per_entry = 1LL *"),
     ("gate sign", "exp(-(double)gate[", "exp((double)gate["),
+    ("e4m3 exponent bias", "ldexp((double)(8 + m), e - 10)", "ldexp((double)(8 + m), e - 9)"),
+    ("e4m3 subnormal quantum", "ldexp((double)m, -9)", "ldexp((double)m, -8)"),
+    ("e4m3 overflow to NaN", "if (v > 448.0)\n        return sign | 0x7E;", "if (v > 448.0)\n        return sign | 0x7F;"),
+    ("e4m3 ties away from zero", "double v = ldexp(rint(ldexp(a, 3 - E)), E - 3);",
+     "double v = ldexp(round(ldexp(a, 3 - E)), E - 3);"),
+    ("fp8 quantise multiplies by the scale", "orc_f64_to_e4m3(knew[d] / ks)", "orc_f64_to_e4m3(knew[d] * ks)"),
+    ("fp8 value scale dropped", "load_cached_row(L, vc, j, vs, vals + n * D);",
+     "load_cached_row(L, vc, j, 1.0, vals + n * D);"),
+    ("roll shift in elements, not bytes", "memmove(kc, kc + D * esize,", "memmove(kc, kc + D,"),
 ]
 
 
