@@ -40,6 +40,7 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 KV_ROW_BYTES = 2 * synth.HEAD_DIM * 2       # K row + V row, bf16, one kv head
+FP8_ROW_BYTES = 2 * synth.HEAD_DIM          # K row + V row, E4M3 codes, one kv head
 DEFAULT_WORKLOAD = "step28_b64_c512_32768"
 SECONDARY_WORKLOAD = "step28_b1_c4096"
 METRIC = "KV-read HBM GB/s (% of GB300 peak); µs per 28-layer decode step"
@@ -57,8 +58,8 @@ def scored_keys(layer_type: int, context: np.ndarray, layout: int) -> np.ndarray
     return np.minimum(context.astype(np.int64), keep) + 1
 
 
-def step_bytes(types, context, num_kv_heads, layout) -> int:
-    return int(sum(scored_keys(t, context, layout).sum() for t in types) * num_kv_heads * KV_ROW_BYTES)
+def step_bytes(types, context, num_kv_heads, layout, row_bytes=KV_ROW_BYTES) -> int:
+    return int(sum(scored_keys(t, context, layout).sum() for t in types) * num_kv_heads * row_bytes)
 
 
 def describe_layers(types) -> str:
@@ -212,11 +213,13 @@ def reduce_timing(elapsed_ms: float, units: float, world: int, device=None) -> t
 class Workload:
     """Device-resident inputs of one workload (caches, per-layer q/k/v, outputs)."""
 
-    def __init__(self, name: str, device, seed: int = 0, layout: int = synth.LAYOUT_AUTO):
+    def __init__(self, name: str, device, seed: int = 0, layout: int = synth.LAYOUT_AUTO, kv: str = "bf16"):
         import torch
         import full_gqa_decode_gb300 as hd
         spec = synth.WORKLOADS[name]
-        self.name, self.spec, self.layout = name, spec, layout
+        self.name, self.spec, self.layout, self.kv = name, spec, layout, kv
+        fp8 = kv == "fp8"
+        self.row_bytes = FP8_ROW_BYTES if fp8 else KV_ROW_BYTES
         self.types = list(spec["layer_types"])
         self.B, self.Hq, self.Hkv = spec["batch"], spec["num_q_heads"], spec["num_kv_heads"]
         D = synth.HEAD_DIM
@@ -225,7 +228,8 @@ class Workload:
         self.max_ctx = int(self.context.max())
         sink = synth.sink_vector(rng, spec["sink"], self.Hq)
         self.cfg = hd.Config(layer_types=self.types, num_q_heads=self.Hq, num_kv_heads=self.Hkv,
-                             cache_layout=layout, max_batch=self.B, max_context=self.max_ctx)
+                             cache_layout=layout, max_batch=self.B, max_context=self.max_ctx,
+                             kv_dtype=hd.HD_KV_FP8_E4M3 if fp8 else hd.HD_KV_BF16)
         self.ctx = hd.hybrid_decode_init(self.cfg)
         self.context_d = torch.from_numpy(self.context).to(device)
         self.sink = None if sink is None else sink.to(device)
@@ -233,10 +237,16 @@ class Workload:
         self.layers, self.io, self.io_gated = [], [], []
         for i, t in enumerate(self.types):
             cap = (synth.WINDOW - 1 if ring else synth.WINDOW) if t == synth.SLIDING else self.max_ctx + 1
-            kc = torch.empty(self.B, self.Hkv, cap, D, dtype=torch.bfloat16, device=device)
+            kc = torch.empty(self.B, self.Hkv, cap, D, dtype=torch.uint8 if fp8 else torch.bfloat16, device=device)
             vc = torch.empty_like(kc)
-            synth.cuda_normal_bf16_(kc, seed * 1000 + 2 * i + 1)
-            synth.cuda_normal_bf16_(vc, seed * 1000 + 2 * i + 2)
+            if fp8:  # per-layer, per-kv-head scales; codes of N(0,1) / scale
+                ks, vs = synth.kv_scales(rng, self.Hkv).to(device), synth.kv_scales(rng, self.Hkv).to(device)
+                synth.cuda_e4m3_codes_(kc, ks, seed * 1000 + 2 * i + 1)
+                synth.cuda_e4m3_codes_(vc, vs, seed * 1000 + 2 * i + 2)
+            else:
+                ks = vs = None
+                synth.cuda_normal_bf16_(kc, seed * 1000 + 2 * i + 1)
+                synth.cuda_normal_bf16_(vc, seed * 1000 + 2 * i + 2)
             g = torch.Generator(device=device)
             g.manual_seed(seed * 1000 + 500 + i)
             q = torch.randn(self.B, self.Hq, D, generator=g, device=device).to(torch.bfloat16)
@@ -244,19 +254,20 @@ class Workload:
             v = torch.randn(self.B, self.Hkv, D, generator=g, device=device).to(torch.bfloat16)
             out = torch.empty(self.B, self.Hq, D, dtype=torch.bfloat16, device=device)
             lse = torch.empty(self.B, self.Hq, dtype=torch.float32, device=device)
-            cache = hd.kv_cache(kc, vc)
-            self.layers.append(dict(q=q, k=k, v=v, kc=kc, vc=vc, out=out, lse=lse, cache=cache))
+            cache = hd.kv_cache(kc, vc, ks, vs)
+            self.layers.append(dict(q=q, k=k, v=v, kc=kc, vc=vc, out=out, lse=lse, cache=cache,
+                                    k_scale=ks, v_scale=vs))
             self.io.append(hd.layer_io(q, k, v, cache, self.sink, out, lse))
             # per-step output-gate logits N(0, 1) for the gated variant of the step
             gate = torch.randn(self.B, self.Hq, generator=g, device=device)
             self.layers[-1]["gate"] = gate
             self.io_gated.append(hd.layer_io(q, k, v, cache, self.sink, out, lse, gate=gate))
-        self.bytes = step_bytes(self.types, self.context, self.Hkv, layout)
+        self.bytes = step_bytes(self.types, self.context, self.Hkv, layout, self.row_bytes)
         full_idx = [i for i, t in enumerate(self.types) if t == synth.FULL]
         self.full_layer_bytes = (int(scored_keys(synth.FULL, self.context, layout).sum()) * self.Hkv
-                                 * KV_ROW_BYTES) if full_idx else 0
+                                 * self.row_bytes) if full_idx else 0
         self.sliding_layer_bytes = (int(scored_keys(synth.SLIDING, self.context, layout).sum()) * self.Hkv
-                                    * KV_ROW_BYTES)
+                                    * self.row_bytes)
 
     def step(self, stream=None, gated=False):
         import full_gqa_decode_gb300 as hd
@@ -287,7 +298,8 @@ def time_steps(run, steps: int, warmup: int, world: int, device) -> float:
 
 def oracle_sample(layer_caches, context, types, Hq, Hkv, sink, rng, threads, layout=synth.LAYOUT_RING):
     """Times the oracle on one [S,S,S,F] block of the step for the given sequences.
-    layer_caches: per layer (kc, vc) uint16 arrays [B, Hkv, cap, D]. Returns (seconds, bytes)."""
+    layer_caches: per layer (kc, vc) uint16 arrays [B, Hkv, cap, D], or (kc, vc, k_scale,
+    v_scale) with uint8 E4M3 codes. Returns (seconds, bytes)."""
     import oracle
     orc = oracle.load()
     D = synth.HEAD_DIM
@@ -295,7 +307,10 @@ def oracle_sample(layer_caches, context, types, Hq, Hkv, sink, rng, threads, lay
     jobs = []
     for li, t in enumerate(types):
         rot, theta = synth.ROPE[t]
-        kc, vc = layer_caches[li]
+        kc, vc = layer_caches[li][:2]
+        scales = {}
+        if kc.dtype == np.uint8:
+            scales = dict(k_scale=layer_caches[li][2], v_scale=layer_caches[li][3])
         for b in range(B):
             q = synth.bits(synth.normal_bf16(rng, (1, Hq, D)))
             k = synth.bits(synth.normal_bf16(rng, (1, Hkv, D)))
@@ -303,8 +318,9 @@ def oracle_sample(layer_caches, context, types, Hq, Hkv, sink, rng, threads, lay
             jobs.append(dict(layer_type=t, layout=layout, window=synth.WINDOW, rotary_dim=rot,
                              rope_theta=theta, context=context[b:b + 1], q=q, k=k, v=v,
                              kcache=np.ascontiguousarray(kc[b:b + 1]), vcache=np.ascontiguousarray(vc[b:b + 1]),
-                             sink=sink))
-    nbytes = step_bytes(types, context, Hkv, layout)
+                             sink=sink, **scales))
+    row = FP8_ROW_BYTES if layer_caches[0][0].dtype == np.uint8 else KV_ROW_BYTES
+    nbytes = step_bytes(types, context, Hkv, layout, row)
     t0 = time.perf_counter()
     with cf.ThreadPoolExecutor(threads) as ex:   # ctypes releases the GIL in the oracle
         list(ex.map(lambda j: orc.decode_layer(**j), jobs))
@@ -382,7 +398,7 @@ def run_ours(args, world, rank, local) -> int:
     torch.cuda.set_device(device)
     peaks = measured_peaks()
     layout = synth.LAYOUT_ROLL if args.layout == "roll" else synth.LAYOUT_RING
-    wl = Workload(args.workload, device, seed=rank, layout=layout)
+    wl = Workload(args.workload, device, seed=rank, layout=layout, kv=args.kv)
     consumer = hd.HD_CONSUMER_TENSOR_CORE if args.consumer == "tensor-core" else hd.HD_CONSUMER_CUDA_CORE
     hd.hybrid_decode_set_consumer(wl.ctx, consumer)
     torch.cuda.synchronize()
@@ -445,18 +461,20 @@ def run_ours(args, world, rank, local) -> int:
 
     result = None
     if rank == 0:
+        fp8 = fp8_step(device, args, consumer, layout, plain_ms) if args.kv == "bf16" and args.secondary else None
         cpu = cpu_baseline(wl, device)
         secondary = secondary_batch1(device, args, consumer) if args.secondary else None
         result = {"metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
                   "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
                   "us_per_step": round(ms_max * 1e3, 1), "higher_is_better": True, "scaling": "weak",
-                  "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+                  "vs_baseline": None, "dtype": "bf16" if args.kv == "bf16" else "fp8_e4m3 KV, f16 MMA",
+                  "data": "synthetic",
                   "frac_of_peak_hbm": round(gbs / peaks["hbm_gbs"], 4),
                   "config": {"workload": wl.name, "global_batch": wl.B * world, "per_gpu_batch": wl.B,
                              "layers": describe_layers(wl.types), "heads": f"{wl.Hq} q / {wl.Hkv} kv",
                              "head_dim": synth.HEAD_DIM, "contexts": describe_lengths(wl.spec["lengths"]),
                              "max_context": wl.max_ctx, "kv_bytes_per_step": wl.bytes,
-                             "sliding_layout": args.layout,
+                             "sliding_layout": args.layout, "kv_dtype": args.kv,
                              "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world}"},
                   "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                   "gpu_launches": int(n1 - n0), "clocks": clk}
@@ -464,6 +482,8 @@ def run_ours(args, world, rank, local) -> int:
                                  "value": round(wl.bytes / (gated_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                                  "ungated_ms_per_step": round(plain_ms, 4),
                                  "overhead_vs_ungated": round(gated_ms / plain_ms - 1.0, 4)}
+        if fp8:
+            result["fp8_kv"] = fp8
         if secondary:
             result["secondary"] = secondary
         print(json.dumps(result), flush=True)
@@ -529,7 +549,11 @@ def cpu_baseline(wl, device) -> dict:
     caches = []
     for i in block:
         l = wl.layers[i]
-        caches.append((synth.bits(l["kc"]), synth.bits(l["vc"])))
+        if wl.kv == "fp8":
+            caches.append((synth.bits(l["kc"]), synth.bits(l["vc"]), l["k_scale"].cpu().numpy(),
+                           l["v_scale"].cpu().numpy()))
+        else:
+            caches.append((synth.bits(l["kc"]), synth.bits(l["vc"])))
     sink = None if wl.sink is None else wl.sink.cpu().numpy()
     threads = cpu_threads()
     layout = synth.LAYOUT_ROLL if wl.layout == synth.LAYOUT_ROLL else synth.LAYOUT_RING
@@ -538,6 +562,38 @@ def cpu_baseline(wl, device) -> dict:
     return {"value": round(nbytes / secs / 1e9, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
             "sample": f"layers 0-3 ([sliding x3, full]) of the step over all {len(wl.context)} sequences, "
                       f"{nbytes / 1e9:.2f} GB scored KV, {secs:.1f} s"}
+
+
+def fp8_step(device, args, consumer, layout, bf16_ms) -> dict:
+    """The same step with E4M3 caches (per-kv-head scales): step time, KV GB/s over
+    the E4M3 bytes, and the full-layer kernel alone (events in a separate pass)."""
+    import torch
+    import full_gqa_decode_gb300 as hd
+    wl = Workload(args.workload, device, seed=0, layout=layout, kv="fp8")
+    hd.hybrid_decode_set_consumer(wl.ctx, consumer)
+    ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
+    hd.hybrid_decode_set_profiling(wl.ctx, hd.HD_PROFILE_FULL)
+    for _ in range(3):
+        wl.step()
+    full_ms, full_n = hd.hybrid_decode_profile(wl.ctx, hd.HD_FULL)
+    hd.hybrid_decode_set_profiling(wl.ctx, 0)
+    flags = hd.hybrid_decode_device_errors(wl.ctx)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x} in the FP8 step")
+    peak = measured_peaks()["hbm_gbs"]
+    res = {"ms_per_step": round(ms, 4), "us_per_step": round(ms * 1e3, 1),
+           "value": round(wl.bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "kv_bytes_per_step": wl.bytes,
+           "speedup_vs_bf16_step": round(bf16_ms / ms, 3)}
+    if full_n:
+        avg = full_ms / full_n
+        res["full_layer_kernel"] = {"achieved": round(wl.full_layer_bytes / (avg * 1e-3) / 1e9, 1), "unit": "GB/s",
+                                    "frac": round(wl.full_layer_bytes / (avg * 1e-3) / 1e9 / peak, 4),
+                                    "avg_launch_ms": round(avg, 4),
+                                    "algorithmic_bytes_per_launch": wl.full_layer_bytes}
+    wl.ctx.close()
+    del wl
+    torch.cuda.empty_cache()
+    return res
 
 
 def secondary_batch1(device, args, consumer) -> dict:
@@ -576,6 +632,8 @@ def main(argv=None) -> int:
                     help="inner loop of the attention kernels")
     ap.add_argument("--layout", choices=["ring", "roll"], default="ring",
                     help="cache layout of the sliding layers")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="cache element type (fp8: E4M3 codes with per-kv-head scales)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -25,6 +25,7 @@ HD_SLIDING, HD_FULL = 0, 1
 HD_LAYOUT_AUTO, HD_LAYOUT_RING, HD_LAYOUT_ROLL = 0, 1, 2
 HD_CONSUMER_CUDA_CORE, HD_CONSUMER_TENSOR_CORE = 0, 1
 HD_PROFILE_SLIDING, HD_PROFILE_FULL = 1 << HD_SLIDING, 1 << HD_FULL
+HD_KV_BF16, HD_KV_FP8_E4M3 = 0, 1
 STATUS = {0: "HD_OK", 1: "HD_ERR_INVALID_ARG", 2: "HD_ERR_UNSUPPORTED", 3: "HD_ERR_CAPACITY",
           4: "HD_ERR_CUDA", 5: "HD_ERR_STATE"}
 DEVERR = {1: "HD_DEVERR_CONTEXT_NEGATIVE", 2: "HD_DEVERR_CONTEXT_CAPACITY",
@@ -49,12 +50,12 @@ class hd_config(ctypes.Structure):
                 ("rotary_dim_sliding", ctypes.c_int32), ("rotary_dim_full", ctypes.c_int32),
                 ("rope_theta_sliding", ctypes.c_double), ("rope_theta_full", ctypes.c_double),
                 ("cache_layout", ctypes.c_int32), ("max_batch", ctypes.c_int32),
-                ("max_context", ctypes.c_int32)]
+                ("max_context", ctypes.c_int32), ("kv_dtype", ctypes.c_int32)]
 
 
 class hd_kv_cache(ctypes.Structure):
     _fields_ = [("k", ctypes.c_void_p), ("v", ctypes.c_void_p), ("seq_stride", ctypes.c_int64),
-                ("capacity", ctypes.c_int32)]
+                ("capacity", ctypes.c_int32), ("k_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p)]
 
 
 class hd_layer_io(ctypes.Structure):
@@ -155,6 +156,7 @@ class Config:
     cache_layout: int = HD_LAYOUT_AUTO
     max_batch: int = 1
     max_context: int = 4096
+    kv_dtype: int = HD_KV_BF16
     _types: object = field(default=None, repr=False)
 
     def to_c(self) -> hd_config:
@@ -162,21 +164,41 @@ class Config:
         return hd_config(len(self.layer_types), self._types, self.num_q_heads, self.num_kv_heads,
                          self.head_dim, self.sliding_window, self.rotary_dim_sliding,
                          self.rotary_dim_full, self.rope_theta_sliding, self.rope_theta_full,
-                         self.cache_layout, self.max_batch, self.max_context)
+                         self.cache_layout, self.max_batch, self.max_context, self.kv_dtype)
 
 
-def kv_cache(k: torch.Tensor, v: torch.Tensor) -> hd_kv_cache:
-    """Describe a cache pair shaped [batch, num_kv_heads, capacity, head_dim] (bf16, CUDA)."""
+_FP8_CACHE_TYPES = (torch.uint8, torch.float8_e4m3fn)
+
+
+def kv_cache(k: torch.Tensor, v: torch.Tensor, k_scale: torch.Tensor | None = None,
+             v_scale: torch.Tensor | None = None) -> hd_kv_cache:
+    """Describe a cache pair shaped [batch, num_kv_heads, capacity, head_dim] on CUDA:
+    bf16, or E4M3 codes (uint8 or float8_e4m3fn) with fp32 ``k_scale``/``v_scale``
+    of shape [num_kv_heads] on the same device (the context's kv_dtype must match)."""
     if k.shape != v.shape or k.dim() != 4 or k.stride() != v.stride():
         raise ValueError("k and v caches must share a [batch, kv_heads, capacity, head_dim] layout")
-    if k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
-        raise ValueError("caches must be bf16")
+    fp8 = k.dtype in _FP8_CACHE_TYPES
+    if fp8:
+        if v.dtype not in _FP8_CACHE_TYPES:
+            raise ValueError("k and v caches must have the same element type")
+        for name, sc in (("k_scale", k_scale), ("v_scale", v_scale)):
+            if sc is None or sc.dtype != torch.float32 or tuple(sc.shape) != (k.shape[1],):
+                raise ValueError(f"an FP8 cache needs {name} as float32 of shape ({k.shape[1]},)")
+            if sc.device != k.device or not sc.is_contiguous():
+                raise ValueError(f"{name} must be contiguous and on the cache's device")
+    else:
+        if k.dtype != torch.bfloat16 or v.dtype != torch.bfloat16:
+            raise ValueError("caches must be bf16, or E4M3 codes with scales")
+        if k_scale is not None or v_scale is not None:
+            raise ValueError("scales belong to FP8 caches only")
     if k.stride(3) != 1 or k.stride(2) != k.shape[3] or k.stride(1) != k.shape[2] * k.shape[3]:
         raise ValueError("each sequence's cache must be contiguous [kv_heads, capacity, head_dim]")
     if not k.is_cuda or not v.is_cuda:
         raise ValueError("caches must be CUDA tensors")
-    c = hd_kv_cache(k.data_ptr(), v.data_ptr(), k.stride(0), k.shape[2])
+    c = hd_kv_cache(k.data_ptr(), v.data_ptr(), k.stride(0), k.shape[2],
+                    k_scale.data_ptr() if fp8 else None, v_scale.data_ptr() if fp8 else None)
     c.batch = k.shape[0]  # sequences the tensors hold; calls may not pass a larger batch
+    c.keep = (k_scale, v_scale)  # the scales must outlive the descriptor
     return c
 
 

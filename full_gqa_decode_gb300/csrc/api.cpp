@@ -77,8 +77,9 @@ struct hd_ctx {
     float *part_o = nullptr;
     float2 *part_ml = nullptr;
     int64_t part_slots = 0;              // capacity in (sequence, chunk) pairs
-    __nv_bfloat16 *stage_k = nullptr;    // [num_layers][max_batch][Hkv][D]
-    __nv_bfloat16 *stage_v = nullptr;
+    uint8_t *stage_k = nullptr;          // [num_layers][max_batch][Hkv][D] entries of the cache type
+    uint8_t *stage_v = nullptr;
+    int kv_type = KV_BF16;
     int32_t *counters = nullptr;         // [max_batch][Hkv] chunk tickets, zero between calls
     int32_t *err = nullptr;
     int consumer = CONSUMER_MMA;
@@ -116,20 +117,22 @@ int sliding_capacity(const hd_ctx *ctx) {
 }
 
 // Encodes the 4-D view {D, capacity, Hkv, batch} of one cache tensor with
-// 64 x kStageKeys boxes and the 128-byte swizzle the consumers index by.
+// (128 bytes) x kStageKeys boxes and the 128-byte swizzle the consumers index by.
 bool encode_cache_map(CUtensorMap *map, const void *base, int64_t seq_stride, int capacity,
-                      int num_kv_heads, int batch) {
+                      int num_kv_heads, int batch, int kv_type) {
     auto fn = encode_fn();
     if (!fn) return false;
+    const cuuint64_t es = (cuuint64_t)kv_elem_bytes(kv_type);
     const cuuint64_t dims[4] = {(cuuint64_t)kHeadDim, (cuuint64_t)capacity,
                                 (cuuint64_t)num_kv_heads, (cuuint64_t)batch};
-    const cuuint64_t strides[3] = {(cuuint64_t)kHeadDim * 2, (cuuint64_t)capacity * kHeadDim * 2,
-                                   (cuuint64_t)seq_stride * 2};
-    const cuuint32_t box[4] = {(cuuint32_t)kBoxCols, (cuuint32_t)kStageKeys, 1, 1};
+    const cuuint64_t strides[3] = {(cuuint64_t)kHeadDim * es, (cuuint64_t)capacity * kHeadDim * es,
+                                   (cuuint64_t)seq_stride * es};
+    const cuuint32_t box[4] = {(cuuint32_t)kv_box_cols(kv_type), (cuuint32_t)kStageKeys, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
-    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(base), dims,
-                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    CUresult r = fn(map, kv_type == KV_FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
+                    const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
 
@@ -138,8 +141,8 @@ hd_status maps_for(hd_ctx *ctx, int layer, const hd_kv_cache &c, int batch, cons
     MapCacheEntry &e = ctx->maps[layer];
     if (e.k != c.k || e.v != c.v || e.seq_stride != c.seq_stride || e.capacity != c.capacity ||
         e.batch != batch) {
-        if (!encode_cache_map(&e.kmap, c.k, c.seq_stride, c.capacity, ctx->cfg.num_kv_heads, batch) ||
-            !encode_cache_map(&e.vmap, c.v, c.seq_stride, c.capacity, ctx->cfg.num_kv_heads, batch)) {
+        if (!encode_cache_map(&e.kmap, c.k, c.seq_stride, c.capacity, ctx->cfg.num_kv_heads, batch, ctx->kv_type) ||
+            !encode_cache_map(&e.vmap, c.v, c.seq_stride, c.capacity, ctx->cfg.num_kv_heads, batch, ctx->kv_type)) {
             e.k = e.v = nullptr;
             return HD_ERR_CUDA;
         }
@@ -156,7 +159,9 @@ hd_status maps_for(hd_ctx *ctx, int layer, const hd_kv_cache &c, int batch, cons
 
 hd_status check_cache(const hd_ctx *ctx, const hd_kv_cache &c) {
     if (!c.k || !c.v || !aligned16(c.k) || !aligned16(c.v)) return HD_ERR_INVALID_ARG;
-    if (c.capacity <= 0 || c.seq_stride % 8 != 0) return HD_ERR_INVALID_ARG;
+    if (c.capacity <= 0 || (c.seq_stride * kv_elem_bytes(ctx->kv_type)) % 16 != 0) return HD_ERR_INVALID_ARG;
+    const bool fp8 = ctx->kv_type == KV_FP8;
+    if (fp8 != (c.k_scale != nullptr) || fp8 != (c.v_scale != nullptr)) return HD_ERR_INVALID_ARG;
     if (c.seq_stride < (int64_t)ctx->cfg.num_kv_heads * c.capacity * kHeadDim)
         return HD_ERR_INVALID_ARG;
     return HD_OK;
@@ -250,15 +255,18 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     a.q_rot = L.q_rot;
     a.table = tab.data;
     a.rotary_dim = tab.rotary_dim;
-    a.new_k = static_cast<const __nv_bfloat16 *>(L.new_k);
-    a.new_v = static_cast<const __nv_bfloat16 *>(L.new_v);
+    a.new_k = L.new_k;
+    a.new_v = L.new_v;
     a.new_kind = L.new_kind;
     a.commit = L.commit;
     a.key_set = L.key_set;
-    a.cache_k = static_cast<__nv_bfloat16 *>(L.cache.k);
-    a.cache_v = static_cast<__nv_bfloat16 *>(L.cache.v);
+    a.cache_k = L.cache.k;
+    a.cache_v = L.cache.v;
     a.seq_stride = L.cache.seq_stride;
     a.capacity = L.cache.capacity;
+    a.kv_type = ctx->kv_type;
+    a.k_scale = L.cache.k_scale;
+    a.v_scale = L.cache.v_scale;
     a.sink = L.sink;
     a.gate = L.gate;
     a.out = static_cast<__nv_bfloat16 *>(L.out);
@@ -289,8 +297,8 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     return HD_OK;
 }
 
-const __nv_bfloat16 *stage_row(const hd_ctx *ctx, const __nv_bfloat16 *base, int layer) {
-    return base + (size_t)layer * ctx->cfg.max_batch * ctx->cfg.num_kv_heads * kHeadDim;
+uint8_t *stage_row(const hd_ctx *ctx, uint8_t *base, int layer) {
+    return base + (size_t)layer * ctx->cfg.max_batch * ctx->cfg.num_kv_heads * kHeadDim * kv_elem_bytes(ctx->kv_type);
 }
 
 // Host checks shared by the attention entry points and decode_step.
@@ -339,6 +347,7 @@ hd_status hd_validate_config(const hd_config *cfg) {
     if (cfg->cache_layout != HD_LAYOUT_AUTO && cfg->cache_layout != HD_LAYOUT_RING &&
         cfg->cache_layout != HD_LAYOUT_ROLL)
         return HD_ERR_INVALID_ARG;
+    if (cfg->kv_dtype != HD_KV_BF16 && cfg->kv_dtype != HD_KV_FP8_E4M3) return HD_ERR_INVALID_ARG;
     if (cfg->sliding_window < 2 || cfg->max_batch <= 0 || cfg->max_context < 0)
         return HD_ERR_INVALID_ARG;
     if (cfg->max_batch > 65535) return HD_ERR_CAPACITY;
@@ -380,6 +389,7 @@ hd_status hybrid_decode_init(const hd_config *cfg, hd_ctx **out_ctx) {
     ctx->num_sms = prop.multiProcessorCount;
     ctx->group = cfg->num_q_heads / cfg->num_kv_heads;
     ctx->sliding_layout = cfg->cache_layout == HD_LAYOUT_ROLL ? HD_LAYOUT_ROLL : HD_LAYOUT_RING;
+    ctx->kv_type = cfg->kv_dtype == HD_KV_FP8_E4M3 ? KV_FP8 : KV_BF16;
     ctx->maps.resize(cfg->num_layers);
 
     bool any_sliding = false, any_full = false;
@@ -409,9 +419,8 @@ hd_status hybrid_decode_init(const hd_config *cfg, hd_ctx **out_ctx) {
               cudaMemset(ctx->counters, 0, (size_t)B * Hkv * sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&ctx->err, sizeof(int32_t)) == cudaSuccess &&
               cudaMemset(ctx->err, 0, sizeof(int32_t)) == cudaSuccess;
-    const size_t stage = (size_t)cfg->num_layers * B * Hkv * kHeadDim;
-    ok = ok && cudaMalloc(&ctx->stage_k, stage * sizeof(__nv_bfloat16)) == cudaSuccess &&
-         cudaMalloc(&ctx->stage_v, stage * sizeof(__nv_bfloat16)) == cudaSuccess;
+    const size_t stage = (size_t)cfg->num_layers * B * Hkv * kHeadDim * kv_elem_bytes(ctx->kv_type);
+    ok = ok && cudaMalloc(&ctx->stage_k, stage) == cudaSuccess && cudaMalloc(&ctx->stage_v, stage) == cudaSuccess;
     if (!ok) {
         free_ctx(ctx);
         return HD_ERR_CUDA;
@@ -453,15 +462,17 @@ hd_status rope_append_kv(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_
     a.key_set = key_set;
     a.window = ctx->cfg.sliding_window;
     a.max_context = ctx->cfg.max_context;
+    a.kv_type = ctx->kv_type;
+    a.k_scale = cache.k_scale;
+    a.v_scale = cache.v_scale;
     if (key_set == KEYS_RING) {
-        const size_t off = (size_t)layer * ctx->cfg.max_batch * ctx->cfg.num_kv_heads * kHeadDim;
-        a.dst_k = ctx->stage_k + off;
-        a.dst_v = ctx->stage_v + off;
+        a.dst_k = stage_row(ctx, ctx->stage_k, layer);
+        a.dst_v = stage_row(ctx, ctx->stage_v, layer);
         a.seq_stride = (int64_t)ctx->cfg.num_kv_heads * kHeadDim;
         a.capacity = 1;
     } else {
-        a.dst_k = static_cast<__nv_bfloat16 *>(cache.k);
-        a.dst_v = static_cast<__nv_bfloat16 *>(cache.v);
+        a.dst_k = cache.k;
+        a.dst_v = cache.v;
         a.seq_stride = cache.seq_stride;
         a.capacity = cache.capacity;
     }
@@ -572,8 +583,11 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
             r.k = static_cast<const __nv_bfloat16 *>(io.k);
             r.v = static_cast<const __nv_bfloat16 *>(io.v);
             r.table = ctx->table_sliding.data;
-            r.dst_k = static_cast<__nv_bfloat16 *>(io.cache.k);
-            r.dst_v = static_cast<__nv_bfloat16 *>(io.cache.v);
+            r.dst_k = io.cache.k;
+            r.dst_v = io.cache.v;
+            r.kv_type = ctx->kv_type;
+            r.k_scale = io.cache.k_scale;
+            r.v_scale = io.cache.v_scale;
             r.seq_stride = io.cache.seq_stride;
             r.capacity = io.cache.capacity;
             r.err = ctx->err;

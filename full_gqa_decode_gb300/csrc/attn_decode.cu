@@ -30,6 +30,9 @@
 // -- merges all partials and the new entry, writes out/lse, stores the new
 // K/V entry (ring slot or append) and resets the counter.  Nothing waits on
 // another CTA.
+#include <cuda_fp16.h>
+
+#include "e4m3.cuh"
 #include "hd_internal.h"
 
 namespace hd {
@@ -138,6 +141,38 @@ __device__ __forceinline__ void mma_1688(float (&d)[4], uint32_t a0, uint32_t a1
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(b0));
 }
+// The same two shapes with f16 operands (the FP8 cache path: E4M3 converts to
+// f16 exactly).
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma_1688_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0));
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+// Eight E4M3 codes (little-endian in two words) to floats.
+__device__ __forceinline__ void unpack_e4m3x8(const uint2 &r, float (&f)[8]) {
+    const uint32_t w[2] = {r.x, r.y};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t h = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1))));
+        const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+        f[2 * i] = v.x;
+        f[2 * i + 1] = v.y;
+    }
+}
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
     return *reinterpret_cast<uint32_t *>(&v);
@@ -150,8 +185,9 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &r, float (&f)[8]) {
         f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
 }
-// Byte offset of 16-byte chunk c (0..31) of row r in a stage's K or V region:
-// box c/8, swizzled chunk (c%8)^(r%8) inside the 128-byte row.
+// Byte offset of 16-byte chunk c (0..31 for bf16, 0..15 for E4M3) of row r in
+// a stage's K or V region: box c/8, swizzled chunk (c%8)^(r%8) inside the
+// 128-byte row.
 __device__ __forceinline__ uint32_t tile_offset(int r, int c) {
     return (c >> 3) * kBoxBytes + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
 }
@@ -165,20 +201,25 @@ __device__ __forceinline__ float f64_to_bf16_value(double x) {
     return __bfloat162float(__float2bfloat16_rn(t));
 }
 
-// Loads what the combine needs from global memory: the new entry (raw k for
-// NEW_ROTATE, the staged key otherwise), its value row, the rotary row at
-// position c, and the group's sink values and output-gate logits.
-// Threads [0, nthreads) share the work.
-template <int G>
+// Loads what the combine needs from global memory: the new entry (raw k and
+// v for NEW_ROTATE, the staged entry otherwise: bf16 values, or E4M3 codes
+// kept in code_s [2][256]), its rotary row at position c, and the group's
+// sink values and output-gate logits.  Threads [0, nthreads) share the work.
+template <int G, int KV>
 __device__ __forceinline__ void load_combine_inputs(const LayerArgs &a, int b, int kvh, int c, float *kraw_s,
                                                     float *vnew_s, float2 *tab_s, float *sink_s, float *gate_s,
-                                                    int nthreads) {
+                                                    uint8_t *code_s, int nthreads) {
     const int t = threadIdx.x;
     if (a.new_kind != NEW_NONE) {
         const size_t e = ((size_t)b * a.num_kv_heads + kvh) * kHeadDim;
         for (int d = t; d < kHeadDim; d += nthreads) {
-            kraw_s[d] = __bfloat162float(a.new_k[e + d]);
-            vnew_s[d] = __bfloat162float(a.new_v[e + d]);
+            if (KV == KV_FP8 && a.new_kind == NEW_STAGED) {
+                code_s[d] = static_cast<const uint8_t *>(a.new_k)[e + d];
+                code_s[kHeadDim + d] = static_cast<const uint8_t *>(a.new_v)[e + d];
+            } else {
+                kraw_s[d] = __bfloat162float(static_cast<const __nv_bfloat16 *>(a.new_k)[e + d]);
+                vnew_s[d] = __bfloat162float(static_cast<const __nv_bfloat16 *>(a.new_v)[e + d]);
+            }
         }
         if (a.new_kind == NEW_ROTATE)
             for (int j = t; j < (a.rotary_dim >> 1); j += nthreads)
@@ -214,12 +255,23 @@ __device__ __forceinline__ int cached_keys(const LayerArgs &a, int c, int *bit) 
 // ---------------------------------------------------------- the consumers --
 
 // CUDA-core consumer: lane owns dims [8*lane, 8*lane+8) of every row; each
-// score is a warp-shuffle reduction.
-template <int G>
+// score is a warp-shuffle reduction.  With an E4M3 cache the rows hold codes:
+// scores take the K scale after the reduction and the output stays in V-code
+// units (the combine applies the V scale).
+template <int G, int KV>
 struct FmaConsumer {
     float qv[G][8], m[G], l[G], acc[G][8];
+    float kscale;
 
-    __device__ void init(const float *q_s, int lane) {
+    __device__ void load_row(const uint8_t *st, int row, int lane, float (&f)[8]) const {
+        if (KV == KV_FP8)
+            unpack_e4m3x8(*reinterpret_cast<const uint2 *>(st + tile_offset(row, lane >> 1) + (lane & 1) * 8), f);
+        else
+            unpack_bf16x8(*reinterpret_cast<const uint4 *>(st + tile_offset(row, lane)), f);
+    }
+
+    __device__ void init(const float *q_s, int lane, float k_scale) {
+        kscale = k_scale;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
 #pragma unroll
@@ -235,7 +287,6 @@ struct FmaConsumer {
     // Rows [row0, row0 + kKeysPerWarp) of a stage; the first nvalid are keys.
     __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane) {
         constexpr int KB = G >= 8 ? 4 : kKeysPerWarp;  // keeps scores, q and acc in registers
-        const int c = lane;
 #pragma unroll
         for (int sb = 0; sb < kKeysPerWarp; sb += KB) {
             const int nv = nvalid - sb;
@@ -245,7 +296,7 @@ struct FmaConsumer {
             for (int r = 0; r < KB; ++r) {
                 const int row = row0 + sb + r;
                 float kf[8];
-                unpack_bf16x8(*reinterpret_cast<const uint4 *>(kst + tile_offset(row, c)), kf);
+                load_row(kst, row, lane, kf);
 #pragma unroll
                 for (int h = 0; h < G; ++h) {
                     float d = 0.f;
@@ -253,6 +304,7 @@ struct FmaConsumer {
                     for (int i = 0; i < 8; ++i) d = fmaf(qv[h][i], kf[i], d);
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+                    if (KV == KV_FP8) d *= kscale;
                     sc[r][h] = (r < nv) ? d : -INFINITY;
                 }
             }
@@ -278,7 +330,7 @@ struct FmaConsumer {
             for (int r = 0; r < KB; ++r) {
                 if (r < nv) {  // rows past the key set may hold NaN: never touch them
                     float vf[8];
-                    unpack_bf16x8(*reinterpret_cast<const uint4 *>(vst + tile_offset(row0 + sb + r, c)), vf);
+                    load_row(vst, row0 + sb + r, lane, vf);
 #pragma unroll
                     for (int h = 0; h < G; ++h)
 #pragma unroll
@@ -315,7 +367,7 @@ struct MmaConsumer {
     float o[16][4];   // O^T tile mt: rows dims 16mt + gid (+8), cols heads 2*t4 (+1)
     float m_run, l_run;  // for head gid; l_run sums this lane's keys only
 
-    __device__ void init(const float *q_s, int lane) {
+    __device__ void init(const float *q_s, int lane, float) {
         const int gid = lane >> 2, t4 = lane & 3;
 #pragma unroll
         for (int ks = 0; ks < 16; ++ks) {
@@ -420,16 +472,160 @@ struct MmaConsumer {
     }
 };
 
+// Tensor-core consumer for an E4M3 cache.  Codes convert exactly to f16
+// (cvt.rn.f16x2.e4m3x2), so both products run as f16 MMAs with fp32
+// accumulation; q is split into an f16 high and low part as above.
+//
+// S = Q K^T: lane (gid, t4) holds key gid.  It reads four 16-byte chunks of
+// the key row, chunk 2*t4 + (p & 1) + 8*(p >> 1) at step p, so that the eight
+// lanes of each shared-memory phase (two keys) hit eight distinct chunks after
+// the swizzle.  Word j of a chunk is the B fragment of k-step 4p + j (dims
+// 16*chunk + 4j .. +3, split as (d, d+1) and (d+2, d+3)); the q fragments
+// are built in init with the same dim order, which leaves every dot product
+// unchanged.
+//
+// O^T += V^T P^T: lane (gid, t4) reads keys 2*t4 and 2*t4+1, chunks gid and
+// 8 + gid; byte_perm pairs the two keys' bytes of one dim, which is the
+// E4M3x2 input of one A register.  Tile mt covers, on row gid, dim
+// 128*(mt / 8) + 16*gid + 2*(mt % 8) and, on row gid + 8, the next dim.
+template <int G>
+struct Fp8MmaConsumer {
+    uint32_t qa[16][4];
+    float o[16][4];
+    float m_run, l_run, kscale;
+
+    __device__ void init(const float *q_s, int lane, float k_scale) {
+        const int gid = lane >> 2, t4 = lane & 3;
+        kscale = k_scale;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int chunk = 2 * t4 + (p & 1) + 8 * (p >> 1);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                uint32_t r[4] = {0u, 0u, 0u, 0u};
+                if (gid < G) {
+                    const float *qh = q_s + gid * kHeadDim + 16 * chunk + 4 * j;
+                    const float x0 = qh[0], x1 = qh[1], x2 = qh[2], x3 = qh[3];
+                    const float h0 = __half2float(__float2half_rn(x0));
+                    const float h1 = __half2float(__float2half_rn(x1));
+                    const float h2 = __half2float(__float2half_rn(x2));
+                    const float h3 = __half2float(__float2half_rn(x3));
+                    r[0] = pack_f16(h0, h1);
+                    r[1] = pack_f16(x0 - h0, x1 - h1);
+                    r[2] = pack_f16(h2, h3);
+                    r[3] = pack_f16(x2 - h2, x3 - h3);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) qa[4 * p + j][i] = r[i];
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 16; ++mt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[mt][j] = 0.f;
+        m_run = -INFINITY;
+        l_run = 0.f;
+    }
+
+    __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane) {
+        const int gid = lane >> 2, t4 = lane & 3;
+        float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int chunk = 2 * t4 + (p & 1) + 8 * (p >> 1);
+            const uint4 kw = *reinterpret_cast<const uint4 *>(kst + tile_offset(row0 + gid, chunk));
+            const uint32_t w[4] = {kw.x, kw.y, kw.z, kw.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] & 0xFFFFu));
+                const uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] >> 16));
+                if (j & 1)
+                    mma_16816_f16(s2, qa[4 * p + j], b0, b1);
+                else
+                    mma_16816_f16(s, qa[4 * p + j], b0, b1);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s[j] += s2[j];
+        const bool ok0 = gid < G && 2 * t4 < nvalid, ok1 = gid < G && 2 * t4 + 1 < nvalid;
+        const float s0 = ok0 ? (s[0] + s[2]) * kscale : -INFINITY;
+        const float s1 = ok1 ? (s[1] + s[3]) * kscale : -INFINITY;
+        float mx = fmaxf(s0, s1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m_run, mx);
+        const float alpha = (mn == -INFINITY) ? 1.f : fast_exp2(m_run - mn);
+        const float p0 = ok0 ? fast_exp2(s0 - mn) : 0.f;
+        const float p1 = ok1 ? fast_exp2(s1 - mn) : 0.f;
+        l_run = fmaf(l_run, alpha, p0 + p1);
+        m_run = mn;
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * t4);
+            const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * t4 + 4);
+#pragma unroll
+            for (int mt = 0; mt < 16; ++mt) {
+                o[mt][0] *= a_lo;
+                o[mt][1] *= a_hi;
+                o[mt][2] *= a_lo;
+                o[mt][3] *= a_hi;
+            }
+        }
+        const uint32_t pb = pack_f16(p0, p1);
+        // Rows past the key set may hold NaN codes; 0 * NaN would poison the sum.
+        uint32_t vmask = 0xFFFFFFFFu;
+        if (nvalid < kKeysPerWarp)
+            vmask = (2 * t4 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 1 < nvalid ? 0xFFFF0000u : 0u);
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const uint4 va = *reinterpret_cast<const uint4 *>(vst + tile_offset(row0 + 2 * t4, 8 * half + gid));
+            const uint4 vb = *reinterpret_cast<const uint4 *>(vst + tile_offset(row0 + 2 * t4 + 1, 8 * half + gid));
+            const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t lo = __byte_perm(wa[w], wb[w], 0x5140);   // a0 b0 a1 b1
+                const uint32_t hi = __byte_perm(wa[w], wb[w], 0x7362);   // a2 b2 a3 b3
+                const int mt = 8 * half + 2 * w;
+                mma_1688_f16(o[mt], e4m3x2_to_f16x2(static_cast<uint16_t>(lo & 0xFFFFu)) & vmask,
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(lo >> 16)) & vmask, pb);
+                mma_1688_f16(o[mt + 1], e4m3x2_to_f16x2(static_cast<uint16_t>(hi & 0xFFFFu)) & vmask,
+                             e4m3x2_to_f16x2(static_cast<uint16_t>(hi >> 16)) & vmask, pb);
+            }
+        }
+    }
+
+    __device__ void store(float *red_o, float *red_m, float *red_l, int warp, int lane) const {
+        const int gid = lane >> 2, t4 = lane & 3;
+        float l = l_run;
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        if (t4 == 0 && gid < G) {
+            red_m[warp * G + gid] = m_run;
+            red_l[warp * G + gid] = l;
+        }
+        const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+#pragma unroll
+        for (int mt = 0; mt < 16; ++mt) {
+            const int d = 128 * (mt >> 3) + 16 * gid + 2 * (mt & 7);
+            if (h0 < G)
+                *reinterpret_cast<float2 *>(red_o + (warp * G + h0) * kHeadDim + d) = make_float2(o[mt][0], o[mt][2]);
+            if (h1 < G)
+                *reinterpret_cast<float2 *>(red_o + (warp * G + h1) * kHeadDim + d) = make_float2(o[mt][1], o[mt][3]);
+        }
+    }
+};
+
 // ------------------------------------------------------------- the kernel --
 
-template <int G, int CONSUMER, int S>
-__global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
+template <int G, int CONSUMER, int S, int KV>
+__global__ void __launch_bounds__(kThreads, S * kv_stage_bytes(KV) <= kStages * kStageBytes ? 2 : 1)
     attn_layer_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const LayerArgs a) {
+    constexpr int kStage = kv_stage_bytes(KV);     // bytes of one stage (K + V of 32 keys)
+    constexpr int kBoxes = kv_boxes_per_row(KV);   // 128-byte boxes per K or V row
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    float *q_s = reinterpret_cast<float *>(smem + S * kStageBytes);          // [G][256]
+    float *q_s = reinterpret_cast<float *>(smem + S * kStage);               // [G][256]
     float *knew_s = q_s + G * kHeadDim;                                        // [256]
     float *vnew_s = knew_s + kHeadDim;                                         // [256]
     float *kraw_s = vnew_s + kHeadDim;                                         // [256]
@@ -438,6 +634,7 @@ __global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(misc + 32);
     uint64_t *empty = full + S;
     int *flag_s = reinterpret_cast<int *>(empty + S);
+    uint8_t *code_s = reinterpret_cast<uint8_t *>(flag_s + 4);                 // [2][256] E4M3 new entry
 
     const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -447,6 +644,8 @@ __global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     asm volatile("griddepcontrol.wait;" ::: "memory");
     const int c = a.context[b];
+    const float kscale = KV == KV_FP8 ? a.k_scale[kvh] : 1.f;
+    const float vscale = KV == KV_FP8 ? a.v_scale[kvh] : 1.f;
     int bit = 0;
     const int n = cached_keys(a, c, &bit);
     if (n < 0) {
@@ -496,8 +695,8 @@ __global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
     // combine's inputs now, in the same round as q.
     const bool has_new = a.new_kind != NEW_NONE;
     if (nchunks == 1)
-        load_combine_inputs<G>(a, b, kvh, c, kraw_s, vnew_s, tab_s, misc + 2 * kMaxGroup, misc + 3 * kMaxGroup,
-                               kThreads);
+        load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, misc + 2 * kMaxGroup,
+                                   misc + 3 * kMaxGroup, code_s, kThreads);
     __syncthreads();
 
     float *red_o = reinterpret_cast<float *>(smem);             // reuses the stage ring
@@ -512,33 +711,34 @@ __global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
                     atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
-                uint8_t *st = smem + slot * kStageBytes;
-                mbar_arrive_expect_tx(&full[slot], kStageBytes);
+                uint8_t *st = smem + slot * kStage;
+                mbar_arrive_expect_tx(&full[slot], kStage);
                 const int row = start + s * kStageKeys;
 #pragma unroll
-                for (int j = 0; j < kBoxesPerRow; ++j)
-                    tma_load_4d(st + j * kBoxBytes, &kmap, &full[slot], j * kBoxCols, row, kvh, b);
+                for (int j = 0; j < kBoxes; ++j)
+                    tma_load_4d(st + j * kBoxBytes, &kmap, &full[slot], j * kv_box_cols(KV), row, kvh, b);
 #pragma unroll
-                for (int j = 0; j < kBoxesPerRow; ++j)
-                    tma_load_4d(st + (kBoxesPerRow + j) * kBoxBytes, &vmap, &full[slot],
-                                j * kBoxCols, row, kvh, b);
+                for (int j = 0; j < kBoxes; ++j)
+                    tma_load_4d(st + (kBoxes + j) * kBoxBytes, &vmap, &full[slot], j * kv_box_cols(KV), row,
+                                kvh, b);
             }
         }
         __syncthreads();
         __syncthreads();
     } else {
-        typename std::conditional<CONSUMER == CONSUMER_MMA, MmaConsumer<G>, FmaConsumer<G>>::type cons;
-        cons.init(q_s, lane);
+        using Mma = typename std::conditional<KV == KV_FP8, Fp8MmaConsumer<G>, MmaConsumer<G>>::type;
+        typename std::conditional<CONSUMER == CONSUMER_MMA, Mma, FmaConsumer<G, KV>>::type cons;
+        cons.init(q_s, lane, kscale);
         for (int s = 0; s < nst; ++s) {
             const int slot = s % S;
             if (!mbar_wait(&full[slot], (s / S) & 1)) {
                 if (lane == 0) atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
                 break;
             }
-            const uint8_t *kst = smem + slot * kStageBytes;
+            const uint8_t *kst = smem + slot * kStage;
             const int row0 = warp * kKeysPerWarp;
             const int nvalid = min(kKeysPerWarp, end - (start + s * kStageKeys + row0));
-            if (nvalid > 0) cons.consume(kst, kst + kBoxesPerRow * kBoxBytes, row0, nvalid, lane);
+            if (nvalid > 0) cons.consume(kst, kst + kBoxes * kBoxBytes, row0, nvalid, lane);
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[slot]);
         }
@@ -596,7 +796,8 @@ __global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
     // fetched them), and each warp's chunk maxima and sums.
     float *sink_s = misc + 2 * kMaxGroup;           // [G]
     float *gate_s = misc + 3 * kMaxGroup;           // [G]
-    if (nchunks > 1) load_combine_inputs<G>(a, b, kvh, c, kraw_s, vnew_s, tab_s, sink_s, gate_s, kThreads);
+    if (nchunks > 1)
+        load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, sink_s, gate_s, code_s, kThreads);
     const float2 *pml = reinterpret_cast<const float2 *>(a.part_ml);
     constexpr int kPerLane = 4;
     float2 ml[kPerLane];
@@ -613,16 +814,35 @@ __global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
     __syncthreads();
     if (has_new) {
         for (int d = threadIdx.x; d < kHeadDim; d += blockDim.x) {
-            float kn;
-            if (a.new_kind == NEW_STAGED || d >= a.rotary_dim) {
-                kn = kraw_s[d];
-            } else {  // rotate the new key in fp64 from the fp32 table, round once to bf16
-                const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
-                const double x1 = kraw_s[j], x2 = kraw_s[j + half];
-                const double cc = tab_s[j].x, ss = tab_s[j].y;
-                kn = f64_to_bf16_value(d < half ? x1 * cc - x2 * ss : x2 * cc + x1 * ss);
+            if (KV == KV_FP8) {
+                // E4M3 entry: quantise (fp64 rotation, one division, one rounding) unless staged;
+                // score it as stored (code * scale) and keep V in code units.
+                if (a.new_kind == NEW_ROTATE) {
+                    double y = kraw_s[d];
+                    if (d < a.rotary_dim) {
+                        const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
+                        const double x1 = kraw_s[j], x2 = kraw_s[j + half];
+                        const double cc = tab_s[j].x, ss = tab_s[j].y;
+                        y = d < half ? __dsub_rn(__dmul_rn(x1, cc), __dmul_rn(x2, ss))
+                                     : __dadd_rn(__dmul_rn(x2, cc), __dmul_rn(x1, ss));
+                    }
+                    code_s[d] = e4m3_from_f64(__ddiv_rn(y, (double)kscale));
+                    code_s[kHeadDim + d] = e4m3_from_f64(__ddiv_rn((double)vnew_s[d], (double)vscale));
+                }
+                knew_s[d] = e4m3_to_f32(code_s[d]) * kscale;
+                vnew_s[d] = e4m3_to_f32(code_s[kHeadDim + d]);
+            } else {
+                float kn;
+                if (a.new_kind == NEW_STAGED || d >= a.rotary_dim) {
+                    kn = kraw_s[d];
+                } else {  // rotate the new key in fp64 from the fp32 table, round once to bf16
+                    const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
+                    const double x1 = kraw_s[j], x2 = kraw_s[j + half];
+                    const double cc = tab_s[j].x, ss = tab_s[j].y;
+                    kn = f64_to_bf16_value(d < half ? x1 * cc - x2 * ss : x2 * cc + x1 * ss);
+                }
+                knew_s[d] = kn;
             }
-            knew_s[d] = kn;
         }
         __syncthreads();
     }
@@ -682,7 +902,7 @@ __global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
             float f = a.sink ? 1.f / (1.f + fast_exp2((sink_s[h] - lse) * kLog2e)) : 1.f;
             // output gate: sigmoid(g) = 1 / (1 + 2^(-g * log2 e)); lse is not gated
             if (a.gate) f *= 1.f / (1.f + fast_exp2(-gate_s[h] * kLog2e));
-            head_s[h] = f / L;
+            head_s[h] = f / L * vscale;   // FP8: partials and the new value are in V-code units
             wnew_s[h] = w_new;
             a.lse[(size_t)b * a.num_q_heads + hg] = lse;
         }
@@ -746,19 +966,24 @@ __global__ void __launch_bounds__(kThreads, S <= kStages ? 2 : 1)
         const int slot = a.commit == COMMIT_RING ? c % a.capacity : c;
         const size_t o = (size_t)b * a.seq_stride + ((size_t)kvh * a.capacity + slot) * kHeadDim;
         for (int d = threadIdx.x; d < kHeadDim; d += blockDim.x) {
-            a.cache_k[o + d] = __float2bfloat16_rn(knew_s[d]);   // exact: knew_s holds bf16 values
-            a.cache_v[o + d] = __float2bfloat16_rn(vnew_s[d]);
+            if (KV == KV_FP8) {
+                static_cast<uint8_t *>(a.cache_k)[o + d] = code_s[d];
+                static_cast<uint8_t *>(a.cache_v)[o + d] = code_s[kHeadDim + d];
+            } else {  // exact: knew_s and vnew_s hold bf16 values
+                static_cast<__nv_bfloat16 *>(a.cache_k)[o + d] = __float2bfloat16_rn(knew_s[d]);
+                static_cast<__nv_bfloat16 *>(a.cache_v)[o + d] = __float2bfloat16_rn(vnew_s[d]);
+            }
         }
     }
 }
 
-template <int G, int CONSUMER, int S>
+template <int G, int CONSUMER, int S, int KV>
 cudaError_t launch_g(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
                      cudaStream_t s) {
     static bool configured = false;
-    const size_t smem = layer_smem_bytes(G, S);
+    const size_t smem = layer_smem_bytes(G, S * kv_stage_bytes(KV) / kStageBytes);
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER, S>,
+        cudaError_t e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER, S, KV>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = true;
@@ -773,35 +998,46 @@ cudaError_t launch_g(const CUtensorMap *km, const CUtensorMap *vm, const LayerAr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attn_layer_kernel<G, CONSUMER, S>, *km, *vm, a);
+    return cudaLaunchKernelEx(&cfg, attn_layer_kernel<G, CONSUMER, S, KV>, *km, *vm, a);
 }
 
-template <int CONSUMER, int S>
+// S counts stages of the cache's type: an E4M3 ring has twice the bf16 count.
+template <int CONSUMER, int S_BF16, int KV>
 cudaError_t launch_c(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
                      int group, cudaStream_t s) {
+    constexpr int S = S_BF16 * kStageBytes / kv_stage_bytes(KV);
     switch (group) {
-    case 1: return launch_g<1, CONSUMER, S>(km, vm, a, batch, s);
-    case 2: return launch_g<2, CONSUMER, S>(km, vm, a, batch, s);
-    case 4: return launch_g<4, CONSUMER, S>(km, vm, a, batch, s);
-    case 8: return launch_g<8, CONSUMER, S>(km, vm, a, batch, s);
+    case 1: return launch_g<1, CONSUMER, S, KV>(km, vm, a, batch, s);
+    case 2: return launch_g<2, CONSUMER, S, KV>(km, vm, a, batch, s);
+    case 4: return launch_g<4, CONSUMER, S, KV>(km, vm, a, batch, s);
+    case 8: return launch_g<8, CONSUMER, S, KV>(km, vm, a, batch, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
+template <int KV>
+cudaError_t launch_kv(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch, int group,
+                      int consumer, int stages, cudaStream_t s) {
+    if (stages == kDeepStages)
+        return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA, kDeepStages, KV>(km, vm, a, batch, group, s)
+                                        : launch_c<CONSUMER_FMA, kDeepStages, KV>(km, vm, a, batch, group, s);
+    return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA, kStages, KV>(km, vm, a, batch, group, s)
+                                    : launch_c<CONSUMER_FMA, kStages, KV>(km, vm, a, batch, group, s);
+}
+
 }  // namespace
 
+// `stages` in bf16 stages: the ring's bytes; an E4M3 ring has twice as many
+// (half-size) stages and so twice the mbarriers.
 size_t layer_smem_bytes(int group, int stages) {
     return 1024 + (size_t)stages * kStageBytes + ((size_t)group * kHeadDim + 4 * kHeadDim + 32) * sizeof(float) +
-           2 * (size_t)stages * sizeof(uint64_t) + 16;
+           2 * (size_t)(2 * stages) * sizeof(uint64_t) + 16 + 2 * kHeadDim;
 }
 
 cudaError_t launch_layer(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
                          int group, int consumer, int stages, cudaStream_t s) {
-    if (stages == kDeepStages)
-        return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA, kDeepStages>(km, vm, a, batch, group, s)
-                                        : launch_c<CONSUMER_FMA, kDeepStages>(km, vm, a, batch, group, s);
-    return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA, kStages>(km, vm, a, batch, group, s)
-                                    : launch_c<CONSUMER_FMA, kStages>(km, vm, a, batch, group, s);
+    return a.kv_type == KV_FP8 ? launch_kv<KV_FP8>(km, vm, a, batch, group, consumer, stages, s)
+                               : launch_kv<KV_BF16>(km, vm, a, batch, group, consumer, stages, s);
 }
 
 }  // namespace hd

@@ -16,12 +16,21 @@ namespace hd {
 constexpr int kHeadDim = 256;     // head_dim this build implements
 constexpr int kMaxGroup = 8;      // query heads per kv head
 constexpr int kStageKeys = 32;    // keys per pipeline stage (rows of one TMA box)
-constexpr int kStages = 3;        // stages per CTA with two CTAs per SM (the default)
-constexpr int kDeepStages = 6;    // stages per CTA with one CTA per SM (grids of at most one CTA per SM)
+constexpr int kStages = 3;        // bf16 stages per CTA with two CTAs per SM (the default)
+constexpr int kDeepStages = 6;    // bf16 stages per CTA with one CTA per SM (grids of at most one CTA per SM)
 constexpr int kBoxCols = 64;      // bf16 columns per 128-byte swizzled box row
 constexpr int kBoxesPerRow = kHeadDim / kBoxCols;                 // 4
 constexpr int kBoxBytes = kStageKeys * 128;                       // 4 KiB
 constexpr int kStageBytes = 2 * kBoxesPerRow * kBoxBytes;         // K + V: 32 KiB
+
+// Cache element types (hd_kv_dtype).  An FP8 stage holds the same 32 keys in
+// half the bytes, so an FP8 ring has twice the stages in the same shared
+// memory: stage counts above are in bf16 stages.
+enum KvType : int32_t { KV_BF16 = 0, KV_FP8 = 1 };
+__host__ __device__ constexpr int kv_elem_bytes(int kv) { return kv == KV_FP8 ? 1 : 2; }
+__host__ __device__ constexpr int kv_box_cols(int kv) { return 128 / kv_elem_bytes(kv); }                       // 64 / 128
+__host__ __device__ constexpr int kv_boxes_per_row(int kv) { return kHeadDim * kv_elem_bytes(kv) / 128; }       // 4 / 2
+__host__ __device__ constexpr int kv_stage_bytes(int kv) { return 2 * kv_boxes_per_row(kv) * kBoxBytes; }       // 32 / 16 KiB
 constexpr int kChunkMin = 64;
 constexpr int kChunkMax = 2048;
 
@@ -41,7 +50,7 @@ enum KeySet : int32_t {
 enum NewEntry : int32_t {
     NEW_NONE = 0,     // already in the scored cache rows
     NEW_ROTATE = 1,   // bf16 k of the step, rotated (fp64, one rounding) in the kernel
-    NEW_STAGED = 2    // already rotated and rounded (ring staging row)
+    NEW_STAGED = 2    // already rotated and rounded (ring staging row, in the cache's type)
 };
 // Where the new entry is stored once every chunk has read the cache.
 enum Commit : int32_t { COMMIT_NONE = 0, COMMIT_APPEND = 1, COMMIT_RING = 2 };
@@ -55,13 +64,16 @@ struct LayerArgs {
     const float *q_rot;            // ... or already rotated, fp32 (when q_bf16 is null)
     const float2 *table;           // [max_context + 1][rotary_dim / 2] (cos, sin)
     int32_t rotary_dim;
-    const __nv_bfloat16 *new_k;    // [batch][Hkv][D] (NEW_ROTATE: raw k; NEW_STAGED: staged)
-    const __nv_bfloat16 *new_v;
+    const void *new_k;             // [batch][Hkv][D] (NEW_ROTATE: raw bf16 k; NEW_STAGED: staged entry)
+    const void *new_v;
     int32_t new_kind, commit, key_set;
-    __nv_bfloat16 *cache_k;        // cache of the layer (also the store target)
-    __nv_bfloat16 *cache_v;
-    int64_t seq_stride;
+    void *cache_k;                 // cache of the layer (also the store target), bf16 or E4M3 codes
+    void *cache_v;
+    int64_t seq_stride;            // elements
     int32_t capacity;
+    int32_t kv_type;               // KV_BF16 / KV_FP8
+    const float *k_scale;          // FP8: [Hkv] dequantisation scales, else null
+    const float *v_scale;
     const float *sink;             // [Hq] or null
     const float *gate;             // [batch][Hq] output-gate logits or null
     __nv_bfloat16 *out;            // [batch][Hq][D]
@@ -84,10 +96,13 @@ struct RopeArgs {
     const __nv_bfloat16 *v;
     float *q_rot;                      // [batch][Hq][D]
     const float2 *table;               // [max_context + 1][rotary_dim / 2] (cos, sin)
-    __nv_bfloat16 *dst_k;              // full: cache; ring: staging; roll: cache
-    __nv_bfloat16 *dst_v;
-    int64_t seq_stride;                // of dst (staging: Hkv * D)
+    void *dst_k;                       // full: cache; ring: staging; roll: cache (bf16 or E4M3)
+    void *dst_v;
+    int64_t seq_stride;                // of dst, elements (staging: Hkv * D)
     int32_t capacity;                  // of dst (staging: 1)
+    int32_t kv_type;                   // KV_BF16 / KV_FP8
+    const float *k_scale;              // FP8: [Hkv] scales, else null
+    const float *v_scale;
     int32_t *err;
     int32_t num_q_heads, num_kv_heads, rotary_dim;
     int32_t key_set, window, max_context;
@@ -95,6 +110,7 @@ struct RopeArgs {
 
 cudaError_t launch_rope_append(const RopeArgs &a, int batch, cudaStream_t s);
 cudaError_t launch_roll_window(const RopeArgs &a, int batch, cudaStream_t s);
+// `stages` in bf16 stages (kStages or kDeepStages); a.kv_type picks the kernel.
 cudaError_t launch_layer(const CUtensorMap *kmap, const CUtensorMap *vmap, const LayerArgs &a,
                          int batch, int group, int consumer, int stages, cudaStream_t s);
 size_t layer_smem_bytes(int group, int stages);

@@ -100,6 +100,7 @@ extern "C" hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_
     if (!cache.k || !cache.v || !aligned16(cache.k) || !aligned16(cache.v) || cache.capacity <= 0 ||
         cache.seq_stride % 8 != 0 || cache.seq_stride < (int64_t)num_kv_heads * cache.capacity * hd::kHeadDim)
         return HD_ERR_INVALID_ARG;
+    if (cache.k_scale || cache.v_scale) return HD_ERR_UNSUPPORTED;   // bf16 caches only
     if (max_context < 0) return HD_ERR_INVALID_ARG;
     if ((int64_t)max_context + 1 > cache.capacity) return HD_ERR_CAPACITY;
 
@@ -142,8 +143,9 @@ extern "C" hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_
     a.new_kind = hd::NEW_NONE;
     a.commit = hd::COMMIT_NONE;
     a.key_set = hd::KEYS_FULL_CACHED;
-    a.cache_k = static_cast<__nv_bfloat16 *>(cache.k);
-    a.cache_v = static_cast<__nv_bfloat16 *>(cache.v);
+    a.cache_k = cache.k;
+    a.cache_v = cache.v;
+    a.kv_type = hd::KV_BF16;
     a.seq_stride = cache.seq_stride;
     a.capacity = cache.capacity;
     a.sink = sink;

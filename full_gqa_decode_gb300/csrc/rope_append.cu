@@ -15,6 +15,9 @@
 // FMA and correctly rounded sums: proved algorithms using rounding to odd",
 // IEEE TC 2008): an odd-rounded binary32 carries enough bits that its
 // round-to-nearest-even to bf16 equals the direct rounding of the double.
+// An E4M3 cache stores e4m3(y / k_scale) of the same fp64 rotation y (one
+// fp64 division, one rounding) and e4m3(v / v_scale).
+#include "e4m3.cuh"
 #include "hd_internal.h"
 
 namespace hd {
@@ -42,16 +45,29 @@ __device__ __forceinline__ float rope_f32(const __nv_bfloat16 *x, int d, int rot
     return d < half ? fmaf(x1, t.x, -x2 * t.y) : fmaf(x2, t.x, x1 * t.y);
 }
 
-// Rotated, bf16-rounded value of dim d of the new key (fp64 path).
-__device__ __forceinline__ __nv_bfloat16 rope_key_bf16(const __nv_bfloat16 *x, int d, int rot,
-                                                       const float2 *cs) {
-    if (d >= rot) return x[d];
+// Rotated value of dim d of the new key in fp64 (both products exact, one rounding).
+__device__ __forceinline__ double rope_key_f64(const __nv_bfloat16 *x, int d, int rot, const float2 *cs) {
+    if (d >= rot) return (double)__bfloat162float(x[d]);
     const int half = rot >> 1;
     const int i = d < half ? d : d - half;
     const double x1 = (double)__bfloat162float(x[i]), x2 = (double)__bfloat162float(x[i + half]);
     const double c = (double)cs[i].x, s = (double)cs[i].y;
-    const double y = d < half ? (x1 * c - x2 * s) : (x2 * c + x1 * s);
-    return f64_to_bf16_rne(y);
+    return d < half ? __dsub_rn(__dmul_rn(x1, c), __dmul_rn(x2, s)) : __dadd_rn(__dmul_rn(x2, c), __dmul_rn(x1, s));
+}
+
+// Stores dim d of the new entry at element offset o of the destination: the
+// rotated key rounded once to bf16 and v bit for bit, or both as E4M3 codes.
+__device__ __forceinline__ void store_entry(const RopeArgs &a, size_t o, int h, const __nv_bfloat16 *kh,
+                                            const __nv_bfloat16 *vh, int d, const float2 *cs) {
+    const double y = rope_key_f64(kh, d, a.rotary_dim, cs);
+    if (a.kv_type == KV_FP8) {
+        static_cast<uint8_t *>(a.dst_k)[o] = e4m3_from_f64(__ddiv_rn(y, (double)a.k_scale[h]));
+        static_cast<uint8_t *>(a.dst_v)[o] =
+            e4m3_from_f64(__ddiv_rn((double)__bfloat162float(vh[d]), (double)a.v_scale[h]));
+    } else {
+        static_cast<__nv_bfloat16 *>(a.dst_k)[o] = d >= a.rotary_dim ? kh[d] : f64_to_bf16_rne(y);
+        static_cast<__nv_bfloat16 *>(a.dst_v)[o] = vh[d];
+    }
 }
 
 // Returns the context of sequence b, or -1 after flagging an unusable one.
@@ -96,30 +112,32 @@ __global__ void __launch_bounds__(256) rope_append_kernel(const RopeArgs a) {
     for (int idx = threadIdx.x; idx < a.num_kv_heads * D; idx += blockDim.x) {
         const int h = idx / D, d = idx % D;
         const size_t o = (size_t)b * a.seq_stride + ((size_t)h * a.capacity + slot) * D + d;
-        a.dst_k[o] = rope_key_bf16(kb + (size_t)h * D, d, rot, cs);
-        a.dst_v[o] = vb[idx];
+        store_entry(a, o, h, kb + (size_t)h * D, vb + (size_t)h * D, d, cs);
     }
 }
 
 // One CTA per (kv head, sequence) of a roll-layout sliding layer: shift the
 // window down by one row once it is full, then write the new entry at the end.
-// Rows move in groups of 8 (one 16-byte chunk per thread for K and for V):
-// each group is read in full before any of it is overwritten, and the next
-// group's first row is written only after the next read phase.
+// Rows move in groups of 256 / (16-byte chunks per row) -- 8 bf16 rows or 16
+// E4M3 rows, one chunk per thread for K and for V: each group is read in full
+// before any of it is overwritten, and the next group's first row is written
+// only after the next read phase.
 __global__ void __launch_bounds__(256) roll_window_kernel(const RopeArgs a) {
     const int h = blockIdx.x, b = blockIdx.y;
     const int c = checked_context(a, b);
     if (c < 0) return;
     const int D = kHeadDim, W = a.window;
-    const size_t base = (size_t)b * a.seq_stride + (size_t)h * a.capacity * D;
-    uint4 *K4 = reinterpret_cast<uint4 *>(a.dst_k + base);
-    uint4 *V4 = reinterpret_cast<uint4 *>(a.dst_v + base);
-    constexpr int kChunksPerRow = kHeadDim * 2 / 16;  // 32
+    const int esize = kv_elem_bytes(a.kv_type);
+    const size_t base = ((size_t)b * a.seq_stride + (size_t)h * a.capacity * D) * esize;   // bytes
+    uint4 *K4 = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(a.dst_k) + base);
+    uint4 *V4 = reinterpret_cast<uint4 *>(static_cast<uint8_t *>(a.dst_v) + base);
+    const int kChunksPerRow = kHeadDim * esize / 16;   // 32 or 16
+    const int kRowsPerGroup = 256 / kChunksPerRow;      // 8 or 16 (blockDim.x == 256)
     int row_new = c;
     if (c >= W) {
         row_new = W - 1;
         const int r_local = threadIdx.x / kChunksPerRow, ch = threadIdx.x % kChunksPerRow;
-        for (int r0 = 0; r0 < W - 1; r0 += 8) {
+        for (int r0 = 0; r0 < W - 1; r0 += kRowsPerGroup) {
             const int src = r0 + 1 + r_local;
             uint4 kk = make_uint4(0, 0, 0, 0), vv = make_uint4(0, 0, 0, 0);
             const bool live = src <= W - 1;
@@ -138,10 +156,8 @@ __global__ void __launch_bounds__(256) roll_window_kernel(const RopeArgs a) {
     const float2 *cs = a.table + (size_t)c * (a.rotary_dim >> 1);
     const __nv_bfloat16 *kh = a.k + ((size_t)b * a.num_kv_heads + h) * D;
     const __nv_bfloat16 *vh = a.v + ((size_t)b * a.num_kv_heads + h) * D;
-    for (int d = threadIdx.x; d < D; d += blockDim.x) {
-        a.dst_k[base + (size_t)row_new * D + d] = rope_key_bf16(kh, d, a.rotary_dim, cs);
-        a.dst_v[base + (size_t)row_new * D + d] = vh[d];
-    }
+    const size_t row_base = (size_t)b * a.seq_stride + ((size_t)h * a.capacity + row_new) * D;  // elements
+    for (int d = threadIdx.x; d < D; d += blockDim.x) store_entry(a, row_base + d, h, kh, vh, d, cs);
 }
 
 }  // namespace
@@ -152,7 +168,7 @@ cudaError_t launch_rope_append(const RopeArgs &a, int batch, cudaStream_t s) {
 }
 
 cudaError_t launch_roll_window(const RopeArgs &a, int batch, cudaStream_t s) {
-    roll_window_kernel<<<dim3(a.num_kv_heads, batch), 256, 0, s>>>(a);
+    roll_window_kernel<<<dim3(a.num_kv_heads, batch), 256, 0, s>>>(a);   // 256 threads: see the kernel
     return cudaGetLastError();
 }
 

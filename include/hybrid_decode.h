@@ -57,7 +57,8 @@
  *   sink             [num_q_heads] fp32
  *   gate             [batch][num_q_heads] fp32 logits
  *   cache k / v      sequence b starts at b * seq_stride; within it
- *                    [num_kv_heads][capacity][head_dim]
+ *                    [num_kv_heads][capacity][head_dim], bf16 or E4M3 codes
+ *   k_scale, v_scale [num_kv_heads] fp32 (FP8 caches)
  */
 #ifndef HYBRID_DECODE_H
 #define HYBRID_DECODE_H
@@ -82,6 +83,18 @@ typedef enum { HD_SLIDING = 0, HD_FULL = 1 } hd_layer_type;
 /* Cache layout of sliding layers (spark_export.py, `SparkStepConfig.cache_layout`):
  * AUTO picks RING for sliding layers; full layers always append. */
 typedef enum { HD_LAYOUT_AUTO = 0, HD_LAYOUT_RING = 1, HD_LAYOUT_ROLL = 2 } hd_layout;
+
+/* Element type of every K/V cache of a context.  HD_KV_FP8_E4M3 is an
+ * extension beyond the pages' bf16 step (they name FlashMLA's FP8 KV cache,
+ * flashmla_sparse.py `is_fp8_kvcache`, only as prior art): entries are OCP FP8
+ * E4M3 codes (torch.float8_e4m3fn bits) with one fp32 scale per kv head for K
+ * and one for V (hd_kv_cache.k_scale / v_scale); a cached value is
+ * code * scale.  The new entry is stored as e4m3(x / scale), x being the fp64
+ * rotated key (one rounding, as for bf16) or the bf16 value, the division
+ * rounded once in fp64 and the quotient rounded once to E4M3 (nearest, ties
+ * to even), finite quotients beyond 448 saturating to +-448; it is scored as
+ * stored.  Attention reads half the bytes of a bf16 cache. */
+typedef enum { HD_KV_BF16 = 0, HD_KV_FP8_E4M3 = 1 } hd_kv_dtype;
 
 /* Bits of the device error word (hybrid_decode_device_errors). */
 enum {
@@ -110,18 +123,23 @@ typedef struct {
     int32_t cache_layout;          /* hd_layout for the sliding layers                 */
     int32_t max_batch;             /* largest batch any call passes                    */
     int32_t max_context;           /* largest context (previous tokens) any call uses  */
+    int32_t kv_dtype;              /* hd_kv_dtype of every cache (0 = bf16)            */
 } hd_config;
 
-/* One layer's KV cache (caller-owned device memory, bf16). capacity is the
- * number of entries per (sequence, kv head): window-1 for a sliding ring,
- * window for a sliding roll window, at least max_context+1 for a full layer.
- * seq_stride >= num_kv_heads*capacity*head_dim and a multiple of 8; k and v
- * 16-byte aligned. */
+/* One layer's KV cache (caller-owned device memory, of the context's
+ * kv_dtype). capacity is the number of entries per (sequence, kv head):
+ * window-1 for a sliding ring, window for a sliding roll window, at least
+ * max_context+1 for a full layer.  seq_stride (in elements) >=
+ * num_kv_heads*capacity*head_dim and a multiple of 16 bytes (8 bf16, 16 E4M3
+ * elements); k and v 16-byte aligned.  k_scale / v_scale: FP8 caches only,
+ * device fp32 [num_kv_heads], required there and NULL for bf16. */
 typedef struct {
     void *k;
     void *v;
     int64_t seq_stride;
     int32_t capacity;
+    const float *k_scale;
+    const float *v_scale;
 } hd_kv_cache;
 
 /* Per-layer tensors of a whole decode step (decode_step). */

@@ -74,8 +74,12 @@ def normal_bf16(rng: np.random.Generator, shape, std: float = 1.0) -> torch.Tens
 
 
 def bits(t: torch.Tensor) -> np.ndarray:
-    """uint16 bit patterns of a bf16 tensor (a copy on the host)."""
-    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    """uint16 bit patterns of a bf16 tensor, or the uint8 codes of an E4M3 cache
+    (a copy on the host)."""
+    t = t.detach().contiguous().cpu()
+    if t.dtype in (torch.uint8, torch.float8_e4m3fn):
+        return t.view(torch.uint8).numpy().copy()
+    return t.view(torch.int16).numpy().view(np.uint16).copy()
 
 
 def from_bits(a: np.ndarray) -> torch.Tensor:
@@ -128,6 +132,45 @@ def cache_with_history(rng: np.random.Generator, batch: int, num_kv_heads: int, 
     t = normal_bf16(rng, (batch, num_kv_heads, capacity, head_dim))
     for b in range(batch):
         t[b, :, int(written[b]):, :] = float("nan")
+    return t
+
+
+E4M3_NAN = 0x7F
+
+
+def kv_scales(rng: np.random.Generator, num_kv_heads: int) -> torch.Tensor:
+    """Per-kv-head fp32 scales amax / 448 for E4M3 caches, amax ~ U[3, 6] (an N(0,1)
+    cache spans about +-4.5, so the largest entries sometimes saturate)."""
+    return torch.from_numpy((rng.uniform(3.0, 6.0, num_kv_heads) / 448.0).astype(np.float32))
+
+
+def e4m3_codes(x: torch.Tensor) -> torch.Tensor:
+    """uint8 E4M3 codes of a float tensor: torch's float8_e4m3fn cast after clamping
+    to the largest finite value (the cast itself maps overflow to NaN)."""
+    return x.float().clamp(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def cache_with_history_fp8(rng: np.random.Generator, batch: int, num_kv_heads: int, capacity: int,
+                           written, scale: torch.Tensor, head_dim: int = HEAD_DIM) -> torch.Tensor:
+    """E4M3 cache [B, Hkv, capacity, D] (uint8 codes): entries [0, written[b]) hold the
+    codes of N(0,1) / scale[h], the rest the NaN code."""
+    x = rng.standard_normal(size=(batch, num_kv_heads, capacity, head_dim), dtype=np.float32)
+    x = x / scale.numpy()[None, :, None, None]
+    c = e4m3_codes(torch.from_numpy(x))
+    for b in range(batch):
+        c[b, :, int(written[b]):, :] = E4M3_NAN
+    return c
+
+
+def cuda_e4m3_codes_(t: torch.Tensor, scale: torch.Tensor, seed: int) -> torch.Tensor:
+    """Fill a CUDA uint8 cache [B, Hkv, cap, D] in place with the E4M3 codes of
+    seeded N(0,1) / scale[h] samples (one sequence and head at a time)."""
+    g = torch.Generator(device=t.device)
+    g.manual_seed(seed)
+    for b in range(t.shape[0]):
+        for h in range(t.shape[1]):
+            x = torch.randn(t.shape[2:], generator=g, device=t.device, dtype=torch.float32)
+            t[b, h].copy_(e4m3_codes(x / scale[h]))
     return t
 
 

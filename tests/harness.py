@@ -47,21 +47,35 @@ def assert_bits_equal(gpu: torch.Tensor, ref_bits: np.ndarray, what: str) -> Non
 
 
 class LayerCase:
-    """Seeded inputs of one layer call: q/k/v, caches with `written` valid entries."""
+    """Seeded inputs of one layer call: q/k/v, caches with `written` valid entries
+    (bf16, or E4M3 codes with per-kv-head scales when kv == "fp8")."""
 
     def __init__(self, rng, batch, num_q_heads, num_kv_heads, capacity, context, written=None,
-                 sink=None, gate=None):
+                 sink=None, gate=None, kv="bf16", k_std=1.0):
         D = synth.HEAD_DIM
         self.context = np.asarray(context, np.int32)
         self.q = synth.normal_bf16(rng, (batch, num_q_heads, D))
-        self.k = synth.normal_bf16(rng, (batch, num_kv_heads, D))
-        self.v = synth.normal_bf16(rng, (batch, num_kv_heads, D))
+        self.k = synth.normal_bf16(rng, (batch, num_kv_heads, D), std=k_std)
+        self.v = synth.normal_bf16(rng, (batch, num_kv_heads, D), std=k_std)
         if written is None:
             written = np.minimum(self.context, capacity)
-        self.kc = synth.cache_with_history(rng, batch, num_kv_heads, capacity, written, D)
-        self.vc = synth.cache_with_history(rng, batch, num_kv_heads, capacity, written, D)
+        self.kv = kv
+        self.k_scale = self.v_scale = None
+        if kv == "fp8":
+            self.k_scale = synth.kv_scales(rng, num_kv_heads)
+            self.v_scale = synth.kv_scales(rng, num_kv_heads)
+            self.kc = synth.cache_with_history_fp8(rng, batch, num_kv_heads, capacity, written, self.k_scale, D)
+            self.vc = synth.cache_with_history_fp8(rng, batch, num_kv_heads, capacity, written, self.v_scale, D)
+        else:
+            self.kc = synth.cache_with_history(rng, batch, num_kv_heads, capacity, written, D)
+            self.vc = synth.cache_with_history(rng, batch, num_kv_heads, capacity, written, D)
         self.sink = sink
         self.gate = gate  # fp32 [batch][num_q_heads] output-gate logits, or None
+
+    def cache(self, hd, kd, vd, dev):
+        if self.kv == "fp8":
+            return hd.kv_cache(kd, vd, self.k_scale.to(dev), self.v_scale.to(dev))
+        return hd.kv_cache(kd, vd)
 
 
 def oracle_layer(orc, case: LayerCase, layer_type: int, layout: int, rotary_dim=None, theta=None):
@@ -72,7 +86,9 @@ def oracle_layer(orc, case: LayerCase, layer_type: int, layout: int, rotary_dim=
                          context=case.context, q=synth.bits(case.q), k=synth.bits(case.k),
                          v=synth.bits(case.v), kcache=kc, vcache=vc,
                          sink=None if case.sink is None else case.sink.numpy(),
-                         gate=None if case.gate is None else case.gate.numpy())
+                         gate=None if case.gate is None else case.gate.numpy(),
+                         k_scale=None if case.k_scale is None else case.k_scale.numpy(),
+                         v_scale=None if case.v_scale is None else case.v_scale.numpy())
     r["kcache"], r["vcache"] = kc, vc
     return r
 
@@ -85,7 +101,7 @@ def gpu_layer(hd, ctx, layer: int, layer_type: int, case: LayerCase, max_context
     qrot = torch.empty(B, Hq, D, dtype=torch.float32, device=dev)
     out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device=dev)
     lse = torch.empty(B, Hq, dtype=torch.float32, device=dev)
-    cache = hd.kv_cache(kd, vd)
+    cache = case.cache(hd, kd, vd, dev)
     sink = None if case.sink is None else case.sink.to(dev)
     gate = None if case.gate is None else case.gate.to(dev)
     hd.rope_append_kv(ctx, layer, ctx_d, case.q.to(dev), case.k.to(dev), case.v.to(dev), qrot, cache)

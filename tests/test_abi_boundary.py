@@ -80,3 +80,34 @@ def test_plan_split_shapes(hd):
     assert hd.hd_plan_split(64, 2, 32769, 152) == (2048, 17)   # batch-64 full layers
     assert hd.hd_plan_split(64, 2, 511, 152) == (512, 1)       # batch-64 ring layers: one chunk
     assert hd.hd_plan_split(1, 2, 4097, 152) == (64, 65)       # batch 1: many short chunks
+
+
+def test_binding_structs_match_the_header(hd, tmp_path):
+    """Every struct field of the ctypes binding sits at the offset the C compiler
+    gives it from include/hybrid_decode.h, and the struct sizes agree."""
+    structs = {"hd_config": hd.hd_config, "hd_kv_cache": hd.hd_kv_cache, "hd_layer_io": hd.hd_layer_io}
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "hybrid_decode.h"', "int main(void) {"]
+    for name, cls in structs.items():
+        lines.append(f'printf("{name} size %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'printf("{name} {field} %zu\\n", offsetof({name}, {field}));')
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "layout"
+    subprocess.run(["gcc", "-std=c11", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)], check=True)
+    got = {}
+    for line in subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.splitlines():
+        s, f, v = line.split()
+        got[(s, f)] = int(v)
+    for name, cls in structs.items():
+        assert got[(name, "size")] == ctypes.sizeof(cls), name
+        for field, _ in cls._fields_:
+            assert got[(name, field)] == getattr(cls, field).offset, (name, field)
+
+
+def test_config_rejects_an_unknown_kv_dtype(hd):
+    cfg = hd.Config(layer_types=[0, 1], kv_dtype=hd.HD_KV_FP8_E4M3)
+    assert hd.hd_validate_config(cfg) == 0
+    cfg.kv_dtype = 2
+    assert hd.hd_validate_config(cfg) == 1
