@@ -117,7 +117,7 @@ int sliding_capacity(const hd_ctx *ctx) {
 }
 
 // Encodes the 4-D view {D, capacity, Hkv, batch} of one cache tensor with
-// (128 bytes) x kStageKeys boxes and the 128-byte swizzle the consumers index by.
+// (128 bytes) x (keys per stage) boxes and the 128-byte swizzle the consumers index by.
 bool encode_cache_map(CUtensorMap *map, const void *base, int64_t seq_stride, int capacity,
                       int num_kv_heads, int batch, int kv_type) {
     auto fn = encode_fn();
@@ -127,7 +127,7 @@ bool encode_cache_map(CUtensorMap *map, const void *base, int64_t seq_stride, in
                                 (cuuint64_t)num_kv_heads, (cuuint64_t)batch};
     const cuuint64_t strides[3] = {(cuuint64_t)kHeadDim * es, (cuuint64_t)capacity * kHeadDim * es,
                                    (cuuint64_t)seq_stride * es};
-    const cuuint32_t box[4] = {(cuuint32_t)kv_box_cols(kv_type), (cuuint32_t)kStageKeys, 1, 1};
+    const cuuint32_t box[4] = {(cuuint32_t)kv_box_cols(kv_type), (cuuint32_t)kv_stage_keys(kv_type), 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, kv_type == KV_FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,

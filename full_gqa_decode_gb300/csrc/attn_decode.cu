@@ -42,8 +42,14 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kQScale = kLog2e * 0.0625f;   // log2(e) / sqrt(256)
 constexpr int kConsumerWarps = 4;
-constexpr int kKeysPerWarp = kStageKeys / kConsumerWarps;  // 8
+constexpr int kKeysPerWarp = kStageKeys / kConsumerWarps;  // 8 (bf16 stages; E4M3 stages give 16)
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
+// bf16 layers run a dedicated producer warp.  E4M3 layers fold the producer
+// into the consumers (the last warp to release a slot refills it): four warps
+// per CTA leave each thread up to 255 registers at two CTAs per SM, which the
+// E4M3 consumer's conversions need (five warps cap it at 168).
+__host__ __device__ constexpr bool own_producer(int kv) { return kv == KV_BF16; }
+__host__ __device__ constexpr int kv_threads(int kv) { return own_producer(kv) ? kThreads : kConsumerWarps * 32; }
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
 // Inside the stage ring (free once every stage is consumed): the warp buffers
 // [warps][G][256] + (m, l) and the combine weights start at 0; this chunk's
@@ -188,8 +194,16 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &r, float (&f)[8]) {
 // Byte offset of 16-byte chunk c (0..31 for bf16, 0..15 for E4M3) of row r in
 // a stage's K or V region: box c/8, swizzled chunk (c%8)^(r%8) inside the
 // 128-byte row.
+template <int KV = KV_BF16>
 __device__ __forceinline__ uint32_t tile_offset(int r, int c) {
-    return (c >> 3) * kBoxBytes + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
+    return (c >> 3) * kv_box_bytes(KV) + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
+}
+// Transpose of an 8x8 matrix of 16-bit elements held one fragment per lane
+// (lane l: row l/4, columns 2(l%4), 2(l%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
 }
 
 // One round-to-nearest-even of a double to bf16, through round-to-odd binary32
@@ -260,14 +274,15 @@ __device__ __forceinline__ int cached_keys(const LayerArgs &a, int c, int *bit) 
 // units (the combine applies the V scale).
 template <int G, int KV>
 struct FmaConsumer {
+    static constexpr int kWK = kv_stage_keys(KV) / kConsumerWarps;   // keys per warp per stage
     float qv[G][8], m[G], l[G], acc[G][8];
     float kscale;
 
     __device__ void load_row(const uint8_t *st, int row, int lane, float (&f)[8]) const {
         if (KV == KV_FP8)
-            unpack_e4m3x8(*reinterpret_cast<const uint2 *>(st + tile_offset(row, lane >> 1) + (lane & 1) * 8), f);
+            unpack_e4m3x8(*reinterpret_cast<const uint2 *>(st + tile_offset<KV>(row, lane >> 1) + (lane & 1) * 8), f);
         else
-            unpack_bf16x8(*reinterpret_cast<const uint4 *>(st + tile_offset(row, lane)), f);
+            unpack_bf16x8(*reinterpret_cast<const uint4 *>(st + tile_offset<KV>(row, lane)), f);
     }
 
     __device__ void init(const float *q_s, int lane, float k_scale) {
@@ -284,11 +299,11 @@ struct FmaConsumer {
         }
     }
 
-    // Rows [row0, row0 + kKeysPerWarp) of a stage; the first nvalid are keys.
+    // Rows [row0, row0 + kWK) of a stage; the first nvalid are keys.
     __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane) {
-        constexpr int KB = G >= 8 ? 4 : kKeysPerWarp;  // keeps scores, q and acc in registers
+        constexpr int KB = G >= 8 ? 4 : 8;  // keeps scores, q and acc in registers
 #pragma unroll
-        for (int sb = 0; sb < kKeysPerWarp; sb += KB) {
+        for (int sb = 0; sb < kWK; sb += KB) {
             const int nv = nvalid - sb;
             if (nv <= 0) break;  // warp-uniform
             float sc[KB][G];
@@ -473,134 +488,196 @@ struct MmaConsumer {
 };
 
 // Tensor-core consumer for an E4M3 cache.  Codes convert exactly to f16
-// (cvt.rn.f16x2.e4m3x2), so both products run as f16 MMAs with fp32
-// accumulation; q is split into an f16 high and low part as above.
+// (cvt.rn.f16x2.e4m3x2), so both products run as f16 MMAs (m16n8k16) with
+// fp32 accumulation.  A warp takes 16 keys of a 64-key stage, and K is the A
+// operand: S^T = K Q^T puts 16 keys on M and the q columns on N -- the f16
+// high part of each head's q and, on the remaining columns, its low part
+// (G <= 4: columns G..2G-1; G = 8: a second tile) -- so q costs two
+// registers per k-step and one MMA covers 16 keys.
 //
-// S = Q K^T: lane (gid, t4) holds key gid.  It reads four 16-byte chunks of
-// the key row, chunk 2*t4 + (p & 1) + 8*(p >> 1) at step p, so that the eight
-// lanes of each shared-memory phase (two keys) hit eight distinct chunks after
-// the swizzle.  Word j of a chunk is the B fragment of k-step 4p + j (dims
-// 16*chunk + 4j .. +3, split as (d, d+1) and (d+2, d+3)); the q fragments
-// are built in init with the same dim order, which leaves every dot product
-// unchanged.
+// K: lane (gid, t4) holds keys gid and gid + 8 and reads 16-byte chunks
+// 2*t4 + (p & 1) + 8*(p >> 1) of both rows at step p (the eight lanes of a
+// shared-memory phase then hit eight distinct chunks after the swizzle).
+// Word j of a chunk is the A fragment of k-step 4p + j: dims (d, d+1) and
+// (d+2, d+3) with d = 16*chunk + 4j; the q columns are built in init with the
+// same dim order, which leaves every dot product unchanged.
 //
-// O^T += V^T P^T: lane (gid, t4) reads keys 2*t4 and 2*t4+1, chunks gid and
-// 8 + gid; byte_perm pairs the two keys' bytes of one dim, which is the
-// E4M3x2 input of one A register.  Tile mt covers, on row gid, dim
+// P: the S^T accumulator, packed to f16, is for each group of 8 keys one
+// fragment of an 8x8 (keys x heads) matrix; movmatrix transposes it into the
+// B operand of O^T += V^T P^T (m16n8k16: dims on M, 16 keys on K, heads on N).
+// V: lane (gid, t4) reads chunk gid (and 8 + gid) of keys 2*t4, 2*t4+1,
+// 2*t4+8, 2*t4+9; byte_perm pairs two keys' bytes of one dim, which is one
+// E4M3x2 A register.  Tile mt covers, on row gid, dim
 // 128*(mt / 8) + 16*gid + 2*(mt % 8) and, on row gid + 8, the next dim.
 template <int G>
 struct Fp8MmaConsumer {
-    uint32_t qa[16][4];
-    float o[16][4];
-    float m_run, l_run, kscale;
+    static constexpr int NT = G == 8 ? 2 : 1;   // n-tiles of q columns
+    static constexpr int kWK = 16;              // keys per warp per stage
+    uint32_t qb[NT][16][2];
+    float o[16][4];                              // O^T tile mt: dims (see above) x heads 2*t4 (+1)
+    float m_run[2], l_run[2];                    // heads 2*t4 + e; l_run sums this lane's keys only
+    float kscale;
 
     __device__ void init(const float *q_s, int lane, float k_scale) {
         const int gid = lane >> 2, t4 = lane & 3;
         kscale = k_scale;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const int chunk = 2 * t4 + (p & 1) + 8 * (p >> 1);
+        for (int t = 0; t < NT; ++t) {
+            // column gid of tile t: head and part (high or low f16 half of q)
+            const bool lo = G == 8 ? t == 1 : gid >= G;
+            const int head = G == 8 ? gid : (gid < G ? gid : gid - G);
+            const bool used = G == 8 || gid < 2 * G;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                uint32_t r[4] = {0u, 0u, 0u, 0u};
-                if (gid < G) {
-                    const float *qh = q_s + gid * kHeadDim + 16 * chunk + 4 * j;
-                    const float x0 = qh[0], x1 = qh[1], x2 = qh[2], x3 = qh[3];
-                    const float h0 = __half2float(__float2half_rn(x0));
-                    const float h1 = __half2float(__float2half_rn(x1));
-                    const float h2 = __half2float(__float2half_rn(x2));
-                    const float h3 = __half2float(__float2half_rn(x3));
-                    r[0] = pack_f16(h0, h1);
-                    r[1] = pack_f16(x0 - h0, x1 - h1);
-                    r[2] = pack_f16(h2, h3);
-                    r[3] = pack_f16(x2 - h2, x3 - h3);
+            for (int p = 0; p < 4; ++p) {
+                const int chunk = 2 * t4 + (p & 1) + 8 * (p >> 1);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t r0 = 0u, r1 = 0u;
+                    if (used) {
+                        const float *qh = q_s + head * kHeadDim + 16 * chunk + 4 * j;
+                        float x[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float h = __half2float(__float2half_rn(qh[i]));
+                            x[i] = lo ? qh[i] - h : h;
+                        }
+                        r0 = pack_f16(x[0], x[1]);
+                        r1 = pack_f16(x[2], x[3]);
+                    }
+                    qb[t][4 * p + j][0] = r0;
+                    qb[t][4 * p + j][1] = r1;
                 }
-#pragma unroll
-                for (int i = 0; i < 4; ++i) qa[4 * p + j][i] = r[i];
             }
         }
 #pragma unroll
         for (int mt = 0; mt < 16; ++mt)
 #pragma unroll
             for (int j = 0; j < 4; ++j) o[mt][j] = 0.f;
-        m_run = -INFINITY;
-        l_run = 0.f;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            m_run[e] = -INFINITY;
+            l_run[e] = 0.f;
+        }
     }
 
     __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane) {
         const int gid = lane >> 2, t4 = lane & 3;
-        float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+        // S^T = K Q^T.  With one q tile, even and odd k-steps go to two accumulators
+        // (half the dependent chain); two tiles are two chains already.
+        float s[NT][4], s2[NT][4];
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) s[t][r] = s2[t][r] = 0.f;
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             const int chunk = 2 * t4 + (p & 1) + 8 * (p >> 1);
-            const uint4 kw = *reinterpret_cast<const uint4 *>(kst + tile_offset(row0 + gid, chunk));
-            const uint32_t w[4] = {kw.x, kw.y, kw.z, kw.w};
+            const uint4 ka = *reinterpret_cast<const uint4 *>(kst + tile_offset<KV_FP8>(row0 + gid, chunk));
+            const uint4 kb = *reinterpret_cast<const uint4 *>(kst + tile_offset<KV_FP8>(row0 + gid + 8, chunk));
+            const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                const uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] & 0xFFFFu));
-                const uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(w[j] >> 16));
-                if (j & 1)
-                    mma_16816_f16(s2, qa[4 * p + j], b0, b1);
-                else
-                    mma_16816_f16(s, qa[4 * p + j], b0, b1);
+                const uint32_t a[4] = {e4m3x2_to_f16x2(static_cast<uint16_t>(wa[j] & 0xFFFFu)),
+                                       e4m3x2_to_f16x2(static_cast<uint16_t>(wb[j] & 0xFFFFu)),
+                                       e4m3x2_to_f16x2(static_cast<uint16_t>(wa[j] >> 16)),
+                                       e4m3x2_to_f16x2(static_cast<uint16_t>(wb[j] >> 16))};
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    if ((j & 1) && NT == 1)
+                        mma_16816_f16(s2[t], a, qb[t][4 * p + j][0], qb[t][4 * p + j][1]);
+                    else
+                        mma_16816_f16(s[t], a, qb[t][4 * p + j][0], qb[t][4 * p + j][1]);
+                }
             }
         }
+        // Scores: registers 0/1 are key gid, 2/3 key gid + 8, for heads 2*t4 + e; add the low part.
+        float sc[4];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) s[j] += s2[j];
-        const bool ok0 = gid < G && 2 * t4 < nvalid, ok1 = gid < G && 2 * t4 + 1 < nvalid;
-        const float s0 = ok0 ? (s[0] + s[2]) * kscale : -INFINITY;
-        const float s1 = ok1 ? (s[1] + s[3]) * kscale : -INFINITY;
-        float mx = fmaxf(s0, s1);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float mn = fmaxf(m_run, mx);
-        const float alpha = (mn == -INFINITY) ? 1.f : fast_exp2(m_run - mn);
-        const float p0 = ok0 ? fast_exp2(s0 - mn) : 0.f;
-        const float p1 = ok1 ? fast_exp2(s1 - mn) : 0.f;
-        l_run = fmaf(l_run, alpha, p0 + p1);
-        m_run = mn;
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
-            const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * t4);
-            const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * t4 + 4);
+        for (int r = 0; r < 4; ++r) sc[r] = s[0][r] + s2[0][r];
+        if (G == 8) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) sc[r] += s[NT - 1][r] + s2[NT - 1][r];
+        } else if (G >= 2) {  // column c + G lives in lane t4 + G/2
+#pragma unroll
+            for (int r = 0; r < 4; ++r) sc[r] += __shfl_xor_sync(0xffffffffu, sc[r], G / 2);
+        } else {              // G = 1: column 1 of the same lane
+            sc[0] += sc[1];
+            sc[2] += sc[3];
+        }
+        const bool k0 = gid < nvalid, k1 = gid + 8 < nvalid;
+        float p[4], alpha[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const bool col = G == 8 || 2 * t4 + e < G;
+            const float x0 = (col && k0) ? sc[e] * kscale : -INFINITY;
+            const float x1 = (col && k1) ? sc[2 + e] * kscale : -INFINITY;
+            float mx = fmaxf(x0, x1);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(m_run[e], mx);
+            alpha[e] = (mn == -INFINITY) ? 1.f : fast_exp2(m_run[e] - mn);
+            p[e] = (col && k0) ? fast_exp2(x0 - mn) : 0.f;
+            p[2 + e] = (col && k1) ? fast_exp2(x1 - mn) : 0.f;
+            l_run[e] = fmaf(l_run[e], alpha[e], p[e] + p[2 + e]);
+            m_run[e] = mn;
+        }
+        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
 #pragma unroll
             for (int mt = 0; mt < 16; ++mt) {
-                o[mt][0] *= a_lo;
-                o[mt][1] *= a_hi;
-                o[mt][2] *= a_lo;
-                o[mt][3] *= a_hi;
+                o[mt][0] *= alpha[0];
+                o[mt][1] *= alpha[1];
+                o[mt][2] *= alpha[0];
+                o[mt][3] *= alpha[1];
             }
         }
-        const uint32_t pb = pack_f16(p0, p1);
+        const uint32_t pb0 = movmatrix_trans(pack_f16(p[0], p[1]));   // keys 2*t4, +1 of head gid
+        const uint32_t pb1 = movmatrix_trans(pack_f16(p[2], p[3]));   // keys 8 + 2*t4, +1
         // Rows past the key set may hold NaN codes; 0 * NaN would poison the sum.
-        uint32_t vmask = 0xFFFFFFFFu;
-        if (nvalid < kKeysPerWarp)
-            vmask = (2 * t4 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 1 < nvalid ? 0xFFFF0000u : 0u);
+        uint32_t m01 = 0xFFFFFFFFu, m89 = 0xFFFFFFFFu;
+        if (nvalid < kWK) {
+            m01 = (2 * t4 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 1 < nvalid ? 0xFFFF0000u : 0u);
+            m89 = (2 * t4 + 8 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 9 < nvalid ? 0xFFFF0000u : 0u);
+        }
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
-            const uint4 va = *reinterpret_cast<const uint4 *>(vst + tile_offset(row0 + 2 * t4, 8 * half + gid));
-            const uint4 vb = *reinterpret_cast<const uint4 *>(vst + tile_offset(row0 + 2 * t4 + 1, 8 * half + gid));
-            const uint32_t wa[4] = {va.x, va.y, va.z, va.w}, wb[4] = {vb.x, vb.y, vb.z, vb.w};
+            const int chunk = 8 * half + gid;
+            const uint4 v0 = *reinterpret_cast<const uint4 *>(vst + tile_offset<KV_FP8>(row0 + 2 * t4, chunk));
+            const uint4 v1 = *reinterpret_cast<const uint4 *>(vst + tile_offset<KV_FP8>(row0 + 2 * t4 + 1, chunk));
+            const uint4 v8 = *reinterpret_cast<const uint4 *>(vst + tile_offset<KV_FP8>(row0 + 2 * t4 + 8, chunk));
+            const uint4 v9 = *reinterpret_cast<const uint4 *>(vst + tile_offset<KV_FP8>(row0 + 2 * t4 + 9, chunk));
+            const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+            const uint32_t w8[4] = {v8.x, v8.y, v8.z, v8.w}, w9[4] = {v9.x, v9.y, v9.z, v9.w};
 #pragma unroll
             for (int w = 0; w < 4; ++w) {
-                const uint32_t lo = __byte_perm(wa[w], wb[w], 0x5140);   // a0 b0 a1 b1
-                const uint32_t hi = __byte_perm(wa[w], wb[w], 0x7362);   // a2 b2 a3 b3
-                const int mt = 8 * half + 2 * w;
-                mma_1688_f16(o[mt], e4m3x2_to_f16x2(static_cast<uint16_t>(lo & 0xFFFFu)) & vmask,
-                             e4m3x2_to_f16x2(static_cast<uint16_t>(lo >> 16)) & vmask, pb);
-                mma_1688_f16(o[mt + 1], e4m3x2_to_f16x2(static_cast<uint16_t>(hi & 0xFFFFu)) & vmask,
-                             e4m3x2_to_f16x2(static_cast<uint16_t>(hi >> 16)) & vmask, pb);
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {   // dims 4w + 2q (row gid) and 4w + 2q + 1 (row gid + 8)
+                    const uint32_t sel = q ? 0x7362u : 0x5140u;   // (key a, key b) byte pairs of two dims
+                    const uint32_t x01 = __byte_perm(w0[w], w1[w], sel);
+                    const uint32_t x89 = __byte_perm(w8[w], w9[w], sel);
+                    const uint32_t a[4] = {e4m3x2_to_f16x2(static_cast<uint16_t>(x01 & 0xFFFFu)) & m01,
+                                           e4m3x2_to_f16x2(static_cast<uint16_t>(x01 >> 16)) & m01,
+                                           e4m3x2_to_f16x2(static_cast<uint16_t>(x89 & 0xFFFFu)) & m89,
+                                           e4m3x2_to_f16x2(static_cast<uint16_t>(x89 >> 16)) & m89};
+                    mma_16816_f16(o[8 * half + 2 * w + q], a, pb0, pb1);
+                }
             }
         }
     }
 
     __device__ void store(float *red_o, float *red_m, float *red_l, int warp, int lane) const {
         const int gid = lane >> 2, t4 = lane & 3;
-        float l = l_run;
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
-        if (t4 == 0 && gid < G) {
-            red_m[warp * G + gid] = m_run;
-            red_l[warp * G + gid] = l;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float l = l_run[e];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            const int h = 2 * t4 + e;
+            if (gid == 0 && h < G) {
+                red_m[warp * G + h] = m_run[e];
+                red_l[warp * G + h] = l;
+            }
         }
         const int h0 = 2 * t4, h1 = 2 * t4 + 1;
 #pragma unroll
@@ -617,11 +694,14 @@ struct Fp8MmaConsumer {
 // ------------------------------------------------------------- the kernel --
 
 template <int G, int CONSUMER, int S, int KV>
-__global__ void __launch_bounds__(kThreads, S * kv_stage_bytes(KV) <= kStages * kStageBytes ? 2 : 1)
+__global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kStages * kStageBytes ? 2 : 1)
     attn_layer_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const LayerArgs a) {
-    constexpr int kStage = kv_stage_bytes(KV);     // bytes of one stage (K + V of 32 keys)
+    constexpr int kStage = kv_stage_bytes(KV);     // bytes of one stage (K + V)
+    constexpr int kKeys = kv_stage_keys(KV);       // keys per stage: 32 bf16, 64 E4M3
+    constexpr int kWarpKeys = kKeys / kConsumerWarps;
     constexpr int kBoxes = kv_boxes_per_row(KV);   // 128-byte boxes per K or V row
+    constexpr int kNThreads = kv_threads(KV);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -634,7 +714,8 @@ __global__ void __launch_bounds__(kThreads, S * kv_stage_bytes(KV) <= kStages * 
     uint64_t *full = reinterpret_cast<uint64_t *>(misc + 32);
     uint64_t *empty = full + S;
     int *flag_s = reinterpret_cast<int *>(empty + S);
-    uint8_t *code_s = reinterpret_cast<uint8_t *>(flag_s + 4);                 // [2][256] E4M3 new entry
+    unsigned *rel_s = reinterpret_cast<unsigned *>(flag_s + 4);                // [S] slot releases (folded producer)
+    uint8_t *code_s = reinterpret_cast<uint8_t *>(rel_s + 16);                 // [2][256] E4M3 new entry
 
     const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -663,14 +744,33 @@ __global__ void __launch_bounds__(kThreads, S * kv_stage_bytes(KV) <= kStages * 
     if (chunk >= nchunks) return;  // uniform over the CTA
     const int start = chunk * a.chunk_keys;
     const int end = min(start + a.chunk_keys, n);
-    const int nst = end > start ? (end - start + kStageKeys - 1) / kStageKeys : 0;
+    const int nst = end > start ? (end - start + kKeys - 1) / kKeys : 0;
 
+    // Stage s of the chunk: one lane issues its K and V boxes into slot s % S.
+    auto issue_stage = [&](int s) {
+        const int slot = s % S;
+        uint8_t *st = smem + slot * kStage;
+        mbar_arrive_expect_tx(&full[slot], kStage);
+        const int row = start + s * kKeys;
+#pragma unroll
+        for (int j = 0; j < kBoxes; ++j)
+            tma_load_4d(st + j * kv_box_bytes(KV), &kmap, &full[slot], j * kv_box_cols(KV), row, kvh, b);
+#pragma unroll
+        for (int j = 0; j < kBoxes; ++j)
+            tma_load_4d(st + (kBoxes + j) * kv_box_bytes(KV), &vmap, &full[slot], j * kv_box_cols(KV), row, kvh,
+                        b);
+    };
+    // Test hook: stages from a.drop_stage on are never issued (a copy that never arrives).
+    auto droppable = [&](int s) { return a.drop_stage >= 0 && s >= a.drop_stage; };
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], kConsumerWarps);
+            rel_s[s] = 0u;
         }
         fence_mbar_init();
+        if (!own_producer(KV))  // folded producer: the first S stages go out before the prologue
+            for (int s = 0; s < min(S, nst) && !droppable(s); ++s) issue_stage(s);
     }
     // q of the group, rotated here from bf16 or taken pre-rotated, scaled to log2 units.
     const float2 *cs = a.q_bf16 ? a.table + (size_t)c * (a.rotary_dim >> 1) : nullptr;
@@ -696,31 +796,22 @@ __global__ void __launch_bounds__(kThreads, S * kv_stage_bytes(KV) <= kStages * 
     const bool has_new = a.new_kind != NEW_NONE;
     if (nchunks == 1)
         load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, misc + 2 * kMaxGroup,
-                                   misc + 3 * kMaxGroup, code_s, kThreads);
+                                   misc + 3 * kMaxGroup, code_s, kNThreads);
     __syncthreads();
 
     float *red_o = reinterpret_cast<float *>(smem);             // reuses the stage ring
     float *red_m = red_o + kConsumerWarps * G * kHeadDim;
     float *red_l = red_m + kConsumerWarps * G;
-    if (warp == kConsumerWarps) {
+    if (own_producer(KV) && warp == kConsumerWarps) {
         if (lane == 0) {  // producer: one lane issues every load of the chunk
             for (int s = 0; s < nst; ++s) {
-                if (s == a.drop_stage) break;  // test hook: a copy that never arrives
+                if (droppable(s)) break;
                 const int slot = s % S;
                 if (s >= S && !mbar_wait(&empty[slot], ((s / S) - 1) & 1)) {
                     atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
-                uint8_t *st = smem + slot * kStage;
-                mbar_arrive_expect_tx(&full[slot], kStage);
-                const int row = start + s * kStageKeys;
-#pragma unroll
-                for (int j = 0; j < kBoxes; ++j)
-                    tma_load_4d(st + j * kBoxBytes, &kmap, &full[slot], j * kv_box_cols(KV), row, kvh, b);
-#pragma unroll
-                for (int j = 0; j < kBoxes; ++j)
-                    tma_load_4d(st + (kBoxes + j) * kBoxBytes, &vmap, &full[slot], j * kv_box_cols(KV), row,
-                                kvh, b);
+                issue_stage(s);
             }
         }
         __syncthreads();
@@ -736,11 +827,26 @@ __global__ void __launch_bounds__(kThreads, S * kv_stage_bytes(KV) <= kStages * 
                 break;
             }
             const uint8_t *kst = smem + slot * kStage;
-            const int row0 = warp * kKeysPerWarp;
-            const int nvalid = min(kKeysPerWarp, end - (start + s * kStageKeys + row0));
-            if (nvalid > 0) cons.consume(kst, kst + kBoxes * kBoxBytes, row0, nvalid, lane);
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[slot]);
+            const int row0 = warp * kWarpKeys;
+            const int nvalid = min(kWarpKeys, end - (start + s * kKeys + row0));
+            if (nvalid > 0) cons.consume(kst, kst + kBoxes * kv_box_bytes(KV), row0, nvalid, lane);
+            __syncwarp();  // orders every lane's reads of the slot before lane 0's release
+            if (lane == 0) {
+                if (own_producer(KV)) {
+                    mbar_arrive(&empty[slot]);
+                } else {
+                    // Folded producer: the last of the consumer warps to release the slot
+                    // refills it with stage s + S (release / acquire through the counter,
+                    // then a proxy fence before the async-proxy write).
+                    __threadfence_block();
+                    const unsigned prev = atomicAdd(&rel_s[slot], 1u);
+                    if (prev % kConsumerWarps == kConsumerWarps - 1 && s + S < nst && !droppable(s + S)) {
+                        __threadfence_block();
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        issue_stage(s + S);
+                    }
+                }
+            }
         }
         __syncthreads();  // every stage consumed: the ring is free for the warp merge
         cons.store(red_o, red_m, red_l, warp, lane);
@@ -797,7 +903,7 @@ __global__ void __launch_bounds__(kThreads, S * kv_stage_bytes(KV) <= kStages * 
     float *sink_s = misc + 2 * kMaxGroup;           // [G]
     float *gate_s = misc + 3 * kMaxGroup;           // [G]
     if (nchunks > 1)
-        load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, sink_s, gate_s, code_s, kThreads);
+        load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, sink_s, gate_s, code_s, kNThreads);
     const float2 *pml = reinterpret_cast<const float2 *>(a.part_ml);
     constexpr int kPerLane = 4;
     float2 ml[kPerLane];
@@ -847,11 +953,11 @@ __global__ void __launch_bounds__(kThreads, S * kv_stage_bytes(KV) <= kStages * 
         __syncthreads();
     }
     // Per head: M = max(chunk maxima, new score), chunk weights 2^(m_j - M) and
-    // L = sum of weighted chunk sums (+ the new entry).  Warp w takes heads w, w+5, ...
+    // L = sum of weighted chunk sums (+ the new entry).  Warp w takes heads w, w + warps, ...
     float *wts = reinterpret_cast<float *>(smem);   // [G][nchunks] (the warp buffers are free)
     float *head_s = misc;                           // [G] scale = sink factor * gate / L
     float *wnew_s = misc + kMaxGroup;               // [G] weight of the new entry
-    for (int h = warp; h < G; h += kThreads / 32) {
+    for (int h = warp; h < G; h += kNThreads / 32) {
         const size_t ph = pbase + (size_t)h * a.max_chunks;
         if (h != warp) {  // a second head for this warp: its pairs were not preloaded
 #pragma unroll
@@ -990,7 +1096,7 @@ cudaError_t launch_g(const CUtensorMap *km, const CUtensorMap *vm, const LayerAr
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.max_chunks, a.num_kv_heads, batch);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kv_threads(KV));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -1031,7 +1137,7 @@ cudaError_t launch_kv(const CUtensorMap *km, const CUtensorMap *vm, const LayerA
 // (half-size) stages and so twice the mbarriers.
 size_t layer_smem_bytes(int group, int stages) {
     return 1024 + (size_t)stages * kStageBytes + ((size_t)group * kHeadDim + 4 * kHeadDim + 32) * sizeof(float) +
-           2 * (size_t)(2 * stages) * sizeof(uint64_t) + 16 + 2 * kHeadDim;
+           2 * (size_t)(2 * stages) * sizeof(uint64_t) + 16 + 16 * sizeof(unsigned) + 2 * kHeadDim;
 }
 
 cudaError_t launch_layer(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,

@@ -23,14 +23,18 @@ constexpr int kBoxesPerRow = kHeadDim / kBoxCols;                 // 4
 constexpr int kBoxBytes = kStageKeys * 128;                       // 4 KiB
 constexpr int kStageBytes = 2 * kBoxesPerRow * kBoxBytes;         // K + V: 32 KiB
 
-// Cache element types (hd_kv_dtype).  An FP8 stage holds the same 32 keys in
-// half the bytes, so an FP8 ring has twice the stages in the same shared
-// memory: stage counts above are in bf16 stages.
+// Cache element types (hd_kv_dtype).  A stage is 32 KiB of K + V either way:
+// 32 bf16 keys (four 64-column boxes per row block) or 64 E4M3 keys (two
+// 128-column boxes of 64 rows), so both rings have the same stage counts.
 enum KvType : int32_t { KV_BF16 = 0, KV_FP8 = 1 };
 __host__ __device__ constexpr int kv_elem_bytes(int kv) { return kv == KV_FP8 ? 1 : 2; }
-__host__ __device__ constexpr int kv_box_cols(int kv) { return 128 / kv_elem_bytes(kv); }                       // 64 / 128
-__host__ __device__ constexpr int kv_boxes_per_row(int kv) { return kHeadDim * kv_elem_bytes(kv) / 128; }       // 4 / 2
-__host__ __device__ constexpr int kv_stage_bytes(int kv) { return 2 * kv_boxes_per_row(kv) * kBoxBytes; }       // 32 / 16 KiB
+__host__ __device__ constexpr int kv_stage_keys(int kv) { return kv == KV_FP8 ? 64 : kStageKeys; }   // box rows
+__host__ __device__ constexpr int kv_box_cols(int kv) { return 128 / kv_elem_bytes(kv); }            // 64 / 128
+__host__ __device__ constexpr int kv_boxes_per_row(int kv) { return kHeadDim * kv_elem_bytes(kv) / 128; }  // 4 / 2
+__host__ __device__ constexpr int kv_box_bytes(int kv) { return kv_stage_keys(kv) * 128; }            // 4 / 8 KiB
+__host__ __device__ constexpr int kv_stage_bytes(int kv) { return 2 * kv_boxes_per_row(kv) * kv_box_bytes(kv); }
+static_assert(kv_stage_bytes(KV_BF16) == kStageBytes && kv_stage_bytes(KV_FP8) == kStageBytes,
+              "both cache types use 32 KiB stages");
 constexpr int kChunkMin = 64;
 constexpr int kChunkMax = 2048;
 
