@@ -24,7 +24,7 @@ LIBRARY = os.path.join(PKG, "libhybriddecode.so")
 HD_SLIDING, HD_FULL = 0, 1
 HD_LAYOUT_AUTO, HD_LAYOUT_RING, HD_LAYOUT_ROLL = 0, 1, 2
 HD_CONSUMER_CUDA_CORE, HD_CONSUMER_TENSOR_CORE = 0, 1
-HD_PROFILE_SLIDING, HD_PROFILE_FULL = 1 << HD_SLIDING, 1 << HD_FULL
+HD_PROFILE_SLIDING, HD_PROFILE_FULL, HD_PROFILE_FIRST_ONLY = 1 << HD_SLIDING, 1 << HD_FULL, 4
 HD_KV_BF16, HD_KV_FP8_E4M3 = 0, 1
 STATUS = {0: "HD_OK", 1: "HD_ERR_INVALID_ARG", 2: "HD_ERR_UNSUPPORTED", 3: "HD_ERR_CAPACITY",
           4: "HD_ERR_CUDA", 5: "HD_ERR_STATE"}
@@ -308,7 +308,8 @@ def hybrid_decode_launch_count(ctx: Context) -> int:
 
 
 def hybrid_decode_set_profiling(ctx: Context, mask: int) -> None:
-    """mask of layer types to bracket with events: HD_PROFILE_SLIDING | HD_PROFILE_FULL, or 0."""
+    """mask of layer types to bracket with events: HD_PROFILE_SLIDING | HD_PROFILE_FULL, or 0;
+    with HD_PROFILE_FIRST_ONLY only the first layer of each type per decode_step."""
     _check(_lib.hybrid_decode_set_profiling(ctx.handle, int(mask)), "hybrid_decode_set_profiling")
 
 

@@ -87,6 +87,7 @@ struct hd_ctx {
     int64_t launches = 0;
     std::vector<MapCacheEntry> maps;     // one per layer
     int32_t profile_mask = 0;           // bit (1 << layer type): bracket that type's launches
+    bool profile_seen[2] = {false, false};  // FIRST_ONLY: a layer of that type was bracketed in this step
     std::vector<cudaEvent_t> ev_begin, ev_end;  // [2][kProfileEvents]: per layer type
     size_t ev_used[2] = {0, 0};
 };
@@ -232,6 +233,7 @@ struct LayerCall {
     const float *gate;
     void *out;
     float *lse;
+    bool pdl;               // previous grid in the stream is this step's previous layer kernel
 };
 
 hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream) {
@@ -285,9 +287,11 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
 
     const int type = sliding ? HD_SLIDING : HD_FULL;
     const size_t slot = (size_t)type * kProfileEvents + ctx->ev_used[type];
-    const bool timed = (ctx->profile_mask & (1 << type)) && ctx->ev_used[type] < (size_t)kProfileEvents;
+    const bool timed = (ctx->profile_mask & (1 << type)) && ctx->ev_used[type] < (size_t)kProfileEvents &&
+                       !((ctx->profile_mask & HD_PROFILE_FIRST_ONLY) && ctx->profile_seen[type]);
+    if (timed) ctx->profile_seen[type] = true;
     if (timed && cudaEventRecord(ctx->ev_begin[slot], stream) != cudaSuccess) return HD_ERR_CUDA;
-    st = cuda_status(launch_layer(km, vm, a, L.batch, ctx->group, ctx->consumer, stages, stream));
+    st = cuda_status(launch_layer(km, vm, a, L.batch, ctx->group, ctx->consumer, stages, L.pdl && !timed, stream));
     if (st != HD_OK) return st;
     ++ctx->launches;
     if (timed) {
@@ -511,6 +515,7 @@ hd_status decode_attn_sliding(hd_ctx *ctx, int32_t layer, int32_t batch, const i
     L.gate = gate;
     L.out = out;
     L.lse = lse;
+    ctx->profile_seen[0] = ctx->profile_seen[1] = false;   // each standalone call is its own step
     return launch_layer_call(ctx, L, static_cast<cudaStream_t>(stream));
 }
 
@@ -537,6 +542,7 @@ hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int3
     L.gate = gate;
     L.out = out;
     L.lse = lse;
+    ctx->profile_seen[0] = ctx->profile_seen[1] = false;   // each standalone call is its own step
     return launch_layer_call(ctx, L, static_cast<cudaStream_t>(stream));
 }
 
@@ -546,6 +552,7 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
                       const hd_layer_io *layers, void *stream) {
     if (!ctx || !layers) return HD_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    ctx->profile_seen[0] = ctx->profile_seen[1] = false;
     for (int i = 0; i < ctx->cfg.num_layers; ++i) {
         const hd_layer_io &io = layers[i];
         hd_status st = check_attention(ctx, i, batch, context, io.cache, io.out, io.lse);
@@ -565,6 +572,9 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
         L.gate = io.gate;
         L.out = io.out;
         L.lse = io.lse;
+        // Start streaming while the previous layer drains, unless a roll shift kernel
+        // runs in between (its writes must be complete before this layer reads).
+        L.pdl = i > 0 && !roll;
         if (!sliding) {
             int hint = 0;
             if ((st = full_hint(ctx, max_context_hint, io.cache, &hint)) != HD_OK) return st;
@@ -642,7 +652,8 @@ hd_status hybrid_decode_launch_count(hd_ctx *ctx, int64_t *launches) {
 }
 
 hd_status hybrid_decode_set_profiling(hd_ctx *ctx, int32_t enable) {
-    if (!ctx || enable < 0 || enable > 3) return HD_ERR_INVALID_ARG;
+    if (!ctx || enable < 0 || enable > (HD_PROFILE_SLIDING | HD_PROFILE_FULL | HD_PROFILE_FIRST_ONLY))
+        return HD_ERR_INVALID_ARG;
     if (enable && ctx->ev_begin.empty()) {
         ctx->ev_begin.resize(2 * kProfileEvents);
         ctx->ev_end.resize(2 * kProfileEvents);

@@ -719,11 +719,13 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
 
     const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    // Programmatic dependent launch: the next layer's grid may be scheduled
-    // while this one finishes, but no global memory is touched before every
-    // write of the previous grid in the stream is complete and visible.
+    // Programmatic dependent launch: the next grid in the stream may start as
+    // soon as every CTA of this one has started.  Launched that way (only
+    // behind another layer of the same step, see launch_layer), a CTA reads its
+    // own layer's inputs and streams its own layer's cache -- nothing the
+    // previous grid writes -- and waits for that grid (griddepcontrol.wait)
+    // only before its first global write.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    asm volatile("griddepcontrol.wait;" ::: "memory");
     const int c = a.context[b];
     const float kscale = KV == KV_FP8 ? a.k_scale[kvh] : 1.f;
     const float vscale = KV == KV_FP8 ? a.v_scale[kvh] : 1.f;
@@ -731,6 +733,7 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     const int n = cached_keys(a, c, &bit);
     if (n < 0) {
         if (chunk == 0) {  // this CTA reports and poisons the outputs of the group
+            asm volatile("griddepcontrol.wait;" ::: "memory");
             if (threadIdx.x == 0) atomicOr(a.err, bit);
             for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
                 const int hg = kvh * G + i / kHeadDim;
@@ -852,6 +855,11 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
         cons.store(red_o, red_m, red_l, warp, lane);
         __syncthreads();
     }
+
+    // Everything above only read this layer's own inputs and cache.  The first
+    // global write (partials, tickets, outputs, the stored entry) waits for the
+    // previous grid in the stream to complete and its writes to be visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // Merge the warps into this chunk's partial: kept in shared memory (past the
     // warp buffers) and, when the sequence has several chunks, written out.
@@ -1085,7 +1093,7 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
 
 template <int G, int CONSUMER, int S, int KV>
 cudaError_t launch_g(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
-                     cudaStream_t s) {
+                     bool pdl, cudaStream_t s) {
     static bool configured = false;
     const size_t smem = layer_smem_bytes(G, S * kv_stage_bytes(KV) / kStageBytes);
     if (!configured) {
@@ -1103,32 +1111,32 @@ cudaError_t launch_g(const CUtensorMap *km, const CUtensorMap *vm, const LayerAr
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, attn_layer_kernel<G, CONSUMER, S, KV>, *km, *vm, a);
 }
 
 // S counts stages of the cache's type: an E4M3 ring has twice the bf16 count.
 template <int CONSUMER, int S_BF16, int KV>
 cudaError_t launch_c(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
-                     int group, cudaStream_t s) {
+                     int group, bool pdl, cudaStream_t s) {
     constexpr int S = S_BF16 * kStageBytes / kv_stage_bytes(KV);
     switch (group) {
-    case 1: return launch_g<1, CONSUMER, S, KV>(km, vm, a, batch, s);
-    case 2: return launch_g<2, CONSUMER, S, KV>(km, vm, a, batch, s);
-    case 4: return launch_g<4, CONSUMER, S, KV>(km, vm, a, batch, s);
-    case 8: return launch_g<8, CONSUMER, S, KV>(km, vm, a, batch, s);
+    case 1: return launch_g<1, CONSUMER, S, KV>(km, vm, a, batch, pdl, s);
+    case 2: return launch_g<2, CONSUMER, S, KV>(km, vm, a, batch, pdl, s);
+    case 4: return launch_g<4, CONSUMER, S, KV>(km, vm, a, batch, pdl, s);
+    case 8: return launch_g<8, CONSUMER, S, KV>(km, vm, a, batch, pdl, s);
     default: return cudaErrorInvalidValue;
     }
 }
 
 template <int KV>
 cudaError_t launch_kv(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch, int group,
-                      int consumer, int stages, cudaStream_t s) {
+                      int consumer, int stages, bool pdl, cudaStream_t s) {
     if (stages == kDeepStages)
-        return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA, kDeepStages, KV>(km, vm, a, batch, group, s)
-                                        : launch_c<CONSUMER_FMA, kDeepStages, KV>(km, vm, a, batch, group, s);
-    return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA, kStages, KV>(km, vm, a, batch, group, s)
-                                    : launch_c<CONSUMER_FMA, kStages, KV>(km, vm, a, batch, group, s);
+        return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA, kDeepStages, KV>(km, vm, a, batch, group, pdl, s)
+                                        : launch_c<CONSUMER_FMA, kDeepStages, KV>(km, vm, a, batch, group, pdl, s);
+    return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA, kStages, KV>(km, vm, a, batch, group, pdl, s)
+                                    : launch_c<CONSUMER_FMA, kStages, KV>(km, vm, a, batch, group, pdl, s);
 }
 
 }  // namespace
@@ -1141,9 +1149,9 @@ size_t layer_smem_bytes(int group, int stages) {
 }
 
 cudaError_t launch_layer(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
-                         int group, int consumer, int stages, cudaStream_t s) {
-    return a.kv_type == KV_FP8 ? launch_kv<KV_FP8>(km, vm, a, batch, group, consumer, stages, s)
-                               : launch_kv<KV_BF16>(km, vm, a, batch, group, consumer, stages, s);
+                         int group, int consumer, int stages, bool pdl, cudaStream_t s) {
+    return a.kv_type == KV_FP8 ? launch_kv<KV_FP8>(km, vm, a, batch, group, consumer, stages, pdl, s)
+                               : launch_kv<KV_BF16>(km, vm, a, batch, group, consumer, stages, pdl, s);
 }
 
 }  // namespace hd

@@ -115,8 +115,12 @@ struct RopeArgs {
 cudaError_t launch_rope_append(const RopeArgs &a, int batch, cudaStream_t s);
 cudaError_t launch_roll_window(const RopeArgs &a, int batch, cudaStream_t s);
 // `stages` in bf16 stages (kStages or kDeepStages); a.kv_type picks the kernel.
+// pdl: launch as a programmatic dependent of the previous grid in the stream.
+// Only correct when that grid is another layer kernel of the same step that
+// writes nothing this launch reads before griddepcontrol.wait (its own inputs
+// and its own cache): the kernel starts streaming before that grid is done.
 cudaError_t launch_layer(const CUtensorMap *kmap, const CUtensorMap *vmap, const LayerArgs &a,
-                         int batch, int group, int consumer, int stages, cudaStream_t s);
+                         int batch, int group, int consumer, int stages, bool pdl, cudaStream_t s);
 size_t layer_smem_bytes(int group, int stages);
 
 }  // namespace hd

@@ -162,7 +162,7 @@ extern "C" hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_
     a.window = 0;
     a.max_context = max_context;
     a.drop_stage = -1;
-    return hd::launch_layer(&kmap, &vmap, a, batch, group, hd::CONSUMER_MMA, stages, s) == cudaSuccess
+    return hd::launch_layer(&kmap, &vmap, a, batch, group, hd::CONSUMER_MMA, stages, false, s) == cudaSuccess
                ? HD_OK
                : HD_ERR_CUDA;
 }

@@ -206,7 +206,11 @@ hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int3
  * layer: q is rotated in the attention kernel and the new entry is rotated,
  * scored and stored (appended, or written to its ring slot after the ring was
  * read) by the combine; a roll layout first shifts its window.  `layers` is a
- * host array [num_layers]. */
+ * host array [num_layers].  A layer's kernel may start reading its own
+ * inputs and streaming its own cache while the previous layer of the call is
+ * still running (it writes nothing before that layer is complete), so within
+ * one call no layer's inputs or cache may alias another layer's outputs or
+ * cache.  The first layer waits for all earlier work in the stream. */
 hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_t max_context_hint,
                       const hd_layer_io *layers, void *stream);
 
@@ -234,14 +238,18 @@ hd_status hybrid_decode_device_errors(hd_ctx *ctx, int32_t *flags, void *stream)
 hd_status hybrid_decode_launch_count(hd_ctx *ctx, int64_t *launches);
 
 /* Profiling: `enable` is a mask of layer types, bit (1 << hd_layer_type):
- * HD_PROFILE_SLIDING, HD_PROFILE_FULL, both, or 0 (off).  Attention-kernel
- * launches of the selected types are bracketed by CUDA events on their stream
- * (up to 4096 launches per type between reads); an event between two launches
- * serialises them, so the unselected types keep overlapping launch latency.
+ * HD_PROFILE_SLIDING, HD_PROFILE_FULL, both, or 0 (off), optionally with
+ * HD_PROFILE_FIRST_ONLY: then only the first layer of each selected type in
+ * each decode_step call is bracketed.  Attention-kernel launches of the
+ * selected types are bracketed by CUDA events on their stream (up to 4096
+ * launches per type between reads), and a bracketed launch does not start
+ * before the previous work in the stream is complete (decode_step otherwise
+ * lets a layer start streaming while the previous layer drains), so the
+ * events time the kernel alone and the other layers keep overlapping.
  * hybrid_decode_profile synchronises on the events and returns, for layers of
  * the given hd_layer_type, the summed kernel time and launch count since the
  * last read, then resets that type's records. */
-enum { HD_PROFILE_SLIDING = 1 << HD_SLIDING, HD_PROFILE_FULL = 1 << HD_FULL };
+enum { HD_PROFILE_SLIDING = 1 << HD_SLIDING, HD_PROFILE_FULL = 1 << HD_FULL, HD_PROFILE_FIRST_ONLY = 4 };
 hd_status hybrid_decode_set_profiling(hd_ctx *ctx, int32_t enable);
 hd_status hybrid_decode_profile(hd_ctx *ctx, int32_t layer_type, double *total_ms, int64_t *launches);
 
