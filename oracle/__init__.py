@@ -116,6 +116,10 @@ class Oracle:
         lib.orc_decode_layer.argtypes = [ctypes.POINTER(OrcLayer), _i32p, _u16p, _u16p, _u16p,
                                          ctypes.c_void_p, ctypes.c_void_p, _f32p, _f32p, _f32p, _f32p,
                                          _f64p, _f64p, _f64p, ctypes.c_void_p]
+        lib.orc_decode_tokens.restype = ctypes.c_int
+        lib.orc_decode_tokens.argtypes = [ctypes.POINTER(OrcLayer), ctypes.c_int, _i32p, _u16p, _u16p, _u16p,
+                                          ctypes.c_void_p, ctypes.c_void_p, _f32p, _f32p, _f32p, _f32p,
+                                          _f64p, _f64p]
         self.lib = lib
         self.path = path
 
@@ -237,3 +241,41 @@ class Oracle:
         if rc != 0:
             raise ValueError(f"oracle rejected the layer arguments (code {rc})")
         return {"out": out, "lse": lse, "qrot": qrot, "k_written": kw}
+
+    def decode_tokens(self, *, layer_type: int, layout: int, window: int, rotary_dim: int,
+                      rope_theta: float, context, q, k, v, kcache, vcache, sink=None, gate=None,
+                      k_scale=None, v_scale=None):
+        """T tokens per sequence in one step: q [B,T,Hq,D], k/v [B,T,Hkv,D] (uint16 bf16
+        bits), caches as in decode_layer (updated in place), gate float32 [B,T,Hq] or
+        None.  Returns dict(out [B,T,Hq,D] f64, lse [B,T,Hq] f64)."""
+        for name, a in (("q", q), ("k", k), ("v", v)):
+            if a.dtype != np.uint16 or not a.flags.c_contiguous or a.ndim != 4:
+                raise ValueError(f"{name} must be C-contiguous uint16 [B, T, heads, D]")
+        fp8 = kcache.dtype == np.uint8
+        for name, a in (("kcache", kcache), ("vcache", vcache)):
+            if a.dtype != (np.uint8 if fp8 else np.uint16) or not a.flags.c_contiguous:
+                raise ValueError(f"{name} must be C-contiguous, uint16 bf16 bits or uint8 E4M3 codes")
+        B, T, Hq, D = q.shape
+        Hkv = k.shape[2]
+        cap = kcache.shape[2]
+        ctx = np.ascontiguousarray(context, dtype=np.int32)
+        L = OrcLayer(B, Hq, Hkv, D, layer_type, layout, window, rotary_dim, float(rope_theta),
+                     cap, Hkv * cap * D, KV_FP8_E4M3 if fp8 else KV_BF16)
+        out = np.zeros((B, T, Hq, D))
+        lse = np.zeros((B, T, Hq))
+        sk = None if sink is None else np.ascontiguousarray(sink, dtype=np.float32)
+        gt = None if gate is None else np.ascontiguousarray(gate, dtype=np.float32).reshape(B, T, Hq)
+        ksc = None if k_scale is None else np.ascontiguousarray(k_scale, dtype=np.float32)
+        vsc = None if v_scale is None else np.ascontiguousarray(v_scale, dtype=np.float32)
+        if fp8 and (ksc is None or vsc is None):
+            raise ValueError("an FP8 cache needs k_scale and v_scale")
+        rc = self.lib.orc_decode_tokens(ctypes.byref(L), T, _ptr(ctx, _i32p), _ptr(q, _u16p), _ptr(k, _u16p),
+                                        _ptr(v, _u16p), kcache.ctypes.data, vcache.ctypes.data,
+                                        _ptr(ksc, _f32p) if ksc is not None else None,
+                                        _ptr(vsc, _f32p) if vsc is not None else None,
+                                        _ptr(sk, _f32p) if sk is not None else None,
+                                        _ptr(gt, _f32p) if gt is not None else None,
+                                        _ptr(out, _f64p), _ptr(lse, _f64p))
+        if rc != 0:
+            raise ValueError(f"oracle rejected the layer arguments (code {rc})")
+        return {"out": out, "lse": lse}

@@ -47,6 +47,12 @@
  *       once to e4m3 (nearest, ties to even), finite values beyond the largest
  *       code saturating to +-448.  The new entry is scored as stored (its
  *       dequantised value).
+ *   R15 multi-token decode (the pages' step is one token; several query
+ *       positions per step are an extension, as in speculative verification):
+ *       T new tokens at positions c .. c+T-1 of one sequence compute exactly
+ *       what T single-token steps compute in order -- token t attends
+ *       causally to the layer's key set at position c+t, which holds the
+ *       earlier new tokens, and the cache ends as after the T steps.
  *
  * Every function below names what pins it in the test suite (tests/).
  */
@@ -480,5 +486,48 @@ int orc_decode_layer(const orc_layer *L, const int32_t *context,
 done:
     free(cs); free(sn); free(x); free(qr); free(knew);
     free(keys); free(vals); free(kb); free(kq); free(vq);
+    return rc;
+}
+
+/* ------------------------------------------------- multi-token decode --- */
+
+/* T tokens per sequence in one step (R15): token t of every sequence is the
+ * single-token step at context[b] + t, run in order, so each token sees the
+ * entries the earlier ones stored.  Layouts: q [B][T][Hq][D], k/v
+ * [B][T][Hkv][D], gate [B][T][Hq] or NULL, out [B][T][Hq][D], lse [B][T][Hq].
+ * Pinned by: a brute-force causal key set built from positions (tests). */
+int orc_decode_tokens(const orc_layer *L, int T, const int32_t *context,
+                      const uint16_t *q, const uint16_t *k, const uint16_t *v,
+                      void *kcache, void *vcache, const float *k_scale, const float *v_scale,
+                      const float *sink, const float *gate, double *out, double *lse)
+{
+    const int B = L->batch, Hq = L->num_q_heads, Hkv = L->num_kv_heads, D = L->head_dim;
+    if (T <= 0 || B < 0)
+        return ORC_ERR_ARG;
+    int32_t *ctx = (int32_t *)malloc(sizeof(int32_t) * (size_t)(B + 1));
+    uint16_t *qt = (uint16_t *)malloc(sizeof(uint16_t) * ((size_t)B * Hq * D + 1));
+    uint16_t *kt = (uint16_t *)malloc(sizeof(uint16_t) * ((size_t)B * Hkv * D + 1));
+    uint16_t *vt = (uint16_t *)malloc(sizeof(uint16_t) * ((size_t)B * Hkv * D + 1));
+    float *gt = (float *)malloc(sizeof(float) * ((size_t)B * Hq + 1));
+    double *ot = (double *)malloc(sizeof(double) * ((size_t)B * Hq * D + 1));
+    double *lt = (double *)malloc(sizeof(double) * ((size_t)B * Hq + 1));
+    int rc = ORC_OK;
+    for (int t = 0; t < T && rc == ORC_OK; ++t) {
+        for (int b = 0; b < B; ++b) {
+            ctx[b] = context[b] + t;
+            memcpy(qt + (size_t)b * Hq * D, q + ((size_t)b * T + t) * Hq * D, sizeof(uint16_t) * Hq * D);
+            memcpy(kt + (size_t)b * Hkv * D, k + ((size_t)b * T + t) * Hkv * D, sizeof(uint16_t) * Hkv * D);
+            memcpy(vt + (size_t)b * Hkv * D, v + ((size_t)b * T + t) * Hkv * D, sizeof(uint16_t) * Hkv * D);
+            if (gate)
+                memcpy(gt + (size_t)b * Hq, gate + ((size_t)b * T + t) * Hq, sizeof(float) * Hq);
+        }
+        rc = orc_decode_layer(L, ctx, qt, kt, vt, kcache, vcache, k_scale, v_scale, sink, gate ? gt : NULL,
+                              ot, lt, NULL, NULL);
+        for (int b = 0; b < B && rc == ORC_OK; ++b) {
+            memcpy(out + ((size_t)b * T + t) * Hq * D, ot + (size_t)b * Hq * D, sizeof(double) * Hq * D);
+            memcpy(lse + ((size_t)b * T + t) * Hq, lt + (size_t)b * Hq, sizeof(double) * Hq);
+        }
+    }
+    free(ctx); free(qt); free(kt); free(vt); free(gt); free(ot); free(lt);
     return rc;
 }

@@ -26,6 +26,9 @@ step, vllm/models/hy_v4/nvidia/flashmla_sparse.py for the sink):
                      saturation; FP8 layers against a scipy brute force on the
                      dequantised cache, against the bf16 layer on values both
                      formats hold exactly, and against the history model
+  multi-token (R15)  T tokens per step against a brute force over positions:
+                     token t's key set is every position of its window up to
+                     c+t, and the caches end holding the extended history
 """
 from __future__ import annotations
 
@@ -656,6 +659,68 @@ def check_fp8_history_model(orc):
                 out = sps.softmax(sc) @ vals[h // g]
                 assert np.allclose(r["out"][0, h], out, rtol=1e-12, atol=1e-12), (layer_type, layout, c, h)
                 assert abs(r["lse"][0, h] - sps.logsumexp(sc)) < 1e-12
+
+
+# -------------------------------------------------------------- multi-token --
+
+def _layout_cache(hist_k, hist_v, layer_type, layout, window, cap, upto, Hkv, D):
+    """Cache [1, Hkv, cap, D] holding positions < upto of a history list as the
+    layout keeps them (NaN elsewhere): full at index p, ring at slot p mod cap,
+    roll the last `window` positions in order."""
+    kc = np.full((1, Hkv, cap, D), NAN_BITS, np.uint16)
+    vc = kc.copy()
+    if layer_type == FULL:
+        idx = {p: p for p in range(upto)}
+    elif layout == RING:
+        idx = {p: p % cap for p in range(max(0, upto - cap), upto)}
+    else:
+        lo = max(0, upto - window)
+        idx = {p: p - lo for p in range(lo, upto)}
+    for p, i in idx.items():
+        kc[0, :, i] = hist_k[p]
+        vc[0, :, i] = hist_v[p]
+    return kc, vc
+
+
+def check_decode_tokens_brute_force(orc):
+    """T tokens in one step: token t (position c+t) attends to every position of its
+    window up to c+t -- cached history and the new tokens 0..t -- with its own RoPE;
+    the caches end holding the history extended by the T written entries."""
+    rng = np.random.default_rng(22)
+    Hq, Hkv, D, rot, theta, W = 4, 2, 16, 8, 1e4, 8
+    g = Hq // Hkv
+    for layer_type, layout in ((FULL, 0), (SLIDING, RING), (SLIDING, ROLL)):
+        for c, T in ((3, 4), (6, 5), (13, 6), (0, 3)):
+            cap = (W - 1 if layout == RING else W) if layer_type == SLIDING else c + T + 2
+            hist_k = [_bf16_bits_random(rng, (Hkv, D)) for _ in range(c)]
+            hist_v = [_bf16_bits_random(rng, (Hkv, D)) for _ in range(c)]
+            kc, vc = _layout_cache(hist_k, hist_v, layer_type, layout, W, cap, c, Hkv, D)
+            q = _bf16_bits_random(rng, (1, T, Hq, D))
+            k = _bf16_bits_random(rng, (1, T, Hkv, D))
+            v = _bf16_bits_random(rng, (1, T, Hkv, D))
+            sink = rng.standard_normal(Hq).astype(np.float32)
+            gate = rng.standard_normal((1, T, Hq)).astype(np.float32)
+            r = orc.decode_tokens(layer_type=layer_type, layout=layout, window=W, rotary_dim=rot,
+                                  rope_theta=theta, context=np.array([c], np.int32), q=q, k=k, v=v,
+                                  kcache=kc, vcache=vc, sink=sink, gate=gate)
+            for t in range(T):
+                pos = c + t
+                cs, sn = orc.rope_angles(pos, rot, theta)
+                kr = _rope_complex(_bits_to_f64(k[0, t]), rot, cs, sn)
+                hist_k.append(np.array([[orc.lib.orc_f64_to_bf16(float(x)) for x in row] for row in kr], np.uint16))
+                hist_v.append(v[0, t])
+                lo = max(0, pos - W + 1) if layer_type == SLIDING else 0
+                keys = _bits_to_f64(np.stack(hist_k[lo:pos + 1], axis=1))   # [Hkv, n, D]
+                vals = _bits_to_f64(np.stack(hist_v[lo:pos + 1], axis=1))
+                qr = _rope_complex(_bits_to_f64(q[0, t]), rot, cs, sn)
+                for h in range(Hq):
+                    sc = keys[h // g] @ qr[h] / math.sqrt(D)
+                    lse = sps.logsumexp(sc)
+                    out = sps.softmax(sc) @ vals[h // g] * sps.expit(lse - float(sink[h])) * sps.expit(float(gate[0, t, h]))
+                    assert np.allclose(r["out"][0, t, h], out, rtol=1e-12, atol=1e-12), (layer_type, layout, c, t, h)
+                    assert abs(r["lse"][0, t, h] - lse) < 1e-12, (layer_type, layout, c, t, h)
+            ek, ev = _layout_cache(hist_k, hist_v, layer_type, layout, W, cap, c + T, Hkv, D)
+            assert np.array_equal(kc, ek) and np.array_equal(vc, ev), (layer_type, layout, c, T)
 
 
 # -------------------------------------------------------------- footprint --

@@ -46,6 +46,8 @@ MUTANTS = [
     ("fp8 value scale dropped", "load_cached_row(L, vc, j, vs, vals + n * D);",
      "load_cached_row(L, vc, j, 1.0, vals + n * D);"),
     ("roll shift in elements, not bytes", "memmove(kc, kc + D * esize,", "memmove(kc, kc + D,"),
+    ("tokens share one position", "ctx[b] = context[b] + t;", "ctx[b] = context[b];"),
+    ("tokens read the wrong q", "q + ((size_t)b * T + t) * Hq * D", "q + ((size_t)b * T) * Hq * D"),
 ]
 
 
