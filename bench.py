@@ -213,11 +213,13 @@ def reduce_timing(elapsed_ms: float, units: float, world: int, device=None) -> t
 class Workload:
     """Device-resident inputs of one workload (caches, per-layer q/k/v, outputs)."""
 
-    def __init__(self, name: str, device, seed: int = 0, layout: int = synth.LAYOUT_AUTO, kv: str = "bf16"):
+    def __init__(self, name: str, device, seed: int = 0, layout: int = synth.LAYOUT_AUTO, kv: str = "bf16",
+                 tokens: int = 1):
         import torch
         import full_gqa_decode_gb300 as hd
         spec = synth.WORKLOADS[name]
-        self.name, self.spec, self.layout, self.kv = name, spec, layout, kv
+        self.name, self.spec, self.layout, self.kv, self.tokens = name, spec, layout, kv, tokens
+        tq = (tokens,) if tokens > 1 else ()   # token index of a multi-token step
         fp8 = kv == "fp8"
         self.row_bytes = FP8_ROW_BYTES if fp8 else KV_ROW_BYTES
         self.types = list(spec["layer_types"])
@@ -228,7 +230,7 @@ class Workload:
         self.max_ctx = int(self.context.max())
         sink = synth.sink_vector(rng, spec["sink"], self.Hq)
         self.cfg = hd.Config(layer_types=self.types, num_q_heads=self.Hq, num_kv_heads=self.Hkv,
-                             cache_layout=layout, max_batch=self.B, max_context=self.max_ctx,
+                             cache_layout=layout, max_batch=self.B, max_context=self.max_ctx + tokens - 1,
                              kv_dtype=hd.HD_KV_FP8_E4M3 if fp8 else hd.HD_KV_BF16)
         self.ctx = hd.hybrid_decode_init(self.cfg)
         self.context_d = torch.from_numpy(self.context).to(device)
@@ -236,7 +238,7 @@ class Workload:
         ring = layout != synth.LAYOUT_ROLL
         self.layers, self.io, self.io_gated = [], [], []
         for i, t in enumerate(self.types):
-            cap = (synth.WINDOW - 1 if ring else synth.WINDOW) if t == synth.SLIDING else self.max_ctx + 1
+            cap = (synth.WINDOW - 1 if ring else synth.WINDOW) if t == synth.SLIDING else self.max_ctx + tokens
             kc = torch.empty(self.B, self.Hkv, cap, D, dtype=torch.uint8 if fp8 else torch.bfloat16, device=device)
             vc = torch.empty_like(kc)
             if fp8:  # per-layer, per-kv-head scales; codes of N(0,1) / scale
@@ -249,17 +251,17 @@ class Workload:
                 synth.cuda_normal_bf16_(vc, seed * 1000 + 2 * i + 2)
             g = torch.Generator(device=device)
             g.manual_seed(seed * 1000 + 500 + i)
-            q = torch.randn(self.B, self.Hq, D, generator=g, device=device).to(torch.bfloat16)
-            k = torch.randn(self.B, self.Hkv, D, generator=g, device=device).to(torch.bfloat16)
-            v = torch.randn(self.B, self.Hkv, D, generator=g, device=device).to(torch.bfloat16)
-            out = torch.empty(self.B, self.Hq, D, dtype=torch.bfloat16, device=device)
-            lse = torch.empty(self.B, self.Hq, dtype=torch.float32, device=device)
+            q = torch.randn(self.B, *tq, self.Hq, D, generator=g, device=device).to(torch.bfloat16)
+            k = torch.randn(self.B, *tq, self.Hkv, D, generator=g, device=device).to(torch.bfloat16)
+            v = torch.randn(self.B, *tq, self.Hkv, D, generator=g, device=device).to(torch.bfloat16)
+            out = torch.empty(self.B, *tq, self.Hq, D, dtype=torch.bfloat16, device=device)
+            lse = torch.empty(self.B, *tq, self.Hq, dtype=torch.float32, device=device)
             cache = hd.kv_cache(kc, vc, ks, vs)
             self.layers.append(dict(q=q, k=k, v=v, kc=kc, vc=vc, out=out, lse=lse, cache=cache,
                                     k_scale=ks, v_scale=vs))
             self.io.append(hd.layer_io(q, k, v, cache, self.sink, out, lse))
             # per-step output-gate logits N(0, 1) for the gated variant of the step
-            gate = torch.randn(self.B, self.Hq, generator=g, device=device)
+            gate = torch.randn(self.B, *tq, self.Hq, generator=g, device=device)
             self.layers[-1]["gate"] = gate
             self.io_gated.append(hd.layer_io(q, k, v, cache, self.sink, out, lse, gate=gate))
         self.bytes = step_bytes(self.types, self.context, self.Hkv, layout, self.row_bytes)
@@ -271,8 +273,30 @@ class Workload:
 
     def step(self, stream=None, gated=False):
         import full_gqa_decode_gb300 as hd
-        hd.decode_step(self.ctx, self.context_d, self.io_gated if gated else self.io, self.B, self.max_ctx,
-                       stream)
+        io = self.io_gated if gated else self.io
+        if self.tokens > 1:
+            hd.decode_step_tokens(self.ctx, self.context_d, io, self.B, self.tokens, self.max_ctx, stream)
+        else:
+            hd.decode_step(self.ctx, self.context_d, io, self.B, self.max_ctx, stream)
+
+    def token_pass_bytes(self) -> int:
+        """Scored-KV bytes a multi-token step reads: the tokens of a sequence run in
+        passes of up to 8 query rows per kv head, each pass scoring the cache at
+        context + first token of the pass (earlier passes' entries included)."""
+        tmax, passes, t0 = max(1, 8 // (self.Hq // self.Hkv)), [], 0
+        while t0 < self.tokens:
+            tp = 1
+            while 2 * tp <= tmax and 2 * tp <= self.tokens - t0:
+                tp *= 2
+            passes.append(t0)
+            t0 += tp
+        total = 0
+        for t0 in passes:
+            ctx = self.context + t0
+            for t in self.types:
+                keys = ctx if t == synth.FULL else np.minimum(ctx, synth.WINDOW - 1)
+                total += int(keys.sum()) * self.Hkv * self.row_bytes
+        return total
 
 
 def time_steps(run, steps: int, warmup: int, world: int, device) -> float:
@@ -465,6 +489,9 @@ def run_ours(args, world, rank, local) -> int:
     result = None
     if rank == 0:
         fp8 = fp8_step(device, args, consumer, layout, plain_ms) if args.kv == "bf16" and args.secondary else None
+        multi = (multi_token_steps(device, args, consumer, layout, plain_ms)
+                 if args.kv == "bf16" and args.secondary and args.layout == "ring" and consumer == hd.HD_CONSUMER_TENSOR_CORE
+                 else None)
         cpu = cpu_baseline(wl, device)
         secondary = secondary_batch1(device, args, consumer) if args.secondary else None
         result = {"metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
@@ -487,6 +514,8 @@ def run_ours(args, world, rank, local) -> int:
                                  "overhead_vs_ungated": round(gated_ms / plain_ms - 1.0, 4)}
         if fp8:
             result["fp8_kv"] = fp8
+        if multi:
+            result["multi_token"] = multi
         if secondary:
             result["secondary"] = secondary
         print(json.dumps(result), flush=True)
@@ -596,6 +625,28 @@ def fp8_step(device, args, consumer, layout, bf16_ms) -> dict:
     wl.ctx.close()
     del wl
     torch.cuda.empty_cache()
+    return res
+
+
+def multi_token_steps(device, args, consumer, layout, single_ms) -> list:
+    """The same step decoding T = 2 and 4 tokens per sequence (decode_step_tokens),
+    against T single-token steps (the plain step time)."""
+    import torch
+    import full_gqa_decode_gb300 as hd
+    res = []
+    for T in (2, 4):
+        wl = Workload(args.workload, device, seed=0, layout=layout, tokens=T)
+        hd.hybrid_decode_set_consumer(wl.ctx, consumer)
+        ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
+        if hd.hybrid_decode_device_errors(wl.ctx):
+            raise RuntimeError(f"device error flags in the {T}-token step")
+        kvb = wl.token_pass_bytes()
+        res.append({"tokens": T, "ms_per_step": round(ms, 4), "tokens_per_s": round(wl.B * T / (ms * 1e-3)),
+                    "us_per_token": round(ms * 1e3 / T, 1), "speedup_vs_single_token_steps": round(T * single_ms / ms, 3),
+                    "kv_bytes_read_per_step": kvb, "GBps": round(kvb / (ms * 1e-3) / 1e9, 1)})
+        wl.ctx.close()
+        del wl
+        torch.cuda.empty_cache()
     return res
 
 

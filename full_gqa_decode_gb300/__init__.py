@@ -76,6 +76,7 @@ _SIGS = {
     "decode_attn_sliding": [_P, _i32, _i32, _P, _P, hd_kv_cache, _P, _P, _P, _P, _P],
     "decode_attn_full": [_P, _i32, _i32, _P, _i32, _P, hd_kv_cache, _P, _P, _P, _P, _P],
     "decode_step": [_P, _i32, _P, _i32, _c.POINTER(hd_layer_io), _P],
+    "decode_step_tokens": [_P, _i32, _i32, _P, _i32, _c.POINTER(hd_layer_io), _P],
     "hybrid_decode_device_errors": [_P, _c.POINTER(_i32), _P],
     "hybrid_decode_launch_count": [_P, _c.POINTER(_i64)],
     "hybrid_decode_set_profiling": [_P, _i32],
@@ -119,14 +120,16 @@ def _check_sink(sink, num_q_heads: int, like: torch.Tensor) -> None:
         raise ValueError("sink must be contiguous")
 
 
-def _check_gate(gate, batch: int, num_q_heads: int, like: torch.Tensor) -> None:
-    """Output-gate logits: fp32, shape (batch, num_q_heads), contiguous, on the query's device."""
+def _check_gate(gate, batch: int, num_q_heads: int, like: torch.Tensor, tokens: int | None = None) -> None:
+    """Output-gate logits: fp32, shape (batch, num_q_heads) -- or (batch, tokens,
+    num_q_heads) for a multi-token step -- contiguous, on the query's device."""
     if gate is None:
         return
     if gate.dtype != torch.float32:
         raise ValueError(f"gate must be float32, got {gate.dtype}")
-    if tuple(gate.shape) != (batch, num_q_heads):
-        raise ValueError(f"gate must have shape ({batch}, {num_q_heads}), got {tuple(gate.shape)}")
+    want = (batch, num_q_heads) if tokens is None else (batch, tokens, num_q_heads)
+    if tuple(gate.shape) != want:
+        raise ValueError(f"gate must have shape {want}, got {tuple(gate.shape)}")
     if gate.device != like.device:
         raise ValueError(f"gate and query must be on the same device ({gate.device} vs {like.device})")
     if not gate.is_contiguous():
@@ -280,9 +283,11 @@ def decode_attn_full(ctx: Context, layer: int, context, q_rot, cache: hd_kv_cach
 
 
 def layer_io(q, k, v, cache: hd_kv_cache, sink, out, lse, gate=None) -> hd_layer_io:
+    """One layer's tensors for decode_step (q [B, Hq, D]) or decode_step_tokens
+    (q [B, T, Hq, D]; k/v/out/lse/gate with the same token index)."""
     if sink is not None:
-        _check_sink(sink, q.shape[1], q)
-    _check_gate(gate, q.shape[0], q.shape[1], q)
+        _check_sink(sink, q.shape[-2], q)
+    _check_gate(gate, q.shape[0], q.shape[-2], q, tokens=q.shape[1] if q.dim() == 4 else None)
     _check_batch(cache, q.shape[0])
     return hd_layer_io(_ptr(q), _ptr(k), _ptr(v), cache, _ptr(sink), _ptr(out), _ptr(lse), _ptr(gate))
 
@@ -292,6 +297,15 @@ def decode_step(ctx: Context, context: torch.Tensor, layers: list, batch: int,
     arr = (hd_layer_io * len(layers))(*layers)
     _check(_lib.decode_step(ctx.handle, batch, _ptr(context), max_context_hint, arr, _stream(stream)),
            "decode_step")
+
+
+def decode_step_tokens(ctx: Context, context: torch.Tensor, layers: list, batch: int, num_tokens: int,
+                       max_context_hint: int = 0, stream=None) -> None:
+    """num_tokens new tokens per sequence (q/out [B, T, Hq, D], k/v [B, T, Hkv, D],
+    lse/gate [B, T, Hq]), equal to num_tokens decode_step calls in order."""
+    arr = (hd_layer_io * len(layers))(*layers)
+    _check(_lib.decode_step_tokens(ctx.handle, batch, num_tokens, _ptr(context), max_context_hint, arr,
+                                   _stream(stream)), "decode_step_tokens")
 
 
 def hybrid_decode_device_errors(ctx: Context, stream=None) -> int:

@@ -9,6 +9,7 @@
 // per query head, NULL for no sink).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <climits>
 #include <cmath>
 #include <cstdint>
@@ -234,6 +235,7 @@ struct LayerCall {
     void *out;
     float *lse;
     bool pdl;               // previous grid in the stream is this step's previous layer kernel
+    int tokens = 1, token0 = 0, total_tokens = 1;   // multi-token decode: this pass's tokens
 };
 
 hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream) {
@@ -245,7 +247,8 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
                &num_chunks, &stages);
     if ((int64_t)L.batch * num_chunks > ctx->part_slots) return HD_ERR_CAPACITY;
     // The combine keeps a weight per (head, chunk) plus a float4 row per head in the stage ring.
-    if (((size_t)ctx->group * num_chunks + 3) * sizeof(float) + (size_t)ctx->group * 64 * 16 >
+    const size_t rows = (size_t)ctx->group * L.tokens;   // query rows per kv head
+    if ((rows * num_chunks + 3) * sizeof(float) + rows * 64 * 16 + (L.total_tokens > 1 ? kMtNewBytes : 0) >
         (size_t)kStages * kStageBytes)
         return HD_ERR_CAPACITY;
     const bool sliding = ctx->layer_types[L.layer] == HD_SLIDING;
@@ -284,6 +287,9 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     a.window = ctx->cfg.sliding_window;
     a.max_context = ctx->cfg.max_context;
     a.drop_stage = ctx->drop_stage;
+    a.tokens = L.tokens;
+    a.token0 = L.token0;
+    a.total_tokens = L.total_tokens;
 
     const int type = sliding ? HD_SLIDING : HD_FULL;
     const size_t slot = (size_t)type * kProfileEvents + ctx->ev_used[type];
@@ -317,11 +323,14 @@ hd_status check_attention(const hd_ctx *ctx, int layer, int batch, const int32_t
     return HD_OK;
 }
 
-hd_status full_hint(const hd_ctx *ctx, int32_t max_context_hint, const hd_kv_cache &cache, int *hint) {
+// Bound on every context[b] of a full-layer call (0: max_context); the last of
+// `tokens` new tokens must have a table row and a cache entry.
+hd_status full_hint(const hd_ctx *ctx, int32_t max_context_hint, const hd_kv_cache &cache, int *hint,
+                    int tokens = 1) {
     if (max_context_hint < 0) return HD_ERR_INVALID_ARG;
-    *hint = max_context_hint == 0 ? ctx->cfg.max_context : max_context_hint;
-    if (*hint > ctx->cfg.max_context) return HD_ERR_CAPACITY;
-    if (*hint + 1 > cache.capacity) return HD_ERR_CAPACITY;
+    *hint = max_context_hint == 0 ? ctx->cfg.max_context - (tokens - 1) : max_context_hint;
+    if (*hint < 0 || *hint + tokens - 1 > ctx->cfg.max_context) return HD_ERR_CAPACITY;
+    if (*hint + tokens > cache.capacity) return HD_ERR_CAPACITY;
     return HD_OK;
 }
 
@@ -417,8 +426,10 @@ hd_status hybrid_decode_init(const hd_config *cfg, hd_ctx **out_ctx) {
         if (s > slots) slots = s;
     }
     ctx->part_slots = slots;
-    bool ok = cudaMalloc(&ctx->part_o, (size_t)slots * Hq * kHeadDim * sizeof(float)) == cudaSuccess &&
-              cudaMalloc(&ctx->part_ml, (size_t)slots * Hq * sizeof(float2)) == cudaSuccess &&
+    // Partials hold up to kMaxGroup rows per kv head (query heads, or heads x tokens).
+    const size_t rows = (size_t)Hkv * kMaxGroup;
+    bool ok = cudaMalloc(&ctx->part_o, (size_t)slots * rows * kHeadDim * sizeof(float)) == cudaSuccess &&
+              cudaMalloc(&ctx->part_ml, (size_t)slots * rows * sizeof(float2)) == cudaSuccess &&
               cudaMalloc(&ctx->counters, (size_t)B * Hkv * sizeof(int32_t)) == cudaSuccess &&
               cudaMemset(ctx->counters, 0, (size_t)B * Hkv * sizeof(int32_t)) == cudaSuccess &&
               cudaMalloc(&ctx->err, sizeof(int32_t)) == cudaSuccess &&
@@ -550,7 +561,19 @@ hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int3
 // rotated, scored and stored by the combine (roll layouts shift first).
 hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_t max_context_hint,
                       const hd_layer_io *layers, void *stream) {
-    if (!ctx || !layers) return HD_ERR_INVALID_ARG;
+    return decode_step_tokens(ctx, batch, 1, context, max_context_hint, layers, stream);
+}
+
+// T tokens per sequence: each layer runs in passes of up to kMaxGroup / group
+// tokens (a power of two), the tokens of a pass being extra query rows that
+// share one stream of the cache.  A pass commits its entries, so the next pass
+// (launched in full stream order) sees them as cached keys at context + token0.
+hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, const int32_t *context,
+                             int32_t max_context_hint, const hd_layer_io *layers, void *stream) {
+    if (!ctx || !layers || num_tokens < 1 || num_tokens > kMaxTokens) return HD_ERR_INVALID_ARG;
+    const bool any_sliding = std::count(ctx->layer_types.begin(), ctx->layer_types.end(), (int)HD_SLIDING) > 0;
+    if (num_tokens > 1 && ((any_sliding && ctx->sliding_layout == HD_LAYOUT_ROLL) || ctx->consumer != CONSUMER_MMA))
+        return HD_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ctx->profile_seen[0] = ctx->profile_seen[1] = false;
     for (int i = 0; i < ctx->cfg.num_layers; ++i) {
@@ -577,8 +600,8 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
         L.pdl = i > 0 && !roll;
         if (!sliding) {
             int hint = 0;
-            if ((st = full_hint(ctx, max_context_hint, io.cache, &hint)) != HD_OK) return st;
-            L.max_keys = hint;
+            if ((st = full_hint(ctx, max_context_hint, io.cache, &hint, num_tokens)) != HD_OK) return st;
+            L.max_keys = hint + num_tokens - 1;
             L.key_set = KEYS_FULL_PREV;
             L.new_kind = NEW_ROTATE;
             L.commit = COMMIT_APPEND;
@@ -614,7 +637,17 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
             L.new_kind = NEW_NONE;
             L.commit = COMMIT_NONE;
         }
-        if ((st = launch_layer_call(ctx, L, s)) != HD_OK) return st;
+        const int tmax = kMaxGroup / ctx->group;
+        L.total_tokens = num_tokens;
+        for (int t0 = 0; t0 < num_tokens;) {
+            int tp = 1;
+            while (2 * tp <= tmax && 2 * tp <= num_tokens - t0) tp *= 2;
+            L.tokens = tp;
+            L.token0 = t0;
+            if (t0 > 0) L.pdl = false;   // the previous pass wrote this layer's cache
+            if ((st = launch_layer_call(ctx, L, s)) != HD_OK) return st;
+            t0 += tp;
+        }
     }
     return HD_OK;
 }

@@ -55,6 +55,9 @@ constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
 // [warps][G][256] + (m, l) and the combine weights start at 0; this chunk's
 // merged partial [G][256] + (m, l) sits past both.
 constexpr int kOwnPartialOffset = 48 * 1024;
+// Multi-token combine: the new entries of up to kMaxTokens tokens (K and V
+// values, E4M3 codes) and the per-row weights of the new entries sit in the
+// last kMtNewBytes of the (then free) stage ring.
 
 // ------------------------------------------------------------ PTX helpers --
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
@@ -250,7 +253,8 @@ __device__ __forceinline__ void load_combine_inputs(const LayerArgs &a, int b, i
 __device__ __forceinline__ int cached_keys(const LayerArgs &a, int c, int *bit) {
     *bit = 0;
     if (c < 0) { *bit = HD_DEVERR_CONTEXT_NEGATIVE; return -1; }
-    if (c > a.max_context) { *bit = HD_DEVERR_CONTEXT_PLAN; return -1; }
+    const int last = c + max(a.tokens, 1) - 1;   // position of the last new token
+    if (last > a.max_context) { *bit = HD_DEVERR_CONTEXT_PLAN; return -1; }
     int n;
     switch (a.key_set) {
     case KEYS_RING: n = min(c, a.capacity); break;
@@ -258,7 +262,7 @@ __device__ __forceinline__ int cached_keys(const LayerArgs &a, int c, int *bit) 
     case KEYS_FULL_CACHED: n = c + 1; break;
     default: n = c; break;  // KEYS_FULL_PREV
     }
-    if (n > a.capacity || (a.commit == COMMIT_APPEND && c >= a.capacity)) {
+    if (n > a.capacity || (a.commit == COMMIT_APPEND && last >= a.capacity)) {
         *bit = HD_DEVERR_CONTEXT_CAPACITY;
         return -1;
     }
@@ -267,6 +271,19 @@ __device__ __forceinline__ int cached_keys(const LayerArgs &a, int c, int *bit) 
 }
 
 // ---------------------------------------------------------- the consumers --
+
+// Ring window of the query rows of a multi-token step: row r (token t) must
+// not see the t oldest ring entries -- positions c-511 .. c+t-512 left its
+// window -- which sit in `cnt[r]` consecutive slots from slot `first`.
+struct RowMask {
+    int first = 0, cap = 1;
+    const int *cnt = nullptr;   // [rows] in shared memory
+    __device__ __forceinline__ bool hidden(int key, int count) const {
+        int rel = key - first;
+        if (rel < 0) rel += cap;
+        return rel < count;
+    }
+};
 
 // CUDA-core consumer: lane owns dims [8*lane, 8*lane+8) of every row; each
 // score is a warp-shuffle reduction.  With an E4M3 cache the rows hold codes:
@@ -299,8 +316,10 @@ struct FmaConsumer {
         }
     }
 
+    __device__ void set_mask(const RowMask &, int) {}
+
     // Rows [row0, row0 + kWK) of a stage; the first nvalid are keys.
-    __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane) {
+    __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane, int) {
         constexpr int KB = G >= 8 ? 4 : 8;  // keeps scores, q and acc in registers
 #pragma unroll
         for (int sb = 0; sb < kWK; sb += KB) {
@@ -376,11 +395,18 @@ struct FmaConsumer {
 // accumulator of S is, register for register, the B operand of
 // O^T += V^T P^T (m16n8k8: dims on M, 8 keys on K, heads on N), whose A
 // operand is V read with ldmatrix.trans.
-template <int G>
+template <int G, bool MT = false>
 struct MmaConsumer {
     uint32_t qa[16][4];
     float o[16][4];   // O^T tile mt: rows dims 16mt + gid (+8), cols heads 2*t4 (+1)
     float m_run, l_run;  // for head gid; l_run sums this lane's keys only
+    RowMask mask;
+    int mcnt;            // MT: ring entries hidden from row gid
+
+    __device__ void set_mask(const RowMask &m, int lane) {
+        mask = m;
+        mcnt = (lane >> 2) < G ? m.cnt[lane >> 2] : 0;
+    }
 
     __device__ void init(const float *q_s, int lane, float) {
         const int gid = lane >> 2, t4 = lane & 3;
@@ -410,7 +436,7 @@ struct MmaConsumer {
         l_run = 0.f;
     }
 
-    __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane) {
+    __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane, int key0) {
         const int gid = lane >> 2, t4 = lane & 3;
         const int lrow = row0 + (lane & 7), lsub = lane >> 3;
         const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
@@ -425,7 +451,11 @@ struct MmaConsumer {
         }
 #pragma unroll
         for (int j = 0; j < 4; ++j) s[j] += s2[j];
-        const bool ok0 = gid < G && 2 * t4 < nvalid, ok1 = gid < G && 2 * t4 + 1 < nvalid;
+        bool ok0 = gid < G && 2 * t4 < nvalid, ok1 = gid < G && 2 * t4 + 1 < nvalid;
+        if (MT) {
+            ok0 = ok0 && !mask.hidden(key0 + 2 * t4, mcnt);
+            ok1 = ok1 && !mask.hidden(key0 + 2 * t4 + 1, mcnt);
+        }
         const float s0 = ok0 ? s[0] + s[2] : -INFINITY;
         const float s1 = ok1 ? s[1] + s[3] : -INFINITY;
         float mx = fmaxf(s0, s1);
@@ -509,7 +539,7 @@ struct MmaConsumer {
 // 2*t4+8, 2*t4+9; byte_perm pairs two keys' bytes of one dim, which is one
 // E4M3x2 A register.  Tile mt covers, on row gid, dim
 // 128*(mt / 8) + 16*gid + 2*(mt % 8) and, on row gid + 8, the next dim.
-template <int G>
+template <int G, bool MT = false>
 struct Fp8MmaConsumer {
     static constexpr int NT = G == 8 ? 2 : 1;   // n-tiles of q columns
     static constexpr int kWK = 16;              // keys per warp per stage
@@ -517,6 +547,14 @@ struct Fp8MmaConsumer {
     float o[16][4];                              // O^T tile mt: dims (see above) x heads 2*t4 (+1)
     float m_run[2], l_run[2];                    // heads 2*t4 + e; l_run sums this lane's keys only
     float kscale;
+    RowMask mask;
+    int mcnt[2];                                 // MT: ring entries hidden from rows 2*t4 + e
+
+    __device__ void set_mask(const RowMask &m, int lane) {
+        mask = m;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) mcnt[e] = 2 * (lane & 3) + e < G ? m.cnt[2 * (lane & 3) + e] : 0;
+    }
 
     __device__ void init(const float *q_s, int lane, float k_scale) {
         const int gid = lane >> 2, t4 = lane & 3;
@@ -560,7 +598,7 @@ struct Fp8MmaConsumer {
         }
     }
 
-    __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane) {
+    __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane, int key0) {
         const int gid = lane >> 2, t4 = lane & 3;
         // S^T = K Q^T.  With one q tile, even and odd k-steps go to two accumulators
         // (half the dependent chain); two tiles are two chains already.
@@ -609,16 +647,21 @@ struct Fp8MmaConsumer {
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
             const bool col = G == 8 || 2 * t4 + e < G;
-            const float x0 = (col && k0) ? sc[e] * kscale : -INFINITY;
-            const float x1 = (col && k1) ? sc[2 + e] * kscale : -INFINITY;
+            bool v0 = col && k0, v1 = col && k1;
+            if (MT) {
+                v0 = v0 && !mask.hidden(key0 + gid, mcnt[e]);
+                v1 = v1 && !mask.hidden(key0 + gid + 8, mcnt[e]);
+            }
+            const float x0 = v0 ? sc[e] * kscale : -INFINITY;
+            const float x1 = v1 ? sc[2 + e] * kscale : -INFINITY;
             float mx = fmaxf(x0, x1);
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
             const float mn = fmaxf(m_run[e], mx);
             alpha[e] = (mn == -INFINITY) ? 1.f : fast_exp2(m_run[e] - mn);
-            p[e] = (col && k0) ? fast_exp2(x0 - mn) : 0.f;
-            p[2 + e] = (col && k1) ? fast_exp2(x1 - mn) : 0.f;
+            p[e] = v0 ? fast_exp2(x0 - mn) : 0.f;
+            p[2 + e] = v1 ? fast_exp2(x1 - mn) : 0.f;
             l_run[e] = fmaf(l_run[e], alpha[e], p[e] + p[2 + e]);
             m_run[e] = mn;
         }
@@ -693,7 +736,10 @@ struct Fp8MmaConsumer {
 
 // ------------------------------------------------------------- the kernel --
 
-template <int G, int CONSUMER, int S, int KV>
+// G: query rows per kv head -- the GQA group, or with MT (multi-token) the
+// group times a.tokens tokens of the same sequence, row r = token r / (G /
+// a.tokens), head r % (G / a.tokens).
+template <int G, int CONSUMER, int S, int KV, bool MT>
 __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kStages * kStageBytes ? 2 : 1)
     attn_layer_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const LayerArgs a) {
@@ -716,6 +762,7 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     int *flag_s = reinterpret_cast<int *>(empty + S);
     unsigned *rel_s = reinterpret_cast<unsigned *>(flag_s + 4);                // [S] slot releases (folded producer)
     uint8_t *code_s = reinterpret_cast<uint8_t *>(rel_s + 16);                 // [2][256] E4M3 new entry
+    int *mcnt_s = reinterpret_cast<int *>(code_s + 2 * kHeadDim);               // [8] MT ring masks
 
     const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -726,7 +773,15 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     // previous grid writes -- and waits for that grid (griddepcontrol.wait)
     // only before its first global write.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const int c = a.context[b];
+    // Tokens of this launch: one, or (MT) a.tokens tokens at positions c .. c + ntok - 1.
+    const int ntok = MT ? a.tokens : 1;
+    const int Gm = G / ntok;                               // model heads per kv head
+    const int c = a.context[b] + (MT ? a.token0 : 0);
+    // Row r of q / out / lse / gate in units of head vectors.
+    auto qrow = [&](int r) -> size_t {
+        if (!MT) return (size_t)b * a.num_q_heads + kvh * G + r;
+        return ((size_t)b * a.total_tokens + a.token0 + r / Gm) * a.num_q_heads + kvh * Gm + r % Gm;
+    };
     const float kscale = KV == KV_FP8 ? a.k_scale[kvh] : 1.f;
     const float vscale = KV == KV_FP8 ? a.v_scale[kvh] : 1.f;
     int bit = 0;
@@ -736,9 +791,9 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
             asm volatile("griddepcontrol.wait;" ::: "memory");
             if (threadIdx.x == 0) atomicOr(a.err, bit);
             for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
-                const int hg = kvh * G + i / kHeadDim;
-                a.out[((size_t)b * a.num_q_heads + hg) * kHeadDim + i % kHeadDim] = __float2bfloat16_rn(NAN);
-                if (i % kHeadDim == 0) a.lse[(size_t)b * a.num_q_heads + hg] = NAN;
+                const size_t r = qrow(i / kHeadDim);
+                a.out[r * kHeadDim + i % kHeadDim] = __float2bfloat16_rn(NAN);
+                if (i % kHeadDim == 0) a.lse[r] = NAN;
             }
         }
         return;
@@ -779,7 +834,7 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     const float2 *cs = a.q_bf16 ? a.table + (size_t)c * (a.rotary_dim >> 1) : nullptr;
     for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
         const int h = i / kHeadDim, d = i % kHeadDim;
-        const size_t row = ((size_t)b * a.num_q_heads + kvh * G + h) * kHeadDim;
+        const size_t row = qrow(h) * kHeadDim;
         float x;
         if (a.q_bf16 == nullptr) {
             x = a.q_rot[row + d];
@@ -789,7 +844,7 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
             const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
             const float x1 = __bfloat162float(a.q_bf16[row + j]);
             const float x2 = __bfloat162float(a.q_bf16[row + j + half]);
-            const float2 t = cs[j];
+            const float2 t = cs[(MT ? (size_t)(h / Gm) * half : 0) + j];   // row of position c + token
             x = d < half ? fmaf(x1, t.x, -x2 * t.y) : fmaf(x2, t.x, x1 * t.y);
         }
         q_s[i] = x * kQScale;
@@ -797,9 +852,20 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     // A sequence with a single chunk is combined by this CTA: fetch the
     // combine's inputs now, in the same round as q.
     const bool has_new = a.new_kind != NEW_NONE;
-    if (nchunks == 1)
+    if (!MT && nchunks == 1)
         load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, misc + 2 * kMaxGroup,
                                    misc + 3 * kMaxGroup, code_s, kNThreads);
+    // MT ring layers: row r (token t) does not see the t oldest ring entries (the
+    // ones its window has passed); rows of a full layer see the whole cache.
+    if (MT && threadIdx.x < G) {
+        const int t = threadIdx.x / Gm;
+        mcnt_s[threadIdx.x] =
+            a.key_set == KEYS_RING ? (c >= a.capacity ? t : max(0, c + t - a.capacity)) : 0;
+    }
+    RowMask mask;
+    mask.first = c >= a.capacity ? c % a.capacity : 0;
+    mask.cap = a.capacity;
+    mask.cnt = mcnt_s;
     __syncthreads();
 
     float *red_o = reinterpret_cast<float *>(smem);             // reuses the stage ring
@@ -820,9 +886,10 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
         __syncthreads();
         __syncthreads();
     } else {
-        using Mma = typename std::conditional<KV == KV_FP8, Fp8MmaConsumer<G>, MmaConsumer<G>>::type;
+        using Mma = typename std::conditional<KV == KV_FP8, Fp8MmaConsumer<G, MT>, MmaConsumer<G, MT>>::type;
         typename std::conditional<CONSUMER == CONSUMER_MMA, Mma, FmaConsumer<G, KV>>::type cons;
         cons.init(q_s, lane, kscale);
+        if (MT) cons.set_mask(mask, lane);
         for (int s = 0; s < nst; ++s) {
             const int slot = s % S;
             if (!mbar_wait(&full[slot], (s / S) & 1)) {
@@ -832,7 +899,8 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
             const uint8_t *kst = smem + slot * kStage;
             const int row0 = warp * kWarpKeys;
             const int nvalid = min(kWarpKeys, end - (start + s * kKeys + row0));
-            if (nvalid > 0) cons.consume(kst, kst + kBoxes * kv_box_bytes(KV), row0, nvalid, lane);
+            if (nvalid > 0)
+                cons.consume(kst, kst + kBoxes * kv_box_bytes(KV), row0, nvalid, lane, start + s * kKeys + row0);
             __syncwarp();  // orders every lane's reads of the slot before lane 0's release
             if (lane == 0) {
                 if (own_producer(KV)) {
@@ -863,7 +931,8 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
 
     // Merge the warps into this chunk's partial: kept in shared memory (past the
     // warp buffers) and, when the sequence has several chunks, written out.
-    const size_t pbase = ((size_t)b * a.num_q_heads + kvh * G) * a.max_chunks;
+    // Partials: G rows per (sequence, kv head), num_kv_heads * G rows per sequence.
+    const size_t pbase = ((size_t)b * a.num_kv_heads * G + kvh * G) * a.max_chunks;
     float *own_o = reinterpret_cast<float *>(smem + kOwnPartialOffset);   // [G][256]
     float2 *own_ml = reinterpret_cast<float2 *>(own_o + G * kHeadDim);    // [G]
     for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
@@ -910,8 +979,21 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     // fetched them), and each warp's chunk maxima and sums.
     float *sink_s = misc + 2 * kMaxGroup;           // [G]
     float *gate_s = misc + 3 * kMaxGroup;           // [G]
-    if (nchunks > 1)
+    if (!MT && nchunks > 1)
         load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, sink_s, gate_s, code_s, kNThreads);
+    if (MT && threadIdx.x < G) {   // per row: the sink of its head, the gate logit of its token and head
+        sink_s[threadIdx.x] = a.sink ? a.sink[kvh * Gm + threadIdx.x % Gm] : 0.f;
+        gate_s[threadIdx.x] = a.gate ? a.gate[qrow(threadIdx.x)] : 0.f;
+    }
+    // New entries of the ntok tokens: values as scored (knew_t), V values (or
+    // V codes' values for E4M3, vnew_t), codes, and per-row new-entry weights.
+    uint8_t *mt_base = smem + S * kStage - kMtNewBytes;
+    float *knew_t = MT ? reinterpret_cast<float *>(mt_base) : knew_s;                      // [ntok][256]
+    float *vnew_t = MT ? knew_t + kMaxTokens * kHeadDim : vnew_s;                            // [ntok][256]
+    uint8_t *code_t = MT ? reinterpret_cast<uint8_t *>(vnew_t + kMaxTokens * kHeadDim) : code_s;
+    const int vcode_off = MT ? kMaxTokens * kHeadDim : kHeadDim;                             // V codes
+    constexpr int WN = MT ? kMaxTokens : 1;                                                  // wnew_t row stride
+    float *wnew_t = MT ? reinterpret_cast<float *>(code_t + 2 * kMaxTokens * kHeadDim) : misc + kMaxGroup;
     const float2 *pml = reinterpret_cast<const float2 *>(a.part_ml);
     constexpr int kPerLane = 4;
     float2 ml[kPerLane];
@@ -927,35 +1009,50 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     }
     __syncthreads();
     if (has_new) {
-        for (int d = threadIdx.x; d < kHeadDim; d += blockDim.x) {
+        for (int idx = threadIdx.x; idx < ntok * kHeadDim; idx += blockDim.x) {
+            const int t = idx / kHeadDim, d = idx % kHeadDim;
+            // Raw k of token t at dim i and its rotary row (MT reads them here; a
+            // single token's were fetched with the combine's other inputs).
+            const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(a.new_k) +
+                                      ((size_t)(b * a.total_tokens + a.token0 + t) * a.num_kv_heads + kvh) * kHeadDim;
+            const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(a.new_v) +
+                                      ((size_t)(b * a.total_tokens + a.token0 + t) * a.num_kv_heads + kvh) * kHeadDim;
+            auto kraw = [&](int i) -> double { return MT ? (double)__bfloat162float(kg[i]) : (double)kraw_s[i]; };
+            auto tab = [&](int j) -> float2 {
+                return MT ? a.table[(size_t)(c + t) * (a.rotary_dim >> 1) + j] : tab_s[j];
+            };
+            const float vraw = MT ? __bfloat162float(vg[d]) : vnew_s[d];
             if (KV == KV_FP8) {
                 // E4M3 entry: quantise (fp64 rotation, one division, one rounding) unless staged;
                 // score it as stored (code * scale) and keep V in code units.
                 if (a.new_kind == NEW_ROTATE) {
-                    double y = kraw_s[d];
+                    double y = kraw(d);
                     if (d < a.rotary_dim) {
                         const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
-                        const double x1 = kraw_s[j], x2 = kraw_s[j + half];
-                        const double cc = tab_s[j].x, ss = tab_s[j].y;
+                        const double x1 = kraw(j), x2 = kraw(j + half);
+                        const float2 cs2 = tab(j);
+                        const double cc = cs2.x, ss = cs2.y;
                         y = d < half ? __dsub_rn(__dmul_rn(x1, cc), __dmul_rn(x2, ss))
                                      : __dadd_rn(__dmul_rn(x2, cc), __dmul_rn(x1, ss));
                     }
-                    code_s[d] = e4m3_from_f64(__ddiv_rn(y, (double)kscale));
-                    code_s[kHeadDim + d] = e4m3_from_f64(__ddiv_rn((double)vnew_s[d], (double)vscale));
+                    code_t[t * kHeadDim + d] = e4m3_from_f64(__ddiv_rn(y, (double)kscale));
+                    code_t[vcode_off + t * kHeadDim + d] = e4m3_from_f64(__ddiv_rn((double)vraw, (double)vscale));
                 }
-                knew_s[d] = e4m3_to_f32(code_s[d]) * kscale;
-                vnew_s[d] = e4m3_to_f32(code_s[kHeadDim + d]);
+                knew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[t * kHeadDim + d]) * kscale;
+                vnew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[vcode_off + t * kHeadDim + d]);
             } else {
                 float kn;
                 if (a.new_kind == NEW_STAGED || d >= a.rotary_dim) {
-                    kn = kraw_s[d];
+                    kn = (float)kraw(d);
                 } else {  // rotate the new key in fp64 from the fp32 table, round once to bf16
                     const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
-                    const double x1 = kraw_s[j], x2 = kraw_s[j + half];
-                    const double cc = tab_s[j].x, ss = tab_s[j].y;
+                    const double x1 = kraw(j), x2 = kraw(j + half);
+                    const float2 cs2 = tab(j);
+                    const double cc = cs2.x, ss = cs2.y;
                     kn = f64_to_bf16_value(d < half ? x1 * cc - x2 * ss : x2 * cc + x1 * ss);
                 }
-                knew_s[d] = kn;
+                knew_t[t * kHeadDim + d] = kn;
+                vnew_t[t * kHeadDim + d] = vraw;
             }
         }
         __syncthreads();
@@ -964,7 +1061,6 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     // L = sum of weighted chunk sums (+ the new entry).  Warp w takes heads w, w + warps, ...
     float *wts = reinterpret_cast<float *>(smem);   // [G][nchunks] (the warp buffers are free)
     float *head_s = misc;                           // [G] scale = sink factor * gate / L
-    float *wnew_s = misc + kMaxGroup;               // [G] weight of the new entry
     for (int h = warp; h < G; h += kNThreads / 32) {
         const size_t ph = pbase + (size_t)h * a.max_chunks;
         if (h != warp) {  // a second head for this warp: its pairs were not preloaded
@@ -975,13 +1071,20 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
                 if (j < nchunks) ml[r] = nchunks == 1 ? own_ml[h] : __ldcg(pml + ph + j);
             }
         }
+        // Scores of the new entries row h sees: its own token's and (MT) the earlier tokens'.
+        const int th = MT ? h / Gm : 0;
         float s_new = -INFINITY;
         if (has_new) {
-            float t = 0.f;
-            for (int d = lane; d < kHeadDim; d += 32) t = fmaf(q_s[h * kHeadDim + d], knew_s[d], t);
+            for (int j = 0; j <= th; ++j) {
+                float t = 0.f;
+                for (int d = lane; d < kHeadDim; d += 32)
+                    t = fmaf(q_s[h * kHeadDim + d], knew_t[j * kHeadDim + d], t);
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-            s_new = t;
+                for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+                if (lane == 0) wnew_t[h * WN + j] = t;
+                s_new = fmaxf(s_new, t);
+            }
+            __syncwarp();
         }
         float M = s_new;
 #pragma unroll
@@ -1007,18 +1110,21 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
         }
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
-        const float w_new = has_new ? fast_exp2(s_new - M) : 0.f;
+        float w_new = 0.f;   // lane j <= th: weight of new entry j
+        if (has_new && lane <= th) w_new = fast_exp2(wnew_t[h * WN + lane] - M);
+        __syncwarp();
+        if (has_new && lane <= th) wnew_t[h * WN + lane] = w_new;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) w_new += __shfl_xor_sync(0xffffffffu, w_new, off);
         L += w_new;
         if (lane == 0) {
-            const int hg = kvh * G + h;
             const float lse = (M + fast_log2(L)) * kLn2;
             // exp(lse) / (exp(lse) + exp(sink)) = 1 / (1 + 2^((sink - lse) * log2 e))
             float f = a.sink ? 1.f / (1.f + fast_exp2((sink_s[h] - lse) * kLog2e)) : 1.f;
             // output gate: sigmoid(g) = 1 / (1 + 2^(-g * log2 e)); lse is not gated
             if (a.gate) f *= 1.f / (1.f + fast_exp2(-gate_s[h] * kLog2e));
             head_s[h] = f / L * vscale;   // FP8: partials and the new value are in V-code units
-            wnew_s[h] = w_new;
-            a.lse[(size_t)b * a.num_q_heads + hg] = lse;
+            a.lse[qrow(h)] = lse;
         }
     }
     __syncthreads();
@@ -1062,42 +1168,51 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
         for (int h = 0; h < G; ++h) {
             const float4 o1 = half_s[h * 64 + dq];
             float o[4] = {acc[h].x + o1.x, acc[h].y + o1.y, acc[h].z + o1.z, acc[h].w + o1.w};
-            const float sc = head_s[h], wn = wnew_s[h];
+            const float sc = head_s[h];
+            if (has_new) {
+                const int th = MT ? h / Gm : 0;
+                for (int j = 0; j <= th; ++j) {
+                    const float wn = wnew_t[h * WN + j];
+                    const float4 vn = *reinterpret_cast<const float4 *>(vnew_t + j * kHeadDim + 4 * dq);
+                    o[0] = fmaf(wn, vn.x, o[0]);
+                    o[1] = fmaf(wn, vn.y, o[1]);
+                    o[2] = fmaf(wn, vn.z, o[2]);
+                    o[3] = fmaf(wn, vn.w, o[3]);
+                }
+            }
             __nv_bfloat16 r[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if (has_new) o[i] = fmaf(wn, vnew_s[4 * dq + i], o[i]);
-                r[i] = __float2bfloat16_rn(o[i] * sc);
-            }
+            for (int i = 0; i < 4; ++i) r[i] = __float2bfloat16_rn(o[i] * sc);
             uint2 packed;
             packed.x = (uint32_t)__bfloat16_as_ushort(r[0]) | ((uint32_t)__bfloat16_as_ushort(r[1]) << 16);
             packed.y = (uint32_t)__bfloat16_as_ushort(r[2]) | ((uint32_t)__bfloat16_as_ushort(r[3]) << 16);
-            *reinterpret_cast<uint2 *>(a.out + ((size_t)b * a.num_q_heads + kvh * G + h) * kHeadDim + 4 * dq) = packed;
+            *reinterpret_cast<uint2 *>(a.out + qrow(h) * kHeadDim + 4 * dq) = packed;
         }
     }
-    // Store the new entry now that every chunk of this (sequence, kv head) has read the cache.
+    // Store the new entries now that every chunk of this (sequence, kv head) has read the cache.
     if (has_new && a.commit != COMMIT_NONE) {
-        const int slot = a.commit == COMMIT_RING ? c % a.capacity : c;
-        const size_t o = (size_t)b * a.seq_stride + ((size_t)kvh * a.capacity + slot) * kHeadDim;
-        for (int d = threadIdx.x; d < kHeadDim; d += blockDim.x) {
+        for (int idx = threadIdx.x; idx < ntok * kHeadDim; idx += blockDim.x) {
+            const int t = idx / kHeadDim, d = idx % kHeadDim;
+            const int slot = a.commit == COMMIT_RING ? (c + t) % a.capacity : c + t;
+            const size_t o = (size_t)b * a.seq_stride + ((size_t)kvh * a.capacity + slot) * kHeadDim + d;
             if (KV == KV_FP8) {
-                static_cast<uint8_t *>(a.cache_k)[o + d] = code_s[d];
-                static_cast<uint8_t *>(a.cache_v)[o + d] = code_s[kHeadDim + d];
-            } else {  // exact: knew_s and vnew_s hold bf16 values
-                static_cast<__nv_bfloat16 *>(a.cache_k)[o + d] = __float2bfloat16_rn(knew_s[d]);
-                static_cast<__nv_bfloat16 *>(a.cache_v)[o + d] = __float2bfloat16_rn(vnew_s[d]);
+                static_cast<uint8_t *>(a.cache_k)[o] = code_t[t * kHeadDim + d];
+                static_cast<uint8_t *>(a.cache_v)[o] = code_t[vcode_off + t * kHeadDim + d];
+            } else {  // exact: the values are bf16 values
+                static_cast<__nv_bfloat16 *>(a.cache_k)[o] = __float2bfloat16_rn(knew_t[t * kHeadDim + d]);
+                static_cast<__nv_bfloat16 *>(a.cache_v)[o] = __float2bfloat16_rn(vnew_t[t * kHeadDim + d]);
             }
         }
     }
 }
 
-template <int G, int CONSUMER, int S, int KV>
+template <int G, int CONSUMER, int S, int KV, bool MT>
 cudaError_t launch_g(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
                      bool pdl, cudaStream_t s) {
     static bool configured = false;
     const size_t smem = layer_smem_bytes(G, S * kv_stage_bytes(KV) / kStageBytes);
     if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER, S, KV>,
+        cudaError_t e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER, S, KV, MT>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
         configured = true;
@@ -1112,7 +1227,7 @@ cudaError_t launch_g(const CUtensorMap *km, const CUtensorMap *vm, const LayerAr
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, attn_layer_kernel<G, CONSUMER, S, KV>, *km, *vm, a);
+    return cudaLaunchKernelEx(&cfg, attn_layer_kernel<G, CONSUMER, S, KV, MT>, *km, *vm, a);
 }
 
 // S counts stages of the cache's type: an E4M3 ring has twice the bf16 count.
@@ -1120,11 +1235,21 @@ template <int CONSUMER, int S_BF16, int KV>
 cudaError_t launch_c(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,
                      int group, bool pdl, cudaStream_t s) {
     constexpr int S = S_BF16 * kStageBytes / kv_stage_bytes(KV);
+    if (a.total_tokens > 1) {   // a pass of a multi-token step: tensor-core consumer, rows = group x tokens
+        if (CONSUMER != CONSUMER_MMA) return cudaErrorInvalidValue;
+        switch (group * a.tokens) {
+        case 1: return launch_g<1, CONSUMER_MMA, S, KV, true>(km, vm, a, batch, pdl, s);
+        case 2: return launch_g<2, CONSUMER_MMA, S, KV, true>(km, vm, a, batch, pdl, s);
+        case 4: return launch_g<4, CONSUMER_MMA, S, KV, true>(km, vm, a, batch, pdl, s);
+        case 8: return launch_g<8, CONSUMER_MMA, S, KV, true>(km, vm, a, batch, pdl, s);
+        default: return cudaErrorInvalidValue;
+        }
+    }
     switch (group) {
-    case 1: return launch_g<1, CONSUMER, S, KV>(km, vm, a, batch, pdl, s);
-    case 2: return launch_g<2, CONSUMER, S, KV>(km, vm, a, batch, pdl, s);
-    case 4: return launch_g<4, CONSUMER, S, KV>(km, vm, a, batch, pdl, s);
-    case 8: return launch_g<8, CONSUMER, S, KV>(km, vm, a, batch, pdl, s);
+    case 1: return launch_g<1, CONSUMER, S, KV, false>(km, vm, a, batch, pdl, s);
+    case 2: return launch_g<2, CONSUMER, S, KV, false>(km, vm, a, batch, pdl, s);
+    case 4: return launch_g<4, CONSUMER, S, KV, false>(km, vm, a, batch, pdl, s);
+    case 8: return launch_g<8, CONSUMER, S, KV, false>(km, vm, a, batch, pdl, s);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -1145,7 +1270,8 @@ cudaError_t launch_kv(const CUtensorMap *km, const CUtensorMap *vm, const LayerA
 // (half-size) stages and so twice the mbarriers.
 size_t layer_smem_bytes(int group, int stages) {
     return 1024 + (size_t)stages * kStageBytes + ((size_t)group * kHeadDim + 4 * kHeadDim + 32) * sizeof(float) +
-           2 * (size_t)(2 * stages) * sizeof(uint64_t) + 16 + 16 * sizeof(unsigned) + 2 * kHeadDim;
+           2 * (size_t)(2 * stages) * sizeof(uint64_t) + 16 + 16 * sizeof(unsigned) + 2 * kHeadDim +
+           kMaxGroup * sizeof(int);
 }
 
 cudaError_t launch_layer(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,

@@ -35,6 +35,9 @@ __host__ __device__ constexpr int kv_box_bytes(int kv) { return kv_stage_keys(kv
 __host__ __device__ constexpr int kv_stage_bytes(int kv) { return 2 * kv_boxes_per_row(kv) * kv_box_bytes(kv); }
 static_assert(kv_stage_bytes(KV_BF16) == kStageBytes && kv_stage_bytes(KV_FP8) == kStageBytes,
               "both cache types use 32 KiB stages");
+constexpr int kMaxTokens = 8;     // tokens per sequence of one multi-token step
+// Shared-memory bytes the multi-token combine keeps at the end of the ring.
+constexpr int kMtNewBytes = 2 * kMaxTokens * kHeadDim * 4 + 2 * kMaxTokens * kHeadDim + kMaxGroup * kMaxTokens * 4;
 constexpr int kChunkMin = 64;
 constexpr int kChunkMax = 2048;
 
@@ -90,6 +93,11 @@ struct LayerArgs {
     int32_t chunk_keys, max_chunks;
     int32_t window, max_context;
     int32_t drop_stage;            // test hook: producers stop issuing at this stage (-1: off)
+    // Multi-token decode: this launch takes `tokens` tokens (1: the single-token
+    // step) of `total_tokens` per sequence, starting at token `token0`, at
+    // positions context + token0 + t; q/k/v/out/lse/gate then carry a token index
+    // after the batch index.
+    int32_t tokens, token0, total_tokens;
 };
 
 // Partial RoPE of q and the new k, and the K/V store.

@@ -214,6 +214,23 @@ hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int3
 hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_t max_context_hint,
                       const hd_layer_io *layers, void *stream);
 
+/* Multi-token decode (an extension: the pages' step is one token): num_tokens
+ * (1..8) new tokens per sequence at positions context[b] .. context[b] +
+ * num_tokens - 1, with the same results as num_tokens decode_step calls in
+ * order -- token t attends causally to its window, which holds the earlier new
+ * tokens -- as in speculative verification.  Layouts gain a token index after
+ * the batch index: q, out [batch][num_tokens][num_q_heads][head_dim]; k, v
+ * [batch][num_tokens][num_kv_heads][head_dim]; lse, gate
+ * [batch][num_tokens][num_q_heads].  The tokens of a sequence are extra query
+ * rows sharing one read of the cache, up to 8 rows per kv head per pass
+ * (group 4: two tokens per pass).  Full layers append num_tokens entries;
+ * sliding ring layers write slots (c + t) mod (window-1) after reading.
+ * HD_ERR_UNSUPPORTED for num_tokens > 1 with a roll layout or the CUDA-core
+ * consumer; for full layers max_context_hint bounds context[b] (0 means
+ * max_context - num_tokens + 1). */
+hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, const int32_t *context,
+                             int32_t max_context_hint, const hd_layer_io *layers, void *stream);
+
 /* Inner loop of the attention kernels (same results within the stated
  * tolerance; the default is the tensor-core one):
  *   HD_CONSUMER_CUDA_CORE   fp32 FMA with warp-shuffle reductions;
