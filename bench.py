@@ -483,6 +483,10 @@ def run_ours(args, world, rank, local) -> int:
     # against the ungated step timed the same way (no profiling events)
     plain_ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
     gated_ms = time_steps(lambda: wl.step(gated=True), args.steps, args.warmup, 1, device)
+    # the same step with every layer in full stream order (no early start)
+    hd.hybrid_decode_set_layer_overlap(wl.ctx, False)
+    serial_ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
+    hd.hybrid_decode_set_layer_overlap(wl.ctx, True)
     if hd.hybrid_decode_device_errors(wl.ctx):
         raise RuntimeError("device error flags during the gated step")
 
@@ -512,6 +516,9 @@ def run_ours(args, world, rank, local) -> int:
                                  "value": round(wl.bytes / (gated_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                                  "ungated_ms_per_step": round(plain_ms, 4),
                                  "overhead_vs_ungated": round(gated_ms / plain_ms - 1.0, 4)}
+        result["layers_in_stream_order"] = {
+            "ms_per_step": round(serial_ms, 4), "value": round(wl.bytes / (serial_ms * 1e-3) / 1e9, 1),
+            "unit": "GB/s", "note": "no layer starts before the previous one is complete"}
         if fp8:
             result["fp8_kv"] = fp8
         if multi:

@@ -85,6 +85,7 @@ _SIGS = {
     "decode_attn_full_static_scratch": [_i32, _i32, _i32, _P, _i32, _P, hd_kv_cache, _P, _P, _P, _P],
     "hybrid_decode_read_probe": [_P, _i64, _P],
     "hybrid_decode_inject_lost_copy": [_P, _i32],
+    "hybrid_decode_set_layer_overlap": [_P, _i32],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -333,6 +334,11 @@ def hybrid_decode_profile(ctx: Context, layer_type: int = HD_FULL) -> tuple[floa
     _check(_lib.hybrid_decode_profile(ctx.handle, layer_type, ctypes.byref(ms), ctypes.byref(n)),
            "hybrid_decode_profile")
     return ms.value, n.value
+
+
+def hybrid_decode_set_layer_overlap(ctx: Context, enable: bool) -> None:
+    """Whether decode_step lets a layer start before the previous one finishes (default on)."""
+    _check(_lib.hybrid_decode_set_layer_overlap(ctx.handle, int(bool(enable))), "hybrid_decode_set_layer_overlap")
 
 
 def hybrid_decode_set_consumer(ctx: Context, consumer: int) -> None:

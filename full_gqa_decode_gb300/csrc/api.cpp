@@ -85,6 +85,7 @@ struct hd_ctx {
     int32_t *err = nullptr;
     int consumer = CONSUMER_MMA;
     int32_t drop_stage = -1;             // test hook, see hybrid_decode_inject_lost_copy
+    bool layer_overlap = true;           // decode_step: layers start before the previous one finishes
     int64_t launches = 0;
     std::vector<MapCacheEntry> maps;     // one per layer
     int32_t profile_mask = 0;           // bit (1 << layer type): bracket that type's launches
@@ -297,7 +298,8 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
                        !((ctx->profile_mask & HD_PROFILE_FIRST_ONLY) && ctx->profile_seen[type]);
     if (timed) ctx->profile_seen[type] = true;
     if (timed && cudaEventRecord(ctx->ev_begin[slot], stream) != cudaSuccess) return HD_ERR_CUDA;
-    st = cuda_status(launch_layer(km, vm, a, L.batch, ctx->group, ctx->consumer, stages, L.pdl && !timed, stream));
+    st = cuda_status(launch_layer(km, vm, a, L.batch, ctx->group, ctx->consumer, stages,
+                                  L.pdl && !timed && ctx->layer_overlap, stream));
     if (st != HD_OK) return st;
     ++ctx->launches;
     if (timed) {
@@ -649,6 +651,12 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
             t0 += tp;
         }
     }
+    return HD_OK;
+}
+
+hd_status hybrid_decode_set_layer_overlap(hd_ctx *ctx, int32_t enable) {
+    if (!ctx || (enable != 0 && enable != 1)) return HD_ERR_INVALID_ARG;
+    ctx->layer_overlap = enable != 0;
     return HD_OK;
 }
 

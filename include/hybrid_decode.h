@@ -231,6 +231,14 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
 hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, const int32_t *context,
                              int32_t max_context_hint, const hd_layer_io *layers, void *stream);
 
+/* Layer overlap in decode_step / decode_step_tokens (default 1): a layer's
+ * kernel starts reading its inputs and streaming its cache while the previous
+ * layer drains, and waits for it only before its first write.  decode_step
+ * takes every layer's q up front; in a model whose next q depends on this
+ * layer's output only the cache prefetch part of that overlap applies.  0
+ * runs every layer in full stream order (measurement, comparison). */
+hd_status hybrid_decode_set_layer_overlap(hd_ctx *ctx, int32_t enable);
+
 /* Inner loop of the attention kernels (same results within the stated
  * tolerance; the default is the tensor-core one):
  *   HD_CONSUMER_CUDA_CORE   fp32 FMA with warp-shuffle reductions;

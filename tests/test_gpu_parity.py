@@ -240,3 +240,24 @@ def test_decode_step_multistep_lockstep(hd, orc, layout):
     for i in range(len(types)):
         assert_bits_equal(dev[i][0], host[i][0], f"layer {i} K cache")
         assert_bits_equal(dev[i][1], host[i][1], f"layer {i} V cache")
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_layer_overlap_changes_no_bit(hd, kv):
+    """decode_step with and without the layer overlap (a layer starting before the
+    previous one finishes) computes the same bits: outputs, lse and caches."""
+    import bench
+    dev = torch.device("cuda")
+    runs = []
+    for overlap in (True, False):
+        wl = bench.Workload("block4_b16_c512_32768", dev, seed=3, kv=kv)
+        hd.hybrid_decode_set_layer_overlap(wl.ctx, overlap)
+        wl.step()
+        torch.cuda.synchronize()
+        assert hd.hybrid_decode_device_errors(wl.ctx) == 0
+        runs.append([(synth.bits(L["out"]), L["lse"].cpu().numpy(), synth.bits(L["kc"]), synth.bits(L["vc"]))
+                     for L in wl.layers])
+        wl.ctx.close()
+    for i, (a, b) in enumerate(zip(*runs)):
+        for x, y in zip(a, b):
+            assert np.array_equal(x, y), f"layer {i} differs with the overlap"
