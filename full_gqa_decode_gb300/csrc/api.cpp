@@ -22,7 +22,8 @@
 
 using namespace hd;
 
-// Chunk size: the smallest power of two (64 .. kChunkMax keys) that gives about
+// Chunk size: the smallest power of two (64 .. chunk_max keys: 2048 bf16, 4096
+// E4M3, i.e. the same bytes) that gives about
 // one CTA per SM over the grid for the longest sequence bound.  If that grid
 // fits in one CTA per SM, it runs so, with the deep ring (one CTA streams as
 // much as two); otherwise the plan aims at two resident CTAs per SM with the
@@ -31,13 +32,14 @@ using namespace hd;
 // filling whole waves with shorter ones); batch 1 gets many short chunks.
 // Chunks grow further if the workspace bound requires it.
 void hd::plan_split(int64_t batch, int64_t num_kv_heads, int64_t max_keys, int64_t num_sms,
-                    int64_t max_slots, int32_t *chunk_keys, int32_t *num_chunks, int32_t *stages) {
+                    int64_t max_slots, int32_t *chunk_keys, int32_t *num_chunks, int32_t *stages,
+                    int64_t chunk_max) {
     auto chunks = [&](int64_t tt) { return max_keys > 0 ? (max_keys + tt - 1) / tt : 1; };
     auto pick = [&](int64_t target) {
         const int64_t want = (batch * num_kv_heads * max_keys + target - 1) / target;
         int64_t t = kChunkMin;
-        while (t < want && t < kChunkMax) t *= 2;
-        while (t < kChunkMax && batch * chunks(t) > max_slots) t *= 2;
+        while (t < want && t < chunk_max) t *= 2;
+        while (t < chunk_max && batch * chunks(t) > max_slots) t *= 2;
         return t;
     };
     int64_t t = pick(num_sms);
@@ -245,7 +247,7 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     if (st != HD_OK) return st;
     int32_t chunk_keys = 0, num_chunks = 0, stages = kStages;
     plan_split(L.batch, ctx->cfg.num_kv_heads, L.max_keys, ctx->num_sms, ctx->part_slots, &chunk_keys,
-               &num_chunks, &stages);
+               &num_chunks, &stages, ctx->kv_type == KV_FP8 ? 2 * kChunkMax : kChunkMax);
     if ((int64_t)L.batch * num_chunks > ctx->part_slots) return HD_ERR_CAPACITY;
     // The combine keeps a weight per (head, chunk) plus a float4 row per head in the stage ring.
     const size_t rows = (size_t)ctx->group * L.tokens;   // query rows per kv head

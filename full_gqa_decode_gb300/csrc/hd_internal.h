@@ -43,8 +43,11 @@ constexpr int kChunkMax = 2048;
 
 // Split plan: keys per chunk (a power of two from kChunkMin to kChunkMax) and
 // chunks per sequence for `max_keys` keys, keeping batch * chunks <= max_slots.
+// chunk_max: kChunkMax for bf16 caches; E4M3 caches use twice as many keys per
+// chunk (the same bytes per CTA), which measured 10 % faster at 131k contexts.
 void plan_split(int64_t batch, int64_t num_kv_heads, int64_t max_keys, int64_t num_sms,
-                int64_t max_slots, int32_t *chunk_keys, int32_t *num_chunks, int32_t *stages = nullptr);
+                int64_t max_slots, int32_t *chunk_keys, int32_t *num_chunks, int32_t *stages = nullptr,
+                int64_t chunk_max = kChunkMax);
 
 // Which cache rows the split pass scores for sequence b with c = context[b].
 enum KeySet : int32_t {
