@@ -584,7 +584,8 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
         const hd_layer_io &io = layers[i];
         hd_status st = check_attention(ctx, i, batch, context, io.cache, io.out, io.lse);
         if (st != HD_OK) return st;
-        if (!io.q || !io.k || !io.v) return HD_ERR_INVALID_ARG;
+        if (!io.q || !io.k || !io.v || !aligned16(io.q) || !aligned16(io.k) || !aligned16(io.v))
+            return HD_ERR_INVALID_ARG;
         const bool sliding = ctx->layer_types[i] == HD_SLIDING;
         const bool roll = sliding && ctx->sliding_layout == HD_LAYOUT_ROLL;
         LayerCall L{};

@@ -220,27 +220,29 @@ __device__ __forceinline__ float f64_to_bf16_value(double x) {
 
 // Loads what the combine needs from global memory: the new entry (raw k and
 // v for NEW_ROTATE, the staged entry otherwise: bf16 values, or E4M3 codes
-// kept in code_s [2][256]), its rotary row at position c, and the group's
-// sink values and output-gate logits.  Threads [0, nthreads) share the work.
+// kept in code_s [2][256]) and the group's sink values and output-gate
+// logits.  (The rotary row at position c is loaded with q.)  Needs 64 threads.
 template <int G, int KV>
 __device__ __forceinline__ void load_combine_inputs(const LayerArgs &a, int b, int kvh, int c, float *kraw_s,
                                                     float *vnew_s, float2 *tab_s, float *sink_s, float *gate_s,
-                                                    uint8_t *code_s, int nthreads) {
+                                                    uint8_t *code_s) {
     const int t = threadIdx.x;
-    if (a.new_kind != NEW_NONE) {
+    if (a.new_kind != NEW_NONE) {   // one 16-byte load per thread, the K row then the V row
         const size_t e = ((size_t)b * a.num_kv_heads + kvh) * kHeadDim;
-        for (int d = t; d < kHeadDim; d += nthreads) {
-            if (KV == KV_FP8 && a.new_kind == NEW_STAGED) {
-                code_s[d] = static_cast<const uint8_t *>(a.new_k)[e + d];
-                code_s[kHeadDim + d] = static_cast<const uint8_t *>(a.new_v)[e + d];
-            } else {
-                kraw_s[d] = __bfloat162float(static_cast<const __nv_bfloat16 *>(a.new_k)[e + d]);
-                vnew_s[d] = __bfloat162float(static_cast<const __nv_bfloat16 *>(a.new_v)[e + d]);
+        if (KV == KV_FP8 && a.new_kind == NEW_STAGED) {   // 256 codes per row
+            if (t < 32) {
+                const uint8_t *src = static_cast<const uint8_t *>(t < 16 ? a.new_k : a.new_v) + e;
+                reinterpret_cast<uint4 *>(code_s + (t < 16 ? 0 : kHeadDim))[t & 15] =
+                    reinterpret_cast<const uint4 *>(src)[t & 15];
             }
+        } else if (t < 64) {                               // 256 bf16 per row
+            const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(t < 32 ? a.new_k : a.new_v) + e;
+            float f[8];
+            unpack_bf16x8(reinterpret_cast<const uint4 *>(src)[t & 31], f);
+            float4 *dst = reinterpret_cast<float4 *>((t < 32 ? kraw_s : vnew_s) + (t & 31) * 8);
+            dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+            dst[1] = make_float4(f[4], f[5], f[6], f[7]);
         }
-        if (a.new_kind == NEW_ROTATE)
-            for (int j = t; j < (a.rotary_dim >> 1); j += nthreads)
-                tab_s[j] = a.table[(size_t)c * (a.rotary_dim >> 1) + j];
     }
     if (t < G) {
         sink_s[t] = a.sink ? a.sink[kvh * G + t] : 0.f;
@@ -803,6 +805,66 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     const int start = chunk * a.chunk_keys;
     const int end = min(start + a.chunk_keys, n);
     const int nst = end > start ? (end - start + kKeys - 1) / kKeys : 0;
+    // New entries of the ntok tokens: values as scored (knew_t), V values (or
+    // V codes' values for E4M3, vnew_t), codes, and per-row new-entry weights.
+    uint8_t *mt_base = smem + S * kStage - kMtNewBytes;
+    float *knew_t = MT ? reinterpret_cast<float *>(mt_base) : knew_s;                      // [ntok][256]
+    float *vnew_t = MT ? knew_t + kMaxTokens * kHeadDim : vnew_s;                            // [ntok][256]
+    uint8_t *code_t = MT ? reinterpret_cast<uint8_t *>(vnew_t + kMaxTokens * kHeadDim) : code_s;
+    const int vcode_off = MT ? kMaxTokens * kHeadDim : kHeadDim;                             // V codes
+    constexpr int WN = MT ? kMaxTokens : 1;                                                  // wnew_t row stride
+    float *wnew_t = MT ? reinterpret_cast<float *>(code_t + 2 * kMaxTokens * kHeadDim) : misc + kMaxGroup;
+    // Makes the new entries of the ntok tokens: the key rotated in fp64 and rounded
+    // once to bf16, or quantised to E4M3 (fp64 rotation, one division, one
+    // rounding; V too), each scored as stored; E4M3 V stays in code units.
+    auto make_new_entries = [&]() {
+        for (int idx = threadIdx.x; idx < ntok * kHeadDim; idx += blockDim.x) {
+            const int t = idx / kHeadDim, d = idx % kHeadDim;
+            // Raw k of token t at dim i and its rotary row (MT reads them here; a
+            // single token's were fetched with the combine's other inputs).
+            const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(a.new_k) +
+                                      ((size_t)(b * a.total_tokens + a.token0 + t) * a.num_kv_heads + kvh) * kHeadDim;
+            const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(a.new_v) +
+                                      ((size_t)(b * a.total_tokens + a.token0 + t) * a.num_kv_heads + kvh) * kHeadDim;
+            auto kraw = [&](int i) -> double { return MT ? (double)__bfloat162float(kg[i]) : (double)kraw_s[i]; };
+            auto tab = [&](int j) -> float2 {
+                return MT ? a.table[(size_t)(c + t) * (a.rotary_dim >> 1) + j] : tab_s[j];
+            };
+            const float vraw = MT ? __bfloat162float(vg[d]) : vnew_s[d];
+            if (KV == KV_FP8) {
+                // E4M3 entry: quantise (fp64 rotation, one division, one rounding) unless staged;
+                // score it as stored (code * scale) and keep V in code units.
+                if (a.new_kind == NEW_ROTATE) {
+                    double y = kraw(d);
+                    if (d < a.rotary_dim) {
+                        const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
+                        const double x1 = kraw(j), x2 = kraw(j + half);
+                        const float2 cs2 = tab(j);
+                        const double cc = cs2.x, ss = cs2.y;
+                        y = d < half ? __dsub_rn(__dmul_rn(x1, cc), __dmul_rn(x2, ss))
+                                     : __dadd_rn(__dmul_rn(x2, cc), __dmul_rn(x1, ss));
+                    }
+                    code_t[t * kHeadDim + d] = e4m3_quotient(y, (double)kscale);
+                    code_t[vcode_off + t * kHeadDim + d] = e4m3_quotient((double)vraw, (double)vscale);
+                }
+                knew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[t * kHeadDim + d]) * kscale;
+                vnew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[vcode_off + t * kHeadDim + d]);
+            } else {
+                float kn;
+                if (a.new_kind == NEW_STAGED || d >= a.rotary_dim) {
+                    kn = (float)kraw(d);
+                } else {  // rotate the new key in fp64 from the fp32 table, round once to bf16
+                    const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
+                    const double x1 = kraw(j), x2 = kraw(j + half);
+                    const float2 cs2 = tab(j);
+                    const double cc = cs2.x, ss = cs2.y;
+                    kn = f64_to_bf16_value(d < half ? x1 * cc - x2 * ss : x2 * cc + x1 * ss);
+                }
+                knew_t[t * kHeadDim + d] = kn;
+                vnew_t[t * kHeadDim + d] = vraw;
+            }
+        }
+    };
 
     // Stage s of the chunk: one lane issues its K and V boxes into slot s % S.
     auto issue_stage = [&](int s) {
@@ -827,34 +889,55 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
             rel_s[s] = 0u;
         }
         fence_mbar_init();
-        if (!own_producer(KV))  // folded producer: the first S stages go out before the prologue
-            for (int s = 0; s < min(S, nst) && !droppable(s); ++s) issue_stage(s);
     }
-    // q of the group, rotated here from bf16 or taken pre-rotated, scaled to log2 units.
-    const float2 *cs = a.q_bf16 ? a.table + (size_t)c * (a.rotary_dim >> 1) : nullptr;
-    for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
-        const int h = i / kHeadDim, d = i % kHeadDim;
-        const size_t row = qrow(h) * kHeadDim;
-        float x;
-        if (a.q_bf16 == nullptr) {
-            x = a.q_rot[row + d];
-        } else if (d >= a.rotary_dim) {
-            x = __bfloat162float(a.q_bf16[row + d]);
-        } else {
-            const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
-            const float x1 = __bfloat162float(a.q_bf16[row + j]);
-            const float x2 = __bfloat162float(a.q_bf16[row + j + half]);
-            const float2 t = cs[(MT ? (size_t)(h / Gm) * half : 0) + j];   // row of position c + token
-            x = d < half ? fmaf(x1, t.x, -x2 * t.y) : fmaf(x2, t.x, x1 * t.y);
-        }
-        q_s[i] = x * kQScale;
-    }
-    // A sequence with a single chunk is combined by this CTA: fetch the
-    // combine's inputs now, in the same round as q.
+    // q of the group in log2 units.  Round 1: the raw q rows (16-byte loads),
+    // the rotary row at position c and, when this CTA will combine a single
+    // chunk, the combine's other inputs -- all requested at once.
     const bool has_new = a.new_kind != NEW_NONE;
+    const int half = a.rotary_dim >> 1;
+    if (a.q_bf16) {
+        for (int i = threadIdx.x; i < G * (kHeadDim / 8); i += blockDim.x) {
+            const int r = i / (kHeadDim / 8), c8 = i % (kHeadDim / 8);
+            float f[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4 *>(a.q_bf16 + qrow(r) * kHeadDim + c8 * 8), f);
+            float4 *dst = reinterpret_cast<float4 *>(q_s + r * kHeadDim + c8 * 8);
+            dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+            dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
+        if (!MT)
+            for (int j = threadIdx.x; j < half; j += blockDim.x) tab_s[j] = a.table[(size_t)c * half + j];
+    } else {
+        for (int i = threadIdx.x; i < G * (kHeadDim / 4); i += blockDim.x)
+            reinterpret_cast<float4 *>(q_s)[i] =
+                reinterpret_cast<const float4 *>(a.q_rot + qrow(i / (kHeadDim / 4)) * kHeadDim)[i % (kHeadDim / 4)];
+    }
     if (!MT && nchunks == 1)
         load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, misc + 2 * kMaxGroup,
-                                   misc + 3 * kMaxGroup, code_s, kNThreads);
+                                   misc + 3 * kMaxGroup, code_s);
+    __syncthreads();
+    // Folded producer: the first S stages go out once the prologue's loads are
+    // in (issued earlier, their traffic delayed those loads).
+    if (!own_producer(KV) && threadIdx.x == 0)
+        for (int s = 0; s < min(S, nst) && !droppable(s); ++s) issue_stage(s);
+    // Round 2: rotate each rotary pair in place (fp32; q only feeds the scores)
+    // and scale every dim to log2 units.
+    if (a.q_bf16) {
+        for (int p = threadIdx.x; p < G * half; p += blockDim.x) {
+            const int r = p / half, j = p % half;
+            const float2 t = MT ? a.table[(size_t)(c + r / Gm) * half + j] : tab_s[j];   // position c + token
+            float *qr = q_s + r * kHeadDim;
+            const float x1 = qr[j], x2 = qr[j + half];
+            qr[j] = fmaf(x1, t.x, -x2 * t.y) * kQScale;
+            qr[j + half] = fmaf(x2, t.x, x1 * t.y) * kQScale;
+        }
+        const int pass = kHeadDim - 2 * half;
+        for (int i = threadIdx.x; i < G * pass; i += blockDim.x) q_s[(i / pass) * kHeadDim + 2 * half + i % pass] *= kQScale;
+    } else {
+        for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) q_s[i] *= kQScale;
+    }
+    // A single chunk is combined by this CTA: make its new entry now, while the
+    // first stages are in flight (its inputs arrived with q).
+    if (!MT && has_new && nchunks == 1) make_new_entries();
     // MT ring layers: row r (token t) does not see the t oldest ring entries (the
     // ones its window has passed); rows of a full layer see the whole cache.
     if (MT && threadIdx.x < G) {
@@ -980,20 +1063,11 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     float *sink_s = misc + 2 * kMaxGroup;           // [G]
     float *gate_s = misc + 3 * kMaxGroup;           // [G]
     if (!MT && nchunks > 1)
-        load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, sink_s, gate_s, code_s, kNThreads);
+        load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, sink_s, gate_s, code_s);
     if (MT && threadIdx.x < G) {   // per row: the sink of its head, the gate logit of its token and head
         sink_s[threadIdx.x] = a.sink ? a.sink[kvh * Gm + threadIdx.x % Gm] : 0.f;
         gate_s[threadIdx.x] = a.gate ? a.gate[qrow(threadIdx.x)] : 0.f;
     }
-    // New entries of the ntok tokens: values as scored (knew_t), V values (or
-    // V codes' values for E4M3, vnew_t), codes, and per-row new-entry weights.
-    uint8_t *mt_base = smem + S * kStage - kMtNewBytes;
-    float *knew_t = MT ? reinterpret_cast<float *>(mt_base) : knew_s;                      // [ntok][256]
-    float *vnew_t = MT ? knew_t + kMaxTokens * kHeadDim : vnew_s;                            // [ntok][256]
-    uint8_t *code_t = MT ? reinterpret_cast<uint8_t *>(vnew_t + kMaxTokens * kHeadDim) : code_s;
-    const int vcode_off = MT ? kMaxTokens * kHeadDim : kHeadDim;                             // V codes
-    constexpr int WN = MT ? kMaxTokens : 1;                                                  // wnew_t row stride
-    float *wnew_t = MT ? reinterpret_cast<float *>(code_t + 2 * kMaxTokens * kHeadDim) : misc + kMaxGroup;
     const float2 *pml = reinterpret_cast<const float2 *>(a.part_ml);
     constexpr int kPerLane = 4;
     float2 ml[kPerLane];
@@ -1008,53 +1082,8 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
         }
     }
     __syncthreads();
-    if (has_new) {
-        for (int idx = threadIdx.x; idx < ntok * kHeadDim; idx += blockDim.x) {
-            const int t = idx / kHeadDim, d = idx % kHeadDim;
-            // Raw k of token t at dim i and its rotary row (MT reads them here; a
-            // single token's were fetched with the combine's other inputs).
-            const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(a.new_k) +
-                                      ((size_t)(b * a.total_tokens + a.token0 + t) * a.num_kv_heads + kvh) * kHeadDim;
-            const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(a.new_v) +
-                                      ((size_t)(b * a.total_tokens + a.token0 + t) * a.num_kv_heads + kvh) * kHeadDim;
-            auto kraw = [&](int i) -> double { return MT ? (double)__bfloat162float(kg[i]) : (double)kraw_s[i]; };
-            auto tab = [&](int j) -> float2 {
-                return MT ? a.table[(size_t)(c + t) * (a.rotary_dim >> 1) + j] : tab_s[j];
-            };
-            const float vraw = MT ? __bfloat162float(vg[d]) : vnew_s[d];
-            if (KV == KV_FP8) {
-                // E4M3 entry: quantise (fp64 rotation, one division, one rounding) unless staged;
-                // score it as stored (code * scale) and keep V in code units.
-                if (a.new_kind == NEW_ROTATE) {
-                    double y = kraw(d);
-                    if (d < a.rotary_dim) {
-                        const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
-                        const double x1 = kraw(j), x2 = kraw(j + half);
-                        const float2 cs2 = tab(j);
-                        const double cc = cs2.x, ss = cs2.y;
-                        y = d < half ? __dsub_rn(__dmul_rn(x1, cc), __dmul_rn(x2, ss))
-                                     : __dadd_rn(__dmul_rn(x2, cc), __dmul_rn(x1, ss));
-                    }
-                    code_t[t * kHeadDim + d] = e4m3_from_f64(__ddiv_rn(y, (double)kscale));
-                    code_t[vcode_off + t * kHeadDim + d] = e4m3_from_f64(__ddiv_rn((double)vraw, (double)vscale));
-                }
-                knew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[t * kHeadDim + d]) * kscale;
-                vnew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[vcode_off + t * kHeadDim + d]);
-            } else {
-                float kn;
-                if (a.new_kind == NEW_STAGED || d >= a.rotary_dim) {
-                    kn = (float)kraw(d);
-                } else {  // rotate the new key in fp64 from the fp32 table, round once to bf16
-                    const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
-                    const double x1 = kraw(j), x2 = kraw(j + half);
-                    const float2 cs2 = tab(j);
-                    const double cc = cs2.x, ss = cs2.y;
-                    kn = f64_to_bf16_value(d < half ? x1 * cc - x2 * ss : x2 * cc + x1 * ss);
-                }
-                knew_t[t * kHeadDim + d] = kn;
-                vnew_t[t * kHeadDim + d] = vraw;
-            }
-        }
+    if (has_new && (MT || nchunks > 1)) {   // a single chunk's entry was made in the prologue
+        make_new_entries();
         __syncthreads();
     }
     // Per head: M = max(chunk maxima, new score), chunk weights 2^(m_j - M) and

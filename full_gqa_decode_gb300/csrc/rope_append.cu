@@ -61,9 +61,8 @@ __device__ __forceinline__ void store_entry(const RopeArgs &a, size_t o, int h, 
                                             const __nv_bfloat16 *vh, int d, const float2 *cs) {
     const double y = rope_key_f64(kh, d, a.rotary_dim, cs);
     if (a.kv_type == KV_FP8) {
-        static_cast<uint8_t *>(a.dst_k)[o] = e4m3_from_f64(__ddiv_rn(y, (double)a.k_scale[h]));
-        static_cast<uint8_t *>(a.dst_v)[o] =
-            e4m3_from_f64(__ddiv_rn((double)__bfloat162float(vh[d]), (double)a.v_scale[h]));
+        static_cast<uint8_t *>(a.dst_k)[o] = e4m3_quotient(y, (double)a.k_scale[h]);
+        static_cast<uint8_t *>(a.dst_v)[o] = e4m3_quotient((double)__bfloat162float(vh[d]), (double)a.v_scale[h]);
     } else {
         static_cast<__nv_bfloat16 *>(a.dst_k)[o] = d >= a.rotary_dim ? kh[d] : f64_to_bf16_rne(y);
         static_cast<__nv_bfloat16 *>(a.dst_v)[o] = vh[d];

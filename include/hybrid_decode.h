@@ -144,9 +144,9 @@ typedef struct {
 
 /* Per-layer tensors of a whole decode step (decode_step). */
 typedef struct {
-    const void *q;        /* bf16 [batch][num_q_heads][head_dim]                   */
-    const void *k;        /* bf16 [batch][num_kv_heads][head_dim]                  */
-    const void *v;        /* bf16 [batch][num_kv_heads][head_dim]                  */
+    const void *q;        /* bf16 [batch][num_q_heads][head_dim], 16-byte aligned  */
+    const void *k;        /* bf16 [batch][num_kv_heads][head_dim], 16-byte aligned */
+    const void *v;        /* bf16 [batch][num_kv_heads][head_dim], 16-byte aligned */
     hd_kv_cache cache;
     const float *sink;    /* fp32 [num_q_heads] or NULL (no sink)                  */
     void *out;            /* bf16 [batch][num_q_heads][head_dim]                   */

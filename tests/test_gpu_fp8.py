@@ -193,3 +193,26 @@ def test_fp8_cache_needs_fp8_context(hd):
     assert e.value.status == 1
     bf16_ctx.close()
     fp8_ctx.close()
+
+
+def test_fp8_quantisation_at_midpoints(hd, orc):
+    """New keys and values placed exactly on E4M3 rounding midpoints (times a
+    power-of-two scale, so the quotient is exact) and one bf16 step either side
+    of them: every written code must equal the oracle's (ties to even)."""
+    torch_codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    vals = torch_codes.view(torch.float8_e4m3fn).float().numpy()
+    pos = np.unique(vals[np.isfinite(vals) & (vals >= 0)])
+    mids = (pos[:-1] + pos[1:]) / 2
+    mids = np.concatenate([mids, mids * (1 + 2.0 ** -7), mids * (1 - 2.0 ** -8), -mids])  # bf16 neighbours, signs
+    scale = 2.0 ** -5
+    B, Hq, Hkv = 4, 8, 2
+    n = B * Hkv * synth.HEAD_DIM
+    x = np.resize(mids * scale, n).astype(np.float32).reshape(B, Hkv, synth.HEAD_DIM)
+    rng = synth.generator(680)
+    ctx = make_ctx(hd, [FULL], max_batch=B, max_context=64)
+    case = LayerCase(rng, B, Hq, Hkv, 65, [0] * B, kv="fp8")   # position 0: the key is not rotated
+    case.k = torch.from_numpy(x).to(torch.bfloat16)
+    case.v = torch.from_numpy(x[::-1].copy()).to(torch.bfloat16)
+    case.k_scale = torch.full((Hkv,), scale, dtype=torch.float32)
+    case.v_scale = torch.full((Hkv,), scale, dtype=torch.float32)
+    check_layer(hd, orc, ctx, 0, FULL, 0, case)
