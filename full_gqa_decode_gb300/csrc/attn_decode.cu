@@ -14,21 +14,25 @@
 // attention output times sigmoid of its gate logit) is applied in the same
 // epilogue scale.
 //
-// Grid: one CTA per (chunk of cached keys, kv head, sequence).  A producer
-// warp streams the chunk's K and V rows through a 3-stage shared-memory ring
-// with TMA tensor loads (128-byte swizzle, completion on mbarriers); four
-// consumer warps each take 8 keys of every 32-key stage, so each K/V row is
-// read from HBM once for the whole GQA group.  Scores are kept in log2 units
-// (q is pre-scaled by log2(e)/sqrt(d)).  Two consumers exist: CUDA-core FMA
-// with warp-shuffle reductions, and tensor-core mma.sync (bf16 in, fp32
-// accumulate) where q is split into a bf16 high and low part on the padded
-// rows of the MMA tile so the scores keep fp32 accuracy.
+// Grid: one CTA per (chunk of cached keys, kv head, sequence).  The chunk's K
+// and V rows stream through a shared-memory ring of 32 KiB stages (3 stages,
+// or 6 with one CTA per SM) with TMA tensor loads (128-byte swizzle,
+// completion on mbarriers); four consumer warps split every stage, so each K/V
+// row is read from HBM once for the whole GQA group.  bf16 caches: 32-key
+// stages, a dedicated producer warp.  E4M3 caches (per-kv-head scales):
+// 64-key stages, the producer folded into the consumers (the last warp to
+// release a slot refills it).  Scores are kept in log2 units (q is pre-scaled
+// by log2(e)/sqrt(d)).  Consumers: CUDA-core FMA with warp-shuffle
+// reductions, and tensor-core mma.sync with fp32 accumulation, where q is
+// split into a high and a low part (bf16, or f16 for E4M3 caches) so the
+// scores keep fp32 accuracy.  With MT, several tokens of a sequence are extra
+// query rows (multi-token decode).
 //
-// Each CTA writes an unnormalised partial (o, m, l) per query head, then takes
+// Each CTA writes an unnormalised partial (o, m, l) per query row, then takes
 // a ticket on a per-(sequence, kv head) counter.  The CTA that draws the last
 // ticket -- every other chunk of that (sequence, kv head) has finished reading
-// -- merges all partials and the new entry, writes out/lse, stores the new
-// K/V entry (ring slot or append) and resets the counter.  Nothing waits on
+// -- merges all partials and the new entries, writes out/lse, stores the new
+// K/V entries (ring slot or append) and resets the counter.  Nothing waits on
 // another CTA.
 #include <cuda_fp16.h>
 
@@ -150,8 +154,7 @@ __device__ __forceinline__ void mma_1688(float (&d)[4], uint32_t a0, uint32_t a1
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(b0));
 }
-// The same two shapes with f16 operands (the FP8 cache path: E4M3 converts to
-// f16 exactly).
+// m16n8k16 with f16 operands (the FP8 cache path: E4M3 converts to f16 exactly).
 __device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
                                               uint32_t b1) {
     asm volatile(
@@ -159,13 +162,6 @@ __device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)
         "{%8,%9}, {%0,%1,%2,%3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-}
-__device__ __forceinline__ void mma_1688_f16(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
-        "{%0,%1,%2,%3};"
-        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(a1), "r"(b0));
 }
 __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
     __half2 v = __floats2half2_rn(lo, hi);
