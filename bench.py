@@ -281,9 +281,9 @@ class Workload:
 
     def token_pass_bytes(self) -> int:
         """Scored-KV bytes a multi-token step reads: the tokens of a sequence run in
-        passes of up to 8 query rows per kv head, each pass scoring the cache at
-        context + first token of the pass (earlier passes' entries included)."""
-        tmax, passes, t0 = max(1, 8 // (self.Hq // self.Hkv)), [], 0
+        passes of up to 16 query rows (and 8 tokens) per kv head, each pass scoring
+        the cache at context + first token of the pass (earlier passes' entries included)."""
+        tmax, passes, t0 = min(8, max(1, 16 // (self.Hq // self.Hkv))), [], 0
         while t0 < self.tokens:
             tp = 1
             while 2 * tp <= tmax and 2 * tp <= self.tokens - t0:

@@ -248,11 +248,12 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     int32_t chunk_keys = 0, num_chunks = 0, stages = kStages;
     plan_split(L.batch, ctx->cfg.num_kv_heads, L.max_keys, ctx->num_sms, ctx->part_slots, &chunk_keys,
                &num_chunks, &stages, ctx->kv_type == KV_FP8 ? 2 * kChunkMax : kChunkMax);
+    if ((int64_t)ctx->group * L.tokens > kMaxGroup) stages = kDeepStages;   // 16 rows: one CTA per SM
     if ((int64_t)L.batch * num_chunks > ctx->part_slots) return HD_ERR_CAPACITY;
     // The combine keeps a weight per (head, chunk) plus a float4 row per head in the stage ring.
     const size_t rows = (size_t)ctx->group * L.tokens;   // query rows per kv head
     if ((rows * num_chunks + 3) * sizeof(float) + rows * 64 * 16 + (L.total_tokens > 1 ? kMtNewBytes : 0) >
-        (size_t)kStages * kStageBytes)
+        (size_t)stages * kStageBytes)
         return HD_ERR_CAPACITY;
     const bool sliding = ctx->layer_types[L.layer] == HD_SLIDING;
     const DeviceTable &tab = sliding ? ctx->table_sliding : ctx->table_full;
@@ -430,8 +431,8 @@ hd_status hybrid_decode_init(const hd_config *cfg, hd_ctx **out_ctx) {
         if (s > slots) slots = s;
     }
     ctx->part_slots = slots;
-    // Partials hold up to kMaxGroup rows per kv head (query heads, or heads x tokens).
-    const size_t rows = (size_t)Hkv * kMaxGroup;
+    // Partials hold up to kMaxRows rows per kv head (query heads, or heads x tokens).
+    const size_t rows = (size_t)Hkv * kMaxRows;
     bool ok = cudaMalloc(&ctx->part_o, (size_t)slots * rows * kHeadDim * sizeof(float)) == cudaSuccess &&
               cudaMalloc(&ctx->part_ml, (size_t)slots * rows * sizeof(float2)) == cudaSuccess &&
               cudaMalloc(&ctx->counters, (size_t)B * Hkv * sizeof(int32_t)) == cudaSuccess &&
@@ -568,9 +569,10 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
     return decode_step_tokens(ctx, batch, 1, context, max_context_hint, layers, stream);
 }
 
-// T tokens per sequence: each layer runs in passes of up to kMaxGroup / group
-// tokens (a power of two), the tokens of a pass being extra query rows that
-// share one stream of the cache.  A pass commits its entries, so the next pass
+// T tokens per sequence: each layer runs in passes of up to kMaxRows / group
+// tokens (a power of two, at most kMaxTokens), the tokens of a pass being extra
+// query rows that share one stream of the cache; passes of more than kMaxGroup
+// rows run one CTA per SM on the deep ring.  A pass commits its entries, so the next pass
 // (launched in full stream order) sees them as cached keys at context + token0.
 hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, const int32_t *context,
                              int32_t max_context_hint, const hd_layer_io *layers, void *stream) {
@@ -642,7 +644,7 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
             L.new_kind = NEW_NONE;
             L.commit = COMMIT_NONE;
         }
-        const int tmax = kMaxGroup / ctx->group;
+        const int tmax = std::min(kMaxTokens, kMaxRows / ctx->group);
         L.total_tokens = num_tokens;
         for (int t0 = 0; t0 < num_tokens;) {
             int tp = 1;

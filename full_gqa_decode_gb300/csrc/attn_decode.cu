@@ -395,6 +395,7 @@ struct FmaConsumer {
 // operand is V read with ldmatrix.trans.
 template <int G, bool MT = false>
 struct MmaConsumer {
+    static constexpr int kWK = 8;   // keys per consume call
     uint32_t qa[16][4];
     float o[16][4];   // O^T tile mt: rows dims 16mt + gid (+8), cols heads 2*t4 (+1)
     float m_run, l_run;  // for head gid; l_run sums this lane's keys only
@@ -736,14 +737,15 @@ struct Fp8MmaConsumer {
 
 // G: query rows per kv head -- the GQA group, or with MT (multi-token) the
 // group times a.tokens tokens of the same sequence, row r = token r / (G /
-// a.tokens), head r % (G / a.tokens).
+// a.tokens), head r % (G / a.tokens).  G = 16 (MT only) runs two row groups
+// of 8: warps 0-1 take rows 0-7 and warps 2-3 rows 8-15, each pair splitting
+// every stage's keys, so each warp keeps the 8-row consumer's registers.
 template <int G, int CONSUMER, int S, int KV, bool MT>
 __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kStages * kStageBytes ? 2 : 1)
     attn_layer_kernel(const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const LayerArgs a) {
     constexpr int kStage = kv_stage_bytes(KV);     // bytes of one stage (K + V)
     constexpr int kKeys = kv_stage_keys(KV);       // keys per stage: 32 bf16, 64 E4M3
-    constexpr int kWarpKeys = kKeys / kConsumerWarps;
     constexpr int kBoxes = kv_boxes_per_row(KV);   // 128-byte boxes per K or V row
     constexpr int kNThreads = kv_threads(KV);
     extern __shared__ uint8_t smem_raw[];
@@ -760,7 +762,7 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     int *flag_s = reinterpret_cast<int *>(empty + S);
     unsigned *rel_s = reinterpret_cast<unsigned *>(flag_s + 4);                // [S] slot releases (folded producer)
     uint8_t *code_s = reinterpret_cast<uint8_t *>(rel_s + 16);                 // [2][256] E4M3 new entry
-    int *mcnt_s = reinterpret_cast<int *>(code_s + 2 * kHeadDim);               // [8] MT ring masks
+    int *mcnt_s = reinterpret_cast<int *>(code_s + 2 * kHeadDim);               // [kMaxRows] MT ring masks
 
     const int chunk = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -810,6 +812,7 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     const int vcode_off = MT ? kMaxTokens * kHeadDim : kHeadDim;                             // V codes
     constexpr int WN = MT ? kMaxTokens : 1;                                                  // wnew_t row stride
     float *wnew_t = MT ? reinterpret_cast<float *>(code_t + 2 * kMaxTokens * kHeadDim) : misc + kMaxGroup;
+    float *rows_t = wnew_t + kMaxRows * kMaxTokens;   // MT: per-row sink, gate, scale [3][kMaxRows]
     // Makes the new entries of the ntok tokens: the key rotated in fp64 and rounded
     // once to bf16, or quantised to E4M3 (fp64 rotation, one division, one
     // rounding; V too), each scored as stored; E4M3 V stays in code units.
@@ -947,9 +950,11 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     mask.cnt = mcnt_s;
     __syncthreads();
 
-    float *red_o = reinterpret_cast<float *>(smem);             // reuses the stage ring
-    float *red_m = red_o + kConsumerWarps * G * kHeadDim;
-    float *red_l = red_m + kConsumerWarps * G;
+    // Row groups: RG groups of CG rows; each group's WPG warps split every stage.
+    constexpr int RG = G > 8 ? G / 8 : 1, CG = G / RG, WPG = kConsumerWarps / RG;
+    float *red_o = reinterpret_cast<float *>(smem);             // [warps][CG][256], reuses the stage ring
+    float *red_m = red_o + kConsumerWarps * CG * kHeadDim;
+    float *red_l = red_m + kConsumerWarps * CG;
     if (own_producer(KV) && warp == kConsumerWarps) {
         if (lane == 0) {  // producer: one lane issues every load of the chunk
             for (int s = 0; s < nst; ++s) {
@@ -965,10 +970,17 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
         __syncthreads();
         __syncthreads();
     } else {
-        using Mma = typename std::conditional<KV == KV_FP8, Fp8MmaConsumer<G, MT>, MmaConsumer<G, MT>>::type;
-        typename std::conditional<CONSUMER == CONSUMER_MMA, Mma, FmaConsumer<G, KV>>::type cons;
-        cons.init(q_s, lane, kscale);
-        if (MT) cons.set_mask(mask, lane);
+        using Mma = typename std::conditional<KV == KV_FP8, Fp8MmaConsumer<CG, MT>, MmaConsumer<CG, MT>>::type;
+        typename std::conditional<CONSUMER == CONSUMER_MMA, Mma, FmaConsumer<CG, KV>>::type cons;
+        constexpr int kCallKeys = decltype(cons)::kWK;          // keys per consume call
+        constexpr int kSpan = kKeys / WPG;                        // keys of a stage per warp
+        const int rg = warp / WPG, kpart = warp % WPG;
+        cons.init(q_s + rg * CG * kHeadDim, lane, kscale);
+        if (MT) {
+            RowMask gm = mask;
+            gm.cnt = mcnt_s + rg * CG;
+            cons.set_mask(gm, lane);
+        }
         for (int s = 0; s < nst; ++s) {
             const int slot = s % S;
             if (!mbar_wait(&full[slot], (s / S) & 1)) {
@@ -976,10 +988,13 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
                 break;
             }
             const uint8_t *kst = smem + slot * kStage;
-            const int row0 = warp * kWarpKeys;
-            const int nvalid = min(kWarpKeys, end - (start + s * kKeys + row0));
-            if (nvalid > 0)
-                cons.consume(kst, kst + kBoxes * kv_box_bytes(KV), row0, nvalid, lane, start + s * kKeys + row0);
+#pragma unroll
+            for (int sub = 0; sub < kSpan; sub += kCallKeys) {
+                const int row0 = kpart * kSpan + sub;
+                const int nvalid = min(kCallKeys, end - (start + s * kKeys + row0));
+                if (nvalid > 0)
+                    cons.consume(kst, kst + kBoxes * kv_box_bytes(KV), row0, nvalid, lane, start + s * kKeys + row0);
+            }
             __syncwarp();  // orders every lane's reads of the slot before lane 0's release
             if (lane == 0) {
                 if (own_producer(KV)) {
@@ -1016,15 +1031,16 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     float2 *own_ml = reinterpret_cast<float2 *>(own_o + G * kHeadDim);    // [G]
     for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
         const int h = i / kHeadDim, d = i % kHeadDim;
+        const int w0 = (h / CG) * WPG, hr = h % CG;   // the warps of this row's group, its row there
         float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, red_m[w * G + h]);
+        for (int w = w0; w < w0 + WPG; ++w) M = fmaxf(M, red_m[w * CG + hr]);
         float o = 0.f, L = 0.f;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            const float wt = (M == -INFINITY) ? 0.f : fast_exp2(red_m[w * G + h] - M);
-            o = fmaf(wt, red_o[(w * G + h) * kHeadDim + d], o);
-            L = fmaf(wt, red_l[w * G + h], L);
+        for (int w = w0; w < w0 + WPG; ++w) {
+            const float wt = (M == -INFINITY) ? 0.f : fast_exp2(red_m[w * CG + hr] - M);
+            o = fmaf(wt, red_o[(w * CG + hr) * kHeadDim + d], o);
+            L = fmaf(wt, red_l[w * CG + hr], L);
         }
         own_o[i] = o;
         if (d == 0) own_ml[h] = make_float2(M, L);
@@ -1056,8 +1072,8 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     // Every global input of the combine is requested in one round: the new
     // entry, its rotary row, the sink and the gate logits (unless the prologue
     // fetched them), and each warp's chunk maxima and sums.
-    float *sink_s = misc + 2 * kMaxGroup;           // [G]
-    float *gate_s = misc + 3 * kMaxGroup;           // [G]
+    float *sink_s = MT ? rows_t : misc + 2 * kMaxGroup;                  // [G]
+    float *gate_s = MT ? rows_t + kMaxRows : misc + 3 * kMaxGroup;       // [G]
     if (!MT && nchunks > 1)
         load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, sink_s, gate_s, code_s);
     if (MT && threadIdx.x < G) {   // per row: the sink of its head, the gate logit of its token and head
@@ -1085,7 +1101,7 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     // Per head: M = max(chunk maxima, new score), chunk weights 2^(m_j - M) and
     // L = sum of weighted chunk sums (+ the new entry).  Warp w takes heads w, w + warps, ...
     float *wts = reinterpret_cast<float *>(smem);   // [G][nchunks] (the warp buffers are free)
-    float *head_s = misc;                           // [G] scale = sink factor * gate / L
+    float *head_s = MT ? rows_t + 2 * kMaxRows : misc;   // [G] scale = sink factor * gate / L
     for (int h = warp; h < G; h += kNThreads / 32) {
         const size_t ph = pbase + (size_t)h * a.max_chunks;
         if (h != warp) {  // a second head for this warp: its pairs were not preloaded
@@ -1267,6 +1283,9 @@ cudaError_t launch_c(const CUtensorMap *km, const CUtensorMap *vm, const LayerAr
         case 2: return launch_g<2, CONSUMER_MMA, S, KV, true>(km, vm, a, batch, pdl, s);
         case 4: return launch_g<4, CONSUMER_MMA, S, KV, true>(km, vm, a, batch, pdl, s);
         case 8: return launch_g<8, CONSUMER_MMA, S, KV, true>(km, vm, a, batch, pdl, s);
+        case 16:   // 16 rows: one CTA per SM with the deep ring
+            if constexpr (S_BF16 == kDeepStages) return launch_g<16, CONSUMER_MMA, S, KV, true>(km, vm, a, batch, pdl, s);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
         }
     }
@@ -1296,7 +1315,7 @@ cudaError_t launch_kv(const CUtensorMap *km, const CUtensorMap *vm, const LayerA
 size_t layer_smem_bytes(int group, int stages) {
     return 1024 + (size_t)stages * kStageBytes + ((size_t)group * kHeadDim + 4 * kHeadDim + 32) * sizeof(float) +
            2 * (size_t)(2 * stages) * sizeof(uint64_t) + 16 + 16 * sizeof(unsigned) + 2 * kHeadDim +
-           kMaxGroup * sizeof(int);
+           kMaxRows * sizeof(int);
 }
 
 cudaError_t launch_layer(const CUtensorMap *km, const CUtensorMap *vm, const LayerArgs &a, int batch,

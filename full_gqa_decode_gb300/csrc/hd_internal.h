@@ -36,8 +36,11 @@ __host__ __device__ constexpr int kv_stage_bytes(int kv) { return 2 * kv_boxes_p
 static_assert(kv_stage_bytes(KV_BF16) == kStageBytes && kv_stage_bytes(KV_FP8) == kStageBytes,
               "both cache types use 32 KiB stages");
 constexpr int kMaxTokens = 8;     // tokens per sequence of one multi-token step
-// Shared-memory bytes the multi-token combine keeps at the end of the ring.
-constexpr int kMtNewBytes = 2 * kMaxTokens * kHeadDim * 4 + 2 * kMaxTokens * kHeadDim + kMaxGroup * kMaxTokens * 4;
+constexpr int kMaxRows = 16;      // query rows per kv head in one kernel (heads x tokens)
+// Shared-memory bytes the multi-token combine keeps at the end of the ring: new
+// K/V values and codes, per-row new-entry weights, and per-row sink, gate and scale.
+constexpr int kMtNewBytes =
+    2 * kMaxTokens * kHeadDim * 4 + 2 * kMaxTokens * kHeadDim + kMaxRows * kMaxTokens * 4 + 3 * kMaxRows * 4;
 constexpr int kChunkMin = 64;
 constexpr int kChunkMax = 2048;
 

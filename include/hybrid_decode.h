@@ -222,8 +222,8 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
  * the batch index: q, out [batch][num_tokens][num_q_heads][head_dim]; k, v
  * [batch][num_tokens][num_kv_heads][head_dim]; lse, gate
  * [batch][num_tokens][num_q_heads].  The tokens of a sequence are extra query
- * rows sharing one read of the cache, up to 8 rows per kv head per pass
- * (group 4: two tokens per pass).  Full layers append num_tokens entries;
+ * rows sharing one read of the cache, up to 16 rows (and 8 tokens) per kv
+ * head per pass (group 4: four tokens per pass).  Full layers append num_tokens entries;
  * sliding ring layers write slots (c + t) mod (window-1) after reading.
  * HD_ERR_UNSUPPORTED for num_tokens > 1 with a roll layout or the CUDA-core
  * consumer; for full layers max_context_hint bounds context[b] (0 means
