@@ -44,7 +44,8 @@ FP8_ROW_BYTES = 2 * synth.HEAD_DIM          # K row + V row, E4M3 codes, one kv 
 DEFAULT_WORKLOAD = "step28_b64_c512_32768"
 SECONDARY_WORKLOAD = "step28_b1_c4096"
 METRIC = "KV-read HBM GB/s (% of GB300 peak); µs per 28-layer decode step"
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "attn_layer_kernel_full_b64_traffic.txt")
+PROFILE_SUMMARY = {"step": os.path.join(ROOT, "profiles", "attn_step_grid_b64_traffic.txt"),
+                   "full": os.path.join(ROOT, "profiles", "attn_layer_kernel_full_b64_traffic.txt")}
 
 
 # ------------------------------------------------------------------ helpers --
@@ -91,19 +92,21 @@ def measured_peaks() -> dict:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("attn_decode.cu", "hd_internal.h"):
+    for f in ("attn_kernel.cuh", "hd_internal.h"):
         with open(os.path.join(ROOT, "full_gqa_decode_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the full-layer split kernel from the committed ncu
-    summary, or None when the summary is absent or the kernel changed since."""
-    if not os.path.exists(PROFILE_SUMMARY):
+def profiled_traffic(kind: str = "step"):
+    """DRAM bytes per launch of the step grid ("step") or of the full-layer kernel
+    ("full") from the committed ncu summary, or None when the summary is absent or
+    the kernel changed since."""
+    path = PROFILE_SUMMARY[kind]
+    if not os.path.exists(path):
         return None
     kv = {}
-    with open(PROFILE_SUMMARY) as f:
+    with open(path) as f:
         for line in f:
             if ":" in line:
                 k, v = line.split(":", 1)
@@ -111,7 +114,7 @@ def profiled_traffic():
     if kv.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
     try:
-        return float(kv["dram_bytes_per_full_launch"])
+        return float(kv["dram_bytes_per_launch"])
     except (KeyError, ValueError):
         return None
 
@@ -427,24 +430,23 @@ def run_ours(args, world, rank, local) -> int:
     hd.hybrid_decode_set_consumer(wl.ctx, consumer)
     torch.cuda.synchronize()
 
-    # device-resident timed region (W warm-up steps first, then exactly K timed steps);
-    # the dominant kernel is timed by events around the first full layer of every
-    # step (that launch alone runs without early start; the others overlap)
-    hd.hybrid_decode_set_profiling(wl.ctx, hd.HD_PROFILE_FULL | hd.HD_PROFILE_FIRST_ONLY)
+    # device-resident timed region (W warm-up steps first, then exactly K timed steps).
+    # With the tensor-core consumer every step is one step grid (the attention of all
+    # layers), the dominant kernel, bracketed by events on its stream; the CUDA-core
+    # consumer runs one kernel per layer, and the first full layer of every step is
+    # bracketed (that launch alone runs without early start; the others overlap).
+    fused = consumer == hd.HD_CONSUMER_TENSOR_CORE
+    kind = hd.HD_PROFILE_KIND_STEP if fused else hd.HD_FULL
+    hd.hybrid_decode_set_profiling(wl.ctx, hd.HD_PROFILE_STEP if fused else hd.HD_PROFILE_FULL | hd.HD_PROFILE_FIRST_ONLY)
     with ClockSampler(device) as clocks:
         for _ in range(args.warmup):
             wl.step()
         torch.cuda.synchronize()
-        hd.hybrid_decode_profile(wl.ctx, hd.HD_FULL)  # drop the warm-up records
+        hd.hybrid_decode_profile(wl.ctx, kind)  # drop the warm-up records
         n0 = hd.hybrid_decode_launch_count(wl.ctx)
         ms = time_steps(wl.step, args.steps, 0, world, device)
         n1 = hd.hybrid_decode_launch_count(wl.ctx)
-        split_ms, split_launches = hd.hybrid_decode_profile(wl.ctx, hd.HD_FULL)
-    # diagnostic pass, outside the timed region: sliding-layer launches alone
-    hd.hybrid_decode_set_profiling(wl.ctx, hd.HD_PROFILE_SLIDING)
-    for _ in range(3):
-        wl.step()
-    slide_ms, slide_launches = hd.hybrid_decode_profile(wl.ctx, hd.HD_SLIDING)
+        dom_ms, dom_launches = hd.hybrid_decode_profile(wl.ctx, kind)
     hd.hybrid_decode_set_profiling(wl.ctx, 0)
     clk = clocks.summary()
     flags = hd.hybrid_decode_device_errors(wl.ctx)
@@ -453,23 +455,25 @@ def run_ours(args, world, rank, local) -> int:
     ms_max, total_bytes = reduce_timing(ms, wl.bytes, world, device)
     gbs = total_bytes / (ms_max * 1e-3) / 1e9
 
-    # roofline of the dominant kernel: the full-layer split-K pass
-    avg_split_ms = split_ms / max(split_launches, 1)
-    achieved = wl.full_layer_bytes / (avg_split_ms * 1e-3) / 1e9 if split_launches else None
+    # diagnostic passes, outside the timed region: one kernel per layer, the first
+    # full layer and every sliding layer bracketed alone
+    layer_kernels = layer_kernel_rooflines(wl, peaks)
+
+    # roofline of the dominant kernel
+    avg_ms = dom_ms / max(dom_launches, 1)
+    per_launch = (wl.bytes * args.steps // max(dom_launches, 1)) if fused else wl.full_layer_bytes
+    achieved = per_launch / (avg_ms * 1e-3) / 1e9 if dom_launches else None
     roofline = {"bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None,
-                "traffic": profiled_traffic(),
-                "kernel": f"attn_layer_kernel, full layers ({args.consumer}); events around the first full "
-                          f"layer of each timed step",
-                "algorithmic_bytes_per_launch": wl.full_layer_bytes,
-                "avg_launch_ms": round(avg_split_ms, 4), "peak_source": peaks["source"]}
-    if slide_launches:
-        avg_slide = slide_ms / slide_launches
-        roofline["sliding_layers"] = {  # separate pass: each launch bracketed by events
-            "achieved": round(wl.sliding_layer_bytes / (avg_slide * 1e-3) / 1e9, 1),
-            "frac": round(wl.sliding_layer_bytes / (avg_slide * 1e-3) / 1e9 / peaks["hbm_gbs"], 4),
-            "algorithmic_bytes_per_launch": wl.sliding_layer_bytes, "avg_launch_ms": round(avg_slide, 4)}
+                "traffic": profiled_traffic("step" if fused else "full"),
+                "kernel": (f"attn_layer_kernel step grid (the attention of all {len(wl.types)} layers); events "
+                           f"around the grid of each timed step" if fused else
+                           f"attn_layer_kernel, full layers ({args.consumer}); events around the first full "
+                           f"layer of each timed step"),
+                "algorithmic_bytes_per_launch": int(per_launch),
+                "avg_launch_ms": round(avg_ms, 4), "launches": int(dom_launches), "peak_source": peaks["source"]}
+    roofline.update(layer_kernels)
 
     read_peak = read_stream_probe(device)
     if read_peak and achieved:
@@ -483,10 +487,14 @@ def run_ours(args, world, rank, local) -> int:
     # against the ungated step timed the same way (no profiling events)
     plain_ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
     gated_ms = time_steps(lambda: wl.step(gated=True), args.steps, args.warmup, 1, device)
-    # the same step with every layer in full stream order (no early start)
+    # the same step with one kernel per layer (early start on), and with every
+    # layer in full stream order (no early start)
+    hd.hybrid_decode_set_step_fusion(wl.ctx, False)
+    per_layer_ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
     hd.hybrid_decode_set_layer_overlap(wl.ctx, False)
     serial_ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
     hd.hybrid_decode_set_layer_overlap(wl.ctx, True)
+    hd.hybrid_decode_set_step_fusion(wl.ctx, True)
     if hd.hybrid_decode_device_errors(wl.ctx):
         raise RuntimeError("device error flags during the gated step")
 
@@ -516,9 +524,12 @@ def run_ours(args, world, rank, local) -> int:
                                  "value": round(wl.bytes / (gated_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                                  "ungated_ms_per_step": round(plain_ms, 4),
                                  "overhead_vs_ungated": round(gated_ms / plain_ms - 1.0, 4)}
+        result["kernel_per_layer"] = {
+            "ms_per_step": round(per_layer_ms, 4), "value": round(wl.bytes / (per_layer_ms * 1e-3) / 1e9, 1),
+            "unit": "GB/s", "note": "step fusion off: one kernel per layer, each starting while the previous drains"}
         result["layers_in_stream_order"] = {
             "ms_per_step": round(serial_ms, 4), "value": round(wl.bytes / (serial_ms * 1e-3) / 1e9, 1),
-            "unit": "GB/s", "note": "no layer starts before the previous one is complete"}
+            "unit": "GB/s", "note": "step fusion off and no layer starts before the previous one is complete"}
         if fp8:
             result["fp8_kv"] = fp8
         if multi:
@@ -551,6 +562,34 @@ def read_stream_probe(device, gib: int = 4):
         times.append(a.elapsed_time(b))
     del buf
     return nbytes / (statistics.median(times) * 1e-3) / 1e9
+
+
+def layer_kernel_rooflines(wl, peaks) -> dict:
+    """Outside the timed region, with step fusion off (one kernel per layer): the
+    first full layer of each of 3 steps and every sliding layer, each launch
+    bracketed by events alone; achieved GB/s over that layer's scored KV bytes."""
+    import full_gqa_decode_gb300 as hd
+    hd.hybrid_decode_set_step_fusion(wl.ctx, False)
+    out = {}
+    for name, mask, kind, nbytes in (("full_layers", hd.HD_PROFILE_FULL | hd.HD_PROFILE_FIRST_ONLY, hd.HD_FULL,
+                                      wl.full_layer_bytes),
+                                     ("sliding_layers", hd.HD_PROFILE_SLIDING, hd.HD_SLIDING,
+                                      wl.sliding_layer_bytes)):
+        hd.hybrid_decode_set_profiling(wl.ctx, mask)
+        for _ in range(3):
+            wl.step()
+        t_ms, n = hd.hybrid_decode_profile(wl.ctx, kind)
+        if n and nbytes:
+            avg = t_ms / n
+            gbs = nbytes / (avg * 1e-3) / 1e9
+            out[name] = {"kernel": "attn_layer_kernel, one layer per launch", "achieved": round(gbs, 1),
+                         "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes_per_launch": nbytes,
+                         "avg_launch_ms": round(avg, 4)}
+    if "full_layers" in out:
+        out["full_layers"]["traffic"] = profiled_traffic("full")
+    hd.hybrid_decode_set_profiling(wl.ctx, 0)
+    hd.hybrid_decode_set_step_fusion(wl.ctx, True)
+    return out
 
 
 def e2e_measure(wl, args, world, device) -> dict:
@@ -611,11 +650,20 @@ def fp8_step(device, args, consumer, layout, bf16_ms) -> dict:
     wl = Workload(args.workload, device, seed=0, layout=layout, kv="fp8")
     hd.hybrid_decode_set_consumer(wl.ctx, consumer)
     ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
+    fused = consumer == hd.HD_CONSUMER_TENSOR_CORE
+    grid_ms, grid_n = 0.0, 0
+    if fused:
+        hd.hybrid_decode_set_profiling(wl.ctx, hd.HD_PROFILE_STEP)
+        for _ in range(3):
+            wl.step()
+        grid_ms, grid_n = hd.hybrid_decode_profile(wl.ctx, hd.HD_PROFILE_KIND_STEP)
+    hd.hybrid_decode_set_step_fusion(wl.ctx, False)
     hd.hybrid_decode_set_profiling(wl.ctx, hd.HD_PROFILE_FULL)
     for _ in range(3):
         wl.step()
     full_ms, full_n = hd.hybrid_decode_profile(wl.ctx, hd.HD_FULL)
     hd.hybrid_decode_set_profiling(wl.ctx, 0)
+    hd.hybrid_decode_set_step_fusion(wl.ctx, True)
     flags = hd.hybrid_decode_device_errors(wl.ctx)
     if flags:
         raise RuntimeError(f"device error flags {flags:#x} in the FP8 step")
@@ -623,6 +671,12 @@ def fp8_step(device, args, consumer, layout, bf16_ms) -> dict:
     res = {"ms_per_step": round(ms, 4), "us_per_step": round(ms * 1e3, 1),
            "value": round(wl.bytes / (ms * 1e-3) / 1e9, 1), "unit": "GB/s", "kv_bytes_per_step": wl.bytes,
            "speedup_vs_bf16_step": round(bf16_ms / ms, 3)}
+    if grid_n:
+        per_launch = wl.bytes * 3 // grid_n
+        avg = grid_ms / grid_n
+        res["step_grid"] = {"achieved": round(per_launch / (avg * 1e-3) / 1e9, 1), "unit": "GB/s",
+                            "frac": round(per_launch / (avg * 1e-3) / 1e9 / peak, 4), "avg_launch_ms": round(avg, 4),
+                            "algorithmic_bytes_per_launch": per_launch}
     if full_n:
         avg = full_ms / full_n
         res["full_layer_kernel"] = {"achieved": round(wl.full_layer_bytes / (avg * 1e-3) / 1e9, 1), "unit": "GB/s",
@@ -675,8 +729,14 @@ def secondary_batch1(device, args, consumer) -> dict:
     with torch.cuda.graph(graph):
         wl.step()
     ms_graph = time_steps(graph.replay, steps, warm, 1, device)
+    hd.hybrid_decode_set_step_fusion(wl.ctx, False)   # one kernel per layer, for comparison
+    ms_layers = time_steps(wl.step, steps, warm, 1, device)
+    hd.hybrid_decode_set_step_fusion(wl.ctx, True)
+    if hd.hybrid_decode_device_errors(wl.ctx):
+        raise RuntimeError("device error flags in the batch-1 step")
     return {"workload": SECONDARY_WORKLOAD, "us_per_step": round(ms * 1e3, 1),
             "us_per_step_cuda_graph": round(ms_graph * 1e3, 1),
+            "us_per_step_kernel_per_layer": round(ms_layers * 1e3, 1),
             "kv_GBps_cuda_graph": round(wl.bytes / (ms_graph * 1e-3) / 1e9, 1),
             "kv_bytes_per_step": wl.bytes, "roofline_us": round(wl.bytes / (measured_peaks()["hbm_gbs"] * 1e9) * 1e6, 1)}
 

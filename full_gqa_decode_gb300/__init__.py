@@ -24,7 +24,8 @@ LIBRARY = os.path.join(PKG, "libhybriddecode.so")
 HD_SLIDING, HD_FULL = 0, 1
 HD_LAYOUT_AUTO, HD_LAYOUT_RING, HD_LAYOUT_ROLL = 0, 1, 2
 HD_CONSUMER_CUDA_CORE, HD_CONSUMER_TENSOR_CORE = 0, 1
-HD_PROFILE_SLIDING, HD_PROFILE_FULL, HD_PROFILE_FIRST_ONLY = 1 << HD_SLIDING, 1 << HD_FULL, 4
+HD_PROFILE_SLIDING, HD_PROFILE_FULL, HD_PROFILE_FIRST_ONLY, HD_PROFILE_STEP = 1 << HD_SLIDING, 1 << HD_FULL, 4, 8
+HD_PROFILE_KIND_STEP = 2
 HD_KV_BF16, HD_KV_FP8_E4M3 = 0, 1
 STATUS = {0: "HD_OK", 1: "HD_ERR_INVALID_ARG", 2: "HD_ERR_UNSUPPORTED", 3: "HD_ERR_CAPACITY",
           4: "HD_ERR_CUDA", 5: "HD_ERR_STATE"}
@@ -86,6 +87,7 @@ _SIGS = {
     "hybrid_decode_read_probe": [_P, _i64, _P],
     "hybrid_decode_inject_lost_copy": [_P, _i32],
     "hybrid_decode_set_layer_overlap": [_P, _i32],
+    "hybrid_decode_set_step_fusion": [_P, _i32],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -323,13 +325,15 @@ def hybrid_decode_launch_count(ctx: Context) -> int:
 
 
 def hybrid_decode_set_profiling(ctx: Context, mask: int) -> None:
-    """mask of layer types to bracket with events: HD_PROFILE_SLIDING | HD_PROFILE_FULL, or 0;
-    with HD_PROFILE_FIRST_ONLY only the first layer of each type per decode_step."""
+    """mask of launches to bracket with events: HD_PROFILE_SLIDING | HD_PROFILE_FULL (layer
+    kernels), HD_PROFILE_STEP (step grids), or 0; with HD_PROFILE_FIRST_ONLY only the first
+    layer kernel of each type per decode_step."""
     _check(_lib.hybrid_decode_set_profiling(ctx.handle, int(mask)), "hybrid_decode_set_profiling")
 
 
 def hybrid_decode_profile(ctx: Context, layer_type: int = HD_FULL) -> tuple[float, int]:
-    """(summed kernel milliseconds, launches) of the given layer type since the last read."""
+    """(summed kernel milliseconds, launches) of the given layer type (or HD_PROFILE_KIND_STEP:
+    step grids) since the last read."""
     ms, n = ctypes.c_double(), ctypes.c_int64()
     _check(_lib.hybrid_decode_profile(ctx.handle, layer_type, ctypes.byref(ms), ctypes.byref(n)),
            "hybrid_decode_profile")
@@ -339,6 +343,11 @@ def hybrid_decode_profile(ctx: Context, layer_type: int = HD_FULL) -> tuple[floa
 def hybrid_decode_set_layer_overlap(ctx: Context, enable: bool) -> None:
     """Whether decode_step lets a layer start before the previous one finishes (default on)."""
     _check(_lib.hybrid_decode_set_layer_overlap(ctx.handle, int(bool(enable))), "hybrid_decode_set_layer_overlap")
+
+
+def hybrid_decode_set_step_fusion(ctx: Context, enable: bool) -> None:
+    """Whether decode_step runs the attention of all layers as one grid (default on)."""
+    _check(_lib.hybrid_decode_set_step_fusion(ctx.handle, int(bool(enable))), "hybrid_decode_set_step_fusion")
 
 
 def hybrid_decode_set_consumer(ctx: Context, consumer: int) -> None:

@@ -17,7 +17,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(ROOT, "_build")
 LIBRARY = os.path.join(PKG, "libhybriddecode.so")
-SOURCES = ["api.cpp", "rope_append.cu", "attn_decode.cu", "noalloc.cu", "read_probe.cu"]
+SOURCES = ["api.cpp", "rope_append.cu", "attn_decode.cu", "attn_decode_fp8.cu", "attn_step.cu",
+           "attn_step_fp8.cu", "noalloc.cu", "read_probe.cu"]
+HEADERS = ["hd_internal.h", "attn_kernel.cuh", "e4m3.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 
@@ -30,7 +32,7 @@ def nvcc() -> str:
 
 def _inputs() -> list[str]:
     files = [os.path.join(CSRC, s) for s in SOURCES]
-    files += [os.path.join(CSRC, "hd_internal.h"), os.path.join(INCLUDE, "hybrid_decode.h")]
+    files += [os.path.join(CSRC, h) for h in HEADERS] + [os.path.join(INCLUDE, "hybrid_decode.h")]
     return files
 
 

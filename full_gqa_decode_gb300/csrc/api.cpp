@@ -67,6 +67,8 @@ struct DeviceTable {
     int32_t rotary_dim = 0;
 };
 
+struct LayerCall;
+
 }  // namespace
 
 struct hd_ctx {
@@ -79,21 +81,29 @@ struct hd_ctx {
     DeviceTable table_sliding, table_full;
     float *part_o = nullptr;
     float2 *part_ml = nullptr;
-    int64_t part_slots = 0;              // capacity in (sequence, chunk) pairs
+    int64_t part_slots = 0;              // single-layer calls: capacity in (sequence, chunk) pairs
+    int64_t part_rows = 0;               // capacity in partial rows ([256] floats + (m, l) each)
     uint8_t *stage_k = nullptr;          // [num_layers][max_batch][Hkv][D] entries of the cache type
     uint8_t *stage_v = nullptr;
     int kv_type = KV_BF16;
-    int32_t *counters = nullptr;         // [max_batch][Hkv] chunk tickets, zero between calls
+    int32_t *counters = nullptr;         // [num_layers][max_batch][Hkv] chunk tickets, zero between calls
     int32_t *err = nullptr;
     int consumer = CONSUMER_MMA;
     int32_t drop_stage = -1;             // test hook, see hybrid_decode_inject_lost_copy
     bool layer_overlap = true;           // decode_step: layers start before the previous one finishes
+    bool fuse_step = true;               // decode_step: one grid for all layers (step tables)
+    StepTable step_table;                // parameters of the step grid being launched
+    std::vector<LayerCall> step_calls;   // the layer calls of the step being launched
+    // Last independence check of decode_step's layers (host memcmp of the array).
+    std::vector<hd_layer_io> indep_layers;
+    int32_t indep_batch = -1, indep_tokens = -1;
+    bool indep_ok = false;
     int64_t launches = 0;
     std::vector<MapCacheEntry> maps;     // one per layer
     int32_t profile_mask = 0;           // bit (1 << layer type): bracket that type's launches
     bool profile_seen[2] = {false, false};  // FIRST_ONLY: a layer of that type was bracketed in this step
-    std::vector<cudaEvent_t> ev_begin, ev_end;  // [2][kProfileEvents]: per layer type
-    size_t ev_used[2] = {0, 0};
+    std::vector<cudaEvent_t> ev_begin, ev_end;  // [3][kProfileEvents]: per layer type, then step grids
+    size_t ev_used[3] = {0, 0, 0};
 };
 
 namespace {
@@ -241,24 +251,19 @@ struct LayerCall {
     int tokens = 1, token0 = 0, total_tokens = 1;   // multi-token decode: this pass's tokens
 };
 
-hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream) {
-    const CUtensorMap *km = nullptr, *vm = nullptr;
-    hd_status st = maps_for(ctx, L.layer, L.cache, L.batch, &km, &vm);
-    if (st != HD_OK) return st;
-    int32_t chunk_keys = 0, num_chunks = 0, stages = kStages;
-    plan_split(L.batch, ctx->cfg.num_kv_heads, L.max_keys, ctx->num_sms, ctx->part_slots, &chunk_keys,
-               &num_chunks, &stages, ctx->kv_type == KV_FP8 ? 2 * kChunkMax : kChunkMax);
-    if ((int64_t)ctx->group * L.tokens > kMaxGroup) stages = kDeepStages;   // 16 rows: one CTA per SM
-    if ((int64_t)L.batch * num_chunks > ctx->part_slots) return HD_ERR_CAPACITY;
-    // The combine keeps a weight per (head, chunk) plus a float4 row per head in the stage ring.
-    const size_t rows = (size_t)ctx->group * L.tokens;   // query rows per kv head
-    if ((rows * num_chunks + 3) * sizeof(float) + rows * 64 * 16 + (L.total_tokens > 1 ? kMtNewBytes : 0) >
-        (size_t)stages * kStageBytes)
-        return HD_ERR_CAPACITY;
+// The combine keeps a weight per (row, chunk) plus a float4 row per row in the stage ring.
+bool combine_fits(size_t rows, int64_t num_chunks, bool mt, int stages) {
+    return (rows * num_chunks + 3) * sizeof(float) + rows * 64 * 16 + (mt ? kMtNewBytes : 0) <=
+           (size_t)stages * kStageBytes;
+}
+
+// Kernel arguments of one layer call with a given split; its partials start at
+// partial row part_row0 of the workspace, its tickets at the layer's counters.
+void fill_layer_args(const hd_ctx *ctx, const LayerCall &L, int32_t chunk_keys, int32_t num_chunks,
+                     int64_t part_row0, LayerArgs &a) {
     const bool sliding = ctx->layer_types[L.layer] == HD_SLIDING;
     const DeviceTable &tab = sliding ? ctx->table_sliding : ctx->table_full;
-
-    LayerArgs a{};
+    a = LayerArgs{};
     a.context = L.context;
     a.q_bf16 = static_cast<const __nv_bfloat16 *>(L.q_bf16);
     a.q_rot = L.q_rot;
@@ -280,9 +285,9 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     a.gate = L.gate;
     a.out = static_cast<__nv_bfloat16 *>(L.out);
     a.lse = L.lse;
-    a.part_o = ctx->part_o;
-    a.part_ml = ctx->part_ml;
-    a.counters = ctx->counters;
+    a.part_o = ctx->part_o + part_row0 * kHeadDim;
+    a.part_ml = ctx->part_ml + part_row0;
+    a.counters = ctx->counters + (size_t)L.layer * ctx->cfg.max_batch * ctx->cfg.num_kv_heads;
     a.err = ctx->err;
     a.num_q_heads = ctx->cfg.num_q_heads;
     a.num_kv_heads = ctx->cfg.num_kv_heads;
@@ -294,7 +299,23 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     a.tokens = L.tokens;
     a.token0 = L.token0;
     a.total_tokens = L.total_tokens;
+}
 
+hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream) {
+    const CUtensorMap *km = nullptr, *vm = nullptr;
+    hd_status st = maps_for(ctx, L.layer, L.cache, L.batch, &km, &vm);
+    if (st != HD_OK) return st;
+    int32_t chunk_keys = 0, num_chunks = 0, stages = kStages;
+    plan_split(L.batch, ctx->cfg.num_kv_heads, L.max_keys, ctx->num_sms, ctx->part_slots, &chunk_keys,
+               &num_chunks, &stages, ctx->kv_type == KV_FP8 ? 2 * kChunkMax : kChunkMax);
+    if ((int64_t)ctx->group * L.tokens > kMaxGroup) stages = kDeepStages;   // 16 rows: one CTA per SM
+    if ((int64_t)L.batch * num_chunks > ctx->part_slots) return HD_ERR_CAPACITY;
+    const size_t rows = (size_t)ctx->group * L.tokens;   // query rows per kv head
+    if (!combine_fits(rows, num_chunks, L.total_tokens > 1, stages)) return HD_ERR_CAPACITY;
+    LayerArgs a;
+    fill_layer_args(ctx, L, chunk_keys, num_chunks, 0, a);
+
+    const bool sliding = ctx->layer_types[L.layer] == HD_SLIDING;
     const int type = sliding ? HD_SLIDING : HD_FULL;
     const size_t slot = (size_t)type * kProfileEvents + ctx->ev_used[type];
     const bool timed = (ctx->profile_mask & (1 << type)) && ctx->ev_used[type] < (size_t)kProfileEvents &&
@@ -310,6 +331,96 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
         ++ctx->ev_used[type];
     }
     return HD_OK;
+}
+
+// Split of a step grid: one chunk size C (a multiple of kChunkMin keys, up to
+// the cache type's chunk maximum) for every layer, each layer then taking
+// ceil(max_keys / C) chunks per (sequence, kv head).  C minimises an estimate
+// of the grid's time in key-reads per SM, each CTA costing its keys plus
+// kChunkMin for its start and combine: a grid that is resident at once (two
+// CTAs per SM) ends with its most loaded SM, ceil(CTAs / SMs) CTAs of up to C
+// keys; a longer grid takes the total over the SMs plus one CTA of tail.
+int32_t plan_step_chunk(const hd_ctx *ctx, const std::vector<LayerCall> &calls, size_t rows, bool mt) {
+    const int64_t Hkv = ctx->cfg.num_kv_heads, sms = ctx->num_sms;
+    const int64_t cmax = ctx->kv_type == KV_FP8 ? 2 * kChunkMax : kChunkMax;
+    const int stages = rows > (size_t)kMaxGroup ? kDeepStages : kStages;
+    int64_t longest = 1;
+    for (const LayerCall &L : calls) longest = std::max<int64_t>(longest, L.max_keys);
+    int64_t best_c = cmax;
+    double best = -1.0;
+    for (int64_t C = kChunkMin; C <= cmax; C += kChunkMin) {
+        int64_t n = 0;
+        double total = 0.0;
+        bool fits = true;
+        for (const LayerCall &L : calls) {
+            const int64_t ch = L.max_keys > 0 ? (L.max_keys + C - 1) / C : 1;
+            n += L.batch * Hkv * ch;
+            total += (double)L.batch * Hkv * (double)(ch * kChunkMin + L.max_keys);
+            fits = fits && combine_fits(rows, ch, mt, stages);
+        }
+        if (!fits) continue;
+        const double per_cta = (double)(std::min(C, longest) + kChunkMin);
+        const double est = n <= 2 * sms ? (double)((n + sms - 1) / sms) * per_cta : total / sms + per_cta;
+        if (best < 0.0 || est <= best) {   // ties: the longer chunk
+            best = est;
+            best_c = C;
+        }
+        if (C >= longest) break;   // longer chunks change nothing
+    }
+    return (int32_t)best_c;
+}
+
+// Launches the layers of one pass as step grids: consecutive layers share a
+// grid while the grid has at most kStepLayers layers and their partials fit
+// the workspace; a layer whose partials alone do not fit runs its own launch.
+hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cudaStream_t stream) {
+    if (calls.empty()) return HD_OK;
+    const int64_t Hkv = ctx->cfg.num_kv_heads;
+    const size_t rows = (size_t)ctx->group * calls[0].tokens;
+    const bool mt = calls[0].total_tokens > 1;
+    const int32_t C = plan_step_chunk(ctx, calls, rows, mt);
+    StepTable &t = ctx->step_table;
+    int64_t part_row = 0, ctas = 0;
+    t.num_layers = 0;
+    auto flush = [&]() -> hd_status {
+        if (t.num_layers == 0) return HD_OK;
+        const int stages = (ctas <= ctx->num_sms || rows > (size_t)kMaxGroup) ? kDeepStages : kStages;
+        const size_t slot = 2 * (size_t)kProfileEvents + ctx->ev_used[2];
+        const bool timed = (ctx->profile_mask & HD_PROFILE_STEP) && ctx->ev_used[2] < (size_t)kProfileEvents;
+        if (timed && cudaEventRecord(ctx->ev_begin[slot], stream) != cudaSuccess) return HD_ERR_CUDA;
+        hd_status st = cuda_status(launch_step(t, (int)ctas, (int)rows, mt, ctx->kv_type, stages, stream));
+        if (st != HD_OK) return st;
+        ++ctx->launches;
+        if (timed) {
+            if (cudaEventRecord(ctx->ev_end[slot], stream) != cudaSuccess) return HD_ERR_CUDA;
+            ++ctx->ev_used[2];
+        }
+        t.num_layers = 0;
+        part_row = ctas = 0;
+        return HD_OK;
+    };
+    for (const LayerCall &L : calls) {
+        const int64_t ch = L.max_keys > 0 ? (L.max_keys + C - 1) / C : 1;
+        const int64_t need = ch > 1 ? (int64_t)L.batch * Hkv * (int64_t)rows * ch : 0;
+        hd_status st = HD_OK;
+        if (need > ctx->part_rows) {   // too large for a shared grid: its own plan and launch
+            if ((st = flush()) != HD_OK || (st = launch_layer_call(ctx, L, stream)) != HD_OK) return st;
+            continue;
+        }
+        if (t.num_layers == kStepLayers || part_row + need > ctx->part_rows ||
+            ctas + (int64_t)L.batch * Hkv * ch > INT_MAX)
+            if ((st = flush()) != HD_OK) return st;
+        const CUtensorMap *km = nullptr, *vm = nullptr;
+        if ((st = maps_for(ctx, L.layer, L.cache, L.batch, &km, &vm)) != HD_OK) return st;
+        LayerLaunch &e = t.layer[t.num_layers++];
+        e.kmap = *km;
+        e.vmap = *vm;
+        fill_layer_args(ctx, L, C, (int32_t)ch, part_row, e.a);
+        e.cta_begin = (int32_t)ctas;
+        part_row += need;
+        ctas += (int64_t)L.batch * Hkv * ch;
+    }
+    return flush();
 }
 
 uint8_t *stage_row(const hd_ctx *ctx, uint8_t *base, int layer) {
@@ -337,6 +448,57 @@ hd_status full_hint(const hd_ctx *ctx, int32_t max_context_hint, const hd_kv_cac
     if (*hint < 0 || *hint + tokens - 1 > ctx->cfg.max_context) return HD_ERR_CAPACITY;
     if (*hint + tokens > cache.capacity) return HD_ERR_CAPACITY;
     return HD_OK;
+}
+
+// Whether no layer of a step call writes memory (out, lse, caches) that another
+// layer of the call reads or writes, so that all layers can run in one grid.
+// The verdict for the last array checked is kept (a memcmp decides reuse).
+bool layers_independent(hd_ctx *ctx, int batch, int tokens, const hd_layer_io *layers) {
+    const size_t n_layers = (size_t)ctx->cfg.num_layers;
+    if (ctx->indep_batch == batch && ctx->indep_tokens == tokens && ctx->indep_layers.size() == n_layers &&
+        std::memcmp(ctx->indep_layers.data(), layers, n_layers * sizeof(hd_layer_io)) == 0)
+        return ctx->indep_ok;
+    struct Range {
+        uintptr_t begin, end;
+        int layer;
+        bool written;
+    };
+    std::vector<Range> r;
+    r.reserve(n_layers * 11);
+    auto add = [&](const void *p, size_t bytes, int layer, bool written) {
+        if (p && bytes) r.push_back({(uintptr_t)p, (uintptr_t)p + bytes, layer, written});
+    };
+    const size_t Hq = ctx->cfg.num_q_heads, Hkv = ctx->cfg.num_kv_heads, D = kHeadDim;
+    const size_t qrows = (size_t)batch * tokens * Hq, kvrows = (size_t)batch * tokens * Hkv;
+    const size_t es = (size_t)kv_elem_bytes(ctx->kv_type);
+    for (int i = 0; i < (int)n_layers; ++i) {
+        const hd_layer_io &io = layers[i];
+        add(io.q, qrows * D * 2, i, false);
+        add(io.k, kvrows * D * 2, i, false);
+        add(io.v, kvrows * D * 2, i, false);
+        add(io.sink, Hq * sizeof(float), i, false);
+        add(io.gate, qrows * sizeof(float), i, false);
+        add(io.cache.k_scale, Hkv * sizeof(float), i, false);
+        add(io.cache.v_scale, Hkv * sizeof(float), i, false);
+        add(io.out, qrows * D * 2, i, true);
+        add(io.lse, qrows * sizeof(float), i, true);
+        const size_t extent = ((size_t)(batch - 1) * io.cache.seq_stride + Hkv * io.cache.capacity * D) * es;
+        add(io.cache.k, extent, i, true);
+        add(io.cache.v, extent, i, true);
+    }
+    std::sort(r.begin(), r.end(), [](const Range &x, const Range &y) { return x.begin < y.begin; });
+    bool ok = true;
+    for (size_t a = 0; a < r.size() && ok; ++a)
+        for (size_t b = a + 1; b < r.size() && r[b].begin < r[a].end; ++b)
+            if (r[a].layer != r[b].layer && (r[a].written || r[b].written)) {
+                ok = false;
+                break;
+            }
+    ctx->indep_layers.assign(layers, layers + n_layers);
+    ctx->indep_batch = batch;
+    ctx->indep_tokens = tokens;
+    ctx->indep_ok = ok;
+    return ok;
 }
 
 }  // namespace
@@ -431,12 +593,24 @@ hd_status hybrid_decode_init(const hd_config *cfg, hd_ctx **out_ctx) {
         if (s > slots) slots = s;
     }
     ctx->part_slots = slots;
-    // Partials hold up to kMaxRows rows per kv head (query heads, or heads x tokens).
-    const size_t rows = (size_t)Hkv * kMaxRows;
-    bool ok = cudaMalloc(&ctx->part_o, (size_t)slots * rows * kHeadDim * sizeof(float)) == cudaSuccess &&
-              cudaMalloc(&ctx->part_ml, (size_t)slots * rows * sizeof(float2)) == cudaSuccess &&
-              cudaMalloc(&ctx->counters, (size_t)B * Hkv * sizeof(int32_t)) == cudaSuccess &&
-              cudaMemset(ctx->counters, 0, (size_t)B * Hkv * sizeof(int32_t)) == cudaSuccess &&
+    // Partial rows: a single-layer call holds up to kMaxRows rows per kv head
+    // (query heads, or heads x tokens) for each of its slots.  A step grid holds
+    // those of all its multi-chunk layers at once: at full batch and the longest
+    // chunk, or at most two CTAs per SM for short steps; up to 2^20 rows (1 GiB),
+    // beyond which a step runs as several grids.
+    int64_t fused = 2LL * ctx->num_sms * kMaxRows;
+    const int64_t cmax = ctx->kv_type == KV_FP8 ? 2 * kChunkMax : kChunkMax;
+    for (int t : ctx->layer_types) {
+        const int64_t keys = t == HD_FULL ? (int64_t)cfg->max_context + kMaxTokens : cfg->sliding_window;
+        const int64_t ch = (keys + cmax - 1) / cmax;
+        if (ch > 1) fused += (int64_t)B * Hkv * kMaxRows * ch;
+    }
+    ctx->part_rows = std::max<int64_t>(slots * Hkv * kMaxRows, std::min<int64_t>(fused, 1LL << 20));
+    const size_t counters = (size_t)cfg->num_layers * B * Hkv * sizeof(int32_t);
+    bool ok = cudaMalloc(&ctx->part_o, (size_t)ctx->part_rows * kHeadDim * sizeof(float)) == cudaSuccess &&
+              cudaMalloc(&ctx->part_ml, (size_t)ctx->part_rows * sizeof(float2)) == cudaSuccess &&
+              cudaMalloc(&ctx->counters, counters) == cudaSuccess &&
+              cudaMemset(ctx->counters, 0, counters) == cudaSuccess &&
               cudaMalloc(&ctx->err, sizeof(int32_t)) == cudaSuccess &&
               cudaMemset(ctx->err, 0, sizeof(int32_t)) == cudaSuccess;
     const size_t stage = (size_t)cfg->num_layers * B * Hkv * kHeadDim * kv_elem_bytes(ctx->kv_type);
@@ -562,8 +736,8 @@ hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int3
     return launch_layer_call(ctx, L, static_cast<cudaStream_t>(stream));
 }
 
-// One kernel per layer: q is rotated in the CTA prologue, the new key is
-// rotated, scored and stored by the combine (roll layouts shift first).
+// q is rotated in the CTA prologue, the new key is rotated, scored and stored
+// by the combine (roll layouts shift first).
 hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_t max_context_hint,
                       const hd_layer_io *layers, void *stream) {
     return decode_step_tokens(ctx, batch, 1, context, max_context_hint, layers, stream);
@@ -582,6 +756,9 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
         return HD_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ctx->profile_seen[0] = ctx->profile_seen[1] = false;
+    // Every layer is checked before anything is launched.
+    std::vector<LayerCall> &calls = ctx->step_calls;
+    calls.assign(ctx->cfg.num_layers, LayerCall{});
     for (int i = 0; i < ctx->cfg.num_layers; ++i) {
         const hd_layer_io &io = layers[i];
         hd_status st = check_attention(ctx, i, batch, context, io.cache, io.out, io.lse);
@@ -590,7 +767,7 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
             return HD_ERR_INVALID_ARG;
         const bool sliding = ctx->layer_types[i] == HD_SLIDING;
         const bool roll = sliding && ctx->sliding_layout == HD_LAYOUT_ROLL;
-        LayerCall L{};
+        LayerCall &L = calls[i];
         L.layer = i;
         L.batch = batch;
         L.context = context;
@@ -602,9 +779,7 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
         L.gate = io.gate;
         L.out = io.out;
         L.lse = io.lse;
-        // Start streaming while the previous layer drains, unless a roll shift kernel
-        // runs in between (its writes must be complete before this layer reads).
-        L.pdl = i > 0 && !roll;
+        L.total_tokens = num_tokens;
         if (!sliding) {
             int hint = 0;
             if ((st = full_hint(ctx, max_context_hint, io.cache, &hint, num_tokens)) != HD_OK) return st;
@@ -618,44 +793,76 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
             L.new_kind = NEW_ROTATE;
             L.commit = COMMIT_RING;
         } else {
-            RopeArgs r{};
-            r.context = context;
-            r.k = static_cast<const __nv_bfloat16 *>(io.k);
-            r.v = static_cast<const __nv_bfloat16 *>(io.v);
-            r.table = ctx->table_sliding.data;
-            r.dst_k = io.cache.k;
-            r.dst_v = io.cache.v;
-            r.kv_type = ctx->kv_type;
-            r.k_scale = io.cache.k_scale;
-            r.v_scale = io.cache.v_scale;
-            r.seq_stride = io.cache.seq_stride;
-            r.capacity = io.cache.capacity;
-            r.err = ctx->err;
-            r.num_q_heads = ctx->cfg.num_q_heads;
-            r.num_kv_heads = ctx->cfg.num_kv_heads;
-            r.rotary_dim = ctx->table_sliding.rotary_dim;
-            r.key_set = KEYS_ROLL;
-            r.window = ctx->cfg.sliding_window;
-            r.max_context = ctx->cfg.max_context;
-            if ((st = cuda_status(launch_roll_window(r, batch, s))) != HD_OK) return st;
-            ++ctx->launches;
             L.max_keys = ctx->cfg.sliding_window;
             L.key_set = KEYS_ROLL;
             L.new_kind = NEW_NONE;
             L.commit = COMMIT_NONE;
         }
-        const int tmax = std::min(kMaxTokens, kMaxRows / ctx->group);
-        L.total_tokens = num_tokens;
+    }
+    // Roll layouts shift their windows (and append) before any attention reads them.
+    for (const LayerCall &L : calls) {
+        if (L.key_set != KEYS_ROLL) continue;
+        RopeArgs r{};
+        r.context = context;
+        r.k = static_cast<const __nv_bfloat16 *>(L.new_k);
+        r.v = static_cast<const __nv_bfloat16 *>(L.new_v);
+        r.table = ctx->table_sliding.data;
+        r.dst_k = L.cache.k;
+        r.dst_v = L.cache.v;
+        r.kv_type = ctx->kv_type;
+        r.k_scale = L.cache.k_scale;
+        r.v_scale = L.cache.v_scale;
+        r.seq_stride = L.cache.seq_stride;
+        r.capacity = L.cache.capacity;
+        r.err = ctx->err;
+        r.num_q_heads = ctx->cfg.num_q_heads;
+        r.num_kv_heads = ctx->cfg.num_kv_heads;
+        r.rotary_dim = ctx->table_sliding.rotary_dim;
+        r.key_set = KEYS_ROLL;
+        r.window = ctx->cfg.sliding_window;
+        r.max_context = ctx->cfg.max_context;
+        hd_status st = cuda_status(launch_roll_window(r, batch, s));
+        if (st != HD_OK) return st;
+        ++ctx->launches;
+    }
+    const int tmax = std::min(kMaxTokens, kMaxRows / ctx->group);
+    if (ctx->fuse_step && ctx->consumer == CONSUMER_MMA && layers_independent(ctx, batch, num_tokens, layers)) {
+        // Step grids, pass by pass: a pass commits its entries, and the next pass's
+        // grid starts after it in full stream order.
+        for (int t0 = 0; t0 < num_tokens;) {
+            int tp = 1;
+            while (2 * tp <= tmax && 2 * tp <= num_tokens - t0) tp *= 2;
+            for (LayerCall &L : calls) {
+                L.tokens = tp;
+                L.token0 = t0;
+                L.pdl = false;
+            }
+            hd_status st = launch_step_calls(ctx, calls, s);
+            if (st != HD_OK) return st;
+            t0 += tp;
+        }
+        return HD_OK;
+    }
+    // One kernel per layer (and pass); a layer's first pass may start streaming
+    // while the previous layer drains.
+    for (LayerCall &L : calls) {
         for (int t0 = 0; t0 < num_tokens;) {
             int tp = 1;
             while (2 * tp <= tmax && 2 * tp <= num_tokens - t0) tp *= 2;
             L.tokens = tp;
             L.token0 = t0;
-            if (t0 > 0) L.pdl = false;   // the previous pass wrote this layer's cache
-            if ((st = launch_layer_call(ctx, L, s)) != HD_OK) return st;
+            L.pdl = L.layer > 0 && t0 == 0;   // a later pass reads what the previous pass wrote
+            hd_status st = launch_layer_call(ctx, L, s);
+            if (st != HD_OK) return st;
             t0 += tp;
         }
     }
+    return HD_OK;
+}
+
+hd_status hybrid_decode_set_step_fusion(hd_ctx *ctx, int32_t enable) {
+    if (!ctx || (enable != 0 && enable != 1)) return HD_ERR_INVALID_ARG;
+    ctx->fuse_step = enable != 0;
     return HD_OK;
 }
 
@@ -698,24 +905,25 @@ hd_status hybrid_decode_launch_count(hd_ctx *ctx, int64_t *launches) {
 }
 
 hd_status hybrid_decode_set_profiling(hd_ctx *ctx, int32_t enable) {
-    if (!ctx || enable < 0 || enable > (HD_PROFILE_SLIDING | HD_PROFILE_FULL | HD_PROFILE_FIRST_ONLY))
+    if (!ctx || enable < 0 || enable > (HD_PROFILE_SLIDING | HD_PROFILE_FULL | HD_PROFILE_FIRST_ONLY | HD_PROFILE_STEP))
         return HD_ERR_INVALID_ARG;
     if (enable && ctx->ev_begin.empty()) {
-        ctx->ev_begin.resize(2 * kProfileEvents);
-        ctx->ev_end.resize(2 * kProfileEvents);
-        for (int i = 0; i < 2 * kProfileEvents; ++i)
+        ctx->ev_begin.resize(3 * kProfileEvents);
+        ctx->ev_end.resize(3 * kProfileEvents);
+        for (int i = 0; i < 3 * kProfileEvents; ++i)
             if (cudaEventCreate(&ctx->ev_begin[i]) != cudaSuccess ||
                 cudaEventCreate(&ctx->ev_end[i]) != cudaSuccess)
                 return HD_ERR_CUDA;
     }
     ctx->profile_mask = enable;
-    ctx->ev_used[0] = ctx->ev_used[1] = 0;
+    ctx->ev_used[0] = ctx->ev_used[1] = ctx->ev_used[2] = 0;
     return HD_OK;
 }
 
 hd_status hybrid_decode_profile(hd_ctx *ctx, int32_t layer_type, double *total_ms, int64_t *launches) {
     if (!ctx || !total_ms || !launches) return HD_ERR_INVALID_ARG;
-    if (layer_type != HD_SLIDING && layer_type != HD_FULL) return HD_ERR_INVALID_ARG;
+    if (layer_type != HD_SLIDING && layer_type != HD_FULL && layer_type != HD_PROFILE_KIND_STEP)
+        return HD_ERR_INVALID_ARG;
     double sum = 0.0;
     const size_t n = ctx->ev_used[layer_type];
     for (size_t i = 0; i < n; ++i) {

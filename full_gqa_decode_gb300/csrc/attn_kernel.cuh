@@ -1,0 +1,1350 @@
+// One decode-attention layer of the hybrid model in one kernel: partial RoPE
+// of q, split-K flash-decoding over the cached keys, and an LSE combine that
+// scores the new entry, folds in the per-head sink and stores the entry.
+//
+// The math is the scaled-dot-product attention of
+// vllm_omni/edge/spark_export.py (`_Layer.forward`: scores = q.k/sqrt(d),
+// softmax over keys, weights @ values, GQA by viewing q as (kv, group, d)),
+// computed blockwise with an online softmax, which that page notes is
+// numerically the same as one fused softmax (ring-branch comment).  The new
+// entry is scored apart from the cache, as that comment's two-key-set form
+// does.  The sink follows vllm/models/hy_v4/nvidia/flashmla_sparse.py
+// (`HYV4FlashMLASparseImpl`): out *= exp(lse) / (exp(lse) + exp(sink)).  The
+// optional output gate of spark_export.py (`_Layer.forward`: each head's
+// attention output times sigmoid of its gate logit) is applied in the same
+// epilogue scale.
+//
+// Grid: one CTA per (chunk of cached keys, kv head, sequence).  The chunk's K
+// and V rows stream through a shared-memory ring of 32 KiB stages (3 stages,
+// or 6 with one CTA per SM) with TMA tensor loads (128-byte swizzle,
+// completion on mbarriers); four consumer warps split every stage, so each K/V
+// row is read from HBM once for the whole GQA group.  bf16 caches: 32-key
+// stages, a dedicated producer warp.  E4M3 caches (per-kv-head scales):
+// 64-key stages, the producer folded into the consumers (the last warp to
+// release a slot refills it).  Scores are kept in log2 units (q is pre-scaled
+// by log2(e)/sqrt(d)).  Consumers: CUDA-core FMA with warp-shuffle
+// reductions, and tensor-core mma.sync with fp32 accumulation, where q is
+// split into a high and a low part (bf16, or f16 for E4M3 caches) so the
+// scores keep fp32 accuracy.  With MT, several tokens of a sequence are extra
+// query rows (multi-token decode).
+//
+// A launch takes one layer (grid: chunks x kv heads x sequences) or, for a
+// whole decode step, a table of up to kStepLayers layers in its parameters
+// (a 1-D grid, each layer's CTAs a contiguous range): the layers of a step are
+// independent, so one grid streams all their caches with no drain between layers.
+//
+// Each CTA writes an unnormalised partial (o, m, l) per query row, then takes
+// a ticket on a per-(sequence, kv head) counter.  The CTA that draws the last
+// ticket -- every other chunk of that (sequence, kv head) has finished reading
+// -- merges all partials and the new entries, writes out/lse, stores the new
+// K/V entries (ring slot or append) and resets the counter.  Nothing waits on
+// another CTA.
+//
+// This header holds the kernel and its launch templates; the translation units
+// attn_decode.cu, attn_decode_fp8.cu, attn_step.cu and attn_step_fp8.cu each
+// instantiate one family (cache type x single layer / step table).
+#pragma once
+
+#include <cuda_fp16.h>
+
+#include "e4m3.cuh"
+#include "hd_internal.h"
+
+namespace hd {
+namespace {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kQScale = kLog2e * 0.0625f;   // log2(e) / sqrt(256)
+constexpr int kConsumerWarps = 4;
+constexpr int kKeysPerWarp = kStageKeys / kConsumerWarps;  // 8 (bf16 stages; E4M3 stages give 16)
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+// bf16 layers run a dedicated producer warp.  E4M3 layers fold the producer
+// into the consumers (the last warp to release a slot refills it): four warps
+// per CTA leave each thread up to 255 registers at two CTAs per SM, which the
+// E4M3 consumer's conversions need (five warps cap it at 168).
+__host__ __device__ constexpr bool own_producer(int kv) { return kv == KV_BF16; }
+__host__ __device__ constexpr int kv_threads(int kv) { return own_producer(kv) ? kThreads : kConsumerWarps * 32; }
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
+// Inside the stage ring (free once every stage is consumed): the warp buffers
+// [warps][G][256] + (m, l) and the combine weights start at 0; this chunk's
+// merged partial [G][256] + (m, l) sits past both.
+constexpr int kOwnPartialOffset = 48 * 1024;
+// Multi-token combine: the new entries of up to kMaxTokens tokens (K and V
+// values, E4M3 codes) and the per-row weights of the new entries sit in the
+// last kMtNewBytes of the (then free) stage ring.
+
+// ------------------------------------------------------------ PTX helpers --
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+// Waits for the phase with the given parity; false once the time limit passed.
+__device__ __forceinline__ bool mbar_wait(uint64_t *bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const unsigned long long t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
+}
+__device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, uint64_t *bar, int x,
+                                            int y, int z, int w) {
+    asm volatile(
+        "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ float fast_exp2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float fast_log2(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                        uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t &r0, uint32_t &r1, uint32_t &r2,
+                                              uint32_t &r3) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+// D += A(16x16 bf16, row) * B(16x8 bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                          uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// D += A(16x8 bf16, row) * B(8x8 bf16, col), fp32 accumulate.
+__device__ __forceinline__ void mma_1688(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0));
+}
+// m16n8k16 with f16 operands (the FP8 cache path: E4M3 converts to f16 exactly).
+__device__ __forceinline__ void mma_16816_f16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0,
+                                              uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+        "{%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+// Eight E4M3 codes (little-endian in two words) to floats.
+__device__ __forceinline__ void unpack_e4m3x8(const uint2 &r, float (&f)[8]) {
+    const uint32_t w[2] = {r.x, r.y};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t h = e4m3x2_to_f16x2(static_cast<uint16_t>(w[i >> 1] >> (16 * (i & 1))));
+        const float2 v = __half22float2(*reinterpret_cast<const __half2 *>(&h));
+        f[2 * i] = v.x;
+        f[2 * i + 1] = v.y;
+    }
+}
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+__device__ __forceinline__ void unpack_bf16x8(const uint4 &r, float (&f)[8]) {
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+    }
+}
+// Byte offset of 16-byte chunk c (0..31 for bf16, 0..15 for E4M3) of row r in
+// a stage's K or V region: box c/8, swizzled chunk (c%8)^(r%8) inside the
+// 128-byte row.
+template <int KV = KV_BF16>
+__device__ __forceinline__ uint32_t tile_offset(int r, int c) {
+    return (c >> 3) * kv_box_bytes(KV) + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
+}
+// Transpose of an 8x8 matrix of 16-bit elements held one fragment per lane
+// (lane l: row l/4, columns 2(l%4), 2(l%4)+1).
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+// One round-to-nearest-even of a double to bf16, through round-to-odd binary32
+// (Boldo & Melquiond, IEEE TC 2008): the odd-rounded binary32 keeps enough bits
+// that rounding it to bf16 equals rounding the double directly.
+__device__ __forceinline__ float f64_to_bf16_value(double x) {
+    float t = __double2float_rz(x);
+    if ((double)t != x && isfinite(t)) t = __uint_as_float(__float_as_uint(t) | 1u);
+    return __bfloat162float(__float2bfloat16_rn(t));
+}
+
+// Loads what the combine needs from global memory: the new entry (raw k and
+// v for NEW_ROTATE, the staged entry otherwise: bf16 values, or E4M3 codes
+// kept in code_s [2][256]) and the group's sink values and output-gate
+// logits.  (The rotary row at position c is loaded with q.)  Needs 64 threads.
+template <int G, int KV>
+__device__ __forceinline__ void load_combine_inputs(const LayerArgs &a, int b, int kvh, int c, float *kraw_s,
+                                                    float *vnew_s, float2 *tab_s, float *sink_s, float *gate_s,
+                                                    uint8_t *code_s) {
+    const int t = threadIdx.x;
+    if (a.new_kind != NEW_NONE) {   // one 16-byte load per thread, the K row then the V row
+        const size_t e = ((size_t)b * a.num_kv_heads + kvh) * kHeadDim;
+        if (KV == KV_FP8 && a.new_kind == NEW_STAGED) {   // 256 codes per row
+            if (t < 32) {
+                const uint8_t *src = static_cast<const uint8_t *>(t < 16 ? a.new_k : a.new_v) + e;
+                reinterpret_cast<uint4 *>(code_s + (t < 16 ? 0 : kHeadDim))[t & 15] =
+                    reinterpret_cast<const uint4 *>(src)[t & 15];
+            }
+        } else if (t < 64) {                               // 256 bf16 per row
+            const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(t < 32 ? a.new_k : a.new_v) + e;
+            float f[8];
+            unpack_bf16x8(reinterpret_cast<const uint4 *>(src)[t & 31], f);
+            float4 *dst = reinterpret_cast<float4 *>((t < 32 ? kraw_s : vnew_s) + (t & 31) * 8);
+            dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+            dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
+    }
+    if (t < G) {
+        sink_s[t] = a.sink ? a.sink[kvh * G + t] : 0.f;
+        gate_s[t] = a.gate ? a.gate[(size_t)b * a.num_q_heads + kvh * G + t] : 0.f;
+    }
+}
+
+// Scored cache keys of sequence context c, or -1 (and the error bit) when c
+// cannot be served by this call.
+__device__ __forceinline__ int cached_keys(const LayerArgs &a, int c, int *bit) {
+    *bit = 0;
+    if (c < 0) { *bit = HD_DEVERR_CONTEXT_NEGATIVE; return -1; }
+    const int last = c + max(a.tokens, 1) - 1;   // position of the last new token
+    if (last > a.max_context) { *bit = HD_DEVERR_CONTEXT_PLAN; return -1; }
+    int n;
+    switch (a.key_set) {
+    case KEYS_RING: n = min(c, a.capacity); break;
+    case KEYS_ROLL: n = min(c + 1, a.window); break;
+    case KEYS_FULL_CACHED: n = c + 1; break;
+    default: n = c; break;  // KEYS_FULL_PREV
+    }
+    if (n > a.capacity || (a.commit == COMMIT_APPEND && last >= a.capacity)) {
+        *bit = HD_DEVERR_CONTEXT_CAPACITY;
+        return -1;
+    }
+    if ((n + a.chunk_keys - 1) / a.chunk_keys > a.max_chunks) { *bit = HD_DEVERR_CONTEXT_PLAN; return -1; }
+    return n;
+}
+
+// ---------------------------------------------------------- the consumers --
+
+// Ring window of the query rows of a multi-token step: row r (token t) must
+// not see the t oldest ring entries -- positions c-511 .. c+t-512 left its
+// window -- which sit in `cnt[r]` consecutive slots from slot `first`.
+struct RowMask {
+    int first = 0, cap = 1;
+    const int *cnt = nullptr;   // [rows] in shared memory
+    __device__ __forceinline__ bool hidden(int key, int count) const {
+        int rel = key - first;
+        if (rel < 0) rel += cap;
+        return rel < count;
+    }
+};
+
+// CUDA-core consumer: lane owns dims [8*lane, 8*lane+8) of every row; each
+// score is a warp-shuffle reduction.  With an E4M3 cache the rows hold codes:
+// scores take the K scale after the reduction and the output stays in V-code
+// units (the combine applies the V scale).
+template <int G, int KV>
+struct FmaConsumer {
+    static constexpr int kWK = kv_stage_keys(KV) / kConsumerWarps;   // keys per warp per stage
+    float qv[G][8], m[G], l[G], acc[G][8];
+    float kscale;
+
+    __device__ void load_row(const uint8_t *st, int row, int lane, float (&f)[8]) const {
+        if (KV == KV_FP8)
+            unpack_e4m3x8(*reinterpret_cast<const uint2 *>(st + tile_offset<KV>(row, lane >> 1) + (lane & 1) * 8), f);
+        else
+            unpack_bf16x8(*reinterpret_cast<const uint4 *>(st + tile_offset<KV>(row, lane)), f);
+    }
+
+    __device__ void init(const float *q_s, int lane, float k_scale) {
+        kscale = k_scale;
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                qv[h][i] = q_s[h * kHeadDim + lane * 8 + i];
+                acc[h][i] = 0.f;
+            }
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+        }
+    }
+
+    __device__ void set_mask(const RowMask &, int) {}
+
+    // Rows [row0, row0 + kWK) of a stage; the first nvalid are keys.
+    __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane, int) {
+        constexpr int KB = G >= 8 ? 4 : 8;  // keeps scores, q and acc in registers
+#pragma unroll
+        for (int sb = 0; sb < kWK; sb += KB) {
+            const int nv = nvalid - sb;
+            if (nv <= 0) break;  // warp-uniform
+            float sc[KB][G];
+#pragma unroll
+            for (int r = 0; r < KB; ++r) {
+                const int row = row0 + sb + r;
+                float kf[8];
+                load_row(kst, row, lane, kf);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    float d = 0.f;
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) d = fmaf(qv[h][i], kf[i], d);
+#pragma unroll
+                    for (int off = 16; off > 0; off >>= 1) d += __shfl_xor_sync(0xffffffffu, d, off);
+                    if (KV == KV_FP8) d *= kscale;
+                    sc[r][h] = (r < nv) ? d : -INFINITY;
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                float mx = sc[0][h];
+#pragma unroll
+                for (int r = 1; r < KB; ++r) mx = fmaxf(mx, sc[r][h]);
+                const float mn = fmaxf(m[h], mx);
+                const float alpha = fast_exp2(m[h] - mn);  // m = -inf -> 0
+                m[h] = mn;
+                l[h] *= alpha;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc[h][i] *= alpha;
+#pragma unroll
+                for (int r = 0; r < KB; ++r) {
+                    const float p = (r < nv) ? fast_exp2(sc[r][h] - mn) : 0.f;
+                    sc[r][h] = p;
+                    l[h] += p;
+                }
+            }
+#pragma unroll
+            for (int r = 0; r < KB; ++r) {
+                if (r < nv) {  // rows past the key set may hold NaN: never touch them
+                    float vf[8];
+                    load_row(vst, row0 + sb + r, lane, vf);
+#pragma unroll
+                    for (int h = 0; h < G; ++h)
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[h][i] = fmaf(sc[r][h], vf[i], acc[h][i]);
+                }
+            }
+        }
+    }
+
+    __device__ void store(float *red_o, float *red_m, float *red_l, int warp, int lane) const {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            float4 *dst = reinterpret_cast<float4 *>(red_o + (warp * G + h) * kHeadDim + lane * 8);
+            dst[0] = make_float4(acc[h][0], acc[h][1], acc[h][2], acc[h][3]);
+            dst[1] = make_float4(acc[h][4], acc[h][5], acc[h][6], acc[h][7]);
+            if (lane == 0) {
+                red_m[warp * G + h] = m[h];
+                red_l[warp * G + h] = l[h];
+            }
+        }
+    }
+};
+
+// Tensor-core consumer.  S = Q K^T with m16n8k16: rows 0..G-1 of the A tile
+// hold bf16(q) and rows 8..8+G-1 hold bf16(q - bf16(q)), so row r plus row r+8
+// of S is q.k to fp32 accuracy; the 8 keys of a warp are the N dimension and
+// the K rows come straight from the swizzled TMA tile with ldmatrix.  The
+// accumulator of S is, register for register, the B operand of
+// O^T += V^T P^T (m16n8k8: dims on M, 8 keys on K, heads on N), whose A
+// operand is V read with ldmatrix.trans.
+template <int G, bool MT = false>
+struct MmaConsumer {
+    static constexpr int kWK = 8;   // keys per consume call
+    uint32_t qa[16][4];
+    float o[16][4];   // O^T tile mt: rows dims 16mt + gid (+8), cols heads 2*t4 (+1)
+    float m_run, l_run;  // for head gid; l_run sums this lane's keys only
+    RowMask mask;
+    int mcnt;            // MT: ring entries hidden from row gid
+
+    __device__ void set_mask(const RowMask &m, int lane) {
+        mask = m;
+        mcnt = (lane >> 2) < G ? m.cnt[lane >> 2] : 0;
+    }
+
+    __device__ void init(const float *q_s, int lane, float) {
+        const int gid = lane >> 2, t4 = lane & 3;
+#pragma unroll
+        for (int ks = 0; ks < 16; ++ks) {
+            uint32_t r[4] = {0u, 0u, 0u, 0u};
+            if (gid < G) {
+                const float *qh = q_s + gid * kHeadDim + 16 * ks + 2 * t4;
+                const float x0 = qh[0], x1 = qh[1], x2 = qh[8], x3 = qh[9];
+                const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
+                const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
+                const float h2 = __bfloat162float(__float2bfloat16_rn(x2));
+                const float h3 = __bfloat162float(__float2bfloat16_rn(x3));
+                r[0] = pack_bf16(h0, h1);
+                r[1] = pack_bf16(x0 - h0, x1 - h1);
+                r[2] = pack_bf16(h2, h3);
+                r[3] = pack_bf16(x2 - h2, x3 - h3);
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j) qa[ks][j] = r[j];
+        }
+#pragma unroll
+        for (int mt = 0; mt < 16; ++mt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[mt][j] = 0.f;
+        m_run = -INFINITY;
+        l_run = 0.f;
+    }
+
+    __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane, int key0) {
+        const int gid = lane >> 2, t4 = lane & 3;
+        const int lrow = row0 + (lane & 7), lsub = lane >> 3;
+        const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
+        // Two accumulators (even / odd k-steps) halve the dependent MMA chain.
+        float s[4] = {0.f, 0.f, 0.f, 0.f}, s2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kbase + tile_offset(lrow, 4 * p + lsub), b0, b1, b2, b3);
+            mma_16816(s, qa[2 * p], b0, b1);
+            mma_16816(s2, qa[2 * p + 1], b2, b3);
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) s[j] += s2[j];
+        bool ok0 = gid < G && 2 * t4 < nvalid, ok1 = gid < G && 2 * t4 + 1 < nvalid;
+        if (MT) {
+            ok0 = ok0 && !mask.hidden(key0 + 2 * t4, mcnt);
+            ok1 = ok1 && !mask.hidden(key0 + 2 * t4 + 1, mcnt);
+        }
+        const float s0 = ok0 ? s[0] + s[2] : -INFINITY;
+        const float s1 = ok1 ? s[1] + s[3] : -INFINITY;
+        float mx = fmaxf(s0, s1);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m_run, mx);
+        const float alpha = (mn == -INFINITY) ? 1.f : fast_exp2(m_run - mn);
+        const float p0 = ok0 ? fast_exp2(s0 - mn) : 0.f;
+        const float p1 = ok1 ? fast_exp2(s1 - mn) : 0.f;
+        l_run = fmaf(l_run, alpha, p0 + p1);
+        m_run = mn;
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * t4);      // head 2*t4
+            const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * t4 + 4);  // head 2*t4+1
+#pragma unroll
+            for (int mt = 0; mt < 16; ++mt) {
+                o[mt][0] *= a_lo;
+                o[mt][1] *= a_hi;
+                o[mt][2] *= a_lo;
+                o[mt][3] *= a_hi;
+            }
+        }
+        const uint32_t pb = pack_bf16(p0, p1);
+        // Rows past the key set may hold NaN; 0 * NaN would poison the sum.
+        uint32_t vmask = 0xFFFFFFFFu;
+        if (nvalid < kKeysPerWarp)
+            vmask = (2 * t4 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 1 < nvalid ? 0xFFFF0000u : 0u);
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            uint32_t a0, a1, a2, a3;
+            ldsm_x4_trans(vbase + tile_offset(lrow, 4 * p + lsub), a0, a1, a2, a3);
+            mma_1688(o[2 * p], a0 & vmask, a1 & vmask, pb);
+            mma_1688(o[2 * p + 1], a2 & vmask, a3 & vmask, pb);
+        }
+    }
+
+    __device__ void store(float *red_o, float *red_m, float *red_l, int warp, int lane) const {
+        const int gid = lane >> 2, t4 = lane & 3;
+        float l = l_run;
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        if (t4 == 0 && gid < G) {
+            red_m[warp * G + gid] = m_run;
+            red_l[warp * G + gid] = l;
+        }
+        const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+#pragma unroll
+        for (int mt = 0; mt < 16; ++mt) {
+            const int d = 16 * mt + gid;
+            if (h0 < G) {
+                red_o[(warp * G + h0) * kHeadDim + d] = o[mt][0];
+                red_o[(warp * G + h0) * kHeadDim + d + 8] = o[mt][2];
+            }
+            if (h1 < G) {
+                red_o[(warp * G + h1) * kHeadDim + d] = o[mt][1];
+                red_o[(warp * G + h1) * kHeadDim + d + 8] = o[mt][3];
+            }
+        }
+    }
+};
+
+// Tensor-core consumer for an E4M3 cache.  Codes convert exactly to f16
+// (cvt.rn.f16x2.e4m3x2), so both products run as f16 MMAs (m16n8k16) with
+// fp32 accumulation.  A warp takes 16 keys of a 64-key stage, and K is the A
+// operand: S^T = K Q^T puts 16 keys on M and the q columns on N -- the f16
+// high part of each head's q and, on the remaining columns, its low part
+// (G <= 4: columns G..2G-1; G = 8: a second tile) -- so q costs two
+// registers per k-step and one MMA covers 16 keys.
+//
+// K: lane (gid, t4) holds keys gid and gid + 8 and reads 16-byte chunks
+// 2*t4 + (p & 1) + 8*(p >> 1) of both rows at step p (the eight lanes of a
+// shared-memory phase then hit eight distinct chunks after the swizzle).
+// Word j of a chunk is the A fragment of k-step 4p + j: dims (d, d+1) and
+// (d+2, d+3) with d = 16*chunk + 4j; the q columns are built in init with the
+// same dim order, which leaves every dot product unchanged.
+//
+// P: the S^T accumulator, packed to f16, is for each group of 8 keys one
+// fragment of an 8x8 (keys x heads) matrix; movmatrix transposes it into the
+// B operand of O^T += V^T P^T (m16n8k16: dims on M, 16 keys on K, heads on N).
+// V: lane (gid, t4) reads chunk gid (and 8 + gid) of keys 2*t4, 2*t4+1,
+// 2*t4+8, 2*t4+9; byte_perm pairs two keys' bytes of one dim, which is one
+// E4M3x2 A register.  Tile mt covers, on row gid, dim
+// 128*(mt / 8) + 16*gid + 2*(mt % 8) and, on row gid + 8, the next dim.
+template <int G, bool MT = false>
+struct Fp8MmaConsumer {
+    static constexpr int NT = G == 8 ? 2 : 1;   // n-tiles of q columns
+    static constexpr int kWK = 16;              // keys per warp per stage
+    uint32_t qb[NT][16][2];
+    float o[16][4];                              // O^T tile mt: dims (see above) x heads 2*t4 (+1)
+    float m_run[2], l_run[2];                    // heads 2*t4 + e; l_run sums this lane's keys only
+    float kscale;
+    RowMask mask;
+    int mcnt[2];                                 // MT: ring entries hidden from rows 2*t4 + e
+
+    __device__ void set_mask(const RowMask &m, int lane) {
+        mask = m;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) mcnt[e] = 2 * (lane & 3) + e < G ? m.cnt[2 * (lane & 3) + e] : 0;
+    }
+
+    __device__ void init(const float *q_s, int lane, float k_scale) {
+        const int gid = lane >> 2, t4 = lane & 3;
+        kscale = k_scale;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            // column gid of tile t: head and part (high or low f16 half of q)
+            const bool lo = G == 8 ? t == 1 : gid >= G;
+            const int head = G == 8 ? gid : (gid < G ? gid : gid - G);
+            const bool used = G == 8 || gid < 2 * G;
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const int chunk = 2 * t4 + (p & 1) + 8 * (p >> 1);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t r0 = 0u, r1 = 0u;
+                    if (used) {
+                        const float *qh = q_s + head * kHeadDim + 16 * chunk + 4 * j;
+                        float x[4];
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            const float h = __half2float(__float2half_rn(qh[i]));
+                            x[i] = lo ? qh[i] - h : h;
+                        }
+                        r0 = pack_f16(x[0], x[1]);
+                        r1 = pack_f16(x[2], x[3]);
+                    }
+                    qb[t][4 * p + j][0] = r0;
+                    qb[t][4 * p + j][1] = r1;
+                }
+            }
+        }
+#pragma unroll
+        for (int mt = 0; mt < 16; ++mt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) o[mt][j] = 0.f;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            m_run[e] = -INFINITY;
+            l_run[e] = 0.f;
+        }
+    }
+
+    __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane, int key0) {
+        const int gid = lane >> 2, t4 = lane & 3;
+        // S^T = K Q^T.  With one q tile, even and odd k-steps go to two accumulators
+        // (half the dependent chain); two tiles are two chains already.
+        float s[NT][4], s2[NT][4];
+#pragma unroll
+        for (int t = 0; t < NT; ++t)
+#pragma unroll
+            for (int r = 0; r < 4; ++r) s[t][r] = s2[t][r] = 0.f;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const int chunk = 2 * t4 + (p & 1) + 8 * (p >> 1);
+            const uint4 ka = *reinterpret_cast<const uint4 *>(kst + tile_offset<KV_FP8>(row0 + gid, chunk));
+            const uint4 kb = *reinterpret_cast<const uint4 *>(kst + tile_offset<KV_FP8>(row0 + gid + 8, chunk));
+            const uint32_t wa[4] = {ka.x, ka.y, ka.z, ka.w}, wb[4] = {kb.x, kb.y, kb.z, kb.w};
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const uint32_t a[4] = {e4m3x2_to_f16x2(static_cast<uint16_t>(wa[j] & 0xFFFFu)),
+                                       e4m3x2_to_f16x2(static_cast<uint16_t>(wb[j] & 0xFFFFu)),
+                                       e4m3x2_to_f16x2(static_cast<uint16_t>(wa[j] >> 16)),
+                                       e4m3x2_to_f16x2(static_cast<uint16_t>(wb[j] >> 16))};
+#pragma unroll
+                for (int t = 0; t < NT; ++t) {
+                    if ((j & 1) && NT == 1)
+                        mma_16816_f16(s2[t], a, qb[t][4 * p + j][0], qb[t][4 * p + j][1]);
+                    else
+                        mma_16816_f16(s[t], a, qb[t][4 * p + j][0], qb[t][4 * p + j][1]);
+                }
+            }
+        }
+        // Scores: registers 0/1 are key gid, 2/3 key gid + 8, for heads 2*t4 + e; add the low part.
+        float sc[4];
+#pragma unroll
+        for (int r = 0; r < 4; ++r) sc[r] = s[0][r] + s2[0][r];
+        if (G == 8) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) sc[r] += s[NT - 1][r] + s2[NT - 1][r];
+        } else if (G >= 2) {  // column c + G lives in lane t4 + G/2
+#pragma unroll
+            for (int r = 0; r < 4; ++r) sc[r] += __shfl_xor_sync(0xffffffffu, sc[r], G / 2);
+        } else {              // G = 1: column 1 of the same lane
+            sc[0] += sc[1];
+            sc[2] += sc[3];
+        }
+        const bool k0 = gid < nvalid, k1 = gid + 8 < nvalid;
+        float p[4], alpha[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            const bool col = G == 8 || 2 * t4 + e < G;
+            bool v0 = col && k0, v1 = col && k1;
+            if (MT) {
+                v0 = v0 && !mask.hidden(key0 + gid, mcnt[e]);
+                v1 = v1 && !mask.hidden(key0 + gid + 8, mcnt[e]);
+            }
+            const float x0 = v0 ? sc[e] * kscale : -INFINITY;
+            const float x1 = v1 ? sc[2 + e] * kscale : -INFINITY;
+            float mx = fmaxf(x0, x1);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+            const float mn = fmaxf(m_run[e], mx);
+            alpha[e] = (mn == -INFINITY) ? 1.f : fast_exp2(m_run[e] - mn);
+            p[e] = v0 ? fast_exp2(x0 - mn) : 0.f;
+            p[2 + e] = v1 ? fast_exp2(x1 - mn) : 0.f;
+            l_run[e] = fmaf(l_run[e], alpha[e], p[e] + p[2 + e]);
+            m_run[e] = mn;
+        }
+        if (__any_sync(0xffffffffu, alpha[0] != 1.f || alpha[1] != 1.f)) {
+#pragma unroll
+            for (int mt = 0; mt < 16; ++mt) {
+                o[mt][0] *= alpha[0];
+                o[mt][1] *= alpha[1];
+                o[mt][2] *= alpha[0];
+                o[mt][3] *= alpha[1];
+            }
+        }
+        const uint32_t pb0 = movmatrix_trans(pack_f16(p[0], p[1]));   // keys 2*t4, +1 of head gid
+        const uint32_t pb1 = movmatrix_trans(pack_f16(p[2], p[3]));   // keys 8 + 2*t4, +1
+        // Rows past the key set may hold NaN codes; 0 * NaN would poison the sum.
+        uint32_t m01 = 0xFFFFFFFFu, m89 = 0xFFFFFFFFu;
+        if (nvalid < kWK) {
+            m01 = (2 * t4 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 1 < nvalid ? 0xFFFF0000u : 0u);
+            m89 = (2 * t4 + 8 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 9 < nvalid ? 0xFFFF0000u : 0u);
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int chunk = 8 * half + gid;
+            const uint4 v0 = *reinterpret_cast<const uint4 *>(vst + tile_offset<KV_FP8>(row0 + 2 * t4, chunk));
+            const uint4 v1 = *reinterpret_cast<const uint4 *>(vst + tile_offset<KV_FP8>(row0 + 2 * t4 + 1, chunk));
+            const uint4 v8 = *reinterpret_cast<const uint4 *>(vst + tile_offset<KV_FP8>(row0 + 2 * t4 + 8, chunk));
+            const uint4 v9 = *reinterpret_cast<const uint4 *>(vst + tile_offset<KV_FP8>(row0 + 2 * t4 + 9, chunk));
+            const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+            const uint32_t w8[4] = {v8.x, v8.y, v8.z, v8.w}, w9[4] = {v9.x, v9.y, v9.z, v9.w};
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+#pragma unroll
+                for (int q = 0; q < 2; ++q) {   // dims 4w + 2q (row gid) and 4w + 2q + 1 (row gid + 8)
+                    const uint32_t sel = q ? 0x7362u : 0x5140u;   // (key a, key b) byte pairs of two dims
+                    const uint32_t x01 = __byte_perm(w0[w], w1[w], sel);
+                    const uint32_t x89 = __byte_perm(w8[w], w9[w], sel);
+                    const uint32_t a[4] = {e4m3x2_to_f16x2(static_cast<uint16_t>(x01 & 0xFFFFu)) & m01,
+                                           e4m3x2_to_f16x2(static_cast<uint16_t>(x01 >> 16)) & m01,
+                                           e4m3x2_to_f16x2(static_cast<uint16_t>(x89 & 0xFFFFu)) & m89,
+                                           e4m3x2_to_f16x2(static_cast<uint16_t>(x89 >> 16)) & m89};
+                    mma_16816_f16(o[8 * half + 2 * w + q], a, pb0, pb1);
+                }
+            }
+        }
+    }
+
+    __device__ void store(float *red_o, float *red_m, float *red_l, int warp, int lane) const {
+        const int gid = lane >> 2, t4 = lane & 3;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+            float l = l_run[e];
+            l += __shfl_xor_sync(0xffffffffu, l, 4);
+            l += __shfl_xor_sync(0xffffffffu, l, 8);
+            l += __shfl_xor_sync(0xffffffffu, l, 16);
+            const int h = 2 * t4 + e;
+            if (gid == 0 && h < G) {
+                red_m[warp * G + h] = m_run[e];
+                red_l[warp * G + h] = l;
+            }
+        }
+        const int h0 = 2 * t4, h1 = 2 * t4 + 1;
+#pragma unroll
+        for (int mt = 0; mt < 16; ++mt) {
+            const int d = 128 * (mt >> 3) + 16 * gid + 2 * (mt & 7);
+            if (h0 < G)
+                *reinterpret_cast<float2 *>(red_o + (warp * G + h0) * kHeadDim + d) = make_float2(o[mt][0], o[mt][2]);
+            if (h1 < G)
+                *reinterpret_cast<float2 *>(red_o + (warp * G + h1) * kHeadDim + d) = make_float2(o[mt][1], o[mt][3]);
+        }
+    }
+};
+
+// ------------------------------------------------------------- the kernel --
+
+// G: query rows per kv head -- the GQA group, or with MT (multi-token) the
+// group times a.tokens tokens of the same sequence, row r = token r / (G /
+// a.tokens), head r % (G / a.tokens).  G = 16 (MT only) runs two row groups
+// of 8: warps 0-1 take rows 0-7 and warps 2-3 rows 8-15, each pair splitting
+// every stage's keys, so each warp keeps the 8-row consumer's registers.
+// NL: layers in the parameter table (1: one layer, grid (chunks, kv heads,
+// sequences); kStepLayers: a step, 1-D grid over the layers' CTA ranges).
+template <int G, int CONSUMER, int S, int KV, bool MT, int NL>
+__global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kStages * kStageBytes ? 2 : 1)
+    attn_layer_kernel(const __grid_constant__ LaunchTable<NL> p) {
+    constexpr int kStage = kv_stage_bytes(KV);     // bytes of one stage (K + V)
+    constexpr int kKeys = kv_stage_keys(KV);       // keys per stage: 32 bf16, 64 E4M3
+    constexpr int kBoxes = kv_boxes_per_row(KV);   // 128-byte boxes per K or V row
+    constexpr int kNThreads = kv_threads(KV);
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    float *q_s = reinterpret_cast<float *>(smem + S * kStage);               // [G][256]
+    float *knew_s = q_s + G * kHeadDim;                                        // [256]
+    float *vnew_s = knew_s + kHeadDim;                                         // [256]
+    float *kraw_s = vnew_s + kHeadDim;                                         // [256]
+    float2 *tab_s = reinterpret_cast<float2 *>(kraw_s + kHeadDim);             // [128]
+    float *misc = reinterpret_cast<float *>(tab_s + kHeadDim / 2);             // [32]
+    uint64_t *full = reinterpret_cast<uint64_t *>(misc + 32);
+    uint64_t *empty = full + S;
+    int *flag_s = reinterpret_cast<int *>(empty + S);
+    unsigned *rel_s = reinterpret_cast<unsigned *>(flag_s + 4);                // [S] slot releases (folded producer)
+    uint8_t *code_s = reinterpret_cast<uint8_t *>(rel_s + 16);                 // [2][256] E4M3 new entry
+    int *mcnt_s = reinterpret_cast<int *>(code_s + 2 * kHeadDim);               // [kMaxRows] MT ring masks
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // This CTA's layer: the last one whose CTA range starts at or before it
+    // (each lane tests one table entry; the ranges ascend).
+    int layer = 0;
+    if constexpr (NL > 1) {
+        static_assert(NL <= 32, "one lane per table entry");
+        const bool started = lane < p.num_layers && p.layer[lane].cta_begin <= (int)blockIdx.x;
+        layer = 31 - __clz(__ballot_sync(0xffffffffu, started));
+    }
+    const LayerLaunch &ll = p.layer[layer];
+    const LayerArgs &a = ll.a;
+    int chunk, kvh, b;
+    if constexpr (NL > 1) {
+        const int local = (int)blockIdx.x - ll.cta_begin;
+        chunk = local % a.max_chunks;
+        kvh = (local / a.max_chunks) % a.num_kv_heads;
+        b = local / (a.max_chunks * a.num_kv_heads);
+    } else {
+        chunk = blockIdx.x;
+        kvh = blockIdx.y;
+        b = blockIdx.z;
+    }
+    // Programmatic dependent launch: the next grid in the stream may start as
+    // soon as every CTA of this one has started.  Launched that way (only
+    // behind another layer of the same step, see launch_layer), a CTA reads its
+    // own layer's inputs and streams its own layer's cache -- nothing the
+    // previous grid writes -- and waits for that grid (griddepcontrol.wait)
+    // only before its first global write.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Tokens of this launch: one, or (MT) a.tokens tokens at positions c .. c + ntok - 1.
+    const int ntok = MT ? a.tokens : 1;
+    const int Gm = G / ntok;                               // model heads per kv head
+    const int c = a.context[b] + (MT ? a.token0 : 0);
+    // Row r of q / out / lse / gate in units of head vectors.
+    auto qrow = [&](int r) -> size_t {
+        if (!MT) return (size_t)b * a.num_q_heads + kvh * G + r;
+        return ((size_t)b * a.total_tokens + a.token0 + r / Gm) * a.num_q_heads + kvh * Gm + r % Gm;
+    };
+    const float kscale = KV == KV_FP8 ? a.k_scale[kvh] : 1.f;
+    const float vscale = KV == KV_FP8 ? a.v_scale[kvh] : 1.f;
+    int bit = 0;
+    const int n = cached_keys(a, c, &bit);
+    if (n < 0) {
+        if (chunk == 0) {  // this CTA reports and poisons the outputs of the group
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+            if (threadIdx.x == 0) atomicOr(a.err, bit);
+            for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
+                const size_t r = qrow(i / kHeadDim);
+                a.out[r * kHeadDim + i % kHeadDim] = __float2bfloat16_rn(NAN);
+                if (i % kHeadDim == 0) a.lse[r] = NAN;
+            }
+        }
+        return;
+    }
+    const int nchunks = max(1, (n + a.chunk_keys - 1) / a.chunk_keys);
+    if (chunk >= nchunks) return;  // uniform over the CTA
+    const int start = chunk * a.chunk_keys;
+    const int end = min(start + a.chunk_keys, n);
+    const int nst = end > start ? (end - start + kKeys - 1) / kKeys : 0;
+    // New entries of the ntok tokens: values as scored (knew_t), V values (or
+    // V codes' values for E4M3, vnew_t), codes, and per-row new-entry weights.
+    uint8_t *mt_base = smem + S * kStage - kMtNewBytes;
+    float *knew_t = MT ? reinterpret_cast<float *>(mt_base) : knew_s;                      // [ntok][256]
+    float *vnew_t = MT ? knew_t + kMaxTokens * kHeadDim : vnew_s;                            // [ntok][256]
+    uint8_t *code_t = MT ? reinterpret_cast<uint8_t *>(vnew_t + kMaxTokens * kHeadDim) : code_s;
+    const int vcode_off = MT ? kMaxTokens * kHeadDim : kHeadDim;                             // V codes
+    constexpr int WN = MT ? kMaxTokens : 1;                                                  // wnew_t row stride
+    float *wnew_t = MT ? reinterpret_cast<float *>(code_t + 2 * kMaxTokens * kHeadDim) : misc + kMaxGroup;
+    float *rows_t = wnew_t + kMaxRows * kMaxTokens;   // MT: per-row sink, gate, scale [3][kMaxRows]
+    // Makes the new entries of the ntok tokens: the key rotated in fp64 and rounded
+    // once to bf16, or quantised to E4M3 (fp64 rotation, one division, one
+    // rounding; V too), each scored as stored; E4M3 V stays in code units.
+    auto make_new_entries = [&]() {
+        for (int idx = threadIdx.x; idx < ntok * kHeadDim; idx += blockDim.x) {
+            const int t = idx / kHeadDim, d = idx % kHeadDim;
+            // Raw k of token t at dim i and its rotary row (MT reads them here; a
+            // single token's were fetched with the combine's other inputs).
+            const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(a.new_k) +
+                                      ((size_t)(b * a.total_tokens + a.token0 + t) * a.num_kv_heads + kvh) * kHeadDim;
+            const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(a.new_v) +
+                                      ((size_t)(b * a.total_tokens + a.token0 + t) * a.num_kv_heads + kvh) * kHeadDim;
+            auto kraw = [&](int i) -> double { return MT ? (double)__bfloat162float(kg[i]) : (double)kraw_s[i]; };
+            auto tab = [&](int j) -> float2 {
+                return MT ? a.table[(size_t)(c + t) * (a.rotary_dim >> 1) + j] : tab_s[j];
+            };
+            const float vraw = MT ? __bfloat162float(vg[d]) : vnew_s[d];
+            if (KV == KV_FP8) {
+                // E4M3 entry: quantise (fp64 rotation, one division, one rounding) unless staged;
+                // score it as stored (code * scale) and keep V in code units.
+                if (a.new_kind == NEW_ROTATE) {
+                    double y = kraw(d);
+                    if (d < a.rotary_dim) {
+                        const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
+                        const double x1 = kraw(j), x2 = kraw(j + half);
+                        const float2 cs2 = tab(j);
+                        const double cc = cs2.x, ss = cs2.y;
+                        y = d < half ? __dsub_rn(__dmul_rn(x1, cc), __dmul_rn(x2, ss))
+                                     : __dadd_rn(__dmul_rn(x2, cc), __dmul_rn(x1, ss));
+                    }
+                    code_t[t * kHeadDim + d] = e4m3_quotient(y, (double)kscale);
+                    code_t[vcode_off + t * kHeadDim + d] = e4m3_quotient((double)vraw, (double)vscale);
+                }
+                knew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[t * kHeadDim + d]) * kscale;
+                vnew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[vcode_off + t * kHeadDim + d]);
+            } else {
+                float kn;
+                if (a.new_kind == NEW_STAGED || d >= a.rotary_dim) {
+                    kn = (float)kraw(d);
+                } else {  // rotate the new key in fp64 from the fp32 table, round once to bf16
+                    const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
+                    const double x1 = kraw(j), x2 = kraw(j + half);
+                    const float2 cs2 = tab(j);
+                    const double cc = cs2.x, ss = cs2.y;
+                    kn = f64_to_bf16_value(d < half ? x1 * cc - x2 * ss : x2 * cc + x1 * ss);
+                }
+                knew_t[t * kHeadDim + d] = kn;
+                vnew_t[t * kHeadDim + d] = vraw;
+            }
+        }
+    };
+
+    // Stage s of the chunk: one lane issues its K and V boxes into slot s % S.
+    auto issue_stage = [&](int s) {
+        const int slot = s % S;
+        uint8_t *st = smem + slot * kStage;
+        mbar_arrive_expect_tx(&full[slot], kStage);
+        const int row = start + s * kKeys;
+#pragma unroll
+        for (int j = 0; j < kBoxes; ++j)
+            tma_load_4d(st + j * kv_box_bytes(KV), &ll.kmap, &full[slot], j * kv_box_cols(KV), row, kvh, b);
+#pragma unroll
+        for (int j = 0; j < kBoxes; ++j)
+            tma_load_4d(st + (kBoxes + j) * kv_box_bytes(KV), &ll.vmap, &full[slot], j * kv_box_cols(KV), row, kvh,
+                        b);
+    };
+    // Test hook: stages from a.drop_stage on are never issued (a copy that never arrives).
+    auto droppable = [&](int s) { return a.drop_stage >= 0 && s >= a.drop_stage; };
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < S; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kConsumerWarps);
+            rel_s[s] = 0u;
+        }
+        fence_mbar_init();
+    }
+    // q of the group in log2 units.  Round 1: the raw q rows (16-byte loads),
+    // the rotary row at position c and, when this CTA will combine a single
+    // chunk, the combine's other inputs -- all requested at once.
+    const bool has_new = a.new_kind != NEW_NONE;
+    const int half = a.rotary_dim >> 1;
+    if (a.q_bf16) {
+        for (int i = threadIdx.x; i < G * (kHeadDim / 8); i += blockDim.x) {
+            const int r = i / (kHeadDim / 8), c8 = i % (kHeadDim / 8);
+            float f[8];
+            unpack_bf16x8(*reinterpret_cast<const uint4 *>(a.q_bf16 + qrow(r) * kHeadDim + c8 * 8), f);
+            float4 *dst = reinterpret_cast<float4 *>(q_s + r * kHeadDim + c8 * 8);
+            dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+            dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
+        if (!MT)
+            for (int j = threadIdx.x; j < half; j += blockDim.x) tab_s[j] = a.table[(size_t)c * half + j];
+    } else {
+        for (int i = threadIdx.x; i < G * (kHeadDim / 4); i += blockDim.x)
+            reinterpret_cast<float4 *>(q_s)[i] =
+                reinterpret_cast<const float4 *>(a.q_rot + qrow(i / (kHeadDim / 4)) * kHeadDim)[i % (kHeadDim / 4)];
+    }
+    if (!MT && nchunks == 1)
+        load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, misc + 2 * kMaxGroup,
+                                   misc + 3 * kMaxGroup, code_s);
+    __syncthreads();
+    // Folded producer: the first S stages go out once the prologue's loads are
+    // in (issued earlier, their traffic delayed those loads).
+    if (!own_producer(KV) && threadIdx.x == 0)
+        for (int s = 0; s < min(S, nst) && !droppable(s); ++s) issue_stage(s);
+    // Round 2: rotate each rotary pair in place (fp32; q only feeds the scores)
+    // and scale every dim to log2 units.
+    if (a.q_bf16) {
+        for (int p = threadIdx.x; p < G * half; p += blockDim.x) {
+            const int r = p / half, j = p % half;
+            const float2 t = MT ? a.table[(size_t)(c + r / Gm) * half + j] : tab_s[j];   // position c + token
+            float *qr = q_s + r * kHeadDim;
+            const float x1 = qr[j], x2 = qr[j + half];
+            qr[j] = fmaf(x1, t.x, -x2 * t.y) * kQScale;
+            qr[j + half] = fmaf(x2, t.x, x1 * t.y) * kQScale;
+        }
+        const int pass = kHeadDim - 2 * half;
+        for (int i = threadIdx.x; i < G * pass; i += blockDim.x) q_s[(i / pass) * kHeadDim + 2 * half + i % pass] *= kQScale;
+    } else {
+        for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) q_s[i] *= kQScale;
+    }
+    // A single chunk is combined by this CTA: make its new entry now, while the
+    // first stages are in flight (its inputs arrived with q).
+    if (!MT && has_new && nchunks == 1) make_new_entries();
+    // MT ring layers: row r (token t) does not see the t oldest ring entries (the
+    // ones its window has passed); rows of a full layer see the whole cache.
+    if (MT && threadIdx.x < G) {
+        const int t = threadIdx.x / Gm;
+        mcnt_s[threadIdx.x] =
+            a.key_set == KEYS_RING ? (c >= a.capacity ? t : max(0, c + t - a.capacity)) : 0;
+    }
+    RowMask mask;
+    mask.first = c >= a.capacity ? c % a.capacity : 0;
+    mask.cap = a.capacity;
+    mask.cnt = mcnt_s;
+    __syncthreads();
+
+    // Row groups: RG groups of CG rows; each group's WPG warps split every stage.
+    constexpr int RG = G > 8 ? G / 8 : 1, CG = G / RG, WPG = kConsumerWarps / RG;
+    float *red_o = reinterpret_cast<float *>(smem);             // [warps][CG][256], reuses the stage ring
+    float *red_m = red_o + kConsumerWarps * CG * kHeadDim;
+    float *red_l = red_m + kConsumerWarps * CG;
+    if (own_producer(KV) && warp == kConsumerWarps) {
+        if (lane == 0) {  // producer: one lane issues every load of the chunk
+            for (int s = 0; s < nst; ++s) {
+                if (droppable(s)) break;
+                const int slot = s % S;
+                if (s >= S && !mbar_wait(&empty[slot], ((s / S) - 1) & 1)) {
+                    atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
+                    break;
+                }
+                issue_stage(s);
+            }
+        }
+        __syncthreads();
+        __syncthreads();
+    } else {
+        using Mma = typename std::conditional<KV == KV_FP8, Fp8MmaConsumer<CG, MT>, MmaConsumer<CG, MT>>::type;
+        typename std::conditional<CONSUMER == CONSUMER_MMA, Mma, FmaConsumer<CG, KV>>::type cons;
+        constexpr int kCallKeys = decltype(cons)::kWK;          // keys per consume call
+        constexpr int kSpan = kKeys / WPG;                        // keys of a stage per warp
+        const int rg = warp / WPG, kpart = warp % WPG;
+        cons.init(q_s + rg * CG * kHeadDim, lane, kscale);
+        if (MT) {
+            RowMask gm = mask;
+            gm.cnt = mcnt_s + rg * CG;
+            cons.set_mask(gm, lane);
+        }
+        for (int s = 0; s < nst; ++s) {
+            const int slot = s % S;
+            if (!mbar_wait(&full[slot], (s / S) & 1)) {
+                if (lane == 0) atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
+                break;
+            }
+            const uint8_t *kst = smem + slot * kStage;
+#pragma unroll
+            for (int sub = 0; sub < kSpan; sub += kCallKeys) {
+                const int row0 = kpart * kSpan + sub;
+                const int nvalid = min(kCallKeys, end - (start + s * kKeys + row0));
+                if (nvalid > 0)
+                    cons.consume(kst, kst + kBoxes * kv_box_bytes(KV), row0, nvalid, lane, start + s * kKeys + row0);
+            }
+            __syncwarp();  // orders every lane's reads of the slot before lane 0's release
+            if (lane == 0) {
+                if (own_producer(KV)) {
+                    mbar_arrive(&empty[slot]);
+                } else {
+                    // Folded producer: the last of the consumer warps to release the slot
+                    // refills it with stage s + S (release / acquire through the counter,
+                    // then a proxy fence before the async-proxy write).
+                    __threadfence_block();
+                    const unsigned prev = atomicAdd(&rel_s[slot], 1u);
+                    if (prev % kConsumerWarps == kConsumerWarps - 1 && s + S < nst && !droppable(s + S)) {
+                        __threadfence_block();
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        issue_stage(s + S);
+                    }
+                }
+            }
+        }
+        __syncthreads();  // every stage consumed: the ring is free for the warp merge
+        cons.store(red_o, red_m, red_l, warp, lane);
+        __syncthreads();
+    }
+
+    // Everything above only read this layer's own inputs and cache.  The first
+    // global write (partials, tickets, outputs, the stored entry) waits for the
+    // previous grid in the stream to complete and its writes to be visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // Merge the warps into this chunk's partial: kept in shared memory (past the
+    // warp buffers) and, when the sequence has several chunks, written out.
+    // Partials: G rows per (sequence, kv head), num_kv_heads * G rows per sequence.
+    const size_t pbase = ((size_t)b * a.num_kv_heads * G + kvh * G) * a.max_chunks;
+    float *own_o = reinterpret_cast<float *>(smem + kOwnPartialOffset);   // [G][256]
+    float2 *own_ml = reinterpret_cast<float2 *>(own_o + G * kHeadDim);    // [G]
+    for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
+        const int h = i / kHeadDim, d = i % kHeadDim;
+        const int w0 = (h / CG) * WPG, hr = h % CG;   // the warps of this row's group, its row there
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = w0; w < w0 + WPG; ++w) M = fmaxf(M, red_m[w * CG + hr]);
+        float o = 0.f, L = 0.f;
+#pragma unroll
+        for (int w = w0; w < w0 + WPG; ++w) {
+            const float wt = (M == -INFINITY) ? 0.f : fast_exp2(red_m[w * CG + hr] - M);
+            o = fmaf(wt, red_o[(w * CG + hr) * kHeadDim + d], o);
+            L = fmaf(wt, red_l[w * CG + hr], L);
+        }
+        own_o[i] = o;
+        if (d == 0) own_ml[h] = make_float2(M, L);
+        if (nchunks > 1) {
+            const size_t pi = pbase + (size_t)h * a.max_chunks + chunk;
+            __stcg(a.part_o + pi * kHeadDim + d, o);
+            if (d == 0) __stcg(reinterpret_cast<float2 *>(a.part_ml) + pi, make_float2(M, L));
+        }
+    }
+    __syncthreads();
+
+    // Ticket: the last chunk of this (sequence, kv head) to finish does the combine.
+    // The acq_rel atomic publishes this CTA's partial (ordered after the barrier)
+    // and, for the last CTA, makes every other chunk's partial visible.
+    if (nchunks > 1) {
+        if (threadIdx.x == 0) {
+            int *ctr = a.counters + (size_t)b * a.num_kv_heads + kvh;
+            int ticket;
+            asm volatile("atom.add.acq_rel.gpu.s32 %0, [%1], 1;" : "=r"(ticket) : "l"(ctr) : "memory");
+            const int last = ticket == nchunks - 1;
+            if (last) atomicExch(ctr, 0);  // ready for the next call on this stream
+            *flag_s = last;
+        }
+        __syncthreads();
+        if (!*flag_s) return;
+    }
+
+    // ---- combine (one CTA per sequence and kv head) ----
+    // Every global input of the combine is requested in one round: the new
+    // entry, its rotary row, the sink and the gate logits (unless the prologue
+    // fetched them), and each warp's chunk maxima and sums.
+    float *sink_s = MT ? rows_t : misc + 2 * kMaxGroup;                  // [G]
+    float *gate_s = MT ? rows_t + kMaxRows : misc + 3 * kMaxGroup;       // [G]
+    if (!MT && nchunks > 1)
+        load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, sink_s, gate_s, code_s);
+    if (MT && threadIdx.x < G) {   // per row: the sink of its head, the gate logit of its token and head
+        sink_s[threadIdx.x] = a.sink ? a.sink[kvh * Gm + threadIdx.x % Gm] : 0.f;
+        gate_s[threadIdx.x] = a.gate ? a.gate[qrow(threadIdx.x)] : 0.f;
+    }
+    const float2 *pml = reinterpret_cast<const float2 *>(a.part_ml);
+    constexpr int kPerLane = 4;
+    float2 ml[kPerLane];
+    {
+        const int h = warp < G ? warp : 0;
+        const size_t ph = pbase + (size_t)h * a.max_chunks;
+#pragma unroll
+        for (int r = 0; r < kPerLane; ++r) {
+            const int j = lane + 32 * r;
+            ml[r] = make_float2(-INFINITY, 0.f);
+            if (j < nchunks) ml[r] = nchunks == 1 ? own_ml[h] : __ldcg(pml + ph + j);
+        }
+    }
+    __syncthreads();
+    if (has_new && (MT || nchunks > 1)) {   // a single chunk's entry was made in the prologue
+        make_new_entries();
+        __syncthreads();
+    }
+    // Per head: M = max(chunk maxima, new score), chunk weights 2^(m_j - M) and
+    // L = sum of weighted chunk sums (+ the new entry).  Warp w takes heads w, w + warps, ...
+    float *wts = reinterpret_cast<float *>(smem);   // [G][nchunks] (the warp buffers are free)
+    float *head_s = MT ? rows_t + 2 * kMaxRows : misc;   // [G] scale = sink factor * gate / L
+    for (int h = warp; h < G; h += kNThreads / 32) {
+        const size_t ph = pbase + (size_t)h * a.max_chunks;
+        if (h != warp) {  // a second head for this warp: its pairs were not preloaded
+#pragma unroll
+            for (int r = 0; r < kPerLane; ++r) {
+                const int j = lane + 32 * r;
+                ml[r] = make_float2(-INFINITY, 0.f);
+                if (j < nchunks) ml[r] = nchunks == 1 ? own_ml[h] : __ldcg(pml + ph + j);
+            }
+        }
+        // Scores of the new entries row h sees: its own token's and (MT) the earlier tokens'.
+        const int th = MT ? h / Gm : 0;
+        float s_new = -INFINITY;
+        if (has_new) {
+            for (int j = 0; j <= th; ++j) {
+                float t = 0.f;
+                for (int d = lane; d < kHeadDim; d += 32)
+                    t = fmaf(q_s[h * kHeadDim + d], knew_t[j * kHeadDim + d], t);
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+                if (lane == 0) wnew_t[h * WN + j] = t;
+                s_new = fmaxf(s_new, t);
+            }
+            __syncwarp();
+        }
+        float M = s_new;
+#pragma unroll
+        for (int r = 0; r < kPerLane; ++r) M = fmaxf(M, ml[r].x);
+        for (int j = lane + 32 * kPerLane; j < nchunks; j += 32) M = fmaxf(M, __ldcg(pml + ph + j).x);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+        float L = 0.f;
+#pragma unroll
+        for (int r = 0; r < kPerLane; ++r) {
+            const int j = lane + 32 * r;
+            if (j < nchunks) {
+                const float w = (ml[r].x == -INFINITY) ? 0.f : fast_exp2(ml[r].x - M);
+                wts[h * nchunks + j] = w;
+                L = fmaf(w, ml[r].y, L);
+            }
+        }
+        for (int j = lane + 32 * kPerLane; j < nchunks; j += 32) {
+            const float2 m2 = __ldcg(pml + ph + j);
+            const float w = (m2.x == -INFINITY) ? 0.f : fast_exp2(m2.x - M);
+            wts[h * nchunks + j] = w;
+            L = fmaf(w, m2.y, L);
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) L += __shfl_xor_sync(0xffffffffu, L, off);
+        float w_new = 0.f;   // lane j <= th: weight of new entry j
+        if (has_new && lane <= th) w_new = fast_exp2(wnew_t[h * WN + lane] - M);
+        __syncwarp();
+        if (has_new && lane <= th) wnew_t[h * WN + lane] = w_new;
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) w_new += __shfl_xor_sync(0xffffffffu, w_new, off);
+        L += w_new;
+        if (lane == 0) {
+            const float lse = (M + fast_log2(L)) * kLn2;
+            // exp(lse) / (exp(lse) + exp(sink)) = 1 / (1 + 2^((sink - lse) * log2 e))
+            float f = a.sink ? 1.f / (1.f + fast_exp2((sink_s[h] - lse) * kLog2e)) : 1.f;
+            // output gate: sigmoid(g) = 1 / (1 + 2^(-g * log2 e)); lse is not gated
+            if (a.gate) f *= 1.f / (1.f + fast_exp2(-gate_s[h] * kLog2e));
+            head_s[h] = f / L * vscale;   // FP8: partials and the new value are in V-code units
+            a.lse[qrow(h)] = lse;
+        }
+    }
+    __syncthreads();
+    // Outputs: thread t < 128 owns dims [4*(t%64), +4) of every head for the
+    // chunks of parity t/64; the two parities meet in shared memory.
+    float4 *half_s = reinterpret_cast<float4 *>(wts + ((G * nchunks + 3) & ~3));   // [G][64], 16-byte aligned
+    const int dq = threadIdx.x & 63, parity = threadIdx.x >> 6;
+    float4 acc[G];
+#pragma unroll
+    for (int h = 0; h < G; ++h) acc[h] = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (nchunks == 1) {
+        if (parity == 0) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float4 v = reinterpret_cast<const float4 *>(own_o)[h * 64 + dq];
+                const float w = wts[h];
+                acc[h] = make_float4(w * v.x, w * v.y, w * v.z, w * v.w);
+            }
+        }
+    } else if (parity < 2) {
+        const float4 *po = reinterpret_cast<const float4 *>(a.part_o) + pbase * (kHeadDim / 4) + dq;
+        for (int j = parity; j < nchunks; j += 2) {
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const float w = wts[h * nchunks + j];
+                const float4 v = __ldcg(po + ((size_t)h * a.max_chunks + j) * (kHeadDim / 4));
+                acc[h].x = fmaf(w, v.x, acc[h].x);
+                acc[h].y = fmaf(w, v.y, acc[h].y);
+                acc[h].z = fmaf(w, v.z, acc[h].z);
+                acc[h].w = fmaf(w, v.w, acc[h].w);
+            }
+        }
+    }
+    if (parity == 1) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) half_s[h * 64 + dq] = acc[h];
+    }
+    __syncthreads();
+    if (parity == 0) {
+#pragma unroll
+        for (int h = 0; h < G; ++h) {
+            const float4 o1 = half_s[h * 64 + dq];
+            float o[4] = {acc[h].x + o1.x, acc[h].y + o1.y, acc[h].z + o1.z, acc[h].w + o1.w};
+            const float sc = head_s[h];
+            if (has_new) {
+                const int th = MT ? h / Gm : 0;
+                for (int j = 0; j <= th; ++j) {
+                    const float wn = wnew_t[h * WN + j];
+                    const float4 vn = *reinterpret_cast<const float4 *>(vnew_t + j * kHeadDim + 4 * dq);
+                    o[0] = fmaf(wn, vn.x, o[0]);
+                    o[1] = fmaf(wn, vn.y, o[1]);
+                    o[2] = fmaf(wn, vn.z, o[2]);
+                    o[3] = fmaf(wn, vn.w, o[3]);
+                }
+            }
+            __nv_bfloat16 r[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) r[i] = __float2bfloat16_rn(o[i] * sc);
+            uint2 packed;
+            packed.x = (uint32_t)__bfloat16_as_ushort(r[0]) | ((uint32_t)__bfloat16_as_ushort(r[1]) << 16);
+            packed.y = (uint32_t)__bfloat16_as_ushort(r[2]) | ((uint32_t)__bfloat16_as_ushort(r[3]) << 16);
+            *reinterpret_cast<uint2 *>(a.out + qrow(h) * kHeadDim + 4 * dq) = packed;
+        }
+    }
+    // Store the new entries now that every chunk of this (sequence, kv head) has read the cache.
+    if (has_new && a.commit != COMMIT_NONE) {
+        for (int idx = threadIdx.x; idx < ntok * kHeadDim; idx += blockDim.x) {
+            const int t = idx / kHeadDim, d = idx % kHeadDim;
+            const int slot = a.commit == COMMIT_RING ? (c + t) % a.capacity : c + t;
+            const size_t o = (size_t)b * a.seq_stride + ((size_t)kvh * a.capacity + slot) * kHeadDim + d;
+            if (KV == KV_FP8) {
+                static_cast<uint8_t *>(a.cache_k)[o] = code_t[t * kHeadDim + d];
+                static_cast<uint8_t *>(a.cache_v)[o] = code_t[vcode_off + t * kHeadDim + d];
+            } else {  // exact: the values are bf16 values
+                static_cast<__nv_bfloat16 *>(a.cache_k)[o] = __float2bfloat16_rn(knew_t[t * kHeadDim + d]);
+                static_cast<__nv_bfloat16 *>(a.cache_v)[o] = __float2bfloat16_rn(vnew_t[t * kHeadDim + d]);
+            }
+        }
+    }
+}
+
+template <int G, int CONSUMER, int S, int KV, bool MT, int NL>
+cudaError_t launch_g(const LaunchTable<NL> &p, dim3 grid, bool pdl, cudaStream_t s) {
+    static bool configured = false;
+    const size_t smem = layer_smem_bytes(G, S * kv_stage_bytes(KV) / kStageBytes);
+    if (!configured) {
+        cudaError_t e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER, S, KV, MT, NL>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        configured = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = dim3(kv_threads(KV));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, attn_layer_kernel<G, CONSUMER, S, KV, MT, NL>, p);
+}
+
+// S counts stages of the cache's type: an E4M3 ring has twice the bf16 count.
+// rows: query rows per kv head (group x tokens of the pass); mt: a pass of a
+// multi-token step.  Step tables (NL > 1) run the tensor-core consumer only.
+template <int CONSUMER, int S_BF16, int KV, int NL>
+cudaError_t launch_c(const LaunchTable<NL> &p, dim3 grid, int rows, bool mt, bool pdl, cudaStream_t s) {
+    constexpr int S = S_BF16 * kStageBytes / kv_stage_bytes(KV);
+    if (mt) {   // tensor-core consumer, rows = group x tokens
+        if (CONSUMER != CONSUMER_MMA) return cudaErrorInvalidValue;
+        switch (rows) {
+        case 1: return launch_g<1, CONSUMER_MMA, S, KV, true, NL>(p, grid, pdl, s);
+        case 2: return launch_g<2, CONSUMER_MMA, S, KV, true, NL>(p, grid, pdl, s);
+        case 4: return launch_g<4, CONSUMER_MMA, S, KV, true, NL>(p, grid, pdl, s);
+        case 8: return launch_g<8, CONSUMER_MMA, S, KV, true, NL>(p, grid, pdl, s);
+        case 16:   // 16 rows: one CTA per SM with the deep ring
+            if constexpr (S_BF16 == kDeepStages) return launch_g<16, CONSUMER_MMA, S, KV, true, NL>(p, grid, pdl, s);
+            return cudaErrorInvalidValue;
+        default: return cudaErrorInvalidValue;
+        }
+    }
+    switch (rows) {
+    case 1: return launch_g<1, CONSUMER, S, KV, false, NL>(p, grid, pdl, s);
+    case 2: return launch_g<2, CONSUMER, S, KV, false, NL>(p, grid, pdl, s);
+    case 4: return launch_g<4, CONSUMER, S, KV, false, NL>(p, grid, pdl, s);
+    case 8: return launch_g<8, CONSUMER, S, KV, false, NL>(p, grid, pdl, s);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+template <int KV, int NL>
+cudaError_t launch_kv(const LaunchTable<NL> &p, dim3 grid, int rows, bool mt, int consumer, int stages, bool pdl,
+                      cudaStream_t s) {
+    if constexpr (NL > 1) {
+        if (consumer != CONSUMER_MMA) return cudaErrorInvalidValue;
+        return stages == kDeepStages ? launch_c<CONSUMER_MMA, kDeepStages, KV, NL>(p, grid, rows, mt, pdl, s)
+                                     : launch_c<CONSUMER_MMA, kStages, KV, NL>(p, grid, rows, mt, pdl, s);
+    } else {
+        if (stages == kDeepStages)
+            return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA, kDeepStages, KV, NL>(p, grid, rows, mt, pdl, s)
+                                            : launch_c<CONSUMER_FMA, kDeepStages, KV, NL>(p, grid, rows, mt, pdl, s);
+        return consumer == CONSUMER_MMA ? launch_c<CONSUMER_MMA, kStages, KV, NL>(p, grid, rows, mt, pdl, s)
+                                        : launch_c<CONSUMER_FMA, kStages, KV, NL>(p, grid, rows, mt, pdl, s);
+    }
+}
+
+}  // namespace
+}  // namespace hd

@@ -126,6 +126,25 @@ struct RopeArgs {
     int32_t key_set, window, max_context;
 };
 
+// Kernel parameters of an attention launch: a table of layers, each with its
+// K and V cache views and arguments.  A single-layer launch (NL = 1) runs a
+// (chunks, kv heads, sequences) grid; a step table (NL = kStepLayers) runs a
+// 1-D grid where layer i owns the CTAs [cta_begin, next layer's cta_begin),
+// ordered (sequence, kv head, chunk) with the chunk fastest.
+constexpr int kStepLayers = 32;
+struct alignas(64) LayerLaunch {
+    CUtensorMap kmap, vmap;
+    LayerArgs a;
+    int32_t cta_begin;
+};
+template <int NL>
+struct LaunchTable {
+    LayerLaunch layer[NL];
+    int32_t num_layers;
+};
+using StepTable = LaunchTable<kStepLayers>;
+static_assert(sizeof(StepTable) <= 32764, "kernel parameters are limited to 32764 bytes");
+
 cudaError_t launch_rope_append(const RopeArgs &a, int batch, cudaStream_t s);
 cudaError_t launch_roll_window(const RopeArgs &a, int batch, cudaStream_t s);
 // `stages` in bf16 stages (kStages or kDeepStages); a.kv_type picks the kernel.
@@ -135,6 +154,19 @@ cudaError_t launch_roll_window(const RopeArgs &a, int batch, cudaStream_t s);
 // and its own cache): the kernel starts streaming before that grid is done.
 cudaError_t launch_layer(const CUtensorMap *kmap, const CUtensorMap *vmap, const LayerArgs &a,
                          int batch, int group, int consumer, int stages, bool pdl, cudaStream_t s);
+// One grid for the t.num_layers layers of a step table (num_ctas CTAs in all;
+// every layer with the same cache type, rows per kv head and pass shape; the
+// tensor-core consumer).  The layers must be independent: no layer reads or
+// writes what another one writes.
+cudaError_t launch_step(const StepTable &t, int num_ctas, int rows, bool mt, int kv, int stages, cudaStream_t s);
+// Per-family launchers, one translation unit each (rows: query rows per kv
+// head; mt: a pass of a multi-token step).
+cudaError_t launch_layer_bf16(const LaunchTable<1> &t, dim3 grid, int rows, bool mt, int consumer, int stages,
+                              bool pdl, cudaStream_t s);
+cudaError_t launch_layer_fp8(const LaunchTable<1> &t, dim3 grid, int rows, bool mt, int consumer, int stages,
+                             bool pdl, cudaStream_t s);
+cudaError_t launch_step_bf16(const StepTable &t, dim3 grid, int rows, bool mt, int stages, cudaStream_t s);
+cudaError_t launch_step_fp8(const StepTable &t, dim3 grid, int rows, bool mt, int stages, cudaStream_t s);
 size_t layer_smem_bytes(int group, int stages);
 
 }  // namespace hd

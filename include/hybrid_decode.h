@@ -201,16 +201,18 @@ hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int3
                            int32_t max_context_hint, const float *q_rot, hd_kv_cache cache,
                            const float *sink, const float *gate, void *out, float *lse, void *stream);
 
-/* One decode step over all layers in order, with the same results as
- * rope_append_kv followed by the layer's attention call, in one kernel per
- * layer: q is rotated in the attention kernel and the new entry is rotated,
- * scored and stored (appended, or written to its ring slot after the ring was
- * read) by the combine; a roll layout first shifts its window.  `layers` is a
- * host array [num_layers].  A layer's kernel may start reading its own
- * inputs and streaming its own cache while the previous layer of the call is
- * still running (it writes nothing before that layer is complete), so within
- * one call no layer's inputs or cache may alias another layer's outputs or
- * cache.  The first layer waits for all earlier work in the stream. */
+/* One decode step over all layers, with the same results as rope_append_kv
+ * followed by the layer's attention call for each layer in order: q is
+ * rotated in the attention kernel and the new entry is rotated, scored and
+ * stored (appended, or written to its ring slot after the ring was read) by
+ * the combine; roll layouts first shift their windows.  `layers` is a host
+ * array [num_layers].  The layers of a call are independent: by default one
+ * grid runs the attention of all of them (hybrid_decode_set_step_fusion),
+ * otherwise one kernel per layer, each of which may start streaming its own
+ * cache while the previous layer is still running.  So within one call no
+ * layer's inputs or cache may alias another layer's outputs or cache.  The
+ * step waits for all earlier work in the stream.  Every layer is checked
+ * before anything is launched. */
 hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_t max_context_hint,
                       const hd_layer_io *layers, void *stream);
 
@@ -238,6 +240,16 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
  * layer's output only the cache prefetch part of that overlap applies.  0
  * runs every layer in full stream order (measurement, comparison). */
 hd_status hybrid_decode_set_layer_overlap(hd_ctx *ctx, int32_t enable);
+
+/* Step fusion in decode_step / decode_step_tokens (default 1): the attention of
+ * all layers of a call (of a pass, with several tokens) runs as one grid --
+ * up to 32 layers per grid, as many as the split-K workspace holds -- with
+ * one chunk size planned over all layers, instead of one kernel per layer.
+ * The results are the same.  It applies with the tensor-core consumer when no
+ * layer's out, lse or cache overlaps memory of another layer of the call
+ * (checked on the host); otherwise, or with 0, each layer runs its own kernel
+ * (overlapping as hybrid_decode_set_layer_overlap says). */
+hd_status hybrid_decode_set_step_fusion(hd_ctx *ctx, int32_t enable);
 
 /* Inner loop of the attention kernels (same results within the stated
  * tolerance; the default is the tensor-core one):
@@ -271,10 +283,20 @@ hd_status hybrid_decode_launch_count(hd_ctx *ctx, int64_t *launches);
  * before the previous work in the stream is complete (decode_step otherwise
  * lets a layer start streaming while the previous layer drains), so the
  * events time the kernel alone and the other layers keep overlapping.
+ * With step fusion on, decode_step launches step grids instead of layer
+ * kernels: HD_PROFILE_STEP brackets each step grid (up to 4096 between reads,
+ * read back with layer_type HD_PROFILE_KIND_STEP); the layer-type bits then
+ * bracket only layers that run their own launch.
  * hybrid_decode_profile synchronises on the events and returns, for layers of
- * the given hd_layer_type, the summed kernel time and launch count since the
- * last read, then resets that type's records. */
-enum { HD_PROFILE_SLIDING = 1 << HD_SLIDING, HD_PROFILE_FULL = 1 << HD_FULL, HD_PROFILE_FIRST_ONLY = 4 };
+ * the given hd_layer_type (or step grids), the summed kernel time and launch
+ * count since the last read, then resets those records. */
+enum {
+    HD_PROFILE_SLIDING = 1 << HD_SLIDING,
+    HD_PROFILE_FULL = 1 << HD_FULL,
+    HD_PROFILE_FIRST_ONLY = 4,
+    HD_PROFILE_STEP = 8
+};
+enum { HD_PROFILE_KIND_STEP = 2 };
 hd_status hybrid_decode_set_profiling(hd_ctx *ctx, int32_t enable);
 hd_status hybrid_decode_profile(hd_ctx *ctx, int32_t layer_type, double *total_ms, int64_t *launches);
 

@@ -74,7 +74,9 @@ class LayerCase:
 
     def cache(self, hd, kd, vd, dev):
         if self.kv == "fp8":
-            return hd.kv_cache(kd, vd, self.k_scale.to(dev), self.v_scale.to(dev))
+            # the descriptor holds raw pointers: keep the device scales alive with the case
+            self.scales_dev = (self.k_scale.to(dev), self.v_scale.to(dev))
+            return hd.kv_cache(kd, vd, *self.scales_dev)
         return hd.kv_cache(kd, vd)
 
 

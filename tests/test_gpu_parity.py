@@ -244,13 +244,15 @@ def test_decode_step_multistep_lockstep(hd, orc, layout):
 
 @pytest.mark.parametrize("kv", ["bf16", "fp8"])
 def test_layer_overlap_changes_no_bit(hd, kv):
-    """decode_step with and without the layer overlap (a layer starting before the
-    previous one finishes) computes the same bits: outputs, lse and caches."""
+    """decode_step layer by layer (no step fusion) with and without the layer
+    overlap (a layer starting before the previous one finishes) computes the same
+    bits: outputs, lse and caches."""
     import bench
     dev = torch.device("cuda")
     runs = []
     for overlap in (True, False):
         wl = bench.Workload("block4_b16_c512_32768", dev, seed=3, kv=kv)
+        hd.hybrid_decode_set_step_fusion(wl.ctx, False)
         hd.hybrid_decode_set_layer_overlap(wl.ctx, overlap)
         wl.step()
         torch.cuda.synchronize()

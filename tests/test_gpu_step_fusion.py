@@ -1,0 +1,172 @@
+"""GPU parity of step grids (decode_step with step fusion, the default): the
+attention of every layer of a step in one grid, with one chunk size planned
+over all layers.  Outputs and lse against the oracle within the harness
+tolerances, written caches bit-exact; launch counts show which path ran."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from harness import FULL, RING, ROLL, SLIDING, LayerCase, assert_bits_equal, assert_lse_close, assert_out_close
+from harness import oracle_layer
+
+pytestmark = pytest.mark.gpu
+D = synth.HEAD_DIM
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _need_gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+
+
+def launches(hd, ctx):
+    return hd.hybrid_decode_launch_count(ctx)
+
+
+class Step:
+    """Seeded inputs of one decode_step over `types`, kept on the device."""
+
+    def __init__(self, hd, rng, types, B, Hq, Hkv, context, layout, max_context, sink=None, kv="bf16"):
+        self.types, self.layout = types, layout
+        self.context = np.asarray(context, np.int32)
+        self.cases, self.ios, self.dev = [], [], []
+        for t in types:
+            cap = (511 if layout == RING else 512) if t == SLIDING else max_context + 1
+            case = LayerCase(rng, B, Hq, Hkv, cap, self.context, sink=sink, kv=kv)
+            kd, vd = case.kc.cuda(), case.vc.cuda()
+            out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+            lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+            keep = (case.q.cuda(), case.k.cuda(), case.v.cuda(), None if sink is None else sink.cuda())
+            self.ios.append(hd.layer_io(keep[0], keep[1], keep[2], case.cache(hd, kd, vd, "cuda"), keep[3],
+                                        out, lse))
+            self.cases.append(case)
+            self.dev.append((out, lse, kd, vd, keep))
+
+    def run(self, hd, ctx, hint=0):
+        hd.decode_step(ctx, torch.from_numpy(self.context).cuda(), self.ios, len(self.context), hint)
+        torch.cuda.synchronize()
+        assert hd.hybrid_decode_device_errors(ctx) == 0
+
+    def check(self, orc):
+        for i, (t, case) in enumerate(zip(self.types, self.cases)):
+            ref = oracle_layer(orc, case, t, self.layout)
+            out, lse, kd, vd, _ = self.dev[i]
+            assert_out_close(out, ref["out"], f"layer {i} out")
+            assert_lse_close(lse, ref["lse"], f"layer {i} lse")
+            assert_bits_equal(kd, ref["kcache"], f"layer {i} K cache")
+            assert_bits_equal(vd, ref["vcache"], f"layer {i} V cache")
+
+
+def make_ctx(hd, types, B, max_context, layout=RING, Hq=8, Hkv=2, kv="bf16"):
+    return hd.hybrid_decode_init(hd.Config(layer_types=types, num_q_heads=Hq, num_kv_heads=Hkv, max_batch=B,
+                                           max_context=max_context, cache_layout=layout,
+                                           kv_dtype=hd.HD_KV_FP8_E4M3 if kv == "fp8" else hd.HD_KV_BF16))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_batch1_28_layer_step_is_one_grid(hd, orc, kv):
+    """The batch-1 28-layer step at context 4096 (many short chunks, one CTA per
+    SM): one launch, equal to the oracle layer by layer."""
+    rng = synth.generator(1101)
+    types = synth.SPARK_LAYER_TYPES
+    ctx = make_ctx(hd, types, 1, 4096, kv=kv)
+    step = Step(hd, rng, types, 1, 8, 2, [4096 - 1], RING, 4096, kv=kv)
+    n0 = launches(hd, ctx)
+    step.run(hd, ctx, hint=4096 - 1)
+    assert launches(hd, ctx) - n0 == 1
+    step.check(orc)
+    ctx.close()
+
+
+@pytest.mark.parametrize("layout", [RING, ROLL])
+def test_step_grid_launch_counts_and_parity(hd, orc, layout):
+    """Ring: one grid for the 28 layers; roll: the 21 window shifts, then one grid."""
+    rng = synth.generator(1102)
+    types = synth.SPARK_LAYER_TYPES
+    ctx = make_ctx(hd, types, 3, 2048, layout=layout)
+    sink = synth.sink_vector(rng, ("normal", 1.0, 0.0), 8)
+    step = Step(hd, rng, types, 3, 8, 2, [0, 700, 2047], layout, 2048, sink=sink)
+    n0 = launches(hd, ctx)
+    step.run(hd, ctx)
+    assert launches(hd, ctx) - n0 == (1 if layout == RING else 1 + types.count(SLIDING))
+    step.check(orc)
+    ctx.close()
+
+
+def test_more_layers_than_one_grid_holds(hd, orc):
+    """40 layers: two grids (32 + 8 layers), same results."""
+    rng = synth.generator(1103)
+    types = [SLIDING, SLIDING, SLIDING, FULL] * 10
+    ctx = make_ctx(hd, types, 2, 1500)
+    step = Step(hd, rng, types, 2, 8, 2, [300, 1499], RING, 1500)
+    n0 = launches(hd, ctx)
+    step.run(hd, ctx)
+    assert launches(hd, ctx) - n0 == 2
+    step.check(orc)
+    ctx.close()
+
+
+@pytest.mark.parametrize("g", [1, 2, 8])
+def test_step_grid_groups(hd, orc, g):
+    rng = synth.generator(1110 + g)
+    types = [SLIDING, FULL, SLIDING, FULL]
+    Hkv = 2
+    sink = synth.sink_vector(rng, ("normal", 2.0 ** 0.5, 0.25), g * Hkv)
+    ctx = make_ctx(hd, types, 5, 3000, Hq=g * Hkv, Hkv=Hkv)
+    step = Step(hd, rng, types, 5, g * Hkv, Hkv, [1, 510, 511, 1800, 2999], RING, 3000, sink=sink)
+    step.run(hd, ctx)
+    step.check(orc)
+    ctx.close()
+
+
+def test_aliased_outputs_run_layer_by_layer(hd, orc):
+    """Layers that share one out/lse buffer are not independent: decode_step
+    launches one kernel per layer in order, so the buffer ends with the last
+    layer's result."""
+    rng = synth.generator(1104)
+    types = [SLIDING, FULL, SLIDING, FULL]
+    B, Hq, Hkv = 2, 8, 2
+    ctx = make_ctx(hd, types, B, 1024)
+    step = Step(hd, rng, types, B, Hq, Hkv, [200, 900], RING, 1024)
+    out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+    for io in step.ios:
+        io.out = out.data_ptr()
+        io.lse = lse.data_ptr()
+    n0 = launches(hd, ctx)
+    step.run(hd, ctx)
+    assert launches(hd, ctx) - n0 == len(types)
+    ref = oracle_layer(orc, step.cases[-1], types[-1], RING)
+    assert_out_close(out, ref["out"], "last layer out")
+    assert_lse_close(lse, ref["lse"], "last layer lse")
+    for i, (t, case) in enumerate(zip(types, step.cases)):
+        r = oracle_layer(orc, case, t, RING)
+        assert_bits_equal(step.dev[i][2], r["kcache"], f"layer {i} K cache")
+        assert_bits_equal(step.dev[i][3], r["vcache"], f"layer {i} V cache")
+    ctx.close()
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_fused_and_layer_by_layer_steps_agree(hd, kv):
+    """The batch-16 block at contexts U[512, 32768] with and without step fusion:
+    the same cache bits, outputs within the output tolerance of each other."""
+    import bench
+    dev = torch.device("cuda")
+    runs, counts = [], []
+    for fuse in (True, False):
+        wl = bench.Workload("block4_b16_c512_32768", dev, seed=5, kv=kv)
+        hd.hybrid_decode_set_step_fusion(wl.ctx, fuse)
+        n0 = launches(hd, wl.ctx)
+        wl.step()
+        torch.cuda.synchronize()
+        counts.append(launches(hd, wl.ctx) - n0)
+        assert hd.hybrid_decode_device_errors(wl.ctx) == 0
+        runs.append([(L["out"].float().cpu().double().numpy(), L["lse"].cpu().double().numpy(),
+                      synth.bits(L["kc"]), synth.bits(L["vc"])) for L in wl.layers])
+        wl.ctx.close()
+    assert counts == [1, 4], counts
+    for i, (a, b) in enumerate(zip(*runs)):
+        assert np.array_equal(a[2], b[2]) and np.array_equal(a[3], b[3]), f"layer {i} caches differ"
+        assert_out_close(torch.from_numpy(a[0]), b[0], f"layer {i} out")
+        assert_lse_close(torch.from_numpy(a[1]), b[1], f"layer {i} lse")

@@ -61,8 +61,11 @@ class TokenLayer:
     def device(self, hd):
         dev = torch.device("cuda")
         self.kd, self.vd = self.kc.to(dev), self.vc.to(dev)
-        self.cache = (hd.kv_cache(self.kd, self.vd, self.k_scale.to(dev), self.v_scale.to(dev))
-                      if self.kv == "fp8" else hd.kv_cache(self.kd, self.vd))
+        if self.kv == "fp8":   # the descriptor holds raw pointers: keep the device scales
+            self.scales_dev = (self.k_scale.to(dev), self.v_scale.to(dev))
+            self.cache = hd.kv_cache(self.kd, self.vd, *self.scales_dev)
+        else:
+            self.cache = hd.kv_cache(self.kd, self.vd)
         B, T, Hq, _ = self.q.shape
         self.out = torch.empty(B, T, Hq, D, dtype=torch.bfloat16, device=dev)
         self.lse = torch.empty(B, T, Hq, dtype=torch.float32, device=dev)
