@@ -570,6 +570,8 @@ def layer_kernel_rooflines(wl, peaks) -> dict:
     bracketed by events alone; achieved GB/s over that layer's scored KV bytes."""
     import full_gqa_decode_gb300 as hd
     hd.hybrid_decode_set_step_fusion(wl.ctx, False)
+    for _ in range(2):   # unbracketed: the layer kernels' first launches load their code
+        wl.step()
     out = {}
     for name, mask, kind, nbytes in (("full_layers", hd.HD_PROFILE_FULL | hd.HD_PROFILE_FIRST_ONLY, hd.HD_FULL,
                                       wl.full_layer_bytes),
@@ -658,6 +660,8 @@ def fp8_step(device, args, consumer, layout, bf16_ms) -> dict:
             wl.step()
         grid_ms, grid_n = hd.hybrid_decode_profile(wl.ctx, hd.HD_PROFILE_KIND_STEP)
     hd.hybrid_decode_set_step_fusion(wl.ctx, False)
+    for _ in range(2):   # unbracketed: the layer kernels' first launches load their code
+        wl.step()
     hd.hybrid_decode_set_profiling(wl.ctx, hd.HD_PROFILE_FULL)
     for _ in range(3):
         wl.step()

@@ -336,13 +336,16 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
 // Split of a step grid: one chunk size C (a multiple of kChunkMin keys, up to
 // the cache type's chunk maximum) for every layer, each layer then taking
 // ceil(max_keys / C) chunks per (sequence, kv head).  C minimises an estimate
-// of the grid's time in key-reads per SM, each CTA costing its keys plus
-// kChunkMin for its start and combine: a grid that is resident at once (two
-// CTAs per SM) ends with its most loaded SM, ceil(CTAs / SMs) CTAs of up to C
-// keys; a longer grid takes the total over the SMs plus one CTA of tail.
+// of the grid's time in key-reads per SM, each CTA costing its keys plus a
+// fixed cost for its start and combine of about 256 KiB of streaming (256
+// bf16 or 512 E4M3 keys; fitted to batch-4 131k-context steps, where
+// 2048-key bf16 chunks beat shorter ones): a grid that is resident at once
+// (two CTAs per SM) ends with its most loaded SM, ceil(CTAs / SMs) CTAs of up
+// to C keys; a longer grid takes the total over the SMs plus one CTA of tail.
 int32_t plan_step_chunk(const hd_ctx *ctx, const std::vector<LayerCall> &calls, size_t rows, bool mt) {
     const int64_t Hkv = ctx->cfg.num_kv_heads, sms = ctx->num_sms;
     const int64_t cmax = ctx->kv_type == KV_FP8 ? 2 * kChunkMax : kChunkMax;
+    const int64_t fixed = (256 << 10) / (kHeadDim * kv_elem_bytes(ctx->kv_type) * 2);   // keys
     const int stages = rows > (size_t)kMaxGroup ? kDeepStages : kStages;
     int64_t longest = 1;
     for (const LayerCall &L : calls) longest = std::max<int64_t>(longest, L.max_keys);
@@ -355,11 +358,11 @@ int32_t plan_step_chunk(const hd_ctx *ctx, const std::vector<LayerCall> &calls, 
         for (const LayerCall &L : calls) {
             const int64_t ch = L.max_keys > 0 ? (L.max_keys + C - 1) / C : 1;
             n += L.batch * Hkv * ch;
-            total += (double)L.batch * Hkv * (double)(ch * kChunkMin + L.max_keys);
+            total += (double)L.batch * Hkv * (double)(ch * fixed + L.max_keys);
             fits = fits && combine_fits(rows, ch, mt, stages);
         }
         if (!fits) continue;
-        const double per_cta = (double)(std::min(C, longest) + kChunkMin);
+        const double per_cta = (double)(std::min(C, longest) + fixed);
         const double est = n <= 2 * sms ? (double)((n + sms - 1) / sms) * per_cta : total / sms + per_cta;
         if (best < 0.0 || est <= best) {   // ties: the longer chunk
             best = est;
@@ -416,7 +419,7 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
         e.kmap = *km;
         e.vmap = *vm;
         fill_layer_args(ctx, L, C, (int32_t)ch, part_row, e.a);
-        e.cta_begin = (int32_t)ctas;
+        t.begin[t.num_layers - 1] = (int32_t)ctas;
         part_row += need;
         ctas += (int64_t)L.batch * Hkv * ch;
     }

@@ -23,7 +23,7 @@ cudaError_t launch_layer(const CUtensorMap *km, const CUtensorMap *vm, const Lay
     t.layer[0].kmap = *km;
     t.layer[0].vmap = *vm;
     t.layer[0].a = a;
-    t.layer[0].cta_begin = 0;
+    t.begin[0] = 0;
     t.num_layers = 1;
     const dim3 grid(a.max_chunks, a.num_kv_heads, batch);
     const bool mt = a.total_tokens > 1;

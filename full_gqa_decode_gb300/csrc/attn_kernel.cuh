@@ -782,14 +782,27 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     int layer = 0;
     if constexpr (NL > 1) {
         static_assert(NL <= 32, "one lane per table entry");
-        const bool started = lane < p.num_layers && p.layer[lane].cta_begin <= (int)blockIdx.x;
+        const bool started = lane < p.num_layers && p.begin[lane] <= (int)blockIdx.x;
         layer = 31 - __clz(__ballot_sync(0xffffffffu, started));
     }
     const LayerLaunch &ll = p.layer[layer];
-    const LayerArgs &a = ll.a;
+    // A step table is indexed at run time, so its layer's arguments are read
+    // through a computed address.  The bf16 kernels at two CTAs per SM (the
+    // register-capped ones) copy them to shared memory once instead, which
+    // measured faster there and slower elsewhere (a single layer's are read
+    // from the parameters at fixed offsets).
+    constexpr bool kArgsInSmem = NL > 1 && KV == KV_BF16 && !MT && S * kStage <= kStages * kStageBytes;
+    __shared__ LayerArgs step_args_s;
+    if constexpr (kArgsInSmem) {
+        static_assert(sizeof(LayerArgs) % 4 == 0, "copied as words");
+        for (int i = threadIdx.x; i < (int)(sizeof(LayerArgs) / 4); i += blockDim.x)
+            reinterpret_cast<uint32_t *>(&step_args_s)[i] = reinterpret_cast<const uint32_t *>(&ll.a)[i];
+        __syncthreads();
+    }
+    const LayerArgs &a = kArgsInSmem ? step_args_s : ll.a;
     int chunk, kvh, b;
     if constexpr (NL > 1) {
-        const int local = (int)blockIdx.x - ll.cta_begin;
+        const int local = (int)blockIdx.x - p.begin[layer];
         chunk = local % a.max_chunks;
         kvh = (local / a.max_chunks) % a.num_kv_heads;
         b = local / (a.max_chunks * a.num_kv_heads);

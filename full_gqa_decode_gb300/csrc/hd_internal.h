@@ -129,18 +129,20 @@ struct RopeArgs {
 // Kernel parameters of an attention launch: a table of layers, each with its
 // K and V cache views and arguments.  A single-layer launch (NL = 1) runs a
 // (chunks, kv heads, sequences) grid; a step table (NL = kStepLayers) runs a
-// 1-D grid where layer i owns the CTAs [cta_begin, next layer's cta_begin),
-// ordered (sequence, kv head, chunk) with the chunk fastest.
+// 1-D grid where layer i owns the CTAs [begin[i], begin[i + 1]), ordered
+// (sequence, kv head, chunk) with the chunk fastest.  The range starts sit
+// together at the front of the table, so a CTA finds its layer with one load
+// per lane from one 128-byte line.
 constexpr int kStepLayers = 32;
 struct alignas(64) LayerLaunch {
     CUtensorMap kmap, vmap;
     LayerArgs a;
-    int32_t cta_begin;
 };
 template <int NL>
 struct LaunchTable {
-    LayerLaunch layer[NL];
+    int32_t begin[NL];
     int32_t num_layers;
+    LayerLaunch layer[NL];
 };
 using StepTable = LaunchTable<kStepLayers>;
 static_assert(sizeof(StepTable) <= 32764, "kernel parameters are limited to 32764 bytes");
