@@ -56,15 +56,18 @@ namespace {
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kQScale = kLog2e * 0.0625f;   // log2(e) / sqrt(256)
-constexpr int kConsumerWarps = 4;
-constexpr int kKeysPerWarp = kStageKeys / kConsumerWarps;  // 8 (bf16 stages; E4M3 stages give 16)
-constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr int kConsumerWarps = 4;   // per CTA; 16-row multi-token passes run twice as many
 // bf16 layers run a dedicated producer warp.  E4M3 layers fold the producer
 // into the consumers (the last warp to release a slot refills it): four warps
 // per CTA leave each thread up to 255 registers at two CTAs per SM, which the
 // E4M3 consumer's conversions need (five warps cap it at 168).
 __host__ __device__ constexpr bool own_producer(int kv) { return kv == KV_BF16; }
-__host__ __device__ constexpr int kv_threads(int kv) { return own_producer(kv) ? kThreads : kConsumerWarps * 32; }
+// 16 query rows run one CTA per SM: eight consumer warps (two per row group of
+// eight rows and stage half) keep as many warps per SM as two 8-row CTAs.
+__host__ __device__ constexpr int consumer_warps(int g) { return g > kMaxGroup ? 2 * kConsumerWarps : kConsumerWarps; }
+__host__ __device__ constexpr int layer_threads(int g, int kv) {
+    return (consumer_warps(g) + (own_producer(kv) ? 1 : 0)) * 32;
+}
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
 // Inside the stage ring (free once every stage is consumed): the warp buffers
 // [warps][G][256] + (m, l) and the combine weights start at 0; this chunk's
@@ -491,7 +494,7 @@ struct MmaConsumer {
         const uint32_t pb = pack_bf16(p0, p1);
         // Rows past the key set may hold NaN; 0 * NaN would poison the sum.
         uint32_t vmask = 0xFFFFFFFFu;
-        if (nvalid < kKeysPerWarp)
+        if (nvalid < kWK)
             vmask = (2 * t4 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 1 < nvalid ? 0xFFFF0000u : 0u);
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
@@ -749,17 +752,19 @@ struct Fp8MmaConsumer {
 // G: query rows per kv head -- the GQA group, or with MT (multi-token) the
 // group times a.tokens tokens of the same sequence, row r = token r / (G /
 // a.tokens), head r % (G / a.tokens).  G = 16 (MT only) runs two row groups
-// of 8: warps 0-1 take rows 0-7 and warps 2-3 rows 8-15, each pair splitting
-// every stage's keys, so each warp keeps the 8-row consumer's registers.
+// of 8 with eight consumer warps: warps 0-3 take rows 0-7 and warps 4-7 rows
+// 8-15, each group splitting every stage's keys, so each warp keeps the 8-row
+// consumer's registers.
 // NL: layers in the parameter table (1: one layer, grid (chunks, kv heads,
 // sequences); kStepLayers: a step, 1-D grid over the layers' CTA ranges).
 template <int G, int CONSUMER, int S, int KV, bool MT, int NL>
-__global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kStages * kStageBytes ? 2 : 1)
+__global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <= kStages * kStageBytes ? 2 : 1)
     attn_layer_kernel(const __grid_constant__ LaunchTable<NL> p) {
     constexpr int kStage = kv_stage_bytes(KV);     // bytes of one stage (K + V)
     constexpr int kKeys = kv_stage_keys(KV);       // keys per stage: 32 bf16, 64 E4M3
     constexpr int kBoxes = kv_boxes_per_row(KV);   // 128-byte boxes per K or V row
-    constexpr int kNThreads = kv_threads(KV);
+    constexpr int kNThreads = layer_threads(G, KV);
+    constexpr int CW = consumer_warps(G);          // consumer warps
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -929,7 +934,7 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kConsumerWarps);
+            mbar_init(&empty[s], CW);
             rel_s[s] = 0u;
         }
         fence_mbar_init();
@@ -996,11 +1001,11 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     __syncthreads();
 
     // Row groups: RG groups of CG rows; each group's WPG warps split every stage.
-    constexpr int RG = G > 8 ? G / 8 : 1, CG = G / RG, WPG = kConsumerWarps / RG;
+    constexpr int RG = G > 8 ? G / 8 : 1, CG = G / RG, WPG = CW / RG;
     float *red_o = reinterpret_cast<float *>(smem);             // [warps][CG][256], reuses the stage ring
-    float *red_m = red_o + kConsumerWarps * CG * kHeadDim;
-    float *red_l = red_m + kConsumerWarps * CG;
-    if (own_producer(KV) && warp == kConsumerWarps) {
+    float *red_m = red_o + CW * CG * kHeadDim;
+    float *red_l = red_m + CW * CG;
+    if (own_producer(KV) && warp == CW) {
         if (lane == 0) {  // producer: one lane issues every load of the chunk
             for (int s = 0; s < nst; ++s) {
                 if (droppable(s)) break;
@@ -1050,7 +1055,7 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
                     // then a proxy fence before the async-proxy write).
                     __threadfence_block();
                     const unsigned prev = atomicAdd(&rel_s[slot], 1u);
-                    if (prev % kConsumerWarps == kConsumerWarps - 1 && s + S < nst && !droppable(s + S)) {
+                    if (prev % CW == CW - 1 && s + S < nst && !droppable(s + S)) {
                         __threadfence_block();
                         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                         issue_stage(s + S);
@@ -1072,7 +1077,12 @@ __global__ void __launch_bounds__(kv_threads(KV), S * kv_stage_bytes(KV) <= kSta
     // warp buffers) and, when the sequence has several chunks, written out.
     // Partials: G rows per (sequence, kv head), num_kv_heads * G rows per sequence.
     const size_t pbase = ((size_t)b * a.num_kv_heads * G + kvh * G) * a.max_chunks;
-    float *own_o = reinterpret_cast<float *>(smem + kOwnPartialOffset);   // [G][256]
+    // this chunk's partial sits past the warp buffers
+    constexpr int kRedBytes = (CW * CG * kHeadDim + 2 * CW * CG) * (int)sizeof(float);
+    constexpr int kOwnOff = kRedBytes <= kOwnPartialOffset ? kOwnPartialOffset : (kRedBytes + 1023) / 1024 * 1024;
+    static_assert(kOwnOff + G * (kHeadDim + 2) * (int)sizeof(float) <= S * kStage - kMtNewBytes,
+                  "warp buffers, own partial and the multi-token entries fit the ring");
+    float *own_o = reinterpret_cast<float *>(smem + kOwnOff);   // [G][256]
     float2 *own_ml = reinterpret_cast<float2 *>(own_o + G * kHeadDim);    // [G]
     for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
         const int h = i / kHeadDim, d = i % kHeadDim;
@@ -1304,7 +1314,7 @@ cudaError_t launch_g(const LaunchTable<NL> &p, dim3 grid, bool pdl, cudaStream_t
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(kv_threads(KV));
+    cfg.blockDim = dim3(layer_threads(G, KV));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
