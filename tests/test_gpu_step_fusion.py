@@ -170,3 +170,29 @@ def test_fused_and_layer_by_layer_steps_agree(hd, kv):
         assert np.array_equal(a[2], b[2]) and np.array_equal(a[3], b[3]), f"layer {i} caches differ"
         assert_out_close(torch.from_numpy(a[0]), b[0], f"layer {i} out")
         assert_lse_close(torch.from_numpy(a[1]), b[1], f"layer {i} lse")
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_lost_copy_in_a_step_grid_times_out_and_recovers(hd, orc, kv):
+    """A copy that never arrives inside a step grid: the bounded waits run out
+    (about one second), the grid reports HD_DEVERR_WAIT_TIMEOUT and returns; the
+    same context then runs a correct step."""
+    import time
+    rng = synth.generator(1120)
+    types = [SLIDING, FULL]
+    ctx = make_ctx(hd, types, 2, 1024, kv=kv)
+    bad = Step(hd, rng, types, 2, 8, 2, [300, 900], RING, 1024, kv=kv)
+    hd.hybrid_decode_inject_lost_copy(ctx, 0)   # no stage arrives (chunks may be one stage long)
+    n0 = launches(hd, ctx)
+    t0 = time.time()
+    hd.decode_step(ctx, torch.from_numpy(bad.context).cuda(), bad.ios, 2)
+    flags = hd.hybrid_decode_device_errors(ctx)
+    elapsed = time.time() - t0
+    assert launches(hd, ctx) - n0 == 1
+    assert flags & 8, f"expected a wait timeout, flags {flags:#x}"
+    assert 0.5 < elapsed < 30.0, elapsed
+    hd.hybrid_decode_inject_lost_copy(ctx, -1)
+    good = Step(hd, rng, types, 2, 8, 2, [300, 900], RING, 1024, kv=kv)
+    good.run(hd, ctx)
+    good.check(orc)
+    ctx.close()
