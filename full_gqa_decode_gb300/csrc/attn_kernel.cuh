@@ -492,10 +492,15 @@ struct MmaConsumer {
             }
         }
         const uint32_t pb = pack_bf16(p0, p1);
-        // Rows past the key set may hold NaN; 0 * NaN would poison the sum.
-        uint32_t vmask = 0xFFFFFFFFu;
+        // Rows past the key set may hold NaN; 0 * NaN would poison the sum, so a
+        // tile with fewer than kWK keys masks its V values (full tiles skip it).
         if (nvalid < kWK)
-            vmask = (2 * t4 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 1 < nvalid ? 0xFFFF0000u : 0u);
+            pv(vbase, lrow, lsub, pb, (2 * t4 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 1 < nvalid ? 0xFFFF0000u : 0u));
+        else
+            pv(vbase, lrow, lsub, pb, 0xFFFFFFFFu);
+    }
+
+    __device__ __forceinline__ void pv(uint32_t vbase, int lrow, int lsub, uint32_t pb, uint32_t vmask) {
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
             uint32_t a0, a1, a2, a3;
@@ -689,12 +694,22 @@ struct Fp8MmaConsumer {
         }
         const uint32_t pb0 = movmatrix_trans(pack_f16(p[0], p[1]));   // keys 2*t4, +1 of head gid
         const uint32_t pb1 = movmatrix_trans(pack_f16(p[2], p[3]));   // keys 8 + 2*t4, +1
-        // Rows past the key set may hold NaN codes; 0 * NaN would poison the sum.
-        uint32_t m01 = 0xFFFFFFFFu, m89 = 0xFFFFFFFFu;
+        // Rows past the key set may hold NaN codes; 0 * NaN would poison the sum,
+        // so a tile with fewer than kWK keys masks its V values (full tiles skip it).
         if (nvalid < kWK) {
-            m01 = (2 * t4 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 1 < nvalid ? 0xFFFF0000u : 0u);
-            m89 = (2 * t4 + 8 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 9 < nvalid ? 0xFFFF0000u : 0u);
+            const uint32_t m01 = (2 * t4 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 1 < nvalid ? 0xFFFF0000u : 0u);
+            const uint32_t m89 = (2 * t4 + 8 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 9 < nvalid ? 0xFFFF0000u : 0u);
+            pv(vst, row0, lane, pb0, pb1, m01, m89);
+        } else {
+            pv(vst, row0, lane, pb0, pb1, 0xFFFFFFFFu, 0xFFFFFFFFu);
         }
+    }
+
+    // O^T += V^T P^T over the tile's 16 keys; m01 / m89 mask the V values of keys
+    // past the key set (all ones for a full tile, where the masks fold away).
+    __device__ __forceinline__ void pv(const uint8_t *vst, int row0, int lane, uint32_t pb0, uint32_t pb1,
+                                       uint32_t m01, uint32_t m89) {
+        const int gid = lane >> 2, t4 = lane & 3;
 #pragma unroll
         for (int half = 0; half < 2; ++half) {
             const int chunk = 8 * half + gid;
