@@ -157,11 +157,12 @@ typedef struct {
 /* Pure host check of a configuration (no device use). */
 hd_status hd_validate_config(const hd_config *cfg);
 
-/* Split-K plan used for a layer call (pure host function, no device use):
- * keys per chunk (a power of two from 64 to 2048) and the number of chunks
- * (the grid's key dimension) for `batch` sequences of at most `max_keys`
- * scored cache keys on `num_sms` SMs.  A call on a context uses the same
- * model, bounded by the context's workspace. */
+/* Split-K plan used for a single-layer call (pure host function, no device
+ * use): keys per chunk (a power of two from 64 to 2048) and the number of
+ * chunks (the grid's key dimension) for `batch` sequences of at most
+ * `max_keys` scored cache keys on `num_sms` SMs.  A call on a context uses the
+ * same model, bounded by the context's workspace.  decode_step's step grid
+ * plans one chunk size over all its layers instead. */
 hd_status hd_plan_split(int32_t batch, int32_t num_kv_heads, int32_t max_keys, int32_t num_sms,
                         int32_t *chunk_keys, int32_t *num_chunks);
 
