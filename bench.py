@@ -240,6 +240,13 @@ class Workload:
         self.sink = None if sink is None else sink.to(device)
         ring = layout != synth.LAYOUT_ROLL
         self.layers, self.io, self.io_gated = [], [], []
+        # every layer's q, k, v (and out, lse) are slices of one buffer each, so a
+        # step's inputs move host -> device in one copy (and its outputs back in two)
+        per_q, per_kv = self.B * tokens * self.Hq * D, self.B * tokens * self.Hkv * D
+        nl = len(self.types)
+        self.qkv = torch.empty(nl, per_q + 2 * per_kv, dtype=torch.bfloat16, device=device)
+        self.outs = torch.empty(nl, per_q, dtype=torch.bfloat16, device=device)
+        self.lses = torch.empty(nl, self.B * tokens * self.Hq, dtype=torch.float32, device=device)
         for i, t in enumerate(self.types):
             cap = (synth.WINDOW - 1 if ring else synth.WINDOW) if t == synth.SLIDING else self.max_ctx + tokens
             kc = torch.empty(self.B, self.Hkv, cap, D, dtype=torch.uint8 if fp8 else torch.bfloat16, device=device)
@@ -254,11 +261,13 @@ class Workload:
                 synth.cuda_normal_bf16_(vc, seed * 1000 + 2 * i + 2)
             g = torch.Generator(device=device)
             g.manual_seed(seed * 1000 + 500 + i)
-            q = torch.randn(self.B, *tq, self.Hq, D, generator=g, device=device).to(torch.bfloat16)
-            k = torch.randn(self.B, *tq, self.Hkv, D, generator=g, device=device).to(torch.bfloat16)
-            v = torch.randn(self.B, *tq, self.Hkv, D, generator=g, device=device).to(torch.bfloat16)
-            out = torch.empty(self.B, *tq, self.Hq, D, dtype=torch.bfloat16, device=device)
-            lse = torch.empty(self.B, *tq, self.Hq, dtype=torch.float32, device=device)
+            q = self.qkv[i, :per_q].view(self.B, *tq, self.Hq, D)
+            k = self.qkv[i, per_q:per_q + per_kv].view(self.B, *tq, self.Hkv, D)
+            v = self.qkv[i, per_q + per_kv:].view(self.B, *tq, self.Hkv, D)
+            for x in (q, k, v):
+                x.copy_(torch.randn(x.shape, generator=g, device=device))
+            out = self.outs[i].view(self.B, *tq, self.Hq, D)
+            lse = self.lses[i].view(self.B, *tq, self.Hq)
             cache = hd.kv_cache(kc, vc, ks, vs)
             self.layers.append(dict(q=q, k=k, v=v, kc=kc, vc=vc, out=out, lse=lse, cache=cache,
                                     k_scale=ks, v_scale=vs))
@@ -596,26 +605,22 @@ def layer_kernel_rooflines(wl, peaks) -> dict:
 
 def e2e_measure(wl, args, world, device) -> dict:
     """Same metric through the public API with pinned host buffers: every step copies
-    that step's q/k/v (all layers) and contexts host->device and reads out/lse back."""
+    that step's q/k/v (all layers, one buffer) and the contexts host->device, runs
+    the step, and reads out and lse (all layers) back."""
     import torch
-    host_in = [(l["q"].cpu().pin_memory(), l["k"].cpu().pin_memory(), l["v"].cpu().pin_memory())
-               for l in wl.layers]
+    host_in = wl.qkv.cpu().pin_memory()
     host_ctx = torch.from_numpy(wl.context).pin_memory()
-    host_out = [(torch.empty_like(l["out"], device="cpu").pin_memory(),
-                 torch.empty_like(l["lse"], device="cpu").pin_memory()) for l in wl.layers]
-    h2d = sum(t.numel() * t.element_size() for trip in host_in for t in trip) + host_ctx.numel() * 4
-    d2h = sum(t.numel() * t.element_size() for pair in host_out for t in pair)
+    host_out = torch.empty_like(wl.outs, device="cpu").pin_memory()
+    host_lse = torch.empty_like(wl.lses, device="cpu").pin_memory()
+    h2d = host_in.numel() * host_in.element_size() + host_ctx.numel() * 4
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
 
     def run():
         wl.context_d.copy_(host_ctx, non_blocking=True)
-        for (q, k, v), l in zip(host_in, wl.layers):
-            l["q"].copy_(q, non_blocking=True)
-            l["k"].copy_(k, non_blocking=True)
-            l["v"].copy_(v, non_blocking=True)
+        wl.qkv.copy_(host_in, non_blocking=True)
         wl.step()
-        for (o, s), l in zip(host_out, wl.layers):
-            o.copy_(l["out"], non_blocking=True)
-            s.copy_(l["lse"], non_blocking=True)
+        host_out.copy_(wl.outs, non_blocking=True)
+        host_lse.copy_(wl.lses, non_blocking=True)
     ms = time_steps(run, args.steps, args.warmup, world, device)
     ms_max, total = reduce_timing(ms, wl.bytes, world, device)
     return {"value": round(total / (ms_max * 1e-3) / 1e9, 1), "unit": "GB/s",
