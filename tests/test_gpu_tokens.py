@@ -74,12 +74,14 @@ class TokenLayer:
         return hd.layer_io(q, k, v, self.cache, sink, self.out, self.lse, gate=gate)
 
 
-def run_case(hd, orc, types, T, Hq, Hkv, context, kv="bf16", seed=0, with_gate=True, max_context=None):
+def run_case(hd, orc, types, T, Hq, Hkv, context, kv="bf16", seed=0, with_gate=True, max_context=None,
+             fuse=True):
     rng = synth.generator(seed)
     B = len(context)
     context = np.asarray(context, np.int32)
     max_context = max_context or int(context.max()) + T
     ctx = _ctx(hd, types, Hq, Hkv, B, max_context, kv)
+    hd.hybrid_decode_set_step_fusion(ctx, fuse)
     sink = synth.sink_vector(rng, ("normal", 1.0, 0.0), Hq)
     layers = [TokenLayer(rng, t, B, T, Hq, Hkv, 511 if t == SLIDING else max_context + 1, context, kv, sink,
                          with_gate) for t in types]
@@ -112,6 +114,13 @@ def test_tokens_ring_and_full(hd, orc, T, g):
 def test_tokens_fp8(hd, orc, T, g):
     Hkv = 2
     run_case(hd, orc, [SLIDING, FULL], T, g * Hkv, Hkv, RING_FULL_CONTEXTS, kv="fp8", seed=800 + 10 * T + g)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+@pytest.mark.parametrize("T", [3, 4])
+def test_tokens_kernel_per_layer(hd, orc, kv, T):
+    """Step fusion off: each layer's passes run as their own kernels."""
+    run_case(hd, orc, [SLIDING, FULL], T, 8, 2, RING_FULL_CONTEXTS, kv=kv, seed=950 + T, fuse=False)
 
 
 def test_tokens_one_equals_decode_step(hd, orc):
