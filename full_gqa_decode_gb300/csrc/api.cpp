@@ -248,6 +248,7 @@ struct LayerCall {
     void *out;
     float *lse;
     bool pdl;               // previous grid in the stream is this step's previous layer kernel
+    bool one_chunk = false; // step grids: the layer needs a single chunk per sequence
     int tokens = 1, token0 = 0, total_tokens = 1;   // multi-token decode: this pass's tokens
 };
 
@@ -356,7 +357,8 @@ int32_t plan_step_chunk(const hd_ctx *ctx, const std::vector<LayerCall> &calls, 
         double total = 0.0;
         bool fits = true;
         for (const LayerCall &L : calls) {
-            const int64_t ch = L.max_keys > 0 ? (L.max_keys + C - 1) / C : 1;
+            const int64_t Cl = L.one_chunk ? std::max<int64_t>(C, L.max_keys) : C;
+            const int64_t ch = L.max_keys > 0 ? (L.max_keys + Cl - 1) / Cl : 1;
             n += L.batch * Hkv * ch;
             total += (double)L.batch * Hkv * (double)(ch * fixed + L.max_keys);
             fits = fits && combine_fits(rows, ch, mt, stages);
@@ -403,7 +405,8 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
         return HD_OK;
     };
     for (const LayerCall &L : calls) {
-        const int64_t ch = L.max_keys > 0 ? (L.max_keys + C - 1) / C : 1;
+        const int64_t Cl = L.one_chunk ? std::max<int64_t>(C, L.max_keys) : C;
+        const int64_t ch = L.max_keys > 0 ? (L.max_keys + Cl - 1) / Cl : 1;
         const int64_t need = ch > 1 ? (int64_t)L.batch * Hkv * (int64_t)rows * ch : 0;
         hd_status st = HD_OK;
         if (need > ctx->part_rows) {   // too large for a shared grid: its own plan and launch
@@ -418,7 +421,7 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
         LayerLaunch &e = t.layer[t.num_layers++];
         e.kmap = *km;
         e.vmap = *vm;
-        fill_layer_args(ctx, L, C, (int32_t)ch, part_row, e.a);
+        fill_layer_args(ctx, L, (int32_t)Cl, (int32_t)ch, part_row, e.a);
         t.begin[t.num_layers - 1] = (int32_t)ctas;
         part_row += need;
         ctas += (int64_t)L.batch * Hkv * ch;
@@ -760,14 +763,20 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ctx->profile_seen[0] = ctx->profile_seen[1] = false;
     // Every layer is checked before anything is launched.
-    std::vector<LayerCall> &calls = ctx->step_calls;
-    calls.assign(ctx->cfg.num_layers, LayerCall{});
     for (int i = 0; i < ctx->cfg.num_layers; ++i) {
         const hd_layer_io &io = layers[i];
         hd_status st = check_attention(ctx, i, batch, context, io.cache, io.out, io.lse);
         if (st != HD_OK) return st;
         if (!io.q || !io.k || !io.v || !aligned16(io.q) || !aligned16(io.k) || !aligned16(io.v))
             return HD_ERR_INVALID_ARG;
+    }
+    const bool fused =
+        ctx->fuse_step && ctx->consumer == CONSUMER_MMA && layers_independent(ctx, batch, num_tokens, layers);
+    std::vector<LayerCall> &calls = ctx->step_calls;
+    calls.assign(ctx->cfg.num_layers, LayerCall{});
+    for (int i = 0; i < ctx->cfg.num_layers; ++i) {
+        const hd_layer_io &io = layers[i];
+        hd_status st = HD_OK;
         const bool sliding = ctx->layer_types[i] == HD_SLIDING;
         const bool roll = sliding && ctx->sliding_layout == HD_LAYOUT_ROLL;
         LayerCall &L = calls[i];
@@ -795,6 +804,12 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
             L.key_set = KEYS_RING;
             L.new_kind = NEW_ROTATE;
             L.commit = COMMIT_RING;
+        } else if (fused) {   // the grid reads the window, then shifts it and stores the new entry
+            L.max_keys = ctx->cfg.sliding_window - 1;
+            L.key_set = KEYS_ROLL_SHIFT;
+            L.new_kind = NEW_ROTATE;
+            L.commit = COMMIT_ROLL;
+            L.one_chunk = true;
         } else {
             L.max_keys = ctx->cfg.sliding_window;
             L.key_set = KEYS_ROLL;
@@ -802,7 +817,8 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
             L.commit = COMMIT_NONE;
         }
     }
-    // Roll layouts shift their windows (and append) before any attention reads them.
+    // Layer kernels of a roll layout: the windows shift (and append) before any
+    // attention reads them.
     for (const LayerCall &L : calls) {
         if (L.key_set != KEYS_ROLL) continue;
         RopeArgs r{};
@@ -829,7 +845,7 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
         ++ctx->launches;
     }
     const int tmax = std::min(kMaxTokens, kMaxRows / ctx->group);
-    if (ctx->fuse_step && ctx->consumer == CONSUMER_MMA && layers_independent(ctx, batch, num_tokens, layers)) {
+    if (fused) {
         // Step grids, pass by pass: a pass commits its entries, and the next pass's
         // grid starts after it in full stream order.
         for (int t0 = 0; t0 < num_tokens;) {

@@ -271,6 +271,7 @@ __device__ __forceinline__ int cached_keys(const LayerArgs &a, int c, int *bit) 
     switch (a.key_set) {
     case KEYS_RING: n = min(c, a.capacity); break;
     case KEYS_ROLL: n = min(c + 1, a.window); break;
+    case KEYS_ROLL_SHIFT: n = min(c, a.window - 1); break;
     case KEYS_FULL_CACHED: n = c + 1; break;
     default: n = c; break;  // KEYS_FULL_PREV
     }
@@ -279,6 +280,10 @@ __device__ __forceinline__ int cached_keys(const LayerArgs &a, int c, int *bit) 
         return -1;
     }
     if ((n + a.chunk_keys - 1) / a.chunk_keys > a.max_chunks) { *bit = HD_DEVERR_CONTEXT_PLAN; return -1; }
+    if (a.key_set == KEYS_ROLL_SHIFT && (n > a.chunk_keys || a.window > a.capacity)) {   // one chunk shifts the window
+        *bit = HD_DEVERR_CONTEXT_PLAN;
+        return -1;
+    }
     return n;
 }
 
@@ -868,6 +873,8 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     const int start = chunk * a.chunk_keys;
     const int end = min(start + a.chunk_keys, n);
     const int nst = end > start ? (end - start + kKeys - 1) / kKeys : 0;
+    // A full rolled window read before its shift: key i is cache row i + 1.
+    const int roff = (a.key_set == KEYS_ROLL_SHIFT && c >= a.window) ? 1 : 0;
     // New entries of the ntok tokens: values as scored (knew_t), V values (or
     // V codes' values for E4M3, vnew_t), codes, and per-row new-entry weights.
     uint8_t *mt_base = smem + S * kStage - kMtNewBytes;
@@ -935,7 +942,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
         const int slot = s % S;
         uint8_t *st = smem + slot * kStage;
         mbar_arrive_expect_tx(&full[slot], kStage);
-        const int row = start + s * kKeys;
+        const int row = roff + start + s * kKeys;
 #pragma unroll
         for (int j = 0; j < kBoxes; ++j)
             tma_load_4d(st + j * kv_box_bytes(KV), &ll.kmap, &full[slot], j * kv_box_cols(KV), row, kvh, b);
@@ -1059,6 +1066,29 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
                 const int nvalid = min(kCallKeys, end - (start + s * kKeys + row0));
                 if (nvalid > 0)
                     cons.consume(kst, kst + kBoxes * kv_box_bytes(KV), row0, nvalid, lane, start + s * kKeys + row0);
+            }
+            if constexpr (NL > 1 && !MT) {
+                // Full rolled window: this warp's rows of the stage (cache rows key + 1)
+                // move down to rows key, before the slot is released.  Every row written
+                // was loaded by this or an earlier stage; later stages load higher rows.
+                // (Step grids are never launched as programmatic dependents, so these
+                // writes need no dependency wait.)
+                if (roff) {
+                    const int key0 = start + s * kKeys + kpart * kSpan;
+                    const int nrows = min(kSpan, end - key0);
+                    constexpr int kChunks = kHeadDim * kv_elem_bytes(KV) / 16;   // 16-byte chunks per row
+                    const size_t seq = ((size_t)b * a.seq_stride + (size_t)kvh * a.capacity * kHeadDim) *
+                                       kv_elem_bytes(KV);
+                    for (int i = lane; i < 2 * nrows * kChunks; i += 32) {
+                        const int v = i >= nrows * kChunks, rem = i - v * nrows * kChunks;
+                        const int r = rem / kChunks, ch = rem % kChunks;
+                        const uint4 x = *reinterpret_cast<const uint4 *>(
+                            kst + v * kBoxes * kv_box_bytes(KV) + tile_offset<KV>(kpart * kSpan + r, ch));
+                        uint8_t *dst = static_cast<uint8_t *>(v ? a.cache_v : a.cache_k) + seq +
+                                       (size_t)(key0 + r) * kHeadDim * kv_elem_bytes(KV) + 16 * ch;
+                        *reinterpret_cast<uint4 *>(dst) = x;
+                    }
+                }
             }
             __syncwarp();  // orders every lane's reads of the slot before lane 0's release
             if (lane == 0) {
@@ -1304,7 +1334,9 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     if (has_new && a.commit != COMMIT_NONE) {
         for (int idx = threadIdx.x; idx < ntok * kHeadDim; idx += blockDim.x) {
             const int t = idx / kHeadDim, d = idx % kHeadDim;
-            const int slot = a.commit == COMMIT_RING ? (c + t) % a.capacity : c + t;
+            const int slot = a.commit == COMMIT_RING   ? (c + t) % a.capacity
+                             : a.commit == COMMIT_ROLL ? min(c, a.window - 1)
+                                                       : c + t;
             const size_t o = (size_t)b * a.seq_stride + ((size_t)kvh * a.capacity + slot) * kHeadDim + d;
             if (KV == KV_FP8) {
                 static_cast<uint8_t *>(a.cache_k)[o] = code_t[t * kHeadDim + d];

@@ -57,7 +57,11 @@ enum KeySet : int32_t {
     KEYS_RING = 0,         // ring slots [0, min(c, capacity)); the new entry is scored apart
     KEYS_ROLL = 1,         // rolled window [0, min(c + 1, window)), the new entry already in it
     KEYS_FULL_CACHED = 2,  // positions [0, c]: the new entry was appended at index c
-    KEYS_FULL_PREV = 3     // positions [0, c): the new entry is scored apart and appended
+    KEYS_FULL_PREV = 3,    // positions [0, c): the new entry is scored apart and appended
+    KEYS_ROLL_SHIFT = 4    // rolled window before this step's shift: rows [0, c) while it is not
+                           // full, else rows [1, window) (row 0 leaves the window); the new entry
+                           // is scored apart, the kernel shifts the rows it read down by one and
+                           // stores the new entry at row min(c, window - 1); one chunk per sequence
 };
 // Where the new entry comes from when it is scored apart from the cache.
 enum NewEntry : int32_t {
@@ -66,7 +70,7 @@ enum NewEntry : int32_t {
     NEW_STAGED = 2    // already rotated and rounded (ring staging row, in the cache's type)
 };
 // Where the new entry is stored once every chunk has read the cache.
-enum Commit : int32_t { COMMIT_NONE = 0, COMMIT_APPEND = 1, COMMIT_RING = 2 };
+enum Commit : int32_t { COMMIT_NONE = 0, COMMIT_APPEND = 1, COMMIT_RING = 2, COMMIT_ROLL = 3 };
 enum Consumer : int32_t { CONSUMER_FMA = 0, CONSUMER_MMA = 1 };
 
 // One attention layer: one CTA per (chunk, kv head, sequence); the last CTA of

@@ -79,18 +79,70 @@ def test_batch1_28_layer_step_is_one_grid(hd, orc, kv):
     ctx.close()
 
 
+@pytest.mark.parametrize("fuse", [True, False])
 @pytest.mark.parametrize("layout", [RING, ROLL])
-def test_step_grid_launch_counts_and_parity(hd, orc, layout):
-    """Ring: one grid for the 28 layers; roll: the 21 window shifts, then one grid."""
+def test_step_grid_launch_counts_and_parity(hd, orc, layout, fuse):
+    """One grid for the 28 layers, roll windows included (the grid shifts them
+    after reading); with fusion off, one kernel per layer plus, for a roll
+    layout, the 21 window-shift kernels."""
     rng = synth.generator(1102)
     types = synth.SPARK_LAYER_TYPES
-    ctx = make_ctx(hd, types, 3, 2048, layout=layout)
+    ctx = make_ctx(hd, types, 4, 2048, layout=layout)
+    hd.hybrid_decode_set_step_fusion(ctx, fuse)
     sink = synth.sink_vector(rng, ("normal", 1.0, 0.0), 8)
-    step = Step(hd, rng, types, 3, 8, 2, [0, 700, 2047], layout, 2048, sink=sink)
+    step = Step(hd, rng, types, 4, 8, 2, [0, 511, 700, 2047], layout, 2048, sink=sink)
     n0 = launches(hd, ctx)
     step.run(hd, ctx)
-    assert launches(hd, ctx) - n0 == (1 if layout == RING else 1 + types.count(SLIDING))
+    expect = 1 if fuse else len(types) + (types.count(SLIDING) if layout == ROLL else 0)
+    assert launches(hd, ctx) - n0 == expect
     step.check(orc)
+    ctx.close()
+
+
+@pytest.mark.parametrize("kv", ["bf16", "fp8"])
+def test_rolled_windows_shift_inside_the_grid_across_steps(hd, orc, kv):
+    """Consecutive step grids over roll-layout layers from contexts that fill the
+    512-row window: every step's outputs and the final windows match the oracle
+    (the grid reads rows 1..511 of a full window, moves them down one row and
+    stores the new entry at row 511)."""
+    rng = synth.generator(1130)
+    types = [SLIDING, FULL, SLIDING]
+    B, Hq, Hkv, steps = 3, 8, 2, 6
+    ctx = make_ctx(hd, types, B, 1200, layout=ROLL, kv=kv)
+    start = np.array([508, 1, 900], np.int32)
+    cases = [LayerCase(rng, B, Hq, Hkv, 512 if t == SLIDING else 1201, start, kv=kv) for t in types]
+    host = [[synth.bits(c.kc), synth.bits(c.vc)] for c in cases]
+    dev = [(c.kc.cuda(), c.vc.cuda()) for c in cases]
+    for s_ in range(steps):
+        context = start + s_
+        ios, keep, refs = [], [], []
+        for i, t in enumerate(types):
+            q = synth.normal_bf16(rng, (B, Hq, D))
+            k = synth.normal_bf16(rng, (B, Hkv, D))
+            v = synth.normal_bf16(rng, (B, Hkv, D))
+            rot, theta = synth.ROPE[t]
+            c = cases[i]
+            refs.append(orc.decode_layer(layer_type=t, layout=ROLL if t == SLIDING else 0, window=synth.WINDOW,
+                                         rotary_dim=rot, rope_theta=theta, context=context, q=synth.bits(q),
+                                         k=synth.bits(k), v=synth.bits(v), kcache=host[i][0], vcache=host[i][1],
+                                         k_scale=None if c.k_scale is None else c.k_scale.numpy(),
+                                         v_scale=None if c.v_scale is None else c.v_scale.numpy()))
+            out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+            lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+            kk = (q.cuda(), k.cuda(), v.cuda(), out, lse)
+            keep.append(kk)
+            ios.append(hd.layer_io(kk[0], kk[1], kk[2], c.cache(hd, dev[i][0], dev[i][1], "cuda"), None, out, lse))
+        n0 = launches(hd, ctx)
+        hd.decode_step(ctx, torch.from_numpy(context).cuda(), ios, B)
+        torch.cuda.synchronize()
+        assert launches(hd, ctx) - n0 == 1
+        assert hd.hybrid_decode_device_errors(ctx) == 0
+        for i in range(len(types)):
+            assert_out_close(keep[i][3], refs[i]["out"], f"step {s_} layer {i} out")
+            assert_lse_close(keep[i][4], refs[i]["lse"], f"step {s_} layer {i} lse")
+    for i in range(len(types)):
+        assert_bits_equal(dev[i][0], host[i][0], f"layer {i} K cache")
+        assert_bits_equal(dev[i][1], host[i][1], f"layer {i} V cache")
     ctx.close()
 
 
