@@ -41,7 +41,8 @@
  * partials, the ring staging rows).  No call after init allocates.  Every call
  * taking a `stream` (a cudaStream_t; NULL = legacy default stream) is
  * asynchronous on that stream.  Calls that use one hd_ctx must be ordered on
- * one stream (the workspace is shared).
+ * one stream (the workspace is shared) and made from one host thread at a
+ * time (the context keeps host-side launch state).
  *
  * Errors: every call returns an hd_status and nothing throws or aborts across
  * the ABI.  Arguments that can be checked on the host are checked before any
