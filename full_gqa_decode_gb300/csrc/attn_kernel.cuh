@@ -32,13 +32,16 @@
 // whole decode step, a table of up to kStepLayers layers in its parameters
 // (a 1-D grid, each layer's CTAs a contiguous range): the layers of a step are
 // independent, so one grid streams all their caches with no drain between layers.
+// In a step grid a roll-layout layer reads its window before this step's
+// shift and writes each row it read one row lower before releasing its stage
+// (spark_export.py roll branch: drop the oldest entry, append the new one).
 //
 // Each CTA writes an unnormalised partial (o, m, l) per query row, then takes
 // a ticket on a per-(sequence, kv head) counter.  The CTA that draws the last
 // ticket -- every other chunk of that (sequence, kv head) has finished reading
 // -- merges all partials and the new entries, writes out/lse, stores the new
-// K/V entries (ring slot or append) and resets the counter.  Nothing waits on
-// another CTA.
+// K/V entries (ring slot, append, or the rolled window's last row) and resets
+// the counter.  Nothing waits on another CTA.
 //
 // This header holds the kernel and its launch templates; the translation units
 // attn_decode.cu, attn_decode_fp8.cu, attn_step.cu and attn_step_fp8.cu each
