@@ -248,3 +248,49 @@ def test_lost_copy_in_a_step_grid_times_out_and_recovers(hd, orc, kv):
     good.run(hd, ctx)
     good.check(orc)
     ctx.close()
+
+
+@pytest.mark.parametrize("layout", [RING, ROLL])
+def test_bad_contexts_in_a_step_grid_are_flagged_and_the_rest_served(hd, orc, layout):
+    """Negative contexts and contexts past max_context inside one step grid: the
+    device flags them, poisons those sequences' out/lse with NaN and leaves their
+    caches alone; every other sequence of every layer is served correctly."""
+    rng = synth.generator(1140)
+    types = [SLIDING, FULL]
+    B, Hq, Hkv = 4, 8, 2
+    context = np.array([10, 150, -3, 60], np.int32)   # max_context 100
+    ctx = make_ctx(hd, types, B, 100, layout=layout)
+    cases = []
+    for t in types:
+        cap = (511 if layout == RING else 512) if t == SLIDING else 101
+        c = LayerCase(rng, B, Hq, Hkv, cap, np.clip(context, 0, 100))
+        c.context = context
+        cases.append(c)
+    ios, keep = [], []
+    for c in cases:
+        kk = (c.q.cuda(), c.k.cuda(), c.v.cuda(), c.kc.cuda(), c.vc.cuda(),
+              torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda"),
+              torch.empty(B, Hq, dtype=torch.float32, device="cuda"))
+        keep.append(kk)
+        ios.append(hd.layer_io(kk[0], kk[1], kk[2], hd.kv_cache(kk[3], kk[4]), None, kk[5], kk[6]))
+    n0 = launches(hd, ctx)
+    hd.decode_step(ctx, torch.from_numpy(context).cuda(), ios, B)
+    torch.cuda.synchronize()
+    assert launches(hd, ctx) - n0 == 1
+    flags = hd.hybrid_decode_device_errors(ctx)
+    assert flags & 1 and flags & 4, f"flags {flags:#x}"
+    good, bad = [0, 3], [1, 2]
+    for i, (t, c) in enumerate(zip(types, cases)):
+        out, lse, kd, vd = keep[i][5], keep[i][6], keep[i][3], keep[i][4]
+        assert torch.isnan(out[bad].float()).all() and torch.isnan(lse[bad]).all(), f"layer {i}"
+        kc0, vc0 = synth.bits(c.kc), synth.bits(c.vc)
+        assert np.array_equal(synth.bits(kd)[bad], kc0[bad]) and np.array_equal(synth.bits(vd)[bad], vc0[bad])
+        sub = LayerCase(rng, 2, Hq, Hkv, c.kc.shape[2], context[good])
+        sub.q, sub.k, sub.v = c.q[good], c.k[good], c.v[good]
+        sub.kc, sub.vc = c.kc[good].contiguous(), c.vc[good].contiguous()
+        ref = oracle_layer(orc, sub, t, layout)
+        assert_out_close(out[good], ref["out"], f"layer {i} out")
+        assert_lse_close(lse[good], ref["lse"], f"layer {i} lse")
+        assert_bits_equal(kd[good], ref["kcache"], f"layer {i} K cache")
+        assert_bits_equal(vd[good], ref["vcache"], f"layer {i} V cache")
+    ctx.close()
