@@ -182,6 +182,12 @@ hd_status check_cache(const hd_ctx *ctx, const hd_kv_cache &c) {
     return HD_OK;
 }
 
+// The context's workspace and tensor maps live on the device it was created on.
+hd_status check_device(const hd_ctx *ctx) {
+    int dev = -1;
+    return cudaGetDevice(&dev) == cudaSuccess && dev == ctx->device ? HD_OK : HD_ERR_STATE;
+}
+
 hd_status check_call(const hd_ctx *ctx, int layer, int batch, const int32_t *context) {
     if (!ctx) return HD_ERR_INVALID_ARG;
     if (layer < 0 || layer >= ctx->cfg.num_layers) return HD_ERR_INVALID_ARG;
@@ -640,7 +646,7 @@ hd_status rope_append_kv(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_
                          const void *q, const void *k, const void *v, float *q_rot,
                          hd_kv_cache cache, void *stream) {
     hd_status st = check_call(ctx, layer, batch, context);
-    if (st != HD_OK) return st;
+    if (st != HD_OK || (st = check_device(ctx)) != HD_OK) return st;
     if (!q || !k || !v || !q_rot || !aligned16(q_rot)) return HD_ERR_INVALID_ARG;
     if ((st = check_cache(ctx, cache)) != HD_OK) return st;
     const bool sliding = ctx->layer_types[layer] == HD_SLIDING;
@@ -691,7 +697,7 @@ hd_status decode_attn_sliding(hd_ctx *ctx, int32_t layer, int32_t batch, const i
                               const float *q_rot, hd_kv_cache cache, const float *sink, const float *gate,
                               void *out, float *lse, void *stream) {
     hd_status st = check_attention(ctx, layer, batch, context, cache, out, lse);
-    if (st != HD_OK) return st;
+    if (st != HD_OK || (st = check_device(ctx)) != HD_OK) return st;
     if (ctx->layer_types[layer] != HD_SLIDING) return HD_ERR_STATE;
     if (!q_rot || !aligned16(q_rot)) return HD_ERR_INVALID_ARG;
     const bool roll = ctx->sliding_layout == HD_LAYOUT_ROLL;
@@ -719,7 +725,7 @@ hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int3
                            int32_t max_context_hint, const float *q_rot, hd_kv_cache cache,
                            const float *sink, const float *gate, void *out, float *lse, void *stream) {
     hd_status st = check_attention(ctx, layer, batch, context, cache, out, lse);
-    if (st != HD_OK) return st;
+    if (st != HD_OK || (st = check_device(ctx)) != HD_OK) return st;
     if (ctx->layer_types[layer] != HD_FULL) return HD_ERR_STATE;
     if (!q_rot || !aligned16(q_rot)) return HD_ERR_INVALID_ARG;
     int hint = 0;
@@ -757,6 +763,7 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
 hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, const int32_t *context,
                              int32_t max_context_hint, const hd_layer_io *layers, void *stream) {
     if (!ctx || !layers || num_tokens < 1 || num_tokens > kMaxTokens) return HD_ERR_INVALID_ARG;
+    if (check_device(ctx) != HD_OK) return HD_ERR_STATE;
     const bool any_sliding = std::count(ctx->layer_types.begin(), ctx->layer_types.end(), (int)HD_SLIDING) > 0;
     if (num_tokens > 1 && ((any_sliding && ctx->sliding_layout == HD_LAYOUT_ROLL) || ctx->consumer != CONSUMER_MMA))
         return HD_ERR_UNSUPPORTED;

@@ -1354,13 +1354,14 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
 
 template <int G, int CONSUMER, int S, int KV, bool MT, int NL>
 cudaError_t launch_g(const LaunchTable<NL> &p, dim3 grid, bool pdl, cudaStream_t s) {
-    static bool configured = false;
+    static std::atomic<uint64_t> configured{0};   // devices whose attribute is set
     const size_t smem = layer_smem_bytes(G, S * kv_stage_bytes(KV) / kStageBytes);
-    if (!configured) {
+    int device = -1;
+    if (!done_on_device(configured, &device)) {
         cudaError_t e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER, S, KV, MT, NL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        configured = true;
+        mark_done_on_device(configured, device);
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;

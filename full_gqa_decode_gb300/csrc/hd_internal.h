@@ -6,12 +6,24 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <atomic>
 #include <cstdint>
 #include <type_traits>
 
 #include "hybrid_decode.h"
 
 namespace hd {
+
+// Per-device one-time setup (kernel attributes are set per device): true when
+// `done` already has the current device's bit; otherwise the caller does the
+// setup and then calls mark_done_on_device.  Devices past 63 always redo it.
+inline bool done_on_device(const std::atomic<uint64_t> &done, int *device) {
+    if (cudaGetDevice(device) != cudaSuccess) *device = -1;
+    return *device >= 0 && *device < 64 && (done.load(std::memory_order_acquire) >> *device & 1u);
+}
+inline void mark_done_on_device(std::atomic<uint64_t> &done, int device) {
+    if (device >= 0 && device < 64) done.fetch_or(1ull << device, std::memory_order_release);
+}
 
 constexpr int kHeadDim = 256;     // head_dim this build implements
 constexpr int kMaxGroup = 8;      // query heads per kv head

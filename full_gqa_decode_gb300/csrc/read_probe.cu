@@ -98,12 +98,13 @@ extern "C" hd_status hybrid_decode_read_probe(const void *buffer, int64_t bytes,
     const int64_t stages = bytes / kProbeStage / ctas;
     if (stages < 1) return HD_ERR_INVALID_ARG;
     const size_t smem = 128 + kProbeStages * kProbeStage + 2 * kProbeStages * sizeof(uint64_t);
-    static bool configured = false;
-    if (!configured) {
+    static std::atomic<uint64_t> configured{0};   // devices whose attribute is set
+    int device = -1;
+    if (!hd::done_on_device(configured, &device)) {
         if (cudaFuncSetAttribute(read_probe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
             cudaSuccess)
             return HD_ERR_CUDA;
-        configured = true;
+        hd::mark_done_on_device(configured, device);
     }
     int32_t *flag = nullptr;
     if (cudaGetSymbolAddress(reinterpret_cast<void **>(&flag), g_probe_timeout) != cudaSuccess) return HD_ERR_CUDA;
