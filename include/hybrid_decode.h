@@ -76,8 +76,8 @@ typedef enum {
     HD_ERR_UNSUPPORTED = 2,  /* a shape this build does not implement (head_dim != 256, group > 8) */
     HD_ERR_CAPACITY = 3,     /* batch > max_batch, cache capacity too small, context hint too large */
     HD_ERR_CUDA = 4,         /* a CUDA runtime/driver call or a launch failed */
-    HD_ERR_STATE = 5         /* wrong layer type for the call, no device available, or  
-                              * the current device is not the context's device        */
+    HD_ERR_STATE = 5         /* wrong layer type for the call, no device available, or
+                              * the current device is not the context's device */
 } hd_status;
 
 typedef enum { HD_SLIDING = 0, HD_FULL = 1 } hd_layer_type;
