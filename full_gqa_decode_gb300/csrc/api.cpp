@@ -414,13 +414,16 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
         const int64_t Cl = L.one_chunk ? std::max<int64_t>(C, L.max_keys) : C;
         const int64_t ch = L.max_keys > 0 ? (L.max_keys + Cl - 1) / Cl : 1;
         const int64_t need = ch > 1 ? (int64_t)L.batch * Hkv * (int64_t)rows * ch : 0;
+        const int64_t layer_ctas = (int64_t)L.batch * Hkv * ch;
         hd_status st = HD_OK;
-        if (need > ctx->part_rows) {   // too large for a shared grid: its own plan and launch
+        // Too large for a shared grid (its partials, its combine's shared memory at
+        // this chunk count, or its CTA count): its own plan and launch, in stream order.
+        if (need > ctx->part_rows || layer_ctas > INT_MAX ||
+            !combine_fits(rows, ch, mt, rows > (size_t)kMaxGroup ? kDeepStages : kStages)) {
             if ((st = flush()) != HD_OK || (st = launch_layer_call(ctx, L, stream)) != HD_OK) return st;
             continue;
         }
-        if (t.num_layers == kStepLayers || part_row + need > ctx->part_rows ||
-            ctas + (int64_t)L.batch * Hkv * ch > INT_MAX)
+        if (t.num_layers == kStepLayers || part_row + need > ctx->part_rows || ctas + layer_ctas > INT_MAX)
             if ((st = flush()) != HD_OK) return st;
         const CUtensorMap *km = nullptr, *vm = nullptr;
         if ((st = maps_for(ctx, L.layer, L.cache, L.batch, &km, &vm)) != HD_OK) return st;
@@ -430,7 +433,7 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
         fill_layer_args(ctx, L, (int32_t)Cl, (int32_t)ch, part_row, e.a);
         t.begin[t.num_layers - 1] = (int32_t)ctas;
         part_row += need;
-        ctas += (int64_t)L.batch * Hkv * ch;
+        ctas += layer_ctas;
     }
     return flush();
 }
