@@ -420,6 +420,7 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
         // this chunk count, or its CTA count): its own plan and launch, in stream order.
         if (need > ctx->part_rows || layer_ctas > INT_MAX ||
             !combine_fits(rows, ch, mt, rows > (size_t)kMaxGroup ? kDeepStages : kStages)) {
+            if (L.key_set == KEYS_ROLL_SHIFT) return HD_ERR_UNSUPPORTED;   // only step grids shift in place
             if ((st = flush()) != HD_OK || (st = launch_layer_call(ctx, L, stream)) != HD_OK) return st;
             continue;
         }
