@@ -48,10 +48,13 @@ def _check_against_oracle(hd, orc, wl, snap, samples, layers=None):
         L = wl.layers[i]
         for b in samples:
             s = snap[i][b]
+            scales = {}
+            if wl.kv == "fp8":
+                scales = dict(k_scale=L["k_scale"].cpu().numpy(), v_scale=L["v_scale"].cpu().numpy())
             ref = orc.decode_layer(layer_type=t, layout=layout if t == synth.SLIDING else 0,
                                    window=synth.WINDOW, rotary_dim=rot, rope_theta=theta,
                                    context=wl.context[b:b + 1], q=s["q"], k=s["k"], v=s["v"],
-                                   kcache=s["kc"], vcache=s["vc"], sink=sink)
+                                   kcache=s["kc"], vcache=s["vc"], sink=sink, **scales)
             assert_out_close(L["out"][b:b + 1], ref["out"], f"layer {i} seq {b} out")
             assert_lse_close(L["lse"][b:b + 1], ref["lse"], f"layer {i} seq {b} lse")
             assert_bits_equal(L["kc"][b:b + 1], s["kc"], f"layer {i} seq {b} K cache")
@@ -67,6 +70,26 @@ def _run(hd, wl):
 def test_step28_batch64_contexts_512_to_32768(hd, orc):
     """The benchmark's own workload: 28 layers, batch 64, c ~ U[512, 32768], sink."""
     wl = bench.Workload("step28_b64_c512_32768", torch.device("cuda"), seed=0)
+    samples = _samples(wl.context)
+    snap = _snapshot(wl, samples)
+    _run(hd, wl)
+    _check_against_oracle(hd, orc, wl, snap, samples)
+    wl.ctx.close()
+
+
+def test_step28_batch64_e4m3_caches(hd, orc):
+    """The same workload with E4M3 caches (per-kv-head scales), as bench.py --kv fp8 runs it."""
+    wl = bench.Workload("step28_b64_c512_32768", torch.device("cuda"), seed=0, kv="fp8")
+    samples = _samples(wl.context)
+    snap = _snapshot(wl, samples)
+    _run(hd, wl)
+    _check_against_oracle(hd, orc, wl, snap, samples)
+    wl.ctx.close()
+
+
+def test_step28_batch64_roll_layout(hd, orc):
+    """The same workload with rolled sliding windows, shifted inside the step grid."""
+    wl = bench.Workload("step28_b64_c512_32768", torch.device("cuda"), seed=0, layout=synth.LAYOUT_ROLL)
     samples = _samples(wl.context)
     snap = _snapshot(wl, samples)
     _run(hd, wl)
