@@ -71,6 +71,8 @@ _i32, _i64 = _c.c_int32, _c.c_int64
 _SIGS = {
     "hd_validate_config": [_c.POINTER(hd_config)],
     "hd_plan_split": [_i32, _i32, _i32, _i32, _c.POINTER(_i32), _c.POINTER(_i32)],
+    "hd_plan_step_split": [_i32, _c.POINTER(_i32), _c.POINTER(_c.c_uint8), _i32, _i32, _i32, _i32, _i32, _i32,
+                           _c.POINTER(_i32)],
     "hybrid_decode_init": [_c.POINTER(hd_config), _c.POINTER(_P)],
     "hybrid_decode_destroy": [_P],
     "rope_append_kv": [_P, _i32, _i32, _P, _P, _P, _P, _P, hd_kv_cache, _P],
@@ -223,6 +225,18 @@ def hd_plan_split(batch: int, num_kv_heads: int, max_keys: int, num_sms: int) ->
     _check(_lib.hd_plan_split(batch, num_kv_heads, max_keys, num_sms, ctypes.byref(ck),
                               ctypes.byref(nc)), "hd_plan_split")
     return ck.value, nc.value
+
+
+def hd_plan_step_split(max_keys, batch: int, num_kv_heads: int, rows: int, num_sms: int,
+                       kv_dtype: int = 0, multi_token: bool = False, one_chunk=None) -> int:
+    """Chunk size decode_step's step grid uses for layers scoring at most max_keys[i] keys."""
+    n = len(max_keys)
+    mk = (ctypes.c_int32 * n)(*[int(x) for x in max_keys])
+    oc = None if one_chunk is None else (ctypes.c_uint8 * n)(*[1 if x else 0 for x in one_chunk])
+    ck = ctypes.c_int32()
+    _check(_lib.hd_plan_step_split(n, mk, oc, batch, num_kv_heads, rows, int(bool(multi_token)), kv_dtype,
+                                   num_sms, ctypes.byref(ck)), "hd_plan_step_split")
+    return ck.value
 
 
 def hd_status_string(status: int) -> str:

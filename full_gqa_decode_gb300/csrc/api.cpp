@@ -350,28 +350,43 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
 // (two CTAs per SM) ends with its most loaded SM, ceil(CTAs / SMs) CTAs of up
 // to C keys; a longer grid takes the total over the SMs plus one CTA of tail.
 int32_t plan_step_chunk(const hd_ctx *ctx, const std::vector<LayerCall> &calls, size_t rows, bool mt) {
-    const int64_t Hkv = ctx->cfg.num_kv_heads, sms = ctx->num_sms;
-    const int64_t cmax = ctx->kv_type == KV_FP8 ? 2 * kChunkMax : kChunkMax;
-    const int64_t fixed = (256 << 10) / (kHeadDim * kv_elem_bytes(ctx->kv_type) * 2);   // keys
+    const int n = (int)calls.size();
+    std::vector<int32_t> batch(n), max_keys(n);
+    std::vector<uint8_t> one(n);
+    for (int i = 0; i < n; ++i) {
+        batch[i] = calls[i].batch;
+        max_keys[i] = calls[i].max_keys;
+        one[i] = calls[i].one_chunk ? 1 : 0;
+    }
+    return plan_step(ctx->cfg.num_kv_heads, ctx->num_sms, ctx->kv_type, rows, mt, n, batch.data(), max_keys.data(),
+                     one.data());
+}
+
+}  // namespace
+
+int32_t hd::plan_step(int64_t Hkv, int64_t sms, int kv_type, size_t rows, bool mt, int n, const int32_t *batch,
+                      const int32_t *max_keys, const uint8_t *one_chunk) {
+    const int64_t cmax = kv_type == KV_FP8 ? 2 * kChunkMax : kChunkMax;
+    const int64_t fixed = (256 << 10) / (kHeadDim * kv_elem_bytes(kv_type) * 2);   // keys
     const int stages = rows > (size_t)kMaxGroup ? kDeepStages : kStages;
     int64_t longest = 1;
-    for (const LayerCall &L : calls) longest = std::max<int64_t>(longest, L.max_keys);
+    for (int i = 0; i < n; ++i) longest = std::max<int64_t>(longest, max_keys[i]);
     int64_t best_c = cmax;
     double best = -1.0;
     for (int64_t C = kChunkMin; C <= cmax; C += kChunkMin) {
-        int64_t n = 0;
+        int64_t ctas = 0;
         double total = 0.0;
         bool fits = true;
-        for (const LayerCall &L : calls) {
-            const int64_t Cl = L.one_chunk ? std::max<int64_t>(C, L.max_keys) : C;
-            const int64_t ch = L.max_keys > 0 ? (L.max_keys + Cl - 1) / Cl : 1;
-            n += L.batch * Hkv * ch;
-            total += (double)L.batch * Hkv * (double)(ch * fixed + L.max_keys);
+        for (int i = 0; i < n; ++i) {
+            const int64_t Cl = one_chunk[i] ? std::max<int64_t>(C, max_keys[i]) : C;
+            const int64_t ch = max_keys[i] > 0 ? (max_keys[i] + Cl - 1) / Cl : 1;
+            ctas += (int64_t)batch[i] * Hkv * ch;
+            total += (double)batch[i] * Hkv * (double)(ch * fixed + max_keys[i]);
             fits = fits && combine_fits(rows, ch, mt, stages);
         }
         if (!fits) continue;
         const double per_cta = (double)(std::min(C, longest) + fixed);
-        const double est = n <= 2 * sms ? (double)((n + sms - 1) / sms) * per_cta : total / sms + per_cta;
+        const double est = ctas <= 2 * sms ? (double)((ctas + sms - 1) / sms) * per_cta : total / sms + per_cta;
         if (best < 0.0 || est <= best) {   // ties: the longer chunk
             best = est;
             best_c = C;
@@ -380,6 +395,8 @@ int32_t plan_step_chunk(const hd_ctx *ctx, const std::vector<LayerCall> &calls, 
     }
     return (int32_t)best_c;
 }
+
+namespace {
 
 // Launches the layers of one pass as step grids: consecutive layers share a
 // grid while the grid has at most kStepLayers layers and their partials fit
@@ -561,6 +578,24 @@ hd_status hd_plan_split(int32_t batch, int32_t num_kv_heads, int32_t max_keys, i
     if (batch <= 0 || num_kv_heads <= 0 || max_keys < 0 || num_sms <= 0 || !chunk_keys || !num_chunks)
         return HD_ERR_INVALID_ARG;
     plan_split(batch, num_kv_heads, max_keys, num_sms, INT64_MAX, chunk_keys, num_chunks);
+    return HD_OK;
+}
+
+hd_status hd_plan_step_split(int32_t num_layers, const int32_t *max_keys, const uint8_t *one_chunk,
+                             int32_t batch, int32_t num_kv_heads, int32_t rows, int32_t multi_token,
+                             int32_t kv_dtype, int32_t num_sms, int32_t *chunk_keys) {
+    if (num_layers <= 0 || !max_keys || batch <= 0 || num_kv_heads <= 0 || rows <= 0 || rows > kMaxRows ||
+        (multi_token != 0 && multi_token != 1) || num_sms <= 0 || !chunk_keys ||
+        (kv_dtype != HD_KV_BF16 && kv_dtype != HD_KV_FP8_E4M3))
+        return HD_ERR_INVALID_ARG;
+    std::vector<int32_t> b(num_layers, batch);
+    std::vector<uint8_t> one(num_layers, 0);
+    for (int i = 0; i < num_layers; ++i) {
+        if (max_keys[i] < 0) return HD_ERR_INVALID_ARG;
+        if (one_chunk) one[i] = one_chunk[i] ? 1 : 0;
+    }
+    *chunk_keys = plan_step(num_kv_heads, num_sms, kv_dtype == HD_KV_FP8_E4M3 ? KV_FP8 : KV_BF16, (size_t)rows,
+                            multi_token != 0, num_layers, b.data(), max_keys, one.data());
     return HD_OK;
 }
 

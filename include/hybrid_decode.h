@@ -168,6 +168,18 @@ hd_status hd_validate_config(const hd_config *cfg);
 hd_status hd_plan_split(int32_t batch, int32_t num_kv_heads, int32_t max_keys, int32_t num_sms,
                         int32_t *chunk_keys, int32_t *num_chunks);
 
+/* Chunk size of a decode_step step grid (pure host function, no device use):
+ * one size, a multiple of 64 keys up to 2048 (bf16) or 4096 (E4M3), for all
+ * num_layers layers of `batch` sequences, layer i scoring at most max_keys[i]
+ * cached keys per sequence; one_chunk (NULL: none) marks layers that take a
+ * single chunk of max(chunk, max_keys[i]) keys (rolled windows).  rows: query
+ * rows per kv head of the pass (group x tokens); multi_token: a pass of a
+ * multi-token step.  It minimises the grid-time estimate decode_step uses (each
+ * CTA's keys plus a fixed ~256 KiB-equivalent start and combine cost, per SM). */
+hd_status hd_plan_step_split(int32_t num_layers, const int32_t *max_keys, const uint8_t *one_chunk,
+                             int32_t batch, int32_t num_kv_heads, int32_t rows, int32_t multi_token,
+                             int32_t kv_dtype, int32_t num_sms, int32_t *chunk_keys);
+
 /* Creates a context on the current CUDA device: validates cfg, builds the
  * RoPE tables for positions 0..max_context (cos/sin in fp64, stored fp32) and
  * allocates the workspace sized by max_batch/max_context.  Synchronous. */

@@ -82,6 +82,50 @@ def test_plan_split_shapes(hd):
     assert hd.hd_plan_split(1, 2, 4097, 152) == (64, 65)       # batch 1: many short chunks
 
 
+def _spark_keys(full_keys, sliding_keys=511):
+    return [sliding_keys, sliding_keys, sliding_keys, full_keys] * 7
+
+
+def test_step_plan_shapes(hd):
+    """The step grid's chunk plan on the benchmark shapes (152 SMs)."""
+    # batch 64, contexts up to 32768: the longest bf16 chunk (sliding layers one chunk)
+    assert hd.hd_plan_step_split(_spark_keys(32768), 64, 2, 4, 152) == 2048
+    # E4M3: the same bytes per chunk, twice the keys
+    assert hd.hd_plan_step_split(_spark_keys(32768), 64, 2, 4, 152, kv_dtype=hd.HD_KV_FP8_E4M3) == 4096
+    # batch 1 at 4096: 140 CTAs of up to 640 keys, one wave on 152 SMs
+    assert hd.hd_plan_step_split(_spark_keys(4096), 1, 2, 4, 152) == 640
+    # 7 full layers at 131072, batch 4: 2048-key chunks (64 per sequence)
+    assert hd.hd_plan_step_split([131072] * 7, 4, 2, 4, 152) == 2048
+
+
+@pytest.mark.parametrize("batch,full_keys", [(1, 1), (1, 700), (2, 4096), (3, 20000), (64, 32768), (256, 8192)])
+def test_step_plan_is_a_multiple_of_64_within_the_limit(hd, batch, full_keys):
+    for kv, cmax in ((hd.HD_KV_BF16, 2048), (hd.HD_KV_FP8_E4M3, 4096)):
+        c = hd.hd_plan_step_split(_spark_keys(full_keys), batch, 2, 4, 152, kv_dtype=kv)
+        assert c % 64 == 0 and 64 <= c <= cmax
+
+
+def test_step_plan_rolled_windows_take_one_chunk(hd):
+    """Rolled windows read their 511 keys in one chunk whatever the plan's size:
+    the plan may pick chunks shorter than 511 for the other layers."""
+    keys = _spark_keys(4096)
+    one = [k == 511 for k in keys]
+    c = hd.hd_plan_step_split(keys, 1, 2, 4, 152, one_chunk=one)
+    assert c % 64 == 0
+    assert max(c, 511) >= 511
+
+
+def test_step_plan_rejects_bad_arguments(hd):
+    with pytest.raises(Exception):
+        hd.hd_plan_step_split([], 1, 2, 4, 152)
+    with pytest.raises(Exception):
+        hd.hd_plan_step_split([100], 0, 2, 4, 152)
+    with pytest.raises(Exception):
+        hd.hd_plan_step_split([100], 1, 2, 17, 152)   # more rows than a pass takes
+    with pytest.raises(Exception):
+        hd.hd_plan_step_split([-1], 1, 2, 4, 152)
+
+
 def test_binding_structs_match_the_header(hd, tmp_path):
     """Every struct field of the ctypes binding sits at the offset the C compiler
     gives it from include/hybrid_decode.h, and the struct sizes agree."""
