@@ -22,6 +22,15 @@
 
 using namespace hd;
 
+namespace hd {
+// Chunk size of a step grid over `n` layers (batch[i] sequences of at most
+// max_keys[i] scored keys; one_chunk[i]: the layer takes a single chunk of
+// max(C, max_keys[i]) keys), with `rows` query rows per kv head and mt for a
+// multi-token pass (the model is described at its definition below).
+int32_t plan_step(int64_t num_kv_heads, int64_t num_sms, int kv_type, size_t rows, bool mt, int n,
+                  const int32_t *batch, const int32_t *max_keys, const uint8_t *one_chunk);
+}  // namespace hd
+
 // Chunk size: the smallest power of two (64 .. chunk_max keys: 2048 bf16, 4096
 // E4M3, i.e. the same bytes) that gives about
 // one CTA per SM over the grid for the longest sequence bound.  If that grid

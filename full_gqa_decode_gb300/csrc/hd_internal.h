@@ -64,13 +64,6 @@ void plan_split(int64_t batch, int64_t num_kv_heads, int64_t max_keys, int64_t n
                 int64_t max_slots, int32_t *chunk_keys, int32_t *num_chunks, int32_t *stages = nullptr,
                 int64_t chunk_max = kChunkMax);
 
-// Chunk size of a step grid over `n` layers (batch[i] sequences of at most
-// max_keys[i] scored keys; one_chunk[i]: the layer takes a single chunk of
-// max(C, max_keys[i]) keys), with `rows` query rows per kv head and mt for a
-// multi-token pass.  See api.cpp for the model.
-int32_t plan_step(int64_t num_kv_heads, int64_t num_sms, int kv_type, size_t rows, bool mt, int n,
-                  const int32_t *batch, const int32_t *max_keys, const uint8_t *one_chunk);
-
 // Which cache rows the split pass scores for sequence b with c = context[b].
 enum KeySet : int32_t {
     KEYS_RING = 0,         // ring slots [0, min(c, capacity)); the new entry is scored apart
