@@ -276,6 +276,8 @@ class Workload:
             gate = torch.randn(self.B, *tq, self.Hq, generator=g, device=device)
             self.layers[-1]["gate"] = gate
             self.io_gated.append(hd.layer_io(q, k, v, cache, self.sink, out, lse, gate=gate))
+        self.io_arr = hd.layer_array(self.ctx, self.io)              # built once, passed every step
+        self.io_gated_arr = hd.layer_array(self.ctx, self.io_gated)
         self.bytes = step_bytes(self.types, self.context, self.Hkv, layout, self.row_bytes)
         full_idx = [i for i, t in enumerate(self.types) if t == synth.FULL]
         self.full_layer_bytes = (int(scored_keys(synth.FULL, self.context, layout).sum()) * self.Hkv
@@ -285,7 +287,7 @@ class Workload:
 
     def step(self, stream=None, gated=False):
         import full_gqa_decode_gb300 as hd
-        io = self.io_gated if gated else self.io
+        io = self.io_gated_arr if gated else self.io_arr
         if self.tokens > 1:
             hd.decode_step_tokens(self.ctx, self.context_d, io, self.B, self.tokens, self.max_ctx, stream)
         else:

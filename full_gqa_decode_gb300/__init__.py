@@ -309,20 +309,32 @@ def layer_io(q, k, v, cache: hd_kv_cache, sink, out, lse, gate=None) -> hd_layer
     return hd_layer_io(_ptr(q), _ptr(k), _ptr(v), cache, _ptr(sink), _ptr(out), _ptr(lse), _ptr(gate))
 
 
-def decode_step(ctx: Context, context: torch.Tensor, layers: list, batch: int,
+def layer_array(ctx: Context, layers) -> ctypes.Array:
+    """The host array of hd_layer_io decode_step reads, one entry per layer of the
+    context; build it once and pass it to every step whose tensors stay the same."""
+    if isinstance(layers, ctypes.Array) and layers._type_ is hd_layer_io:
+        arr = layers
+    else:
+        arr = (hd_layer_io * len(layers))(*layers)
+    if len(arr) != len(ctx.cfg.layer_types):
+        raise ValueError(f"decode_step needs one hd_layer_io per layer ({len(ctx.cfg.layer_types)}), got {len(arr)}")
+    return arr
+
+
+def decode_step(ctx: Context, context: torch.Tensor, layers, batch: int,
                 max_context_hint: int = 0, stream=None) -> None:
-    arr = (hd_layer_io * len(layers))(*layers)
-    _check(_lib.decode_step(ctx.handle, batch, _ptr(context), max_context_hint, arr, _stream(stream)),
-           "decode_step")
+    """layers: a list of hd_layer_io (one per layer) or an array from layer_array()."""
+    _check(_lib.decode_step(ctx.handle, batch, _ptr(context), max_context_hint, layer_array(ctx, layers),
+                            _stream(stream)), "decode_step")
 
 
 def decode_step_tokens(ctx: Context, context: torch.Tensor, layers: list, batch: int, num_tokens: int,
                        max_context_hint: int = 0, stream=None) -> None:
     """num_tokens new tokens per sequence (q/out [B, T, Hq, D], k/v [B, T, Hkv, D],
-    lse/gate [B, T, Hq]), equal to num_tokens decode_step calls in order."""
-    arr = (hd_layer_io * len(layers))(*layers)
-    _check(_lib.decode_step_tokens(ctx.handle, batch, num_tokens, _ptr(context), max_context_hint, arr,
-                                   _stream(stream)), "decode_step_tokens")
+    lse/gate [B, T, Hq]), equal to num_tokens decode_step calls in order.  layers as
+    for decode_step."""
+    _check(_lib.decode_step_tokens(ctx.handle, batch, num_tokens, _ptr(context), max_context_hint,
+                                   layer_array(ctx, layers), _stream(stream)), "decode_step_tokens")
 
 
 def hybrid_decode_device_errors(ctx: Context, stream=None) -> int:
