@@ -30,10 +30,13 @@
  *     sliding roll layout shifts its window by one once full and appends
  *     (`cache_layout` docstring; ring and roll branches).
  *
- * Numeric contract: bf16 q/k/v/caches/out, fp32 accumulation, fp32 lse.  RoPE
- * tables hold fp32 cos/sin evaluated in fp64 at init.  The written key is
+ * Numeric contract: bf16 q/k/v/caches/out (or E4M3 caches with per-kv-head
+ * fp32 scales, hd_config.kv_dtype), fp32 accumulation, fp32 lse.  RoPE tables
+ * hold fp32 cos/sin evaluated in fp64 at init.  The written key is
  * bf16_rne(k1*c - k2*s) / bf16_rne(k2*c + k1*s) computed in fp64 from the fp32
  * table values, so it is reproducible bit for bit; V is stored bit for bit.
+ * An E4M3 entry is e4m3_rne(x / scale) of that fp64 value (of the bf16 v for
+ * V), with the quotient rounded once, so it is reproducible bit for bit too.
  *
  * Memory and ownership: every tensor argument is a DEVICE pointer owned by the
  * caller (PyTorch allocates them); the library owns only the hd_ctx and the
