@@ -294,3 +294,65 @@ def test_bad_contexts_in_a_step_grid_are_flagged_and_the_rest_served(hd, orc, la
         assert_bits_equal(kd[good], ref["kcache"], f"layer {i} K cache")
         assert_bits_equal(vd[good], ref["vcache"], f"layer {i} V cache")
     ctx.close()
+
+
+def test_step_grid_replays_from_a_cuda_graph(hd, orc):
+    """decode_step captured once in a CUDA graph and replayed over several steps:
+    the grid's parameters (layer table, chunk plan) are fixed at capture, while the
+    contexts, q/k/v and caches live in device buffers the replays update; every
+    replay must equal the oracle's step."""
+    rng = synth.generator(1150)
+    types = [SLIDING, FULL, SLIDING, FULL]
+    B, Hq, Hkv, hint = 2, 8, 2, 1200
+    ctx = make_ctx(hd, types, B, hint)
+    start = np.array([505, 40], np.int32)
+    cases = [LayerCase(rng, B, Hq, Hkv, 511 if t == SLIDING else hint + 1, start) for t in types]
+    host = [[synth.bits(c.kc), synth.bits(c.vc)] for c in cases]
+    dev = [(c.kc.cuda(), c.vc.cuda()) for c in cases]
+    ctx_d = torch.from_numpy(start).cuda()
+    qkv = [(torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda"),
+            torch.empty(B, Hkv, D, dtype=torch.bfloat16, device="cuda"),
+            torch.empty(B, Hkv, D, dtype=torch.bfloat16, device="cuda")) for _ in types]
+    outs = [(torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda"),
+             torch.empty(B, Hq, dtype=torch.float32, device="cuda")) for _ in types]
+    ios = hd.layer_array(ctx, [hd.layer_io(q, k, v, hd.kv_cache(*dev[i]), None, outs[i][0], outs[i][1])
+                               for i, (q, k, v) in enumerate(qkv)])
+    # one eager step on copies of the caches first (the kernel's one-time setup
+    # happens outside the capture; the real caches stay as they are)
+    spare = [(k.clone(), v.clone()) for k, v in dev]
+    hd.decode_step(ctx, ctx_d, [hd.layer_io(q, k, v, hd.kv_cache(*spare[i]), None, outs[i][0], outs[i][1])
+                                for i, (q, k, v) in enumerate(qkv)], B, hint)
+    torch.cuda.synchronize()
+    assert hd.hybrid_decode_device_errors(ctx) == 0
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(side):   # capture only: nothing runs, so the caches stay as they are
+        with torch.cuda.graph(graph, stream=side):
+            hd.decode_step(ctx, ctx_d, ios, B, hint, stream=side)
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    for s_ in range(5):
+        context = start + s_
+        ctx_d.copy_(torch.from_numpy(context))
+        refs = []
+        for i, t in enumerate(types):
+            q = synth.normal_bf16(rng, (B, Hq, D))
+            k = synth.normal_bf16(rng, (B, Hkv, D))
+            v = synth.normal_bf16(rng, (B, Hkv, D))
+            for dst, src in zip(qkv[i], (q, k, v)):
+                dst.copy_(src)
+            rot, theta = synth.ROPE[t]
+            refs.append(orc.decode_layer(layer_type=t, layout=RING if t == SLIDING else 0, window=synth.WINDOW,
+                                         rotary_dim=rot, rope_theta=theta, context=context, q=synth.bits(q),
+                                         k=synth.bits(k), v=synth.bits(v), kcache=host[i][0], vcache=host[i][1]))
+        graph.replay()
+        torch.cuda.synchronize()
+        assert hd.hybrid_decode_device_errors(ctx) == 0
+        for i in range(len(types)):
+            assert_out_close(outs[i][0], refs[i]["out"], f"replay {s_} layer {i} out")
+            assert_lse_close(outs[i][1], refs[i]["lse"], f"replay {s_} layer {i} lse")
+    for i in range(len(types)):
+        assert_bits_equal(dev[i][0], host[i][0], f"layer {i} K cache")
+        assert_bits_equal(dev[i][1], host[i][1], f"layer {i} V cache")
+    ctx.close()
