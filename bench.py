@@ -30,6 +30,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -132,7 +133,7 @@ class ClockSampler:
             self.gpu = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
         except Exception:
             self.gpu = str(device.index)
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_dev{device.index}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"hd_bench_clocks_dev{device.index}.csv")
 
     def __enter__(self):
         try:

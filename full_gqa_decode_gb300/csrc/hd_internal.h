@@ -25,7 +25,7 @@ inline void mark_done_on_device(std::atomic<uint64_t> &done, int device) {
     if (device >= 0 && device < 64) done.fetch_or(1ull << device, std::memory_order_release);
 }
 
-constexpr int kHeadDim = 256;     // head_dim this build implements
+constexpr int kHeadDim = 256;     // the head_dim this library implements
 constexpr int kMaxGroup = 8;      // query heads per kv head
 constexpr int kStageKeys = 32;    // keys per pipeline stage (rows of one TMA box)
 constexpr int kStages = 3;        // bf16 stages per CTA with two CTAs per SM (the default)

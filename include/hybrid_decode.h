@@ -76,7 +76,7 @@ extern "C" {
 typedef enum {
     HD_OK = 0,
     HD_ERR_INVALID_ARG = 1,  /* null pointer, bad size, bad enum, misaligned buffer */
-    HD_ERR_UNSUPPORTED = 2,  /* a shape this build does not implement (head_dim != 256, group > 8) */
+    HD_ERR_UNSUPPORTED = 2,  /* a shape this library does not implement (head_dim != 256, group > 8) */
     HD_ERR_CAPACITY = 3,     /* batch > max_batch, cache capacity too small, context hint too large */
     HD_ERR_CUDA = 4,         /* a CUDA runtime/driver call or a launch failed */
     HD_ERR_STATE = 5         /* wrong layer type for the call, no device available, or
