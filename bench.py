@@ -64,6 +64,19 @@ def step_bytes(types, context, num_kv_heads, layout, row_bytes=KV_ROW_BYTES) -> 
     return int(sum(scored_keys(t, context, layout).sum() for t in types) * num_kv_heads * row_bytes)
 
 
+def step_plan(types, batch, num_kv_heads, group, max_ctx, layout, kv, num_sms) -> dict:
+    """The step grid's chunk plan for a single-token step (hd_plan_step_split, the
+    model decode_step uses) and the CTA count it gives."""
+    import full_gqa_decode_gb300 as hd
+    roll = layout == synth.LAYOUT_ROLL
+    keys = [max_ctx if t == synth.FULL else (synth.WINDOW - 1) for t in types]
+    one = [roll and t == synth.SLIDING for t in types]
+    c = hd.hd_plan_step_split(keys, batch, num_kv_heads, group, num_sms,
+                              kv_dtype=hd.HD_KV_FP8_E4M3 if kv == "fp8" else hd.HD_KV_BF16, one_chunk=one)
+    ctas = sum(batch * num_kv_heads * (1 if o else max(1, -(-k // c))) for k, o in zip(keys, one))
+    return {"chunk_keys": c, "grid_ctas": ctas}
+
+
 def describe_layers(types) -> str:
     n_full = sum(1 for t in types if t == synth.FULL)
     if list(types) == synth.SPARK_LAYER_TYPES:
@@ -529,6 +542,9 @@ def run_ours(args, world, rank, local) -> int:
                              "head_dim": synth.HEAD_DIM, "contexts": describe_lengths(wl.spec["lengths"]),
                              "max_context": wl.max_ctx, "kv_bytes_per_step": wl.bytes,
                              "sliding_layout": args.layout, "kv_dtype": args.kv,
+                             "step_grid": step_plan(wl.types, wl.B, wl.Hkv, wl.Hq // wl.Hkv, wl.max_ctx, wl.layout,
+                                                    args.kv, torch.cuda.get_device_properties(device).multi_processor_count)
+                             if fused else None,
                              "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world}"},
                   "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                   "gpu_launches": int(n1 - n0), "clocks": clk}

@@ -62,3 +62,15 @@ def test_step_bytes_of_the_4k_step_match_the_footprint_model(orc):
     c = np.array([4096], np.int32)
     hybrid, _ = orc.kv_cache_bytes(synth.SPARK_LAYER_TYPES, synth.LAYOUT_RING, 512, 2, 256, 4096)
     assert bench.step_bytes(synth.SPARK_LAYER_TYPES, c, 2, synth.LAYOUT_RING) == hybrid + 28 * 2048
+
+
+def test_step_plan_of_the_benchmark_workloads():
+    """The chunk plan and CTA count bench.py reports for its step grids (152 SMs)."""
+    import synth as s
+    assert bench.step_plan(s.SPARK_LAYER_TYPES, 64, 2, 4, 32679, s.LAYOUT_RING, "bf16", 152) == \
+        {"chunk_keys": 2048, "grid_ctas": 17024}
+    assert bench.step_plan(s.SPARK_LAYER_TYPES, 1, 2, 4, 4096, s.LAYOUT_RING, "bf16", 152) == \
+        {"chunk_keys": 640, "grid_ctas": 140}
+    # rolled windows take one chunk per sequence whatever the chunk size
+    roll = bench.step_plan(s.SPARK_LAYER_TYPES, 1, 2, 4, 4096, s.LAYOUT_ROLL, "bf16", 152)
+    assert roll["grid_ctas"] == 2 * (21 * 1 + 7 * -(-4096 // roll["chunk_keys"]))
