@@ -45,8 +45,12 @@ FP8_ROW_BYTES = 2 * synth.HEAD_DIM          # K row + V row, E4M3 codes, one kv 
 DEFAULT_WORKLOAD = "step28_b64_c512_32768"
 SECONDARY_WORKLOAD = "step28_b1_c4096"
 METRIC = "KV-read HBM GB/s (% of GB300 peak); µs per 28-layer decode step"
-PROFILE_SUMMARY = {"step": os.path.join(ROOT, "profiles", "attn_step_grid_b64_traffic.txt"),
-                   "full": os.path.join(ROOT, "profiles", "attn_layer_kernel_full_b64_traffic.txt")}
+# ncu DRAM-byte captures on the small block4_b16 case (about 1.2 GB on the device,
+# larger than L2): DRAM bytes per algorithmic byte, scaled to a launch of the
+# benchmarked workload (the kernels read every K/V row once, so traffic grows with
+# the scored keys).
+PROFILE_SUMMARY = {"step": os.path.join(ROOT, "profiles", "attn_step_grid_block4_b16_traffic.txt"),
+                   "full": os.path.join(ROOT, "profiles", "attn_layer_kernel_full_block4_b16_traffic.txt")}
 
 
 # ------------------------------------------------------------------ helpers --
@@ -112,10 +116,11 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(kind: str = "step"):
+def profiled_traffic(kind: str, algorithmic_bytes: int):
     """DRAM bytes per launch of the step grid ("step") or of the full-layer kernel
-    ("full") from the committed ncu summary, or None when the summary is absent or
-    the kernel changed since."""
+    ("full") for a launch of `algorithmic_bytes` scored-KV bytes: the committed ncu
+    summary's DRAM bytes per algorithmic byte (small case) times those bytes.  None
+    when the summary is absent or the kernel changed since it was taken."""
     path = PROFILE_SUMMARY[kind]
     if not os.path.exists(path):
         return None
@@ -128,7 +133,7 @@ def profiled_traffic(kind: str = "step"):
     if kv.get("kernel_source_sha256_16") != kernel_source_hash():
         return None
     try:
-        return float(kv["dram_bytes_per_launch"])
+        return round(float(kv["dram_bytes_per_algorithmic_byte"]) * algorithmic_bytes)
     except (KeyError, ValueError):
         return None
 
@@ -403,9 +408,26 @@ def cpu_threads() -> int:
 
 # ----------------------------------------------------------------- the arms --
 
+def workload_config(spec, name, context, layout_name, kv, world) -> dict:
+    """The `config` object of the JSON line, the same for both arms."""
+    types = list(spec["layer_types"])
+    layout = synth.LAYOUT_ROLL if layout_name == "roll" else synth.LAYOUT_RING
+    row = FP8_ROW_BYTES if kv == "fp8" else KV_ROW_BYTES
+    B = len(context)
+    return {"workload": name, "global_batch": B * world, "per_gpu_batch": B,
+            "layers": describe_layers(types), "heads": f"{spec['num_q_heads']} q / {spec['num_kv_heads']} kv",
+            "head_dim": synth.HEAD_DIM, "contexts": describe_lengths(spec["lengths"]),
+            "max_context": int(context.max()),
+            "kv_bytes_per_step": step_bytes(types, context, spec["num_kv_heads"], layout, row),
+            "sliding_layout": layout_name, "kv_dtype": kv,
+            "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world}"}
+
+
 def run_reference(args, world, rank) -> int:
     """The oracle, as it stands, on the host cores: each step is a bounded sample
-    (one [S,S,S,F] block of the step over every sequence)."""
+    (one [S,S,S,F] block of the step over every sequence).  ms_per_step is the
+    timed block's own time; the whole 28-layer step at the same rate is given
+    apart as ms_per_step_extrapolated."""
     if rank != 0:
         return 0
     spec = synth.WORKLOADS[args.workload]
@@ -425,17 +447,19 @@ def run_reference(args, world, rank) -> int:
         secs += s
         nbytes += n
     gbs = nbytes / secs / 1e9
-    full_bytes = step_bytes(spec["layer_types"], context, spec["num_kv_heads"], synth.LAYOUT_RING)
+    config = workload_config(spec, args.workload, context, "ring", "bf16", world)
     sample = (f"one [sliding x3, full] block of the 28-layer step over all {len(context)} sequences "
-              f"({nbytes // args.steps / 1e9:.2f} GB of scored KV per step); fp64 oracle, "
-              f"{threads} host threads")
+              f"({nbytes // args.steps / 1e9:.2f} GB of scored KV per step, caches drawn on the host "
+              f"from the same recipe); fp64 oracle, {threads} host threads")
     line = {"impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": round(full_bytes / (gbs * 1e9) * 1e3, 3), "higher_is_better": True,
+            "ms_per_step": round(secs / args.steps * 1e3, 3),
+            "ms_per_step_extrapolated": round(config["kv_bytes_per_step"] / (gbs * 1e9) * 1e3, 3),
+            "ms_per_step_note": "ms_per_step times the sampled [sliding x3, full] block; "
+                                "ms_per_step_extrapolated is the whole 28-layer step at the same GB/s",
+            "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": args.workload, "global_batch": int(len(context)),
-                       "contexts": "uniform [512, 32768]" if spec["lengths"][0] == "uniform" else str(spec["lengths"]),
-                       "l2": "inputs larger than L2", "parallelism": f"dp{world}"},
+            "config": config,
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -450,7 +474,10 @@ def run_ours(args, world, rank, local) -> int:
     torch.cuda.set_device(device)
     peaks = measured_peaks()
     layout = synth.LAYOUT_ROLL if args.layout == "roll" else synth.LAYOUT_RING
-    wl = Workload(args.workload, device, seed=rank, layout=layout, kv=args.kv)
+    wl = Workload(args.workload, device, seed=rank, layout=layout, kv=args.kv, tokens=args.tokens)
+    # KV bytes a step reads: the scored keys, or with several tokens per sequence
+    # every pass's read of the cache
+    step_kv = wl.token_pass_bytes() if args.tokens > 1 else wl.bytes
     consumer = hd.HD_CONSUMER_TENSOR_CORE if args.consumer == "tensor-core" else hd.HD_CONSUMER_CUDA_CORE
     hd.hybrid_decode_set_consumer(wl.ctx, consumer)
     torch.cuda.synchronize()
@@ -460,7 +487,8 @@ def run_ours(args, world, rank, local) -> int:
     # layers), the dominant kernel, bracketed by events on its stream; the CUDA-core
     # consumer runs one kernel per layer, and the first full layer of every step is
     # bracketed (that launch alone runs without early start; the others overlap).
-    fused = consumer == hd.HD_CONSUMER_TENSOR_CORE
+    fused = consumer == hd.HD_CONSUMER_TENSOR_CORE and args.fusion == "on"
+    hd.hybrid_decode_set_step_fusion(wl.ctx, fused)
     kind = hd.HD_PROFILE_KIND_STEP if fused else hd.HD_FULL
     hd.hybrid_decode_set_profiling(wl.ctx, hd.HD_PROFILE_STEP if fused else hd.HD_PROFILE_FULL | hd.HD_PROFILE_FIRST_ONLY)
     with ClockSampler(device) as clocks:
@@ -477,21 +505,23 @@ def run_ours(args, world, rank, local) -> int:
     flags = hd.hybrid_decode_device_errors(wl.ctx)
     if flags:
         raise RuntimeError(f"device error flags {flags:#x} during the benchmark")
-    ms_max, total_bytes = reduce_timing(ms, wl.bytes, world, device)
+    ms_max, total_bytes = reduce_timing(ms, step_kv, world, device)
     gbs = total_bytes / (ms_max * 1e-3) / 1e9
 
     # diagnostic passes, outside the timed region: one kernel per layer, the first
     # full layer and every sliding layer bracketed alone
-    layer_kernels = layer_kernel_rooflines(wl, peaks)
+    layer_kernels = layer_kernel_rooflines(wl, peaks) if args.tokens == 1 else {}
 
     # roofline of the dominant kernel
     avg_ms = dom_ms / max(dom_launches, 1)
-    per_launch = (wl.bytes * args.steps // max(dom_launches, 1)) if fused else wl.full_layer_bytes
+    per_launch = (step_kv * args.steps // max(dom_launches, 1)) if fused else wl.full_layer_bytes
     achieved = per_launch / (avg_ms * 1e-3) / 1e9 if dom_launches else None
     roofline = {"bound": "hbm", "achieved": round(achieved, 1) if achieved else None,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s",
                 "frac": round(achieved / peaks["hbm_gbs"], 4) if achieved else None,
-                "traffic": profiled_traffic("step" if fused else "full"),
+                "traffic": profiled_traffic("step" if fused else "full", per_launch),
+                "traffic_source": "ncu DRAM read+write bytes per algorithmic byte on block4_b16_c512_32768 "
+                                  "(profiles/), times this launch's algorithmic bytes",
                 "kernel": (f"attn_layer_kernel step grid (the attention of all {len(wl.types)} layers); events "
                            f"around the grid of each timed step" if fused else
                            f"attn_layer_kernel, full layers ({args.consumer}); events around the first full "
@@ -531,39 +561,41 @@ def run_ours(args, world, rank, local) -> int:
                  else None)
         cpu = cpu_baseline(wl, device)
         secondary = secondary_batch1(device, args, consumer) if args.secondary else None
+        others = (baseline_configs(device, args, consumer, read_peak)
+                  if args.secondary and args.kv == "bf16" and args.workload == DEFAULT_WORKLOAD
+                  and consumer == hd.HD_CONSUMER_TENSOR_CORE else None)
         result = {"metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
                   "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
                   "us_per_step": round(ms_max * 1e3, 1), "higher_is_better": True, "scaling": "weak",
                   "vs_baseline": None, "dtype": "bf16" if args.kv == "bf16" else "fp8_e4m3 KV, f16 MMA",
                   "data": "synthetic",
                   "frac_of_peak_hbm": round(gbs / peaks["hbm_gbs"], 4),
-                  "config": {"workload": wl.name, "global_batch": wl.B * world, "per_gpu_batch": wl.B,
-                             "layers": describe_layers(wl.types), "heads": f"{wl.Hq} q / {wl.Hkv} kv",
-                             "head_dim": synth.HEAD_DIM, "contexts": describe_lengths(wl.spec["lengths"]),
-                             "max_context": wl.max_ctx, "kv_bytes_per_step": wl.bytes,
-                             "sliding_layout": args.layout, "kv_dtype": args.kv,
-                             "step_grid": step_plan(wl.types, wl.B, wl.Hkv, wl.Hq // wl.Hkv, wl.max_ctx, wl.layout,
-                                                    args.kv, torch.cuda.get_device_properties(device).multi_processor_count)
-                             if fused else None,
-                             "l2": "inputs larger than L2 (no flush)", "parallelism": f"dp{world}"},
+                  "config": workload_config(wl.spec, wl.name, wl.context, args.layout, args.kv, world),
+                  "step_grid": step_plan(wl.types, wl.B, wl.Hkv, wl.Hq // wl.Hkv, wl.max_ctx, wl.layout,
+                                         args.kv, torch.cuda.get_device_properties(device).multi_processor_count)
+                  if fused else None,
                   "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                   "gpu_launches": int(n1 - n0), "clocks": clk}
         result["output_gate"] = {"ms_per_step": round(gated_ms, 4),
-                                 "value": round(wl.bytes / (gated_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+                                 "value": round(step_kv / (gated_ms * 1e-3) / 1e9, 1), "unit": "GB/s",
                                  "ungated_ms_per_step": round(plain_ms, 4),
                                  "overhead_vs_ungated": round(gated_ms / plain_ms - 1.0, 4)}
         result["kernel_per_layer"] = {
-            "ms_per_step": round(per_layer_ms, 4), "value": round(wl.bytes / (per_layer_ms * 1e-3) / 1e9, 1),
+            "ms_per_step": round(per_layer_ms, 4), "value": round(step_kv / (per_layer_ms * 1e-3) / 1e9, 1),
             "unit": "GB/s", "note": "step fusion off: one kernel per layer, each starting while the previous drains"}
         result["layers_in_stream_order"] = {
-            "ms_per_step": round(serial_ms, 4), "value": round(wl.bytes / (serial_ms * 1e-3) / 1e9, 1),
+            "ms_per_step": round(serial_ms, 4), "value": round(step_kv / (serial_ms * 1e-3) / 1e9, 1),
             "unit": "GB/s", "note": "step fusion off and no layer starts before the previous one is complete"}
+        if args.tokens > 1:
+            result["config"].update(tokens_per_sequence=args.tokens, kv_bytes_read_per_step=step_kv)
         if fp8:
             result["fp8_kv"] = fp8
         if multi:
             result["multi_token"] = multi
         if secondary:
             result["secondary"] = secondary
+        if others:
+            result["baseline_configs"] = others
         print(json.dumps(result), flush=True)
     return 0
 
@@ -616,7 +648,7 @@ def layer_kernel_rooflines(wl, peaks) -> dict:
                          "frac": round(gbs / peaks["hbm_gbs"], 4), "algorithmic_bytes_per_launch": nbytes,
                          "avg_launch_ms": round(avg, 4)}
     if "full_layers" in out:
-        out["full_layers"]["traffic"] = profiled_traffic("full")
+        out["full_layers"]["traffic"] = profiled_traffic("full", wl.full_layer_bytes)
     hd.hybrid_decode_set_profiling(wl.ctx, 0)
     hd.hybrid_decode_set_step_fusion(wl.ctx, True)
     return out
@@ -641,7 +673,7 @@ def e2e_measure(wl, args, world, device) -> dict:
         host_out.copy_(wl.outs, non_blocking=True)
         host_lse.copy_(wl.lses, non_blocking=True)
     ms = time_steps(run, args.steps, args.warmup, world, device)
-    ms_max, total = reduce_timing(ms, wl.bytes, world, device)
+    ms_max, total = reduce_timing(ms, wl.token_pass_bytes() if wl.tokens > 1 else wl.bytes, world, device)
     return {"value": round(total / (ms_max * 1e-3) / 1e9, 1), "unit": "GB/s",
             "ms_per_step": round(ms_max, 4), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
@@ -750,6 +782,72 @@ def multi_token_steps(device, args, consumer, layout, single_ms) -> list:
     return res
 
 
+def roll_shift_bytes(wl) -> int:
+    """Bytes a roll layout writes per step to shift its full windows down one
+    row (K and V, every sliding layer), apart from the scored-key reads."""
+    full = (wl.context >= synth.WINDOW).astype(np.int64) * (synth.WINDOW - 1)
+    n_sliding = sum(1 for t in wl.types if t == synth.SLIDING)
+    return int(full.sum()) * wl.Hkv * wl.row_bytes * n_sliding
+
+
+def timed_workload(name, device, args, consumer, layout, read_peak) -> dict:
+    """One workload's step (step grids on): ms per step, scored-KV GB/s, the grid
+    alone by events, and fractions of the copy peak and of the read stream."""
+    import torch
+    import full_gqa_decode_gb300 as hd
+    wl = Workload(name, device, seed=0, layout=layout)
+    hd.hybrid_decode_set_consumer(wl.ctx, consumer)
+    ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
+    hd.hybrid_decode_set_profiling(wl.ctx, hd.HD_PROFILE_STEP)
+    for _ in range(3):
+        wl.step()
+    grid_ms, grid_n = hd.hybrid_decode_profile(wl.ctx, hd.HD_PROFILE_KIND_STEP)
+    hd.hybrid_decode_set_profiling(wl.ctx, 0)
+    hd.hybrid_decode_set_step_fusion(wl.ctx, False)
+    per_layer_ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
+    hd.hybrid_decode_set_step_fusion(wl.ctx, True)
+    flags = hd.hybrid_decode_device_errors(wl.ctx)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x} in {name}")
+    peak = measured_peaks()["hbm_gbs"]
+    gbs = wl.bytes / (ms * 1e-3) / 1e9
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    plan = step_plan(wl.types, wl.B, wl.Hkv, wl.Hq // wl.Hkv, wl.max_ctx, wl.layout, "bf16", sms)
+    res = {"ms_per_step": round(ms, 4), "us_per_step": round(ms * 1e3, 1), "value": round(gbs, 1), "unit": "GB/s",
+           "kv_bytes_per_step": wl.bytes, "frac_of_peak_hbm": round(gbs / peak, 4),
+           "frac_of_read_stream": round(gbs / read_peak, 4) if read_peak else None,
+           "step_grid": dict(plan, chunks_per_full_sequence=-(-(wl.max_ctx + 1) // plan["chunk_keys"]))}
+    if grid_n:
+        avg = grid_ms / grid_n
+        per_launch = wl.bytes * 3 // grid_n
+        res["step_grid"].update({"launches_per_step": grid_n // 3, "avg_launch_ms": round(avg, 4),
+                                 "achieved": round(per_launch / (avg * 1e-3) / 1e9, 1),
+                                 "frac": round(per_launch / (avg * 1e-3) / 1e9 / peak, 4)})
+    res["kernel_per_layer"] = {"ms_per_step": round(per_layer_ms, 4),
+                               "value": round(wl.bytes / (per_layer_ms * 1e-3) / 1e9, 1), "unit": "GB/s"}
+    if layout == synth.LAYOUT_ROLL:
+        res["roll_shift_bytes_per_step"] = roll_shift_bytes(wl)
+    wl.ctx.close()
+    del wl
+    torch.cuda.empty_cache()
+    return res
+
+
+def baseline_configs(device, args, consumer, read_peak) -> dict:
+    """The other benchmark configurations, each as its own step: seven full layers
+    at batch 4 and context 131072 (one chunk plan over the step grid), and the
+    group-8 batch-256 mixed-length step with ring and with roll windows."""
+    out = {"full7_b4_c131072": timed_workload("full7_b4_c131072", device, args, consumer, synth.LAYOUT_RING,
+                                              read_peak)}
+    g8 = {lay: timed_workload("step28_b256_g8_mixed", device, args, consumer,
+                              synth.LAYOUT_RING if lay == "ring" else synth.LAYOUT_ROLL, read_peak)
+          for lay in ("ring", "roll")}
+    g8["roll_over_ring_time"] = round(g8["roll"]["ms_per_step"] / g8["ring"]["ms_per_step"], 4)
+    g8["ring_saves"] = round(1.0 - g8["ring"]["ms_per_step"] / g8["roll"]["ms_per_step"], 4)
+    out["step28_b256_g8_mixed"] = g8
+    return out
+
+
 def secondary_batch1(device, args, consumer) -> dict:
     """The 28-layer step at batch 1, context 4096 (launch-latency bound), launched
     eagerly and replayed from a CUDA graph of one decode_step."""
@@ -794,6 +892,10 @@ def main(argv=None) -> int:
                     help="cache layout of the sliding layers")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
                     help="cache element type (fp8: E4M3 codes with per-kv-head scales)")
+    ap.add_argument("--tokens", type=int, default=1, choices=range(1, 9), metavar="T",
+                    help="new tokens per sequence and step (decode_step_tokens); GB/s then counts every pass's cache read")
+    ap.add_argument("--fusion", choices=["on", "off"], default="on",
+                    help="off: the timed steps run one kernel per layer (the dominant kernel is then the full layer's)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -27,6 +27,7 @@ HD_CONSUMER_CUDA_CORE, HD_CONSUMER_TENSOR_CORE = 0, 1
 HD_PROFILE_SLIDING, HD_PROFILE_FULL, HD_PROFILE_FIRST_ONLY, HD_PROFILE_STEP = 1 << HD_SLIDING, 1 << HD_FULL, 4, 8
 HD_PROFILE_KIND_STEP = 2
 HD_KV_BF16, HD_KV_FP8_E4M3 = 0, 1
+HD_STATIC_SCRATCH_BYTES = 64 << 20   # the allocation-free entry point's scratch array
 STATUS = {0: "HD_OK", 1: "HD_ERR_INVALID_ARG", 2: "HD_ERR_UNSUPPORTED", 3: "HD_ERR_CAPACITY",
           4: "HD_ERR_CUDA", 5: "HD_ERR_STATE"}
 DEVERR = {1: "HD_DEVERR_CONTEXT_NEGATIVE", 2: "HD_DEVERR_CONTEXT_CAPACITY",
@@ -86,10 +87,13 @@ _SIGS = {
     "hybrid_decode_profile": [_P, _i32, _c.POINTER(_c.c_double), _c.POINTER(_i64)],
     "hybrid_decode_set_consumer": [_P, _i32],
     "decode_attn_full_static_scratch": [_i32, _i32, _i32, _P, _i32, _P, hd_kv_cache, _P, _P, _P, _P],
+    "decode_attn_full_static_scratch_plan": [_i32, _i32, _i32, _i32, _i32, _c.POINTER(_i64), _c.POINTER(_i32),
+                                             _c.POINTER(_i32)],
     "hybrid_decode_read_probe": [_P, _i64, _P],
     "hybrid_decode_inject_lost_copy": [_P, _i32],
     "hybrid_decode_set_layer_overlap": [_P, _i32],
     "hybrid_decode_set_step_fusion": [_P, _i32],
+    "hybrid_decode_set_cluster_combine": [_P, _i32],
 }
 for _name, _args in _SIGS.items():
     _fn = getattr(_lib, _name)
@@ -376,6 +380,12 @@ def hybrid_decode_set_step_fusion(ctx: Context, enable: bool) -> None:
     _check(_lib.hybrid_decode_set_step_fusion(ctx.handle, int(bool(enable))), "hybrid_decode_set_step_fusion")
 
 
+def hybrid_decode_set_cluster_combine(ctx: Context, enable: bool) -> None:
+    """Single-layer launches of small grids merge their chunks inside a
+    thread-block cluster (default True), or through the workspace (False)."""
+    _check(_lib.hybrid_decode_set_cluster_combine(ctx.handle, 1 if enable else 0), "hybrid_decode_set_cluster_combine")
+
+
 def hybrid_decode_set_consumer(ctx: Context, consumer: int) -> None:
     """HD_CONSUMER_CUDA_CORE or HD_CONSUMER_TENSOR_CORE (the default)."""
     _check(_lib.hybrid_decode_set_consumer(ctx.handle, consumer), "hybrid_decode_set_consumer")
@@ -394,6 +404,17 @@ def decode_attn_full_static_scratch(num_kv_heads: int, context, max_context: int
                                                 max_context, _ptr(q_rot), cache, _ptr(sink), _ptr(out),
                                                 _ptr(lse), _stream(stream)),
            "decode_attn_full_static_scratch")
+
+
+def decode_attn_full_static_scratch_plan(batch: int, num_q_heads: int, num_kv_heads: int, max_context: int,
+                                         num_sms: int) -> tuple[int, int, int, int]:
+    """(scratch bytes, keys per chunk, chunks, status) of decode_attn_full_static_scratch
+    for this shape (pure host function).  Status 0: the call fits the array; 3
+    (HD_ERR_CAPACITY): it would be refused; 1 / 2: the shape is rejected."""
+    nbytes, chunk, chunks = _i64(0), _i32(0), _i32(0)
+    st = _lib.decode_attn_full_static_scratch_plan(batch, num_q_heads, num_kv_heads, max_context, num_sms,
+                                                   ctypes.byref(nbytes), ctypes.byref(chunk), ctypes.byref(chunks))
+    return nbytes.value, chunk.value, chunks.value, st
 
 
 def hybrid_decode_read_probe(buffer: torch.Tensor, stream=None) -> int:

@@ -98,6 +98,8 @@ struct hd_ctx {
     int32_t *counters = nullptr;         // [num_layers][max_batch][Hkv] chunk tickets, zero between calls
     int32_t *err = nullptr;
     int consumer = CONSUMER_MMA;
+    int cluster_max = 0;                 // largest cluster the single-layer kernel runs with (0: none)
+    bool cluster_combine = true;         // single-layer calls: small grids merge chunks in a cluster
     int32_t drop_stage = -1;             // test hook, see hybrid_decode_inject_lost_copy
     bool layer_overlap = true;           // decode_step: layers start before the previous one finishes
     bool fuse_step = true;               // decode_step: one grid for all layers (step tables)
@@ -268,12 +270,6 @@ struct LayerCall {
     int tokens = 1, token0 = 0, total_tokens = 1;   // multi-token decode: this pass's tokens
 };
 
-// The combine keeps a weight per (row, chunk) plus a float4 row per row in the stage ring.
-bool combine_fits(size_t rows, int64_t num_chunks, bool mt, int stages) {
-    return (rows * num_chunks + 3) * sizeof(float) + rows * 64 * 16 + (mt ? kMtNewBytes : 0) <=
-           (size_t)stages * kStageBytes;
-}
-
 // Kernel arguments of one layer call with a given split; its partials start at
 // partial row part_row0 of the workspace, its tickets at the layer's counters.
 void fill_layer_args(const hd_ctx *ctx, const LayerCall &L, int32_t chunk_keys, int32_t num_chunks,
@@ -316,6 +312,7 @@ void fill_layer_args(const hd_ctx *ctx, const LayerCall &L, int32_t chunk_keys, 
     a.tokens = L.tokens;
     a.token0 = L.token0;
     a.total_tokens = L.total_tokens;
+    a.cluster = 0;
 }
 
 hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream) {
@@ -323,14 +320,40 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     hd_status st = maps_for(ctx, L.layer, L.cache, L.batch, &km, &vm);
     if (st != HD_OK) return st;
     int32_t chunk_keys = 0, num_chunks = 0, stages = kStages;
-    plan_split(L.batch, ctx->cfg.num_kv_heads, L.max_keys, ctx->num_sms, ctx->part_slots, &chunk_keys,
-               &num_chunks, &stages, ctx->kv_type == KV_FP8 ? 2 * kChunkMax : kChunkMax);
+    if (L.one_chunk) {   // a rolled window shifted in place: one CTA reads each sequence's window
+        chunk_keys = (std::max(L.max_keys, 1) + kChunkMin - 1) / kChunkMin * kChunkMin;
+        num_chunks = 1;
+        stages = (int64_t)L.batch * ctx->cfg.num_kv_heads <= ctx->num_sms ? kDeepStages : kStages;
+    } else {
+        plan_split(L.batch, ctx->cfg.num_kv_heads, L.max_keys, ctx->num_sms, ctx->part_slots, &chunk_keys,
+                   &num_chunks, &stages, ctx->kv_type == KV_FP8 ? 2 * kChunkMax : kChunkMax);
+    }
+    // Small grids (at most one CTA per SM) of single-token calls run every chunk
+    // of a (sequence, kv head) in one thread-block cluster and merge the chunks'
+    // partials in distributed shared memory, with no workspace round trip; the
+    // sequence is then split into at most cluster_max chunks.
+    int32_t cluster = 0;
+    if (ctx->cluster_combine && ctx->cluster_max > 1 && L.total_tokens == 1 && !L.one_chunk && L.max_keys > 0) {
+        const int64_t units = (int64_t)L.batch * ctx->cfg.num_kv_heads;
+        int64_t ck = chunk_keys, k = num_chunks;
+        if (k > ctx->cluster_max) {
+            ck = ((L.max_keys + ctx->cluster_max - 1) / ctx->cluster_max + kChunkMin - 1) / kChunkMin * kChunkMin;
+            k = (L.max_keys + ck - 1) / ck;
+        }
+        if (k > 1 && units * k <= ctx->num_sms) {
+            chunk_keys = (int32_t)ck;
+            num_chunks = (int32_t)k;
+            stages = kDeepStages;
+            cluster = (int32_t)k;
+        }
+    }
     if ((int64_t)ctx->group * L.tokens > kMaxGroup) stages = kDeepStages;   // 16 rows: one CTA per SM
     if ((int64_t)L.batch * num_chunks > ctx->part_slots) return HD_ERR_CAPACITY;
     const size_t rows = (size_t)ctx->group * L.tokens;   // query rows per kv head
     if (!combine_fits(rows, num_chunks, L.total_tokens > 1, stages)) return HD_ERR_CAPACITY;
     LayerArgs a;
     fill_layer_args(ctx, L, chunk_keys, num_chunks, 0, a);
+    a.cluster = cluster;
 
     const bool sliding = ctx->layer_types[L.layer] == HD_SLIDING;
     const int type = sliding ? HD_SLIDING : HD_FULL;
@@ -456,7 +479,6 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
         // this chunk count, or its CTA count): its own plan and launch, in stream order.
         if (need > ctx->part_rows || layer_ctas > INT_MAX ||
             !combine_fits(rows, ch, mt, rows > (size_t)kMaxGroup ? kDeepStages : kStages)) {
-            if (L.key_set == KEYS_ROLL_SHIFT) return HD_ERR_UNSUPPORTED;   // only step grids shift in place
             if ((st = flush()) != HD_OK || (st = launch_layer_call(ctx, L, stream)) != HD_OK) return st;
             continue;
         }
@@ -641,6 +663,7 @@ hd_status hybrid_decode_init(const hd_config *cfg, hd_ctx **out_ctx) {
     ctx->sliding_layout = cfg->cache_layout == HD_LAYOUT_ROLL ? HD_LAYOUT_ROLL : HD_LAYOUT_RING;
     ctx->kv_type = cfg->kv_dtype == HD_KV_FP8_E4M3 ? KV_FP8 : KV_BF16;
     ctx->maps.resize(cfg->num_layers);
+    ctx->cluster_max = layer_cluster_limit(ctx->group, ctx->kv_type);
 
     bool any_sliding = false, any_full = false;
     for (int t : ctx->layer_types) (t == HD_SLIDING ? any_sliding : any_full) = true;
@@ -822,9 +845,7 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
                              int32_t max_context_hint, const hd_layer_io *layers, void *stream) {
     if (!ctx || !layers || num_tokens < 1 || num_tokens > kMaxTokens) return HD_ERR_INVALID_ARG;
     if (check_device(ctx) != HD_OK) return HD_ERR_STATE;
-    const bool any_sliding = std::count(ctx->layer_types.begin(), ctx->layer_types.end(), (int)HD_SLIDING) > 0;
-    if (num_tokens > 1 && ((any_sliding && ctx->sliding_layout == HD_LAYOUT_ROLL) || ctx->consumer != CONSUMER_MMA))
-        return HD_ERR_UNSUPPORTED;
+    if (num_tokens > 1 && ctx->consumer != CONSUMER_MMA) return HD_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ctx->profile_seen[0] = ctx->profile_seen[1] = false;
     // Every layer is checked before anything is launched.
@@ -835,8 +856,10 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
         if (!io.q || !io.k || !io.v || !aligned16(io.q) || !aligned16(io.k) || !aligned16(io.v))
             return HD_ERR_INVALID_ARG;
     }
-    const bool fused =
-        ctx->fuse_step && ctx->consumer == CONSUMER_MMA && layers_independent(ctx, batch, num_tokens, layers);
+    // Independent layers (the call's contract) may share one grid, or overlap as
+    // one kernel per layer; layers that alias run one kernel per layer in full order.
+    const bool indep = layers_independent(ctx, batch, num_tokens, layers);
+    const bool fused = ctx->fuse_step && ctx->consumer == CONSUMER_MMA && indep;
     std::vector<LayerCall> &calls = ctx->step_calls;
     calls.assign(ctx->cfg.num_layers, LayerCall{});
     for (int i = 0; i < ctx->cfg.num_layers; ++i) {
@@ -869,45 +892,13 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
             L.key_set = KEYS_RING;
             L.new_kind = NEW_ROTATE;
             L.commit = COMMIT_RING;
-        } else if (fused) {   // the grid reads the window, then shifts it and stores the new entry
+        } else {   // the kernel reads the window, then shifts it and stores the new entries
             L.max_keys = ctx->cfg.sliding_window - 1;
             L.key_set = KEYS_ROLL_SHIFT;
             L.new_kind = NEW_ROTATE;
             L.commit = COMMIT_ROLL;
             L.one_chunk = true;
-        } else {
-            L.max_keys = ctx->cfg.sliding_window;
-            L.key_set = KEYS_ROLL;
-            L.new_kind = NEW_NONE;
-            L.commit = COMMIT_NONE;
         }
-    }
-    // Layer kernels of a roll layout: the windows shift (and append) before any
-    // attention reads them.
-    for (const LayerCall &L : calls) {
-        if (L.key_set != KEYS_ROLL) continue;
-        RopeArgs r{};
-        r.context = context;
-        r.k = static_cast<const __nv_bfloat16 *>(L.new_k);
-        r.v = static_cast<const __nv_bfloat16 *>(L.new_v);
-        r.table = ctx->table_sliding.data;
-        r.dst_k = L.cache.k;
-        r.dst_v = L.cache.v;
-        r.kv_type = ctx->kv_type;
-        r.k_scale = L.cache.k_scale;
-        r.v_scale = L.cache.v_scale;
-        r.seq_stride = L.cache.seq_stride;
-        r.capacity = L.cache.capacity;
-        r.err = ctx->err;
-        r.num_q_heads = ctx->cfg.num_q_heads;
-        r.num_kv_heads = ctx->cfg.num_kv_heads;
-        r.rotary_dim = ctx->table_sliding.rotary_dim;
-        r.key_set = KEYS_ROLL;
-        r.window = ctx->cfg.sliding_window;
-        r.max_context = ctx->cfg.max_context;
-        hd_status st = cuda_status(launch_roll_window(r, batch, s));
-        if (st != HD_OK) return st;
-        ++ctx->launches;
     }
     const int tmax = std::min(kMaxTokens, kMaxRows / ctx->group);
     if (fused) {
@@ -935,7 +926,7 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
             while (2 * tp <= tmax && 2 * tp <= num_tokens - t0) tp *= 2;
             L.tokens = tp;
             L.token0 = t0;
-            L.pdl = L.layer > 0 && t0 == 0;   // a later pass reads what the previous pass wrote
+            L.pdl = indep && L.layer > 0 && t0 == 0;   // a later pass reads what the previous pass wrote
             hd_status st = launch_layer_call(ctx, L, s);
             if (st != HD_OK) return st;
             t0 += tp;
@@ -947,6 +938,12 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
 hd_status hybrid_decode_set_step_fusion(hd_ctx *ctx, int32_t enable) {
     if (!ctx || (enable != 0 && enable != 1)) return HD_ERR_INVALID_ARG;
     ctx->fuse_step = enable != 0;
+    return HD_OK;
+}
+
+hd_status hybrid_decode_set_cluster_combine(hd_ctx *ctx, int32_t enable) {
+    if (!ctx || (enable != 0 && enable != 1)) return HD_ERR_INVALID_ARG;
+    ctx->cluster_combine = enable != 0;
     return HD_OK;
 }
 

@@ -12,6 +12,17 @@ size_t layer_smem_bytes(int group, int stages) {
            kMaxRows * sizeof(int);
 }
 
+int layer_cluster_limit(int group, int kv) {
+    if (kv == KV_FP8) return layer_cluster_limit_fp8(group);
+    switch (group) {
+    case 1: return cluster_limit_g<1, KV_BF16>();
+    case 2: return cluster_limit_g<2, KV_BF16>();
+    case 4: return cluster_limit_g<4, KV_BF16>();
+    case 8: return cluster_limit_g<8, KV_BF16>();
+    default: return 0;
+    }
+}
+
 cudaError_t launch_layer_bf16(const LaunchTable<1> &t, dim3 grid, int rows, bool mt, int consumer, int stages,
                               bool pdl, cudaStream_t s) {
     return launch_kv<KV_BF16, 1>(t, grid, rows, mt, consumer, stages, pdl, s);

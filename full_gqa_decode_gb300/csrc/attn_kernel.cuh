@@ -53,6 +53,14 @@
 #include "e4m3.cuh"
 #include "hd_internal.h"
 
+// Build switches of the attention kernel (measured choices; see the comments at their use).
+#ifndef HD_STEP_NEW_IN_EVERY_CTA
+#define HD_STEP_NEW_IN_EVERY_CTA 0
+#endif
+#ifndef HD_STEP_ISSUE_EARLY
+#define HD_STEP_ISSUE_EARLY 1
+#endif
+
 namespace hd {
 namespace {
 
@@ -131,6 +139,31 @@ __device__ __forceinline__ void tma_load_4d(void *dst, const CUtensorMap *map, u
         " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
         : "memory");
+}
+// Distributed shared memory of a thread-block cluster: the address of the same
+// shared variable in CTA `rank` of the cluster, loads from it, and the
+// cluster-wide barrier (release / acquire: shared-memory writes before it are
+// visible to every CTA of the cluster after it).
+__device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+    return v;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 __device__ __forceinline__ float fast_exp2(float x) {
     float y;
@@ -229,38 +262,6 @@ __device__ __forceinline__ float f64_to_bf16_value(double x) {
     float t = __double2float_rz(x);
     if ((double)t != x && isfinite(t)) t = __uint_as_float(__float_as_uint(t) | 1u);
     return __bfloat162float(__float2bfloat16_rn(t));
-}
-
-// Loads what the combine needs from global memory: the new entry (raw k and
-// v for NEW_ROTATE, the staged entry otherwise: bf16 values, or E4M3 codes
-// kept in code_s [2][256]) and the group's sink values and output-gate
-// logits.  (The rotary row at position c is loaded with q.)  Needs 64 threads.
-template <int G, int KV>
-__device__ __forceinline__ void load_combine_inputs(const LayerArgs &a, int b, int kvh, int c, float *kraw_s,
-                                                    float *vnew_s, float2 *tab_s, float *sink_s, float *gate_s,
-                                                    uint8_t *code_s) {
-    const int t = threadIdx.x;
-    if (a.new_kind != NEW_NONE) {   // one 16-byte load per thread, the K row then the V row
-        const size_t e = ((size_t)b * a.num_kv_heads + kvh) * kHeadDim;
-        if (KV == KV_FP8 && a.new_kind == NEW_STAGED) {   // 256 codes per row
-            if (t < 32) {
-                const uint8_t *src = static_cast<const uint8_t *>(t < 16 ? a.new_k : a.new_v) + e;
-                reinterpret_cast<uint4 *>(code_s + (t < 16 ? 0 : kHeadDim))[t & 15] =
-                    reinterpret_cast<const uint4 *>(src)[t & 15];
-            }
-        } else if (t < 64) {                               // 256 bf16 per row
-            const __nv_bfloat16 *src = static_cast<const __nv_bfloat16 *>(t < 32 ? a.new_k : a.new_v) + e;
-            float f[8];
-            unpack_bf16x8(reinterpret_cast<const uint4 *>(src)[t & 31], f);
-            float4 *dst = reinterpret_cast<float4 *>((t < 32 ? kraw_s : vnew_s) + (t & 31) * 8);
-            dst[0] = make_float4(f[0], f[1], f[2], f[3]);
-            dst[1] = make_float4(f[4], f[5], f[6], f[7]);
-        }
-    }
-    if (t < G) {
-        sink_s[t] = a.sink ? a.sink[kvh * G + t] : 0.f;
-        gate_s[t] = a.gate ? a.gate[(size_t)b * a.num_q_heads + kvh * G + t] : 0.f;
-    }
 }
 
 // Scored cache keys of sequence context c, or -1 (and the error bit) when c
@@ -815,11 +816,11 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     }
     const LayerLaunch &ll = p.layer[layer];
     // A step table is indexed at run time, so its layer's arguments are read
-    // through a computed address.  The bf16 kernels at two CTAs per SM (the
-    // register-capped ones) copy them to shared memory once instead, which
-    // measured faster there and slower elsewhere (a single layer's are read
-    // from the parameters at fixed offsets).
-    constexpr bool kArgsInSmem = NL > 1 && KV == KV_BF16 && !MT && S * kStage <= kStages * kStageBytes;
+    // through a computed address (a single layer's from the parameters at fixed
+    // offsets).  Copying them to shared memory once measured faster in the
+    // register-capped bf16 kernels (two CTAs per SM) only while they had registers
+    // to spare; it is off.
+    constexpr bool kArgsInSmem = false;
     __shared__ LayerArgs step_args_s;
     if constexpr (kArgsInSmem) {
         static_assert(sizeof(LayerArgs) % 4 == 0, "copied as words");
@@ -872,12 +873,18 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
         return;
     }
     const int nchunks = max(1, (n + a.chunk_keys - 1) / a.chunk_keys);
-    if (chunk >= nchunks) return;  // uniform over the CTA
+    // Cluster launches: every CTA of the cluster takes part in its barriers, so a
+    // chunk past the sequence's keys stays, with no keys, instead of leaving.
+    const int clus = NL == 1 ? a.cluster : 0;
+    if (chunk >= nchunks && clus <= 1) return;  // uniform over the CTA
     const int start = chunk * a.chunk_keys;
     const int end = min(start + a.chunk_keys, n);
     const int nst = end > start ? (end - start + kKeys - 1) / kKeys : 0;
     // A full rolled window read before its shift: key i is cache row i + 1.
     const int roff = (a.key_set == KEYS_ROLL_SHIFT && c >= a.window) ? 1 : 0;
+    // After the pass the rolled window drops its sh oldest rows (rows sh.. move down
+    // by sh) and takes the ntok new entries after them: once full, sh = ntok.
+    const int sh = a.key_set == KEYS_ROLL_SHIFT ? max(0, min(c, a.window) + ntok - a.window) : 0;
     // New entries of the ntok tokens: values as scored (knew_t), V values (or
     // V codes' values for E4M3, vnew_t), codes, and per-row new-entry weights.
     uint8_t *mt_base = smem + S * kStage - kMtNewBytes;
@@ -886,8 +893,8 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     uint8_t *code_t = MT ? reinterpret_cast<uint8_t *>(vnew_t + kMaxTokens * kHeadDim) : code_s;
     const int vcode_off = MT ? kMaxTokens * kHeadDim : kHeadDim;                             // V codes
     constexpr int WN = MT ? kMaxTokens : 1;                                                  // wnew_t row stride
-    float *wnew_t = MT ? reinterpret_cast<float *>(code_t + 2 * kMaxTokens * kHeadDim) : misc + kMaxGroup;
-    float *rows_t = wnew_t + kMaxRows * kMaxTokens;   // MT: per-row sink, gate, scale [3][kMaxRows]
+    // MT: per-row sink, gate, scale [3][kMaxRows] past the per-row new-entry weights
+    float *rows_t = reinterpret_cast<float *>(code_t + 2 * kMaxTokens * kHeadDim) + kMaxRows * kMaxTokens;
     // Makes the new entries of the ntok tokens: the key rotated in fp64 and rounded
     // once to bf16, or quantised to E4M3 (fp64 rotation, one division, one
     // rounding; V too), each scored as stored; E4M3 V stays in code units.
@@ -956,43 +963,105 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     };
     // Test hook: stages from a.drop_stage on are never issued (a copy that never arrives).
     auto droppable = [&](int s) { return a.drop_stage >= 0 && s >= a.drop_stage; };
-    if (threadIdx.x == 0) {
+
+    // Round 1 of the prologue: every thread requests its share of q (bf16 rows,
+    // or fp32 rotated rows), the rotary row at position c and, for a
+    // single-token pass, the new entry, the sinks and the gate logits, into
+    // registers.  Then the thread that issues the copies initialises the
+    // barriers and sends the first stages: the small requests reach memory ahead
+    // of the stream, and the stream starts before they are back.
+    const bool has_new = a.new_kind != NEW_NONE;
+    // Where a single-token pass makes its new entry (rotation or quantisation,
+    // score): in the prologue of every CTA of a single-layer launch (whichever
+    // CTA combines then has it at hand, which shortens the layer's critical
+    // path), or -- in step grids, where throughput matters more than one
+    // layer's latency -- only in the CTA of a single-chunk sequence, the
+    // combining CTA of a longer one making it after its ticket.
+    constexpr bool kNewInEveryCta = NL == 1 || HD_STEP_NEW_IN_EVERY_CTA;
+    const bool new_early = !MT && has_new && (kNewInEveryCta || nchunks == 1 || clus > 1);
+    const int half = a.rotary_dim >> 1;
+    constexpr int kQLoads = (G * (kHeadDim / 4) + kNThreads - 1) / kNThreads;   // 16-byte q loads per thread
+    const int nq16 = a.q_bf16 ? G * (kHeadDim / 8) : G * (kHeadDim / 4);
+    uint4 qld[kQLoads];
+#pragma unroll
+    for (int k = 0; k < kQLoads; ++k) {
+        const int i = threadIdx.x + k * kNThreads;
+        if (i < nq16) {
+            qld[k] = a.q_bf16 ? reinterpret_cast<const uint4 *>(a.q_bf16 + qrow(i / (kHeadDim / 8)) * kHeadDim)[i % (kHeadDim / 8)]
+                              : reinterpret_cast<const uint4 *>(a.q_rot + qrow(i / (kHeadDim / 4)) * kHeadDim)[i % (kHeadDim / 4)];
+        }
+    }
+    static_assert(kNThreads >= kHeadDim / 2, "one rotary pair per thread");
+    const bool tab_ld = a.q_bf16 && !MT && (int)threadIdx.x < half;
+    float2 tld = make_float2(0.f, 0.f);
+    if (tab_ld) tld = a.table[(size_t)c * half + threadIdx.x];
+    // the new entry: 16-byte loads, the K row then the V row (bf16: 32 each; E4M3 codes: 16 each)
+    const bool codes_ld = KV == KV_FP8 && a.new_kind == NEW_STAGED;
+    const int new_ld = new_early ? (codes_ld ? 32 : 64) : 0;
+    uint4 nld = make_uint4(0u, 0u, 0u, 0u);
+    if ((int)threadIdx.x < new_ld) {
+        const int per = new_ld / 2, t = threadIdx.x;
+        const size_t e = ((size_t)b * a.num_kv_heads + kvh) * kHeadDim * (codes_ld ? 1 : 2);
+        const uint8_t *src = static_cast<const uint8_t *>(t < per ? a.new_k : a.new_v) + e;
+        nld = reinterpret_cast<const uint4 *>(src)[t % per];
+    }
+    float sld = 0.f, gld = 0.f;
+    if (!MT && (int)threadIdx.x < G) {
+        if (a.sink) sld = a.sink[kvh * G + threadIdx.x];
+        if (a.gate) gld = a.gate[(size_t)b * a.num_q_heads + kvh * G + threadIdx.x];
+    }
+
+    constexpr int kIssuer = own_producer(KV) ? CW * 32 : 0;
+    constexpr bool kIssueEarly = NL == 1 || HD_STEP_ISSUE_EARLY;
+    const int early = min(S, nst);   // stages issued before the prologue ends
+    if (threadIdx.x == kIssuer) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], CW);
             rel_s[s] = 0u;
         }
         fence_mbar_init();
+        if (kIssueEarly)
+            for (int s = 0; s < early && !droppable(s); ++s) issue_stage(s);
     }
-    // q of the group in log2 units.  Round 1: the raw q rows (16-byte loads),
-    // the rotary row at position c and, when this CTA will combine a single
-    // chunk, the combine's other inputs -- all requested at once.
-    const bool has_new = a.new_kind != NEW_NONE;
-    const int half = a.rotary_dim >> 1;
-    if (a.q_bf16) {
-        for (int i = threadIdx.x; i < G * (kHeadDim / 8); i += blockDim.x) {
-            const int r = i / (kHeadDim / 8), c8 = i % (kHeadDim / 8);
+
+    // Round 1 lands: q in shared memory as fp32, the rotary row, the new entry
+    // (bf16 values as fp32, or E4M3 codes), the sinks and the gate logits.
+#pragma unroll
+    for (int k = 0; k < kQLoads; ++k) {
+        const int i = threadIdx.x + k * kNThreads;
+        if (i < nq16) {
+            if (a.q_bf16) {
+                float f[8];
+                unpack_bf16x8(qld[k], f);
+                float4 *dst = reinterpret_cast<float4 *>(q_s) + 2 * i;
+                dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+                dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+            } else {
+                reinterpret_cast<uint4 *>(q_s)[i] = qld[k];
+            }
+        }
+    }
+    if (tab_ld) tab_s[threadIdx.x] = tld;
+    if ((int)threadIdx.x < new_ld) {
+        const int per = new_ld / 2, t = threadIdx.x;
+        if (codes_ld) {
+            reinterpret_cast<uint4 *>(code_s + (t < per ? 0 : kHeadDim))[t % per] = nld;
+        } else {
             float f[8];
-            unpack_bf16x8(*reinterpret_cast<const uint4 *>(a.q_bf16 + qrow(r) * kHeadDim + c8 * 8), f);
-            float4 *dst = reinterpret_cast<float4 *>(q_s + r * kHeadDim + c8 * 8);
+            unpack_bf16x8(nld, f);
+            float4 *dst = reinterpret_cast<float4 *>((t < per ? kraw_s : vnew_s) + (t % per) * 8);
             dst[0] = make_float4(f[0], f[1], f[2], f[3]);
             dst[1] = make_float4(f[4], f[5], f[6], f[7]);
         }
-        if (!MT)
-            for (int j = threadIdx.x; j < half; j += blockDim.x) tab_s[j] = a.table[(size_t)c * half + j];
-    } else {
-        for (int i = threadIdx.x; i < G * (kHeadDim / 4); i += blockDim.x)
-            reinterpret_cast<float4 *>(q_s)[i] =
-                reinterpret_cast<const float4 *>(a.q_rot + qrow(i / (kHeadDim / 4)) * kHeadDim)[i % (kHeadDim / 4)];
     }
-    if (!MT && nchunks == 1)
-        load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, misc + 2 * kMaxGroup,
-                                   misc + 3 * kMaxGroup, code_s);
+    if (!MT && (int)threadIdx.x < G) {
+        misc[2 * kMaxGroup + threadIdx.x] = sld;   // sink of row threadIdx.x
+        misc[3 * kMaxGroup + threadIdx.x] = gld;   // gate logit of row threadIdx.x
+    }
     __syncthreads();
-    // Folded producer: the first S stages go out once the prologue's loads are
-    // in (issued earlier, their traffic delayed those loads).
-    if (!own_producer(KV) && threadIdx.x == 0)
-        for (int s = 0; s < min(S, nst) && !droppable(s); ++s) issue_stage(s);
+    if (!kIssueEarly && threadIdx.x == kIssuer)
+        for (int s = 0; s < early && !droppable(s); ++s) issue_stage(s);
     // Round 2: rotate each rotary pair in place (fp32; q only feeds the scores)
     // and scale every dim to log2 units.
     if (a.q_bf16) {
@@ -1009,21 +1078,38 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     } else {
         for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) q_s[i] *= kQScale;
     }
-    // A single chunk is combined by this CTA: make its new entry now, while the
-    // first stages are in flight (its inputs arrived with q).
-    if (!MT && has_new && nchunks == 1) make_new_entries();
-    // MT ring layers: row r (token t) does not see the t oldest ring entries (the
-    // ones its window has passed); rows of a full layer see the whole cache.
+    // Single-token passes make the new entry here, in every CTA, while the first
+    // stages are in flight (its inputs arrived with q): whichever CTA combines
+    // the sequence then has it, and its score, at hand.
+    if (new_early) make_new_entries();
+    // MT sliding layers: row r (token t) does not see the oldest cached entries its
+    // window has passed -- t of them once the window is full: ring slots from the
+    // oldest one (slot c mod capacity), or the first keys of a rolled window read
+    // before its shift (both windows hold window - 1 scored entries); rows of a
+    // full layer see the whole cache.
     if (MT && threadIdx.x < G) {
         const int t = threadIdx.x / Gm;
+        const int held = a.key_set == KEYS_RING ? a.capacity : a.window - 1;
         mcnt_s[threadIdx.x] =
-            a.key_set == KEYS_RING ? (c >= a.capacity ? t : max(0, c + t - a.capacity)) : 0;
+            a.key_set == KEYS_RING || a.key_set == KEYS_ROLL_SHIFT ? (c >= held ? t : max(0, c + t - held)) : 0;
     }
     RowMask mask;
-    mask.first = c >= a.capacity ? c % a.capacity : 0;
+    mask.first = a.key_set == KEYS_RING && c >= a.capacity ? c % a.capacity : 0;
     mask.cap = a.capacity;
     mask.cnt = mcnt_s;
     __syncthreads();
+    // The new entry's score per query row (log2 units: q is pre-scaled), kept
+    // for the epilogue; the consumer warps take a row each.
+    float *wnew_t = MT ? reinterpret_cast<float *>(code_t + 2 * kMaxTokens * kHeadDim) : misc + kMaxGroup;
+    if (new_early && warp < CW) {
+        for (int h = warp; h < G; h += CW) {
+            float t = 0.f;
+            for (int d = lane; d < kHeadDim; d += 32) t = fmaf(q_s[h * kHeadDim + d], knew_t[d], t);
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+            if (lane == 0) wnew_t[h] = t;
+        }
+    }
 
     // Row groups: RG groups of CG rows; each group's WPG warps split every stage.
     constexpr int RG = G > 8 ? G / 8 : 1, CG = G / RG, WPG = CW / RG;
@@ -1032,7 +1118,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     float *red_l = red_m + CW * CG;
     if (own_producer(KV) && warp == CW) {
         if (lane == 0) {  // producer: one lane issues every load of the chunk
-            for (int s = 0; s < nst; ++s) {
+            for (int s = early; s < nst; ++s) {
                 if (droppable(s)) break;
                 const int slot = s % S;
                 if (s >= S && !mbar_wait(&empty[slot], ((s / S) - 1) & 1)) {
@@ -1070,12 +1156,15 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
                 if (nvalid > 0)
                     cons.consume(kst, kst + kBoxes * kv_box_bytes(KV), row0, nvalid, lane, start + s * kKeys + row0);
             }
-            if constexpr (NL > 1 && !MT) {
-                // Full rolled window: this warp's rows of the stage (cache rows key + 1)
-                // move down to rows key, before the slot is released.  Every row written
-                // was loaded by this or an earlier stage; later stages load higher rows.
-                // (Step grids are never launched as programmatic dependents, so these
-                // writes need no dependency wait.)
+            // Rolled window: this warp's rows of the stage (cache rows key + roff) move
+            // down by sh rows before the slot is released; rows below sh leave the
+            // window.  Every row written was loaded by this or an earlier stage; later
+            // stages load higher rows.  A single token moves a full window by one row
+            // (sh = roff); several tokens by the entries that leave it, which only the
+            // first row group writes (the groups read the same keys).  A layer kernel
+            // launched as a programmatic dependent follows another layer of the step,
+            // which never touches this cache, so these writes need no dependency wait.
+            if constexpr (!MT) {
                 if (roff) {
                     const int key0 = start + s * kKeys + kpart * kSpan;
                     const int nrows = min(kSpan, end - key0);
@@ -1089,6 +1178,25 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
                             kst + v * kBoxes * kv_box_bytes(KV) + tile_offset<KV>(kpart * kSpan + r, ch));
                         uint8_t *dst = static_cast<uint8_t *>(v ? a.cache_v : a.cache_k) + seq +
                                        (size_t)(key0 + r) * kHeadDim * kv_elem_bytes(KV) + 16 * ch;
+                        *reinterpret_cast<uint4 *>(dst) = x;
+                    }
+                }
+            } else {
+                if (sh > 0 && rg == 0) {
+                    const int key0 = start + s * kKeys + kpart * kSpan;
+                    const int nrows = min(kSpan, end - key0);
+                    constexpr int kChunks = kHeadDim * kv_elem_bytes(KV) / 16;
+                    const size_t seq = ((size_t)b * a.seq_stride + (size_t)kvh * a.capacity * kHeadDim) *
+                                       kv_elem_bytes(KV);
+                    for (int i = lane; i < 2 * nrows * kChunks; i += 32) {
+                        const int v = i >= nrows * kChunks, rem = i - v * nrows * kChunks;
+                        const int r = rem / kChunks, ch = rem % kChunks;
+                        const int row = key0 + r + roff;
+                        if (row < sh) continue;
+                        const uint4 x = *reinterpret_cast<const uint4 *>(
+                            kst + v * kBoxes * kv_box_bytes(KV) + tile_offset<KV>(kpart * kSpan + r, ch));
+                        uint8_t *dst = static_cast<uint8_t *>(v ? a.cache_v : a.cache_k) + seq +
+                                       (size_t)(row - sh) * kHeadDim * kv_elem_bytes(KV) + 16 * ch;
                         *reinterpret_cast<uint4 *>(dst) = x;
                     }
                 }
@@ -1116,43 +1224,233 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
         __syncthreads();
     }
 
+    // Per query row: this chunk's maximum M and sum L over the warps of the
+    // row's group, and each warp's weight 2^(m_w - M) (shared memory only).
+    // Partials: G rows per (sequence, kv head), num_kv_heads * G rows per sequence.
+    const size_t pbase = ((size_t)b * a.num_kv_heads * G + kvh * G) * a.max_chunks;
+    // this chunk's partial, the warp weights and the rows' lse sit past the warp buffers
+    constexpr int kRedBytes = (CW * CG * kHeadDim + 2 * CW * CG) * (int)sizeof(float);
+    constexpr int kOwnOff = kRedBytes <= kOwnPartialOffset ? kOwnPartialOffset : (kRedBytes + 1023) / 1024 * 1024;
+    static_assert(kOwnOff + G * (kHeadDim + 2 + WPG + 1 + kMaxCluster) * (int)sizeof(float) <= S * kStage - kMtNewBytes,
+                  "warp buffers, own partial and the multi-token entries fit the ring");
+    float *own_o = reinterpret_cast<float *>(smem + kOwnOff);   // [G][256]
+    float2 *own_ml = reinterpret_cast<float2 *>(own_o + G * kHeadDim);    // [G]
+    float *wwarp = reinterpret_cast<float *>(own_ml + G);                 // [G][WPG]
+    float *lse_s = wwarp + G * WPG;                                        // [G]
+    float *wclu = lse_s + G;                                               // [G][kMaxCluster] cluster weights
+    float *sink_s = MT ? rows_t : misc + 2 * kMaxGroup;                  // [G]
+    float *gate_s = MT ? rows_t + kMaxRows : misc + 3 * kMaxGroup;       // [G]
+    float *head_s = MT ? rows_t + 2 * kMaxRows : misc;   // [G] scale = sink factor * gate / L
+    // A single-token CTA of a single-layer launch holding the only chunk of its
+    // sequence finishes the rows itself: the new entry joins the maximum and the
+    // sum here.  (Step grids take the general combine below: the shorter path
+    // costs registers that their two-CTA-per-SM kernels do not have.)
+    const bool finish = NL == 1 && !MT && nchunks == 1 && clus <= 1;
+    if (threadIdx.x < G) {
+        const int h = threadIdx.x, w0 = (h / CG) * WPG, hr = h % CG;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = w0; w < w0 + WPG; ++w) M = fmaxf(M, red_m[w * CG + hr]);
+        const float s_new = finish && has_new ? wnew_t[h] : -INFINITY;
+        M = fmaxf(M, s_new);
+        float L = 0.f;
+#pragma unroll
+        for (int w = w0; w < w0 + WPG; ++w) {
+            const float m = red_m[w * CG + hr];
+            const float wt = (m == -INFINITY) ? 0.f : fast_exp2(m - M);
+            wwarp[h * WPG + (w - w0)] = wt;
+            L = fmaf(wt, red_l[w * CG + hr], L);
+        }
+        if (finish) {
+            const float w_new = has_new ? fast_exp2(s_new - M) : 0.f;
+            wnew_t[h] = w_new;
+            L += w_new;
+            const float lse = (M + fast_log2(L)) * kLn2;
+            // exp(lse) / (exp(lse) + exp(sink)) = 1 / (1 + 2^((sink - lse) * log2 e))
+            float f = a.sink ? 1.f / (1.f + fast_exp2((sink_s[h] - lse) * kLog2e)) : 1.f;
+            // output gate: sigmoid(g) = 1 / (1 + 2^(-g * log2 e)); lse is not gated
+            if (a.gate) f *= 1.f / (1.f + fast_exp2(-gate_s[h] * kLog2e));
+            head_s[h] = f / L * vscale;   // FP8: partials and the new value are in V-code units
+            lse_s[h] = lse;
+        } else {
+            own_ml[h] = make_float2(M, L);
+        }
+    }
+    __syncthreads();
+
+    // Stores the new entries now that every chunk of this (sequence, kv head) has read the cache.
+    auto store_new_entries = [&]() {
+        if (!has_new || a.commit == COMMIT_NONE) return;
+        for (int idx = threadIdx.x; idx < ntok * kHeadDim; idx += blockDim.x) {
+            const int t = idx / kHeadDim, d = idx % kHeadDim;
+            const int slot = a.commit == COMMIT_RING   ? (c + t) % a.capacity
+                             : a.commit == COMMIT_ROLL ? min(c, a.window) + t - sh
+                                                       : c + t;
+            const size_t o = (size_t)b * a.seq_stride + ((size_t)kvh * a.capacity + slot) * kHeadDim + d;
+            if (KV == KV_FP8) {
+                static_cast<uint8_t *>(a.cache_k)[o] = code_t[t * kHeadDim + d];
+                static_cast<uint8_t *>(a.cache_v)[o] = code_t[vcode_off + t * kHeadDim + d];
+            } else {  // exact: the values are bf16 values
+                static_cast<__nv_bfloat16 *>(a.cache_k)[o] = __float2bfloat16_rn(knew_t[t * kHeadDim + d]);
+                static_cast<__nv_bfloat16 *>(a.cache_v)[o] = __float2bfloat16_rn(vnew_t[t * kHeadDim + d]);
+            }
+        }
+    };
+    // Row h of the warps' outputs at dims [4 dq, 4 dq + 4), weighted by the warp weights.
+    const float4 *red_o4 = reinterpret_cast<const float4 *>(red_o);
+    auto warp_sum = [&](int h, int dq) -> float4 {
+        const int w0 = (h / CG) * WPG, hr = h % CG;
+        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < WPG; ++w) {
+            const float wt = wwarp[h * WPG + w];
+            const float4 v = red_o4[((w0 + w) * CG + hr) * (kHeadDim / 4) + dq];
+            o.x = fmaf(wt, v.x, o.x);
+            o.y = fmaf(wt, v.y, o.y);
+            o.z = fmaf(wt, v.z, o.z);
+            o.w = fmaf(wt, v.w, o.w);
+        }
+        return o;
+    };
+    auto store_out = [&](int h, int dq, const float (&o)[4]) {
+        const float sc = head_s[h];
+        __nv_bfloat16 r[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) r[i] = __float2bfloat16_rn(o[i] * sc);
+        uint2 packed;
+        packed.x = (uint32_t)__bfloat16_as_ushort(r[0]) | ((uint32_t)__bfloat16_as_ushort(r[1]) << 16);
+        packed.y = (uint32_t)__bfloat16_as_ushort(r[2]) | ((uint32_t)__bfloat16_as_ushort(r[3]) << 16);
+        *reinterpret_cast<uint2 *>(a.out + qrow(h) * kHeadDim + 4 * dq) = packed;
+    };
+
+    // (single-layer deep-ring launches only: the host sends clusters nowhere else)
+    if constexpr (NL == 1 && !MT && S * kStage > kStages * kStageBytes) {
+        if (clus > 1) {
+            // Cluster combine: CTA r of the cluster holds chunk r's partial in its
+            // shared memory.  After the cluster barrier every CTA reads all chunks'
+            // (m, l) pairs, forms the rows' maximum, weights, sum and lse (the new
+            // entry included), and merges its own slice of the dims from every
+            // chunk's partial -- all before the dependency wait, since none of it
+            // touches global memory; then it stores its slice of out, and rank 0
+            // stores lse and the new entry.  A last barrier keeps every CTA's
+            // shared memory alive until the others have read it.
+            for (int i = threadIdx.x; i < G * (kHeadDim / 4); i += blockDim.x)
+                reinterpret_cast<float4 *>(own_o)[i] = warp_sum(i / (kHeadDim / 4), i % (kHeadDim / 4));
+            cluster_sync_all();
+            const int rank = chunk;   // the cluster spans the chunk dimension
+            if (threadIdx.x < G) {
+                const int h = threadIdx.x;
+                float2 ml_r[kMaxCluster];
+                float M = has_new ? wnew_t[h] : -INFINITY;
+#pragma unroll
+                for (int r = 0; r < kMaxCluster; ++r) {
+                    ml_r[r] = make_float2(-INFINITY, 0.f);
+                    if (r < clus) ml_r[r] = ld_dsmem_f2(dsmem_addr(own_ml + h, r));
+                    M = fmaxf(M, ml_r[r].x);
+                }
+                float L = 0.f;
+#pragma unroll
+                for (int r = 0; r < kMaxCluster; ++r) {
+                    const float w = (ml_r[r].x == -INFINITY) ? 0.f : fast_exp2(ml_r[r].x - M);
+                    if (r < clus) wclu[h * kMaxCluster + r] = w;
+                    L = fmaf(w, ml_r[r].y, L);
+                }
+                const float w_new = has_new ? fast_exp2(wnew_t[h] - M) : 0.f;
+                L += w_new;
+                wnew_t[h] = w_new;
+                const float lse = (M + fast_log2(L)) * kLn2;
+                float f = a.sink ? 1.f / (1.f + fast_exp2((sink_s[h] - lse) * kLog2e)) : 1.f;
+                if (a.gate) f *= 1.f / (1.f + fast_exp2(-gate_s[h] * kLog2e));
+                head_s[h] = f / L * vscale;
+                lse_s[h] = lse;
+            }
+            __syncthreads();
+            // this CTA's float4 columns of every row
+            const int col0 = rank * (kHeadDim / 4) / clus, col1 = (rank + 1) * (kHeadDim / 4) / clus;
+            const int ncol = col1 - col0;
+            constexpr int kTasks = (G * (kHeadDim / 8) + kNThreads - 1) / kNThreads;   // clusters have >= 2 CTAs
+            float res[kTasks][4];
+#pragma unroll
+            for (int k = 0; k < kTasks; ++k) {
+                const int i = threadIdx.x + k * kNThreads;
+                if (i < G * ncol) {
+                    const int h = i / ncol, dq = col0 + i % ncol;
+                    float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+                    for (int r = 0; r < clus; ++r) {
+                        const float w = wclu[h * kMaxCluster + r];
+                        const float4 v = ld_dsmem_f4(dsmem_addr(reinterpret_cast<const float4 *>(own_o) + h * 64 + dq, r));
+                        o.x = fmaf(w, v.x, o.x);
+                        o.y = fmaf(w, v.y, o.y);
+                        o.z = fmaf(w, v.z, o.z);
+                        o.w = fmaf(w, v.w, o.w);
+                    }
+                    if (has_new) {
+                        const float wn = wnew_t[h];
+                        const float4 vn = reinterpret_cast<const float4 *>(vnew_t)[dq];
+                        o.x = fmaf(wn, vn.x, o.x);
+                        o.y = fmaf(wn, vn.y, o.y);
+                        o.z = fmaf(wn, vn.z, o.z);
+                        o.w = fmaf(wn, vn.w, o.w);
+                    }
+                    res[k][0] = o.x;
+                    res[k][1] = o.y;
+                    res[k][2] = o.z;
+                    res[k][3] = o.w;
+                }
+            }
+            asm volatile("griddepcontrol.wait;" ::: "memory");
+#pragma unroll
+            for (int k = 0; k < kTasks; ++k) {
+                const int i = threadIdx.x + k * kNThreads;
+                if (i < G * ncol) store_out(i / ncol, col0 + i % ncol, res[k]);
+            }
+            if (rank == 0) {
+                if (threadIdx.x < G) a.lse[qrow(threadIdx.x)] = lse_s[threadIdx.x];
+                store_new_entries();
+            }
+            cluster_sync_all();
+            return;
+        }
+    }
+
     // Everything above only read this layer's own inputs and cache.  The first
     // global write (partials, tickets, outputs, the stored entry) waits for the
     // previous grid in the stream to complete and its writes to be visible.
     asm volatile("griddepcontrol.wait;" ::: "memory");
 
-    // Merge the warps into this chunk's partial: kept in shared memory (past the
-    // warp buffers) and, when the sequence has several chunks, written out.
-    // Partials: G rows per (sequence, kv head), num_kv_heads * G rows per sequence.
-    const size_t pbase = ((size_t)b * a.num_kv_heads * G + kvh * G) * a.max_chunks;
-    // this chunk's partial sits past the warp buffers
-    constexpr int kRedBytes = (CW * CG * kHeadDim + 2 * CW * CG) * (int)sizeof(float);
-    constexpr int kOwnOff = kRedBytes <= kOwnPartialOffset ? kOwnPartialOffset : (kRedBytes + 1023) / 1024 * 1024;
-    static_assert(kOwnOff + G * (kHeadDim + 2) * (int)sizeof(float) <= S * kStage - kMtNewBytes,
-                  "warp buffers, own partial and the multi-token entries fit the ring");
-    float *own_o = reinterpret_cast<float *>(smem + kOwnOff);   // [G][256]
-    float2 *own_ml = reinterpret_cast<float2 *>(own_o + G * kHeadDim);    // [G]
-    for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) {
-        const int h = i / kHeadDim, d = i % kHeadDim;
-        const int w0 = (h / CG) * WPG, hr = h % CG;   // the warps of this row's group, its row there
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = w0; w < w0 + WPG; ++w) M = fmaxf(M, red_m[w * CG + hr]);
-        float o = 0.f, L = 0.f;
-#pragma unroll
-        for (int w = w0; w < w0 + WPG; ++w) {
-            const float wt = (M == -INFINITY) ? 0.f : fast_exp2(red_m[w * CG + hr] - M);
-            o = fmaf(wt, red_o[(w * CG + hr) * kHeadDim + d], o);
-            L = fmaf(wt, red_l[w * CG + hr], L);
+    if (finish) {
+        // out = (sum of the warps' weighted rows + w_new * v_new) * scale, lse, the new entry.
+        for (int i = threadIdx.x; i < G * (kHeadDim / 4); i += blockDim.x) {
+            const int h = i / (kHeadDim / 4), dq = i % (kHeadDim / 4);
+            const float4 o4 = warp_sum(h, dq);
+            float o[4] = {o4.x, o4.y, o4.z, o4.w};
+            if (has_new) {
+                const float wn = wnew_t[h];
+                const float4 vn = reinterpret_cast<const float4 *>(vnew_t)[dq];
+                o[0] = fmaf(wn, vn.x, o[0]);
+                o[1] = fmaf(wn, vn.y, o[1]);
+                o[2] = fmaf(wn, vn.z, o[2]);
+                o[3] = fmaf(wn, vn.w, o[3]);
+            }
+            store_out(h, dq, o);
         }
-        own_o[i] = o;
-        if (d == 0) own_ml[h] = make_float2(M, L);
-        if (nchunks > 1) {
-            const size_t pi = pbase + (size_t)h * a.max_chunks + chunk;
-            __stcg(a.part_o + pi * kHeadDim + d, o);
-            if (d == 0) __stcg(reinterpret_cast<float2 *>(a.part_ml) + pi, make_float2(M, L));
-        }
+        if (threadIdx.x < G) a.lse[qrow(threadIdx.x)] = lse_s[threadIdx.x];
+        store_new_entries();
+        return;
     }
+
+    // This chunk's partial: kept in shared memory (a multi-token pass with one
+    // chunk combines from it) and, when the sequence has several chunks, written out.
+    for (int i = threadIdx.x; i < G * (kHeadDim / 4); i += blockDim.x) {
+        const int h = i / (kHeadDim / 4), dq = i % (kHeadDim / 4);
+        const float4 o4 = warp_sum(h, dq);
+        reinterpret_cast<float4 *>(own_o)[i] = o4;
+        if (nchunks > 1)
+            __stcg(reinterpret_cast<float4 *>(a.part_o) + (pbase + (size_t)h * a.max_chunks + chunk) * (kHeadDim / 4) + dq,
+                   o4);
+    }
+    if (nchunks > 1 && threadIdx.x < G)
+        __stcg(a.part_ml + pbase + (size_t)threadIdx.x * a.max_chunks + chunk, own_ml[threadIdx.x]);
     __syncthreads();
 
     // Ticket: the last chunk of this (sequence, kv head) to finish does the combine.
@@ -1172,13 +1470,9 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     }
 
     // ---- combine (one CTA per sequence and kv head) ----
-    // Every global input of the combine is requested in one round: the new
-    // entry, its rotary row, the sink and the gate logits (unless the prologue
-    // fetched them), and each warp's chunk maxima and sums.
-    float *sink_s = MT ? rows_t : misc + 2 * kMaxGroup;                  // [G]
-    float *gate_s = MT ? rows_t + kMaxRows : misc + 3 * kMaxGroup;       // [G]
-    if (!MT && nchunks > 1)
-        load_combine_inputs<G, KV>(a, b, kvh, c, kraw_s, vnew_s, tab_s, sink_s, gate_s, code_s);
+    // A single-token pass made its new entry, its scores, sink and gate values
+    // in the prologue; a multi-token pass reads and makes them here, with each
+    // warp's chunk maxima and sums requested in the same round.
     if (MT && threadIdx.x < G) {   // per row: the sink of its head, the gate logit of its token and head
         sink_s[threadIdx.x] = a.sink ? a.sink[kvh * Gm + threadIdx.x % Gm] : 0.f;
         gate_s[threadIdx.x] = a.gate ? a.gate[qrow(threadIdx.x)] : 0.f;
@@ -1196,18 +1490,33 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
             if (j < nchunks) ml[r] = nchunks == 1 ? own_ml[h] : __ldcg(pml + ph + j);
         }
     }
-    __syncthreads();
-    if (has_new && (MT || nchunks > 1)) {   // a single chunk's entry was made in the prologue
-        make_new_entries();
-        __syncthreads();
+    // New entries made here: a multi-token pass's, or a step grid's longer sequence's.
+    const bool new_late = has_new && !new_early;
+    if (!MT && new_late && (int)threadIdx.x < (codes_ld ? 32 : 64)) {
+        const int per = codes_ld ? 16 : 32, t = threadIdx.x;
+        const size_t e = ((size_t)b * a.num_kv_heads + kvh) * kHeadDim * (codes_ld ? 1 : 2);
+        const uint4 x = reinterpret_cast<const uint4 *>(static_cast<const uint8_t *>(t < per ? a.new_k : a.new_v) + e)[t % per];
+        if (codes_ld) {
+            reinterpret_cast<uint4 *>(code_s + (t < per ? 0 : kHeadDim))[t % per] = x;
+        } else {
+            float f[8];
+            unpack_bf16x8(x, f);
+            float4 *dst = reinterpret_cast<float4 *>((t < per ? kraw_s : vnew_s) + (t % per) * 8);
+            dst[0] = make_float4(f[0], f[1], f[2], f[3]);
+            dst[1] = make_float4(f[4], f[5], f[6], f[7]);
+        }
     }
-    // Per head: M = max(chunk maxima, new score), chunk weights 2^(m_j - M) and
-    // L = sum of weighted chunk sums (+ the new entry).  Warp w takes heads w, w + warps, ...
+    if (new_late) {
+        __syncthreads();
+        make_new_entries();
+    }
+    __syncthreads();
+    // Per row: M = max(chunk maxima, new scores), chunk weights 2^(m_j - M) and
+    // L = sum of weighted chunk sums (+ the new entries).  Warp w takes rows w, w + warps, ...
     float *wts = reinterpret_cast<float *>(smem);   // [G][nchunks] (the warp buffers are free)
-    float *head_s = MT ? rows_t + 2 * kMaxRows : misc;   // [G] scale = sink factor * gate / L
     for (int h = warp; h < G; h += kNThreads / 32) {
         const size_t ph = pbase + (size_t)h * a.max_chunks;
-        if (h != warp) {  // a second head for this warp: its pairs were not preloaded
+        if (h != warp) {  // a second row for this warp: its pairs were not preloaded
 #pragma unroll
             for (int r = 0; r < kPerLane; ++r) {
                 const int j = lane + 32 * r;
@@ -1219,14 +1528,18 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
         const int th = MT ? h / Gm : 0;
         float s_new = -INFINITY;
         if (has_new) {
-            for (int j = 0; j <= th; ++j) {
-                float t = 0.f;
-                for (int d = lane; d < kHeadDim; d += 32)
-                    t = fmaf(q_s[h * kHeadDim + d], knew_t[j * kHeadDim + d], t);
+            if (!new_late) {
+                s_new = wnew_t[h];   // scored in the prologue
+            } else {
+                for (int j = 0; j <= th; ++j) {
+                    float t = 0.f;
+                    for (int d = lane; d < kHeadDim; d += 32)
+                        t = fmaf(q_s[h * kHeadDim + d], knew_t[j * kHeadDim + d], t);
 #pragma unroll
-                for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
-                if (lane == 0) wnew_t[h * WN + j] = t;
-                s_new = fmaxf(s_new, t);
+                    for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+                    if (lane == 0) wnew_t[h * WN + j] = t;
+                    s_new = fmaxf(s_new, t);
+                }
             }
             __syncwarp();
         }
@@ -1263,17 +1576,16 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
         L += w_new;
         if (lane == 0) {
             const float lse = (M + fast_log2(L)) * kLn2;
-            // exp(lse) / (exp(lse) + exp(sink)) = 1 / (1 + 2^((sink - lse) * log2 e))
             float f = a.sink ? 1.f / (1.f + fast_exp2((sink_s[h] - lse) * kLog2e)) : 1.f;
-            // output gate: sigmoid(g) = 1 / (1 + 2^(-g * log2 e)); lse is not gated
             if (a.gate) f *= 1.f / (1.f + fast_exp2(-gate_s[h] * kLog2e));
             head_s[h] = f / L * vscale;   // FP8: partials and the new value are in V-code units
             a.lse[qrow(h)] = lse;
         }
     }
     __syncthreads();
-    // Outputs: thread t < 128 owns dims [4*(t%64), +4) of every head for the
-    // chunks of parity t/64; the two parities meet in shared memory.
+    // Outputs: thread t < 128 owns dims [4*(t%64), +4) of every row for the
+    // chunks of parity t/64, several chunks' loads in flight at once; the two
+    // parities meet in shared memory.
     float4 *half_s = reinterpret_cast<float4 *>(wts + ((G * nchunks + 3) & ~3));   // [G][64], 16-byte aligned
     const int dq = threadIdx.x & 63, parity = threadIdx.x >> 6;
     float4 acc[G];
@@ -1290,7 +1602,26 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
         }
     } else if (parity < 2) {
         const float4 *po = reinterpret_cast<const float4 *>(a.part_o) + pbase * (kHeadDim / 4) + dq;
-        for (int j = parity; j < nchunks; j += 2) {
+        constexpr int U = G >= 16 ? 1 : (G >= 8 ? 2 : 4);   // chunks per round of loads
+        int j = parity;
+        for (; j + 2 * (U - 1) < nchunks; j += 2 * U) {
+            float4 v[U][G];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int h = 0; h < G; ++h) v[u][h] = __ldcg(po + ((size_t)h * a.max_chunks + j + 2 * u) * (kHeadDim / 4));
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float w = wts[h * nchunks + j + 2 * u];
+                    acc[h].x = fmaf(w, v[u][h].x, acc[h].x);
+                    acc[h].y = fmaf(w, v[u][h].y, acc[h].y);
+                    acc[h].z = fmaf(w, v[u][h].z, acc[h].z);
+                    acc[h].w = fmaf(w, v[u][h].w, acc[h].w);
+                }
+        }
+        for (; j < nchunks; j += 2) {
 #pragma unroll
             for (int h = 0; h < G; ++h) {
                 const float w = wts[h * nchunks + j];
@@ -1312,7 +1643,6 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
         for (int h = 0; h < G; ++h) {
             const float4 o1 = half_s[h * 64 + dq];
             float o[4] = {acc[h].x + o1.x, acc[h].y + o1.y, acc[h].z + o1.z, acc[h].w + o1.w};
-            const float sc = head_s[h];
             if (has_new) {
                 const int th = MT ? h / Gm : 0;
                 for (int j = 0; j <= th; ++j) {
@@ -1324,32 +1654,10 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
                     o[3] = fmaf(wn, vn.w, o[3]);
                 }
             }
-            __nv_bfloat16 r[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) r[i] = __float2bfloat16_rn(o[i] * sc);
-            uint2 packed;
-            packed.x = (uint32_t)__bfloat16_as_ushort(r[0]) | ((uint32_t)__bfloat16_as_ushort(r[1]) << 16);
-            packed.y = (uint32_t)__bfloat16_as_ushort(r[2]) | ((uint32_t)__bfloat16_as_ushort(r[3]) << 16);
-            *reinterpret_cast<uint2 *>(a.out + qrow(h) * kHeadDim + 4 * dq) = packed;
+            store_out(h, dq, o);
         }
     }
-    // Store the new entries now that every chunk of this (sequence, kv head) has read the cache.
-    if (has_new && a.commit != COMMIT_NONE) {
-        for (int idx = threadIdx.x; idx < ntok * kHeadDim; idx += blockDim.x) {
-            const int t = idx / kHeadDim, d = idx % kHeadDim;
-            const int slot = a.commit == COMMIT_RING   ? (c + t) % a.capacity
-                             : a.commit == COMMIT_ROLL ? min(c, a.window - 1)
-                                                       : c + t;
-            const size_t o = (size_t)b * a.seq_stride + ((size_t)kvh * a.capacity + slot) * kHeadDim + d;
-            if (KV == KV_FP8) {
-                static_cast<uint8_t *>(a.cache_k)[o] = code_t[t * kHeadDim + d];
-                static_cast<uint8_t *>(a.cache_v)[o] = code_t[vcode_off + t * kHeadDim + d];
-            } else {  // exact: the values are bf16 values
-                static_cast<__nv_bfloat16 *>(a.cache_k)[o] = __float2bfloat16_rn(knew_t[t * kHeadDim + d]);
-                static_cast<__nv_bfloat16 *>(a.cache_v)[o] = __float2bfloat16_rn(vnew_t[t * kHeadDim + d]);
-            }
-        }
-    }
+    store_new_entries();
 }
 
 template <int G, int CONSUMER, int S, int KV, bool MT, int NL>
@@ -1360,6 +1668,9 @@ cudaError_t launch_g(const LaunchTable<NL> &p, dim3 grid, bool pdl, cudaStream_t
     if (!done_on_device(configured, &device)) {
         cudaError_t e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER, S, KV, MT, NL>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e == cudaSuccess && NL == 1)   // clusters of up to 16 CTAs (single-layer launches)
+            e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER, S, KV, MT, NL>,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
         if (e != cudaSuccess) return e;
         mark_done_on_device(configured, device);
     }
@@ -1368,12 +1679,54 @@ cudaError_t launch_g(const LaunchTable<NL> &p, dim3 grid, bool pdl, cudaStream_t
     cfg.blockDim = dim3(layer_threads(G, KV));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchAttribute attr[2];
+    int n = 0;
+    if (pdl) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n++].val.programmaticStreamSerializationAllowed = 1;
+    }
+    if (NL == 1 && p.layer[0].a.cluster > 1) {
+        if (MT || S * kv_stage_bytes(KV) <= kStages * kStageBytes || grid.x != (unsigned)p.layer[0].a.cluster ||
+            p.layer[0].a.cluster > kMaxCluster)
+            return cudaErrorInvalidValue;
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = (unsigned)p.layer[0].a.cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n++].val.clusterDim.z = 1;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = pdl ? 1 : 0;
+    cfg.numAttrs = n;
     return cudaLaunchKernelEx(&cfg, attn_layer_kernel<G, CONSUMER, S, KV, MT, NL>, p);
+}
+
+// Largest cluster size (16, then 8) with which the single-layer deep-ring kernel
+// (tensor-core consumer, one token) fits at least one cluster on the device; 0 if
+// neither does.
+template <int G, int KV>
+int cluster_limit_g() {
+    constexpr int S = kDeepStages * kStageBytes / kv_stage_bytes(KV);
+    auto kernel = attn_layer_kernel<G, CONSUMER_MMA, S, KV, false, 1>;
+    const size_t smem = layer_smem_bytes(G, kDeepStages);
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess ||
+        cudaFuncSetAttribute(kernel, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        return 0;
+    for (int k : {kMaxCluster, 8}) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(k, 1, 1);
+        cfg.blockDim = dim3(layer_threads(G, KV));
+        cfg.dynamicSmemBytes = smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)k;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kernel, &cfg) == cudaSuccess && clusters > 0) return k;
+        cudaGetLastError();   // clear a refused query
+    }
+    return 0;
 }
 
 // S counts stages of the cache's type: an E4M3 ring has twice the bf16 count.

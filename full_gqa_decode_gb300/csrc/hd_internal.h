@@ -64,16 +64,25 @@ void plan_split(int64_t batch, int64_t num_kv_heads, int64_t max_keys, int64_t n
                 int64_t max_slots, int32_t *chunk_keys, int32_t *num_chunks, int32_t *stages = nullptr,
                 int64_t chunk_max = kChunkMax);
 
+// Shared memory of the combine: a weight per (query row, chunk) plus a float4
+// row per query row (and, for a multi-token pass, the new entries), inside the
+// stage ring of `stages` bf16 stages that the CTA no longer needs then.
+inline bool combine_fits(size_t rows, int64_t num_chunks, bool mt, int stages) {
+    return (rows * num_chunks + 3) * sizeof(float) + rows * 64 * 16 + (mt ? kMtNewBytes : 0) <=
+           (size_t)stages * kStageBytes;
+}
+
 // Which cache rows the split pass scores for sequence b with c = context[b].
 enum KeySet : int32_t {
     KEYS_RING = 0,         // ring slots [0, min(c, capacity)); the new entry is scored apart
     KEYS_ROLL = 1,         // rolled window [0, min(c + 1, window)), the new entry already in it
     KEYS_FULL_CACHED = 2,  // positions [0, c]: the new entry was appended at index c
     KEYS_FULL_PREV = 3,    // positions [0, c): the new entry is scored apart and appended
-    KEYS_ROLL_SHIFT = 4    // rolled window before this step's shift: rows [0, c) while it is not
-                           // full, else rows [1, window) (row 0 leaves the window); the new entry
-                           // is scored apart, the kernel shifts the rows it read down by one and
-                           // stores the new entry at row min(c, window - 1); one chunk per sequence
+    KEYS_ROLL_SHIFT = 4    // rolled window before this pass's shift: rows [0, c) while it is not
+                           // full, else rows [1, window) (row 0 leaves the window); the new entries
+                           // are scored apart, the kernel shifts the rows it read down by
+                           // sh = max(0, min(c, window) + tokens - window) rows and stores token t's
+                           // entry at row min(c, window) + t - sh; one chunk per sequence
 };
 // Where the new entry comes from when it is scored apart from the cache.
 enum NewEntry : int32_t {
@@ -120,6 +129,10 @@ struct LayerArgs {
     // positions context + token0 + t; q/k/v/out/lse/gate then carry a token index
     // after the batch index.
     int32_t tokens, token0, total_tokens;
+    // Single-layer launches only: > 1 when the grid runs in thread-block clusters of
+    // that many CTAs along the chunk dimension (every chunk of a (sequence, kv head)
+    // in one cluster), whose partials then merge through distributed shared memory.
+    int32_t cluster;
 };
 
 // Partial RoPE of q and the new k, and the K/V store.
@@ -186,5 +199,10 @@ cudaError_t launch_layer_fp8(const LaunchTable<1> &t, dim3 grid, int rows, bool 
 cudaError_t launch_step_bf16(const StepTable &t, dim3 grid, int rows, bool mt, int stages, cudaStream_t s);
 cudaError_t launch_step_fp8(const StepTable &t, dim3 grid, int rows, bool mt, int stages, cudaStream_t s);
 size_t layer_smem_bytes(int group, int stages);
+// Largest cluster (16 or 8 CTAs, 0 if none) that single-layer launches of the
+// deep-ring kernel for this group and cache type can run with on the current device.
+int layer_cluster_limit(int group, int kv);
+int layer_cluster_limit_fp8(int group);
+constexpr int kMaxCluster = 16;
 
 }  // namespace hd

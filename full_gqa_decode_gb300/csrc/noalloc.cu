@@ -16,10 +16,12 @@
 // (different streams, or different host threads without ordering) race on it
 // and give wrong results; order such calls on one stream.
 //
-// Setup: the first call on a device, with that device current, looks up the
-// array's device address with cudaGetSymbolAddress and caches it for that
-// device (in host code the array's name is only a host-side stand-in, not a
-// device address).  Make that first call before any stream capture.
+// Setup: the first call in a CUDA context (per device, with that device
+// current) looks up the array's device address with cudaGetSymbolAddress and
+// caches it together with the context's id (in host code the array's name is
+// only a host-side stand-in, not a device address).  A context that was torn
+// down and made again (cudaDeviceReset) has a new id, so its first call looks
+// the address up again.  Make the first call before any stream capture.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -28,7 +30,7 @@
 
 namespace {
 
-constexpr size_t kScratchBytes = 64ull << 20;  // 64 MiB
+constexpr size_t kScratchBytes = HD_STATIC_SCRATCH_BYTES;
 constexpr int kMaxDevices = 64;
 
 // Chunk partials (o, then (m, l)), then the per-(sequence, kv head) tickets and
@@ -36,33 +38,63 @@ constexpr int kMaxDevices = 64;
 // word are cleared again before every launch.
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
+struct ScratchAddress {
+    unsigned long long context_id = 0;
+    void *ptr = nullptr;
+};
 std::mutex g_mutex;
-void *g_scratch_ptr[kMaxDevices] = {};
+ScratchAddress g_scratch_addr[kMaxDevices];
+
+template <class F>
+F driver_entry(const char *name, int version) {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion(name, &p, version, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+        return reinterpret_cast<F>(p);
+    return nullptr;
+}
+
+// Id of the current CUDA context (0 when none is current yet or it cannot be read).
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        get_current = driver_entry<PFN_cuCtxGetCurrent_v4000>("cuCtxGetCurrent", 4000);
+        get_id = driver_entry<PFN_cuCtxGetId_v12000>("cuCtxGetId", 12000);
+    });
+    if (!get_current || !get_id) return 0;
+    CUcontext c = nullptr;
+    unsigned long long id = 0;
+    if (get_current(&c) != CUDA_SUCCESS || !c || get_id(c, &id) != CUDA_SUCCESS) return 0;
+    return id;
+}
 
 hd_status scratch_for_current_device(unsigned char **ptr) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return HD_ERR_STATE;
+    const unsigned long long id = current_context_id();
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (!g_scratch_ptr[dev]) {
+    ScratchAddress &e = g_scratch_addr[dev];
+    if (!e.ptr || id == 0 || e.context_id != id) {
+        // The lookup binds the device's primary context if none is current yet.
         void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) return HD_ERR_CUDA;
-        g_scratch_ptr[dev] = p;
+        if (cudaGetSymbolAddress(&p, g_scratch) != cudaSuccess || p == nullptr) {
+            e = ScratchAddress{};
+            return HD_ERR_CUDA;
+        }
+        e.ptr = p;
+        e.context_id = current_context_id();
     }
-    *ptr = static_cast<unsigned char *>(g_scratch_ptr[dev]);
+    *ptr = static_cast<unsigned char *>(e.ptr);
     return HD_OK;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
+    std::call_once(once, [] { fn = driver_entry<PFN_cuTensorMapEncodeTiled_v12000>("cuTensorMapEncodeTiled", 12000); });
     return fn;
 }
 
@@ -83,7 +115,49 @@ bool encode(CUtensorMap *map, const void *base, const hd_kv_cache &c, int num_kv
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15) == 0; }
 
+// Scratch layout of one call: partial outputs, then (m, l) pairs, then the
+// tickets and the error word.
+struct ScratchPlan {
+    int32_t chunk_keys = 0, num_chunks = 0, stages = hd::kStages;
+    size_t o_bytes = 0, ml_bytes = 0, ctr_bytes = 0, total = 0;
+};
+
+hd_status plan_scratch(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads, int32_t max_context,
+                       int32_t num_sms, ScratchPlan *p) {
+    if (batch <= 0 || batch > 65535 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0 || max_context < 0 || max_context == INT32_MAX || num_sms <= 0)
+        return HD_ERR_INVALID_ARG;
+    const int group = num_q_heads / num_kv_heads;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return HD_ERR_UNSUPPORTED;
+    // Chunks no larger in number than the array can hold at the largest chunk size.
+    const int64_t per_slot = (int64_t)num_q_heads * (hd::kHeadDim * sizeof(float) + sizeof(float2));
+    hd::plan_split(batch, num_kv_heads, (int64_t)max_context + 1, num_sms, (int64_t)(kScratchBytes / 2) / per_slot,
+                   &p->chunk_keys, &p->num_chunks, &p->stages);
+    const size_t slots = (size_t)batch * num_q_heads * p->num_chunks;
+    p->o_bytes = slots * hd::kHeadDim * sizeof(float);
+    p->ml_bytes = slots * sizeof(float2);
+    p->ctr_bytes = (size_t)batch * num_kv_heads * sizeof(int32_t);
+    p->total = p->o_bytes + p->ml_bytes + p->ctr_bytes + sizeof(int32_t);
+    if (p->total > kScratchBytes) return HD_ERR_CAPACITY;
+    if (!hd::combine_fits((size_t)group, p->num_chunks, false, p->stages)) return HD_ERR_CAPACITY;
+    return HD_OK;
+}
+
 }  // namespace
+
+extern "C" hd_status decode_attn_full_static_scratch_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                                          int32_t max_context, int32_t num_sms,
+                                                          int64_t *scratch_bytes, int32_t *chunk_keys,
+                                                          int32_t *num_chunks) {
+    ScratchPlan p;
+    const hd_status st = plan_scratch(batch, num_q_heads, num_kv_heads, max_context, num_sms, &p);
+    if (st == HD_OK || st == HD_ERR_CAPACITY) {
+        if (scratch_bytes) *scratch_bytes = (int64_t)p.total;
+        if (chunk_keys) *chunk_keys = p.chunk_keys;
+        if (num_chunks) *num_chunks = p.num_chunks;
+    }
+    return st;
+}
 
 extern "C" hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                                      const int32_t *context, int32_t max_context,
@@ -91,14 +165,10 @@ extern "C" hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_
                                                      const float *sink, void *out, float *lse,
                                                      void *stream) {
     // Arguments (host checks, before anything touches the device).
-    if (batch <= 0 || batch > 65535 || num_q_heads <= 0 || num_kv_heads <= 0 ||
-        num_q_heads % num_kv_heads != 0)
-        return HD_ERR_INVALID_ARG;
-    const int group = num_q_heads / num_kv_heads;
-    if (group != 1 && group != 2 && group != 4 && group != 8) return HD_ERR_UNSUPPORTED;
     if (!context || !q_rot || !out || !lse || !aligned16(q_rot)) return HD_ERR_INVALID_ARG;
     if (!cache.k || !cache.v || !aligned16(cache.k) || !aligned16(cache.v) || cache.capacity <= 0 ||
-        cache.seq_stride % 8 != 0 || cache.seq_stride < (int64_t)num_kv_heads * cache.capacity * hd::kHeadDim)
+        cache.seq_stride % 8 != 0 || num_kv_heads <= 0 ||
+        cache.seq_stride < (int64_t)num_kv_heads * cache.capacity * hd::kHeadDim)
         return HD_ERR_INVALID_ARG;
     if (cache.k_scale || cache.v_scale) return HD_ERR_UNSUPPORTED;   // bf16 caches only
     if (max_context < 0) return HD_ERR_INVALID_ARG;
@@ -108,24 +178,10 @@ extern "C" hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_
     if (cudaGetDevice(&device) != cudaSuccess ||
         cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
         return HD_ERR_STATE;
-    int32_t chunk_keys = 0, num_chunks = 0;
-    hd_status st = HD_OK;
-    // Chunks no larger in number than the array can hold at the largest chunk size.
-    const int64_t per_slot = (int64_t)num_q_heads * (hd::kHeadDim * sizeof(float) + sizeof(float2));
-    int32_t stages = hd::kStages;
-    hd::plan_split(batch, num_kv_heads, max_context + 1, num_sms, (int64_t)(kScratchBytes / 2) / per_slot,
-                   &chunk_keys, &num_chunks, &stages);
-
-    // Scratch layout and the size limit: calls needing more than the array are refused.
-    const size_t slots = (size_t)batch * num_q_heads * num_chunks;
-    const size_t o_bytes = slots * hd::kHeadDim * sizeof(float);
-    const size_t ml_bytes = slots * sizeof(float2);
-    const size_t ctr_bytes = (size_t)batch * num_kv_heads * sizeof(int32_t);
-    const size_t need = o_bytes + ml_bytes + ctr_bytes + sizeof(int32_t);
-    if (need > kScratchBytes) return HD_ERR_CAPACITY;
-    if (((size_t)group * num_chunks + 3) * sizeof(float) + (size_t)group * 64 * 16 >
-        (size_t)hd::kStages * hd::kStageBytes)
-        return HD_ERR_CAPACITY;
+    // The split plan and the size limit: calls needing more than the array are refused.
+    ScratchPlan plan;
+    hd_status st = plan_scratch(batch, num_q_heads, num_kv_heads, max_context, num_sms, &plan);
+    if (st != HD_OK) return st;
 
     unsigned char *scratch = nullptr;
     if ((st = scratch_for_current_device(&scratch)) != HD_OK) return st;
@@ -134,8 +190,8 @@ extern "C" hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_
         return HD_ERR_CUDA;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    int32_t *counters = reinterpret_cast<int32_t *>(scratch + o_bytes + ml_bytes);
-    if (cudaMemsetAsync(counters, 0, ctr_bytes + sizeof(int32_t), s) != cudaSuccess) return HD_ERR_CUDA;
+    int32_t *counters = reinterpret_cast<int32_t *>(scratch + plan.o_bytes + plan.ml_bytes);
+    if (cudaMemsetAsync(counters, 0, plan.ctr_bytes + sizeof(int32_t), s) != cudaSuccess) return HD_ERR_CUDA;
 
     hd::LayerArgs a{};
     a.context = context;
@@ -152,17 +208,19 @@ extern "C" hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_
     a.out = static_cast<__nv_bfloat16 *>(out);
     a.lse = lse;
     a.part_o = reinterpret_cast<float *>(scratch);
-    a.part_ml = reinterpret_cast<float2 *>(scratch + o_bytes);
+    a.part_ml = reinterpret_cast<float2 *>(scratch + plan.o_bytes);
     a.counters = counters;
     a.err = counters + (size_t)batch * num_kv_heads;
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = num_kv_heads;
-    a.chunk_keys = chunk_keys;
-    a.max_chunks = num_chunks;
+    a.chunk_keys = plan.chunk_keys;
+    a.max_chunks = plan.num_chunks;
     a.window = 0;
     a.max_context = max_context;
     a.drop_stage = -1;
-    return hd::launch_layer(&kmap, &vmap, a, batch, group, hd::CONSUMER_MMA, stages, false, s) == cudaSuccess
+    a.tokens = a.total_tokens = 1;
+    return hd::launch_layer(&kmap, &vmap, a, batch, num_q_heads / num_kv_heads, hd::CONSUMER_MMA, plan.stages, false,
+                            s) == cudaSuccess
                ? HD_OK
                : HD_ERR_CUDA;
 }

@@ -183,9 +183,15 @@ hd_status hd_plan_step_split(int32_t num_layers, const int32_t *max_keys, const 
                              int32_t batch, int32_t num_kv_heads, int32_t rows, int32_t multi_token,
                              int32_t kv_dtype, int32_t num_sms, int32_t *chunk_keys);
 
-/* Creates a context on the current CUDA device: validates cfg, builds the
- * RoPE tables for positions 0..max_context (cos/sin in fp64, stored fp32) and
- * allocates the workspace sized by max_batch/max_context.  Synchronous. */
+/* Creates a context on the current CUDA device: validates cfg (the checks of
+ * spark_export.py `SparkStepConfig.__post_init__`), builds the RoPE tables for
+ * positions 0..max_context -- per layer type, cos/sin of
+ * position * theta^(-2i/rotary_dim) as `_angles` defines them, evaluated in
+ * fp64 and stored fp32 -- and allocates the workspace sized by
+ * max_batch/max_context.  Synchronous.  Errors: HD_ERR_INVALID_ARG /
+ * HD_ERR_UNSUPPORTED from the config checks, HD_ERR_UNSUPPORTED on a device
+ * that is not sm_103, HD_ERR_CUDA when an allocation fails (nothing is left
+ * allocated then). */
 hd_status hybrid_decode_init(const hd_config *cfg, hd_ctx **out_ctx);
 
 /* Frees the context and its workspace (synchronises the device first). */
@@ -201,29 +207,48 @@ hd_status rope_append_kv(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_
                          const void *q, const void *k, const void *v, float *q_rot,
                          hd_kv_cache cache, void *stream);
 
-/* Attention of a sliding layer over its window: the ring's valid slots plus
- * the staged new entry (ring), or the rolled window (roll); split-K over the
- * keys, then an LSE combine that applies the sink and the output gate (either
- * may be NULL), writes out/lse and commits the staged ring entry.  Must
- * follow rope_append_kv of the same layer on the same stream. */
+/* Attention of a sliding layer over its window (spark_export.py
+ * `_Layer.forward`: the ring branch scores the cached ring and the new entry
+ * as two key sets of one softmax and leaves the slot write to the runtime;
+ * the roll branch scores the shifted window; the window of
+ * `SparkStepConfig.cache_len` counts the current token): the ring's valid
+ * slots plus the staged new entry (ring), or the rolled window (roll);
+ * split-K over the keys, then an LSE combine that applies the sink
+ * (flashmla_sparse.py `HYV4FlashMLASparseImpl`) and the output gate (either
+ * may be NULL), writes out/lse and commits the staged ring entry to slot
+ * context[b] mod (window-1).  Must follow rope_append_kv of the same layer on
+ * the same stream.  Errors: HD_ERR_STATE for a full layer or a device other
+ * than the context's; HD_ERR_CAPACITY when cache.capacity is not the layout's
+ * (window-1 ring, window roll); contexts beyond max_context are flagged on
+ * the device (HD_DEVERR_*) and give NaN out/lse for that sequence. */
 hd_status decode_attn_sliding(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
                               const float *q_rot, hd_kv_cache cache, const float *sink,
                               const float *gate, void *out, float *lse, void *stream);
 
-/* Attention of a full layer over positions 0..context[b] (the new entry was
- * appended by rope_append_kv): split-K over chunks of keys sized from
- * max_context_hint (an upper bound on every context[b] of this call, <=
- * max_context; 0 means max_context), then the LSE combine with the sink and
- * the output gate (either may be NULL). */
+/* Attention of a full layer over positions 0..context[b] (spark_export.py
+ * `_Layer.forward` on a full-attention layer: every cached position plus the
+ * new one; `SparkStepConfig.cache_len` of a full layer is the whole context;
+ * the new entry was appended at index context[b] by rope_append_kv):
+ * split-K over chunks of keys sized from max_context_hint (an upper bound on
+ * every context[b] of this call, <= max_context; 0 means max_context), then
+ * the LSE combine with the sink (flashmla_sparse.py `HYV4FlashMLASparseImpl`)
+ * and the output gate (either may be NULL).  Errors: HD_ERR_STATE for a
+ * sliding layer or a device other than the context's; HD_ERR_CAPACITY when
+ * the hint exceeds max_context or cache.capacity <= hint; a context[b] above
+ * the hint or the capacity is flagged on the device and gives NaN out/lse. */
 hd_status decode_attn_full(hd_ctx *ctx, int32_t layer, int32_t batch, const int32_t *context,
                            int32_t max_context_hint, const float *q_rot, hd_kv_cache cache,
                            const float *sink, const float *gate, void *out, float *lse, void *stream);
 
-/* One decode step over all layers, with the same results as rope_append_kv
+/* One decode step over all layers (spark_export.py `SparkDecodeStep.forward`:
+ * every layer of the step with its own cache pair, the layer's type picking
+ * its window, rotary table and cache layout as `SparkStepConfig.layout_for`
+ * does), with the same results as rope_append_kv
  * followed by the layer's attention call for each layer in order: q is
  * rotated in the attention kernel and the new entry is rotated, scored and
  * stored (appended, or written to its ring slot after the ring was read) by
- * the combine; roll layouts first shift their windows.  `layers` is a host
+ * the combine; a roll layout's kernel reads the window, shifts it down by one
+ * row once it is full and stores the new entry at its end.  `layers` is a host
  * array [num_layers].  The layers of a call are independent: by default one
  * grid runs the attention of all of them (hybrid_decode_set_step_fusion),
  * otherwise one kernel per layer, each of which may start streaming its own
@@ -244,8 +269,10 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
  * [batch][num_tokens][num_q_heads].  The tokens of a sequence are extra query
  * rows sharing one read of the cache, up to 16 rows (and 8 tokens) per kv
  * head per pass (group 4: four tokens per pass).  Full layers append num_tokens entries;
- * sliding ring layers write slots (c + t) mod (window-1) after reading.
- * HD_ERR_UNSUPPORTED for num_tokens > 1 with a roll layout or the CUDA-core
+ * sliding ring layers write slots (c + t) mod (window-1) after reading;
+ * sliding roll layers read their window once, then drop the entries that leave
+ * it (the window shifts down by that many rows) and append the num_tokens
+ * entries.  HD_ERR_UNSUPPORTED for num_tokens > 1 with the CUDA-core
  * consumer; for full layers max_context_hint bounds context[b] (0 means
  * max_context - num_tokens + 1). */
 hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, const int32_t *context,
@@ -268,6 +295,16 @@ hd_status hybrid_decode_set_layer_overlap(hd_ctx *ctx, int32_t enable);
  * (checked on the host); otherwise, or with 0, each layer runs its own kernel
  * (overlapping as hybrid_decode_set_layer_overlap says). */
 hd_status hybrid_decode_set_step_fusion(hd_ctx *ctx, int32_t enable);
+
+/* Chunk merge of single-layer launches (default 1): when a call's grid is
+ * small enough for one CTA per SM, every chunk of a (sequence, kv head) runs in
+ * one thread-block cluster (up to 16 CTAs on this part), and the chunks'
+ * partials merge through distributed shared memory, each CTA finishing a slice
+ * of the output; otherwise (and with 0) the last chunk to finish merges them
+ * from the workspace.  The results are the same within the stated tolerance.
+ * Applies to rope_append_kv's attention calls and to decode_step without step
+ * fusion; step grids always merge through the workspace. */
+hd_status hybrid_decode_set_cluster_combine(hd_ctx *ctx, int32_t enable);
 
 /* Inner loop of the attention kernels (same results within the stated
  * tolerance; the default is the tensor-core one):
@@ -318,6 +355,10 @@ enum { HD_PROFILE_KIND_STEP = 2 };
 hd_status hybrid_decode_set_profiling(hd_ctx *ctx, int32_t enable);
 hd_status hybrid_decode_profile(hd_ctx *ctx, int32_t layer_type, double *total_ms, int64_t *launches);
 
+/* Bytes of the file-scope device array that decode_attn_full_static_scratch
+ * uses as its split-K scratch (64 MiB). */
+#define HD_STATIC_SCRATCH_BYTES (64u << 20)
+
 /* Full-layer attention that allocates nothing (no counterpart in the paper;
  * it exists for callers that cannot call cudaMalloc once running, such as a
  * plugin inside a runtime that pre-plans every device allocation, or a
@@ -325,21 +366,38 @@ hd_status hybrid_decode_profile(hd_ctx *ctx, int32_t layer_type, double *total_m
  * Same result as decode_attn_full (after rope_append_kv appended the new
  * entry at index context[b]; scores positions 0..context[b]), but it needs no
  * hd_ctx: the caller passes the inputs and outputs and the shape, and the
- * split-K scratch lives in one 64 MiB file-scope device array of the library
- * (held on every GPU that uses the library until the process exits).
+ * split-K scratch lives in one HD_STATIC_SCRATCH_BYTES file-scope device
+ * array of the library (held on every GPU that uses the library until the
+ * process exits).  bf16 caches only (k_scale / v_scale must be NULL).
  *   max_context  upper bound on every context[b] of this call; max_context+1
  *                <= cache.capacity.
- * Returns HD_ERR_CAPACITY when the call's scratch (about batch * num_q_heads *
- * chunks * 1032 bytes, chunks = ceil((max_context+1)/chunk) with chunk <= 2048)
- * would exceed 64 MiB.  All calls share the array and it keeps the last
- * call's contents (the tickets are cleared at every call), so calls that
- * overlap on the GPU race: order them on one stream.  The first call on a
- * device looks up the array's address for that device; make it before any
- * stream capture.  Invalid contexts give NaN out/lse for that sequence. */
+ * Returns HD_ERR_CAPACITY, before anything is launched, when the call's
+ * scratch would exceed the array (decode_attn_full_static_scratch_plan gives
+ * the figure: about batch * num_q_heads * chunks * 1032 bytes, chunks =
+ * ceil((max_context+1)/chunk) with chunk <= 2048).  All calls share the array
+ * and it keeps the last call's contents (the tickets and the error word are
+ * cleared at every call), so calls that overlap on the GPU race: order them on
+ * one stream.  The first call in a CUDA context looks up the array's address
+ * for that device and context; make it before any stream capture (a context
+ * made again after cudaDeviceReset gets its own lookup at its first call).
+ * Device-side faults of the inputs are not reported: a context[b] outside
+ * [0, max_context] gives NaN out/lse for that sequence, and a pipeline wait
+ * that runs out (one second) leaves that sequence's out/lse meaningless; the
+ * error word that records both lives in the shared array and no call reads
+ * it back. */
 hd_status decode_attn_full_static_scratch(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
                                           const int32_t *context, int32_t max_context,
                                           const float *q_rot, hd_kv_cache cache, const float *sink,
                                           void *out, float *lse, void *stream);
+
+/* The split plan of decode_attn_full_static_scratch and the scratch bytes it
+ * needs, for `num_sms` SMs (pure host function, no device use): HD_OK when
+ * the call fits the array, HD_ERR_CAPACITY when it would be refused (the
+ * outputs are still written), HD_ERR_INVALID_ARG / HD_ERR_UNSUPPORTED for
+ * shapes the entry point rejects.  Output pointers may be NULL. */
+hd_status decode_attn_full_static_scratch_plan(int32_t batch, int32_t num_q_heads, int32_t num_kv_heads,
+                                               int32_t max_context, int32_t num_sms, int64_t *scratch_bytes,
+                                               int32_t *chunk_keys, int32_t *num_chunks);
 
 /* Measurement utility (no counterpart in the pages): one pass of a pure read
  * stream over `bytes` of the device buffer (16-byte aligned), through shared

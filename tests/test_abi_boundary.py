@@ -155,3 +155,42 @@ def test_config_rejects_an_unknown_kv_dtype(hd):
     assert hd.hd_validate_config(cfg) == 0
     cfg.kv_dtype = 2
     assert hd.hd_validate_config(cfg) == 1
+
+
+def test_static_scratch_plan_counts_the_scratch_it_needs(hd):
+    """The allocation-free entry point's scratch: one (o[256], m, l) partial per
+    (sequence, query head, chunk), one ticket per (sequence, kv head) and the
+    error word, against the array's size; every key is covered by the chunks."""
+    for B, Hq, Hkv, mc in [(1, 8, 2, 0), (6, 8, 2, 9000), (64, 16, 2, 4096), (256, 8, 2, 8191), (3, 2, 2, 2048)]:
+        nbytes, chunk, chunks, st = hd.decode_attn_full_static_scratch_plan(B, Hq, Hkv, mc, 152)
+        assert st == 0, (B, Hq, Hkv, mc)
+        assert chunk * chunks >= mc + 1 and chunk * (chunks - 1) < mc + 1
+        assert nbytes == B * Hq * chunks * (256 * 4 + 8) + B * Hkv * 4 + 4
+        assert nbytes <= hd.HD_STATIC_SCRATCH_BYTES
+
+
+def test_static_scratch_plan_refuses_beyond_the_array(hd):
+    # 16 sequences, group 8, 131072 keys: 64 chunks of 2048 keys per sequence
+    nbytes, chunk, chunks, st = hd.decode_attn_full_static_scratch_plan(16, 64, 8, 131071, 152)
+    assert (st, chunk, chunks) == (3, 2048, 64)
+    assert nbytes == 16 * 64 * 64 * 1032 + 16 * 8 * 4 + 4 > hd.HD_STATIC_SCRATCH_BYTES
+    # the largest context that still fits at this shape, found by bisection, and the next one refused
+    lo, hi = 0, 131071
+    while lo + 1 < hi:
+        mid = (lo + hi) // 2
+        if hd.decode_attn_full_static_scratch_plan(16, 64, 8, mid, 152)[3] == 0:
+            lo = mid
+        else:
+            hi = mid
+    assert hd.decode_attn_full_static_scratch_plan(16, 64, 8, lo, 152)[0] <= hd.HD_STATIC_SCRATCH_BYTES
+    nb, _, _, st = hd.decode_attn_full_static_scratch_plan(16, 64, 8, hi, 152)
+    assert st == 3 and nb > hd.HD_STATIC_SCRATCH_BYTES
+
+
+def test_static_scratch_plan_rejects_bad_shapes(hd):
+    plan = hd.decode_attn_full_static_scratch_plan
+    assert plan(0, 8, 2, 10, 152)[3] == 1          # no sequences
+    assert plan(4, 6, 4, 10, 152)[3] == 1          # heads not a multiple
+    assert plan(4, 8, 2, -1, 152)[3] == 1          # negative context bound
+    assert plan(4, 8, 2, 10, 0)[3] == 1            # no SMs
+    assert plan(4, 32, 2, 10, 152)[3] == 2         # group 16

@@ -263,3 +263,23 @@ def test_layer_overlap_changes_no_bit(hd, kv):
     for i, (a, b) in enumerate(zip(*runs)):
         for x, y in zip(a, b):
             assert np.array_equal(x, y), f"layer {i} differs with the overlap"
+
+
+@pytest.mark.parametrize("cluster", [True, False])
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_single_layer_chunk_merge_paths(hd, orc, g, cluster):
+    """Single-layer calls on small grids merge their chunks inside a thread-block
+    cluster (up to 16 chunks per (sequence, kv head), the default) or through the
+    workspace: both against the oracle, for a full layer whose longest sequence
+    needs more chunks than a cluster holds and a sliding ring layer."""
+    rng = synth.generator(1500 + g)
+    B, Hkv = 3, 2
+    contexts = [0, 1500, 6000]
+    ctx = make_ctx(hd, [SLIDING, FULL], Hq=g * Hkv, max_batch=B, max_context=6000)
+    hd.hybrid_decode_set_cluster_combine(ctx, cluster)
+    sink = sink_for(rng, "neg_inf", g * Hkv)
+    check_layer(hd, orc, ctx, 0, SLIDING, RING, LayerCase(rng, B, g * Hkv, Hkv, 511, contexts, sink=sink))
+    check_layer(hd, orc, ctx, 1, FULL, 0, LayerCase(rng, B, g * Hkv, Hkv, 6001, contexts, sink=sink))
+    # the same layers again: the merge leaves nothing behind that the next call reads
+    check_layer(hd, orc, ctx, 1, FULL, 0, LayerCase(rng, B, g * Hkv, Hkv, 6001, [6000, 3, 2047], sink=sink))
+    ctx.close()

@@ -83,8 +83,8 @@ def test_batch1_28_layer_step_is_one_grid(hd, orc, kv):
 @pytest.mark.parametrize("layout", [RING, ROLL])
 def test_step_grid_launch_counts_and_parity(hd, orc, layout, fuse):
     """One grid for the 28 layers, roll windows included (the grid shifts them
-    after reading); with fusion off, one kernel per layer plus, for a roll
-    layout, the 21 window-shift kernels."""
+    after reading); with fusion off, one kernel per layer (a roll layer's kernel
+    shifts its own window after reading it)."""
     rng = synth.generator(1102)
     types = synth.SPARK_LAYER_TYPES
     ctx = make_ctx(hd, types, 4, 2048, layout=layout)
@@ -93,7 +93,7 @@ def test_step_grid_launch_counts_and_parity(hd, orc, layout, fuse):
     step = Step(hd, rng, types, 4, 8, 2, [0, 511, 700, 2047], layout, 2048, sink=sink)
     n0 = launches(hd, ctx)
     step.run(hd, ctx)
-    expect = 1 if fuse else len(types) + (types.count(SLIDING) if layout == ROLL else 0)
+    expect = 1 if fuse else len(types)
     assert launches(hd, ctx) - n0 == expect
     step.check(orc)
     ctx.close()

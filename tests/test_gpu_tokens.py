@@ -75,17 +75,18 @@ class TokenLayer:
 
 
 def run_case(hd, orc, types, T, Hq, Hkv, context, kv="bf16", seed=0, with_gate=True, max_context=None,
-             fuse=True):
+             fuse=True, layout=RING):
     rng = synth.generator(seed)
     B = len(context)
     context = np.asarray(context, np.int32)
     max_context = max_context or int(context.max()) + T
-    ctx = _ctx(hd, types, Hq, Hkv, B, max_context, kv)
+    ctx = _ctx(hd, types, Hq, Hkv, B, max_context, kv, layout=layout)
     hd.hybrid_decode_set_step_fusion(ctx, fuse)
     sink = synth.sink_vector(rng, ("normal", 1.0, 0.0), Hq)
-    layers = [TokenLayer(rng, t, B, T, Hq, Hkv, 511 if t == SLIDING else max_context + 1, context, kv, sink,
+    window = synth.WINDOW - 1 if layout == RING else synth.WINDOW
+    layers = [TokenLayer(rng, t, B, T, Hq, Hkv, window if t == SLIDING else max_context + 1, context, kv, sink,
                          with_gate) for t in types]
-    refs = [L.oracle(orc, context, RING) for L in layers]
+    refs = [L.oracle(orc, context, layout) for L in layers]
     ios = [L.device(hd) for L in layers]
     hd.decode_step_tokens(ctx, torch.from_numpy(context).cuda(), ios, B, T)
     torch.cuda.synchronize()
@@ -107,6 +108,31 @@ def test_tokens_ring_and_full(hd, orc, T, g):
     """A [sliding ring, full] pair with T tokens across the ring's wrap points."""
     Hkv = 2
     run_case(hd, orc, [SLIDING, FULL], T, g * Hkv, Hkv, RING_FULL_CONTEXTS, seed=700 + 10 * T + g)
+
+
+ROLL_CONTEXTS = [0, 1, 300, 505, 508, 509, 510, 511, 512, 513, 700, 1500]
+
+
+@pytest.mark.parametrize("fuse", [True, False])
+@pytest.mark.parametrize("T", [2, 3, 4, 8])
+@pytest.mark.parametrize("g", [1, 2, 4, 8])
+def test_tokens_roll_and_full(hd, orc, T, g, fuse):
+    """A [sliding roll, full] pair with T tokens while the rolled window fills up
+    and once it is full: each token sees its own window (the window is read once,
+    before it shifts by the entries that leave it), and the window ends as after
+    T single-token steps.  Step fusion on (one grid) and off (one kernel per layer)."""
+    Hkv = 2
+    run_case(hd, orc, [SLIDING, FULL], T, g * Hkv, Hkv, ROLL_CONTEXTS, seed=1300 + 10 * T + g, fuse=fuse,
+             layout=ROLL)
+
+
+@pytest.mark.parametrize("T", [2, 5])
+def test_tokens_roll_fp8(hd, orc, T):
+    run_case(hd, orc, [SLIDING, FULL], T, 8, 2, ROLL_CONTEXTS, kv="fp8", seed=1400 + T, layout=ROLL)
+
+
+def test_tokens_roll_28_layer_step(hd, orc):
+    run_case(hd, orc, synth.SPARK_LAYER_TYPES, 4, 8, 2, [510, 1500, 3], seed=1410, layout=ROLL)
 
 
 @pytest.mark.parametrize("T", [2, 4, 5])
@@ -177,14 +203,9 @@ def test_tokens_match_sequential_gpu_steps(hd):
 
 
 def test_tokens_unsupported_paths(hd):
+    """Several tokens need the tensor-core consumer."""
     rng = synth.generator(905)
     B, T, Hq, Hkv = 1, 2, 8, 2
-    ctx = _ctx(hd, [SLIDING], Hq, Hkv, B, 100, layout=ROLL)
-    L = TokenLayer(rng, SLIDING, B, T, Hq, Hkv, 512, np.array([10], np.int32), "bf16", None, False)
-    with pytest.raises(hd.HDError) as e:
-        hd.decode_step_tokens(ctx, torch.tensor([10], dtype=torch.int32, device="cuda"), [L.device(hd)], B, T)
-    assert e.value.status == 2
-    ctx.close()
     ctx = _ctx(hd, [FULL], Hq, Hkv, B, 100)
     hd.hybrid_decode_set_consumer(ctx, hd.HD_CONSUMER_CUDA_CORE)
     L = TokenLayer(rng, FULL, B, T, Hq, Hkv, 101, np.array([10], np.int32), "bf16", None, False)
