@@ -1117,7 +1117,48 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     float *red_m = red_o + CW * CG * kHeadDim;
     float *red_l = red_m + CW * CG;
     if (own_producer(KV) && warp == CW) {
-        if (lane == 0) {  // producer: one lane issues every load of the chunk
+        if (MT && sh > 0) {
+            // Multi-token pass over a rolled window (bf16): the producer warp moves
+            // each stage's rows down by sh once the stage has landed -- rows below
+            // sh leave the window -- and only then refills the slot; every row
+            // written was loaded by this or an earlier stage and later stages load
+            // higher rows.  (This keeps the copy out of the consumers' registers.)
+            constexpr int kChunks = kHeadDim * kv_elem_bytes(KV) / 16;   // 16-byte chunks per row
+            const size_t seq = ((size_t)b * a.seq_stride + (size_t)kvh * a.capacity * kHeadDim) * kv_elem_bytes(KV);
+            for (int s = 0; s < nst; ++s) {
+                const int slot = s % S;
+                if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (s / S) & 1))) {
+                    if (lane == 0) atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
+                    break;
+                }
+                const uint8_t *st = smem + slot * kStage;
+                const int key0 = start + s * kKeys, nrows = min(kKeys, end - key0);
+                for (int i = lane; i < 2 * nrows * kChunks; i += 32) {
+                    const int v = i >= nrows * kChunks, rem = i - v * nrows * kChunks;
+                    const int r = rem / kChunks, ch = rem % kChunks, row = key0 + r + roff;
+                    if (row < sh) continue;
+                    const uint4 x = *reinterpret_cast<const uint4 *>(st + v * kBoxes * kv_box_bytes(KV) +
+                                                                     tile_offset<KV>(r, ch));
+                    *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(v ? a.cache_v : a.cache_k) + seq +
+                                               (size_t)(row - sh) * kHeadDim * kv_elem_bytes(KV) + 16 * ch) = x;
+                }
+                __syncwarp();
+                int stop = 0;
+                if (lane == 0 && s + S < nst) {
+                    if (droppable(s + S)) {
+                        stop = 1;
+                    } else if (!mbar_wait(&empty[slot], (s / S) & 1)) {
+                        atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
+                        stop = 1;
+                    } else {
+                        // this warp's reads of the slot come before the copy engine's write
+                        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                        issue_stage(s + S);
+                    }
+                }
+                if (__shfl_sync(0xffffffffu, stop, 0)) break;
+            }
+        } else if (lane == 0) {  // producer: one lane issues every load of the chunk
             for (int s = early; s < nst; ++s) {
                 if (droppable(s)) break;
                 const int slot = s % S;
@@ -1160,10 +1201,11 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
             // down by sh rows before the slot is released; rows below sh leave the
             // window.  Every row written was loaded by this or an earlier stage; later
             // stages load higher rows.  A single token moves a full window by one row
-            // (sh = roff); several tokens by the entries that leave it, which only the
-            // first row group writes (the groups read the same keys).  A layer kernel
-            // launched as a programmatic dependent follows another layer of the step,
-            // which never touches this cache, so these writes need no dependency wait.
+            // (sh = roff); several tokens by the entries that leave it -- with bf16
+            // caches the producer warp does that, with E4M3 caches the first row group
+            // (the groups read the same keys).  A layer kernel launched as a
+            // programmatic dependent follows another layer of the step, which never
+            // touches this cache, so these writes need no dependency wait.
             if constexpr (!MT) {
                 if (roff) {
                     const int key0 = start + s * kKeys + kpart * kSpan;
@@ -1181,7 +1223,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
                         *reinterpret_cast<uint4 *>(dst) = x;
                     }
                 }
-            } else {
+            } else if constexpr (!own_producer(KV)) {   // E4M3: no producer warp to do it
                 if (sh > 0 && rg == 0) {
                     const int key0 = start + s * kKeys + kpart * kSpan;
                     const int nrows = min(kSpan, end - key0);
