@@ -548,6 +548,9 @@ def run_ours(args, world, rank, local) -> int:
     per_layer_ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
     hd.hybrid_decode_set_layer_overlap(wl.ctx, False)
     serial_ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
+    # the same stream-order step replayed from a CUDA graph (how a serving loop
+    # launches a decode step): the launches no longer wait on the host
+    serial_graph_ms = graph_steps(wl, args, device)
     hd.hybrid_decode_set_layer_overlap(wl.ctx, True)
     hd.hybrid_decode_set_step_fusion(wl.ctx, True)
     if hd.hybrid_decode_device_errors(wl.ctx):
@@ -585,7 +588,9 @@ def run_ours(args, world, rank, local) -> int:
             "unit": "GB/s", "note": "step fusion off: one kernel per layer, each starting while the previous drains"}
         result["layers_in_stream_order"] = {
             "ms_per_step": round(serial_ms, 4), "value": round(step_kv / (serial_ms * 1e-3) / 1e9, 1),
-            "unit": "GB/s", "note": "step fusion off and no layer starts before the previous one is complete"}
+            "unit": "GB/s", "note": "step fusion off and no layer starts before the previous one is complete",
+            "cuda_graph": {"ms_per_step": round(serial_graph_ms, 4),
+                           "value": round(step_kv / (serial_graph_ms * 1e-3) / 1e9, 1), "unit": "GB/s"}}
         if args.tokens > 1:
             result["config"].update(tokens_per_sequence=args.tokens, kv_bytes_read_per_step=step_kv)
         if fp8:
@@ -848,6 +853,23 @@ def baseline_configs(device, args, consumer, read_peak) -> dict:
     return out
 
 
+def graph_steps(wl, args, device) -> float:
+    """ms per step of the workload's step (in the context's current mode) captured
+    once in a CUDA graph and replayed."""
+    import torch
+    side = torch.cuda.Stream(device)
+    side.wait_stream(torch.cuda.current_stream(device))
+    with torch.cuda.stream(side):
+        wl.step()
+    torch.cuda.current_stream(device).wait_stream(side)
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        wl.step()
+    ms = time_steps(graph.replay, args.steps, args.warmup, 1, device)
+    del graph
+    return ms
+
+
 def secondary_batch1(device, args, consumer) -> dict:
     """The 28-layer step at batch 1, context 4096 (launch-latency bound), launched
     eagerly and replayed from a CUDA graph of one decode_step."""
@@ -868,12 +890,18 @@ def secondary_batch1(device, args, consumer) -> dict:
     ms_graph = time_steps(graph.replay, steps, warm, 1, device)
     hd.hybrid_decode_set_step_fusion(wl.ctx, False)   # one kernel per layer, for comparison
     ms_layers = time_steps(wl.step, steps, warm, 1, device)
+    hd.hybrid_decode_set_layer_overlap(wl.ctx, False)   # and every layer in full stream order
+    ms_serial = time_steps(wl.step, steps, warm, 1, device)
+    ms_serial_graph = graph_steps(wl, argparse.Namespace(steps=steps, warmup=warm), device)
+    hd.hybrid_decode_set_layer_overlap(wl.ctx, True)
     hd.hybrid_decode_set_step_fusion(wl.ctx, True)
     if hd.hybrid_decode_device_errors(wl.ctx):
         raise RuntimeError("device error flags in the batch-1 step")
     return {"workload": SECONDARY_WORKLOAD, "us_per_step": round(ms * 1e3, 1),
             "us_per_step_cuda_graph": round(ms_graph * 1e3, 1),
             "us_per_step_kernel_per_layer": round(ms_layers * 1e3, 1),
+            "us_per_step_layers_in_stream_order": round(ms_serial * 1e3, 1),
+            "us_per_step_layers_in_stream_order_cuda_graph": round(ms_serial_graph * 1e3, 1),
             "kv_GBps_cuda_graph": round(wl.bytes / (ms_graph * 1e-3) / 1e9, 1),
             "kv_bytes_per_step": wl.bytes, "roofline_us": round(wl.bytes / (measured_peaks()["hbm_gbs"] * 1e9) * 1e6, 1)}
 

@@ -60,6 +60,12 @@
 #ifndef HD_STEP_ISSUE_EARLY
 #define HD_STEP_ISSUE_EARLY 1
 #endif
+#ifndef HD_STEP_ARGS_IN_SMEM
+#define HD_STEP_ARGS_IN_SMEM 0
+#endif
+#ifndef HD_STEP_FINISH
+#define HD_STEP_FINISH 0
+#endif
 
 namespace hd {
 namespace {
@@ -68,17 +74,26 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kQScale = kLog2e * 0.0625f;   // log2(e) / sqrt(256)
 constexpr int kConsumerWarps = 4;   // per CTA; 16-row multi-token passes run twice as many
-// bf16 layers run a dedicated producer warp.  E4M3 layers fold the producer
-// into the consumers (the last warp to release a slot refills it): four warps
-// per CTA leave each thread up to 255 registers at two CTAs per SM, which the
-// E4M3 consumer's conversions need (five warps cap it at 168).
-__host__ __device__ constexpr bool own_producer(int kv) { return kv == KV_BF16; }
+// Who issues the copies.  bf16 single-layer kernels, multi-token passes and
+// one-CTA-per-SM grids run a dedicated producer warp (lower latency for small
+// grids: the batch-1 step 23.5 vs 27 us, the 16-row pass 3.12 vs 3.62 ms).
+// E4M3 kernels and the bf16 single-token step grids of two CTAs per SM fold the
+// producer into the consumers (the last warp to release a slot refills it):
+// four warps per CTA leave each thread up to 255 registers at two CTAs per SM,
+// where five warps cap it at 168 -- the E4M3 consumer's conversions need them,
+// and the bf16 step grid spilled at the cap (folded: 2.265 vs 2.303 ms at
+// batch 64, 4.444 vs 4.498 ms at group 8).
+__host__ __device__ constexpr bool own_producer(int kv, int nl, bool mt, bool deep) {
+    return kv == KV_BF16 && (nl == 1 || mt || deep);
+}
 // 16 query rows run one CTA per SM: eight consumer warps (two per row group of
 // eight rows and stage half) keep as many warps per SM as two 8-row CTAs.
 __host__ __device__ constexpr int consumer_warps(int g) { return g > kMaxGroup ? 2 * kConsumerWarps : kConsumerWarps; }
-__host__ __device__ constexpr int layer_threads(int g, int kv) {
-    return (consumer_warps(g) + (own_producer(kv) ? 1 : 0)) * 32;
+__host__ __device__ constexpr int layer_threads(int g, int kv, int nl, bool mt, bool deep) {
+    return (consumer_warps(g) + (own_producer(kv, nl, mt, deep) ? 1 : 0)) * 32;
 }
+// A ring of more than the default bytes: one CTA per SM.
+__host__ __device__ constexpr bool deep_ring(int s, int kv) { return s * kv_stage_bytes(kv) > kStages * kStageBytes; }
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
 // Inside the stage ring (free once every stage is consumed): the warp buffers
 // [warps][G][256] + (m, l) and the combine weights start at 0; this chunk's
@@ -240,6 +255,32 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &r, float (&f)[8]) {
         f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
 }
+// q, once rotated and scaled, is kept as one 32-bit word per element: the value
+// rounded to 16 bits in the low half and the remainder rounded to 16 bits in the
+// high half -- bf16 with bf16 caches, f16 with E4M3 caches (the operand types of
+// the tensor-core consumers) -- so hi + lo carries about 18 (bf16) or 22 (f16)
+// significant bits.  The split is made once per element when q is rotated; the
+// consumers build their operand fragments from it with byte permutes.
+template <int KV>
+__device__ __forceinline__ uint32_t q_split(float x) {
+    if (KV == KV_FP8) {
+        const __half h = __float2half_rn(x);
+        const __half l = __float2half_rn(x - __half2float(h));
+        return (uint32_t)__half_as_ushort(h) | ((uint32_t)__half_as_ushort(l) << 16);
+    } else {
+        const __nv_bfloat16 h = __float2bfloat16_rn(x);
+        const __nv_bfloat16 l = __float2bfloat16_rn(x - __bfloat162float(h));
+        return (uint32_t)__bfloat16_as_ushort(h) | ((uint32_t)__bfloat16_as_ushort(l) << 16);
+    }
+}
+template <int KV>
+__device__ __forceinline__ float q_join(uint32_t w) {
+    if (KV == KV_FP8)
+        return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFFu))) +
+               __half2float(__ushort_as_half((unsigned short)(w >> 16)));
+    return __uint_as_float(w << 16) + __uint_as_float(w & 0xFFFF0000u);
+}
+
 // Byte offset of 16-byte chunk c (0..31 for bf16, 0..15 for E4M3) of row r in
 // a stage's K or V region: box c/8, swizzled chunk (c%8)^(r%8) inside the
 // 128-byte row.
@@ -323,13 +364,13 @@ struct FmaConsumer {
             unpack_bf16x8(*reinterpret_cast<const uint4 *>(st + tile_offset<KV>(row, lane)), f);
     }
 
-    __device__ void init(const float *q_s, int lane, float k_scale) {
+    __device__ void init(const uint32_t *qw, int lane, float k_scale) {
         kscale = k_scale;
 #pragma unroll
         for (int h = 0; h < G; ++h) {
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                qv[h][i] = q_s[h * kHeadDim + lane * 8 + i];
+                qv[h][i] = q_join<KV>(qw[h * kHeadDim + lane * 8 + i]);
                 acc[h][i] = 0.f;
             }
             m[h] = -INFINITY;
@@ -430,22 +471,18 @@ struct MmaConsumer {
         mcnt = (lane >> 2) < G ? m.cnt[lane >> 2] : 0;
     }
 
-    __device__ void init(const float *q_s, int lane, float) {
+    __device__ void init(const uint32_t *qw, int lane, float) {
         const int gid = lane >> 2, t4 = lane & 3;
 #pragma unroll
         for (int ks = 0; ks < 16; ++ks) {
             uint32_t r[4] = {0u, 0u, 0u, 0u};
-            if (gid < G) {
-                const float *qh = q_s + gid * kHeadDim + 16 * ks + 2 * t4;
-                const float x0 = qh[0], x1 = qh[1], x2 = qh[8], x3 = qh[9];
-                const float h0 = __bfloat162float(__float2bfloat16_rn(x0));
-                const float h1 = __bfloat162float(__float2bfloat16_rn(x1));
-                const float h2 = __bfloat162float(__float2bfloat16_rn(x2));
-                const float h3 = __bfloat162float(__float2bfloat16_rn(x3));
-                r[0] = pack_bf16(h0, h1);
-                r[1] = pack_bf16(x0 - h0, x1 - h1);
-                r[2] = pack_bf16(h2, h3);
-                r[3] = pack_bf16(x2 - h2, x3 - h3);
+            if (gid < G) {   // dims 16 ks + 2 t4 (+1) and the same + 8: high parts, then low parts
+                const uint2 w0 = *reinterpret_cast<const uint2 *>(qw + gid * kHeadDim + 16 * ks + 2 * t4);
+                const uint2 w8 = *reinterpret_cast<const uint2 *>(qw + gid * kHeadDim + 16 * ks + 2 * t4 + 8);
+                r[0] = __byte_perm(w0.x, w0.y, 0x5410);
+                r[1] = __byte_perm(w0.x, w0.y, 0x7632);
+                r[2] = __byte_perm(w8.x, w8.y, 0x5410);
+                r[3] = __byte_perm(w8.x, w8.y, 0x7632);
             }
 #pragma unroll
             for (int j = 0; j < 4; ++j) qa[ks][j] = r[j];
@@ -583,7 +620,7 @@ struct Fp8MmaConsumer {
         for (int e = 0; e < 2; ++e) mcnt[e] = 2 * (lane & 3) + e < G ? m.cnt[2 * (lane & 3) + e] : 0;
     }
 
-    __device__ void init(const float *q_s, int lane, float k_scale) {
+    __device__ void init(const uint32_t *qw, int lane, float k_scale) {
         const int gid = lane >> 2, t4 = lane & 3;
         kscale = k_scale;
 #pragma unroll
@@ -598,16 +635,11 @@ struct Fp8MmaConsumer {
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     uint32_t r0 = 0u, r1 = 0u;
-                    if (used) {
-                        const float *qh = q_s + head * kHeadDim + 16 * chunk + 4 * j;
-                        float x[4];
-#pragma unroll
-                        for (int i = 0; i < 4; ++i) {
-                            const float h = __half2float(__float2half_rn(qh[i]));
-                            x[i] = lo ? qh[i] - h : h;
-                        }
-                        r0 = pack_f16(x[0], x[1]);
-                        r1 = pack_f16(x[2], x[3]);
+                    if (used) {   // four dims: their f16 high parts, or their low parts
+                        const uint4 w = *reinterpret_cast<const uint4 *>(qw + head * kHeadDim + 16 * chunk + 4 * j);
+                        const uint32_t sel = lo ? 0x7632u : 0x5410u;
+                        r0 = __byte_perm(w.x, w.y, sel);
+                        r1 = __byte_perm(w.z, w.w, sel);
                     }
                     qb[t][4 * p + j][0] = r0;
                     qb[t][4 * p + j][1] = r1;
@@ -782,16 +814,20 @@ struct Fp8MmaConsumer {
 // NL: layers in the parameter table (1: one layer, grid (chunks, kv heads,
 // sequences); kStepLayers: a step, 1-D grid over the layers' CTA ranges).
 template <int G, int CONSUMER, int S, int KV, bool MT, int NL>
-__global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <= kStages * kStageBytes ? 2 : 1)
+__global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV)), deep_ring(S, KV) ? 1 : 2)
     attn_layer_kernel(const __grid_constant__ LaunchTable<NL> p) {
     constexpr int kStage = kv_stage_bytes(KV);     // bytes of one stage (K + V)
     constexpr int kKeys = kv_stage_keys(KV);       // keys per stage: 32 bf16, 64 E4M3
     constexpr int kBoxes = kv_boxes_per_row(KV);   // 128-byte boxes per K or V row
-    constexpr int kNThreads = layer_threads(G, KV);
+    constexpr int kNThreads = layer_threads(G, KV, NL, MT, deep_ring(S, KV));
+    constexpr bool kOwnProducer = own_producer(KV, NL, MT, deep_ring(S, KV));
     constexpr int CW = consumer_warps(G);          // consumer warps
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // The ring starts on a 1024-byte boundary of the shared window (the 128-byte
+    // swizzle repeats every 1024 bytes).  Offsetting the array pointer, rather than
+    // rounding an integer address, keeps every pointer below in the shared space,
+    // so the compiler emits shared-memory loads and stores for them.
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     float *q_s = reinterpret_cast<float *>(smem + S * kStage);               // [G][256]
     float *knew_s = q_s + G * kHeadDim;                                        // [256]
     float *vnew_s = knew_s + kHeadDim;                                         // [256]
@@ -820,7 +856,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     // offsets).  Copying them to shared memory once measured faster in the
     // register-capped bf16 kernels (two CTAs per SM) only while they had registers
     // to spare; it is off.
-    constexpr bool kArgsInSmem = false;
+    constexpr bool kArgsInSmem = NL > 1 && HD_STEP_ARGS_IN_SMEM && KV == KV_BF16 && !kOwnProducer;
     __shared__ LayerArgs step_args_s;
     if constexpr (kArgsInSmem) {
         static_assert(sizeof(LayerArgs) % 4 == 0, "copied as words");
@@ -899,50 +935,55 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     // once to bf16, or quantised to E4M3 (fp64 rotation, one division, one
     // rounding; V too), each scored as stored; E4M3 V stays in code units.
     auto make_new_entries = [&]() {
-        for (int idx = threadIdx.x; idx < ntok * kHeadDim; idx += blockDim.x) {
-            const int t = idx / kHeadDim, d = idx % kHeadDim;
+        // One task per rotary pair (dims j and j + rotary_dim / 2 share their
+        // inputs) and one per pass-through dim: one round over the CTA for a
+        // fully rotated key.
+        const int hr = a.rotary_dim >> 1;
+        const int per = kHeadDim - hr;   // tasks per token
+        for (int idx = threadIdx.x; idx < ntok * per; idx += blockDim.x) {
+            const int t = idx / per, u = idx % per;
+            const bool pair = u < hr;
+            const int d0 = pair ? u : u + hr;
             // Raw k of token t at dim i and its rotary row (MT reads them here; a
-            // single token's were fetched with the combine's other inputs).
+            // single token's were fetched with the prologue's other inputs).
             const __nv_bfloat16 *kg = static_cast<const __nv_bfloat16 *>(a.new_k) +
                                       ((size_t)(b * a.total_tokens + a.token0 + t) * a.num_kv_heads + kvh) * kHeadDim;
             const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(a.new_v) +
                                       ((size_t)(b * a.total_tokens + a.token0 + t) * a.num_kv_heads + kvh) * kHeadDim;
             auto kraw = [&](int i) -> double { return MT ? (double)__bfloat162float(kg[i]) : (double)kraw_s[i]; };
-            auto tab = [&](int j) -> float2 {
-                return MT ? a.table[(size_t)(c + t) * (a.rotary_dim >> 1) + j] : tab_s[j];
-            };
-            const float vraw = MT ? __bfloat162float(vg[d]) : vnew_s[d];
-            if (KV == KV_FP8) {
-                // E4M3 entry: quantise (fp64 rotation, one division, one rounding) unless staged;
-                // score it as stored (code * scale) and keep V in code units.
-                if (a.new_kind == NEW_ROTATE) {
-                    double y = kraw(d);
-                    if (d < a.rotary_dim) {
-                        const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
-                        const double x1 = kraw(j), x2 = kraw(j + half);
-                        const float2 cs2 = tab(j);
-                        const double cc = cs2.x, ss = cs2.y;
-                        y = d < half ? __dsub_rn(__dmul_rn(x1, cc), __dmul_rn(x2, ss))
-                                     : __dadd_rn(__dmul_rn(x2, cc), __dmul_rn(x1, ss));
+            auto vraw = [&](int i) -> float { return MT ? __bfloat162float(vg[i]) : vnew_s[i]; };
+            // the key in fp64: rotated from the fp32 table (exact products, one
+            // rounding), or passed through / already staged
+            double y0, y1 = 0.0;
+            if (pair && a.new_kind == NEW_ROTATE) {
+                const double x1 = kraw(u), x2 = kraw(u + hr);
+                const float2 cs2 = MT ? a.table[(size_t)(c + t) * hr + u] : tab_s[u];
+                const double cc = cs2.x, ss = cs2.y;
+                y0 = __dsub_rn(__dmul_rn(x1, cc), __dmul_rn(x2, ss));
+                y1 = __dadd_rn(__dmul_rn(x2, cc), __dmul_rn(x1, ss));
+            } else if (!(KV == KV_FP8 && a.new_kind == NEW_STAGED)) {
+                y0 = kraw(d0);
+                if (pair) y1 = kraw(u + hr);
+            }
+            for (int e = 0; e < (pair ? 2 : 1); ++e) {
+                const int d = e ? u + hr : d0;
+                const double y = e ? y1 : y0;
+                const float vr = vraw(d);
+                if (KV == KV_FP8) {
+                    // E4M3 entry: quantise (one division, one rounding) unless staged;
+                    // score it as stored (code * scale) and keep V in code units.
+                    if (a.new_kind == NEW_ROTATE) {
+                        code_t[t * kHeadDim + d] = e4m3_quotient(y, (double)kscale);
+                        code_t[vcode_off + t * kHeadDim + d] = e4m3_quotient((double)vr, (double)vscale);
                     }
-                    code_t[t * kHeadDim + d] = e4m3_quotient(y, (double)kscale);
-                    code_t[vcode_off + t * kHeadDim + d] = e4m3_quotient((double)vraw, (double)vscale);
+                    knew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[t * kHeadDim + d]) * kscale;
+                    vnew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[vcode_off + t * kHeadDim + d]);
+                } else {
+                    // a rotated key is rounded once to bf16; other values are bf16 already
+                    knew_t[t * kHeadDim + d] =
+                        (pair && a.new_kind == NEW_ROTATE) ? f64_to_bf16_value(y) : (float)y;
+                    vnew_t[t * kHeadDim + d] = vr;
                 }
-                knew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[t * kHeadDim + d]) * kscale;
-                vnew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[vcode_off + t * kHeadDim + d]);
-            } else {
-                float kn;
-                if (a.new_kind == NEW_STAGED || d >= a.rotary_dim) {
-                    kn = (float)kraw(d);
-                } else {  // rotate the new key in fp64 from the fp32 table, round once to bf16
-                    const int half = a.rotary_dim >> 1, j = d < half ? d : d - half;
-                    const double x1 = kraw(j), x2 = kraw(j + half);
-                    const float2 cs2 = tab(j);
-                    const double cc = cs2.x, ss = cs2.y;
-                    kn = f64_to_bf16_value(d < half ? x1 * cc - x2 * ss : x2 * cc + x1 * ss);
-                }
-                knew_t[t * kHeadDim + d] = kn;
-                vnew_t[t * kHeadDim + d] = vraw;
             }
         }
     };
@@ -1011,7 +1052,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
         if (a.gate) gld = a.gate[(size_t)b * a.num_q_heads + kvh * G + threadIdx.x];
     }
 
-    constexpr int kIssuer = own_producer(KV) ? CW * 32 : 0;
+    constexpr int kIssuer = kOwnProducer ? CW * 32 : 0;
     constexpr bool kIssueEarly = NL == 1 || HD_STEP_ISSUE_EARLY;
     const int early = min(S, nst);   // stages issued before the prologue ends
     if (threadIdx.x == kIssuer) {
@@ -1064,19 +1105,24 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
         for (int s = 0; s < early && !droppable(s); ++s) issue_stage(s);
     // Round 2: rotate each rotary pair in place (fp32; q only feeds the scores)
     // and scale every dim to log2 units.
+    // (each element's word replaces its fp32 value in place)
+    uint32_t *q_w = reinterpret_cast<uint32_t *>(q_s);
     if (a.q_bf16) {
         for (int p = threadIdx.x; p < G * half; p += blockDim.x) {
             const int r = p / half, j = p % half;
             const float2 t = MT ? a.table[(size_t)(c + r / Gm) * half + j] : tab_s[j];   // position c + token
             float *qr = q_s + r * kHeadDim;
             const float x1 = qr[j], x2 = qr[j + half];
-            qr[j] = fmaf(x1, t.x, -x2 * t.y) * kQScale;
-            qr[j + half] = fmaf(x2, t.x, x1 * t.y) * kQScale;
+            q_w[r * kHeadDim + j] = q_split<KV>(fmaf(x1, t.x, -x2 * t.y) * kQScale);
+            q_w[r * kHeadDim + j + half] = q_split<KV>(fmaf(x2, t.x, x1 * t.y) * kQScale);
         }
         const int pass = kHeadDim - 2 * half;
-        for (int i = threadIdx.x; i < G * pass; i += blockDim.x) q_s[(i / pass) * kHeadDim + 2 * half + i % pass] *= kQScale;
+        for (int i = threadIdx.x; i < G * pass; i += blockDim.x) {
+            const int e = (i / pass) * kHeadDim + 2 * half + i % pass;
+            q_w[e] = q_split<KV>(q_s[e] * kQScale);
+        }
     } else {
-        for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) q_s[i] *= kQScale;
+        for (int i = threadIdx.x; i < G * kHeadDim; i += blockDim.x) q_w[i] = q_split<KV>(q_s[i] * kQScale);
     }
     // Single-token passes make the new entry here, in every CTA, while the first
     // stages are in flight (its inputs arrived with q): whichever CTA combines
@@ -1104,7 +1150,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     if (new_early && warp < CW) {
         for (int h = warp; h < G; h += CW) {
             float t = 0.f;
-            for (int d = lane; d < kHeadDim; d += 32) t = fmaf(q_s[h * kHeadDim + d], knew_t[d], t);
+            for (int d = lane; d < kHeadDim; d += 32) t = fmaf(q_join<KV>(q_w[h * kHeadDim + d]), knew_t[d], t);
 #pragma unroll
             for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
             if (lane == 0) wnew_t[h] = t;
@@ -1116,7 +1162,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     float *red_o = reinterpret_cast<float *>(smem);             // [warps][CG][256], reuses the stage ring
     float *red_m = red_o + CW * CG * kHeadDim;
     float *red_l = red_m + CW * CG;
-    if (own_producer(KV) && warp == CW) {
+    if (kOwnProducer && warp == CW) {
         if (MT && sh > 0) {
             // Multi-token pass over a rolled window (bf16): the producer warp moves
             // each stage's rows down by sh once the stage has landed -- rows below
@@ -1177,7 +1223,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
         constexpr int kCallKeys = decltype(cons)::kWK;          // keys per consume call
         constexpr int kSpan = kKeys / WPG;                        // keys of a stage per warp
         const int rg = warp / WPG, kpart = warp % WPG;
-        cons.init(q_s + rg * CG * kHeadDim, lane, kscale);
+        cons.init(q_w + rg * CG * kHeadDim, lane, kscale);
         if (MT) {
             RowMask gm = mask;
             gm.cnt = mcnt_s + rg * CG;
@@ -1223,7 +1269,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
                         *reinterpret_cast<uint4 *>(dst) = x;
                     }
                 }
-            } else if constexpr (!own_producer(KV)) {   // E4M3: no producer warp to do it
+            } else if constexpr (!kOwnProducer) {   // no producer warp to do it
                 if (sh > 0 && rg == 0) {
                     const int key0 = start + s * kKeys + kpart * kSpan;
                     const int nrows = min(kSpan, end - key0);
@@ -1245,7 +1291,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
             }
             __syncwarp();  // orders every lane's reads of the slot before lane 0's release
             if (lane == 0) {
-                if (own_producer(KV)) {
+                if (kOwnProducer) {
                     mbar_arrive(&empty[slot]);
                 } else {
                     // Folded producer: the last of the consumer warps to release the slot
@@ -1287,7 +1333,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
     // sequence finishes the rows itself: the new entry joins the maximum and the
     // sum here.  (Step grids take the general combine below: the shorter path
     // costs registers that their two-CTA-per-SM kernels do not have.)
-    const bool finish = NL == 1 && !MT && nchunks == 1 && clus <= 1;
+    const bool finish = (NL == 1 || HD_STEP_FINISH) && !MT && nchunks == 1 && clus <= 1;
     if (threadIdx.x < G) {
         const int h = threadIdx.x, w0 = (h / CG) * WPG, hr = h % CG;
         float M = -INFINITY;
@@ -1576,7 +1622,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV), S * kv_stage_bytes(KV) <
                 for (int j = 0; j <= th; ++j) {
                     float t = 0.f;
                     for (int d = lane; d < kHeadDim; d += 32)
-                        t = fmaf(q_s[h * kHeadDim + d], knew_t[j * kHeadDim + d], t);
+                        t = fmaf(q_join<KV>(q_w[h * kHeadDim + d]), knew_t[j * kHeadDim + d], t);
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
                     if (lane == 0) wnew_t[h * WN + j] = t;
@@ -1718,7 +1764,7 @@ cudaError_t launch_g(const LaunchTable<NL> &p, dim3 grid, bool pdl, cudaStream_t
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(layer_threads(G, KV));
+    cfg.blockDim = dim3(layer_threads(G, KV, NL, MT, deep_ring(S, KV)));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -1755,7 +1801,7 @@ int cluster_limit_g() {
     for (int k : {kMaxCluster, 8}) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(k, 1, 1);
-        cfg.blockDim = dim3(layer_threads(G, KV));
+        cfg.blockDim = dim3(layer_threads(G, KV, 1, false, true));
         cfg.dynamicSmemBytes = smem;
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
