@@ -110,7 +110,7 @@ def measured_peaks() -> dict:
 
 def kernel_source_hash() -> str:
     h = hashlib.sha256()
-    for f in ("attn_kernel.cuh", "hd_internal.h"):
+    for f in ("attn_kernel.cuh", "hd_internal.h", "rope_round.cuh", "e4m3.cuh"):
         with open(os.path.join(ROOT, "full_gqa_decode_gb300", "csrc", f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]

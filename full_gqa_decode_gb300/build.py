@@ -19,7 +19,7 @@ BUILD_DIR = os.path.join(ROOT, "_build")
 LIBRARY = os.path.join(PKG, "libhybriddecode.so")
 SOURCES = ["api.cpp", "rope_append.cu", "attn_decode.cu", "attn_decode_fp8.cu", "attn_step.cu",
            "attn_step_fp8.cu", "noalloc.cu", "read_probe.cu"]
-HEADERS = ["hd_internal.h", "attn_kernel.cuh", "e4m3.cuh"]
+HEADERS = ["hd_internal.h", "attn_kernel.cuh", "e4m3.cuh", "rope_round.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

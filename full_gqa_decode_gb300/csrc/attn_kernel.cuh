@@ -52,6 +52,7 @@
 
 #include "e4m3.cuh"
 #include "hd_internal.h"
+#include "rope_round.cuh"
 
 // Build switches of the attention kernel (measured choices; see the comments at their use).
 #ifndef HD_STEP_NEW_IN_EVERY_CTA
@@ -64,7 +65,7 @@
 #define HD_STEP_ARGS_IN_SMEM 0
 #endif
 #ifndef HD_STEP_FINISH
-#define HD_STEP_FINISH 0
+#define HD_STEP_FINISH 1
 #endif
 
 namespace hd {
@@ -294,15 +295,6 @@ __device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
     uint32_t y;
     asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
     return y;
-}
-
-// One round-to-nearest-even of a double to bf16, through round-to-odd binary32
-// (Boldo & Melquiond, IEEE TC 2008): the odd-rounded binary32 keeps enough bits
-// that rounding it to bf16 equals rounding the double directly.
-__device__ __forceinline__ float f64_to_bf16_value(double x) {
-    float t = __double2float_rz(x);
-    if ((double)t != x && isfinite(t)) t = __uint_as_float(__float_as_uint(t) | 1u);
-    return __bfloat162float(__float2bfloat16_rn(t));
 }
 
 // Scored cache keys of sequence context c, or -1 (and the error bit) when c
@@ -950,17 +942,23 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
                                       ((size_t)(b * a.total_tokens + a.token0 + t) * a.num_kv_heads + kvh) * kHeadDim;
             const __nv_bfloat16 *vg = static_cast<const __nv_bfloat16 *>(a.new_v) +
                                       ((size_t)(b * a.total_tokens + a.token0 + t) * a.num_kv_heads + kvh) * kHeadDim;
-            auto kraw = [&](int i) -> double { return MT ? (double)__bfloat162float(kg[i]) : (double)kraw_s[i]; };
+            auto kraw = [&](int i) -> float { return MT ? __bfloat162float(kg[i]) : kraw_s[i]; };
             auto vraw = [&](int i) -> float { return MT ? __bfloat162float(vg[i]) : vnew_s[i]; };
-            // the key in fp64: rotated from the fp32 table (exact products, one
-            // rounding), or passed through / already staged
-            double y0, y1 = 0.0;
+            // the key: rotated from the fp32 table -- in fp64 (exact products, one
+            // rounding) for E4M3, rounded once to bf16 otherwise -- or passed
+            // through / already staged
+            double y0 = 0.0, y1 = 0.0;
             if (pair && a.new_kind == NEW_ROTATE) {
-                const double x1 = kraw(u), x2 = kraw(u + hr);
+                const float x1 = kraw(u), x2 = kraw(u + hr);
                 const float2 cs2 = MT ? a.table[(size_t)(c + t) * hr + u] : tab_s[u];
-                const double cc = cs2.x, ss = cs2.y;
-                y0 = __dsub_rn(__dmul_rn(x1, cc), __dmul_rn(x2, ss));
-                y1 = __dadd_rn(__dmul_rn(x2, cc), __dmul_rn(x1, ss));
+                if (KV == KV_FP8) {
+                    const double cc = cs2.x, ss = cs2.y;
+                    y0 = __dsub_rn(__dmul_rn((double)x1, cc), __dmul_rn((double)x2, ss));
+                    y1 = __dadd_rn(__dmul_rn((double)x2, cc), __dmul_rn((double)x1, ss));
+                } else {
+                    y0 = rotated_bf16(x1, cs2.x, x2, cs2.y);
+                    y1 = rotated_bf16(x2, cs2.x, -x1, cs2.y);
+                }
             } else if (!(KV == KV_FP8 && a.new_kind == NEW_STAGED)) {
                 y0 = kraw(d0);
                 if (pair) y1 = kraw(u + hr);
@@ -979,9 +977,8 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
                     knew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[t * kHeadDim + d]) * kscale;
                     vnew_t[t * kHeadDim + d] = e4m3_to_f32(code_t[vcode_off + t * kHeadDim + d]);
                 } else {
-                    // a rotated key is rounded once to bf16; other values are bf16 already
-                    knew_t[t * kHeadDim + d] =
-                        (pair && a.new_kind == NEW_ROTATE) ? f64_to_bf16_value(y) : (float)y;
+                    // (a rotated key was rounded once to bf16; other values are bf16 already)
+                    knew_t[t * kHeadDim + d] = (float)y;
                     vnew_t[t * kHeadDim + d] = vr;
                 }
             }
@@ -1329,10 +1326,10 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
     float *sink_s = MT ? rows_t : misc + 2 * kMaxGroup;                  // [G]
     float *gate_s = MT ? rows_t + kMaxRows : misc + 3 * kMaxGroup;       // [G]
     float *head_s = MT ? rows_t + 2 * kMaxRows : misc;   // [G] scale = sink factor * gate / L
-    // A single-token CTA of a single-layer launch holding the only chunk of its
-    // sequence finishes the rows itself: the new entry joins the maximum and the
-    // sum here.  (Step grids take the general combine below: the shorter path
-    // costs registers that their two-CTA-per-SM kernels do not have.)
+    // A single-token CTA holding the only chunk of its sequence finishes the rows
+    // itself: the new entry joins the maximum and the sum here.  (In step grids
+    // this measured 0.1-0.7 % faster than the general combine once their
+    // two-CTA kernels folded the producer and had registers to spare.)
     const bool finish = (NL == 1 || HD_STEP_FINISH) && !MT && nchunks == 1 && clus <= 1;
     if (threadIdx.x < G) {
         const int h = threadIdx.x, w0 = (h / CG) * WPG, hr = h % CG;

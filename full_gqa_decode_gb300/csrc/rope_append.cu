@@ -8,32 +8,20 @@
 // ring slot for this position (staged here, committed after the ring was
 // read), or a window shifted by one (roll).
 //
-// q is rotated in fp32 (it only feeds the attention).  The stored key is
-// rotated in fp64 from the fp32 table values: both products are exact, so
-// the result is one rounding of the exact rotation, and it is then rounded
-// once to bf16 via round-to-odd to binary32 (Boldo & Melquiond, "Emulation of
-// FMA and correctly rounded sums: proved algorithms using rounding to odd",
-// IEEE TC 2008): an odd-rounded binary32 carries enough bits that its
-// round-to-nearest-even to bf16 equals the direct rounding of the double.
-// An E4M3 cache stores e4m3(y / k_scale) of the same fp64 rotation y (one
-// fp64 division, one rounding) and e4m3(v / v_scale).
+// q is rotated in fp32 (it only feeds the attention).  The stored key is the
+// rotation from the fp32 table values, both products exact, rounded once to
+// bf16 (rope_round.cuh: a binary32 evaluation when it is provably far from a
+// rounding midpoint, else fp64 and round-to-odd).  An E4M3 cache stores
+// e4m3(y / k_scale) of the fp64 rotation y (one fp64 division, one rounding)
+// and e4m3(v / v_scale).
 #include "e4m3.cuh"
 #include "hd_internal.h"
+#include "rope_round.cuh"
 
 namespace hd {
 namespace {
 
 __device__ __forceinline__ void set_err(int32_t *err, int32_t bit) { atomicOr(err, bit); }
-
-// One round-to-nearest-even of a double to bf16, through round-to-odd binary32.
-__device__ __forceinline__ __nv_bfloat16 f64_to_bf16_rne(double x) {
-    float t = __double2float_rz(x);
-    if ((double)t != x && isfinite(t)) {
-        unsigned u = __float_as_uint(t) | 1u;   // sticky bit: round to odd
-        t = __uint_as_float(u);
-    }
-    return __float2bfloat16_rn(t);
-}
 
 // Rotated value of dim d of one head vector x (bf16, global), fp32 path.
 __device__ __forceinline__ float rope_f32(const __nv_bfloat16 *x, int d, int rot, const float2 *cs) {
@@ -59,12 +47,19 @@ __device__ __forceinline__ double rope_key_f64(const __nv_bfloat16 *x, int d, in
 // rotated key rounded once to bf16 and v bit for bit, or both as E4M3 codes.
 __device__ __forceinline__ void store_entry(const RopeArgs &a, size_t o, int h, const __nv_bfloat16 *kh,
                                             const __nv_bfloat16 *vh, int d, const float2 *cs) {
-    const double y = rope_key_f64(kh, d, a.rotary_dim, cs);
     if (a.kv_type == KV_FP8) {
+        const double y = rope_key_f64(kh, d, a.rotary_dim, cs);
         static_cast<uint8_t *>(a.dst_k)[o] = e4m3_quotient(y, (double)a.k_scale[h]);
         static_cast<uint8_t *>(a.dst_v)[o] = e4m3_quotient((double)__bfloat162float(vh[d]), (double)a.v_scale[h]);
     } else {
-        static_cast<__nv_bfloat16 *>(a.dst_k)[o] = d >= a.rotary_dim ? kh[d] : f64_to_bf16_rne(y);
+        __nv_bfloat16 k = kh[d];
+        if (d < a.rotary_dim) {
+            const int half = a.rotary_dim >> 1, i = d < half ? d : d - half;
+            const float x1 = __bfloat162float(kh[i]), x2 = __bfloat162float(kh[i + half]);
+            const float2 t = cs[i];
+            k = __float2bfloat16_rn(d < half ? rotated_bf16(x1, t.x, x2, t.y) : rotated_bf16(x2, t.x, -x1, t.y));
+        }
+        static_cast<__nv_bfloat16 *>(a.dst_k)[o] = k;
         static_cast<__nv_bfloat16 *>(a.dst_v)[o] = vh[d];
     }
 }

@@ -283,3 +283,63 @@ def test_single_layer_chunk_merge_paths(hd, orc, g, cluster):
     # the same layers again: the merge leaves nothing behind that the next call reads
     check_layer(hd, orc, ctx, 1, FULL, 0, LayerCase(rng, B, g * Hkv, Hkv, 6001, [6000, 3, 2047], sink=sink))
     ctx.close()
+
+
+def _near_midpoint_keys(orc, rng, context, Hkv, layer_type, tries=20000):
+    """New keys [B][Hkv][256] (bf16 bits) whose rotated pairs land within three
+    binary32 units of a bf16 rounding midpoint: the first output of even pairs,
+    the second of odd pairs.  Such values take the kernels' binary64 rounding
+    path; found by seeded random search (the expected bits come from the oracle)."""
+    rot, theta = synth.ROPE[layer_type]
+    half = rot // 2
+    B = len(context)
+    keys = synth.bits(synth.normal_bf16(rng, (B, Hkv, synth.HEAD_DIM)))
+    even = (np.arange(half) % 2 == 0)[:, None]
+    for b in range(B):
+        cs, sn = orc.rope_angles(int(context[b]), rot, theta)
+        c, s = cs.astype(np.float64)[:, None], sn.astype(np.float64)[:, None]
+        for h in range(Hkv):
+            f = rng.standard_normal((2, half, tries)).astype(np.float32).view(np.uint32)
+            cand = ((f + 0x7FFF + ((f >> 16) & 1)) >> 16).astype(np.uint16)       # nearest-even bf16
+            x1 = (cand[0].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            x2 = (cand[1].astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+            y = np.where(even, x1 * c - x2 * s, x2 * c + x1 * s)                # exact products, one rounding
+            low = (y.astype(np.float32).view(np.uint32) & 0xFFFF).astype(np.int64)
+            ok = (np.abs(low - 0x8000) <= 3) & (y != 0)
+            for i in range(half):
+                hit = np.flatnonzero(ok[i])
+                if len(hit):
+                    keys[b, h, i], keys[b, h, i + half] = cand[0, i, hit[0]], cand[1, i, hit[0]]
+    return keys
+
+
+@pytest.mark.parametrize("layer_type", [SLIDING, FULL])
+def test_new_keys_near_bf16_rounding_midpoints(hd, orc, layer_type):
+    """The written key is bf16_rne(x1 c - x2 s) of the exact rotation.  Keys whose
+    rotation sits next to a bf16 rounding midpoint -- where the kernels' binary32
+    evaluation defers to binary64 -- are stored bit-exactly, both by decode_step
+    (rotated in the attention kernel) and by rope_append_kv."""
+    rng = synth.generator(1600 + layer_type)
+    B, Hq, Hkv = 3, 8, 2
+    context = np.array([5, 700, 3000], np.int32)
+    cap = 511 if layer_type == SLIDING else 3001
+    case = LayerCase(rng, B, Hq, Hkv, cap, context)
+    case.k = torch.from_numpy(_near_midpoint_keys(orc, rng, context, Hkv, layer_type).view(np.int16)).view(torch.bfloat16)
+    ref = oracle_layer(orc, case, layer_type, RING)
+    # decode_step: the attention kernel rotates and stores the entry
+    ctx = make_ctx(hd, [layer_type], max_batch=B, max_context=3000)
+    kd, vd = case.kc.cuda(), case.vc.cuda()
+    out = torch.empty(B, Hq, 256, dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+    dev = (case.q.cuda(), case.k.cuda(), case.v.cuda())
+    io = [hd.layer_io(dev[0], dev[1], dev[2], hd.kv_cache(kd, vd), None, out, lse)]
+    hd.decode_step(ctx, torch.from_numpy(context).cuda(), io, B)
+    torch.cuda.synchronize()
+    assert hd.hybrid_decode_device_errors(ctx) == 0
+    assert_bits_equal(kd, ref["kcache"], "K cache written by decode_step")
+    assert_out_close(out, ref["out"])
+    # rope_append_kv + the attention call: the rope kernel stores the entry
+    ctx2 = make_ctx(hd, [layer_type], max_batch=B, max_context=3000)
+    got = check_layer(hd, orc, ctx2, 0, layer_type, RING, case)
+    ctx.close()
+    ctx2.close()
