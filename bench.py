@@ -478,7 +478,9 @@ def run_ours(args, world, rank, local) -> int:
     # KV bytes a step reads: the scored keys, or with several tokens per sequence
     # every pass's read of the cache
     step_kv = wl.token_pass_bytes() if args.tokens > 1 else wl.bytes
-    consumer = hd.HD_CONSUMER_TENSOR_CORE if args.consumer == "tensor-core" else hd.HD_CONSUMER_CUDA_CORE
+    consumer = {"tensor-core": hd.HD_CONSUMER_TENSOR_CORE, "cuda-core": hd.HD_CONSUMER_CUDA_CORE,
+                "tensor-memory": hd.HD_CONSUMER_TENSOR_MEMORY}[args.consumer]
+    tensor = consumer != hd.HD_CONSUMER_CUDA_CORE
     hd.hybrid_decode_set_consumer(wl.ctx, consumer)
     torch.cuda.synchronize()
 
@@ -487,7 +489,7 @@ def run_ours(args, world, rank, local) -> int:
     # layers), the dominant kernel, bracketed by events on its stream; the CUDA-core
     # consumer runs one kernel per layer, and the first full layer of every step is
     # bracketed (that launch alone runs without early start; the others overlap).
-    fused = consumer == hd.HD_CONSUMER_TENSOR_CORE and args.fusion == "on"
+    fused = tensor and args.fusion == "on"
     hd.hybrid_decode_set_step_fusion(wl.ctx, fused)
     kind = hd.HD_PROFILE_KIND_STEP if fused else hd.HD_FULL
     hd.hybrid_decode_set_profiling(wl.ctx, hd.HD_PROFILE_STEP if fused else hd.HD_PROFILE_FULL | hd.HD_PROFILE_FIRST_ONLY)
@@ -560,13 +562,13 @@ def run_ours(args, world, rank, local) -> int:
     if rank == 0:
         fp8 = fp8_step(device, args, consumer, layout, plain_ms) if args.kv == "bf16" and args.secondary else None
         multi = (multi_token_steps(device, args, consumer, layout, plain_ms)
-                 if args.kv == "bf16" and args.secondary and args.layout == "ring" and consumer == hd.HD_CONSUMER_TENSOR_CORE
+                 if args.kv == "bf16" and args.secondary and args.layout == "ring" and tensor
                  else None)
         cpu = cpu_baseline(wl, device)
         secondary = secondary_batch1(device, args, consumer) if args.secondary else None
         others = (baseline_configs(device, args, consumer, read_peak)
                   if args.secondary and args.kv == "bf16" and args.workload == DEFAULT_WORKLOAD
-                  and consumer == hd.HD_CONSUMER_TENSOR_CORE else None)
+                  and tensor else None)
         result = {"metric": METRIC, "value": round(gbs, 1), "unit": "GB/s", "n_gpus": world,
                   "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_max, 4),
                   "us_per_step": round(ms_max * 1e3, 1), "higher_is_better": True, "scaling": "weak",
@@ -724,7 +726,7 @@ def fp8_step(device, args, consumer, layout, bf16_ms) -> dict:
     wl = Workload(args.workload, device, seed=0, layout=layout, kv="fp8")
     hd.hybrid_decode_set_consumer(wl.ctx, consumer)
     ms = time_steps(wl.step, args.steps, args.warmup, 1, device)
-    fused = consumer == hd.HD_CONSUMER_TENSOR_CORE
+    fused = consumer != hd.HD_CONSUMER_CUDA_CORE
     grid_ms, grid_n = 0.0, 0
     if fused:
         hd.hybrid_decode_set_profiling(wl.ctx, hd.HD_PROFILE_STEP)
@@ -781,6 +783,14 @@ def multi_token_steps(device, args, consumer, layout, single_ms) -> list:
         res.append({"tokens": T, "ms_per_step": round(ms, 4), "tokens_per_s": round(wl.B * T / (ms * 1e-3)),
                     "us_per_token": round(ms * 1e3 / T, 1), "speedup_vs_single_token_steps": round(T * single_ms / ms, 3),
                     "kv_bytes_read_per_step": kvb, "GBps": round(kvb / (ms * 1e-3) / 1e9, 1)})
+        if (wl.Hq // wl.Hkv) * T == 16 and consumer == hd.HD_CONSUMER_TENSOR_CORE:
+            # the same 16-row passes on tcgen05 (tensor memory), measured beside the default
+            hd.hybrid_decode_set_consumer(wl.ctx, hd.HD_CONSUMER_TENSOR_MEMORY)
+            ms_tm = time_steps(wl.step, args.steps, args.warmup, 1, device)
+            if hd.hybrid_decode_device_errors(wl.ctx):
+                raise RuntimeError(f"device error flags in the {T}-token step (tensor memory)")
+            res[-1]["tensor_memory_consumer"] = {"ms_per_step": round(ms_tm, 4),
+                                                 "GBps": round(kvb / (ms_tm * 1e-3) / 1e9, 1)}
         wl.ctx.close()
         del wl
         torch.cuda.empty_cache()
@@ -914,8 +924,8 @@ def main(argv=None) -> int:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(synth.WORKLOADS))
     ap.add_argument("--no-secondary", dest="secondary", action="store_false")
-    ap.add_argument("--consumer", choices=["tensor-core", "cuda-core"], default="tensor-core",
-                    help="inner loop of the attention kernels")
+    ap.add_argument("--consumer", choices=["tensor-core", "cuda-core", "tensor-memory"], default="tensor-core",
+                    help="inner loop of the attention kernels (tensor-memory: tcgen05 for 16-row multi-token passes)")
     ap.add_argument("--layout", choices=["ring", "roll"], default="ring",
                     help="cache layout of the sliding layers")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",

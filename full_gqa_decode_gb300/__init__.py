@@ -23,7 +23,7 @@ LIBRARY = os.path.join(PKG, "libhybriddecode.so")
 
 HD_SLIDING, HD_FULL = 0, 1
 HD_LAYOUT_AUTO, HD_LAYOUT_RING, HD_LAYOUT_ROLL = 0, 1, 2
-HD_CONSUMER_CUDA_CORE, HD_CONSUMER_TENSOR_CORE = 0, 1
+HD_CONSUMER_CUDA_CORE, HD_CONSUMER_TENSOR_CORE, HD_CONSUMER_TENSOR_MEMORY = 0, 1, 2
 HD_PROFILE_SLIDING, HD_PROFILE_FULL, HD_PROFILE_FIRST_ONLY, HD_PROFILE_STEP = 1 << HD_SLIDING, 1 << HD_FULL, 4, 8
 HD_PROFILE_KIND_STEP = 2
 HD_KV_BF16, HD_KV_FP8_E4M3 = 0, 1
@@ -387,7 +387,8 @@ def hybrid_decode_set_cluster_combine(ctx: Context, enable: bool) -> None:
 
 
 def hybrid_decode_set_consumer(ctx: Context, consumer: int) -> None:
-    """HD_CONSUMER_CUDA_CORE or HD_CONSUMER_TENSOR_CORE (the default)."""
+    """HD_CONSUMER_CUDA_CORE, HD_CONSUMER_TENSOR_CORE (the default) or
+    HD_CONSUMER_TENSOR_MEMORY (tcgen05 for 16-row multi-token passes over bf16 caches)."""
     _check(_lib.hybrid_decode_set_consumer(ctx.handle, consumer), "hybrid_decode_set_consumer")
 
 

@@ -457,7 +457,7 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
         const size_t slot = 2 * (size_t)kProfileEvents + ctx->ev_used[2];
         const bool timed = (ctx->profile_mask & HD_PROFILE_STEP) && ctx->ev_used[2] < (size_t)kProfileEvents;
         if (timed && cudaEventRecord(ctx->ev_begin[slot], stream) != cudaSuccess) return HD_ERR_CUDA;
-        hd_status st = cuda_status(launch_step(t, (int)ctas, (int)rows, mt, ctx->kv_type, stages, stream));
+        hd_status st = cuda_status(launch_step(t, (int)ctas, (int)rows, mt, ctx->kv_type, ctx->consumer, stages, stream));
         if (st != HD_OK) return st;
         ++ctx->launches;
         if (timed) {
@@ -845,7 +845,7 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
                              int32_t max_context_hint, const hd_layer_io *layers, void *stream) {
     if (!ctx || !layers || num_tokens < 1 || num_tokens > kMaxTokens) return HD_ERR_INVALID_ARG;
     if (check_device(ctx) != HD_OK) return HD_ERR_STATE;
-    if (num_tokens > 1 && ctx->consumer != CONSUMER_MMA) return HD_ERR_UNSUPPORTED;
+    if (num_tokens > 1 && !tensor_consumer(ctx->consumer)) return HD_ERR_UNSUPPORTED;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     ctx->profile_seen[0] = ctx->profile_seen[1] = false;
     // Every layer is checked before anything is launched.
@@ -859,7 +859,7 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
     // Independent layers (the call's contract) may share one grid, or overlap as
     // one kernel per layer; layers that alias run one kernel per layer in full order.
     const bool indep = layers_independent(ctx, batch, num_tokens, layers);
-    const bool fused = ctx->fuse_step && ctx->consumer == CONSUMER_MMA && indep;
+    const bool fused = ctx->fuse_step && tensor_consumer(ctx->consumer) && indep;
     std::vector<LayerCall> &calls = ctx->step_calls;
     calls.assign(ctx->cfg.num_layers, LayerCall{});
     for (int i = 0; i < ctx->cfg.num_layers; ++i) {
@@ -961,9 +961,12 @@ hd_status hybrid_decode_inject_lost_copy(hd_ctx *ctx, int32_t stage) {
 
 hd_status hybrid_decode_set_consumer(hd_ctx *ctx, int32_t consumer) {
     if (!ctx) return HD_ERR_INVALID_ARG;
-    if (consumer != HD_CONSUMER_CUDA_CORE && consumer != HD_CONSUMER_TENSOR_CORE)
-        return HD_ERR_INVALID_ARG;
-    ctx->consumer = consumer == HD_CONSUMER_TENSOR_CORE ? CONSUMER_MMA : CONSUMER_FMA;
+    switch (consumer) {
+    case HD_CONSUMER_CUDA_CORE: ctx->consumer = CONSUMER_FMA; break;
+    case HD_CONSUMER_TENSOR_CORE: ctx->consumer = CONSUMER_MMA; break;
+    case HD_CONSUMER_TENSOR_MEMORY: ctx->consumer = CONSUMER_UMMA; break;
+    default: return HD_ERR_INVALID_ARG;
+    }
     return HD_OK;
 }
 

@@ -43,10 +43,12 @@ cudaError_t launch_layer(const CUtensorMap *km, const CUtensorMap *vm, const Lay
                                : launch_layer_bf16(t, grid, rows, mt, consumer, stages, pdl, s);
 }
 
-cudaError_t launch_step(const StepTable &t, int num_ctas, int rows, bool mt, int kv, int stages, cudaStream_t s) {
+cudaError_t launch_step(const StepTable &t, int num_ctas, int rows, bool mt, int kv, int consumer, int stages,
+                        cudaStream_t s) {
     if (t.num_layers < 1 || t.num_layers > kStepLayers || num_ctas < 1) return cudaErrorInvalidValue;
     const dim3 grid(num_ctas);
-    return kv == KV_FP8 ? launch_step_fp8(t, grid, rows, mt, stages, s) : launch_step_bf16(t, grid, rows, mt, stages, s);
+    return kv == KV_FP8 ? launch_step_fp8(t, grid, rows, mt, stages, s)
+                        : launch_step_bf16(t, grid, rows, mt, consumer, stages, s);
 }
 
 }  // namespace hd

@@ -87,12 +87,26 @@ constexpr int kConsumerWarps = 4;   // per CTA; 16-row multi-token passes run tw
 __host__ __device__ constexpr bool own_producer(int kv, int nl, bool mt, bool deep) {
     return kv == KV_BF16 && (nl == 1 || mt || deep);
 }
-// 16 query rows run one CTA per SM: eight consumer warps (two per row group of
-// eight rows and stage half) keep as many warps per SM as two 8-row CTAs.
-__host__ __device__ constexpr int consumer_warps(int g) { return g > kMaxGroup ? 2 * kConsumerWarps : kConsumerWarps; }
-__host__ __device__ constexpr int layer_threads(int g, int kv, int nl, bool mt, bool deep) {
-    return (consumer_warps(g) + (own_producer(kv, nl, mt, deep) ? 1 : 0)) * 32;
+// With the tensor-memory consumer, a 16-row multi-token pass over a bf16 cache
+// (one CTA per SM) runs on the tcgen05 tensor cores: four softmax warps, the
+// producer warp and one warp that owns the tensor memory and issues the MMAs
+// (see "Tensor-memory pass" below).
+__host__ __device__ constexpr bool umma_pass(int g, int kv, bool mt, bool deep, int consumer) {
+    return consumer == CONSUMER_UMMA && kv == KV_BF16 && mt && g == kMaxRows && deep;
 }
+// 16 query rows on mma.sync run one CTA per SM: eight consumer warps (two per row
+// group of eight rows and stage half) keep as many warps per SM as two 8-row CTAs.
+__host__ __device__ constexpr int consumer_warps(int g) { return g > kMaxGroup ? 2 * kConsumerWarps : kConsumerWarps; }
+__host__ __device__ constexpr int layer_threads(int g, int kv, int nl, bool mt, bool deep,
+                                                int consumer = CONSUMER_MMA) {
+    return umma_pass(g, kv, mt, deep, consumer) ? (kConsumerWarps + 2) * 32
+                                      : (consumer_warps(g) + (own_producer(kv, nl, mt, deep) ? 1 : 0)) * 32;
+}
+// Shared memory of a tensor-memory pass past the common layout: two P^T buffers
+// of 64 keys x 16 rows (bf16), the softmax warps' row maxima and sums, fifteen
+// mbarriers and the tensor-memory address.
+constexpr int kUmmaPBytes = 64 * kMaxRows * 2;
+constexpr int kUmmaExtraBytes = 128 + 2 * kUmmaPBytes + 3 * kConsumerWarps * kMaxRows * 4 + 16 * 8 + 16;
 // A ring of more than the default bytes: one CTA per SM.
 __host__ __device__ constexpr bool deep_ring(int s, int kv) { return s * kv_stage_bytes(kv) > kStages * kStageBytes; }
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
@@ -121,6 +135,18 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t by
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+// Non-blocking test of a phase (the tensor-memory pass's MMA warp polls two barriers).
+__device__ __forceinline__ bool mbar_test_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
 }
 __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     uint32_t ok;
@@ -256,6 +282,75 @@ __device__ __forceinline__ void unpack_bf16x8(const uint4 &r, float (&f)[8]) {
         f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
     }
 }
+// ---------------------------------------------------------- tcgen05 helpers --
+// Tensor memory: 128 lanes x 512 columns of 32-bit cells per SM.  An address is
+// (lane << 16) | column; a warp reads the 32 lanes of its quarter (warp id % 4).
+__device__ __forceinline__ void tmem_alloc(uint32_t *dst_smem, uint32_t ncols) {   // whole warp
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {   // whole warp
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+// Shared-memory matrix descriptor: start, leading and stride byte offsets (16-byte
+// units), the fixed version field, and the swizzle (2: 128-byte, 0: none).  For a
+// 128-byte-swizzled K-major tile the stride offset steps 8-row groups and a k-step
+// of 16 elements advances the start by 32 bytes inside the 1024-byte atom; for
+// MN-major tiles the leading offset steps along M/N and the stride along K
+// (128-byte swizzle), the other way round without swizzle.
+__device__ __forceinline__ uint64_t umma_desc(uint32_t addr, uint32_t lbo, uint32_t sbo, uint32_t swizzle) {
+    return (uint64_t)((addr & 0x3FFFFu) >> 4) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
+           ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | ((uint64_t)swizzle << 61);
+}
+// Instruction descriptor of kind::f16: fp32 accumulator, bf16 A and B, K-major (0)
+// or MN-major (1) operands, N / 8 and M / 16.
+__host__ __device__ constexpr uint32_t umma_idesc_bf16(int m, int n, int a_mn, int b_mn) {
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)a_mn << 15) | ((uint32_t)b_mn << 16) |
+           ((uint32_t)(n >> 3) << 17) | ((uint32_t)(m >> 4) << 24);
+}
+// D (+)= A B^T on the tensor cores, issued by one thread.
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a, uint64_t b, uint32_t idesc, bool acc) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(a), "l"(b), "r"(idesc), "r"((uint32_t)acc)
+        : "memory");
+}
+// The mbarrier receives one arrival once every MMA this thread issued so far is complete.
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+// 32 consecutive columns of this thread's lane, then the wait for the load.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+    uint32_t r[32];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+// Byte offset of element (operand row n, dim d) of the q operand: 2G rows (the
+// high parts of rows 0..G-1, then their low parts) x 256 dims, K-major in column
+// blocks of 64 dims x 2G rows x 128 bytes, 16-byte chunks swizzled.
+template <int G>
+__device__ __forceinline__ uint32_t umma_q_offset(int n, int d) {
+    return (d >> 6) * (2 * G * 128) + n * 128 + ((((d >> 3) & 7) ^ (n & 7)) << 4) + 2 * (d & 7);
+}
+// Tensor-memory columns of a pass: scores S^T (2 x 32: high, low) at 0, O^T (2 x 32) at 64.
+constexpr uint32_t kUmmaCols = 128;
+
 // q, once rotated and scaled, is kept as one 32-bit word per element: the value
 // rounded to 16 bits in the low half and the remainder rounded to 16 bits in the
 // high half -- bf16 with bf16 caches, f16 with E4M3 caches (the operand types of
@@ -805,15 +900,20 @@ struct Fp8MmaConsumer {
 // consumer's registers.
 // NL: layers in the parameter table (1: one layer, grid (chunks, kv heads,
 // sequences); kStepLayers: a step, 1-D grid over the layers' CTA ranges).
-template <int G, int CONSUMER, int S, int KV, bool MT, int NL>
-__global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV)), deep_ring(S, KV) ? 1 : 2)
+template <int G, int CONSUMER, int SP, int KV, bool MT, int NL>
+__global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV), CONSUMER), deep_ring(SP, KV) ? 1 : 2)
     attn_layer_kernel(const __grid_constant__ LaunchTable<NL> p) {
-    constexpr int kStage = kv_stage_bytes(KV);     // bytes of one stage (K + V)
-    constexpr int kKeys = kv_stage_keys(KV);       // keys per stage: 32 bf16, 64 E4M3
+    // SP: the ring in 32 KiB stages.  A tensor-memory pass takes them in pairs:
+    // 64-key stages, each K or V box column two 32-row boxes one after the other.
+    constexpr bool kUmma = umma_pass(G, KV, MT, deep_ring(SP, KV), CONSUMER);
+    constexpr int S = kUmma ? SP / 2 : SP;                               // ring slots
+    constexpr int kStage = (kUmma ? 2 : 1) * kv_stage_bytes(KV);        // bytes of one stage (K + V)
+    constexpr int kKeys = (kUmma ? 2 : 1) * kv_stage_keys(KV);          // keys per stage: 32 bf16, 64 E4M3 or tcgen05
+    constexpr int kBoxB = (kUmma ? 2 : 1) * kv_box_bytes(KV);           // bytes of one box column of a stage
     constexpr int kBoxes = kv_boxes_per_row(KV);   // 128-byte boxes per K or V row
-    constexpr int kNThreads = layer_threads(G, KV, NL, MT, deep_ring(S, KV));
-    constexpr bool kOwnProducer = own_producer(KV, NL, MT, deep_ring(S, KV));
-    constexpr int CW = consumer_warps(G);          // consumer warps
+    constexpr int kNThreads = layer_threads(G, KV, NL, MT, deep_ring(SP, KV), CONSUMER);
+    constexpr bool kOwnProducer = own_producer(KV, NL, MT, deep_ring(SP, KV));
+    constexpr int CW = kUmma ? kConsumerWarps : consumer_warps(G);      // consumer (softmax) warps
     extern __shared__ uint8_t smem_raw[];
     // The ring starts on a 1024-byte boundary of the shared window (the 128-byte
     // swizzle repeats every 1024 bytes).  Offsetting the array pointer, rather than
@@ -832,6 +932,17 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
     unsigned *rel_s = reinterpret_cast<unsigned *>(flag_s + 4);                // [S] slot releases (folded producer)
     uint8_t *code_s = reinterpret_cast<uint8_t *>(rel_s + 16);                 // [2][256] E4M3 new entry
     int *mcnt_s = reinterpret_cast<int *>(code_s + 2 * kHeadDim);               // [kMaxRows] MT ring masks
+    // Tensor-memory pass: P^T buffers, the softmax warps' row maxima (two sets) and
+    // sums, its mbarriers and the tensor-memory address (kUmmaExtraBytes).
+    uint8_t *u_base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(mcnt_s + kMaxRows) + 127) & ~static_cast<uintptr_t>(127));
+    uint8_t *p_s = u_base;                                                           // [2][64 keys x 16 rows] bf16
+    float *umax_s = reinterpret_cast<float *>(p_s + 2 * kUmmaPBytes);               // [2][warps][16]
+    float *usum_s = umax_s + 2 * kConsumerWarps * kMaxRows;                         // [warps][16]
+    // s[2] p[2] o[2] done x[2], then the V halves' full[3] and empty[3] (the K halves use full / empty)
+    uint64_t *ubar = reinterpret_cast<uint64_t *>(usum_s + kConsumerWarps * kMaxRows);
+    uint64_t *fullv = ubar + 9, *emptyv = ubar + 12;
+    uint32_t *taddr_s = reinterpret_cast<uint32_t *>(ubar + 16);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // This CTA's layer: the last one whose CTA range starts at or before it
@@ -986,18 +1097,37 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
     };
 
     // Stage s of the chunk: one lane issues its K and V boxes into slot s % S.
+    // A tensor-memory pass loads (and releases) a stage's K and V halves separately:
+    // the K half is free once its scores are computed.
+    auto issue_half = [&](int s, int v) {
+        const int slot = s % S;
+        uint8_t *st = smem + slot * kStage + v * kBoxes * kBoxB;
+        uint64_t *bar = v ? &fullv[slot] : &full[slot];
+        mbar_arrive_expect_tx(bar, kStage / 2);
+        const int row = roff + start + s * kKeys;
+#pragma unroll
+        for (int j = 0; j < kBoxes; ++j)
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                tma_load_4d(st + j * kBoxB + h * kv_box_bytes(KV), v ? &ll.vmap : &ll.kmap, bar, j * kv_box_cols(KV),
+                            row + h * kv_stage_keys(KV), kvh, b);
+    };
     auto issue_stage = [&](int s) {
+        if constexpr (kUmma) {
+            issue_half(s, 0);
+            issue_half(s, 1);
+            return;
+        }
         const int slot = s % S;
         uint8_t *st = smem + slot * kStage;
         mbar_arrive_expect_tx(&full[slot], kStage);
         const int row = roff + start + s * kKeys;
 #pragma unroll
         for (int j = 0; j < kBoxes; ++j)
-            tma_load_4d(st + j * kv_box_bytes(KV), &ll.kmap, &full[slot], j * kv_box_cols(KV), row, kvh, b);
+            tma_load_4d(st + j * kBoxB, &ll.kmap, &full[slot], j * kv_box_cols(KV), row, kvh, b);
 #pragma unroll
         for (int j = 0; j < kBoxes; ++j)
-            tma_load_4d(st + (kBoxes + j) * kv_box_bytes(KV), &ll.vmap, &full[slot], j * kv_box_cols(KV), row, kvh,
-                        b);
+            tma_load_4d(st + (kBoxes + j) * kBoxB, &ll.vmap, &full[slot], j * kv_box_cols(KV), row, kvh, b);
     };
     // Test hook: stages from a.drop_stage on are never issued (a copy that never arrives).
     auto droppable = [&](int s) { return a.drop_stage >= 0 && s >= a.drop_stage; };
@@ -1055,12 +1185,23 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
     if (threadIdx.x == kIssuer) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], CW);
+            mbar_init(&empty[s], kUmma ? 1 : CW);   // tensor-memory pass: released by an MMA commit
             rel_s[s] = 0u;
+        }
+        if constexpr (kUmma) {
+            static_assert(S <= 3, "three V-half barriers of each kind");
+            for (int i = 0; i < 15; ++i) mbar_init(&ubar[i], (i >= 2 && i < 4) || i == 7 || i == 8 ? kConsumerWarps : 1);
         }
         fence_mbar_init();
         if (kIssueEarly)
             for (int s = 0; s < early && !droppable(s); ++s) issue_stage(s);
+    }
+
+    if constexpr (kUmma) {
+        if (warp == CW + 1) {   // the MMA warp owns the tensor memory of the pass
+            tmem_alloc(taddr_s, kUmmaCols);
+            tc_fence_before();
+        }
     }
 
     // Round 1 lands: q in shared memory as fp32, the rotary row, the new entry
@@ -1104,7 +1245,45 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
     // and scale every dim to log2 units.
     // (each element's word replaces its fp32 value in place)
     uint32_t *q_w = reinterpret_cast<uint32_t *>(q_s);
-    if (a.q_bf16) {
+    if constexpr (kUmma) {
+        // The B operand of S^T = K Q^T: operand rows 0..G-1 hold the bf16 high parts
+        // of the q rows and rows G..2G-1 their low parts, K-major with the 128-byte
+        // swizzle; a key's two scores are added after the MMA.  (One MMA costs the
+        // same for N = 16 and N = 32, so the split costs no extra instructions.)
+        // Every element is rotated and split into registers first, then written over
+        // the fp32 rows.
+        constexpr int kPer = (G * kHeadDim + kNThreads - 1) / kNThreads;
+        uint32_t wv[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int e = threadIdx.x + k * kNThreads;
+            float v = 0.f;
+            if (e < G * kHeadDim) {
+                const int r = e / kHeadDim, j = e % kHeadDim;
+                v = q_s[e];
+                if (a.q_bf16 && j < 2 * half) {
+                    const int jj = j < half ? j : j - half;
+                    const float2 t = a.table[(size_t)(c + r / Gm) * half + jj];   // position c + token
+                    const float x1 = q_s[r * kHeadDim + jj], x2 = q_s[r * kHeadDim + jj + half];
+                    v = j < half ? fmaf(x1, t.x, -x2 * t.y) : fmaf(x2, t.x, x1 * t.y);
+                }
+                v *= kQScale;
+            }
+            wv[k] = q_split<KV>(v);
+        }
+        __syncthreads();   // every read of the fp32 rows comes before the first write
+        uint16_t *q16 = reinterpret_cast<uint16_t *>(q_s);
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int e = threadIdx.x + k * kNThreads;
+            if (e < G * kHeadDim) {
+                const int r = e / kHeadDim, j = e % kHeadDim;
+                q16[umma_q_offset<G>(r, j) / 2] = (uint16_t)(wv[k] & 0xFFFFu);
+                q16[umma_q_offset<G>(G + r, j) / 2] = (uint16_t)(wv[k] >> 16);
+            }
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // visible to the tensor cores
+    } else if (a.q_bf16) {
         for (int p = threadIdx.x; p < G * half; p += blockDim.x) {
             const int r = p / half, j = p % half;
             const float2 t = MT ? a.table[(size_t)(c + r / Gm) * half + j] : tab_s[j];   // position c + token
@@ -1155,10 +1334,12 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
     }
 
     // Row groups: RG groups of CG rows; each group's WPG warps split every stage.
-    constexpr int RG = G > 8 ? G / 8 : 1, CG = G / RG, WPG = CW / RG;
-    float *red_o = reinterpret_cast<float *>(smem);             // [warps][CG][256], reuses the stage ring
-    float *red_m = red_o + CW * CG * kHeadDim;
-    float *red_l = red_m + CW * CG;
+    // (A tensor-memory pass leaves one partial of all G rows.)
+    constexpr int RG = kUmma ? 1 : (G > 8 ? G / 8 : 1), CG = G / RG, WPG = kUmma ? 1 : CW / RG;
+    constexpr int NRW = RG * WPG;                                // warp partials per row
+    float *red_o = reinterpret_cast<float *>(smem);             // [NRW][CG][256], reuses the stage ring
+    float *red_m = red_o + NRW * CG * kHeadDim;
+    float *red_l = red_m + NRW * CG;
     if (kOwnProducer && warp == CW) {
         if (MT && sh > 0) {
             // Multi-token pass over a rolled window (bf16): the producer warp moves
@@ -1170,7 +1351,9 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
             const size_t seq = ((size_t)b * a.seq_stride + (size_t)kvh * a.capacity * kHeadDim) * kv_elem_bytes(KV);
             for (int s = 0; s < nst; ++s) {
                 const int slot = s % S;
-                if (!__all_sync(0xffffffffu, mbar_wait(&full[slot], (s / S) & 1))) {
+                bool landed = mbar_wait(&full[slot], (s / S) & 1);
+                if constexpr (kUmma) landed = landed && mbar_wait(&fullv[slot], (s / S) & 1);
+                if (!__all_sync(0xffffffffu, landed)) {
                     if (lane == 0) atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
@@ -1180,8 +1363,8 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
                     const int v = i >= nrows * kChunks, rem = i - v * nrows * kChunks;
                     const int r = rem / kChunks, ch = rem % kChunks, row = key0 + r + roff;
                     if (row < sh) continue;
-                    const uint4 x = *reinterpret_cast<const uint4 *>(st + v * kBoxes * kv_box_bytes(KV) +
-                                                                     tile_offset<KV>(r, ch));
+                    const uint4 x = *reinterpret_cast<const uint4 *>(
+                        st + v * kBoxes * kBoxB + (ch >> 3) * kBoxB + r * 128 + ((((ch & 7) ^ (r & 7))) << 4));
                     *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(v ? a.cache_v : a.cache_k) + seq +
                                                (size_t)(row - sh) * kHeadDim * kv_elem_bytes(KV) + 16 * ch) = x;
                 }
@@ -1190,7 +1373,8 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
                 if (lane == 0 && s + S < nst) {
                     if (droppable(s + S)) {
                         stop = 1;
-                    } else if (!mbar_wait(&empty[slot], (s / S) & 1)) {
+                    } else if (!mbar_wait(&empty[slot], (s / S) & 1) ||
+                               (kUmma && !mbar_wait(&emptyv[slot], (s / S) & 1))) {
                         atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
                         stop = 1;
                     } else {
@@ -1201,19 +1385,253 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
                 }
                 if (__shfl_sync(0xffffffffu, stop, 0)) break;
             }
-        } else if (lane == 0) {  // producer: one lane issues every load of the chunk
+        } else if (lane < (kUmma ? 2 : 1)) {
+            // producer: one lane issues every load of the chunk (a tensor-memory pass:
+            // lane 0 the K halves, lane 1 the V halves, each as its half is released)
             for (int s = early; s < nst; ++s) {
                 if (droppable(s)) break;
                 const int slot = s % S;
-                if (s >= S && !mbar_wait(&empty[slot], ((s / S) - 1) & 1)) {
+                uint64_t *emp = kUmma && lane == 1 ? &emptyv[slot] : &empty[slot];
+                if (s >= S && !mbar_wait(emp, ((s / S) - 1) & 1)) {
                     atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
-                issue_stage(s);
+                if constexpr (kUmma)
+                    issue_half(s, lane);
+                else
+                    issue_stage(s);
             }
         }
         __syncthreads();
         __syncthreads();
+    } else if constexpr (kUmma) {
+        // Tensor-memory pass (16 query rows, 64-key stages).  Per stage s:
+        //   S^T = K Q^T        tcgen05 M=64 (keys) x N=32 (rows: q high, q low) x K=256,
+        //                      A = the K tile, B = the q operand; into columns 32 (s % 2)
+        //   softmax            four warps: lane l < 16 of warp w scores key 16w + l for all
+        //                      rows (high + low); row maxima over warps through shared
+        //                      memory; P^T in bf16 to shared memory (MN-major, no swizzle)
+        //   O^T_s = V^T P^T    M=128 (dims, two halves) x N=16 x K=64 keys, A = the V tile
+        //                      read MN-major; into columns 64 + 32 (s % 2), a fresh sum
+        //   o = o * alpha_s + O^T_s   in the softmax warps' registers (lane = dim)
+        // The MMA warp issues S^T of stage s + 1 before O^T of stage s, so the softmax of
+        // one stage overlaps the MMAs of its neighbours; the commit after O^T_s releases
+        // the slot.  Every wait is bounded and warp-uniform.
+        if (warp == CW + 1) {
+            tc_fence_after();
+            const uint32_t tbase = *taddr_s;
+            if (lane == 0) {
+                constexpr uint32_t kIdQK = umma_idesc_bf16(64, 2 * G, 0, 0);
+                constexpr uint32_t kIdPV = umma_idesc_bf16(128, G, 1, 1);
+                // Descriptors are built once; an operand's k-step or slot only moves the
+                // start-address field (16-byte units; shared addresses stay below 2^18),
+                // so each MMA costs one 64-bit add per operand.
+                const uint64_t kd0 = umma_desc(smem_u32(smem), 16, 1024, 2);                    // K tiles
+                const uint64_t vd0 = umma_desc(smem_u32(smem) + kBoxes * kBoxB, kBoxB, 1024, 2);  // V tiles
+                const uint64_t qd0 = umma_desc(smem_u32(q_s), 16, 1024, 2);
+                const uint64_t pd0 = umma_desc(smem_u32(p_s), 256, 128, 0);
+                // Event loop: O^T of the oldest scored stage as soon as its P^T (and V
+                // half) is there, else the scores of the next stage whose K half has
+                // landed -- at most one stage ahead of the softmax warps (two score
+                // buffers).  Each commit releases what its MMAs read.
+                int q = 0, pv = 0;   // next stage to score, next stage to weight
+                unsigned long long t_last = globaltimer_ns();
+                unsigned spins = 0;
+                while (pv < nst) {
+                    if (pv < q && mbar_test_wait(&fullv[pv % S], (pv / S) & 1) &&
+                        mbar_test_wait(&ubar[2 + (pv & 1)], (pv >> 1) & 1)) {
+                        tc_fence_after();
+                        const uint64_t vd = vd0 + (uint64_t)((pv % S) * (kStage >> 4));
+                        const uint64_t pd = pd0 + (uint64_t)((pv & 1) * (kUmmaPBytes >> 4));
+                        const uint32_t dO = tbase + 64 + (pv & 1) * 32;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int t = 0; t < 4; ++t)
+                                umma_bf16(dO + h * 16, vd + (uint64_t)((2 * h * kBoxB + t * 2048) >> 4),
+                                          pd + (uint64_t)((t * 512) >> 4), kIdPV, t > 0);
+                        umma_commit(&ubar[4 + (pv & 1)]);
+                        umma_commit(&emptyv[pv % S]);
+                        ++pv;
+                        spins = 0;
+                    } else if (q < nst && q <= pv + 1 && mbar_test_wait(&full[q % S], (q / S) & 1)) {
+                        tc_fence_after();
+                        const uint64_t kd = kd0 + (uint64_t)((q % S) * (kStage >> 4));
+                        const uint32_t dS = tbase + (q & 1) * 32;
+#pragma unroll
+                        for (int kk = 0; kk < 16; ++kk)
+                            umma_bf16(dS, kd + (uint64_t)(((kk >> 2) * kBoxB + (kk & 3) * 32) >> 4),
+                                      qd0 + (uint64_t)(((kk >> 2) * (2 * G * 128) + (kk & 3) * 32) >> 4), kIdQK, kk > 0);
+                        umma_commit(&ubar[q & 1]);
+                        umma_commit(&empty[q % S]);
+                        ++q;
+                        spins = 0;
+                    } else if (++spins == 1) {
+                        t_last = globaltimer_ns();
+                    } else if ((spins & 63) == 0 && globaltimer_ns() - t_last > kWaitLimitNs) {
+                        atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
+                        break;
+                    }
+                }
+                // every MMA issued above is complete before the tensor memory is freed
+                umma_commit(&ubar[6]);
+                if (!mbar_wait(&ubar[6], 0)) atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
+            }
+            __syncwarp();
+            __syncthreads();
+            __syncthreads();
+        } else {
+            static_assert(G == 16, "one tcgen05.ld of 32 score columns (high, low) per stage");
+            tc_fence_after();
+            const uint32_t tl = *taddr_s + ((uint32_t)(32 * warp) << 16);   // this warp's lane quarter
+            const int kl = lane & 15;
+            float m_run[G], l_part[G], al_prev[G], o_acc[2 * G];
+            int cnt[G];
+#pragma unroll
+            for (int r = 0; r < G; ++r) {
+                m_run[r] = -INFINITY;
+                l_part[r] = 0.f;
+                al_prev[r] = 1.f;
+                o_acc[r] = 0.f;
+                o_acc[G + r] = 0.f;
+                cnt[r] = mcnt_s[r];
+            }
+            bool ok = true;
+            auto fail = [&]() {
+                if (lane == 0) atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
+                ok = false;
+            };
+            // O^T of stage ps joins the running sum (its rows rescaled by alpha_ps).
+            auto fold = [&](int ps) -> bool {
+                if (!__all_sync(0xffffffffu, mbar_wait(&ubar[4 + (ps & 1)], (ps >> 1) & 1))) return false;
+                tc_fence_after();
+                float ov[2 * G];
+                tmem_ld32(tl + 64 + (ps & 1) * 32, ov);
+#pragma unroll
+                for (int r = 0; r < G; ++r) {
+                    o_acc[r] = fmaf(o_acc[r], al_prev[r], ov[r]);
+                    o_acc[G + r] = fmaf(o_acc[G + r], al_prev[r], ov[G + r]);
+                }
+                return true;
+            };
+            for (int s = 0; s < nst; ++s) {
+                const int sb = s & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(&ubar[sb], (s >> 1) & 1))) {
+                    fail();
+                    break;
+                }
+                tc_fence_after();
+                float x[G];
+                {
+                    float hl[2 * G];
+                    tmem_ld32(tl + sb * 32, hl);
+#pragma unroll
+                    for (int r = 0; r < G; ++r) x[r] = hl[r] + hl[G + r];
+                }
+                const int kin = 16 * warp + kl;   // this lane's key in the stage (lanes < 16)
+                const int key = start + s * kKeys + kin;
+                const bool live = lane < 16 && key < end;
+#pragma unroll
+                for (int r = 0; r < G; ++r) x[r] = live && !(MT && mask.hidden(key, cnt[r])) ? x[r] : -INFINITY;
+                // Row maxima over the warp's 16 keys: each step halves the rows a lane
+                // keeps (lane bit 8, 4, 2, 1), so lane l ends with row l.
+                float mx[G];
+#pragma unroll
+                for (int r = 0; r < G; ++r) mx[r] = x[r];
+#pragma unroll
+                for (int w = G / 2; w >= 1; w >>= 1) {
+                    const bool up = (lane & w) != 0;
+#pragma unroll
+                    for (int i = 0; i < w; ++i) {
+                        const float keep = up ? mx[i + w] : mx[i], send = up ? mx[i] : mx[i + w];
+                        mx[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
+                    }
+                }
+                float *um = umax_s + sb * kConsumerWarps * kMaxRows;
+                if (lane < 16) um[warp * kMaxRows + lane] = mx[0];
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ubar[7 + sb]);
+                if (!__all_sync(0xffffffffu, mbar_wait(&ubar[7 + sb], (s >> 1) & 1))) {
+                    fail();
+                    break;
+                }
+                float mst = um[kl];
+#pragma unroll
+                for (int w = 1; w < kConsumerWarps; ++w) mst = fmaxf(mst, um[w * kMaxRows + kl]);
+                float alpha[G], pv[G];
+#pragma unroll
+                for (int r = 0; r < G; ++r) {
+                    const float mn = fmaxf(m_run[r], __shfl_sync(0xffffffffu, mst, r));
+                    alpha[r] = mn == -INFINITY ? 1.f : fast_exp2(m_run[r] - mn);
+                    m_run[r] = mn;
+                    pv[r] = x[r] == -INFINITY ? 0.f : fast_exp2(x[r] - mn);
+                    l_part[r] = fmaf(l_part[r], alpha[r], pv[r]);
+                }
+                // P^T of this stage, MN-major without swizzle: key k, row r at
+                // (k / 8) * 256 + (k % 8) * 16 + (r / 8) * 128 + (r % 8) * 2.
+                if (lane < 16) {
+                    uint8_t *pb = p_s + sb * kUmmaPBytes + (kin >> 3) * 256 + (kin & 7) * 16;
+                    *reinterpret_cast<uint4 *>(pb) = make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]),
+                                                                pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
+                    *reinterpret_cast<uint4 *>(pb + 128) = make_uint4(pack_bf16(pv[8], pv[9]), pack_bf16(pv[10], pv[11]),
+                                                                      pack_bf16(pv[12], pv[13]), pack_bf16(pv[14], pv[15]));
+                }
+                // Rows past the key set may hold NaN; 0 * NaN would poison O^T, so the V
+                // rows of a short stage are cleared (the K rows only reach masked scores).
+                const int nv = end - (start + s * kKeys);
+                if (nv < kKeys) {
+                    if (!__all_sync(0xffffffffu, mbar_wait(&fullv[s % S], (s / S) & 1))) {   // the V half has landed
+                        fail();
+                        break;
+                    }
+                    uint8_t *vst = smem + (s % S) * kStage + kBoxes * kBoxB;
+                    const int per = (kKeys - nv) * 8;   // 16-byte chunks per box column
+                    for (int i = threadIdx.x; i < kBoxes * per; i += kConsumerWarps * 32)
+                        *reinterpret_cast<uint4 *>(vst + (i / per) * kBoxB + (nv + (i % per) / 8) * 128 + (i % 8) * 16) =
+                            make_uint4(0u, 0u, 0u, 0u);
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");   // P^T and V for the tensor cores
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&ubar[2 + sb]);
+                if (s >= 1 && !fold(s - 1)) {
+                    fail();
+                    break;
+                }
+#pragma unroll
+                for (int r = 0; r < G; ++r) al_prev[r] = alpha[r];
+            }
+            if (ok && nst > 0 && !fold(nst - 1)) fail();
+            tc_fence_before();
+            // This chunk's row sums over the 64 lanes that scored: lane l < 16 ends with row l.
+#pragma unroll
+            for (int w = G / 2; w >= 1; w >>= 1) {
+                const bool up = (lane & w) != 0;
+#pragma unroll
+                for (int i = 0; i < w; ++i) {
+                    const float keep = up ? l_part[i + w] : l_part[i], send = up ? l_part[i] : l_part[i + w];
+                    l_part[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
+                }
+            }
+            if (lane < 16) usum_s[warp * kMaxRows + lane] = l_part[0];
+            __syncthreads();   // every stage consumed: the ring is free for the partial
+            const int d0 = 32 * warp + lane;
+#pragma unroll
+            for (int r = 0; r < G; ++r) {
+                red_o[r * kHeadDim + d0] = o_acc[r];
+                red_o[r * kHeadDim + 128 + d0] = o_acc[G + r];
+            }
+            if (warp == 0 && lane < G) {
+                float m = m_run[0], l = 0.f;
+#pragma unroll
+                for (int r = 1; r < G; ++r) m = lane == r ? m_run[r] : m;
+#pragma unroll
+                for (int w = 0; w < kConsumerWarps; ++w) l += usum_s[w * kMaxRows + lane];
+                red_m[lane] = m;
+                red_l[lane] = l;
+            }
+            __syncthreads();
+        }
     } else {
         using Mma = typename std::conditional<KV == KV_FP8, Fp8MmaConsumer<CG, MT>, MmaConsumer<CG, MT>>::type;
         typename std::conditional<CONSUMER == CONSUMER_MMA, Mma, FmaConsumer<CG, KV>>::type cons;
@@ -1308,13 +1726,19 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
         cons.store(red_o, red_m, red_l, warp, lane);
         __syncthreads();
     }
+    if constexpr (kUmma) {
+        if (warp == CW + 1) {   // every tensor-memory read and MMA is complete (barriers above)
+            tc_fence_after();
+            tmem_dealloc(*taddr_s, kUmmaCols);
+        }
+    }
 
     // Per query row: this chunk's maximum M and sum L over the warps of the
     // row's group, and each warp's weight 2^(m_w - M) (shared memory only).
     // Partials: G rows per (sequence, kv head), num_kv_heads * G rows per sequence.
     const size_t pbase = ((size_t)b * a.num_kv_heads * G + kvh * G) * a.max_chunks;
     // this chunk's partial, the warp weights and the rows' lse sit past the warp buffers
-    constexpr int kRedBytes = (CW * CG * kHeadDim + 2 * CW * CG) * (int)sizeof(float);
+    constexpr int kRedBytes = (NRW * CG * kHeadDim + 2 * NRW * CG) * (int)sizeof(float);
     constexpr int kOwnOff = kRedBytes <= kOwnPartialOffset ? kOwnPartialOffset : (kRedBytes + 1023) / 1024 * 1024;
     static_assert(kOwnOff + G * (kHeadDim + 2 + WPG + 1 + kMaxCluster) * (int)sizeof(float) <= S * kStage - kMtNewBytes,
                   "warp buffers, own partial and the multi-token entries fit the ring");
@@ -1618,8 +2042,17 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
             } else {
                 for (int j = 0; j <= th; ++j) {
                     float t = 0.f;
-                    for (int d = lane; d < kHeadDim; d += 32)
-                        t = fmaf(q_join<KV>(q_w[h * kHeadDim + d]), knew_t[j * kHeadDim + d], t);
+                    for (int d = lane; d < kHeadDim; d += 32) {
+                        float qv;
+                        if constexpr (kUmma) {   // the q operand: bf16 high and low parts
+                            const uint16_t *q16 = reinterpret_cast<const uint16_t *>(q_s);
+                            qv = __uint_as_float((uint32_t)q16[umma_q_offset<G>(h, d) / 2] << 16) +
+                                 __uint_as_float((uint32_t)q16[umma_q_offset<G>(G + h, d) / 2] << 16);
+                        } else {
+                            qv = q_join<KV>(q_w[h * kHeadDim + d]);
+                        }
+                        t = fmaf(qv, knew_t[j * kHeadDim + d], t);
+                    }
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
                     if (lane == 0) wnew_t[h * WN + j] = t;
@@ -1748,7 +2181,8 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(S, KV))
 template <int G, int CONSUMER, int S, int KV, bool MT, int NL>
 cudaError_t launch_g(const LaunchTable<NL> &p, dim3 grid, bool pdl, cudaStream_t s) {
     static std::atomic<uint64_t> configured{0};   // devices whose attribute is set
-    const size_t smem = layer_smem_bytes(G, S * kv_stage_bytes(KV) / kStageBytes);
+    const size_t smem = layer_smem_bytes(G, S * kv_stage_bytes(KV) / kStageBytes) +
+                        (umma_pass(G, KV, MT, deep_ring(S, KV), CONSUMER) ? kUmmaExtraBytes : 0);
     int device = -1;
     if (!done_on_device(configured, &device)) {
         cudaError_t e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER, S, KV, MT, NL>,
@@ -1761,7 +2195,7 @@ cudaError_t launch_g(const LaunchTable<NL> &p, dim3 grid, bool pdl, cudaStream_t
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = grid;
-    cfg.blockDim = dim3(layer_threads(G, KV, NL, MT, deep_ring(S, KV)));
+    cfg.blockDim = dim3(layer_threads(G, KV, NL, MT, deep_ring(S, KV), CONSUMER));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
@@ -1845,6 +2279,15 @@ cudaError_t launch_c(const LaunchTable<NL> &p, dim3 grid, int rows, bool mt, boo
 template <int KV, int NL>
 cudaError_t launch_kv(const LaunchTable<NL> &p, dim3 grid, int rows, bool mt, int consumer, int stages, bool pdl,
                       cudaStream_t s) {
+    // The tensor-memory consumer takes 16-row multi-token passes over bf16 caches;
+    // every other pass of such a call runs the tensor-core consumer.
+    if (consumer == CONSUMER_UMMA) {
+        if constexpr (KV == KV_BF16) {
+            if (mt && rows == kMaxRows && stages == kDeepStages)
+                return launch_g<kMaxRows, CONSUMER_UMMA, kDeepStages, KV_BF16, true, NL>(p, grid, pdl, s);
+        }
+        consumer = CONSUMER_MMA;
+    }
     if constexpr (NL > 1) {
         if (consumer != CONSUMER_MMA) return cudaErrorInvalidValue;
         return stages == kDeepStages ? launch_c<CONSUMER_MMA, kDeepStages, KV, NL>(p, grid, rows, mt, pdl, s)

@@ -4,8 +4,9 @@
 
 namespace hd {
 
-cudaError_t launch_step_bf16(const StepTable &t, dim3 grid, int rows, bool mt, int stages, cudaStream_t s) {
-    return launch_kv<KV_BF16, kStepLayers>(t, grid, rows, mt, CONSUMER_MMA, stages, false, s);
+cudaError_t launch_step_bf16(const StepTable &t, dim3 grid, int rows, bool mt, int consumer, int stages,
+                             cudaStream_t s) {
+    return launch_kv<KV_BF16, kStepLayers>(t, grid, rows, mt, consumer, stages, false, s);
 }
 
 }  // namespace hd

@@ -92,7 +92,9 @@ enum NewEntry : int32_t {
 };
 // Where the new entry is stored once every chunk has read the cache.
 enum Commit : int32_t { COMMIT_NONE = 0, COMMIT_APPEND = 1, COMMIT_RING = 2, COMMIT_ROLL = 3 };
-enum Consumer : int32_t { CONSUMER_FMA = 0, CONSUMER_MMA = 1 };
+enum Consumer : int32_t { CONSUMER_FMA = 0, CONSUMER_MMA = 1, CONSUMER_UMMA = 2 };
+// Tensor-core consumers (mma.sync, or tcgen05 for the passes it takes).
+constexpr bool tensor_consumer(int c) { return c == CONSUMER_MMA || c == CONSUMER_UMMA; }
 
 // One attention layer: one CTA per (chunk, kv head, sequence); the last CTA of
 // each (sequence, kv head) combines the chunks.
@@ -186,17 +188,19 @@ cudaError_t launch_roll_window(const RopeArgs &a, int batch, cudaStream_t s);
 cudaError_t launch_layer(const CUtensorMap *kmap, const CUtensorMap *vmap, const LayerArgs &a,
                          int batch, int group, int consumer, int stages, bool pdl, cudaStream_t s);
 // One grid for the t.num_layers layers of a step table (num_ctas CTAs in all;
-// every layer with the same cache type, rows per kv head and pass shape; the
+// every layer with the same cache type, rows per kv head and pass shape; a
 // tensor-core consumer).  The layers must be independent: no layer reads or
 // writes what another one writes.
-cudaError_t launch_step(const StepTable &t, int num_ctas, int rows, bool mt, int kv, int stages, cudaStream_t s);
+cudaError_t launch_step(const StepTable &t, int num_ctas, int rows, bool mt, int kv, int consumer, int stages,
+                        cudaStream_t s);
 // Per-family launchers, one translation unit each (rows: query rows per kv
 // head; mt: a pass of a multi-token step).
 cudaError_t launch_layer_bf16(const LaunchTable<1> &t, dim3 grid, int rows, bool mt, int consumer, int stages,
                               bool pdl, cudaStream_t s);
 cudaError_t launch_layer_fp8(const LaunchTable<1> &t, dim3 grid, int rows, bool mt, int consumer, int stages,
                              bool pdl, cudaStream_t s);
-cudaError_t launch_step_bf16(const StepTable &t, dim3 grid, int rows, bool mt, int stages, cudaStream_t s);
+cudaError_t launch_step_bf16(const StepTable &t, dim3 grid, int rows, bool mt, int consumer, int stages,
+                             cudaStream_t s);
 cudaError_t launch_step_fp8(const StepTable &t, dim3 grid, int rows, bool mt, int stages, cudaStream_t s);
 size_t layer_smem_bytes(int group, int stages);
 // Largest cluster (16 or 8 CTAs, 0 if none) that single-layer launches of the

@@ -75,13 +75,15 @@ class TokenLayer:
 
 
 def run_case(hd, orc, types, T, Hq, Hkv, context, kv="bf16", seed=0, with_gate=True, max_context=None,
-             fuse=True, layout=RING):
+             fuse=True, layout=RING, consumer=None):
     rng = synth.generator(seed)
     B = len(context)
     context = np.asarray(context, np.int32)
     max_context = max_context or int(context.max()) + T
     ctx = _ctx(hd, types, Hq, Hkv, B, max_context, kv, layout=layout)
     hd.hybrid_decode_set_step_fusion(ctx, fuse)
+    if consumer is not None:
+        hd.hybrid_decode_set_consumer(ctx, consumer)
     sink = synth.sink_vector(rng, ("normal", 1.0, 0.0), Hq)
     window = synth.WINDOW - 1 if layout == RING else synth.WINDOW
     layers = [TokenLayer(rng, t, B, T, Hq, Hkv, window if t == SLIDING else max_context + 1, context, kv, sink,
@@ -160,6 +162,35 @@ def test_tokens_long_context_many_chunks(hd, orc):
 
 def test_tokens_28_layer_step(hd, orc):
     run_case(hd, orc, synth.SPARK_LAYER_TYPES, 4, 8, 2, [700, 1500, 3], seed=903)
+
+
+# The tensor-memory consumer runs the 16-row passes (g x tokens per pass = 16) on
+# tcgen05 with 64-key stages; other passes of the same call run mma.sync.
+@pytest.mark.parametrize("fuse", [True, False])
+@pytest.mark.parametrize("T,g", [(4, 4), (2, 8), (8, 2), (8, 4)])
+def test_tokens_tensor_memory_consumer(hd, orc, T, g, fuse):
+    Hkv = 2
+    run_case(hd, orc, [SLIDING, FULL], T, g * Hkv, Hkv, RING_FULL_CONTEXTS, seed=1500 + 10 * T + g, fuse=fuse,
+             consumer=hd.HD_CONSUMER_TENSOR_MEMORY)
+
+
+@pytest.mark.parametrize("T", [4, 8])
+def test_tokens_tensor_memory_roll(hd, orc, T):
+    run_case(hd, orc, [SLIDING, FULL], T, 8, 2, ROLL_CONTEXTS, seed=1600 + T, layout=ROLL,
+             consumer=hd.HD_CONSUMER_TENSOR_MEMORY)
+
+
+def test_tokens_tensor_memory_long_context_and_28_layers(hd, orc):
+    run_case(hd, orc, [FULL], 4, 8, 2, [40000, 39000 - 7], seed=1610, with_gate=False,
+             consumer=hd.HD_CONSUMER_TENSOR_MEMORY)
+    run_case(hd, orc, synth.SPARK_LAYER_TYPES, 4, 8, 2, [700, 1500, 3], seed=1611,
+             consumer=hd.HD_CONSUMER_TENSOR_MEMORY)
+
+
+def test_tokens_tensor_memory_fp8_falls_back(hd, orc):
+    """E4M3 caches have no tensor-memory pass: the same call runs mma.sync."""
+    run_case(hd, orc, [SLIDING, FULL], 4, 8, 2, RING_FULL_CONTEXTS, kv="fp8", seed=1620,
+             consumer=hd.HD_CONSUMER_TENSOR_MEMORY)
 
 
 def test_tokens_match_sequential_gpu_steps(hd):
