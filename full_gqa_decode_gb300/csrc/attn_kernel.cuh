@@ -67,6 +67,9 @@
 #ifndef HD_STEP_FINISH
 #define HD_STEP_FINISH 1
 #endif
+#ifndef HD_WIDE_MT
+#define HD_WIDE_MT 1
+#endif
 
 namespace hd {
 namespace {
@@ -544,9 +547,18 @@ struct FmaConsumer {
 // accumulator of S is, register for register, the B operand of
 // O^T += V^T P^T (m16n8k8: dims on M, 8 keys on K, heads on N), whose A
 // operand is V read with ldmatrix.trans.
-template <int G, bool MT = false>
+//
+// WIDE (16-row multi-token passes, 64-key stages of 8 KiB box columns): a call
+// takes 16 keys as two 8-key tiles, so the score MMAs run as four independent
+// chains, one softmax round covers 16 keys, and O^T += V^T P^T runs as m16n8k16
+// (the two tiles' P fragments are its two B registers).
+template <int G, bool MT = false, bool WIDE = false>
 struct MmaConsumer {
-    static constexpr int kWK = 8;   // keys per consume call
+    static constexpr int kWK = WIDE ? 16 : 8;   // keys per consume call
+    static constexpr int kBoxB = (WIDE ? 2 : 1) * kv_box_bytes(KV_BF16);   // box column stride
+    __device__ static __forceinline__ uint32_t off(int r, int c) {
+        return (c >> 3) * kBoxB + r * 128 + ((((c & 7) ^ (r & 7))) << 4);
+    }
     uint32_t qa[16][4];
     float o[16][4];   // O^T tile mt: rows dims 16mt + gid (+8), cols heads 2*t4 (+1)
     float m_run, l_run;  // for head gid; l_run sums this lane's keys only
@@ -583,6 +595,10 @@ struct MmaConsumer {
     }
 
     __device__ void consume(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane, int key0) {
+        if constexpr (WIDE) {
+            consume16(kst, vst, row0, nvalid, lane, key0);
+            return;
+        }
         const int gid = lane >> 2, t4 = lane & 3;
         const int lrow = row0 + (lane & 7), lsub = lane >> 3;
         const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
@@ -591,7 +607,7 @@ struct MmaConsumer {
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + tile_offset(lrow, 4 * p + lsub), b0, b1, b2, b3);
+            ldsm_x4(kbase + off(lrow, 4 * p + lsub), b0, b1, b2, b3);
             mma_16816(s, qa[2 * p], b0, b1);
             mma_16816(s2, qa[2 * p + 1], b2, b3);
         }
@@ -637,9 +653,82 @@ struct MmaConsumer {
 #pragma unroll
         for (int p = 0; p < 8; ++p) {
             uint32_t a0, a1, a2, a3;
-            ldsm_x4_trans(vbase + tile_offset(lrow, 4 * p + lsub), a0, a1, a2, a3);
+            ldsm_x4_trans(vbase + off(lrow, 4 * p + lsub), a0, a1, a2, a3);
             mma_1688(o[2 * p], a0 & vmask, a1 & vmask, pb);
             mma_1688(o[2 * p + 1], a2 & vmask, a3 & vmask, pb);
+        }
+    }
+
+    // 16 keys row0..row0+15: tile A the first 8, tile B the next 8.
+    __device__ void consume16(const uint8_t *kst, const uint8_t *vst, int row0, int nvalid, int lane, int key0) {
+        const int gid = lane >> 2, t4 = lane & 3;
+        const int lrow = row0 + (lane & 7), lsub = lane >> 3;
+        const uint32_t kbase = smem_u32(kst), vbase = smem_u32(vst);
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sa2[4] = {0.f, 0.f, 0.f, 0.f};
+        float sb[4] = {0.f, 0.f, 0.f, 0.f}, sb2[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+            ldsm_x4(kbase + off(lrow, 4 * p + lsub), a0, a1, a2, a3);
+            ldsm_x4(kbase + off(lrow + 8, 4 * p + lsub), b0, b1, b2, b3);
+            mma_16816(sa, qa[2 * p], a0, a1);
+            mma_16816(sb, qa[2 * p], b0, b1);
+            mma_16816(sa2, qa[2 * p + 1], a2, a3);
+            mma_16816(sb2, qa[2 * p + 1], b2, b3);
+        }
+        // lane (gid, t4) scores keys 2t4, 2t4+1 (tile A) and 8+2t4, 9+2t4 (tile B) for row gid
+        float x[4] = {sa[0] + sa2[0] + sa[2] + sa2[2], sa[1] + sa2[1] + sa[3] + sa2[3],
+                      sb[0] + sb2[0] + sb[2] + sb2[2], sb[1] + sb2[1] + sb[3] + sb2[3]};
+        const int kk[4] = {2 * t4, 2 * t4 + 1, 8 + 2 * t4, 9 + 2 * t4};
+        bool ok[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            ok[i] = gid < G && kk[i] < nvalid;
+            if (MT) ok[i] = ok[i] && !mask.hidden(key0 + kk[i], mcnt);
+            x[i] = ok[i] ? x[i] : -INFINITY;
+        }
+        float mx = fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3]));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float mn = fmaxf(m_run, mx);
+        const float alpha = (mn == -INFINITY) ? 1.f : fast_exp2(m_run - mn);
+        float pr[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pr[i] = ok[i] ? fast_exp2(x[i] - mn) : 0.f;
+        l_run = fmaf(l_run, alpha, (pr[0] + pr[1]) + (pr[2] + pr[3]));
+        m_run = mn;
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+            const float a_lo = __shfl_sync(0xffffffffu, alpha, 8 * t4);      // head 2*t4
+            const float a_hi = __shfl_sync(0xffffffffu, alpha, 8 * t4 + 4);  // head 2*t4+1
+#pragma unroll
+            for (int mt = 0; mt < 16; ++mt) {
+                o[mt][0] *= a_lo;
+                o[mt][1] *= a_hi;
+                o[mt][2] *= a_lo;
+                o[mt][3] *= a_hi;
+            }
+        }
+        // P^T fragments of m16n8k16: keys 2t4, 2t4+1 (tile A) and 8+2t4, 9+2t4 (tile B) of head gid.
+        const uint32_t pa = pack_bf16(pr[0], pr[1]), pb = pack_bf16(pr[2], pr[3]);
+        // V^T tile mt (dims 16mt..16mt+15 x 16 keys) with ldmatrix.trans: lanes 0-7 the
+        // first 8 keys at dims 16mt.., 8-15 the same keys at dims 16mt+8.., 16-31 the
+        // next 8 keys likewise.  Rows past the key set may hold NaN (0 * NaN would
+        // poison the sum), so a short call masks its V values.
+        const int vrow = row0 + (lane & 7) + ((lane >> 4) << 3), vsub = (lane >> 3) & 1;
+        uint32_t ma = 0xFFFFFFFFu, mb = 0xFFFFFFFFu;
+        if (nvalid < kWK) {
+            ma = (2 * t4 < nvalid ? 0x0000FFFFu : 0u) | (2 * t4 + 1 < nvalid ? 0xFFFF0000u : 0u);
+            mb = (8 + 2 * t4 < nvalid ? 0x0000FFFFu : 0u) | (9 + 2 * t4 < nvalid ? 0xFFFF0000u : 0u);
+        }
+#pragma unroll
+        for (int mt = 0; mt < 16; ++mt) {
+            uint32_t v[4];
+            ldsm_x4_trans(vbase + off(vrow, 2 * mt + vsub), v[0], v[1], v[2], v[3]);
+            v[0] &= ma;
+            v[1] &= ma;
+            v[2] &= mb;
+            v[3] &= mb;
+            mma_16816(o[mt], v, pa, pb);
         }
     }
 
@@ -903,13 +992,15 @@ struct Fp8MmaConsumer {
 template <int G, int CONSUMER, int SP, int KV, bool MT, int NL>
 __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV), CONSUMER), deep_ring(SP, KV) ? 1 : 2)
     attn_layer_kernel(const __grid_constant__ LaunchTable<NL> p) {
-    // SP: the ring in 32 KiB stages.  A tensor-memory pass takes them in pairs:
-    // 64-key stages, each K or V box column two 32-row boxes one after the other.
+    // SP: the ring in 32 KiB stages.  A 16-row multi-token pass over a bf16 cache
+    // takes them in pairs: 64-key stages, each K or V box column two 32-row boxes
+    // one after the other (16 keys per consumer warp and stage, or the tcgen05 tile).
     constexpr bool kUmma = umma_pass(G, KV, MT, deep_ring(SP, KV), CONSUMER);
-    constexpr int S = kUmma ? SP / 2 : SP;                               // ring slots
-    constexpr int kStage = (kUmma ? 2 : 1) * kv_stage_bytes(KV);        // bytes of one stage (K + V)
-    constexpr int kKeys = (kUmma ? 2 : 1) * kv_stage_keys(KV);          // keys per stage: 32 bf16, 64 E4M3 or tcgen05
-    constexpr int kBoxB = (kUmma ? 2 : 1) * kv_box_bytes(KV);           // bytes of one box column of a stage
+    constexpr bool kWide = kUmma || (HD_WIDE_MT && KV == KV_BF16 && MT && G == kMaxRows && deep_ring(SP, KV));
+    constexpr int S = kWide ? SP / 2 : SP;                               // ring slots
+    constexpr int kStage = (kWide ? 2 : 1) * kv_stage_bytes(KV);        // bytes of one stage (K + V)
+    constexpr int kKeys = (kWide ? 2 : 1) * kv_stage_keys(KV);          // keys per stage: 32 bf16, 64 E4M3 or wide
+    constexpr int kBoxB = (kWide ? 2 : 1) * kv_box_bytes(KV);           // bytes of one box column of a stage
     constexpr int kBoxes = kv_boxes_per_row(KV);   // 128-byte boxes per K or V row
     constexpr int kNThreads = layer_threads(G, KV, NL, MT, deep_ring(SP, KV), CONSUMER);
     constexpr bool kOwnProducer = own_producer(KV, NL, MT, deep_ring(SP, KV));
@@ -1122,12 +1213,19 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
         uint8_t *st = smem + slot * kStage;
         mbar_arrive_expect_tx(&full[slot], kStage);
         const int row = roff + start + s * kKeys;
+        constexpr int kHalves = kWide ? 2 : 1;   // 32-row boxes per box column
 #pragma unroll
         for (int j = 0; j < kBoxes; ++j)
-            tma_load_4d(st + j * kBoxB, &ll.kmap, &full[slot], j * kv_box_cols(KV), row, kvh, b);
+#pragma unroll
+            for (int h = 0; h < kHalves; ++h)
+                tma_load_4d(st + j * kBoxB + h * kv_box_bytes(KV), &ll.kmap, &full[slot], j * kv_box_cols(KV),
+                            row + h * kv_stage_keys(KV), kvh, b);
 #pragma unroll
         for (int j = 0; j < kBoxes; ++j)
-            tma_load_4d(st + (kBoxes + j) * kBoxB, &ll.vmap, &full[slot], j * kv_box_cols(KV), row, kvh, b);
+#pragma unroll
+            for (int h = 0; h < kHalves; ++h)
+                tma_load_4d(st + (kBoxes + j) * kBoxB + h * kv_box_bytes(KV), &ll.vmap, &full[slot],
+                            j * kv_box_cols(KV), row + h * kv_stage_keys(KV), kvh, b);
     };
     // Test hook: stages from a.drop_stage on are never issued (a copy that never arrives).
     auto droppable = [&](int s) { return a.drop_stage >= 0 && s >= a.drop_stage; };
@@ -1633,7 +1731,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
             __syncthreads();
         }
     } else {
-        using Mma = typename std::conditional<KV == KV_FP8, Fp8MmaConsumer<CG, MT>, MmaConsumer<CG, MT>>::type;
+        using Mma = typename std::conditional<KV == KV_FP8, Fp8MmaConsumer<CG, MT>, MmaConsumer<CG, MT, kWide>>::type;
         typename std::conditional<CONSUMER == CONSUMER_MMA, Mma, FmaConsumer<CG, KV>>::type cons;
         constexpr int kCallKeys = decltype(cons)::kWK;          // keys per consume call
         constexpr int kSpan = kKeys / WPG;                        // keys of a stage per warp
@@ -1656,7 +1754,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                 const int row0 = kpart * kSpan + sub;
                 const int nvalid = min(kCallKeys, end - (start + s * kKeys + row0));
                 if (nvalid > 0)
-                    cons.consume(kst, kst + kBoxes * kv_box_bytes(KV), row0, nvalid, lane, start + s * kKeys + row0);
+                    cons.consume(kst, kst + kBoxes * kBoxB, row0, nvalid, lane, start + s * kKeys + row0);
             }
             // Rolled window: this warp's rows of the stage (cache rows key + roff) move
             // down by sh rows before the slot is released; rows below sh leave the
