@@ -80,7 +80,8 @@ constexpr float kQScale = kLog2e * 0.0625f;   // log2(e) / sqrt(256)
 constexpr int kConsumerWarps = 4;   // per CTA; 16-row multi-token passes run twice as many
 // Who issues the copies.  bf16 single-layer kernels, multi-token passes and
 // one-CTA-per-SM grids run a dedicated producer warp (lower latency for small
-// grids: the batch-1 step 23.5 vs 27 us, the 16-row pass 3.12 vs 3.62 ms).
+// grids: the batch-1 step 23.5 vs 27 us, the 16-row pass 3.12 vs 3.62 ms, and
+// with 64-key stages 2.975 vs 3.002 ms although folding removed its spills).
 // E4M3 kernels and the bf16 single-token step grids of two CTAs per SM fold the
 // producer into the consumers (the last warp to release a slot refills it):
 // four warps per CTA leave each thread up to 255 registers at two CTAs per SM,
@@ -1794,8 +1795,9 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                         const int r = rem / kChunks, ch = rem % kChunks;
                         const int row = key0 + r + roff;
                         if (row < sh) continue;
+                        const int rr = kpart * kSpan + r;
                         const uint4 x = *reinterpret_cast<const uint4 *>(
-                            kst + v * kBoxes * kv_box_bytes(KV) + tile_offset<KV>(kpart * kSpan + r, ch));
+                            kst + v * kBoxes * kBoxB + (ch >> 3) * kBoxB + rr * 128 + ((((ch & 7) ^ (rr & 7))) << 4));
                         uint8_t *dst = static_cast<uint8_t *>(v ? a.cache_v : a.cache_k) + seq +
                                        (size_t)(row - sh) * kHeadDim * kv_elem_bytes(KV) + 16 * ch;
                         *reinterpret_cast<uint4 *>(dst) = x;
