@@ -266,6 +266,7 @@ struct LayerCall {
     void *out;
     float *lse;
     bool pdl;               // previous grid in the stream is this step's previous layer kernel
+    bool early = false;     // pdl: the layer may read and stream before that grid completes
     bool one_chunk = false; // step grids: the layer needs a single chunk per sequence
     int tokens = 1, token0 = 0, total_tokens = 1;   // multi-token decode: this pass's tokens
 };
@@ -354,6 +355,7 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     LayerArgs a;
     fill_layer_args(ctx, L, chunk_keys, num_chunks, 0, a);
     a.cluster = cluster;
+    a.wait_first = L.pdl && !L.early ? 1 : 0;
 
     const bool sliding = ctx->layer_types[L.layer] == HD_SLIDING;
     const int type = sliding ? HD_SLIDING : HD_FULL;
@@ -363,7 +365,7 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
     if (timed) ctx->profile_seen[type] = true;
     if (timed && cudaEventRecord(ctx->ev_begin[slot], stream) != cudaSuccess) return HD_ERR_CUDA;
     st = cuda_status(launch_layer(km, vm, a, L.batch, ctx->group, ctx->consumer, stages,
-                                  L.pdl && !timed && ctx->layer_overlap, stream));
+                                  L.pdl && !timed, stream));
     if (st != HD_OK) return st;
     ++ctx->launches;
     if (timed) {
@@ -926,7 +928,12 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
             while (2 * tp <= tmax && 2 * tp <= num_tokens - t0) tp *= 2;
             L.tokens = tp;
             L.token0 = t0;
-            L.pdl = indep && L.layer > 0 && t0 == 0;   // a later pass reads what the previous pass wrote
+            // Every layer after the first is a programmatic dependent of the previous
+            // kernel: independent layers with overlap on read and stream before it
+            // completes; otherwise (full stream order) they wait before their first read.
+            // (A later pass reads what the previous pass wrote.)
+            L.pdl = L.layer > 0 && t0 == 0;
+            L.early = indep && ctx->layer_overlap;
             hd_status st = launch_layer_call(ctx, L, s);
             if (st != HD_OK) return st;
             t0 += tp;

@@ -1076,8 +1076,11 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     // behind another layer of the same step, see launch_layer), a CTA reads its
     // own layer's inputs and streams its own layer's cache -- nothing the
     // previous grid writes -- and waits for that grid (griddepcontrol.wait)
-    // only before its first global write.
+    // only before its first global write; in full stream order (wait_first) it
+    // waits before anything else, which still hides the launch behind the
+    // previous grid's last CTAs.
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    if (a.wait_first) asm volatile("griddepcontrol.wait;" ::: "memory");
     // Tokens of this launch: one, or (MT) a.tokens tokens at positions c .. c + ntok - 1.
     const int ntok = MT ? a.tokens : 1;
     const int Gm = G / ntok;                               // model heads per kv head

@@ -135,6 +135,9 @@ struct LayerArgs {
     // that many CTAs along the chunk dimension (every chunk of a (sequence, kv head)
     // in one cluster), whose partials then merge through distributed shared memory.
     int32_t cluster;
+    // Launched as a programmatic dependent in full stream order: the kernel waits
+    // for the previous grid before its first read (0: only before its first write).
+    int32_t wait_first;
 };
 
 // Partial RoPE of q and the new k, and the K/V store.
