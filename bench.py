@@ -314,9 +314,11 @@ class Workload:
 
     def token_pass_bytes(self) -> int:
         """Scored-KV bytes a multi-token step reads: the tokens of a sequence run in
-        passes of up to 16 query rows (and 8 tokens) per kv head, each pass scoring
-        the cache at context + first token of the pass (earlier passes' entries included)."""
-        tmax, passes, t0 = min(8, max(1, 16 // (self.Hq // self.Hkv))), [], 0
+        passes of up to 32 query rows with bf16 caches (16 with E4M3) and 8 tokens per
+        kv head, each pass scoring the cache at context + first token of the pass
+        (earlier passes' entries included)."""
+        rows = 16 if self.kv == "fp8" else 32
+        tmax, passes, t0 = min(8, max(1, rows // (self.Hq // self.Hkv))), [], 0
         while t0 < self.tokens:
             tp = 1
             while 2 * tp <= tmax and 2 * tp <= self.tokens - t0:
@@ -768,12 +770,12 @@ def fp8_step(device, args, consumer, layout, bf16_ms) -> dict:
 
 
 def multi_token_steps(device, args, consumer, layout, single_ms) -> list:
-    """The same step decoding T = 2 and 4 tokens per sequence (decode_step_tokens),
+    """The same step decoding T = 2, 4 and 8 tokens per sequence (decode_step_tokens),
     against T single-token steps (the plain step time)."""
     import torch
     import full_gqa_decode_gb300 as hd
     res = []
-    for T in (2, 4):
+    for T in (2, 4, 8):   # group 4: 8, 16 and 32 query rows per kv head (32: the tcgen05 pass)
         wl = Workload(args.workload, device, seed=0, layout=layout, tokens=T)
         hd.hybrid_decode_set_consumer(wl.ctx, consumer)
         ms = time_steps(wl.step, args.steps, args.warmup, 1, device)

@@ -348,7 +348,8 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
             cluster = (int32_t)k;
         }
     }
-    if ((int64_t)ctx->group * L.tokens > kMaxGroup) stages = kDeepStages;   // 16 rows: one CTA per SM
+    if ((int64_t)ctx->group * L.tokens > kMaxGroup)   // 16 or 32 rows: one CTA per SM
+        stages = deep_stages_for((size_t)ctx->group * L.tokens);
     if ((int64_t)L.batch * num_chunks > ctx->part_slots) return HD_ERR_CAPACITY;
     const size_t rows = (size_t)ctx->group * L.tokens;   // query rows per kv head
     if (!combine_fits(rows, num_chunks, L.total_tokens > 1, stages)) return HD_ERR_CAPACITY;
@@ -403,7 +404,7 @@ int32_t hd::plan_step(int64_t Hkv, int64_t sms, int kv_type, size_t rows, bool m
                       const int32_t *max_keys, const uint8_t *one_chunk) {
     const int64_t cmax = kv_type == KV_FP8 ? 2 * kChunkMax : kChunkMax;
     const int64_t fixed = (256 << 10) / (kHeadDim * kv_elem_bytes(kv_type) * 2);   // keys
-    const int stages = rows > (size_t)kMaxGroup ? kDeepStages : kStages;
+    const int stages = rows > (size_t)kMaxGroup ? deep_stages_for(rows) : kStages;
     int64_t longest = 1;
     for (int i = 0; i < n; ++i) longest = std::max<int64_t>(longest, max_keys[i]);
     int64_t best_c = cmax;
@@ -455,7 +456,9 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
     t.num_layers = 0;
     auto flush = [&]() -> hd_status {
         if (t.num_layers == 0) return HD_OK;
-        const int stages = (ctas <= ctx->num_sms || rows > (size_t)kMaxGroup) ? kDeepStages : kStages;
+        const int stages = rows > (size_t)kMaxGroup ? deep_stages_for(rows)
+                           : ctas <= ctx->num_sms  ? kDeepStages
+                                                   : kStages;
         const size_t slot = 2 * (size_t)kProfileEvents + ctx->ev_used[2];
         const bool timed = (ctx->profile_mask & HD_PROFILE_STEP) && ctx->ev_used[2] < (size_t)kProfileEvents;
         if (timed && cudaEventRecord(ctx->ev_begin[slot], stream) != cudaSuccess) return HD_ERR_CUDA;
@@ -480,7 +483,7 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
         // Too large for a shared grid (its partials, its combine's shared memory at
         // this chunk count, or its CTA count): its own plan and launch, in stream order.
         if (need > ctx->part_rows || layer_ctas > INT_MAX ||
-            !combine_fits(rows, ch, mt, rows > (size_t)kMaxGroup ? kDeepStages : kStages)) {
+            !combine_fits(rows, ch, mt, rows > (size_t)kMaxGroup ? deep_stages_for(rows) : kStages)) {
             if ((st = flush()) != HD_OK || (st = launch_layer_call(ctx, L, stream)) != HD_OK) return st;
             continue;
         }
@@ -902,7 +905,9 @@ hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, con
             L.one_chunk = true;
         }
     }
-    const int tmax = std::min(kMaxTokens, kMaxRows / ctx->group);
+    // rows per pass: up to 32 with bf16 caches (the tcgen05 pass), else 16
+    const int rows_cap = ctx->kv_type == KV_BF16 ? kMaxRows : kMaxRowsMma;
+    const int tmax = std::min(kMaxTokens, rows_cap / ctx->group);
     if (fused) {
         // Step grids, pass by pass: a pass commits its entries, and the next pass's
         // grid starts after it in full stream order.

@@ -91,26 +91,28 @@ constexpr int kConsumerWarps = 4;   // per CTA; 16-row multi-token passes run tw
 __host__ __device__ constexpr bool own_producer(int kv, int nl, bool mt, bool deep) {
     return kv == KV_BF16 && (nl == 1 || mt || deep);
 }
-// With the tensor-memory consumer, a 16-row multi-token pass over a bf16 cache
-// (one CTA per SM) runs on the tcgen05 tensor cores: four softmax warps, the
-// producer warp and one warp that owns the tensor memory and issues the MMAs
-// (see "Tensor-memory pass" below).
+// With the tensor-memory consumer, a multi-token pass of 16 or 32 rows over a
+// bf16 cache (one CTA per SM) runs on the tcgen05 tensor cores: four softmax
+// warps per 16 rows, the producer warp and one warp that owns the tensor memory
+// and issues the MMAs (see "Tensor-memory pass" below).
 __host__ __device__ constexpr bool umma_pass(int g, int kv, bool mt, bool deep, int consumer) {
-    return consumer == CONSUMER_UMMA && kv == KV_BF16 && mt && g == kMaxRows && deep;
+    return consumer == CONSUMER_UMMA && kv == KV_BF16 && mt && (g == 16 || g == 32) && deep;
 }
 // 16 query rows on mma.sync run one CTA per SM: eight consumer warps (two per row
 // group of eight rows and stage half) keep as many warps per SM as two 8-row CTAs.
 __host__ __device__ constexpr int consumer_warps(int g) { return g > kMaxGroup ? 2 * kConsumerWarps : kConsumerWarps; }
 __host__ __device__ constexpr int layer_threads(int g, int kv, int nl, bool mt, bool deep,
                                                 int consumer = CONSUMER_MMA) {
-    return umma_pass(g, kv, mt, deep, consumer) ? (kConsumerWarps + 2) * 32
+    return umma_pass(g, kv, mt, deep, consumer) ? (kConsumerWarps * (g / 16) + 2) * 32
                                       : (consumer_warps(g) + (own_producer(kv, nl, mt, deep) ? 1 : 0)) * 32;
 }
-// Shared memory of a tensor-memory pass past the common layout: two P^T buffers
-// of 64 keys x 16 rows (bf16), the softmax warps' row maxima and sums, fifteen
-// mbarriers and the tensor-memory address.
-constexpr int kUmmaPBytes = 64 * kMaxRows * 2;
-constexpr int kUmmaExtraBytes = 128 + 2 * kUmmaPBytes + 3 * kConsumerWarps * kMaxRows * 4 + 16 * 8 + 16;
+// Shared memory of a tensor-memory pass of g rows past the common layout: two
+// P^T buffers of 64 keys x g rows (bf16), the softmax warps' row maxima and sums,
+// seventeen mbarriers and the tensor-memory address.
+__host__ __device__ constexpr int umma_p_bytes(int g) { return 64 * g * 2; }
+__host__ __device__ constexpr int umma_extra_bytes(int g) {
+    return 128 + 2 * umma_p_bytes(g) + 3 * kConsumerWarps * g * 4 + 20 * 8 + 16;
+}
 // A ring of more than the default bytes: one CTA per SM.
 __host__ __device__ constexpr bool deep_ring(int s, int kv) { return s * kv_stage_bytes(kv) > kStages * kStageBytes; }
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
@@ -329,7 +331,19 @@ __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                  : "memory");
 }
-// 32 consecutive columns of this thread's lane, then the wait for the load.
+// 16 (32) consecutive columns of this thread's lane, then the wait for the load.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr)
+        : "memory");
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
     uint32_t r[32];
     asm volatile(
@@ -352,8 +366,9 @@ template <int G>
 __device__ __forceinline__ uint32_t umma_q_offset(int n, int d) {
     return (d >> 6) * (2 * G * 128) + n * 128 + ((((d >> 3) & 7) ^ (n & 7)) << 4) + 2 * (d & 7);
 }
-// Tensor-memory columns of a pass: scores S^T (2 x 32: high, low) at 0, O^T (2 x 32) at 64.
-constexpr uint32_t kUmmaCols = 128;
+// Tensor-memory columns of a pass of g rows: scores S^T (2 buffers of 2g: high,
+// low) at 0, O^T (2 buffers of 2g: two dim halves) at 4g; 8g in all.
+__host__ __device__ constexpr uint32_t umma_cols(int g) { return 8u * (uint32_t)g; }
 
 // q, once rotated and scaled, is kept as one 32-bit word per element: the value
 // rounded to 16 bits in the low half and the remainder rounded to 16 bits in the
@@ -997,7 +1012,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     // takes them in pairs: 64-key stages, each K or V box column two 32-row boxes
     // one after the other (16 keys per consumer warp and stage, or the tcgen05 tile).
     constexpr bool kUmma = umma_pass(G, KV, MT, deep_ring(SP, KV), CONSUMER);
-    constexpr bool kWide = kUmma || (HD_WIDE_MT && KV == KV_BF16 && MT && G == kMaxRows && deep_ring(SP, KV));
+    constexpr bool kWide = kUmma || (HD_WIDE_MT && KV == KV_BF16 && MT && G == kMaxRowsMma && deep_ring(SP, KV));
     constexpr int S = kWide ? SP / 2 : SP;                               // ring slots
     constexpr int kStage = (kWide ? 2 : 1) * kv_stage_bytes(KV);        // bytes of one stage (K + V)
     constexpr int kKeys = (kWide ? 2 : 1) * kv_stage_keys(KV);          // keys per stage: 32 bf16, 64 E4M3 or wide
@@ -1005,7 +1020,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     constexpr int kBoxes = kv_boxes_per_row(KV);   // 128-byte boxes per K or V row
     constexpr int kNThreads = layer_threads(G, KV, NL, MT, deep_ring(SP, KV), CONSUMER);
     constexpr bool kOwnProducer = own_producer(KV, NL, MT, deep_ring(SP, KV));
-    constexpr int CW = kUmma ? kConsumerWarps : consumer_warps(G);      // consumer (softmax) warps
+    constexpr int CW = kUmma ? kConsumerWarps * (G / 16) : consumer_warps(G);   // consumer (softmax) warps
     extern __shared__ uint8_t smem_raw[];
     // The ring starts on a 1024-byte boundary of the shared window (the 128-byte
     // swizzle repeats every 1024 bytes).  Offsetting the array pointer, rather than
@@ -1025,16 +1040,17 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     uint8_t *code_s = reinterpret_cast<uint8_t *>(rel_s + 16);                 // [2][256] E4M3 new entry
     int *mcnt_s = reinterpret_cast<int *>(code_s + 2 * kHeadDim);               // [kMaxRows] MT ring masks
     // Tensor-memory pass: P^T buffers, the softmax warps' row maxima (two sets) and
-    // sums, its mbarriers and the tensor-memory address (kUmmaExtraBytes).
+    // sums, its mbarriers and the tensor-memory address (umma_extra_bytes).
     uint8_t *u_base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(mcnt_s + kMaxRows) + 127) & ~static_cast<uintptr_t>(127));
-    uint8_t *p_s = u_base;                                                           // [2][64 keys x 16 rows] bf16
-    float *umax_s = reinterpret_cast<float *>(p_s + 2 * kUmmaPBytes);               // [2][warps][16]
-    float *usum_s = umax_s + 2 * kConsumerWarps * kMaxRows;                         // [warps][16]
-    // s[2] p[2] o[2] done x[2], then the V halves' full[3] and empty[3] (the K halves use full / empty)
-    uint64_t *ubar = reinterpret_cast<uint64_t *>(usum_s + kConsumerWarps * kMaxRows);
-    uint64_t *fullv = ubar + 9, *emptyv = ubar + 12;
-    uint32_t *taddr_s = reinterpret_cast<uint32_t *>(ubar + 16);
+    constexpr int kPB = umma_p_bytes(G);                                            // one P^T buffer
+    uint8_t *p_s = u_base;                                                           // [2][64 keys x G rows] bf16
+    float *umax_s = reinterpret_cast<float *>(p_s + 2 * kPB);                       // [2][G / 16][4 warps][16]
+    float *usum_s = umax_s + 2 * kConsumerWarps * G;                                // [softmax warps][16]
+    // s[2] p[2] o[2] done x[2][2], then the V halves' full[3] and empty[3] (the K halves use full / empty)
+    uint64_t *ubar = reinterpret_cast<uint64_t *>(usum_s + kConsumerWarps * G);
+    uint64_t *fullv = ubar + 11, *emptyv = ubar + 14;
+    uint32_t *taddr_s = reinterpret_cast<uint32_t *>(ubar + 20);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // This CTA's layer: the last one whose CTA range starts at or before it
@@ -1292,7 +1308,8 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
         }
         if constexpr (kUmma) {
             static_assert(S <= 3, "three V-half barriers of each kind");
-            for (int i = 0; i < 15; ++i) mbar_init(&ubar[i], (i >= 2 && i < 4) || i == 7 || i == 8 ? kConsumerWarps : 1);
+            for (int i = 0; i < 17; ++i)
+                mbar_init(&ubar[i], i == 2 || i == 3 ? CW : (i >= 7 && i < 11) ? kConsumerWarps : 1);
         }
         fence_mbar_init();
         if (kIssueEarly)
@@ -1301,7 +1318,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
 
     if constexpr (kUmma) {
         if (warp == CW + 1) {   // the MMA warp owns the tensor memory of the pass
-            tmem_alloc(taddr_s, kUmmaCols);
+            tmem_alloc(taddr_s, umma_cols(G));
             tc_fence_before();
         }
     }
@@ -1507,14 +1524,15 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
         __syncthreads();
         __syncthreads();
     } else if constexpr (kUmma) {
-        // Tensor-memory pass (16 query rows, 64-key stages).  Per stage s:
-        //   S^T = K Q^T        tcgen05 M=64 (keys) x N=32 (rows: q high, q low) x K=256,
-        //                      A = the K tile, B = the q operand; into columns 32 (s % 2)
-        //   softmax            four warps: lane l < 16 of warp w scores key 16w + l for all
-        //                      rows (high + low); row maxima over warps through shared
-        //                      memory; P^T in bf16 to shared memory (MN-major, no swizzle)
-        //   O^T_s = V^T P^T    M=128 (dims, two halves) x N=16 x K=64 keys, A = the V tile
-        //                      read MN-major; into columns 64 + 32 (s % 2), a fresh sum
+        // Tensor-memory pass (G = 16 or 32 query rows, 64-key stages).  Per stage s:
+        //   S^T = K Q^T        tcgen05 M=64 (keys) x N=2G (rows: q high, q low) x K=256,
+        //                      A = the K tile, B = the q operand; into columns 2G (s % 2)
+        //   softmax            four warps per 16 rows: lane l < 16 of warp w scores key
+        //                      16 (w % 4) + l for the group's rows (high + low); row maxima
+        //                      over the group's warps through shared memory; P^T in bf16
+        //                      to shared memory (MN-major, no swizzle)
+        //   O^T_s = V^T P^T    M=128 (dims, two halves) x N=G x K=64 keys, A = the V tile
+        //                      read MN-major; into columns 4G + 2G (s % 2), a fresh sum
         //   o = o * alpha_s + O^T_s   in the softmax warps' registers (lane = dim)
         // The MMA warp issues S^T of stage s + 1 before O^T of stage s, so the softmax of
         // one stage overlaps the MMAs of its neighbours; the commit after O^T_s releases
@@ -1531,7 +1549,9 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                 const uint64_t kd0 = umma_desc(smem_u32(smem), 16, 1024, 2);                    // K tiles
                 const uint64_t vd0 = umma_desc(smem_u32(smem) + kBoxes * kBoxB, kBoxB, 1024, 2);  // V tiles
                 const uint64_t qd0 = umma_desc(smem_u32(q_s), 16, 1024, 2);
-                const uint64_t pd0 = umma_desc(smem_u32(p_s), 256, 128, 0);
+                // P^T: 8 keys x 8 rows per 128-byte core matrix, rows first (stride offset
+                // 128), then keys (leading offset 16G bytes per 8 keys)
+                const uint64_t pd0 = umma_desc(smem_u32(p_s), 16 * G, 128, 0);
                 // Event loop: O^T of the oldest scored stage as soon as its P^T (and V
                 // half) is there, else the scores of the next stage whose K half has
                 // landed -- at most one stage ahead of the softmax warps (two score
@@ -1544,14 +1564,14 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                         mbar_test_wait(&ubar[2 + (pv & 1)], (pv >> 1) & 1)) {
                         tc_fence_after();
                         const uint64_t vd = vd0 + (uint64_t)((pv % S) * (kStage >> 4));
-                        const uint64_t pd = pd0 + (uint64_t)((pv & 1) * (kUmmaPBytes >> 4));
-                        const uint32_t dO = tbase + 64 + (pv & 1) * 32;
+                        const uint64_t pd = pd0 + (uint64_t)((pv & 1) * (kPB >> 4));
+                        const uint32_t dO = tbase + 4 * G + (pv & 1) * 2 * G;
 #pragma unroll
                         for (int h = 0; h < 2; ++h)
 #pragma unroll
                             for (int t = 0; t < 4; ++t)
-                                umma_bf16(dO + h * 16, vd + (uint64_t)((2 * h * kBoxB + t * 2048) >> 4),
-                                          pd + (uint64_t)((t * 512) >> 4), kIdPV, t > 0);
+                                umma_bf16(dO + h * G, vd + (uint64_t)((2 * h * kBoxB + t * 2048) >> 4),
+                                          pd + (uint64_t)((t * 32 * G) >> 4), kIdPV, t > 0);
                         umma_commit(&ubar[4 + (pv & 1)]);
                         umma_commit(&emptyv[pv % S]);
                         ++pv;
@@ -1559,7 +1579,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                     } else if (q < nst && q <= pv + 1 && mbar_test_wait(&full[q % S], (q / S) & 1)) {
                         tc_fence_after();
                         const uint64_t kd = kd0 + (uint64_t)((q % S) * (kStage >> 4));
-                        const uint32_t dS = tbase + (q & 1) * 32;
+                        const uint32_t dS = tbase + (q & 1) * 2 * G;
 #pragma unroll
                         for (int kk = 0; kk < 16; ++kk)
                             umma_bf16(dS, kd + (uint64_t)(((kk >> 2) * kBoxB + (kk & 3) * 32) >> 4),
@@ -1583,36 +1603,50 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
             __syncthreads();
             __syncthreads();
         } else {
-            static_assert(G == 16, "one tcgen05.ld of 32 score columns (high, low) per stage");
+            // Warp w: rows r0..r0+15 of its group, keys 16 (w % 4) .. + 15 of each stage
+            // (tensor-memory lanes of its quarter).
+            constexpr int R = 16;
+            const int grp = warp / kConsumerWarps, quarter = warp % kConsumerWarps, r0 = R * grp;
             tc_fence_after();
-            const uint32_t tl = *taddr_s + ((uint32_t)(32 * warp) << 16);   // this warp's lane quarter
+            const uint32_t tl = *taddr_s + ((uint32_t)(32 * quarter) << 16);   // this warp's lane quarter
             const int kl = lane & 15;
-            float m_run[G], l_part[G], al_prev[G], o_acc[2 * G];
-            int cnt[G];
+            // Lane l (and l + 16) keeps row l's running maximum and the last stage's
+            // weight; the rows' values reach every lane by shuffles (registers are
+            // scarce with 32 rows: ten warps leave 168 per thread).
+            float m_row = -INFINITY, al_row = 1.f;
+            float l_part[R], o_acc[2 * R];
+            int cnt[R];
 #pragma unroll
-            for (int r = 0; r < G; ++r) {
-                m_run[r] = -INFINITY;
+            for (int r = 0; r < R; ++r) {
                 l_part[r] = 0.f;
-                al_prev[r] = 1.f;
                 o_acc[r] = 0.f;
-                o_acc[G + r] = 0.f;
-                cnt[r] = mcnt_s[r];
+                o_acc[R + r] = 0.f;
+                cnt[r] = mcnt_s[r0 + r];
             }
             bool ok = true;
             auto fail = [&]() {
                 if (lane == 0) atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
                 ok = false;
             };
-            // O^T of stage ps joins the running sum (its rows rescaled by alpha_ps).
+            // O^T of stage ps joins the running sum (its rows rescaled by alpha_ps, row
+            // r's weight held by lane r).
+            float al_prev = 1.f;
             auto fold = [&](int ps) -> bool {
                 if (!__all_sync(0xffffffffu, mbar_wait(&ubar[4 + (ps & 1)], (ps >> 1) & 1))) return false;
                 tc_fence_after();
-                float ov[2 * G];
-                tmem_ld32(tl + 64 + (ps & 1) * 32, ov);
+                float ov[2 * R];
+                const uint32_t oc = tl + 4 * G + (ps & 1) * 2 * G + r0;   // half h at + h * G
+                if constexpr (G == 16) {
+                    tmem_ld32(oc, ov);
+                } else {
+                    tmem_ld16(oc, ov);
+                    tmem_ld16(oc + G, ov + R);
+                }
 #pragma unroll
-                for (int r = 0; r < G; ++r) {
-                    o_acc[r] = fmaf(o_acc[r], al_prev[r], ov[r]);
-                    o_acc[G + r] = fmaf(o_acc[G + r], al_prev[r], ov[G + r]);
+                for (int r = 0; r < R; ++r) {
+                    const float al = __shfl_sync(0xffffffffu, al_prev, r);
+                    o_acc[r] = fmaf(o_acc[r], al, ov[r]);
+                    o_acc[R + r] = fmaf(o_acc[R + r], al, ov[R + r]);
                 }
                 return true;
             };
@@ -1623,25 +1657,31 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                     break;
                 }
                 tc_fence_after();
-                float x[G];
+                float x[R];
                 {
-                    float hl[2 * G];
-                    tmem_ld32(tl + sb * 32, hl);
+                    float hl[2 * R];
+                    const uint32_t sc = tl + sb * 2 * G + r0;   // high parts; the low ones at + G
+                    if constexpr (G == 16) {
+                        tmem_ld32(sc, hl);
+                    } else {
+                        tmem_ld16(sc, hl);
+                        tmem_ld16(sc + G, hl + R);
+                    }
 #pragma unroll
-                    for (int r = 0; r < G; ++r) x[r] = hl[r] + hl[G + r];
+                    for (int r = 0; r < R; ++r) x[r] = hl[r] + hl[R + r];
                 }
-                const int kin = 16 * warp + kl;   // this lane's key in the stage (lanes < 16)
+                const int kin = 16 * quarter + kl;   // this lane's key in the stage (lanes < 16)
                 const int key = start + s * kKeys + kin;
                 const bool live = lane < 16 && key < end;
 #pragma unroll
-                for (int r = 0; r < G; ++r) x[r] = live && !(MT && mask.hidden(key, cnt[r])) ? x[r] : -INFINITY;
+                for (int r = 0; r < R; ++r) x[r] = live && !(MT && mask.hidden(key, cnt[r])) ? x[r] : -INFINITY;
                 // Row maxima over the warp's 16 keys: each step halves the rows a lane
                 // keeps (lane bit 8, 4, 2, 1), so lane l ends with row l.
-                float mx[G];
+                float mx[R];
 #pragma unroll
-                for (int r = 0; r < G; ++r) mx[r] = x[r];
+                for (int r = 0; r < R; ++r) mx[r] = x[r];
 #pragma unroll
-                for (int w = G / 2; w >= 1; w >>= 1) {
+                for (int w = R / 2; w >= 1; w >>= 1) {
                     const bool up = (lane & w) != 0;
 #pragma unroll
                     for (int i = 0; i < w; ++i) {
@@ -1649,30 +1689,34 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                         mx[i] = fmaxf(keep, __shfl_xor_sync(0xffffffffu, send, w));
                     }
                 }
-                float *um = umax_s + sb * kConsumerWarps * kMaxRows;
-                if (lane < 16) um[warp * kMaxRows + lane] = mx[0];
+                float *um = umax_s + (sb * (G / 16) + grp) * kConsumerWarps * R;
+                uint64_t *xbar = &ubar[7 + 2 * sb + grp];
+                if (lane < 16) um[quarter * R + lane] = mx[0];
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&ubar[7 + sb]);
-                if (!__all_sync(0xffffffffu, mbar_wait(&ubar[7 + sb], (s >> 1) & 1))) {
+                if (lane == 0) mbar_arrive(xbar);
+                if (!__all_sync(0xffffffffu, mbar_wait(xbar, (s >> 1) & 1))) {
                     fail();
                     break;
                 }
                 float mst = um[kl];
 #pragma unroll
-                for (int w = 1; w < kConsumerWarps; ++w) mst = fmaxf(mst, um[w * kMaxRows + kl]);
-                float alpha[G], pv[G];
+                for (int w = 1; w < kConsumerWarps; ++w) mst = fmaxf(mst, um[w * R + kl]);
+                // row kl: new maximum and the weight of what came before
+                const float mn_row = fmaxf(m_row, mst);
+                al_row = mn_row == -INFINITY ? 1.f : fast_exp2(m_row - mn_row);
+                m_row = mn_row;
+                float pv[R];
 #pragma unroll
-                for (int r = 0; r < G; ++r) {
-                    const float mn = fmaxf(m_run[r], __shfl_sync(0xffffffffu, mst, r));
-                    alpha[r] = mn == -INFINITY ? 1.f : fast_exp2(m_run[r] - mn);
-                    m_run[r] = mn;
+                for (int r = 0; r < R; ++r) {
+                    const float mn = __shfl_sync(0xffffffffu, mn_row, r);
+                    const float alpha = __shfl_sync(0xffffffffu, al_row, r);
                     pv[r] = x[r] == -INFINITY ? 0.f : fast_exp2(x[r] - mn);
-                    l_part[r] = fmaf(l_part[r], alpha[r], pv[r]);
+                    l_part[r] = fmaf(l_part[r], alpha, pv[r]);
                 }
-                // P^T of this stage, MN-major without swizzle: key k, row r at
-                // (k / 8) * 256 + (k % 8) * 16 + (r / 8) * 128 + (r % 8) * 2.
+                // P^T of this stage, MN-major without swizzle: key k, row j at
+                // (k / 8) * 16G + (k % 8) * 16 + (j / 8) * 128 + (j % 8) * 2.
                 if (lane < 16) {
-                    uint8_t *pb = p_s + sb * kUmmaPBytes + (kin >> 3) * 256 + (kin & 7) * 16;
+                    uint8_t *pb = p_s + sb * kPB + (kin >> 3) * 16 * G + (kin & 7) * 16 + (r0 >> 3) * 128;
                     *reinterpret_cast<uint4 *>(pb) = make_uint4(pack_bf16(pv[0], pv[1]), pack_bf16(pv[2], pv[3]),
                                                                 pack_bf16(pv[4], pv[5]), pack_bf16(pv[6], pv[7]));
                     *reinterpret_cast<uint4 *>(pb + 128) = make_uint4(pack_bf16(pv[8], pv[9]), pack_bf16(pv[10], pv[11]),
@@ -1688,7 +1732,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                     }
                     uint8_t *vst = smem + (s % S) * kStage + kBoxes * kBoxB;
                     const int per = (kKeys - nv) * 8;   // 16-byte chunks per box column
-                    for (int i = threadIdx.x; i < kBoxes * per; i += kConsumerWarps * 32)
+                    for (int i = threadIdx.x; i < kBoxes * per; i += CW * 32)
                         *reinterpret_cast<uint4 *>(vst + (i / per) * kBoxB + (nv + (i % per) / 8) * 128 + (i % 8) * 16) =
                             make_uint4(0u, 0u, 0u, 0u);
                 }
@@ -1700,14 +1744,13 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                     fail();
                     break;
                 }
-#pragma unroll
-                for (int r = 0; r < G; ++r) al_prev[r] = alpha[r];
+                al_prev = al_row;
             }
             if (ok && nst > 0 && !fold(nst - 1)) fail();
             tc_fence_before();
             // This chunk's row sums over the 64 lanes that scored: lane l < 16 ends with row l.
 #pragma unroll
-            for (int w = G / 2; w >= 1; w >>= 1) {
+            for (int w = R / 2; w >= 1; w >>= 1) {
                 const bool up = (lane & w) != 0;
 #pragma unroll
                 for (int i = 0; i < w; ++i) {
@@ -1715,22 +1758,20 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                     l_part[i] = keep + __shfl_xor_sync(0xffffffffu, send, w);
                 }
             }
-            if (lane < 16) usum_s[warp * kMaxRows + lane] = l_part[0];
+            if (lane < 16) usum_s[warp * R + lane] = l_part[0];
             __syncthreads();   // every stage consumed: the ring is free for the partial
-            const int d0 = 32 * warp + lane;
+            const int d0 = 32 * quarter + lane;
 #pragma unroll
-            for (int r = 0; r < G; ++r) {
-                red_o[r * kHeadDim + d0] = o_acc[r];
-                red_o[r * kHeadDim + 128 + d0] = o_acc[G + r];
+            for (int r = 0; r < R; ++r) {
+                red_o[(r0 + r) * kHeadDim + d0] = o_acc[r];
+                red_o[(r0 + r) * kHeadDim + 128 + d0] = o_acc[R + r];
             }
-            if (warp == 0 && lane < G) {
-                float m = m_run[0], l = 0.f;
+            if (quarter == 0 && lane < R) {
+                float l = 0.f;
 #pragma unroll
-                for (int r = 1; r < G; ++r) m = lane == r ? m_run[r] : m;
-#pragma unroll
-                for (int w = 0; w < kConsumerWarps; ++w) l += usum_s[w * kMaxRows + lane];
-                red_m[lane] = m;
-                red_l[lane] = l;
+                for (int w = 0; w < kConsumerWarps; ++w) l += usum_s[(grp * kConsumerWarps + w) * R + lane];
+                red_m[r0 + lane] = m_row;
+                red_l[r0 + lane] = l;
             }
             __syncthreads();
         }
@@ -1832,7 +1873,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     if constexpr (kUmma) {
         if (warp == CW + 1) {   // every tensor-memory read and MMA is complete (barriers above)
             tc_fence_after();
-            tmem_dealloc(*taddr_s, kUmmaCols);
+            tmem_dealloc(*taddr_s, umma_cols(G));
         }
     }
 
@@ -2285,7 +2326,7 @@ template <int G, int CONSUMER, int S, int KV, bool MT, int NL>
 cudaError_t launch_g(const LaunchTable<NL> &p, dim3 grid, bool pdl, cudaStream_t s) {
     static std::atomic<uint64_t> configured{0};   // devices whose attribute is set
     const size_t smem = layer_smem_bytes(G, S * kv_stage_bytes(KV) / kStageBytes) +
-                        (umma_pass(G, KV, MT, deep_ring(S, KV), CONSUMER) ? kUmmaExtraBytes : 0);
+                        (umma_pass(G, KV, MT, deep_ring(S, KV), CONSUMER) ? umma_extra_bytes(G) : 0);
     int device = -1;
     if (!done_on_device(configured, &device)) {
         cudaError_t e = cudaFuncSetAttribute(attn_layer_kernel<G, CONSUMER, S, KV, MT, NL>,
@@ -2382,13 +2423,17 @@ cudaError_t launch_c(const LaunchTable<NL> &p, dim3 grid, int rows, bool mt, boo
 template <int KV, int NL>
 cudaError_t launch_kv(const LaunchTable<NL> &p, dim3 grid, int rows, bool mt, int consumer, int stages, bool pdl,
                       cudaStream_t s) {
-    // The tensor-memory consumer takes 16-row multi-token passes over bf16 caches;
-    // every other pass of such a call runs the tensor-core consumer.
-    if (consumer == CONSUMER_UMMA) {
+    // Multi-token passes of 32 rows over bf16 caches (more than mma.sync holds in
+    // registers) run the tcgen05 pass with a 128 KiB ring; with the tensor-memory
+    // consumer so do 16-row passes.  Every other pass runs mma.sync.
+    if (consumer == CONSUMER_UMMA || consumer == CONSUMER_MMA) {
         if constexpr (KV == KV_BF16) {
-            if (mt && rows == kMaxRows && stages == kDeepStages)
-                return launch_g<kMaxRows, CONSUMER_UMMA, kDeepStages, KV_BF16, true, NL>(p, grid, pdl, s);
+            if (consumer == CONSUMER_UMMA && mt && rows == 16 && stages == kDeepStages)
+                return launch_g<16, CONSUMER_UMMA, kDeepStages, KV_BF16, true, NL>(p, grid, pdl, s);
+            if (mt && rows == 32 && stages == kUmma32Stages)
+                return launch_g<32, CONSUMER_UMMA, kUmma32Stages, KV_BF16, true, NL>(p, grid, pdl, s);
         }
+        if (rows > kMaxRowsMma) return cudaErrorInvalidValue;
         consumer = CONSUMER_MMA;
     }
     if constexpr (NL > 1) {

@@ -48,7 +48,8 @@ __host__ __device__ constexpr int kv_stage_bytes(int kv) { return 2 * kv_boxes_p
 static_assert(kv_stage_bytes(KV_BF16) == kStageBytes && kv_stage_bytes(KV_FP8) == kStageBytes,
               "both cache types use 32 KiB stages");
 constexpr int kMaxTokens = 8;     // tokens per sequence of one multi-token step
-constexpr int kMaxRows = 16;      // query rows per kv head in one kernel (heads x tokens)
+constexpr int kMaxRows = 32;      // query rows per kv head in one kernel (heads x tokens)
+constexpr int kMaxRowsMma = 16;   // ... with the mma.sync consumers (32: the tcgen05 pass only)
 // Shared-memory bytes the multi-token combine keeps at the end of the ring: new
 // K/V values and codes, per-row new-entry weights, and per-row sink, gate and scale.
 constexpr int kMtNewBytes =
@@ -67,6 +68,11 @@ void plan_split(int64_t batch, int64_t num_kv_heads, int64_t max_keys, int64_t n
 // Shared memory of the combine: a weight per (query row, chunk) plus a float4
 // row per query row (and, for a multi-token pass, the new entries), inside the
 // stage ring of `stages` bf16 stages that the CTA no longer needs then.
+// bf16 stages of the one-CTA-per-SM ring for a pass of more than kMaxGroup rows:
+// the 32-row tensor-memory pass keeps 128 KiB (its q operand takes 32 KiB).
+constexpr int kUmma32Stages = 4;
+inline int deep_stages_for(size_t rows) { return rows > (size_t)kMaxRowsMma ? kUmma32Stages : kDeepStages; }
+
 inline bool combine_fits(size_t rows, int64_t num_chunks, bool mt, int stages) {
     return (rows * num_chunks + 3) * sizeof(float) + rows * 64 * 16 + (mt ? kMtNewBytes : 0) <=
            (size_t)stages * kStageBytes;

@@ -308,15 +308,18 @@ hd_status hybrid_decode_set_cluster_combine(hd_ctx *ctx, int32_t enable);
 
 /* Inner loop of the attention kernels (same results within the stated
  * tolerance; the default is the tensor-core one):
- *   HD_CONSUMER_CUDA_CORE     fp32 FMA with warp-shuffle reductions;
+ *   HD_CONSUMER_CUDA_CORE     fp32 FMA with warp-shuffle reductions (one
+ *                             token per sequence only);
  *   HD_CONSUMER_TENSOR_CORE   mma.sync bf16 (q split into a bf16 high and low
- *                             part) with fp32 accumulation;
- *   HD_CONSUMER_TENSOR_MEMORY as HD_CONSUMER_TENSOR_CORE, except that
- *                             multi-token passes of 16 query rows per kv head
- *                             over bf16 caches run on the tcgen05 tensor cores
- *                             (scores and outputs accumulated in tensor memory,
- *                             64-key stages).  Measured slower than the default
- *                             on GB300 for that shape; kept selectable. */
+ *                             part) with fp32 accumulation; multi-token passes
+ *                             of 32 query rows per kv head over bf16 caches
+ *                             (group x tokens, e.g. 4 x 8 or 8 x 4) run on the
+ *                             tcgen05 tensor cores with scores and outputs in
+ *                             tensor memory, one read of the cache for the 32
+ *                             rows;
+ *   HD_CONSUMER_TENSOR_MEMORY as HD_CONSUMER_TENSOR_CORE, and passes of 16
+ *                             rows also on tcgen05 (measured slower on GB300
+ *                             for that shape; kept selectable). */
 enum { HD_CONSUMER_CUDA_CORE = 0, HD_CONSUMER_TENSOR_CORE = 1, HD_CONSUMER_TENSOR_MEMORY = 2 };
 hd_status hybrid_decode_set_consumer(hd_ctx *ctx, int32_t consumer);
 

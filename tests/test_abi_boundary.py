@@ -121,7 +121,7 @@ def test_step_plan_rejects_bad_arguments(hd):
     with pytest.raises(Exception):
         hd.hd_plan_step_split([100], 0, 2, 4, 152)
     with pytest.raises(Exception):
-        hd.hd_plan_step_split([100], 1, 2, 17, 152)   # more rows than a pass takes
+        hd.hd_plan_step_split([100], 1, 2, 33, 152)   # more rows than a pass takes
     with pytest.raises(Exception):
         hd.hd_plan_step_split([-1], 1, 2, 4, 152)
 

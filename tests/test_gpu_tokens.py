@@ -164,24 +164,26 @@ def test_tokens_28_layer_step(hd, orc):
     run_case(hd, orc, synth.SPARK_LAYER_TYPES, 4, 8, 2, [700, 1500, 3], seed=903)
 
 
-# The tensor-memory consumer runs the 16-row passes (g x tokens per pass = 16) on
+# The tensor-memory consumer runs passes of 16 or 32 rows (g x tokens per pass) on
 # tcgen05 with 64-key stages; other passes of the same call run mma.sync.
 @pytest.mark.parametrize("fuse", [True, False])
-@pytest.mark.parametrize("T,g", [(4, 4), (2, 8), (8, 2), (8, 4)])
+@pytest.mark.parametrize("T,g", [(4, 4), (2, 8), (8, 2), (8, 4), (4, 8), (8, 8), (3, 8)])
 def test_tokens_tensor_memory_consumer(hd, orc, T, g, fuse):
     Hkv = 2
     run_case(hd, orc, [SLIDING, FULL], T, g * Hkv, Hkv, RING_FULL_CONTEXTS, seed=1500 + 10 * T + g, fuse=fuse,
              consumer=hd.HD_CONSUMER_TENSOR_MEMORY)
 
 
-@pytest.mark.parametrize("T", [4, 8])
-def test_tokens_tensor_memory_roll(hd, orc, T):
-    run_case(hd, orc, [SLIDING, FULL], T, 8, 2, ROLL_CONTEXTS, seed=1600 + T, layout=ROLL,
+@pytest.mark.parametrize("T,g", [(4, 4), (8, 4), (4, 8)])
+def test_tokens_tensor_memory_roll(hd, orc, T, g):
+    run_case(hd, orc, [SLIDING, FULL], T, 2 * g, 2, ROLL_CONTEXTS, seed=1600 + 10 * T + g, layout=ROLL,
              consumer=hd.HD_CONSUMER_TENSOR_MEMORY)
 
 
 def test_tokens_tensor_memory_long_context_and_28_layers(hd, orc):
     run_case(hd, orc, [FULL], 4, 8, 2, [40000, 39000 - 7], seed=1610, with_gate=False,
+             consumer=hd.HD_CONSUMER_TENSOR_MEMORY)
+    run_case(hd, orc, [FULL], 4, 16, 2, [40000, 39000 - 7], seed=1612, with_gate=False,
              consumer=hd.HD_CONSUMER_TENSOR_MEMORY)
     run_case(hd, orc, synth.SPARK_LAYER_TYPES, 4, 8, 2, [700, 1500, 3], seed=1611,
              consumer=hd.HD_CONSUMER_TENSOR_MEMORY)
