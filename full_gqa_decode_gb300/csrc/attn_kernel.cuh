@@ -1013,7 +1013,11 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     // one after the other (16 keys per consumer warp and stage, or the tcgen05 tile).
     constexpr bool kUmma = umma_pass(G, KV, MT, deep_ring(SP, KV), CONSUMER);
     constexpr bool kWide = kUmma || (HD_WIDE_MT && KV == KV_BF16 && MT && G == kMaxRowsMma && deep_ring(SP, KV));
-    constexpr int S = kWide ? SP / 2 : SP;                               // ring slots
+    // A tensor-memory pass keeps K and V halves in rings of their own: (SP + 1) / 2
+    // K slots and SP / 2 V slots (a K half is free once its scores are computed).
+    constexpr int S = kUmma ? (SP + 1) / 2 : kWide ? SP / 2 : SP;        // ring slots (of K halves)
+    constexpr int SV = kUmma ? SP / 2 : S;                               // slots of V halves
+    constexpr int kRingBytes = SP * kv_stage_bytes(KV);                  // the whole ring
     constexpr int kStage = (kWide ? 2 : 1) * kv_stage_bytes(KV);        // bytes of one stage (K + V)
     constexpr int kKeys = (kWide ? 2 : 1) * kv_stage_keys(KV);          // keys per stage: 32 bf16, 64 E4M3 or wide
     constexpr int kBoxB = (kWide ? 2 : 1) * kv_box_bytes(KV);           // bytes of one box column of a stage
@@ -1027,7 +1031,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     // rounding an integer address, keeps every pointer below in the shared space,
     // so the compiler emits shared-memory loads and stores for them.
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    float *q_s = reinterpret_cast<float *>(smem + S * kStage);               // [G][256]
+    float *q_s = reinterpret_cast<float *>(smem + kRingBytes);               // [G][256]
     float *knew_s = q_s + G * kHeadDim;                                        // [256]
     float *vnew_s = knew_s + kHeadDim;                                         // [256]
     float *kraw_s = vnew_s + kHeadDim;                                         // [256]
@@ -1137,7 +1141,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     const int sh = a.key_set == KEYS_ROLL_SHIFT ? max(0, min(c, a.window) + ntok - a.window) : 0;
     // New entries of the ntok tokens: values as scored (knew_t), V values (or
     // V codes' values for E4M3, vnew_t), codes, and per-row new-entry weights.
-    uint8_t *mt_base = smem + S * kStage - kMtNewBytes;
+    uint8_t *mt_base = smem + kRingBytes - kMtNewBytes;
     float *knew_t = MT ? reinterpret_cast<float *>(mt_base) : knew_s;                      // [ntok][256]
     float *vnew_t = MT ? knew_t + kMaxTokens * kHeadDim : vnew_s;                            // [ntok][256]
     uint8_t *code_t = MT ? reinterpret_cast<uint8_t *>(vnew_t + kMaxTokens * kHeadDim) : code_s;
@@ -1211,8 +1215,8 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     // A tensor-memory pass loads (and releases) a stage's K and V halves separately:
     // the K half is free once its scores are computed.
     auto issue_half = [&](int s, int v) {
-        const int slot = s % S;
-        uint8_t *st = smem + slot * kStage + v * kBoxes * kBoxB;
+        const int slot = v ? s % SV : s % S;
+        uint8_t *st = smem + (v ? S + slot : slot) * (kStage / 2);
         uint64_t *bar = v ? &fullv[slot] : &full[slot];
         mbar_arrive_expect_tx(bar, kStage / 2);
         const int row = roff + start + s * kKeys;
@@ -1224,11 +1228,6 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                             row + h * kv_stage_keys(KV), kvh, b);
     };
     auto issue_stage = [&](int s) {
-        if constexpr (kUmma) {
-            issue_half(s, 0);
-            issue_half(s, 1);
-            return;
-        }
         const int slot = s % S;
         uint8_t *st = smem + slot * kStage;
         mbar_arrive_expect_tx(&full[slot], kStage);
@@ -1300,6 +1299,14 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     constexpr int kIssuer = kOwnProducer ? CW * 32 : 0;
     constexpr bool kIssueEarly = NL == 1 || HD_STEP_ISSUE_EARLY;
     const int early = min(S, nst);   // stages issued before the prologue ends
+    auto issue_first = [&]() {
+        if constexpr (kUmma) {   // as many K and V halves as their rings hold
+            for (int s = 0; s < early && !droppable(s); ++s) issue_half(s, 0);
+            for (int s = 0; s < min(SV, nst) && !droppable(s); ++s) issue_half(s, 1);
+        } else {
+            for (int s = 0; s < early && !droppable(s); ++s) issue_stage(s);
+        }
+    };
     if (threadIdx.x == kIssuer) {
         for (int s = 0; s < S; ++s) {
             mbar_init(&full[s], 1);
@@ -1312,8 +1319,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                 mbar_init(&ubar[i], i == 2 || i == 3 ? CW : (i >= 7 && i < 11) ? kConsumerWarps : 1);
         }
         fence_mbar_init();
-        if (kIssueEarly)
-            for (int s = 0; s < early && !droppable(s); ++s) issue_stage(s);
+        if (kIssueEarly) issue_first();
     }
 
     if constexpr (kUmma) {
@@ -1358,8 +1364,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
         misc[3 * kMaxGroup + threadIdx.x] = gld;   // gate logit of row threadIdx.x
     }
     __syncthreads();
-    if (!kIssueEarly && threadIdx.x == kIssuer)
-        for (int s = 0; s < early && !droppable(s); ++s) issue_stage(s);
+    if (!kIssueEarly && threadIdx.x == kIssuer) issue_first();
     // Round 2: rotate each rotary pair in place (fp32; q only feeds the scores)
     // and scale every dim to log2 units.
     // (each element's word replaces its fp32 value in place)
@@ -1469,31 +1474,55 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
             constexpr int kChunks = kHeadDim * kv_elem_bytes(KV) / 16;   // 16-byte chunks per row
             const size_t seq = ((size_t)b * a.seq_stride + (size_t)kvh * a.capacity * kHeadDim) * kv_elem_bytes(KV);
             for (int s = 0; s < nst; ++s) {
-                const int slot = s % S;
+                const int slot = s % S, vslot = s % SV;
                 bool landed = mbar_wait(&full[slot], (s / S) & 1);
-                if constexpr (kUmma) landed = landed && mbar_wait(&fullv[slot], (s / S) & 1);
+                if constexpr (kUmma) landed = landed && mbar_wait(&fullv[vslot], (s / SV) & 1);
                 if (!__all_sync(0xffffffffu, landed)) {
                     if (lane == 0) atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
-                const uint8_t *st = smem + slot * kStage;
+                const uint8_t *kst = kUmma ? smem + slot * (kStage / 2) : smem + slot * kStage;
+                const uint8_t *vst = kUmma ? smem + (S + vslot) * (kStage / 2) : kst + kBoxes * kBoxB;
                 const int key0 = start + s * kKeys, nrows = min(kKeys, end - key0);
                 for (int i = lane; i < 2 * nrows * kChunks; i += 32) {
                     const int v = i >= nrows * kChunks, rem = i - v * nrows * kChunks;
                     const int r = rem / kChunks, ch = rem % kChunks, row = key0 + r + roff;
                     if (row < sh) continue;
                     const uint4 x = *reinterpret_cast<const uint4 *>(
-                        st + v * kBoxes * kBoxB + (ch >> 3) * kBoxB + r * 128 + ((((ch & 7) ^ (r & 7))) << 4));
+                        (v ? vst : kst) + (ch >> 3) * kBoxB + r * 128 + ((((ch & 7) ^ (r & 7))) << 4));
                     *reinterpret_cast<uint4 *>(static_cast<uint8_t *>(v ? a.cache_v : a.cache_k) + seq +
                                                (size_t)(row - sh) * kHeadDim * kv_elem_bytes(KV) + 16 * ch) = x;
                 }
                 __syncwarp();
                 int stop = 0;
-                if (lane == 0 && s + S < nst) {
+                if constexpr (kUmma) {
+                    // refill the K slot with stage s + S and the V slot with stage s + SV
+                    if (lane == 0 && s + S < nst) {
+                        if (droppable(s + S)) {
+                            stop = 1;
+                        } else if (!mbar_wait(&empty[slot], (s / S) & 1)) {
+                            atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
+                            stop = 1;
+                        } else {
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                            issue_half(s + S, 0);
+                        }
+                    }
+                    if (lane == 0 && !stop && s + SV < nst) {
+                        if (droppable(s + SV)) {
+                            stop = 1;
+                        } else if (!mbar_wait(&emptyv[vslot], (s / SV) & 1)) {
+                            atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
+                            stop = 1;
+                        } else {
+                            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                            issue_half(s + SV, 1);
+                        }
+                    }
+                } else if (lane == 0 && s + S < nst) {
                     if (droppable(s + S)) {
                         stop = 1;
-                    } else if (!mbar_wait(&empty[slot], (s / S) & 1) ||
-                               (kUmma && !mbar_wait(&emptyv[slot], (s / S) & 1))) {
+                    } else if (!mbar_wait(&empty[slot], (s / S) & 1)) {
                         atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
                         stop = 1;
                     } else {
@@ -1507,11 +1536,12 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
         } else if (lane < (kUmma ? 2 : 1)) {
             // producer: one lane issues every load of the chunk (a tensor-memory pass:
             // lane 0 the K halves, lane 1 the V halves, each as its half is released)
-            for (int s = early; s < nst; ++s) {
+            const int ns = kUmma && lane == 1 ? SV : S;   // slots of this lane's ring
+            for (int s = min(ns, nst); s < nst; ++s) {
                 if (droppable(s)) break;
-                const int slot = s % S;
+                const int slot = s % ns;
                 uint64_t *emp = kUmma && lane == 1 ? &emptyv[slot] : &empty[slot];
-                if (s >= S && !mbar_wait(emp, ((s / S) - 1) & 1)) {
+                if (s >= ns && !mbar_wait(emp, ((s / ns) - 1) & 1)) {
                     atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
                     break;
                 }
@@ -1546,8 +1576,8 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                 // Descriptors are built once; an operand's k-step or slot only moves the
                 // start-address field (16-byte units; shared addresses stay below 2^18),
                 // so each MMA costs one 64-bit add per operand.
-                const uint64_t kd0 = umma_desc(smem_u32(smem), 16, 1024, 2);                    // K tiles
-                const uint64_t vd0 = umma_desc(smem_u32(smem) + kBoxes * kBoxB, kBoxB, 1024, 2);  // V tiles
+                const uint64_t kd0 = umma_desc(smem_u32(smem), 16, 1024, 2);                      // K halves
+                const uint64_t vd0 = umma_desc(smem_u32(smem) + S * (kStage / 2), kBoxB, 1024, 2);  // V halves
                 const uint64_t qd0 = umma_desc(smem_u32(q_s), 16, 1024, 2);
                 // P^T: 8 keys x 8 rows per 128-byte core matrix, rows first (stride offset
                 // 128), then keys (leading offset 16G bytes per 8 keys)
@@ -1560,10 +1590,10 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                 unsigned long long t_last = globaltimer_ns();
                 unsigned spins = 0;
                 while (pv < nst) {
-                    if (pv < q && mbar_test_wait(&fullv[pv % S], (pv / S) & 1) &&
+                    if (pv < q && mbar_test_wait(&fullv[pv % SV], (pv / SV) & 1) &&
                         mbar_test_wait(&ubar[2 + (pv & 1)], (pv >> 1) & 1)) {
                         tc_fence_after();
-                        const uint64_t vd = vd0 + (uint64_t)((pv % S) * (kStage >> 4));
+                        const uint64_t vd = vd0 + (uint64_t)((pv % SV) * ((kStage / 2) >> 4));
                         const uint64_t pd = pd0 + (uint64_t)((pv & 1) * (kPB >> 4));
                         const uint32_t dO = tbase + 4 * G + (pv & 1) * 2 * G;
 #pragma unroll
@@ -1573,12 +1603,12 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                                 umma_bf16(dO + h * G, vd + (uint64_t)((2 * h * kBoxB + t * 2048) >> 4),
                                           pd + (uint64_t)((t * 32 * G) >> 4), kIdPV, t > 0);
                         umma_commit(&ubar[4 + (pv & 1)]);
-                        umma_commit(&emptyv[pv % S]);
+                        umma_commit(&emptyv[pv % SV]);
                         ++pv;
                         spins = 0;
                     } else if (q < nst && q <= pv + 1 && mbar_test_wait(&full[q % S], (q / S) & 1)) {
                         tc_fence_after();
-                        const uint64_t kd = kd0 + (uint64_t)((q % S) * (kStage >> 4));
+                        const uint64_t kd = kd0 + (uint64_t)((q % S) * ((kStage / 2) >> 4));
                         const uint32_t dS = tbase + (q & 1) * 2 * G;
 #pragma unroll
                         for (int kk = 0; kk < 16; ++kk)
@@ -1726,11 +1756,11 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                 // rows of a short stage are cleared (the K rows only reach masked scores).
                 const int nv = end - (start + s * kKeys);
                 if (nv < kKeys) {
-                    if (!__all_sync(0xffffffffu, mbar_wait(&fullv[s % S], (s / S) & 1))) {   // the V half has landed
+                    if (!__all_sync(0xffffffffu, mbar_wait(&fullv[s % SV], (s / SV) & 1))) {   // the V half has landed
                         fail();
                         break;
                     }
-                    uint8_t *vst = smem + (s % S) * kStage + kBoxes * kBoxB;
+                    uint8_t *vst = smem + (S + s % SV) * (kStage / 2);
                     const int per = (kKeys - nv) * 8;   // 16-byte chunks per box column
                     for (int i = threadIdx.x; i < kBoxes * per; i += CW * 32)
                         *reinterpret_cast<uint4 *>(vst + (i / per) * kBoxB + (nv + (i % per) / 8) * 128 + (i % 8) * 16) =
@@ -1884,7 +1914,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     // this chunk's partial, the warp weights and the rows' lse sit past the warp buffers
     constexpr int kRedBytes = (NRW * CG * kHeadDim + 2 * NRW * CG) * (int)sizeof(float);
     constexpr int kOwnOff = kRedBytes <= kOwnPartialOffset ? kOwnPartialOffset : (kRedBytes + 1023) / 1024 * 1024;
-    static_assert(kOwnOff + G * (kHeadDim + 2 + WPG + 1 + kMaxCluster) * (int)sizeof(float) <= S * kStage - kMtNewBytes,
+    static_assert(kOwnOff + G * (kHeadDim + 2 + WPG + 1 + kMaxCluster) * (int)sizeof(float) <= kRingBytes - kMtNewBytes,
                   "warp buffers, own partial and the multi-token entries fit the ring");
     float *own_o = reinterpret_cast<float *>(smem + kOwnOff);   // [G][256]
     float2 *own_ml = reinterpret_cast<float2 *>(own_o + G * kHeadDim);    // [G]
@@ -1977,7 +2007,7 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     };
 
     // (single-layer deep-ring launches only: the host sends clusters nowhere else)
-    if constexpr (NL == 1 && !MT && S * kStage > kStages * kStageBytes) {
+    if constexpr (NL == 1 && !MT && kRingBytes > kStages * kStageBytes) {
         if (clus > 1) {
             // Cluster combine: CTA r of the cluster holds chunk r's partial in its
             // shared memory.  After the cluster barrier every CTA reads all chunks'
@@ -2430,7 +2460,7 @@ cudaError_t launch_kv(const LaunchTable<NL> &p, dim3 grid, int rows, bool mt, in
         if constexpr (KV == KV_BF16) {
             if (consumer == CONSUMER_UMMA && mt && rows == 16 && stages == kDeepStages)
                 return launch_g<16, CONSUMER_UMMA, kDeepStages, KV_BF16, true, NL>(p, grid, pdl, s);
-            if (mt && rows == 32 && stages == kUmma32Stages)
+            if (mt && rows == 32 && stages == kUmma32Stages)   // three K-half and two V-half slots
                 return launch_g<32, CONSUMER_UMMA, kUmma32Stages, KV_BF16, true, NL>(p, grid, pdl, s);
         }
         if (rows > kMaxRowsMma) return cudaErrorInvalidValue;

@@ -69,8 +69,9 @@ void plan_split(int64_t batch, int64_t num_kv_heads, int64_t max_keys, int64_t n
 // row per query row (and, for a multi-token pass, the new entries), inside the
 // stage ring of `stages` bf16 stages that the CTA no longer needs then.
 // bf16 stages of the one-CTA-per-SM ring for a pass of more than kMaxGroup rows:
-// the 32-row tensor-memory pass keeps 128 KiB (its q operand takes 32 KiB).
-constexpr int kUmma32Stages = 4;
+// the 32-row tensor-memory pass keeps 160 KiB -- three K halves and two V halves of
+// 64-key stages (its q operand takes 32 KiB).
+constexpr int kUmma32Stages = 5;
 inline int deep_stages_for(size_t rows) { return rows > (size_t)kMaxRowsMma ? kUmma32Stages : kDeepStages; }
 
 inline bool combine_fits(size_t rows, int64_t num_chunks, bool mt, int stages) {
