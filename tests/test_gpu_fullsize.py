@@ -154,3 +154,36 @@ def test_group8_batch256_ring_and_roll(hd, orc):
     _check_against_oracle(hd, orc, roll, snap_roll, samples, layers=[0, 1, 3])
     ring.ctx.close()
     roll.ctx.close()
+
+
+def _check_tokens_against_oracle(orc, wl, snap, samples):
+    """Every layer of a multi-token step for the sampled sequences: the oracle's
+    T single-token steps in order (its caches updated in place)."""
+    sink = None if wl.sink is None else wl.sink.cpu().numpy()
+    layout = synth.LAYOUT_ROLL if wl.layout == synth.LAYOUT_ROLL else synth.LAYOUT_RING
+    for i, t in enumerate(wl.types):
+        rot, theta = synth.ROPE[t]
+        L = wl.layers[i]
+        for b in samples:
+            s = snap[i][b]
+            kc, vc = s["kc"].copy(), s["vc"].copy()
+            ref = orc.decode_tokens(layer_type=t, layout=layout if t == synth.SLIDING else 0, window=synth.WINDOW,
+                                    rotary_dim=rot, rope_theta=theta, context=wl.context[b:b + 1], q=s["q"],
+                                    k=s["k"], v=s["v"], kcache=kc, vcache=vc, sink=sink, gate=None,
+                                    k_scale=None, v_scale=None)
+            assert_out_close(L["out"][b:b + 1], ref["out"], f"layer {i} seq {b} out")
+            assert_lse_close(L["lse"][b:b + 1], ref["lse"], f"layer {i} seq {b} lse")
+            assert_bits_equal(L["kc"][b:b + 1], kc, f"layer {i} seq {b} K cache")
+            assert_bits_equal(L["vc"][b:b + 1], vc, f"layer {i} seq {b} V cache")
+
+
+def test_step28_batch64_eight_tokens(hd, orc):
+    """The benchmark workload decoding 8 tokens per sequence, as bench.py's
+    multi_token T = 8 runs it: 32 query rows per kv head, one tcgen05 pass per
+    layer over the whole cache."""
+    wl = bench.Workload("step28_b64_c512_32768", torch.device("cuda"), seed=0, tokens=8)
+    samples = _samples(wl.context)
+    snap = _snapshot(wl, samples)
+    _run(hd, wl)
+    _check_tokens_against_oracle(orc, wl, snap, samples)
+    wl.ctx.close()
