@@ -841,10 +841,10 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
     return decode_step_tokens(ctx, batch, 1, context, max_context_hint, layers, stream);
 }
 
-// T tokens per sequence: each layer runs in passes of up to kMaxRows / group
-// tokens (a power of two, at most kMaxTokens), the tokens of a pass being extra
-// query rows that share one stream of the cache; passes of more than kMaxGroup
-// rows run one CTA per SM on the deep ring.  A pass commits its entries, so the next pass
+// T tokens per sequence: each layer runs in passes of up to 32 (bf16 caches: the
+// tcgen05 pass) or 16 rows / group tokens (a power of two, at most kMaxTokens),
+// the tokens of a pass being extra query rows that share one stream of the
+// cache; passes of more than kMaxGroup rows run one CTA per SM on a deep ring.  A pass commits its entries, so the next pass
 // (launched in full stream order) sees them as cached keys at context + token0.
 hd_status decode_step_tokens(hd_ctx *ctx, int32_t batch, int32_t num_tokens, const int32_t *context,
                              int32_t max_context_hint, const hd_layer_io *layers, void *stream) {

@@ -267,8 +267,10 @@ hd_status decode_step(hd_ctx *ctx, int32_t batch, const int32_t *context, int32_
  * the batch index: q, out [batch][num_tokens][num_q_heads][head_dim]; k, v
  * [batch][num_tokens][num_kv_heads][head_dim]; lse, gate
  * [batch][num_tokens][num_q_heads].  The tokens of a sequence are extra query
- * rows sharing one read of the cache, up to 16 rows (and 8 tokens) per kv
- * head per pass (group 4: four tokens per pass).  Full layers append num_tokens entries;
+ * rows sharing one read of the cache, up to 32 rows (bf16 caches; 16 with
+ * E4M3) and 8 tokens per kv head per pass (group 4: eight tokens in one pass;
+ * 32-row passes run on the tcgen05 tensor cores, see hybrid_decode_set_consumer).
+ * Full layers append num_tokens entries;
  * sliding ring layers write slots (c + t) mod (window-1) after reading;
  * sliding roll layers read their window once, then drop the entries that leave
  * it (the window shifts down by that many rows) and append the num_tokens
