@@ -26,7 +26,10 @@
 // reductions, and tensor-core mma.sync with fp32 accumulation, where q is
 // split into a high and a low part (bf16, or f16 for E4M3 caches) so the
 // scores keep fp32 accuracy.  With MT, several tokens of a sequence are extra
-// query rows (multi-token decode).
+// query rows (multi-token decode): 16 rows run on 64-key stages (16 keys per
+// warp and call), and 32 rows -- more accumulators than registers hold -- on
+// the 5th-generation tensor cores (tcgen05.mma, scores and outputs in tensor
+// memory; see "Tensor-memory pass").
 //
 // A launch takes one layer (grid: chunks x kv heads x sequences) or, for a
 // whole decode step, a table of up to kStepLayers layers in its parameters
@@ -56,7 +59,7 @@
 
 // Build switches of the attention kernel (measured choices; see the comments at their use).
 #ifndef HD_STEP_NEW_IN_EVERY_CTA
-#define HD_STEP_NEW_IN_EVERY_CTA 0
+#define HD_STEP_NEW_IN_EVERY_CTA 1
 #endif
 #ifndef HD_STEP_ISSUE_EARLY
 #define HD_STEP_ISSUE_EARLY 1
@@ -1257,12 +1260,14 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     // of the stream, and the stream starts before they are back.
     const bool has_new = a.new_kind != NEW_NONE;
     // Where a single-token pass makes its new entry (rotation or quantisation,
-    // score): in the prologue of every CTA of a single-layer launch (whichever
-    // CTA combines then has it at hand, which shortens the layer's critical
-    // path), or -- in step grids, where throughput matters more than one
-    // layer's latency -- only in the CTA of a single-chunk sequence, the
-    // combining CTA of a longer one making it after its ticket.
-    constexpr bool kNewInEveryCta = NL == 1 || HD_STEP_NEW_IN_EVERY_CTA;
+    // score): in the prologue of every CTA, while the first stages are in flight
+    // (whichever CTA combines then has it at hand, which shortens the critical
+    // path: the bf16 batch-1 step grid 22.1 -> 21.75 us, the batch-64 one
+    // unchanged since the key's rotation takes the binary32 path); in E4M3 step
+    // grids (fp64 rotation and quantisation: +0.8 % at batch 64 in every CTA), and
+    // with the switch off, only the CTA of a single-chunk sequence, the combining
+    // CTA of a longer one making it after its ticket.
+    constexpr bool kNewInEveryCta = NL == 1 || (HD_STEP_NEW_IN_EVERY_CTA && KV == KV_BF16);
     const bool new_early = !MT && has_new && (kNewInEveryCta || nchunks == 1 || clus > 1);
     const int half = a.rotary_dim >> 1;
     constexpr int kQLoads = (G * (kHeadDim / 4) + kNThreads - 1) / kNThreads;   // 16-byte q loads per thread
