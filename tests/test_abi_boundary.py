@@ -194,3 +194,13 @@ def test_static_scratch_plan_rejects_bad_shapes(hd):
     assert plan(4, 8, 2, -1, 152)[3] == 1          # negative context bound
     assert plan(4, 8, 2, 10, 0)[3] == 1            # no SMs
     assert plan(4, 32, 2, 10, 152)[3] == 2         # group 16
+
+
+@pytest.mark.parametrize("rows", [16, 32])
+def test_step_plan_multi_token_passes_fit_their_ring(hd, rows):
+    """Multi-token passes of 16 rows (six-stage ring) and 32 rows (the tcgen05 pass's
+    160 KiB ring): the step plan picks a chunk whose combine fits that ring, for the
+    benchmark's batch-64 step and the 131k-context case."""
+    for keys, batch in ((_spark_keys(32768 + 8), 64), ([131072 + 8] * 7, 4)):
+        c = hd.hd_plan_step_split(keys, batch, 2, rows, 152, multi_token=True)
+        assert c % 64 == 0 and 64 <= c <= 2048
