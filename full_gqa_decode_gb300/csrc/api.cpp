@@ -713,6 +713,10 @@ hd_status hybrid_decode_init(const hd_config *cfg, hd_ctx **out_ctx) {
               cudaMemset(ctx->err, 0, sizeof(int32_t)) == cudaSuccess;
     const size_t stage = (size_t)cfg->num_layers * B * Hkv * kHeadDim * kv_elem_bytes(ctx->kv_type);
     ok = ok && cudaMalloc(&ctx->stage_k, stage) == cudaSuccess && cudaMalloc(&ctx->stage_v, stage) == cudaSuccess;
+    // The tables, zeroed counters and error word are complete before any call, on
+    // whatever stream the caller uses (a non-blocking stream is not ordered after
+    // the legacy-stream copies and memsets above).
+    ok = ok && cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
         free_ctx(ctx);
         return HD_ERR_CUDA;
