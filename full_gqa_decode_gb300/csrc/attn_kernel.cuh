@@ -1538,22 +1538,52 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
                 }
                 if (__shfl_sync(0xffffffffu, stop, 0)) break;
             }
-        } else if (lane < (kUmma ? 2 : 1)) {
-            // producer: one lane issues every load of the chunk (a tensor-memory pass:
-            // lane 0 the K halves, lane 1 the V halves, each as its half is released)
-            const int ns = kUmma && lane == 1 ? SV : S;   // slots of this lane's ring
-            for (int s = min(ns, nst); s < nst; ++s) {
-                if (droppable(s)) break;
-                const int slot = s % ns;
-                uint64_t *emp = kUmma && lane == 1 ? &emptyv[slot] : &empty[slot];
-                if (s >= ns && !mbar_wait(emp, ((s / ns) - 1) & 1)) {
-                    atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
-                    break;
+        } else if (lane == 0) {
+            if constexpr (kUmma) {
+                // Tensor-memory pass: K and V halves have rings of their own; one lane
+                // polls both (non-blocking) and refills each half as soon as its slot
+                // is released, K first.
+                int sk = min(S, nst), sv = min(SV, nst);   // next K and V halves to issue
+                unsigned long long t_last = globaltimer_ns();
+                unsigned spins = 0;
+                while (sk < nst || sv < nst) {
+                    bool did = false;
+                    if (sk < nst) {
+                        if (droppable(sk)) {
+                            sk = nst;
+                        } else if (mbar_test_wait(&empty[sk % S], ((sk / S) - 1) & 1)) {
+                            issue_half(sk++, 0);
+                            did = true;
+                        }
+                    }
+                    if (sv < nst) {
+                        if (droppable(sv)) {
+                            sv = nst;
+                        } else if (mbar_test_wait(&emptyv[sv % SV], ((sv / SV) - 1) & 1)) {
+                            issue_half(sv++, 1);
+                            did = true;
+                        }
+                    }
+                    if (did) {
+                        spins = 0;
+                    } else if (++spins == 1) {
+                        t_last = globaltimer_ns();
+                    } else if ((spins & 63) == 0 && globaltimer_ns() - t_last > kWaitLimitNs) {
+                        atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
+                        break;
+                    }
                 }
-                if constexpr (kUmma)
-                    issue_half(s, lane);
-                else
+            } else {
+                // producer: one lane issues every load of the chunk
+                for (int s = early; s < nst; ++s) {
+                    if (droppable(s)) break;
+                    const int slot = s % S;
+                    if (s >= S && !mbar_wait(&empty[slot], ((s / S) - 1) & 1)) {
+                        atomicOr(a.err, HD_DEVERR_WAIT_TIMEOUT);
+                        break;
+                    }
                     issue_stage(s);
+                }
             }
         }
         __syncthreads();
