@@ -683,7 +683,7 @@ hd_status hybrid_decode_init(const hd_config *cfg, hd_ctx **out_ctx) {
         free_ctx(ctx);
         return st;
     }
-    const int Hq = cfg->num_q_heads, Hkv = cfg->num_kv_heads, B = cfg->max_batch;
+    const int Hkv = cfg->num_kv_heads, B = cfg->max_batch;
     int64_t slots = 0;
     if (any_full) slots = part_slot_capacity(B, cfg->max_context + 1, ctx->num_sms);
     if (any_sliding) {
