@@ -404,7 +404,7 @@ int32_t hd::plan_step(int64_t Hkv, int64_t sms, int kv_type, size_t rows, bool m
                       const int32_t *max_keys, const uint8_t *one_chunk) {
     const int64_t cmax = kv_type == KV_FP8 ? 2 * kChunkMax : kChunkMax;
     const int64_t fixed = (256 << 10) / (kHeadDim * kv_elem_bytes(kv_type) * 2);   // keys
-    const int stages = rows > (size_t)kMaxGroup ? deep_stages_for(rows) : kStages;
+    const int stages = step_stages(kv_type, rows, mt);
     int64_t longest = 1;
     for (int i = 0; i < n; ++i) longest = std::max<int64_t>(longest, max_keys[i]);
     int64_t best_c = cmax;
@@ -458,7 +458,7 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
         if (t.num_layers == 0) return HD_OK;
         const int stages = rows > (size_t)kMaxGroup ? deep_stages_for(rows)
                            : ctas <= ctx->num_sms  ? kDeepStages
-                                                   : kStages;
+                                                   : step_stages(ctx->kv_type, rows, mt);
         const size_t slot = 2 * (size_t)kProfileEvents + ctx->ev_used[2];
         const bool timed = (ctx->profile_mask & HD_PROFILE_STEP) && ctx->ev_used[2] < (size_t)kProfileEvents;
         if (timed && cudaEventRecord(ctx->ev_begin[slot], stream) != cudaSuccess) return HD_ERR_CUDA;
@@ -483,7 +483,7 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
         // Too large for a shared grid (its partials, its combine's shared memory at
         // this chunk count, or its CTA count): its own plan and launch, in stream order.
         if (need > ctx->part_rows || layer_ctas > INT_MAX ||
-            !combine_fits(rows, ch, mt, rows > (size_t)kMaxGroup ? deep_stages_for(rows) : kStages)) {
+            !combine_fits(rows, ch, mt, step_stages(ctx->kv_type, rows, mt))) {
             if ((st = flush()) != HD_OK || (st = launch_layer_call(ctx, L, stream)) != HD_OK) return st;
             continue;
         }

@@ -116,8 +116,11 @@ __host__ __device__ constexpr int umma_p_bytes(int g) { return 64 * g * 2; }
 __host__ __device__ constexpr int umma_extra_bytes(int g) {
     return 128 + 2 * umma_p_bytes(g) + 3 * kConsumerWarps * g * 4 + 20 * 8 + 16;
 }
-// A ring of more than the default bytes: one CTA per SM.
+// A ring of more than the default bytes: one CTA per SM; of at most two stages: three.
 __host__ __device__ constexpr bool deep_ring(int s, int kv) { return s * kv_stage_bytes(kv) > kStages * kStageBytes; }
+__host__ __device__ constexpr int ctas_per_sm(int s, int kv) {
+    return deep_ring(s, kv) ? 1 : s * kv_stage_bytes(kv) <= kTripleStages * kStageBytes ? 3 : 2;
+}
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // 1 s
 // Inside the stage ring (free once every stage is consumed): the warp buffers
 // [warps][G][256] + (m, l) and the combine weights start at 0; this chunk's
@@ -1009,7 +1012,7 @@ struct Fp8MmaConsumer {
 // NL: layers in the parameter table (1: one layer, grid (chunks, kv heads,
 // sequences); kStepLayers: a step, 1-D grid over the layers' CTA ranges).
 template <int G, int CONSUMER, int SP, int KV, bool MT, int NL>
-__global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV), CONSUMER), deep_ring(SP, KV) ? 1 : 2)
+__global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV), CONSUMER), ctas_per_sm(SP, KV))
     attn_layer_kernel(const __grid_constant__ LaunchTable<NL> p) {
     // SP: the ring in 32 KiB stages.  A 16-row multi-token pass over a bf16 cache
     // takes them in pairs: 64-key stages, each K or V box column two 32-row boxes
@@ -1948,9 +1951,15 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     const size_t pbase = ((size_t)b * a.num_kv_heads * G + kvh * G) * a.max_chunks;
     // this chunk's partial, the warp weights and the rows' lse sit past the warp buffers
     constexpr int kRedBytes = (NRW * CG * kHeadDim + 2 * NRW * CG) * (int)sizeof(float);
-    constexpr int kOwnOff = kRedBytes <= kOwnPartialOffset ? kOwnPartialOffset : (kRedBytes + 1023) / 1024 * 1024;
-    static_assert(kOwnOff + G * (kHeadDim + 2 + WPG + 1 + kMaxCluster) * (int)sizeof(float) <= kRingBytes - kMtNewBytes,
+    // (a two-stage ring, single-token only, has its own partial right past the warp buffers)
+    constexpr int kRedEnd = (kRedBytes + 1023) / 1024 * 1024;
+    constexpr int kOwnOff = kRingBytes <= kTripleStages * kStageBytes ? kRedEnd
+                            : kRedBytes <= kOwnPartialOffset          ? kOwnPartialOffset
+                                                                      : kRedEnd;
+    static_assert(kOwnOff + G * (kHeadDim + 2 + WPG + 1 + kMaxCluster) * (int)sizeof(float) <=
+                      kRingBytes - (MT ? kMtNewBytes : 0),
                   "warp buffers, own partial and the multi-token entries fit the ring");
+    static_assert(!MT || kRingBytes > kTripleStages * kStageBytes, "multi-token passes keep at least three stages");
     float *own_o = reinterpret_cast<float *>(smem + kOwnOff);   // [G][256]
     float2 *own_ml = reinterpret_cast<float2 *>(own_o + G * kHeadDim);    // [G]
     float *wwarp = reinterpret_cast<float *>(own_ml + G);                 // [G][WPG]
@@ -2503,6 +2512,12 @@ cudaError_t launch_kv(const LaunchTable<NL> &p, dim3 grid, int rows, bool mt, in
     }
     if constexpr (NL > 1) {
         if (consumer != CONSUMER_MMA) return cudaErrorInvalidValue;
+        if constexpr (KV == KV_FP8) {   // three CTAs per SM: single-token grids of kTripleRows rows
+            if (stages == kTripleStages) {
+                if (mt || rows != kTripleRows) return cudaErrorInvalidValue;
+                return launch_g<kTripleRows, CONSUMER_MMA, kTripleStages, KV, false, NL>(p, grid, pdl, s);
+            }
+        }
         return stages == kDeepStages ? launch_c<CONSUMER_MMA, kDeepStages, KV, NL>(p, grid, rows, mt, pdl, s)
                                      : launch_c<CONSUMER_MMA, kStages, KV, NL>(p, grid, rows, mt, pdl, s);
     } else {

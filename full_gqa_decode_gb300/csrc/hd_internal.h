@@ -30,6 +30,8 @@ constexpr int kMaxGroup = 8;      // query heads per kv head
 constexpr int kStageKeys = 32;    // keys per pipeline stage (rows of one TMA box)
 constexpr int kStages = 3;        // bf16 stages per CTA with two CTAs per SM (the default)
 constexpr int kDeepStages = 6;    // bf16 stages per CTA with one CTA per SM (grids of at most one CTA per SM)
+constexpr int kTripleStages = 2;  // stages per CTA with three CTAs per SM (E4M3 step grids of 4 rows)
+constexpr int kTripleRows = 4;
 constexpr int kBoxCols = 64;      // bf16 columns per 128-byte swizzled box row
 constexpr int kBoxesPerRow = kHeadDim / kBoxCols;                 // 4
 constexpr int kBoxBytes = kStageKeys * 128;                       // 4 KiB
@@ -65,15 +67,27 @@ void plan_split(int64_t batch, int64_t num_kv_heads, int64_t max_keys, int64_t n
                 int64_t max_slots, int32_t *chunk_keys, int32_t *num_chunks, int32_t *stages = nullptr,
                 int64_t chunk_max = kChunkMax);
 
-// Shared memory of the combine: a weight per (query row, chunk) plus a float4
-// row per query row (and, for a multi-token pass, the new entries), inside the
-// stage ring of `stages` bf16 stages that the CTA no longer needs then.
 // bf16 stages of the one-CTA-per-SM ring for a pass of more than kMaxGroup rows:
 // the 32-row tensor-memory pass keeps 160 KiB -- three K halves and two V halves of
 // 64-key stages (its q operand takes 32 KiB).
 constexpr int kUmma32Stages = 5;
 inline int deep_stages_for(size_t rows) { return rows > (size_t)kMaxRowsMma ? kUmma32Stages : kDeepStages; }
 
+// Ring of a step grid with more CTAs than SMs.  Single-token E4M3 grids of
+// kTripleRows rows (group 4) run three CTAs per SM on two-stage rings: twelve
+// consumer warps per SM hide more of the per-tile conversion and MMA chain than
+// eight do on three-stage rings (the batch-64 E4M3 step 1.206 -> 1.175 ms, the
+// 131k-context one 0.543 -> 0.536 ms).  At the 168 registers that three CTAs
+// leave a thread, groups 1 and 2 spill, and group 8 does not fit three rings in
+// shared memory; those grids, and all others, keep two CTAs per SM.
+inline int step_stages(int kv, size_t rows, bool mt) {
+    if (rows > (size_t)kMaxGroup) return deep_stages_for(rows);
+    return kv == KV_FP8 && !mt && rows == (size_t)kTripleRows ? kTripleStages : kStages;
+}
+
+// Shared memory of the combine: a weight per (query row, chunk) plus a float4
+// row per query row (and, for a multi-token pass, the new entries), inside the
+// stage ring of `stages` bf16 stages that the CTA no longer needs then.
 inline bool combine_fits(size_t rows, int64_t num_chunks, bool mt, int stages) {
     return (rows * num_chunks + 3) * sizeof(float) + rows * 64 * 16 + (mt ? kMtNewBytes : 0) <=
            (size_t)stages * kStageBytes;

@@ -129,6 +129,48 @@ def test_fp8_decode_step_28_layers(hd, orc, layout, consumer):
 
 
 @pytest.mark.parametrize("layout", [RING, ROLL])
+def test_fp8_step_grid_three_ctas_per_sm(hd, orc, layout):
+    """A group-4 E4M3 step grid with more CTAs than SMs (three CTAs per SM on
+    two-stage rings): full layers in several chunks with a ragged last one, sliding
+    layers in one, contexts from empty to the bound; every layer against the oracle."""
+    import math
+    rng = synth.generator(655)
+    B, Hq, Hkv, D, mc = 8, 8, 2, 256, 3000
+    context = np.array([0, 1, 511, 512, 1024, 1500, 2047, mc - 1], np.int32)
+    types = synth.SPARK_LAYER_TYPES
+    keys = [511 if t == SLIDING else mc + 1 for t in types]
+    chunk = hd.hd_plan_step_split(keys, B, Hkv, Hq // Hkv, 152, kv_dtype=hd.HD_KV_FP8_E4M3)
+    ctas = sum(B * Hkv * max(1, math.ceil(k / chunk)) for k in keys)
+    assert ctas > torch.cuda.get_device_properties(0).multi_processor_count
+    ctx = make_ctx(hd, types, layout=layout, max_batch=B, max_context=mc)
+    sink = synth.sink_vector(rng, ("normal", 2.0 ** 0.5, 0.25), Hq)
+    cases, ios, keep = [], [], []
+    for t in types:
+        cap = (511 if layout == RING else 512) if t == SLIDING else mc + 1
+        case = LayerCase(rng, B, Hq, Hkv, cap, context, sink=sink, kv="fp8")
+        kd, vd = case.kc.cuda(), case.vc.cuda()
+        out = torch.empty(B, Hq, D, dtype=torch.bfloat16, device="cuda")
+        lse = torch.empty(B, Hq, dtype=torch.float32, device="cuda")
+        dev_in = (case.q.cuda(), case.k.cuda(), case.v.cuda(), sink.cuda())
+        cache = case.cache(hd, kd, vd, torch.device("cuda"))
+        ios.append(hd.layer_io(dev_in[0], dev_in[1], dev_in[2], cache, dev_in[3], out, lse))
+        cases.append(case)
+        keep.append((out, lse, kd, vd, dev_in, cache))
+    launches = hd.hybrid_decode_launch_count(ctx)
+    hd.decode_step(ctx, torch.from_numpy(context).cuda(), ios, B)
+    torch.cuda.synchronize()
+    assert hd.hybrid_decode_launch_count(ctx) - launches == 1, "one step grid"
+    assert hd.hybrid_decode_device_errors(ctx) == 0
+    for i, (t, case) in enumerate(zip(types, cases)):
+        ref = oracle_layer(orc, case, t, layout)
+        out, lse, kd, vd = keep[i][:4]
+        assert_out_close(out, ref["out"], f"layer {i} out")
+        assert_lse_close(lse, ref["lse"], f"layer {i} lse")
+        assert_bits_equal(kd, ref["kcache"], f"layer {i} K codes")
+        assert_bits_equal(vd, ref["vcache"], f"layer {i} V codes")
+
+
+@pytest.mark.parametrize("layout", [RING, ROLL])
 def test_fp8_decode_step_multistep_lockstep(hd, orc, layout):
     """30 consecutive decode_step calls of a [S,S,S,F] block across the window: every
     output and, at the end, every cache code equals the oracle's."""
