@@ -383,8 +383,9 @@ hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream
 // fixed cost for its start and combine of about 256 KiB of streaming (256
 // bf16 or 512 E4M3 keys; fitted to batch-4 131k-context steps, where
 // 2048-key bf16 chunks beat shorter ones): a grid that is resident at once
-// (two CTAs per SM) ends with its most loaded SM, ceil(CTAs / SMs) CTAs of up
-// to C keys; a longer grid takes the total over the SMs plus one CTA of tail.
+// (two CTAs per SM in the model, also for the E4M3 grids that hold three) ends
+// with its most loaded SM, ceil(CTAs / SMs) CTAs of up to C keys; a longer grid
+// takes the total over the SMs plus one CTA of tail.
 int32_t plan_step_chunk(const hd_ctx *ctx, const std::vector<LayerCall> &calls, size_t rows, bool mt) {
     const int n = (int)calls.size();
     std::vector<int32_t> batch(n), max_keys(n);
