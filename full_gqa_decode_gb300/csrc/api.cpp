@@ -68,7 +68,9 @@ struct MapCacheEntry {
     const void *k = nullptr, *v = nullptr;
     int64_t seq_stride = 0;
     int32_t capacity = 0, batch = 0;
-    CUtensorMap kmap, vmap;
+    CUtensorMap kmap, vmap;     // boxes of one stage's keys
+    bool wide_valid = false;    // kmapw / vmapw encoded for this cache
+    CUtensorMap kmapw, vmapw;   // boxes of kWideBoxRows keys (64-key bf16 stages)
 };
 
 struct DeviceTable {
@@ -144,9 +146,9 @@ int sliding_capacity(const hd_ctx *ctx) {
 }
 
 // Encodes the 4-D view {D, capacity, Hkv, batch} of one cache tensor with
-// (128 bytes) x (keys per stage) boxes and the 128-byte swizzle the consumers index by.
+// (128 bytes) x (box_rows keys) boxes and the 128-byte swizzle the consumers index by.
 bool encode_cache_map(CUtensorMap *map, const void *base, int64_t seq_stride, int capacity,
-                      int num_kv_heads, int batch, int kv_type) {
+                      int num_kv_heads, int batch, int kv_type, int box_rows) {
     auto fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t es = (cuuint64_t)kv_elem_bytes(kv_type);
@@ -154,7 +156,7 @@ bool encode_cache_map(CUtensorMap *map, const void *base, int64_t seq_stride, in
                                 (cuuint64_t)num_kv_heads, (cuuint64_t)batch};
     const cuuint64_t strides[3] = {(cuuint64_t)kHeadDim * es, (cuuint64_t)capacity * kHeadDim * es,
                                    (cuuint64_t)seq_stride * es};
-    const cuuint32_t box[4] = {(cuuint32_t)kv_box_cols(kv_type), (cuuint32_t)kv_stage_keys(kv_type), 1, 1};
+    const cuuint32_t box[4] = {(cuuint32_t)kv_box_cols(kv_type), (cuuint32_t)box_rows, 1, 1};
     const cuuint32_t estr[4] = {1, 1, 1, 1};
     CUresult r = fn(map, kv_type == KV_FP8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4,
                     const_cast<void *>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -163,13 +165,17 @@ bool encode_cache_map(CUtensorMap *map, const void *base, int64_t seq_stride, in
     return r == CUDA_SUCCESS;
 }
 
-hd_status maps_for(hd_ctx *ctx, int layer, const hd_kv_cache &c, int batch, const CUtensorMap **km,
+// wide: the maps of a pass of 64-key bf16 stages (wide_stage_pass).
+hd_status maps_for(hd_ctx *ctx, int layer, const hd_kv_cache &c, int batch, bool wide, const CUtensorMap **km,
                    const CUtensorMap **vm) {
     MapCacheEntry &e = ctx->maps[layer];
+    const int Hkv = ctx->cfg.num_kv_heads;
     if (e.k != c.k || e.v != c.v || e.seq_stride != c.seq_stride || e.capacity != c.capacity ||
         e.batch != batch) {
-        if (!encode_cache_map(&e.kmap, c.k, c.seq_stride, c.capacity, ctx->cfg.num_kv_heads, batch, ctx->kv_type) ||
-            !encode_cache_map(&e.vmap, c.v, c.seq_stride, c.capacity, ctx->cfg.num_kv_heads, batch, ctx->kv_type)) {
+        const int rows = kv_stage_keys(ctx->kv_type);
+        e.wide_valid = false;
+        if (!encode_cache_map(&e.kmap, c.k, c.seq_stride, c.capacity, Hkv, batch, ctx->kv_type, rows) ||
+            !encode_cache_map(&e.vmap, c.v, c.seq_stride, c.capacity, Hkv, batch, ctx->kv_type, rows)) {
             e.k = e.v = nullptr;
             return HD_ERR_CUDA;
         }
@@ -179,8 +185,14 @@ hd_status maps_for(hd_ctx *ctx, int layer, const hd_kv_cache &c, int batch, cons
         e.capacity = c.capacity;
         e.batch = batch;
     }
-    *km = &e.kmap;
-    *vm = &e.vmap;
+    if (wide && !e.wide_valid) {
+        if (!encode_cache_map(&e.kmapw, c.k, c.seq_stride, c.capacity, Hkv, batch, ctx->kv_type, kWideBoxRows) ||
+            !encode_cache_map(&e.vmapw, c.v, c.seq_stride, c.capacity, Hkv, batch, ctx->kv_type, kWideBoxRows))
+            return HD_ERR_CUDA;
+        e.wide_valid = true;
+    }
+    *km = wide ? &e.kmapw : &e.kmap;
+    *vm = wide ? &e.vmapw : &e.vmap;
     return HD_OK;
 }
 
@@ -318,7 +330,8 @@ void fill_layer_args(const hd_ctx *ctx, const LayerCall &L, int32_t chunk_keys, 
 
 hd_status launch_layer_call(hd_ctx *ctx, const LayerCall &L, cudaStream_t stream) {
     const CUtensorMap *km = nullptr, *vm = nullptr;
-    hd_status st = maps_for(ctx, L.layer, L.cache, L.batch, &km, &vm);
+    const bool wide = wide_stage_pass(ctx->kv_type, (size_t)ctx->group * L.tokens, ctx->consumer == CONSUMER_UMMA);
+    hd_status st = maps_for(ctx, L.layer, L.cache, L.batch, wide, &km, &vm);
     if (st != HD_OK) return st;
     int32_t chunk_keys = 0, num_chunks = 0, stages = kStages;
     if (L.one_chunk) {   // a rolled window shifted in place: one CTA reads each sequence's window
@@ -491,7 +504,9 @@ hd_status launch_step_calls(hd_ctx *ctx, const std::vector<LayerCall> &calls, cu
         if (t.num_layers == kStepLayers || part_row + need > ctx->part_rows || ctas + layer_ctas > INT_MAX)
             if ((st = flush()) != HD_OK) return st;
         const CUtensorMap *km = nullptr, *vm = nullptr;
-        if ((st = maps_for(ctx, L.layer, L.cache, L.batch, &km, &vm)) != HD_OK) return st;
+        if ((st = maps_for(ctx, L.layer, L.cache, L.batch, wide_stage_pass(ctx->kv_type, rows, ctx->consumer == CONSUMER_UMMA),
+                           &km, &vm)) != HD_OK)
+            return st;
         LayerLaunch &e = t.layer[t.num_layers++];
         e.kmap = *km;
         e.vmap = *vm;

@@ -70,9 +70,6 @@
 #ifndef HD_STEP_FINISH
 #define HD_STEP_FINISH 1
 #endif
-#ifndef HD_WIDE_MT
-#define HD_WIDE_MT 1
-#endif
 
 namespace hd {
 namespace {
@@ -1028,6 +1025,13 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
     constexpr int kKeys = (kWide ? 2 : 1) * kv_stage_keys(KV);          // keys per stage: 32 bf16, 64 E4M3 or wide
     constexpr int kBoxB = (kWide ? 2 : 1) * kv_box_bytes(KV);           // bytes of one box column of a stage
     constexpr int kBoxes = kv_boxes_per_row(KV);   // 128-byte boxes per K or V row
+    // Rows of one TMA box (the host encodes the layer's tensor maps to match) and
+    // boxes per box column of a stage.  A box of r rows fills r * 128 contiguous
+    // bytes in the 128-byte swizzle, so two 32-row boxes and one 64-row box leave
+    // the same layout.
+    constexpr int kBoxRows = kWide ? kWideBoxRows : kv_stage_keys(KV);
+    constexpr int kPieces = kKeys / kBoxRows;
+    static_assert(kPieces * kBoxRows == kKeys, "whole boxes per stage");
     constexpr int kNThreads = layer_threads(G, KV, NL, MT, deep_ring(SP, KV), CONSUMER);
     constexpr bool kOwnProducer = own_producer(KV, NL, MT, deep_ring(SP, KV));
     constexpr int CW = kUmma ? kConsumerWarps * (G / 16) : consumer_warps(G);   // consumer (softmax) warps
@@ -1229,28 +1233,27 @@ __global__ void __launch_bounds__(layer_threads(G, KV, NL, MT, deep_ring(SP, KV)
 #pragma unroll
         for (int j = 0; j < kBoxes; ++j)
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-                tma_load_4d(st + j * kBoxB + h * kv_box_bytes(KV), v ? &ll.vmap : &ll.kmap, bar, j * kv_box_cols(KV),
-                            row + h * kv_stage_keys(KV), kvh, b);
+            for (int h = 0; h < kPieces; ++h)
+                tma_load_4d(st + j * kBoxB + h * kBoxRows * 128, v ? &ll.vmap : &ll.kmap, bar, j * kv_box_cols(KV),
+                            row + h * kBoxRows, kvh, b);
     };
     auto issue_stage = [&](int s) {
         const int slot = s % S;
         uint8_t *st = smem + slot * kStage;
         mbar_arrive_expect_tx(&full[slot], kStage);
         const int row = roff + start + s * kKeys;
-        constexpr int kHalves = kWide ? 2 : 1;   // 32-row boxes per box column
 #pragma unroll
         for (int j = 0; j < kBoxes; ++j)
 #pragma unroll
-            for (int h = 0; h < kHalves; ++h)
-                tma_load_4d(st + j * kBoxB + h * kv_box_bytes(KV), &ll.kmap, &full[slot], j * kv_box_cols(KV),
-                            row + h * kv_stage_keys(KV), kvh, b);
+            for (int h = 0; h < kPieces; ++h)
+                tma_load_4d(st + j * kBoxB + h * kBoxRows * 128, &ll.kmap, &full[slot], j * kv_box_cols(KV),
+                            row + h * kBoxRows, kvh, b);
 #pragma unroll
         for (int j = 0; j < kBoxes; ++j)
 #pragma unroll
-            for (int h = 0; h < kHalves; ++h)
-                tma_load_4d(st + (kBoxes + j) * kBoxB + h * kv_box_bytes(KV), &ll.vmap, &full[slot],
-                            j * kv_box_cols(KV), row + h * kv_stage_keys(KV), kvh, b);
+            for (int h = 0; h < kPieces; ++h)
+                tma_load_4d(st + (kBoxes + j) * kBoxB + h * kBoxRows * 128, &ll.vmap, &full[slot],
+                            j * kv_box_cols(KV), row + h * kBoxRows, kvh, b);
     };
     // Test hook: stages from a.drop_stage on are never issued (a copy that never arrives).
     auto droppable = [&](int s) { return a.drop_stage >= 0 && s >= a.drop_stage; };

@@ -12,6 +12,19 @@
 
 #include "hybrid_decode.h"
 
+// Build switches shared by the host planner and the kernels (measured choices).
+// 16-row multi-token passes over bf16 caches take 64-key stages (two 8-row
+// groups, 16 keys per consumer warp and call).
+#ifndef HD_WIDE_MT
+#define HD_WIDE_MT 1
+#endif
+// The 64-key stages of those passes (and of the tcgen05 passes) load one 64-row
+// box per 128-byte column of K and V -- 8 copies a stage -- instead of two
+// 32-row boxes.
+#ifndef HD_WIDE_BOX64
+#define HD_WIDE_BOX64 1
+#endif
+
 namespace hd {
 
 // Per-device one-time setup (kernel attributes are set per device): true when
@@ -72,6 +85,13 @@ void plan_split(int64_t batch, int64_t num_kv_heads, int64_t max_keys, int64_t n
 // 64-key stages (its q operand takes 32 KiB).
 constexpr int kUmma32Stages = 5;
 inline int deep_stages_for(size_t rows) { return rows > (size_t)kMaxRowsMma ? kUmma32Stages : kDeepStages; }
+
+// Passes of 64-key bf16 stages: 16 rows on mma.sync (HD_WIDE_MT) or on tcgen05,
+// and 32 rows (tcgen05 only).  Their tensor maps have kWideBoxRows-row boxes.
+constexpr int kWideBoxRows = HD_WIDE_BOX64 ? 2 * kStageKeys : kStageKeys;
+inline bool wide_stage_pass(int kv, size_t rows, bool tensor_memory) {
+    return kv == KV_BF16 && rows > (size_t)kMaxGroup && (HD_WIDE_MT || tensor_memory || rows > (size_t)kMaxRowsMma);
+}
 
 // Ring of a step grid with more CTAs than SMs.  Single-token E4M3 grids of
 // kTripleRows rows (group 4) run three CTAs per SM on two-stage rings: twelve
